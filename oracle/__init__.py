@@ -1,0 +1,271 @@
+"""CPU oracle of the Stable Latent MoE feed-forward layer -- TEST INFRASTRUCTURE ONLY.
+
+Only the test-suite, ``__graft_entry__.smoke()`` and the CPU-baseline leg of ``bench.py``
+import this package.  The product path (the CUDA library and its Python binding) never
+imports, links or calls it, and it shares no code with them.
+
+The arithmetic lives in ``lmoe_oracle.c`` (fp64, fp32 routing, OpenMP over tokens); this
+module compiles it with gcc on first use and wraps each function with ctypes.  Every step
+cites the passage it follows in the C source.  ``forward`` chains the steps in the order
+the layer defines them:
+
+    lat    = x . W_down^T                              latent down-projection
+    z      = lat . W_r^T   (rounded to fp32)           router logits
+    tau    = k-th largest sigmoid score per expert     Quantile Balancing (in-batch)
+    idx, g = top-K of fl32(s - tau), gates s / sum s   routing
+    z_n    = RMSNorm(sum_j g_j SiTU-FFN_{idx_j}(lat))  routed experts in the latent
+    ys     = sum_s SiTU-FFN_s(x)                       shared experts at full width
+    y      = residual + z_n . W_up^T + ys
+
+Parity status: every function is pinned by the CPU tests in ``tests/test_oracle_*.py``
+(closed forms, library special cases, brute force on tiny inputs, invariants).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from dataclasses import dataclass
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "lmoe_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+_dbl_p = ctypes.POINTER(ctypes.c_double)
+_flt_p = ctypes.POINTER(ctypes.c_float)
+_u16_p = ctypes.POINTER(ctypes.c_uint16)
+_i32_p = ctypes.POINTER(ctypes.c_int32)
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (no FMA contraction, no fast-math) and return its path."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-ffp-contract=off", "-fno-fast-math",
+           "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        lib = ctypes.CDLL(build())
+        lib.oracle_sigmoid32.restype = ctypes.c_float
+        lib.oracle_sigmoid32.argtypes = [ctypes.c_float]
+        lib.oracle_situ.restype = ctypes.c_double
+        lib.oracle_situ.argtypes = [ctypes.c_double] * 3
+        lib.oracle_num_threads.restype = ctypes.c_int
+        for name in ("oracle_latent", "oracle_router_logits", "oracle_scores",
+                     "oracle_thresholds", "oracle_route", "oracle_situ_vec",
+                     "oracle_routed", "oracle_shared", "oracle_output"):
+            getattr(lib, name).restype = None
+        _lib = lib
+        return lib
+
+
+def _p(a: np.ndarray, ptype):
+    assert a.flags["C_CONTIGUOUS"], "oracle inputs must be C-contiguous"
+    return a.ctypes.data_as(ptype)
+
+
+def _u16(a) -> np.ndarray:
+    """bf16 bit patterns as a C-contiguous uint16 array (accepts numpy uint16/int16 or a
+    torch bf16 tensor)."""
+    if hasattr(a, "dtype") and str(a.dtype) == "torch.bfloat16":
+        import torch
+        a = a.detach().contiguous().view(torch.int16).cpu().numpy()
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.int16:
+        a = a.view(np.uint16)
+    assert a.dtype == np.uint16, a.dtype
+    return a
+
+
+def num_threads() -> int:
+    return int(_load().oracle_num_threads())
+
+
+def sigmoid32(z: float) -> float:
+    return float(_load().oracle_sigmoid32(ctypes.c_float(z)))
+
+
+def scores(logits: np.ndarray) -> np.ndarray:
+    lg = np.ascontiguousarray(logits, dtype=np.float32)
+    out = np.empty_like(lg)
+    _load().oracle_scores(ctypes.c_longlong(lg.size), _p(lg, _flt_p), _p(out, _flt_p))
+    return out
+
+
+def situ(g, v, c: float = 100.0) -> np.ndarray:
+    g = np.ascontiguousarray(g, dtype=np.float64)
+    v = np.ascontiguousarray(v, dtype=np.float64)
+    assert g.shape == v.shape
+    out = np.empty_like(g)
+    _load().oracle_situ_vec(ctypes.c_longlong(g.size), _p(g, _dbl_p), _p(v, _dbl_p),
+                            ctypes.c_double(c), _p(out, _dbl_p))
+    return out
+
+
+def fair_share_rank(T: int, K: int, E: int) -> int:
+    """k = max(1, floor(T*K/E)), at most T: the rank of the Quantile-Balancing threshold."""
+    if T <= 0:
+        return 0
+    return min(T, max(1, (T * K) // E))
+
+
+def thresholds(logits: np.ndarray, k: int) -> np.ndarray:
+    lg = np.ascontiguousarray(logits, dtype=np.float32)
+    T, E = lg.shape
+    tau = np.empty(E, dtype=np.float32)
+    _load().oracle_thresholds(T, E, int(k), _p(lg, _flt_p), _p(tau, _flt_p))
+    return tau
+
+
+def route(logits: np.ndarray, tau, K: int):
+    """Returns (idx int32 [T,K], gate fp32 [T,K], scores fp32 [T,E])."""
+    lg = np.ascontiguousarray(logits, dtype=np.float32)
+    T, E = lg.shape
+    idx = np.empty((T, K), dtype=np.int32)
+    gate = np.empty((T, K), dtype=np.float32)
+    sc = np.empty((T, E), dtype=np.float32)
+    tp = None
+    if tau is not None:
+        tau = np.ascontiguousarray(tau, dtype=np.float32)
+        assert tau.shape == (E,)
+        tp = _p(tau, _flt_p)
+    _load().oracle_route(T, E, K, _p(lg, _flt_p), tp, _p(idx, _i32_p), _p(gate, _flt_p),
+                         _p(sc, _flt_p))
+    return idx, gate, sc
+
+
+def latent(x, w_down) -> np.ndarray:
+    x, w_down = _u16(x), _u16(w_down)
+    n, d = x.shape
+    L = w_down.shape[0]
+    assert w_down.shape == (L, d)
+    lat = np.empty((n, L), dtype=np.float64)
+    _load().oracle_latent(n, d, L, _p(x, _u16_p), _p(w_down, _u16_p), _p(lat, _dbl_p))
+    return lat
+
+
+def router_logits(lat: np.ndarray, w_router) -> np.ndarray:
+    lat = np.ascontiguousarray(lat, dtype=np.float64)
+    w_router = _u16(w_router)
+    n, L = lat.shape
+    E = w_router.shape[0]
+    assert w_router.shape == (E, L)
+    out = np.empty((n, E), dtype=np.float64)
+    _load().oracle_router_logits(n, L, E, _p(lat, _dbl_p), _p(w_router, _u16_p),
+                                 _p(out, _dbl_p))
+    return out
+
+
+def routed(lat, idx, gate, w_gate, w_value, w_edown, gamma, c=100.0, eps=1e-6):
+    lat = np.ascontiguousarray(lat, dtype=np.float64)
+    idx = np.ascontiguousarray(idx, dtype=np.int32)
+    gate = np.ascontiguousarray(gate, dtype=np.float32)
+    w_gate, w_value, w_edown = _u16(w_gate), _u16(w_value), _u16(w_edown)
+    gamma = np.ascontiguousarray(gamma, dtype=np.float32)
+    n, L = lat.shape
+    E, I, L2 = w_gate.shape
+    K = idx.shape[1]
+    assert L2 == L and w_value.shape == w_gate.shape and w_edown.shape == (E, L, I)
+    assert gate.shape == idx.shape == (n, K) and gamma.shape == (L,)
+    assert n == 0 or (idx.min() >= 0 and idx.max() < E)
+    z = np.empty((n, L), dtype=np.float64)
+    _load().oracle_routed(n, L, E, K, I, _p(lat, _dbl_p), _p(idx, _i32_p), _p(gate, _flt_p),
+                          _p(w_gate, _u16_p), _p(w_value, _u16_p), _p(w_edown, _u16_p),
+                          _p(gamma, _flt_p), ctypes.c_double(c), ctypes.c_double(eps),
+                          _p(z, _dbl_p))
+    return z
+
+
+def shared(x, w_sgate, w_svalue, w_sdown, c=100.0):
+    x = _u16(x)
+    w_sgate, w_svalue, w_sdown = _u16(w_sgate), _u16(w_svalue), _u16(w_sdown)
+    n, d = x.shape
+    S, Is, d2 = w_sgate.shape
+    assert d2 == d and w_svalue.shape == w_sgate.shape and w_sdown.shape == (S, d, Is)
+    ys = np.empty((n, d), dtype=np.float64)
+    _load().oracle_shared(n, d, S, Is, _p(x, _u16_p), _p(w_sgate, _u16_p),
+                          _p(w_svalue, _u16_p), _p(w_sdown, _u16_p), ctypes.c_double(c),
+                          _p(ys, _dbl_p))
+    return ys
+
+
+def output(z, ys, w_up, residual=None):
+    z = np.ascontiguousarray(z, dtype=np.float64)
+    ys = np.ascontiguousarray(ys, dtype=np.float64)
+    w_up = _u16(w_up)
+    n, L = z.shape
+    d = w_up.shape[0]
+    assert w_up.shape == (d, L) and ys.shape == (n, d)
+    rp = None
+    if residual is not None:
+        residual = _u16(residual)
+        assert residual.shape == (n, d)
+        rp = _p(residual, _u16_p)
+    y = np.empty((n, d), dtype=np.float64)
+    _load().oracle_output(n, d, L, _p(z, _dbl_p), _p(ys, _dbl_p), _p(w_up, _u16_p), rp,
+                          _p(y, _dbl_p))
+    return y
+
+
+@dataclass
+class OracleResult:
+    y: np.ndarray            # [n, d] fp64 layer output
+    lat: np.ndarray          # [n, L] fp64 latent
+    logits: np.ndarray       # [n, E] fp32 router logits used for routing
+    tau: np.ndarray | None   # [E] fp32 thresholds used (None: no balancing)
+    idx: np.ndarray          # [n, K] int32
+    gate: np.ndarray         # [n, K] fp32
+    z: np.ndarray            # [n, L] fp64 normalised aggregated latent
+    ys: np.ndarray           # [n, d] fp64 shared-expert output
+
+
+def forward(w: dict, x, K: int, residual=None, tau="batch", logits_in=None, c=100.0,
+            eps=1e-6) -> OracleResult:
+    """The whole layer on the rows of ``x``.
+
+    w: dict of weights (bf16 tensors or uint16 bit arrays, fp32 gamma) with keys w_down,
+       w_router, w_gate, w_value, w_edown, gamma, w_up, w_sgate, w_svalue, w_sdown.
+    tau: "batch" -> thresholds solved over the rows of x (k = fair_share_rank);
+         None -> plain top-K without balancing; an array -> those thresholds.
+    logits_in: fp32 [n, E] router logits to route on instead of the computed ones.
+    """
+    xs = _u16(x)
+    n = xs.shape[0]
+    lat = latent(xs, w["w_down"])
+    if logits_in is None:
+        lg = router_logits(lat, w["w_router"]).astype(np.float32)
+    else:
+        lg = np.ascontiguousarray(logits_in, dtype=np.float32)
+    E = lg.shape[1]
+    if isinstance(tau, str):
+        assert tau == "batch"
+        tau_v = thresholds(lg, fair_share_rank(n, K, E))
+    elif tau is None:
+        tau_v = None
+    else:
+        tau_v = np.ascontiguousarray(tau, dtype=np.float32)
+    idx, gate, _ = route(lg, tau_v, K)
+    gamma = w["gamma"]
+    if hasattr(gamma, "detach"):
+        gamma = gamma.detach().float().cpu().numpy()
+    z = routed(lat, idx, gate, w["w_gate"], w["w_value"], w["w_edown"], gamma, c, eps)
+    ys = shared(xs, w["w_sgate"], w["w_svalue"], w["w_sdown"], c)
+    y = output(z, ys, w["w_up"], residual)
+    return OracleResult(y=y, lat=lat, logits=lg, tau=tau_v, idx=idx, gate=gate, z=z, ys=ys)

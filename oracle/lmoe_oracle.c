@@ -1,0 +1,335 @@
+/*
+ * lmoe_oracle.c -- plain, slow, obviously correct CPU oracle of the Stable Latent MoE
+ * feed-forward layer.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path links, loads or calls this file;
+ * only the test-suite, the smoke check and the CPU-baseline leg of the benchmark do.  It
+ * shares no code, header, table or constant with the CUDA library.
+ *
+ * Precision: every step runs in IEEE double from the bf16 bit patterns of the inputs,
+ * widened exactly, with no intermediate rounding -- except the routing decision (score,
+ * threshold, top-K, gates), which is defined in fp32 so that a device implementation can
+ * reproduce it bit for bit.  Build with -ffp-contract=off: the fp32 routing arithmetic must
+ * not be fused by the compiler (fmaf is called explicitly where a fused op is meant).
+ *
+ * Sources (web pages on Kimi K3; none prints an equation, so each formula below is the
+ * plainest reading of the words, and the readings are listed where they are made):
+ *   [TPP]  "The 2.8-Trillion-Parameter Problem: Why Bigger Models Break the Old Playbook",
+ *          aitrending.vip summary -- sections "TL;DR" and "Technical Details".
+ *   [IK3]  the same title, "Part 1 of Inside Kimi K3" (Towards AI article, wpnews.pro copy) --
+ *          its passages on Mixture of Experts, Stable LatentMoE, the stabilizers, and
+ *          Quantile Balancing.
+ *   [SU]   "苏神复盘 Kimi K3：896 个专家背后，藏着哪些关键技术取舍？" (daily-ai-frontier),
+ *          "Merged summary", bullets "LatentMoE" and "Stable LatentMoE".
+ *
+ * Layout conventions: all matrices row-major; weights stored [out, in].
+ *   x        [n, d]        bf16 bits      hidden state (7168 wide in K3)
+ *   w_down   [L, d]        bf16 bits      latent down-projection (L = d/2)
+ *   w_router [E, L]        bf16 bits      router
+ *   w_gate   [E, I, L]     bf16 bits      routed expert gate branch
+ *   w_value  [E, I, L]     bf16 bits      routed expert value branch
+ *   w_edown  [E, L, I]     bf16 bits      routed expert down projection
+ *   gamma    [L]           fp32           RMSNorm weight
+ *   w_up     [d, L]        bf16 bits      up-projection back to the hidden width
+ *   w_sgate  [S, Is, d]    bf16 bits      shared experts, gate branch
+ *   w_svalue [S, Is, d]    bf16 bits      shared experts, value branch
+ *   w_sdown  [S, d, Is]    bf16 bits      shared experts, down projection
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* bf16 bit pattern -> double, exactly (bf16 is the top half of an fp32). */
+static double bf(uint16_t b) {
+  uint32_t u = (uint32_t)b << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return (double)f;
+}
+
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* Latent down-projection.  [TPP] Technical Details, "Stable Latent MoE with Compression":
+ * the 7168-wide hidden state is projected to 3584 dimensions before routing; [IK3] Stable
+ * LatentMoE passage: the projection happens first, experts then work in the latent.
+ * No bias is mentioned anywhere, so none is used.
+ *   lat[t, l] = sum_i x[t, i] * w_down[l, i]                                               */
+void oracle_latent(int n, int d, int L, const uint16_t *x, const uint16_t *w_down,
+                   double *lat) {
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int t = 0; t < n; ++t) {
+    for (int l = 0; l < L; ++l) {
+      double acc = 0.0;
+      for (int i = 0; i < d; ++i)
+        acc += bf(x[(size_t)t * d + i]) * bf(w_down[(size_t)l * d + i]);
+      lat[(size_t)t * L + l] = acc;
+    }
+  }
+}
+
+/* Router logits.  [IK3] Mixture-of-Experts passage: a lightweight router looks at each
+ * token; [SU] LatentMoE bullet: routing happens in the latent space.  Reading: a linear
+ * router without bias on the latent, z[t, e] = sum_l lat[t, l] * w_router[e, l].         */
+void oracle_router_logits(int n, int L, int E, const double *lat, const uint16_t *w_router,
+                          double *logits) {
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int t = 0; t < n; ++t) {
+    for (int e = 0; e < E; ++e) {
+      double acc = 0.0;
+      for (int l = 0; l < L; ++l)
+        acc += lat[(size_t)t * L + l] * bf(w_router[(size_t)e * L + l]);
+      logits[(size_t)t * E + e] = acc;
+    }
+  }
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* Router score s = sigmoid(z), in fp32, specified to the last bit.  The pages name no
+ * score function; the reading is the logistic sigmoid.  So that routing decisions can be
+ * reproduced exactly, the fp32 evaluation is fixed here step by step:
+ *   1. clamp z to [-88, 88];  x = -z
+ *   2. Cody-Waite range reduction (W. J. Cody and W. Waite, "Software Manual for the
+ *      Elementary Functions", 1980): n = rint(fl(x * log2(e))),
+ *      r = fma(-n, LN2_HI, x), r = fma(-n, LN2_LO, r), where LN2_HI = 22713/32768 has 15
+ *      significant bits (so n * LN2_HI is exact for |n| <= 127) and LN2_LO = fl32(ln2 - LN2_HI)
+ *   3. p = Taylor polynomial of exp(r) of degree 7, coefficients fl32(1/k!), by Horner's
+ *      rule with one fma per step, highest degree first
+ *   4. e = (p * 2^n1) * 2^n2 with n1 = n/2 (toward zero), n2 = n - n1 (both powers normal)
+ *   5. s = 1 / (1 + e), each operation one IEEE round-to-nearest fp32 operation.        */
+float oracle_sigmoid32(float z) {
+  const float LOG2E = 0x1.715476p+0f;      /* fl32(1/ln 2) */
+  const float LN2_HI = 0x1.62e4p-1f;       /* 22713/32768 */
+  const float LN2_LO = 0x1.7f7d1cp-20f;    /* fl32(ln 2 - 22713/32768) */
+  const float C7 = 0x1.a01a02p-13f;        /* fl32(1/5040) */
+  const float C6 = 0x1.6c16c2p-10f;        /* fl32(1/720)  */
+  const float C5 = 0x1.111112p-7f;         /* fl32(1/120)  */
+  const float C4 = 0x1.555556p-5f;         /* fl32(1/24)   */
+  const float C3 = 0x1.555556p-3f;         /* fl32(1/6)    */
+  const float C2 = 0.5f, C1 = 1.0f, C0 = 1.0f;
+  if (z > 88.0f) z = 88.0f;
+  if (z < -88.0f) z = -88.0f;
+  float x = -z;
+  float t = x * LOG2E;
+  float nf = rintf(t);
+  float r = fmaf(-nf, LN2_HI, x);
+  r = fmaf(-nf, LN2_LO, r);
+  float p = C7;
+  p = fmaf(p, r, C6);
+  p = fmaf(p, r, C5);
+  p = fmaf(p, r, C4);
+  p = fmaf(p, r, C3);
+  p = fmaf(p, r, C2);
+  p = fmaf(p, r, C1);
+  p = fmaf(p, r, C0);
+  int n = (int)nf;
+  int n1 = n / 2, n2 = n - n1;
+  uint32_t b1 = (uint32_t)(n1 + 127) << 23, b2 = (uint32_t)(n2 + 127) << 23;
+  float s1, s2;
+  memcpy(&s1, &b1, 4);
+  memcpy(&s2, &b2, 4);
+  float e = (p * s1) * s2;
+  float den = 1.0f + e;
+  return 1.0f / den;
+}
+
+void oracle_scores(long long count, const float *logits, float *scores) {
+#pragma omp parallel for schedule(static)
+  for (long long i = 0; i < count; ++i) scores[i] = oracle_sigmoid32(logits[i]);
+}
+
+static int cmp_float_desc(const void *a, const void *b) {
+  float x = *(const float *)a, y = *(const float *)b;
+  return (x < y) - (x > y);
+}
+
+/* Quantile-Balancing threshold.  [IK3] Quantile Balancing passage: the threshold is read
+ * off the batch's score distribution -- the score an expert needs to stay within its fair
+ * share of tokens; [SU] Stable LatentMoE bullet: it solves directly for per-expert Top-K
+ * thresholds.  Reading: tau[e] = the k-th largest score in column e of the batch's score
+ * matrix, k = max(1, floor(T*K/E)), at most T (the caller passes k).  Computed by sorting
+ * each column in full.                                                                   */
+void oracle_thresholds(int T, int E, int k, const float *logits, float *tau) {
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int e = 0; e < E; ++e) {
+    float *col = (float *)malloc(sizeof(float) * (size_t)(T > 0 ? T : 1));
+    for (int t = 0; t < T; ++t) col[t] = oracle_sigmoid32(logits[(size_t)t * E + e]);
+    qsort(col, (size_t)T, sizeof(float), cmp_float_desc);
+    tau[e] = (T > 0 && k >= 1 && k <= T) ? col[k - 1] : 0.0f;
+    free(col);
+  }
+}
+
+typedef struct {
+  float a;
+  int e;
+} route_key;
+
+/* Order: larger a first; equal a (IEEE equality, so -0 == +0) -> smaller expert id first. */
+static int cmp_route(const void *pa, const void *pb) {
+  const route_key *x = (const route_key *)pa, *y = (const route_key *)pb;
+  if (x->a > y->a) return -1;
+  if (x->a < y->a) return 1;
+  return (x->e > y->e) - (x->e < y->e);
+}
+
+/* Top-K routing.  [TPP] Technical Details: a lightweight router selects 16 of the 896
+ * routed experts per token; [SU]: Quantile Balancing replaces the bias updates of the
+ * predecessor, so the thresholds take the bias's place.  Reading:
+ *   a[t, e] = fl32(s[t, e] - tau[e])          (tau == NULL: no balancing, a = s)
+ *   the K experts with the largest a, ties to the smaller expert id, listed in that order
+ *   gate[t, j] = fl32(s_j / S), S = fl32 sum of the selected s in slot order j = 0..K-1.  */
+void oracle_route(int T, int E, int K, const float *logits, const float *tau, int32_t *idx,
+                  float *gate, float *scores) {
+#pragma omp parallel for schedule(dynamic, 16)
+  for (int t = 0; t < T; ++t) {
+    route_key *keys = (route_key *)malloc(sizeof(route_key) * (size_t)E);
+    float *s = (float *)malloc(sizeof(float) * (size_t)E);
+    for (int e = 0; e < E; ++e) {
+      s[e] = oracle_sigmoid32(logits[(size_t)t * E + e]);
+      if (scores) scores[(size_t)t * E + e] = s[e];
+      keys[e].a = tau ? (s[e] - tau[e]) : s[e];
+      keys[e].e = e;
+    }
+    qsort(keys, (size_t)E, sizeof(route_key), cmp_route);
+    float sum = 0.0f;
+    for (int j = 0; j < K; ++j) sum = sum + s[keys[j].e];
+    for (int j = 0; j < K; ++j) {
+      idx[(size_t)t * K + j] = keys[j].e;
+      gate[(size_t)t * K + j] = s[keys[j].e] / sum;
+    }
+    free(keys);
+    free(s);
+  }
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* SiTU-GLU.  [TPP] Technical Details, "Stabilization Mechanisms", and [IK3] stabilizers
+ * passage: the gate and the value branch are smoothly capped to about +-100 in magnitude,
+ * and the activation behaves like SwiGLU near zero; [SU] Stable LatentMoE bullet: it
+ * soft-caps SwiGLU outliers.  Reading: each branch goes through c*tanh(./c), c = 100, and
+ * the capped branches are combined as in SwiGLU:  silu(c tanh(g/c)) * c tanh(v/c).        */
+double oracle_situ(double g, double v, double c) {
+  double gc = c * tanh(g / c);
+  double vc = c * tanh(v / c);
+  return gc / (1.0 + exp(-gc)) * vc;
+}
+
+void oracle_situ_vec(long long count, const double *g, const double *v, double c,
+                     double *out) {
+  for (long long i = 0; i < count; ++i) out[i] = oracle_situ(g[i], v[i], c);
+}
+
+/* Routed experts in the latent, gate-weighted aggregation, RMSNorm.
+ * [TPP] Technical Details: experts operate in the compressed latent space and their
+ * outputs are projected back to full width; [IK3]: their outputs are combined, then
+ * projected back up; RMSNorm sits right before the up-projection; [SU]: RMSNorm after
+ * expert aggregation and before up-projection.
+ *   h = SiTU(lat . Wg[e]^T, lat . Wv[e]^T)          [I]
+ *   o = h . Wed[e]^T                                [L]
+ *   u = sum_j gate[t, j] * o_j
+ *   z = gamma * u / sqrt(mean(u^2) + eps)                                                  */
+void oracle_routed(int n, int L, int E, int K, int I, const double *lat, const int32_t *idx,
+                   const float *gate, const uint16_t *w_gate, const uint16_t *w_value,
+                   const uint16_t *w_edown, const float *gamma, double c, double eps,
+                   double *z) {
+  (void)E;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int t = 0; t < n; ++t) {
+    double *u = (double *)calloc((size_t)L, sizeof(double));
+    double *h = (double *)malloc(sizeof(double) * (size_t)I);
+    const double *lt = lat + (size_t)t * L;
+    for (int j = 0; j < K; ++j) {
+      int e = idx[(size_t)t * K + j];
+      double g = (double)gate[(size_t)t * K + j];
+      const uint16_t *Wg = w_gate + (size_t)e * I * L;
+      const uint16_t *Wv = w_value + (size_t)e * I * L;
+      const uint16_t *Wd = w_edown + (size_t)e * L * I;
+      for (int i = 0; i < I; ++i) {
+        double ag = 0.0, av = 0.0;
+        for (int l = 0; l < L; ++l) {
+          ag += lt[l] * bf(Wg[(size_t)i * L + l]);
+          av += lt[l] * bf(Wv[(size_t)i * L + l]);
+        }
+        h[i] = oracle_situ(ag, av, c);
+      }
+      for (int l = 0; l < L; ++l) {
+        double o = 0.0;
+        for (int i = 0; i < I; ++i) o += h[i] * bf(Wd[(size_t)l * I + i]);
+        u[l] += g * o;
+      }
+    }
+    double ms = 0.0;
+    for (int l = 0; l < L; ++l) ms += u[l] * u[l];
+    ms /= (double)L;
+    double inv = 1.0 / sqrt(ms + eps);
+    for (int l = 0; l < L; ++l) z[(size_t)t * L + l] = (double)gamma[l] * u[l] * inv;
+    free(u);
+    free(h);
+  }
+}
+
+/* Shared experts.  [TPP] TL;DR and Technical Details: 2 shared experts next to the 896
+ * routed ones; [SU] LatentMoE bullet: 2 always-on shared experts offset the latent
+ * bottleneck.  Reading: they see the full-width hidden state (only the routed path is
+ * compressed, [TPP] Technical Details) and use the same SiTU-GLU FFN form; every token
+ * passes through every shared expert with weight 1.
+ *   ys[t] = sum_s SiTU(x . Wsg[s]^T, x . Wsv[s]^T) . Wsd[s]^T                               */
+void oracle_shared(int n, int d, int S, int Is, const uint16_t *x, const uint16_t *w_sgate,
+                   const uint16_t *w_svalue, const uint16_t *w_sdown, double c, double *ys) {
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int t = 0; t < n; ++t) {
+    double *h = (double *)malloc(sizeof(double) * (size_t)Is);
+    double *out = ys + (size_t)t * d;
+    for (int m = 0; m < d; ++m) out[m] = 0.0;
+    for (int s = 0; s < S; ++s) {
+      const uint16_t *Wg = w_sgate + (size_t)s * Is * d;
+      const uint16_t *Wv = w_svalue + (size_t)s * Is * d;
+      const uint16_t *Wd = w_sdown + (size_t)s * d * Is;
+      for (int i = 0; i < Is; ++i) {
+        double ag = 0.0, av = 0.0;
+        for (int k = 0; k < d; ++k) {
+          double xv = bf(x[(size_t)t * d + k]);
+          ag += xv * bf(Wg[(size_t)i * d + k]);
+          av += xv * bf(Wv[(size_t)i * d + k]);
+        }
+        h[i] = oracle_situ(ag, av, c);
+      }
+      for (int m = 0; m < d; ++m) {
+        double acc = 0.0;
+        for (int i = 0; i < Is; ++i) acc += h[i] * bf(Wd[(size_t)m * Is + i]);
+        out[m] += acc;
+      }
+    }
+    free(h);
+  }
+}
+
+/* Up-projection and residual.  [TPP] Technical Details: outputs are projected back to
+ * full width; the residual stream stays 7168 wide; [IK3] baseline decoder passage: the FFN
+ * is wrapped in a residual connection.
+ *   y[t, m] = residual[t, m] + sum_l z[t, l] * w_up[m, l] + ys[t, m]
+ * (residual == NULL: no residual term).                                                   */
+void oracle_output(int n, int d, int L, const double *z, const double *ys,
+                   const uint16_t *w_up, const uint16_t *residual, double *y) {
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int t = 0; t < n; ++t) {
+    for (int m = 0; m < d; ++m) {
+      double acc = 0.0;
+      for (int l = 0; l < L; ++l) acc += z[(size_t)t * L + l] * bf(w_up[(size_t)m * L + l]);
+      double r = residual ? bf(residual[(size_t)t * d + m]) : 0.0;
+      y[(size_t)t * d + m] = r + acc + ys[(size_t)t * d + m];
+    }
+  }
+}
