@@ -1,0 +1,186 @@
+/*
+ * lmoe.h -- C ABI of the Stable Latent MoE feed-forward layer on one GB300 (sm_103a).
+ *
+ * The layer (Kimi K3; sources below) replaces the dense FFN of a decoder block:
+ *   lat    = x . W_down^T                          hidden d -> latent L (L = d/2 in K3)
+ *   logits = lat . W_r^T,  s = sigmoid(logits)     router over E routed experts
+ *   tau[e] = k-th largest s[:, e] in the batch     Quantile-Balancing threshold
+ *   top-K of fl32(s - tau) per token               K experts per token, gates s / sum(s)
+ *   h      = SiTU(lat . W_g[e]^T, lat . W_v[e]^T)  routed experts work in the latent
+ *   u      = sum_j gate_j (h_j . W_ed[e_j]^T)      gate-weighted aggregation
+ *   z      = gamma * u / sqrt(mean(u^2) + eps)     RMSNorm before the up-projection
+ *   y      = residual + z . W_up^T + sum_s SiTU(x . W_sg[s]^T, x . W_sv[s]^T) . W_sd[s]^T
+ * with SiTU(g, v) = silu(c tanh(g/c)) * c tanh(v/c), c = 100.
+ *
+ * Sources:
+ *   [TPP] "The 2.8-Trillion-Parameter Problem: Why Bigger Models Break the Old Playbook"
+ *         (aitrending.vip summary), sections "TL;DR" and "Technical Details".
+ *   [IK3] The same title, "Part 1 of Inside Kimi K3" (Towards AI article): passages on
+ *         Mixture of Experts, Stable LatentMoE, the stabilizers and Quantile Balancing.
+ *   [SU]  "苏神复盘 Kimi K3：896 个专家背后，藏着哪些关键技术取舍？" (daily-ai-frontier),
+ *         "Merged summary", bullets "LatentMoE" and "Stable LatentMoE".
+ * The pages give the structure in words only; the score function, where the threshold
+ * acts, the gate normalisation and the SiTU-GLU formula are readings, stated at each call.
+ *
+ * Conventions for every entry point:
+ *   - Every pointer argument is DEVICE memory owned by the caller, unless stated.  The
+ *     library allocates nothing, keeps no global state between calls and may be called
+ *     concurrently on different streams with disjoint buffers.
+ *   - bf16 tensors are raw IEEE bfloat16 bit patterns; all matrices are row-major and
+ *     weights are stored [out, in].
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Every call is
+ *     asynchronous on that stream and returns after enqueueing its kernels.
+ *   - Return value: LMOE_OK, or an LMOE_ERR_* code for a rejected argument or a failed
+ *     launch; nothing is enqueued when an argument is rejected.  Errors raised on the
+ *     device (a bounded wait that ran out) are read with lmoe_last_device_error after the
+ *     stream has synchronised.
+ *   - Inputs must be finite.  NaN router logits give an unspecified (but in-bounds)
+ *     selection.
+ */
+#ifndef LMOE_H
+#define LMOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum lmoe_status {
+  LMOE_OK = 0,
+  LMOE_ERR_INVALID_ARG = 1,          /* null pointer, negative size, bad combination */
+  LMOE_ERR_UNSUPPORTED = 2,          /* shape outside the supported set (see lmoe_forward) */
+  LMOE_ERR_CUDA = 3,                 /* a CUDA runtime/driver call or a launch failed */
+  LMOE_ERR_DEVICE_TIMEOUT = 4,       /* a device-side wait ran out (from lmoe_last_device_error) */
+  LMOE_ERR_WORKSPACE_TOO_SMALL = 5   /* workspace or packed buffer smaller than required */
+};
+
+/* Layer sizes.  K3: d=7168, L=3584, E=896, K=16, S=2 ([TPP] Technical Details; [SU]
+ * LatentMoE bullet); the pages give no intermediate sizes I and Is. */
+typedef struct lmoe_dims {
+  int T;      /* tokens in the batch, >= 0 */
+  int d;      /* hidden width */
+  int L;      /* latent width */
+  int E;      /* routed experts */
+  int K;      /* routed experts per token */
+  int I;      /* routed expert intermediate size */
+  int S;      /* shared experts */
+  int Is;     /* shared expert intermediate size */
+  float c;    /* SiTU-GLU cap (100 for K3) */
+  float eps;  /* RMSNorm epsilon (1e-6) */
+} lmoe_dims;
+
+/* Unpacked weights as a caller holds them (device pointers, bf16 unless stated). */
+typedef struct lmoe_weights {
+  const void *w_down;    /* [L, d]      latent down-projection */
+  const void *w_router;  /* [E, L]      router */
+  const void *w_gate;    /* [E, I, L]   routed experts, gate branch */
+  const void *w_value;   /* [E, I, L]   routed experts, value branch */
+  const void *w_edown;   /* [E, L, I]   routed experts, down projection */
+  const float *gamma;    /* [L] fp32    RMSNorm weight */
+  const void *w_up;      /* [d, L]      up-projection */
+  const void *w_sgate;   /* [S, Is, d]  shared experts, gate branch */
+  const void *w_svalue;  /* [S, Is, d]  shared experts, value branch */
+  const void *w_sdown;   /* [S, d, Is]  shared experts, down projection */
+} lmoe_weights;
+
+/* Optional routing inputs and debug outputs of lmoe_forward.  Any member may be NULL. */
+typedef struct lmoe_io {
+  const float *tau_in;   /* [E] thresholds to route against (e.g. from a prefill batch) */
+  int balance;           /* used when tau_in == NULL: 1 = solve thresholds from this batch
+                            (Quantile Balancing), 0 = plain top-K without thresholds */
+  const float *logits_in;/* [T, E] fp32 router logits to route on instead of computing
+                            them from the latent (replay, or routing done elsewhere) */
+  float *logits_out;     /* [T, E] router logits used */
+  float *tau_out;        /* [E] thresholds used (zeros when balance == 0) */
+  int32_t *idx_out;      /* [T, K] selected experts, slot order */
+  float *gate_out;       /* [T, K] gates */
+  int32_t *counts_out;   /* [E] tokens routed to each expert */
+} lmoe_io;
+
+/* Bytes of the packed weight buffer for `dims` (0 if the dims are invalid). */
+size_t lmoe_packed_bytes(const lmoe_dims *dims);
+
+/* Repack unpacked weights into the layout lmoe_forward reads: the shared gate/value rows
+ * are stacked under W_down and interleaved in groups of 16 rows, the routed gate/value rows
+ * likewise per expert, and W_up and the shared down-projections are concatenated along
+ * their input dimension.  `packed` (device, packed_bytes >= lmoe_packed_bytes(dims), 256-byte
+ * aligned) is overwritten; the inputs are only read.  Pure function of its inputs. */
+int lmoe_pack_weights(const lmoe_dims *dims, const lmoe_weights *w, void *packed,
+                      size_t packed_bytes, void *stream);
+
+/* Bytes of device workspace lmoe_forward needs for `dims` (0 if the dims are invalid). */
+size_t lmoe_workspace_bytes(const lmoe_dims *dims);
+
+/* Quantile-Balancing thresholds.  [IK3] Quantile Balancing passage: each step's routing
+ * thresholds are read off the distribution of the router scores -- the score an expert
+ * needs to stay within its fair share of tokens; [SU] Stable LatentMoE bullet: it solves
+ * directly for per-expert Top-K thresholds.  Reading: tau[e] = the k-th largest
+ * s[t, e] = sigmoid(logits[t, e]) over the T tokens, with k = k_rank, or, when k_rank <= 0,
+ * k = max(1, floor(T*K/E)) (at most T).  Bit-exact: s uses the fp32 sigmoid specified at
+ * lmoe_route, and the threshold is one of the s values.
+ *   logits [T, E] fp32 (read), tau [E] fp32 (written).  T == 0 writes nothing.
+ * Errors: INVALID_ARG for null pointers or T < 0, E < 1, K < 1, k_rank > T. */
+int lmoe_thresholds(const float *logits, int T, int E, int K, int k_rank, float *tau,
+                    void *stream);
+
+/* Top-K routing.  [TPP] Technical Details: a lightweight router selects 16 of 896 routed
+ * experts per token; [SU]: Quantile Balancing replaces the predecessor's bias updates.
+ * Readings: s = sigmoid(logits) evaluated in fp32 by a fixed sequence of IEEE operations
+ * (clamp to [-88, 88]; Cody-Waite reduction by ln 2 split as 22713/32768 + fl32 remainder;
+ * degree-7 Taylor polynomial of exp with fl32(1/k!) coefficients by fma Horner; scaling by
+ * two exact powers of two; 1/(1+e) with round-to-nearest add and divide); a[t, e] =
+ * fl32(s - tau[e]) (tau == NULL: a = s); the K largest a, ties to the lower expert id, in
+ * that order; gate_j = fl32(s_j / sum), sum accumulated in fp32 in slot order.
+ *   logits [T, E] fp32, tau [E] or NULL, idx [T, K] int32, gate [T, K] fp32,
+ *   scores_out [T, E] fp32 or NULL.  Requires 1 <= K <= min(E, 32), E <= 4096.
+ * Errors: INVALID_ARG (null outputs, T < 0), UNSUPPORTED (K or E out of range). */
+int lmoe_route(const float *logits, const float *tau, int T, int E, int K, int32_t *idx,
+               float *gate, float *scores_out, void *stream);
+
+/* The whole layer, y = FFN(x) (+ residual), as stated at the top of this header.
+ *   packed   weights from lmoe_pack_weights for the same dims
+ *   x        [T, d] bf16;  residual [T, d] bf16 or NULL (then no residual term)
+ *   y        [T, d] bf16 output (may not alias x or residual)
+ *   workspace, ws_bytes >= lmoe_workspace_bytes(dims), 256-byte aligned; its contents are
+ *            scratch between calls (its first word carries the device error flag)
+ *   io       routing options and debug outputs, or NULL (= in-batch thresholds)
+ * Supported shapes: d, L, I, Is multiples of 64; 1 <= K <= min(E, 32); E <= 4096 and a
+ * multiple of 16;
+ * L <= 16384; T * K < 2^31.  T == 0 is a no-op.
+ * Arithmetic: bf16 operands on the tensor cores with fp32 accumulation; the latent, the
+ * expert intermediates and the normalised latent are rounded to bf16 between GEMMs;
+ * routing is fp32 and reproduces lmoe_thresholds / lmoe_route on the logits it uses.
+ * Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE_TOO_SMALL, CUDA. */
+int lmoe_forward(const lmoe_dims *dims, const void *packed, const void *x,
+                 const void *residual, void *y, void *workspace, size_t ws_bytes,
+                 const lmoe_io *io, void *stream);
+
+/* Building block of lmoe_forward, exposed for verification: C = A . B^T on the tensor
+ * cores (tcgen05, fp32 accumulation in TMEM), with A [M, Kd] and B [N, Kd] bf16 row-major
+ * (K-major) and C [M, N] fp32.  Requires Kd % 64 == 0, N % 16 == 0, 16-byte aligned
+ * pointers.  dev_flag: one caller-owned device word (zero it first); it receives the same
+ * error bits as the forward workspace's flag if a device-side wait runs out. */
+int lmoe_gemm_bf16(const void *A, const void *B, float *C, int M, int N, int Kd,
+                   uint32_t *dev_flag, void *stream);
+
+/* Synchronously read and clear the device error flag that lmoe_forward's kernels write
+ * into `workspace`.  Every device-side wait is bounded (2 s by default; the environment
+ * variable LMOE_WAIT_LIMIT_MS overrides it), and LMOE_FAULT_INJECT=stall makes the first
+ * GEMM of a call wait on a barrier that nothing arrives on, so that this path can be
+ * tested: its kernels then give up, free their tensor memory and return.  Returns LMOE_OK or LMOE_ERR_DEVICE_TIMEOUT (a bounded wait ran out;
+ * the kernel returned early and y is not valid).  Call after the stream has synchronised. */
+int lmoe_last_device_error(void *workspace);
+
+/* Static description of a status code. */
+const char *lmoe_error_string(int status);
+
+/* Library version, e.g. "lmoe 0.1 sm_103a". */
+const char *lmoe_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LMOE_H */

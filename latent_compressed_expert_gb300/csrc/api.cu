@@ -1,0 +1,373 @@
+// api.cu -- the extern "C" entry points declared in include/lmoe.h: argument checks,
+// buffer layouts, and the sequence of kernel launches of one forward pass.
+#include <stdlib.h>
+#include <string.h>
+
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace lmoe {
+
+static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+static bool dims_ok(const lmoe_dims* D) {
+  if (!D) return false;
+  if (D->T < 0 || D->d <= 0 || D->L <= 0 || D->E <= 0 || D->K <= 0 || D->I <= 0 || D->S < 0 ||
+      D->Is < 0)
+    return false;
+  if (!(D->c > 0.0f) || !(D->eps >= 0.0f)) return false;
+  return true;
+}
+
+static int dims_supported(const lmoe_dims* D) {
+  if (!dims_ok(D)) return LMOE_ERR_INVALID_ARG;
+  if (D->d % 64 || D->L % 64 || D->I % 64) return LMOE_ERR_UNSUPPORTED;
+  if (D->S > 0 && (D->Is <= 0 || D->Is % 64)) return LMOE_ERR_UNSUPPORTED;
+  if (D->K > D->E || D->K > 32 || D->E > 4096 || D->E % 16) return LMOE_ERR_UNSUPPORTED;
+  if (D->L > 16384) return LMOE_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(D->T) * D->K >= (int64_t{1} << 31)) return LMOE_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(D->E) * 2 * D->I >= (int64_t{1} << 31) ||
+      static_cast<int64_t>(D->E) * D->L >= (int64_t{1} << 31))
+    return LMOE_ERR_UNSUPPORTED;
+  return LMOE_OK;
+}
+
+static int shared_width(const lmoe_dims& D) { return D.S > 0 ? D.S * D.Is : 0; }
+
+PackedLayout packed_layout(const lmoe_dims& D) {
+  PackedLayout P{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off += align_up(bytes, 1024);
+    return o;
+  };
+  const size_t sw = static_cast<size_t>(shared_width(D));
+  P.w1 = take((static_cast<size_t>(D.L) + 2 * sw) * D.d * 2);
+  P.wr = take(static_cast<size_t>(D.E) * D.L * 2);
+  P.wgu = take(static_cast<size_t>(D.E) * 2 * D.I * D.L * 2);
+  P.wed = take(static_cast<size_t>(D.E) * D.L * D.I * 2);
+  P.w2 = take(static_cast<size_t>(D.d) * (D.L + sw) * 2);
+  P.gamma = take(static_cast<size_t>(D.L) * 4);
+  P.total = off;
+  return P;
+}
+
+WorkspaceLayout workspace_layout(const lmoe_dims& D) {
+  WorkspaceLayout W{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off += align_up(bytes > 0 ? bytes : 1, 256);
+    return o;
+  };
+  const size_t T = static_cast<size_t>(D.T), TK = T * D.K;
+  const size_t nb = static_cast<size_t>(ceil_div(D.T, DISPATCH_TOKENS));
+  W.err = take(256);
+  W.lat = take(T * D.L * 2);
+  W.logits = take(T * D.E * 4);
+  W.tau = take(static_cast<size_t>(D.E) * 4);
+  W.idx = take(TK * 4);
+  W.gate = take(TK * 4);
+  W.masks = take(nb * D.E * 4);
+  W.base = take(nb * D.E * 4);
+  W.offsets = take((static_cast<size_t>(D.E) + 1) * 4);
+  W.mt_off = take((static_cast<size_t>(D.E) + 1) * 4);
+  W.inv = take(TK * 4);
+  W.lat_p = take(TK * D.L * 2);
+  W.h = take(TK * D.I * 2);
+  W.o = take(TK * D.L * 2);
+  W.zh = take(T * (D.L + shared_width(D)) * 2);
+  W.total = off;
+  return W;
+}
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+static uint64_t wait_limit_ns() {
+  // Upper bound of any single device-side wait.  Legitimate waits last microseconds.
+  const char* s = getenv("LMOE_WAIT_LIMIT_MS");
+  if (s && *s) {
+    const long v = strtol(s, nullptr, 10);
+    if (v > 0 && v < 60000) return static_cast<uint64_t>(v) * 1000000ull;
+  }
+  return 2000ull * 1000000ull;
+}
+
+// Test hook: LMOE_FAULT_INJECT=stall makes the first GEMM of each call wait on a barrier
+// that nothing arrives on, so the bounded-wait error path can be exercised without any
+// fault.  Read at every call.
+static bool inject_stall() {
+  const char* s = getenv("LMOE_FAULT_INJECT");
+  return s && strcmp(s, "stall") == 0;
+}
+
+static GemmArgs gemm_defaults(uint32_t* err, float c) {
+  GemmArgs g{};
+  g.err = err;
+  g.c = c;
+  g.timeout_ns = wait_limit_ns();
+  return g;
+}
+
+}  // namespace lmoe
+
+using namespace lmoe;
+
+extern "C" {
+
+const char* lmoe_error_string(int status) {
+  switch (status) {
+    case LMOE_OK: return "ok";
+    case LMOE_ERR_INVALID_ARG: return "invalid argument";
+    case LMOE_ERR_UNSUPPORTED: return "unsupported shape";
+    case LMOE_ERR_CUDA: return "CUDA call or kernel launch failed";
+    case LMOE_ERR_DEVICE_TIMEOUT: return "a device-side wait ran out of time";
+    case LMOE_ERR_WORKSPACE_TOO_SMALL: return "workspace or packed buffer too small";
+    default: return "unknown status";
+  }
+}
+
+const char* lmoe_version(void) { return "lmoe 0.1 sm_103a"; }
+
+size_t lmoe_packed_bytes(const lmoe_dims* dims) {
+  if (dims_supported(dims) != LMOE_OK) return 0;
+  return packed_layout(*dims).total;
+}
+
+size_t lmoe_workspace_bytes(const lmoe_dims* dims) {
+  if (dims_supported(dims) != LMOE_OK) return 0;
+  return workspace_layout(*dims).total;
+}
+
+int lmoe_pack_weights(const lmoe_dims* dims, const lmoe_weights* w, void* packed,
+                      size_t packed_bytes, void* stream) {
+  const int rc = dims_supported(dims);
+  if (rc != LMOE_OK) return rc;
+  if (!w || !packed || !w->w_down || !w->w_router || !w->w_gate || !w->w_value || !w->w_edown ||
+      !w->gamma || !w->w_up)
+    return LMOE_ERR_INVALID_ARG;
+  if (dims->S > 0 && (!w->w_sgate || !w->w_svalue || !w->w_sdown)) return LMOE_ERR_INVALID_ARG;
+  const void* ptrs[] = {packed,  w->w_down,  w->w_router, w->w_gate,   w->w_value,
+                        w->w_edown, w->gamma, w->w_up};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return LMOE_ERR_INVALID_ARG;
+  if (dims->S > 0 && (!aligned16(w->w_sgate) || !aligned16(w->w_svalue) || !aligned16(w->w_sdown)))
+    return LMOE_ERR_INVALID_ARG;
+  const PackedLayout P = packed_layout(*dims);
+  if (packed_bytes < P.total) return LMOE_ERR_WORKSPACE_TOO_SMALL;
+  return launch_pack(*dims, *w, P, static_cast<uint8_t*>(packed),
+                     static_cast<cudaStream_t>(stream));
+}
+
+int lmoe_thresholds(const float* logits, int T, int E, int K, int k_rank, float* tau,
+                    void* stream) {
+  if (T < 0 || E < 1 || K < 1 || k_rank > T) return LMOE_ERR_INVALID_ARG;
+  if (T == 0) return LMOE_OK;
+  if (!logits || !tau) return LMOE_ERR_INVALID_ARG;
+  int k = k_rank;
+  if (k <= 0) {
+    const int64_t f = static_cast<int64_t>(T) * K / E;
+    k = static_cast<int>(f < 1 ? 1 : (f > T ? T : f));
+  }
+  return launch_thresholds(logits, T, E, k, tau, static_cast<cudaStream_t>(stream));
+}
+
+int lmoe_route(const float* logits, const float* tau, int T, int E, int K, int32_t* idx,
+               float* gate, float* scores_out, void* stream) {
+  if (T < 0 || E < 1 || K < 1) return LMOE_ERR_INVALID_ARG;
+  if (K > E || K > 32 || E > 4096) return LMOE_ERR_UNSUPPORTED;
+  if (T == 0) return LMOE_OK;
+  if (!logits || !idx || !gate) return LMOE_ERR_INVALID_ARG;
+  return launch_route(logits, tau, T, E, K, idx, gate, scores_out,
+                      static_cast<cudaStream_t>(stream));
+}
+
+int lmoe_gemm_bf16(const void* A, const void* B, float* C, int M, int N, int Kd,
+                   uint32_t* dev_flag, void* stream) {
+  if (M < 0 || N <= 0 || Kd <= 0 || !C || !A || !B || !dev_flag) return LMOE_ERR_INVALID_ARG;
+  if (N % 16 || Kd % 64) return LMOE_ERR_UNSUPPORTED;
+  if (!aligned16(A) || !aligned16(B) || !aligned16(C)) return LMOE_ERR_INVALID_ARG;
+  if (M == 0) return LMOE_OK;
+  GemmArgs g = gemm_defaults(dev_flag, 1.0f);
+  g.M = M;
+  g.N = N;
+  g.Kd = Kd;
+  g.epi = EPI_F32;
+  g.outf = C;
+  g.ldf = N;
+  return launch_gemm(A, static_cast<uint64_t>(M), Kd, B, static_cast<uint64_t>(N), Kd, g,
+                     static_cast<cudaStream_t>(stream));
+}
+
+int lmoe_last_device_error(void* workspace) {
+  if (!workspace) return LMOE_ERR_INVALID_ARG;
+  uint32_t flag = 0;
+  if (cudaMemcpy(&flag, workspace, sizeof flag, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return LMOE_ERR_CUDA;
+  if (flag == 0) return LMOE_OK;
+  const uint32_t zero = 0;
+  if (cudaMemcpy(workspace, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
+    return LMOE_ERR_CUDA;
+  if (flag & DEVERR_BAD_INDEX) return LMOE_ERR_INVALID_ARG;
+  return LMOE_ERR_DEVICE_TIMEOUT;
+}
+
+int lmoe_forward(const lmoe_dims* dims, const void* packed, const void* x, const void* residual,
+                 void* y, void* workspace, size_t ws_bytes, const lmoe_io* io, void* stream_) {
+  int rc = dims_supported(dims);
+  if (rc != LMOE_OK) return rc;
+  const lmoe_dims D = *dims;
+  if (D.T == 0) return LMOE_OK;
+  if (!packed || !x || !y || !workspace) return LMOE_ERR_INVALID_ARG;
+  if (!aligned16(packed) || !aligned16(x) || !aligned16(y) || !aligned16(workspace) ||
+      (residual && !aligned16(residual)))
+    return LMOE_ERR_INVALID_ARG;
+  if (y == x || (residual && y == residual)) return LMOE_ERR_INVALID_ARG;
+  const WorkspaceLayout W = workspace_layout(D);
+  if (ws_bytes < W.total) return LMOE_ERR_WORKSPACE_TOO_SMALL;
+  lmoe_io opt{};
+  opt.balance = 1;
+  if (io) opt = *io;
+  if ((opt.tau_in && !aligned16(opt.tau_in)) || (opt.logits_in && !aligned16(opt.logits_in)))
+    return LMOE_ERR_INVALID_ARG;
+
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  using bf = __nv_bfloat16;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const uint8_t* pk = static_cast<const uint8_t*>(packed);
+  const PackedLayout P = packed_layout(D);
+  uint32_t* err = reinterpret_cast<uint32_t*>(ws + W.err);
+  bf* lat = reinterpret_cast<bf*>(ws + W.lat);
+  bf* zh = reinterpret_cast<bf*>(ws + W.zh);
+  const int sw = shared_width(D);
+  const int ldz = D.L + sw;
+  const int T = D.T, TK = D.T * D.K;
+
+  if (cudaMemsetAsync(err, 0, sizeof(uint32_t), stream) != cudaSuccess) return LMOE_ERR_CUDA;
+
+  // 1. x . [W_down ; W_shared_gate/value]^T: latent (bf16) and SiTU(shared) into zh[:, L:]
+  {
+    GemmArgs g = gemm_defaults(err, D.c);
+    g.M = T;
+    g.N = D.L + 2 * sw;
+    g.Kd = D.d;
+    g.epi = EPI_SPLIT;
+    g.split = D.L;
+    g.out0 = lat;
+    g.ld0 = D.L;
+    g.out1 = zh + D.L;
+    g.ld1 = ldz;
+    g.inject_stall = inject_stall() ? 1 : 0;
+    rc = launch_gemm(x, T, D.d, pk + P.w1, static_cast<uint64_t>(g.N), D.d, g, stream);
+    if (rc != LMOE_OK) return rc;
+  }
+  // 2. router logits = lat . W_r^T (fp32), unless the caller supplies them
+  const float* logits = opt.logits_in;
+  if (!logits) {
+    GemmArgs g = gemm_defaults(err, D.c);
+    g.M = T;
+    g.N = D.E;
+    g.Kd = D.L;
+    g.epi = EPI_F32;
+    g.outf = reinterpret_cast<float*>(ws + W.logits);
+    g.ldf = D.E;
+    rc = launch_gemm(lat, T, D.L, pk + P.wr, static_cast<uint64_t>(D.E), D.L, g, stream);
+    if (rc != LMOE_OK) return rc;
+    logits = g.outf;
+  }
+  // 3. thresholds
+  const float* tau = opt.tau_in;
+  if (!tau && opt.balance) {
+    float* t = reinterpret_cast<float*>(ws + W.tau);
+    const int64_t f = static_cast<int64_t>(T) * D.K / D.E;
+    const int k = static_cast<int>(f < 1 ? 1 : (f > T ? T : f));
+    rc = launch_thresholds(logits, T, D.E, k, t, stream);
+    if (rc != LMOE_OK) return rc;
+    tau = t;
+  }
+  // 4. top-K routing
+  int32_t* idx = reinterpret_cast<int32_t*>(ws + W.idx);
+  float* gate = reinterpret_cast<float*>(ws + W.gate);
+  rc = launch_route(logits, tau, T, D.E, D.K, idx, gate, nullptr, stream);
+  if (rc != LMOE_OK) return rc;
+  // 5. dispatch into expert-contiguous segments
+  int32_t* offsets = reinterpret_cast<int32_t*>(ws + W.offsets);
+  int32_t* mt_off = reinterpret_cast<int32_t*>(ws + W.mt_off);
+  int32_t* inv = reinterpret_cast<int32_t*>(ws + W.inv);
+  bf* lat_p = reinterpret_cast<bf*>(ws + W.lat_p);
+  rc = launch_dispatch(idx, lat, T, D.E, D.K, D.L, reinterpret_cast<uint32_t*>(ws + W.masks),
+                       reinterpret_cast<uint32_t*>(ws + W.base), offsets, mt_off, inv, lat_p,
+                       opt.counts_out, err, stream);
+  if (rc != LMOE_OK) return rc;
+  // 6. grouped gate/value GEMM with SiTU-GLU: h = SiTU(lat_p . W_gu[e]^T)
+  bf* h = reinterpret_cast<bf*>(ws + W.h);
+  {
+    GemmArgs g = gemm_defaults(err, D.c);
+    g.grouped = 1;
+    g.E = D.E;
+    g.seg_off = offsets;
+    g.mt_off = mt_off;
+    g.N = 2 * D.I;
+    g.Kd = D.L;
+    g.epi = EPI_SITU;
+    g.out1 = h;
+    g.ld1 = D.I;
+    rc = launch_gemm(lat_p, static_cast<uint64_t>(TK), D.L, pk + P.wgu,
+                     static_cast<uint64_t>(D.E) * 2 * D.I, D.L, g, stream);
+    if (rc != LMOE_OK) return rc;
+  }
+  // 7. grouped down GEMM: o = h . W_ed[e]^T
+  bf* o = reinterpret_cast<bf*>(ws + W.o);
+  {
+    GemmArgs g = gemm_defaults(err, D.c);
+    g.grouped = 1;
+    g.E = D.E;
+    g.seg_off = offsets;
+    g.mt_off = mt_off;
+    g.N = D.L;
+    g.Kd = D.I;
+    g.epi = EPI_BF16;
+    g.out0 = o;
+    g.ld0 = D.L;
+    rc = launch_gemm(h, static_cast<uint64_t>(TK), D.I, pk + P.wed,
+                     static_cast<uint64_t>(D.E) * D.L, D.I, g, stream);
+    if (rc != LMOE_OK) return rc;
+  }
+  // 8. gate-weighted combine + RMSNorm -> zh[:, :L]
+  rc = launch_combine(o, gate, inv, reinterpret_cast<const float*>(pk + P.gamma), T, D.K, D.L,
+                      D.eps, zh, ldz, stream);
+  if (rc != LMOE_OK) return rc;
+  // 9. y = residual + [z | hs] . [W_up | W_sd]^T
+  {
+    GemmArgs g = gemm_defaults(err, D.c);
+    g.M = T;
+    g.N = D.d;
+    g.Kd = ldz;
+    g.epi = EPI_RESID;
+    g.out0 = static_cast<bf*>(y);
+    g.ld0 = D.d;
+    g.resid = static_cast<const bf*>(residual);
+    g.ldr = D.d;
+    rc = launch_gemm(zh, T, ldz, pk + P.w2, static_cast<uint64_t>(D.d), ldz, g, stream);
+    if (rc != LMOE_OK) return rc;
+  }
+  // debug outputs
+  auto copy = [&](void* dst, const void* src, size_t bytes) {
+    return cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, stream) == cudaSuccess;
+  };
+  if (opt.logits_out && !copy(opt.logits_out, logits, static_cast<size_t>(T) * D.E * 4))
+    return LMOE_ERR_CUDA;
+  if (opt.tau_out) {
+    const bool ok = tau ? copy(opt.tau_out, tau, static_cast<size_t>(D.E) * 4)
+                        : cudaMemsetAsync(opt.tau_out, 0, static_cast<size_t>(D.E) * 4,
+                                          stream) == cudaSuccess;
+    if (!ok) return LMOE_ERR_CUDA;
+  }
+  if (opt.idx_out && !copy(opt.idx_out, idx, static_cast<size_t>(TK) * 4)) return LMOE_ERR_CUDA;
+  if (opt.gate_out && !copy(opt.gate_out, gate, static_cast<size_t>(TK) * 4))
+    return LMOE_ERR_CUDA;
+  return LMOE_OK;
+}
+
+}  // extern "C"

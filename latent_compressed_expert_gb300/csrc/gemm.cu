@@ -1,0 +1,460 @@
+// gemm.cu -- persistent, warp-specialised bf16 GEMM on the 5th-generation tensor cores.
+//
+//   C[M, N] = A[M, Kd] . B[N, Kd]^T      (A and B K-major, fp32 accumulation in TMEM)
+//
+// One CTA per SM walks a list of 128 x BN output tiles (BN = 128 or 256):
+//   warp 0      TMA producer: 64-wide K slices of A (128 rows) and B (BN rows) into a ring
+//               of shared-memory stages, completing on per-stage "full" mbarriers;
+//   warp 1      allocates 2 x BN TMEM columns (two accumulators) and issues
+//               tcgen05.mma (M=128, N=BN, K=16) from one thread; tcgen05.commit frees each
+//               stage ("empty") and announces each finished accumulator ("tmem_full");
+//   warps 2-5   epilogue: tcgen05.ld of 32 columns at a time, the fused operation (plain
+//               bf16 / fp32 store, SiTU-GLU on interleaved gate/value columns, residual add),
+//               then release the accumulator ("tmem_empty") so the MMA of the tile after
+//               next can start while this one is written out.
+// Grouped mode runs one GEMM per expert segment: A rows are the expert's contiguous rows
+// of the permuted activations (segment offsets produced on the device), B rows the
+// expert's weight slice; tiles are enumerated from a device-side prefix sum of row-tile
+// counts, so no count ever travels back to the host.
+//
+// Every wait is bounded (globaltimer); on time-out a role records an error bit in global
+// memory, raises a shared abort flag that makes the other roles give up too, waits for
+// its in-flight copies and MMAs, and the CTA frees its TMEM and exits.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.cuh"
+#include "ptx.cuh"
+
+namespace lmoe {
+
+template <int BN>
+struct GemmCfg {
+  static constexpr int A_BYTES = BLOCK_M * BLOCK_K * 2;
+  static constexpr int B_BYTES = BN * BLOCK_K * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES = (BN == 256) ? 4 : 6;
+  static constexpr int TMEM_COLS = 2 * BN;
+  static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
+  static constexpr int NUM_BARS = 2 * STAGES + 6;
+  static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
+  static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;  // + slack for 1024 alignment
+  static constexpr uint32_t IDESC = ptx::idesc_bf16_f32(BLOCK_M, BN);
+  static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "tiles must stay 1024-aligned");
+  static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+};
+
+constexpr int GEMM_THREADS = 192;
+constexpr int RASTER_GROUP_M = 16;
+
+struct TileCoord {
+  int a_row;    // first row of A (and of the output) of this tile
+  int row_end;  // rows >= row_end are not part of this problem
+  int b_row;    // first row of B
+  int n0;       // first output column
+};
+
+template <int BN>
+__device__ __forceinline__ TileCoord decode_tile(const GemmArgs& g, int nt, int mt_dense,
+                                                 int tile) {
+  TileCoord c;
+  if (!g.grouped) {
+    // groups of RASTER_GROUP_M row tiles sweep all column tiles, rows fastest, so the
+    // CTAs in flight share a few A row-panels and B column-panels in L2
+    const int span = RASTER_GROUP_M * nt;
+    const int grp = tile / span;
+    const int first_m = grp * RASTER_GROUP_M;
+    const int gm = min(RASTER_GROUP_M, mt_dense - first_m);
+    const int local = tile - grp * span;
+    const int m = first_m + local % gm;
+    const int n = local / gm;
+    c.a_row = m * BLOCK_M;
+    c.row_end = g.M;
+    c.b_row = n * BN;
+    c.n0 = n * BN;
+  } else {
+    // tiles of expert e occupy [mt_off[e] * nt, mt_off[e+1] * nt); rows fastest so the
+    // row tiles of one expert that share a weight slice run side by side
+    const int q = tile / nt;
+    int lo = 0, hi = g.E;  // mt_off[lo] <= q < mt_off[hi]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (__ldg(g.mt_off + mid) <= q)
+        lo = mid;
+      else
+        hi = mid;
+    }
+    const int e = lo;
+    const int mt0 = __ldg(g.mt_off + e);
+    const int mte = __ldg(g.mt_off + e + 1) - mt0;
+    const int local = tile - mt0 * nt;
+    const int n = local / mte, m = local % mte;
+    c.a_row = __ldg(g.seg_off + e) + m * BLOCK_M;
+    c.row_end = __ldg(g.seg_off + e + 1);
+    c.b_row = e * g.N + n * BN;
+    c.n0 = n * BN;
+  }
+  return c;
+}
+
+__device__ __forceinline__ void raise_error(const GemmArgs& g, volatile int* abort_flag,
+                                            uint32_t code) {
+  *abort_flag = 1;
+  atomicOr(g.err, code);
+}
+
+// Bounded wait that ignores the abort flag (used to drain in-flight work).
+__device__ __forceinline__ bool wait_drain(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = ptx::globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 0u && ptx::globaltimer_ns() - t0 > limit_ns) return false;
+  }
+}
+
+__device__ __forceinline__ uint4 pack8_bf16(const float* v) {
+  uint4 w;
+  __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&w);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+  return w;
+}
+
+__device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const float (&v)[32]) {
+  uint4* o = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) o[q] = pack8_bf16(v + 8 * q);
+}
+
+// SiTU-GLU: silu(c tanh(g/c)) * c tanh(v/c).  ("The 2.8-Trillion-Parameter Problem",
+// Technical Details / Stabilization Mechanisms: gate and value smoothly capped to about
+// +-100, SwiGLU-like near zero; the tanh cap is this library's reading of "smoothly caps".)
+__device__ __forceinline__ float situ(float g, float v, float c, float inv_c) {
+  const float gc = c * ptx::tanh_approx(g * inv_c);
+  const float vc = c * ptx::tanh_approx(v * inv_c);
+  const float sg = __fdividef(gc, 1.0f + __expf(fminf(-gc, 80.0f)));
+  return sg * vc;
+}
+
+// 32 accumulator columns = 16 gate (0..15) + the matching 16 value (16..31) -> 16 outputs.
+__device__ __forceinline__ void store_situ16(__nv_bfloat16* dst, const float (&v)[32], float c,
+                                             float inv_c) {
+  float o[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) o[i] = situ(v[i], v[16 + i], c, inv_c);
+  uint4* p = reinterpret_cast<uint4*>(dst);
+  p[0] = pack8_bf16(o);
+  p[1] = pack8_bf16(o + 8);
+}
+
+__device__ __forceinline__ void epilogue_store(const GemmArgs& g, int row, int col0,
+                                               float (&v)[32], float c, float inv_c) {
+  const size_t r = static_cast<size_t>(row);
+  switch (g.epi) {
+    case EPI_BF16:
+      store_bf16x32(g.out0 + r * g.ld0 + col0, v);
+      break;
+    case EPI_F32: {
+      float4* o = reinterpret_cast<float4*>(g.outf + r * g.ldf + col0);
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        o[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+      break;
+    }
+    case EPI_SITU:
+      store_situ16(g.out1 + r * g.ld1 + col0 / 2, v, c, inv_c);
+      break;
+    case EPI_SPLIT:
+      if (col0 < g.split)
+        store_bf16x32(g.out0 + r * g.ld0 + col0, v);
+      else
+        store_situ16(g.out1 + r * g.ld1 + (col0 - g.split) / 2, v, c, inv_c);
+      break;
+    case EPI_RESID:
+    default: {
+      if (g.resid) {
+        const uint4* rp = reinterpret_cast<const uint4*>(g.resid + r * g.ldr + col0);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint4 raw = __ldg(rp + q);
+          const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float2 f = __bfloat1622float2(h[i]);
+            v[8 * q + 2 * i] += f.x;
+            v[8 * q + 2 * i + 1] += f.y;
+          }
+        }
+      }
+      store_bf16x32(g.out0 + r * g.ld0 + col0, v);
+      break;
+    }
+  }
+}
+
+// Last, partly valid 32-column slice (plain stores only; the GLU modes need whole slices).
+__device__ __forceinline__ void epilogue_store_partial(const GemmArgs& g, int row, int col0,
+                                                   int ncols, const float (&v)[32]) {
+  const size_t r = static_cast<size_t>(row);
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    if (i >= ncols) break;
+    const int col = col0 + i;
+    if (g.epi == EPI_F32) {
+      g.outf[r * g.ldf + col] = v[i];
+    } else if (g.epi == EPI_BF16) {
+      g.out0[r * g.ld0 + col] = __float2bfloat16_rn(v[i]);
+    } else if (g.epi == EPI_RESID) {
+      const float rv = g.resid ? __bfloat162float(g.resid[r * g.ldr + col]) : 0.0f;
+      g.out0[r * g.ld0 + col] = __float2bfloat16_rn(v[i] + rv);
+    }
+  }
+}
+
+template <int BN>
+__global__ void __launch_bounds__(GEMM_THREADS, 1)
+gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA,
+                    const __grid_constant__ CUtensorMap tmB, const GemmArgs g) {
+  using C = GemmCfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = ptx::smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
+  uint64_t* empty = full + C::STAGES;
+  uint64_t* tfull = empty + C::STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint64_t* stall = drain + 1;  // never arrived on (fault-injection hook)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::MISC_OFF);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nt = (g.N + BN - 1) / BN;
+  const int nk = g.Kd / BLOCK_K;
+  const int mt_dense = g.grouped ? 0 : (g.M + BLOCK_M - 1) / BLOCK_M;
+  const int total = g.grouped ? __ldg(g.mt_off + g.E) * nt : mt_dense * nt;
+  const uint64_t limit = g.timeout_ns;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      ptx::mbar_init(&full[s], 1);
+      ptx::mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      ptx::mbar_init(&tfull[a], 1);
+      ptx::mbar_init(&tempty[a], 128);
+    }
+    ptx::mbar_init(drain, 1);
+    ptx::mbar_init(stall, 1);
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::prefetch_tmap(&tmA);
+    ptx::prefetch_tmap(&tmB);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(tmem_slot, C::TMEM_COLS);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ TMA producer
+      uint32_t it = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+        const TileCoord tc = decode_tile<BN>(g, nt, mt_dense, tile);
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int s = static_cast<int>(it % C::STAGES);
+          const uint32_t ph = (it / C::STAGES) & 1u;
+          if (!ptx::mbar_wait(&empty[s], ph ^ 1u, abort_flag, limit)) {
+            raise_error(g, abort_flag, DEVERR_TIMEOUT_PRODUCER);
+            ok = false;
+            break;
+          }
+          uint8_t* sa = smem + s * C::STAGE_BYTES;
+          ptx::mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
+          ptx::tma_load_2d(sa, &tmA, &full[s], kb * BLOCK_K, tc.a_row);
+          ptx::tma_load_2d(sa + C::A_BYTES, &tmB, &full[s], kb * BLOCK_K, tc.b_row);
+        }
+      }
+      // every issued copy must land before the CTA may exit
+      const uint32_t first = it > static_cast<uint32_t>(C::STAGES) ? it - C::STAGES : 0u;
+      for (uint32_t j = first; j < it; ++j) {
+        if (!wait_drain(&full[j % C::STAGES], (j / C::STAGES) & 1u, limit)) {
+          raise_error(g, abort_flag, DEVERR_TIMEOUT_DRAIN);
+          break;
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ MMA issuer
+      uint32_t it = 0;
+      int lt = 0;
+      bool stalled = false;
+      if (g.inject_stall && !ptx::mbar_wait(stall, 0u, abort_flag, limit)) {
+        raise_error(g, abort_flag, DEVERR_TIMEOUT_MMA);
+        stalled = true;
+      }
+      for (int tile = blockIdx.x; !stalled && tile < total; tile += gridDim.x, ++lt) {
+        const int acc = lt & 1;
+        const uint32_t aph = static_cast<uint32_t>(lt >> 1) & 1u;
+        if (!ptx::mbar_wait(&tempty[acc], aph ^ 1u, abort_flag, limit)) {
+          raise_error(g, abort_flag, DEVERR_TIMEOUT_MMA);
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        bool ok = true;
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int s = static_cast<int>(it % C::STAGES);
+          const uint32_t ph = (it / C::STAGES) & 1u;
+          if (!ptx::mbar_wait(&full[s], ph, abort_flag, limit)) {
+            raise_error(g, abort_flag, DEVERR_TIMEOUT_MMA);
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t sa = ptx::smem_u32(smem + s * C::STAGE_BYTES);
+          const uint32_t sb = sa + C::A_BYTES;
+#pragma unroll
+          for (int k = 0; k < BLOCK_K / 16; ++k)
+            ptx::umma_bf16(d_tmem, ptx::smem_desc_sw128(sa + k * 32),
+                           ptx::smem_desc_sw128(sb + k * 32), C::IDESC, (kb | k) != 0 ? 1u : 0u);
+          ptx::umma_commit(&empty[s]);
+        }
+        if (!ok) break;
+        ptx::umma_commit(&tfull[acc]);
+      }
+      // all MMAs issued by this thread complete before TMEM is released
+      ptx::umma_commit(drain);
+      if (!wait_drain(drain, 0u, limit)) raise_error(g, abort_flag, DEVERR_TIMEOUT_DRAIN);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue (warps 2..5)
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const float c = g.c, inv_c = 1.0f / g.c;
+    int lt = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++lt) {
+      const int acc = lt & 1;
+      const uint32_t aph = static_cast<uint32_t>(lt >> 1) & 1u;
+      const bool got = ptx::mbar_wait(&tfull[acc], aph, abort_flag, limit);
+      if (!__all_sync(0xffffffffu, got)) {
+        if (lane == 0) raise_error(g, abort_flag, DEVERR_TIMEOUT_EPILOGUE);
+        break;
+      }
+      ptx::tc_fence_after();
+      const TileCoord tc = decode_tile<BN>(g, nt, mt_dense, tile);
+      const int row = tc.a_row + q * 32 + lane;
+      const bool row_ok = row < tc.row_end;
+      const uint32_t tbase =
+          tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
+#pragma unroll 1
+      for (int ch = 0; ch < BN / 32; ++ch) {
+        const int col0 = tc.n0 + ch * 32;
+        if (col0 >= g.N) break;  // uniform across the warp
+        float v[32];
+        ptx::tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(ch * 32), v);
+        if (row_ok) {
+          if (col0 + 32 <= g.N)
+            epilogue_store(g, row, col0, v, c, inv_c);
+          else
+            epilogue_store_partial(g, row, col0, g.N - col0, v);
+        }
+      }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(&tempty[acc]);
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------------------------
+// host side
+// ------------------------------------------------------------------------------------
+static PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+bool make_tmap_bf16(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint64_t ld,
+                    uint32_t box_rows) {
+  auto enc = tmap_encoder();
+  if (!enc || rows == 0 || cols == 0 || (reinterpret_cast<uintptr_t>(ptr) & 15u) != 0 ||
+      (ld * 2) % 16 != 0)
+    return false;
+  const cuuint64_t gdim[2] = {cols, rows};
+  const cuuint64_t gstride[1] = {ld * 2};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(BLOCK_K), box_rows};
+  const cuuint32_t estride[2] = {1, 1};
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), gdim,
+                         gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int BN>
+static int launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& g,
+                     cudaStream_t stream) {
+  using C = GemmCfg<BN>;
+  if (cudaFuncSetAttribute(gemm_tcgen05_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           C::SMEM_BYTES) != cudaSuccess)
+    return LMOE_ERR_CUDA;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return LMOE_ERR_CUDA;
+  int grid = sms;
+  if (!g.grouped) {
+    const int64_t tiles = ceil_div(g.M, BLOCK_M) * ceil_div(g.N, BN);
+    if (tiles < grid) grid = static_cast<int>(tiles);
+  }
+  if (grid <= 0) return LMOE_OK;
+  gemm_tcgen05_kernel<BN><<<grid, GEMM_THREADS, C::SMEM_BYTES, stream>>>(ta, tb, g);
+  return cudaGetLastError() == cudaSuccess ? LMOE_OK : LMOE_ERR_CUDA;
+}
+
+int launch_gemm(const void* A, uint64_t a_rows, int a_ld, const void* B, uint64_t b_rows,
+                int b_ld, const GemmArgs& g, cudaStream_t stream) {
+  if (g.Kd % BLOCK_K != 0 || g.Kd <= 0 || g.N <= 0) return LMOE_ERR_UNSUPPORTED;
+  const bool glu = g.epi == EPI_SITU || g.epi == EPI_SPLIT;
+  if (g.N % (glu ? 32 : 16) != 0 || (g.epi == EPI_SPLIT && g.split % 32 != 0))
+    return LMOE_ERR_UNSUPPORTED;
+  if (!g.grouped && g.M == 0) return LMOE_OK;
+  const int bn = (g.N % 256 == 0) ? 256 : 128;
+  CUtensorMap ta, tb;
+  if (!make_tmap_bf16(&ta, A, a_rows, static_cast<uint64_t>(g.Kd), static_cast<uint64_t>(a_ld),
+                      BLOCK_M) ||
+      !make_tmap_bf16(&tb, B, b_rows, static_cast<uint64_t>(g.Kd), static_cast<uint64_t>(b_ld),
+                      static_cast<uint32_t>(bn)))
+    return LMOE_ERR_CUDA;
+  return bn == 256 ? launch_bn<256>(ta, tb, g, stream) : launch_bn<128>(ta, tb, g, stream);
+}
+
+}  // namespace lmoe

@@ -1,0 +1,81 @@
+// kernels.cuh -- internal launchers and buffer layouts of the lmoe library.
+#pragma once
+
+#include <cuda.h>
+#include <stddef.h>
+
+#include "common.cuh"
+
+namespace lmoe {
+
+// Offsets (bytes) of the pieces of the packed weight buffer; every piece 1024-aligned.
+struct PackedLayout {
+  size_t w1, wr, wgu, wed, w2, gamma, total;
+};
+
+// Offsets (bytes) of the forward workspace; every buffer 256-aligned.
+struct WorkspaceLayout {
+  size_t err, lat, logits, tau, idx, gate, masks, base, offsets, mt_off, inv, lat_p, h, o, zh,
+      total;
+};
+
+PackedLayout packed_layout(const lmoe_dims& D);
+WorkspaceLayout workspace_layout(const lmoe_dims& D);
+
+// Epilogues of the tcgen05 GEMM.
+enum EpiMode : int {
+  EPI_BF16 = 0,   // out0[r, c] = bf16(acc)
+  EPI_F32 = 1,    // outf[r, c] = acc
+  EPI_SITU = 2,   // out1[r, c/2 + i] = bf16(SiTU(gate_i, value_i)) over 16+16 interleave
+  EPI_SPLIT = 3,  // columns < split: EPI_BF16 to out0; others: EPI_SITU to out1 (c - split)
+  EPI_RESID = 4   // out0[r, c] = bf16(acc + resid[r, c]) (resid may be null)
+};
+
+struct GemmArgs {
+  int M;                  // dense: rows of A and of the output
+  int N;                  // output columns (per group), multiple of 32
+  int Kd;                 // reduction length, multiple of 64
+  int grouped;            // 0: dense; 1: one problem per expert segment
+  int E;                  // groups
+  const int32_t* seg_off; // [E+1] first row of each segment (grouped)
+  const int32_t* mt_off;  // [E+1] prefix sum of the segments' 128-row tile counts
+  int epi;
+  int split;
+  __nv_bfloat16* out0;
+  int ld0;
+  __nv_bfloat16* out1;
+  int ld1;
+  float* outf;
+  int ldf;
+  const __nv_bfloat16* resid;
+  int ldr;
+  float c;                // SiTU cap
+  uint32_t* err;          // device error flag (never null)
+  unsigned long long timeout_ns;
+  int inject_stall;       // test hook: the MMA role first waits on a barrier nobody arrives
+                          // on, so every role runs into its bounded wait and aborts
+};
+
+// Encodes a 2-D bf16 row-major [rows, cols] (row stride ld elements) TMA map with a
+// 64 x box_rows box and the 128-byte swizzle.  Returns false on failure.
+bool make_tmap_bf16(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint64_t ld,
+                    uint32_t box_rows);
+
+int launch_gemm(const void* A, uint64_t a_rows, int a_ld, const void* B, uint64_t b_rows,
+                int b_ld, const GemmArgs& args, cudaStream_t stream);
+
+int launch_route(const float* logits, const float* tau, int T, int E, int K, int32_t* idx,
+                 float* gate, float* scores_out, cudaStream_t stream);
+int launch_thresholds(const float* logits, int T, int E, int k, float* tau,
+                      cudaStream_t stream);
+int launch_dispatch(const int32_t* idx, const __nv_bfloat16* lat, int T, int E, int K, int L,
+                    uint32_t* masks, uint32_t* base, int32_t* offsets, int32_t* mt_off,
+                    int32_t* inv, __nv_bfloat16* lat_p, int32_t* counts_out, uint32_t* err,
+                    cudaStream_t stream);
+int launch_combine(const __nv_bfloat16* o, const float* gate, const int32_t* inv,
+                   const float* gamma, int T, int K, int L, float eps, __nv_bfloat16* z,
+                   int ldz, cudaStream_t stream);
+int launch_pack(const lmoe_dims& D, const lmoe_weights& w, const PackedLayout& P, uint8_t* base,
+                cudaStream_t stream);
+
+}  // namespace lmoe

@@ -1,0 +1,261 @@
+"""ctypes binding of liblmoe.so (include/lmoe.h): argument marshalling only.
+
+Every step of the layer runs in the library's CUDA kernels; PyTorch provides device
+memory and the current stream.  There is no CPU fallback: if the library is missing or
+its CUDA calls fail, these functions raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "liblmoe.so")
+
+LMOE_OK = 0
+LMOE_ERR_INVALID_ARG = 1
+LMOE_ERR_UNSUPPORTED = 2
+LMOE_ERR_CUDA = 3
+LMOE_ERR_DEVICE_TIMEOUT = 4
+LMOE_ERR_WORKSPACE_TOO_SMALL = 5
+
+# Every symbol the header declares, with its ctypes signature.
+_vp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+
+
+class Dims(ctypes.Structure):
+    _fields_ = [("T", _i), ("d", _i), ("L", _i), ("E", _i), ("K", _i), ("I", _i), ("S", _i),
+                ("Is", _i), ("c", _f), ("eps", _f)]
+
+
+class Weights(ctypes.Structure):
+    _fields_ = [(n, _vp) for n in ("w_down", "w_router", "w_gate", "w_value", "w_edown", "gamma",
+                                   "w_up", "w_sgate", "w_svalue", "w_sdown")]
+
+
+class IO(ctypes.Structure):
+    _fields_ = [("tau_in", _vp), ("balance", _i), ("logits_in", _vp), ("logits_out", _vp),
+                ("tau_out", _vp), ("idx_out", _vp), ("gate_out", _vp), ("counts_out", _vp)]
+
+
+SIGNATURES = {
+    "lmoe_packed_bytes": (_sz, [ctypes.POINTER(Dims)]),
+    "lmoe_pack_weights": (_i, [ctypes.POINTER(Dims), ctypes.POINTER(Weights), _vp, _sz, _vp]),
+    "lmoe_workspace_bytes": (_sz, [ctypes.POINTER(Dims)]),
+    "lmoe_thresholds": (_i, [_vp, _i, _i, _i, _i, _vp, _vp]),
+    "lmoe_route": (_i, [_vp, _vp, _i, _i, _i, _vp, _vp, _vp, _vp]),
+    "lmoe_forward": (_i, [ctypes.POINTER(Dims), _vp, _vp, _vp, _vp, _vp, _sz, ctypes.POINTER(IO),
+                          _vp]),
+    "lmoe_gemm_bf16": (_i, [_vp, _vp, _vp, _i, _i, _i, _vp, _vp]),
+    "lmoe_last_device_error": (_i, [_vp]),
+    "lmoe_error_string": (ctypes.c_char_p, [_i]),
+    "lmoe_version": (ctypes.c_char_p, []),
+}
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load():
+    """Load liblmoe.so (built by ``python -m latent_compressed_expert_gb300.build``)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is not built; run "
+                               "`python -m latent_compressed_expert_gb300.build` (needs nvcc)")
+        lib = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+        return lib
+
+
+class LmoeError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        msg = load().lmoe_error_string(code).decode()
+        super().__init__(f"{what}: {msg} (status {code})")
+        self.code = code
+
+
+def _check(code: int, what: str):
+    if code != LMOE_OK:
+        raise LmoeError(code, what)
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("lmoe: tensors must be CUDA device tensors")
+    if not t.is_contiguous():
+        raise ValueError("lmoe: tensors must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _expect(t, dtype, shape, name):
+    if t.dtype != dtype or tuple(t.shape) != tuple(shape):
+        raise ValueError(f"lmoe: {name} must be {dtype} {tuple(shape)}, got {t.dtype} "
+                         f"{tuple(t.shape)}")
+
+
+def make_dims(T, d, L, E, K, I, S, Is, c=100.0, eps=1e-6) -> Dims:
+    return Dims(T, d, L, E, K, I, S, Is, c, eps)
+
+
+def dims_of(shape, T=None) -> Dims:
+    """Dims from an object with T, d, L, E, K, I, S, Is (and optionally c, eps)."""
+    return make_dims(shape.T if T is None else T, shape.d, shape.L, shape.E, shape.K, shape.I,
+                     shape.S, shape.Is, getattr(shape, "c", 100.0), getattr(shape, "eps", 1e-6))
+
+
+def packed_bytes(dims: Dims) -> int:
+    return int(load().lmoe_packed_bytes(ctypes.byref(dims)))
+
+
+def workspace_bytes(dims: Dims) -> int:
+    return int(load().lmoe_workspace_bytes(ctypes.byref(dims)))
+
+
+def pack_weights(dims: Dims, w: dict, stream=None) -> torch.Tensor:
+    """Repack a dict of unpacked weights (bf16 [out, in], gamma fp32) into one device
+    buffer in the layout lmoe_forward reads."""
+    D = dims
+    bf = torch.bfloat16
+    _expect(w["w_down"], bf, (D.L, D.d), "w_down")
+    _expect(w["w_router"], bf, (D.E, D.L), "w_router")
+    _expect(w["w_gate"], bf, (D.E, D.I, D.L), "w_gate")
+    _expect(w["w_value"], bf, (D.E, D.I, D.L), "w_value")
+    _expect(w["w_edown"], bf, (D.E, D.L, D.I), "w_edown")
+    _expect(w["gamma"], torch.float32, (D.L,), "gamma")
+    _expect(w["w_up"], bf, (D.d, D.L), "w_up")
+    if D.S > 0:
+        _expect(w["w_sgate"], bf, (D.S, D.Is, D.d), "w_sgate")
+        _expect(w["w_svalue"], bf, (D.S, D.Is, D.d), "w_svalue")
+        _expect(w["w_sdown"], bf, (D.S, D.d, D.Is), "w_sdown")
+    nbytes = packed_bytes(D)
+    if nbytes == 0:
+        raise LmoeError(LMOE_ERR_UNSUPPORTED, "lmoe_packed_bytes")
+    dev = w["w_down"].device
+    packed = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    W = Weights(*[_ptr(w.get(n)) for n, _ in Weights._fields_])
+    _check(load().lmoe_pack_weights(ctypes.byref(D), ctypes.byref(W), _ptr(packed), nbytes,
+                                    _stream(stream)), "lmoe_pack_weights")
+    return packed
+
+
+def thresholds(logits: torch.Tensor, K: int, k_rank: int = 0, stream=None) -> torch.Tensor:
+    T, E = logits.shape
+    _expect(logits, torch.float32, (T, E), "logits")
+    tau = torch.empty(E, dtype=torch.float32, device=logits.device)
+    _check(load().lmoe_thresholds(_ptr(logits), T, E, K, k_rank, _ptr(tau), _stream(stream)),
+           "lmoe_thresholds")
+    return tau
+
+
+def route(logits: torch.Tensor, tau, K: int, want_scores: bool = False, stream=None):
+    """Returns (idx int32 [T,K], gate fp32 [T,K]) and, with want_scores, scores [T,E]."""
+    T, E = logits.shape
+    _expect(logits, torch.float32, (T, E), "logits")
+    if tau is not None:
+        _expect(tau, torch.float32, (E,), "tau")
+    dev = logits.device
+    idx = torch.empty((T, K), dtype=torch.int32, device=dev)
+    gate = torch.empty((T, K), dtype=torch.float32, device=dev)
+    sc = torch.empty((T, E), dtype=torch.float32, device=dev) if want_scores else None
+    _check(load().lmoe_route(_ptr(logits), _ptr(tau), T, E, K, _ptr(idx), _ptr(gate), _ptr(sc),
+                             _stream(stream)), "lmoe_route")
+    return (idx, gate, sc) if want_scores else (idx, gate)
+
+
+def gemm_bf16(A: torch.Tensor, B: torch.Tensor, stream=None) -> torch.Tensor:
+    """C = A . B^T (fp32) on the tcgen05 GEMM of the library."""
+    M, Kd = A.shape
+    N = B.shape[0]
+    _expect(A, torch.bfloat16, (M, Kd), "A")
+    _expect(B, torch.bfloat16, (N, Kd), "B")
+    C = torch.empty((M, N), dtype=torch.float32, device=A.device)
+    flag = torch.zeros(4, dtype=torch.int32, device=A.device)
+    _check(load().lmoe_gemm_bf16(_ptr(A), _ptr(B), _ptr(C), M, N, Kd, _ptr(flag),
+                                 _stream(stream)), "lmoe_gemm_bf16")
+    return C, flag
+
+
+def last_device_error(workspace: torch.Tensor) -> int:
+    return int(load().lmoe_last_device_error(_ptr(workspace)))
+
+
+class Layer:
+    """One Stable Latent MoE layer on the device: packed weights + a workspace sized for up
+    to ``max_tokens`` tokens.  ``forward`` is one lmoe_forward call."""
+
+    def __init__(self, shape, weights: dict, max_tokens: int | None = None, stream=None):
+        self.shape = shape
+        self.max_tokens = shape.T if max_tokens is None else max_tokens
+        self.dims = dims_of(shape, T=self.max_tokens)
+        self.device = weights["w_down"].device
+        self.packed = pack_weights(self.dims, weights, stream)
+        self.ws_bytes = workspace_bytes(self.dims)
+        self.workspace = torch.empty(self.ws_bytes, dtype=torch.uint8, device=self.device)
+
+    def forward(self, x: torch.Tensor, residual: torch.Tensor | None = None, y=None,
+                tau: torch.Tensor | None = None, balance: bool = True,
+                logits_in: torch.Tensor | None = None, debug: bool = False, stream=None):
+        sh = self.shape
+        T = x.shape[0]
+        if T > self.max_tokens:
+            raise ValueError(f"lmoe: {T} tokens exceed the workspace's {self.max_tokens}")
+        _expect(x, torch.bfloat16, (T, sh.d), "x")
+        if residual is not None:
+            _expect(residual, torch.bfloat16, (T, sh.d), "residual")
+        if y is None:
+            y = torch.empty((T, sh.d), dtype=torch.bfloat16, device=x.device)
+        dims = dims_of(sh, T=T)
+        io = IO()
+        io.balance = 1 if balance else 0
+        dbg = {}
+        if tau is not None:
+            _expect(tau, torch.float32, (sh.E,), "tau")
+            io.tau_in = _ptr(tau)
+        if logits_in is not None:
+            _expect(logits_in, torch.float32, (T, sh.E), "logits_in")
+            io.logits_in = _ptr(logits_in)
+        if debug:
+            dev = x.device
+            dbg["logits"] = torch.empty((T, sh.E), dtype=torch.float32, device=dev)
+            dbg["tau"] = torch.empty(sh.E, dtype=torch.float32, device=dev)
+            dbg["idx"] = torch.empty((T, sh.K), dtype=torch.int32, device=dev)
+            dbg["gate"] = torch.empty((T, sh.K), dtype=torch.float32, device=dev)
+            dbg["counts"] = torch.empty(sh.E, dtype=torch.int32, device=dev)
+            io.logits_out = _ptr(dbg["logits"])
+            io.tau_out = _ptr(dbg["tau"])
+            io.idx_out = _ptr(dbg["idx"])
+            io.gate_out = _ptr(dbg["gate"])
+            io.counts_out = _ptr(dbg["counts"])
+        _check(load().lmoe_forward(ctypes.byref(dims), _ptr(self.packed), _ptr(x), _ptr(residual),
+                                   _ptr(y), _ptr(self.workspace), self.ws_bytes,
+                                   ctypes.byref(io), _stream(stream)), "lmoe_forward")
+        return (y, dbg) if debug else y
+
+    def forward_host(self, x_host: torch.Tensor, y_host: torch.Tensor, x_dev: torch.Tensor,
+                     y_dev: torch.Tensor, residual_from_x: bool = True, stream=None):
+        """End-to-end call from host memory: copy x (pinned host) to the device, run the
+        layer, copy y back to pinned host memory; all on one stream, asynchronous."""
+        x_dev.copy_(x_host, non_blocking=True)
+        self.forward(x_dev, residual=x_dev if residual_from_x else None, y=y_dev, stream=stream)
+        y_host.copy_(y_dev, non_blocking=True)
+        return y_host
+
+    def device_error(self) -> int:
+        return last_device_error(self.workspace)

@@ -79,15 +79,23 @@ def _pick(count: int, frac: float, g: torch.Generator, device) -> torch.Tensor:
     return torch.randperm(count, generator=g, device=device)[:m]
 
 
+def outlier_router_gain(sh: LayerShape, outlier_frac: float, outlier_scale: float) -> float:
+    """Router weight gain that keeps the router logits ~N(0, 1) when x carries outliers:
+    the latent's expected mean square grows from 1 to 1 + frac * (scale^2 - 1), so the
+    router's N(0, 1/fan_in) weights are scaled by the inverse square root of that."""
+    return (1.0 + outlier_frac * (outlier_scale ** 2 - 1.0)) ** -0.5
+
+
 def make_weights(sh: LayerShape, seed: int, device="cpu", hot_row_frac: float = 0.0,
-                 hot_scale: float = 500.0) -> dict:
+                 hot_scale: float = 500.0, router_gain: float = 1.0) -> dict:
     """All weights of one layer, bf16 [out, in] (gamma fp32).  ``hot_row_frac`` > 0 scales
     that fraction (at least one) of the routed and shared gate and value rows by
-    ``hot_scale``."""
+    ``hot_scale``; ``router_gain`` scales the router's standard deviation."""
     bf = torch.bfloat16
     w = {}
     w["w_down"] = _normal((sh.L, sh.d), sh.d ** -0.5, _gen(seed, "w_down", device), device, bf)
-    w["w_router"] = _normal((sh.E, sh.L), sh.L ** -0.5, _gen(seed, "w_router", device), device, bf)
+    w["w_router"] = _normal((sh.E, sh.L), router_gain * sh.L ** -0.5,
+                            _gen(seed, "w_router", device), device, bf)
     w["w_gate"] = _normal((sh.E, sh.I, sh.L), sh.L ** -0.5, _gen(seed, "w_gate", device), device, bf)
     w["w_value"] = _normal((sh.E, sh.I, sh.L), sh.L ** -0.5, _gen(seed, "w_value", device), device, bf)
     w["w_edown"] = _normal((sh.E, sh.L, sh.I), sh.I ** -0.5, _gen(seed, "w_edown", device), device, bf)

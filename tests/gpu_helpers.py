@@ -1,0 +1,82 @@
+"""Shared pieces of the GPU parity tests: running the oracle on a subset of tokens, the
+output tolerance, and the near-tie rule for routing decisions taken on two different
+(but each correct within its precision) sets of router logits."""
+from __future__ import annotations
+
+from dataclasses import replace
+
+import numpy as np
+import torch
+
+from latent_compressed_expert_gb300 import synth
+
+# Output tolerance for bf16 operands with fp32 accumulation (stated for the layer):
+#   max |y - y_ref| <= 2e-2 * RMS(y_ref)   and   sum |y - y_ref| / sum |y_ref| <= 5e-3
+MAX_ERR_REL_RMS = 2e-2
+MEAN_REL_ERR = 5e-3
+
+
+def error_stats(y, ref):
+    y = np.asarray(y, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    err = np.abs(y - ref)
+    rms = float(np.sqrt(np.mean(ref * ref)))
+    return {"max_err": float(err.max()), "rms_ref": rms,
+            "max_err_over_rms": float(err.max() / rms) if rms > 0 else float("inf"),
+            "mean_rel_err": float(err.sum() / max(np.abs(ref).sum(), 1e-300))}
+
+
+def assert_close(y, ref, tag=""):
+    s = error_stats(y, ref)
+    assert np.all(np.isfinite(np.asarray(y, dtype=np.float64))), tag
+    assert s["max_err_over_rms"] <= MAX_ERR_REL_RMS, (tag, s)
+    assert s["mean_rel_err"] <= MEAN_REL_ERR, (tag, s)
+    return s
+
+
+def weights_to_host(w: dict) -> dict:
+    return {k: v.detach().cpu() for k, v in w.items()}
+
+
+def oracle_rows(oracle, w_host: dict, x_rows, idx_rows, gate_rows, residual_rows=None,
+                c=100.0, eps=1e-6):
+    """Layer output of the given tokens with the given routing (fp64 oracle).  Only the
+    experts these tokens use are handed to the oracle (indices remapped accordingly)."""
+    idx_rows = np.asarray(idx_rows, dtype=np.int64)
+    used, remap = np.unique(idx_rows, return_inverse=True)
+    remap = remap.reshape(idx_rows.shape).astype(np.int32)
+    sel = torch.as_tensor(used)
+    lat = oracle.latent(x_rows, w_host["w_down"])
+    z = oracle.routed(lat, remap, gate_rows, w_host["w_gate"][sel].contiguous(),
+                      w_host["w_value"][sel].contiguous(), w_host["w_edown"][sel].contiguous(),
+                      w_host["gamma"].numpy(), c, eps)
+    ys = oracle.shared(x_rows, w_host["w_sgate"], w_host["w_svalue"], w_host["w_sdown"], c)
+    return oracle.output(z, ys, w_host["w_up"], residual_rows)
+
+
+def routing_agrees_up_to_ties(oracle, logits_ref, tau_ref, idx_gpu, K, delta):
+    """Per token: True where the GPU's expert set equals the oracle's.  Where they differ,
+    assert that every expert in the symmetric difference has an oracle key a = s - tau
+    within `delta` of the oracle's K-th largest key (a near-tie that the logits' rounding
+    decides).  Returns the boolean mask of tokens with identical sets."""
+    idx_ref, _, s_ref = oracle.route(logits_ref, tau_ref, K)
+    a = s_ref.astype(np.float64) - (tau_ref.astype(np.float64)[None, :] if tau_ref is not None else 0.0)
+    same = np.zeros(len(idx_gpu), dtype=bool)
+    for t in range(len(idx_gpu)):
+        g, r = set(idx_gpu[t].tolist()), set(idx_ref[t].tolist())
+        if g == r:
+            same[t] = True
+            continue
+        kth = np.sort(a[t])[::-1][K - 1]
+        for e in g ^ r:
+            assert abs(a[t, e] - kth) <= delta, (t, e, a[t, e], kth, delta)
+    return same, idx_ref
+
+
+def mid_shape(T=1000):
+    """Several tiles in every GEMM dimension, ragged tails, expert segments of ~125 rows."""
+    return synth.LayerShape("mid", T=T, d=1024, L=512, E=64, K=8, I=256, S=2, Is=512)
+
+
+def with_T(sh, T):
+    return replace(sh, T=T)

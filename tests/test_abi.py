@@ -1,0 +1,128 @@
+"""The C-ABI library builds, loads and exports every function include/lmoe.h declares; the
+host-side argument checks and size queries behave as documented.  No call here launches
+a kernel, so these run without a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from latent_compressed_expert_gb300 import build, lmoe, synth
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "lmoe.h")
+
+
+# Calls below pass fake device addresses that the host-side checks must reject before any
+# CUDA call; they are host-logic tests and stay off machines with a GPU, where a check that
+# let one through would touch a bogus address.
+no_gpu = pytest.mark.skipif(__import__("torch").cuda.is_available(),
+                            reason="fake-pointer host checks run on CPU-only machines")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return lmoe.load()
+
+
+def _declared():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(lmoe_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared()
+    assert {"lmoe_forward", "lmoe_route", "lmoe_thresholds"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+    # and the binding knows a signature for each of them
+    assert set(names) == set(lmoe.SIGNATURES)
+
+
+def test_version_and_error_strings(lib):
+    assert lib.lmoe_version().decode().startswith("lmoe")
+    for code in range(6):
+        assert lib.lmoe_error_string(code)
+    assert lib.lmoe_error_string(99) == b"unknown status"
+
+
+def test_size_queries(lib):
+    d = lmoe.dims_of(synth.PREFILL)
+    pb = lmoe.packed_bytes(d)
+    # every weight once (bf16) plus gamma (fp32), up to 1 KB alignment per piece
+    sh = synth.PREFILL
+    weights = (sh.L * sh.d + sh.E * sh.L + 3 * sh.E * sh.I * sh.L + sh.d * sh.L
+               + 3 * sh.S * sh.Is * sh.d) * 2 + sh.L * 4
+    assert weights <= pb <= weights + 6 * 1024
+    assert lmoe.workspace_bytes(d) > sh.T * sh.K * sh.L * 2 * 2  # lat_p and o dominate
+    # T = 0 is valid and small
+    assert 0 < lmoe.workspace_bytes(lmoe.dims_of(synth.PREFILL, T=0)) < 1 << 20
+
+
+@no_gpu
+@pytest.mark.parametrize("field,value,code", [
+    ("d", 100, lmoe.LMOE_ERR_UNSUPPORTED),    # not a multiple of 64
+    ("L", 96, lmoe.LMOE_ERR_UNSUPPORTED),
+    ("I", 32, lmoe.LMOE_ERR_UNSUPPORTED),
+    ("K", 33, lmoe.LMOE_ERR_UNSUPPORTED),     # K > 32
+    ("E", 8, lmoe.LMOE_ERR_UNSUPPORTED),      # K = 16 > E
+    ("E", 900, lmoe.LMOE_ERR_UNSUPPORTED),    # not a multiple of 16
+    ("T", -1, lmoe.LMOE_ERR_INVALID_ARG),
+    ("c", 0.0, lmoe.LMOE_ERR_INVALID_ARG),
+])
+def test_unsupported_dims_are_rejected(lib, field, value, code):
+    d = lmoe.dims_of(synth.PREFILL)
+    setattr(d, field, value)
+    assert lmoe.packed_bytes(d) == 0 and lmoe.workspace_bytes(d) == 0
+    rc = lib.lmoe_forward(ctypes.byref(d), None, None, None, None, None, 0, None, None)
+    assert rc == code
+
+
+@no_gpu
+def test_forward_argument_checks(lib):
+    d = lmoe.dims_of(synth.TINY)
+    # missing buffers
+    assert lib.lmoe_forward(ctypes.byref(d), None, None, None, None, None, 0, None, None) \
+        == lmoe.LMOE_ERR_INVALID_ARG
+    # T == 0 is a no-op that touches nothing
+    d0 = lmoe.dims_of(synth.TINY, T=0)
+    assert lib.lmoe_forward(ctypes.byref(d0), None, None, None, None, None, 0, None, None) \
+        == lmoe.LMOE_OK
+    # misaligned pointers are rejected before any launch
+    fake = ctypes.c_void_p(0x1000)
+    bad = ctypes.c_void_p(0x1001)
+    ws = lmoe.workspace_bytes(d)
+    assert lib.lmoe_forward(ctypes.byref(d), fake, bad, None, fake, fake, ws, None, None) \
+        == lmoe.LMOE_ERR_INVALID_ARG
+    # y aliasing x is rejected
+    assert lib.lmoe_forward(ctypes.byref(d), fake, fake, None, fake, ctypes.c_void_p(0x2000),
+                            ws, None, None) == lmoe.LMOE_ERR_INVALID_ARG
+    # a workspace one byte short is rejected
+    assert lib.lmoe_forward(ctypes.byref(d), fake, fake, None, ctypes.c_void_p(0x3000),
+                            ctypes.c_void_p(0x4000), ws - 1, None, None) \
+        == lmoe.LMOE_ERR_WORKSPACE_TOO_SMALL
+
+
+@no_gpu
+def test_route_and_threshold_argument_checks(lib):
+    fake = ctypes.c_void_p(0x1000)
+    assert lib.lmoe_route(fake, None, 4, 8, 9, fake, fake, None, None) == lmoe.LMOE_ERR_UNSUPPORTED
+    assert lib.lmoe_route(fake, None, 4, 64, 33, fake, fake, None, None) == lmoe.LMOE_ERR_UNSUPPORTED
+    assert lib.lmoe_route(fake, None, 4, 8192, 4, fake, fake, None, None) == lmoe.LMOE_ERR_UNSUPPORTED
+    assert lib.lmoe_route(fake, None, -1, 8, 4, fake, fake, None, None) == lmoe.LMOE_ERR_INVALID_ARG
+    assert lib.lmoe_route(None, None, 4, 8, 4, None, None, None, None) == lmoe.LMOE_ERR_INVALID_ARG
+    assert lib.lmoe_route(None, None, 0, 8, 4, None, None, None, None) == lmoe.LMOE_OK
+    assert lib.lmoe_thresholds(fake, 10, 8, 4, 11, fake, None) == lmoe.LMOE_ERR_INVALID_ARG
+    assert lib.lmoe_thresholds(None, 10, 8, 4, 0, None, None) == lmoe.LMOE_ERR_INVALID_ARG
+    assert lib.lmoe_thresholds(None, 0, 8, 4, 0, None, None) == lmoe.LMOE_OK
+    assert lib.lmoe_gemm_bf16(fake, fake, fake, 4, 24, 64, fake, None) == lmoe.LMOE_ERR_UNSUPPORTED
+    assert lib.lmoe_gemm_bf16(fake, fake, fake, 4, 32, 96, fake, None) == lmoe.LMOE_ERR_UNSUPPORTED
+    assert lib.lmoe_gemm_bf16(fake, fake, fake, 4, 32, 64, None, None) == lmoe.LMOE_ERR_INVALID_ARG
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    import torch
+    logits = torch.zeros(4, 16)
+    with pytest.raises(ValueError):
+        lmoe.route(logits, None, 4)

@@ -1,0 +1,88 @@
+"""GPU parity of the routing kernels (bit-exact against the oracle on the same fp32 logits)
+and of the tensor-core GEMM building block (against a float64 matmul)."""
+import numpy as np
+import pytest
+import torch
+
+from latent_compressed_expert_gb300 import lmoe, synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from latent_compressed_expert_gb300 import build
+    build.build()
+    lmoe.load()
+    return torch.device("cuda:0")
+
+
+# ----------------------------------------------------------------------------------------
+# tcgen05 GEMM
+# ----------------------------------------------------------------------------------------
+@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (200, 256, 128), (1, 16, 64), (300, 640, 448),
+                                   (513, 384, 1024), (64, 896, 3584), (1000, 1280, 512),
+                                   (4096, 512, 256)])
+def test_gemm_matches_float64(dev, M, N, K):
+    g = torch.Generator(device=dev).manual_seed(M * 7 + N * 3 + K)
+    A = torch.randn(M, K, generator=g, device=dev).to(torch.bfloat16)
+    B = torch.randn(N, K, generator=g, device=dev).to(torch.bfloat16)
+    C, flag = lmoe.gemm_bf16(A, B)
+    torch.cuda.synchronize()
+    assert int(flag[0]) == 0
+    ref = A.double() @ B.double().T
+    bound = K * 2.0 ** -23 * (A.double().abs() @ B.double().abs().T) + 1e-30
+    err = (C.double() - ref).abs()
+    assert bool((err <= bound).all()), float((err / bound).max())
+
+
+# ----------------------------------------------------------------------------------------
+# routing: bit-exact against the oracle on identical fp32 logits
+# ----------------------------------------------------------------------------------------
+def _logits(T, E, kind, seed):
+    if kind == "normal":
+        return synth.make_logits(T, E, seed)
+    if kind == "ties":
+        return synth.make_uniform_logits(T, E, seed, quantum=0.25)
+    if kind == "saturated":          # many scores round to exactly 1.0 (and to ~0)
+        return synth.make_logits(T, E, seed, scale=30.0)
+    if kind == "zipf":
+        return synth.make_logits(T, E, seed, zipf_s=1.1)
+    raise ValueError(kind)
+
+
+ROUTE_CASES = [(64, 16, 4, "normal"), (1000, 64, 4, "ties"), (8192, 896, 16, "normal"),
+               (257, 896, 16, "ties"), (1, 896, 16, "normal"), (33, 16, 16, "normal"),
+               (100, 4096, 32, "normal"), (500, 896, 16, "saturated"), (2048, 448, 8, "zipf"),
+               (3, 48, 1, "normal")]
+
+
+@pytest.mark.parametrize("T,E,K,kind", ROUTE_CASES)
+def test_route_bit_exact(dev, oracle_mod, T, E, K, kind):
+    lg = _logits(T, E, kind, seed=T + E + K)
+    lg_np = lg.numpy()
+    tau_np = oracle_mod.thresholds(lg_np, oracle_mod.fair_share_rank(T, K, E))
+    for tau in (tau_np, None):
+        idx, gate, sc = lmoe.route(lg.to(dev), None if tau is None else torch.from_numpy(tau).to(dev),
+                                   K, want_scores=True)
+        r_idx, r_gate, r_sc = oracle_mod.route(lg_np, tau, K)
+        assert np.array_equal(sc.cpu().numpy().view(np.int32), r_sc.view(np.int32))
+        assert np.array_equal(idx.cpu().numpy(), r_idx)
+        assert np.array_equal(gate.cpu().numpy().view(np.int32), r_gate.view(np.int32))
+
+
+THRESH_CASES = [(64, 16, 4, 0), (8192, 896, 16, 0), (32768, 896, 16, 0), (40000, 64, 4, 0),
+                (100, 32, 4, 1), (100, 32, 4, 100), (7, 16, 16, 0), (1, 896, 16, 0),
+                (3000, 448, 8, 0)]
+
+
+@pytest.mark.parametrize("T,E,K,k_rank", THRESH_CASES)
+def test_thresholds_bit_exact(dev, oracle_mod, T, E, K, k_rank):
+    for kind in ("normal", "ties", "saturated"):
+        lg = _logits(T, E, kind, seed=T * 3 + E)
+        tau = lmoe.thresholds(lg.to(dev), K, k_rank)
+        k = k_rank if k_rank > 0 else oracle_mod.fair_share_rank(T, K, E)
+        ref = oracle_mod.thresholds(lg.numpy(), k)
+        assert np.array_equal(tau.cpu().numpy().view(np.int32), ref.view(np.int32)), kind

@@ -1,0 +1,307 @@
+"""GPU parity of the whole layer (lmoe_forward) against the fp64 oracle.
+
+Two ways of routing are checked.  With caller-supplied router logits (lmoe_io.logits_in)
+both sides route on identical fp32 values, so thresholds, selections and gates must agree
+bit for bit and the outputs of every token are compared.  With the layer's own router the
+GPU's logits (bf16 latent, fp32 accumulation) differ from the oracle's fp64 logits by a
+bounded amount: they are compared against that bound, selections must agree except at
+near-ties inside it, and outputs are compared on the tokens whose selection agrees.
+"""
+import numpy as np
+import pytest
+import torch
+
+import gpu_helpers as H
+from latent_compressed_expert_gb300 import lmoe, synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from latent_compressed_expert_gb300 import build
+    build.build()
+    lmoe.load()
+    return torch.device("cuda:0")
+
+
+def _layer(sh, seed, dev, hot=0.0, router_gain=1.0, max_tokens=None):
+    w = synth.make_weights(sh, seed, device="cpu", hot_row_frac=hot, router_gain=router_gain)
+    wd = {k: v.to(dev) for k, v in w.items()}
+    return w, lmoe.Layer(sh, wd, max_tokens=max_tokens)
+
+
+def _logit_bound(lat64, w_router):
+    """|z_gpu - z_ref| <= 2^-8 * sum_l |lat_l W_el| + 1e-5: the latent is rounded to bf16
+    (relative 2^-9) before the router GEMM, which accumulates in fp32."""
+    return 2.0 ** -8 * (np.abs(lat64) @ np.abs(w_router.double().numpy()).T) + 1e-5
+
+
+# ----------------------------------------------------------------------------------------
+# tiny shape: whole layer, every token, caller-supplied logits -> bit-exact routing
+# ----------------------------------------------------------------------------------------
+@pytest.mark.parametrize("mode", ["batch", "none", "given"])
+@pytest.mark.parametrize("with_residual", [False, True])
+def test_tiny_layer_with_given_logits(dev, oracle_mod, mode, with_residual):
+    sh = synth.TINY
+    w, layer = _layer(sh, seed=0, dev=dev, hot=0.01)
+    x = synth.make_x(sh, seed=0)
+    logits = synth.make_logits(sh.T, sh.E, seed=0)
+    tau_given = oracle_mod.thresholds(synth.make_logits(8 * sh.T, sh.E, seed=5).numpy(),
+                                      oracle_mod.fair_share_rank(8 * sh.T, sh.K, sh.E))
+    tau_arg = {"batch": "batch", "none": None, "given": tau_given}[mode]
+    res = x if with_residual else None
+    ref = oracle_mod.forward(w, x, sh.K, residual=res, tau=tau_arg, logits_in=logits.numpy())
+    xd = x.to(dev)
+    y, dbg = layer.forward(xd, residual=xd if with_residual else None,
+                           tau=torch.from_numpy(tau_given).to(dev) if mode == "given" else None,
+                           balance=(mode != "none"), logits_in=logits.to(dev), debug=True)
+    torch.cuda.synchronize()
+    assert layer.device_error() == 0
+    assert np.array_equal(dbg["idx"].cpu().numpy(), ref.idx)
+    assert np.array_equal(dbg["gate"].cpu().numpy().view(np.int32), ref.gate.view(np.int32))
+    if ref.tau is not None:
+        assert np.array_equal(dbg["tau"].cpu().numpy().view(np.int32), ref.tau.view(np.int32))
+    counts = np.bincount(ref.idx.ravel(), minlength=sh.E)
+    assert np.array_equal(dbg["counts"].cpu().numpy(), counts)
+    H.assert_close(y.float().cpu().numpy(), ref.y, f"tiny/{mode}/{with_residual}")
+
+
+# ----------------------------------------------------------------------------------------
+# tiny and mid shapes with the layer's own router
+# ----------------------------------------------------------------------------------------
+@pytest.mark.parametrize("shape_name", ["tiny", "mid"])
+def test_layer_with_own_router(dev, oracle_mod, shape_name):
+    sh = synth.TINY if shape_name == "tiny" else H.mid_shape()
+    w, layer = _layer(sh, seed=1, dev=dev, hot=0.01)
+    x = synth.make_x(sh, seed=1)
+    xd = x.to(dev)
+    y, dbg = layer.forward(xd, residual=None, debug=True)
+    torch.cuda.synchronize()
+    assert layer.device_error() == 0
+    ref = oracle_mod.forward(w, x, sh.K, residual=None, tau="batch")
+    lg_gpu = dbg["logits"].cpu().numpy().astype(np.float64)
+    bound = _logit_bound(ref.lat, w["w_router"])
+    assert np.all(np.abs(lg_gpu - ref.logits.astype(np.float64)) <= bound)
+    # thresholds: each GPU tau is the k-th largest of the GPU's own scores of its column
+    _, _, s_gpu = lmoe.route(dbg["logits"], None, sh.K, want_scores=True)
+    s_gpu = s_gpu.cpu().numpy()
+    tau_gpu = dbg["tau"].cpu().numpy()
+    k = oracle_mod.fair_share_rank(sh.T, sh.K, sh.E)
+    assert np.all((s_gpu >= tau_gpu[None, :]).sum(0) >= k)
+    assert np.all((s_gpu > tau_gpu[None, :]).sum(0) < k)
+    # and within the score error of the oracle's thresholds
+    dz = float(np.abs(lg_gpu - ref.logits).max())
+    assert np.all(np.abs(tau_gpu.astype(np.float64) - ref.tau) <= 0.25 * dz + 1e-6)
+    # selections agree except at near-ties that the logit rounding decides
+    delta = 0.5 * dz + 1e-6
+    same, _ = H.routing_agrees_up_to_ties(oracle_mod, ref.logits, ref.tau,
+                                          dbg["idx"].cpu().numpy(), sh.K, delta)
+    assert same.mean() >= 0.9
+    H.assert_close(y.float().cpu().numpy()[same], ref.y[same], f"{shape_name}/own-router")
+
+
+# ----------------------------------------------------------------------------------------
+# ragged and degenerate shapes
+# ----------------------------------------------------------------------------------------
+EDGE_SHAPES = [
+    ("T1", synth.TINY.with_tokens(1)),
+    ("T7", synth.TINY.with_tokens(7)),
+    ("T129", synth.TINY.with_tokens(129)),
+    ("K_eq_E", synth.LayerShape("kE", T=40, d=256, L=128, E=16, K=16, I=64, S=2, Is=128)),
+    ("K1", synth.LayerShape("k1", T=300, d=256, L=128, E=32, K=1, I=64, S=2, Is=128)),
+    ("no_shared", synth.LayerShape("s0", T=100, d=256, L=128, E=16, K=4, I=64, S=0, Is=0)),
+    ("one_shared", synth.LayerShape("s1", T=77, d=384, L=192, E=48, K=6, I=128, S=1, Is=192)),
+    ("K32", synth.LayerShape("k32", T=50, d=256, L=128, E=64, K=32, I=64, S=2, Is=64)),
+]
+
+
+@pytest.mark.parametrize("name,sh", EDGE_SHAPES, ids=[n for n, _ in EDGE_SHAPES])
+def test_edge_shapes(dev, oracle_mod, name, sh):
+    w, layer = _layer(sh, seed=2, dev=dev, hot=0.01)
+    x = synth.make_x(sh, seed=2)
+    logits = synth.make_logits(sh.T, sh.E, seed=2)
+    ref = oracle_mod.forward(w, x, sh.K, residual=x, tau="batch", logits_in=logits.numpy())
+    xd = x.to(dev)
+    y, dbg = layer.forward(xd, residual=xd, logits_in=logits.to(dev), debug=True)
+    torch.cuda.synchronize()
+    assert layer.device_error() == 0
+    assert np.array_equal(dbg["idx"].cpu().numpy(), ref.idx)
+    H.assert_close(y.float().cpu().numpy(), ref.y, name)
+
+
+def test_empty_batch_is_a_no_op(dev):
+    sh = synth.TINY
+    _, layer = _layer(sh, seed=3, dev=dev)
+    x = torch.empty((0, sh.d), dtype=torch.bfloat16, device=dev)
+    y = layer.forward(x)
+    torch.cuda.synchronize()
+    assert y.shape == (0, sh.d)
+
+
+def test_forward_is_deterministic(dev):
+    sh = H.mid_shape()
+    _, layer = _layer(sh, seed=4, dev=dev)
+    x = synth.make_x(sh, seed=4).to(dev)
+    y1 = layer.forward(x, residual=x).clone()
+    y2 = layer.forward(x, residual=x).clone()
+    torch.cuda.synchronize()
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+
+
+# ----------------------------------------------------------------------------------------
+# full K3 widths (sampled tokens against the oracle)
+# ----------------------------------------------------------------------------------------
+def _sample_rows(T, n, seed):
+    rng = np.random.default_rng(seed)
+    rows = set(range(min(4, T))) | set(range(max(0, T - 4), T))
+    rows |= set(rng.choice(T, size=min(T, n), replace=False).tolist())
+    return np.array(sorted(rows))
+
+
+@pytest.fixture(scope="module")
+def prefill(dev):
+    """The benchmark's workload: K3 prefill, T=8192, x with 0.1 % of elements x1000,
+    in-batch Quantile-Balancing thresholds, the layer's own router."""
+    sh = synth.PREFILL
+    gain = synth.outlier_router_gain(sh, 0.001, 1000.0)
+    w = synth.make_weights(sh, seed=2, device=dev, router_gain=gain)
+    layer = lmoe.Layer(sh, w)
+    x = synth.make_x(sh, seed=2, device=dev, outlier_frac=0.001)
+    return sh, w, layer, x
+
+
+def test_prefill_given_logits_bit_exact_routing(dev, oracle_mod, prefill):
+    sh, w, layer, x = prefill
+    logits = synth.make_logits(sh.T, sh.E, seed=12)
+    y, dbg = layer.forward(x, residual=None, logits_in=logits.to(dev), debug=True)
+    torch.cuda.synchronize()
+    assert layer.device_error() == 0
+    lg = logits.numpy()
+    tau = oracle_mod.thresholds(lg, oracle_mod.fair_share_rank(sh.T, sh.K, sh.E))
+    idx, gate, _ = oracle_mod.route(lg, tau, sh.K)
+    assert np.array_equal(dbg["tau"].cpu().numpy().view(np.int32), tau.view(np.int32))
+    assert np.array_equal(dbg["idx"].cpu().numpy(), idx)
+    assert np.array_equal(dbg["gate"].cpu().numpy().view(np.int32), gate.view(np.int32))
+    rows = _sample_rows(sh.T, 12, seed=0)
+    wh = H.weights_to_host(w)
+    xr = x[rows].cpu()
+    ref = H.oracle_rows(oracle_mod, wh, xr, idx[rows], gate[rows], None)
+    H.assert_close(y[rows].float().cpu().numpy(), ref, "prefill/given-logits")
+
+
+def test_prefill_own_router(dev, oracle_mod, prefill):
+    """Exactly the benchmark's call; the oracle computes all 8192 tokens' latents and logits
+    (for the in-batch thresholds) and the full output of sampled tokens."""
+    sh, w, layer, x = prefill
+    y, dbg = layer.forward(x, residual=None, debug=True)
+    torch.cuda.synchronize()
+    assert layer.device_error() == 0
+    wh = H.weights_to_host(w)
+    xh = x.cpu()
+    lat = oracle_mod.latent(xh, wh["w_down"])
+    lg_ref = oracle_mod.router_logits(lat, wh["w_router"])
+    lg_gpu = dbg["logits"].cpu().numpy().astype(np.float64)
+    bound = _logit_bound(lat, wh["w_router"])
+    assert np.all(np.abs(lg_gpu - lg_ref) <= bound)
+    lg32 = lg_ref.astype(np.float32)
+    tau_ref = oracle_mod.thresholds(lg32, oracle_mod.fair_share_rank(sh.T, sh.K, sh.E))
+    dz = float(np.abs(lg_gpu - lg_ref).max())
+    tau_gpu = dbg["tau"].cpu().numpy()
+    assert np.all(np.abs(tau_gpu.astype(np.float64) - tau_ref) <= 0.25 * dz + 1e-6)
+    idx_gpu = dbg["idx"].cpu().numpy()
+    same, idx_ref = H.routing_agrees_up_to_ties(oracle_mod, lg32, tau_ref, idx_gpu, sh.K,
+                                                0.5 * dz + 1e-6)
+    assert same.mean() >= 0.9
+    # load balance: every expert near its fair share T*K/E
+    counts = dbg["counts"].cpu().numpy()
+    assert counts.sum() == sh.T * sh.K
+    rows = [r for r in _sample_rows(sh.T, 16, seed=1) if same[r]]
+    _, gate_ref, _ = oracle_mod.route(lg32[rows], tau_ref, sh.K)
+    ref = H.oracle_rows(oracle_mod, wh, xh[rows], idx_ref[rows], gate_ref, None)
+    H.assert_close(y[rows].float().cpu().numpy(), ref, "prefill/own-router")
+
+
+def test_e64_layer(dev, oracle_mod):
+    """Reduced expert pool at full width (E=64, K=4, T=4096), the layer's own router."""
+    sh = synth.E64
+    w = synth.make_weights(sh, seed=1, device=dev)
+    layer = lmoe.Layer(sh, w)
+    x = synth.make_x(sh, seed=1, device=dev)
+    y, dbg = layer.forward(x, residual=x, debug=True)
+    torch.cuda.synchronize()
+    assert layer.device_error() == 0
+    wh = H.weights_to_host(w)
+    xh = x.cpu()
+    lat = oracle_mod.latent(xh, wh["w_down"])
+    lg_ref = oracle_mod.router_logits(lat, wh["w_router"])
+    lg_gpu = dbg["logits"].cpu().numpy().astype(np.float64)
+    assert np.all(np.abs(lg_gpu - lg_ref) <= _logit_bound(lat, wh["w_router"]))
+    lg32 = lg_ref.astype(np.float32)
+    tau_ref = oracle_mod.thresholds(lg32, oracle_mod.fair_share_rank(sh.T, sh.K, sh.E))
+    dz = float(np.abs(lg_gpu - lg_ref).max())
+    same, idx_ref = H.routing_agrees_up_to_ties(oracle_mod, lg32, tau_ref,
+                                                dbg["idx"].cpu().numpy(), sh.K, 0.5 * dz + 1e-6)
+    assert same.mean() >= 0.9
+    rows = [r for r in _sample_rows(sh.T, 16, seed=2) if same[r]]
+    _, gate_ref, _ = oracle_mod.route(lg32[rows], tau_ref, sh.K)
+    ref = H.oracle_rows(oracle_mod, wh, xh[rows], idx_ref[rows], gate_ref, xh[rows])
+    H.assert_close(y[rows].float().cpu().numpy(), ref, "e64")
+
+
+def test_decode_layer(dev, oracle_mod):
+    """K3 decode: T=64 against thresholds of a prefill batch (passed in); every token."""
+    sh = synth.DECODE
+    w = synth.make_weights(sh, seed=3, device=dev)
+    layer = lmoe.Layer(sh, w)
+    x = synth.make_x(sh, seed=3, device=dev)
+    prefill_logits = synth.make_logits(8192, sh.E, seed=3).numpy()
+    tau = oracle_mod.thresholds(prefill_logits, oracle_mod.fair_share_rank(8192, sh.K, sh.E))
+    y, dbg = layer.forward(x, residual=None, tau=torch.from_numpy(tau).to(dev), debug=True)
+    torch.cuda.synchronize()
+    assert layer.device_error() == 0
+    wh = H.weights_to_host(w)
+    xh = x.cpu()
+    lat = oracle_mod.latent(xh, wh["w_down"])
+    lg_ref = oracle_mod.router_logits(lat, wh["w_router"])
+    lg_gpu = dbg["logits"].cpu().numpy().astype(np.float64)
+    assert np.all(np.abs(lg_gpu - lg_ref) <= _logit_bound(lat, wh["w_router"]))
+    assert np.array_equal(dbg["tau"].cpu().numpy().view(np.int32), tau.view(np.int32))
+    lg32 = lg_ref.astype(np.float32)
+    dz = float(np.abs(lg_gpu - lg_ref).max())
+    same, idx_ref = H.routing_agrees_up_to_ties(oracle_mod, lg32, tau, dbg["idx"].cpu().numpy(),
+                                                sh.K, 0.25 * dz + 1e-6)
+    assert same.mean() >= 0.9
+    rows = np.nonzero(same)[0]
+    _, gate_ref, _ = oracle_mod.route(lg32[rows], tau, sh.K)
+    ref = H.oracle_rows(oracle_mod, wh, xh[rows], idx_ref[rows], gate_ref, None)
+    H.assert_close(y[rows].float().cpu().numpy(), ref, "decode")
+
+
+def test_skew_router_given_logits(dev, oracle_mod):
+    """T=32768 with Zipf(1.1)-biased router logits: in-batch thresholds restore balance;
+    routing bit-exact, sampled outputs against the oracle."""
+    sh = synth.SKEW
+    w = synth.make_weights(sh, seed=4, device=dev)
+    layer = lmoe.Layer(sh, w)
+    x = synth.make_x(sh, seed=4, device=dev)
+    logits = synth.make_logits(sh.T, sh.E, seed=4, zipf_s=1.1)
+    y, dbg = layer.forward(x, residual=None, logits_in=logits.to(dev), debug=True)
+    torch.cuda.synchronize()
+    assert layer.device_error() == 0
+    lg = logits.numpy()
+    tau = oracle_mod.thresholds(lg, oracle_mod.fair_share_rank(sh.T, sh.K, sh.E))
+    idx, gate, _ = oracle_mod.route(lg, tau, sh.K)
+    assert np.array_equal(dbg["idx"].cpu().numpy(), idx)
+    assert np.array_equal(dbg["gate"].cpu().numpy().view(np.int32), gate.view(np.int32))
+    plain, _, _ = oracle_mod.route(lg, None, sh.K)
+    fair = sh.T * sh.K / sh.E
+    before = np.bincount(plain.ravel(), minlength=sh.E) / fair
+    after = dbg["counts"].cpu().numpy() / fair
+    assert before.max() > 5.0 and after.max() < 1.6
+    rows = _sample_rows(sh.T, 8, seed=3)
+    wh = H.weights_to_host(w)
+    ref = H.oracle_rows(oracle_mod, wh, x[rows].cpu(), idx[rows], gate[rows], None)
+    H.assert_close(y[rows].float().cpu().numpy(), ref, "skew")
