@@ -1,0 +1,418 @@
+"""Benchmark of the Stable Latent MoE layer on GB300.
+
+Workload (one "step" = one lmoe_forward over one batch): the K3 prefill layer, T=8192
+tokens, d=7168, latent 3584, E=896 routed experts, top-16, 2 shared experts (I_s=2048),
+routed I=512, bf16 with fp32 accumulation; x ~ N(0,1) with 0.1 % of its elements x1000;
+weights ~ N(0, 1/fan_in) (router weights scaled to keep the logits ~N(0,1) under those
+outliers); in-batch Quantile-Balancing thresholds; residual = x.  Synthetic data, seed 2.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  Under torchrun each rank runs its own batch on its own GPU
+(weak scaling, no collective on the data path); the time is the max over ranks.
+``--impl reference`` times the CPU oracle (the only reference there is) on host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import glob
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from latent_compressed_expert_gb300 import lmoe, synth  # noqa: E402
+
+METRIC = "latent-MoE layer tokens/s at 896E/top-16; TFLOP/s & % bf16 / HBM roofline"
+UNIT = "tokens/s"
+SEED = 2
+OUTLIER_FRAC, OUTLIER_SCALE = 0.001, 1000.0
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ----------------------------------------------------------------------------------------
+# algorithmic work of each stage (what the method must read/write/compute at minimum)
+# ----------------------------------------------------------------------------------------
+def stage_work(sh, touched: int, residual: bool = True) -> dict:
+    T, d, L, E, K, I, S, Is = sh.T, sh.d, sh.L, sh.E, sh.K, sh.I, sh.S, sh.Is
+    sw = S * Is
+    bf, f4 = 2, 4
+    w = {
+        "latent_shared": (2.0 * T * d * (L + 2 * sw),
+                          (T * d + (L + 2 * sw) * d + T * L + T * sw) * bf),
+        "router": (2.0 * T * L * E, (T * L + E * L) * bf + T * E * f4),
+        "thresholds": (0.0, T * E * f4 + E * f4),
+        "route": (0.0, T * E * f4 + E * f4 + T * K * 8),
+        "dispatch": (0.0, T * K * 4 + T * L * bf + T * K * L * bf + T * K * 4),
+        "expert_gate_up": (2.0 * T * K * L * 2 * I,
+                           touched * 2 * I * L * bf + T * K * L * bf + T * K * I * bf),
+        "expert_down": (2.0 * T * K * I * L, touched * L * I * bf + T * K * (I + L) * bf),
+        "combine": (0.0, T * K * L * bf + T * K * 8 + T * L * bf + L * f4),
+        "output": (2.0 * T * (L + sw) * d,
+                   (T * (L + sw) + d * (L + sw) + T * d * (2 if residual else 1)) * bf),
+    }
+    return {k: {"flop": v[0], "bytes": float(v[1])} for k, v in w.items()}
+
+
+def layer_work(sh, touched: int) -> tuple[float, float]:
+    """FLOP of the layer (461.5 MFLOP per token at the K3 shape) and its algorithmic bytes:
+    every touched weight once, x and the residual read, y written."""
+    T, d, L, E, K, I, S, Is = sh.T, sh.d, sh.L, sh.E, sh.K, sh.I, sh.S, sh.Is
+    flop_tok = 2.0 * (d * L + L * E + K * (L * 2 * I + I * L) + 3 * S * Is * d + L * d)
+    wbytes = (L * d + E * L + touched * 3 * I * L + L * d + 3 * S * Is * d) * 2 + L * 4
+    return flop_tok * T, float(wbytes + 3 * T * d * 2)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            m = json.load(f)
+        return {"hbm_gbs": float(m["hbm_gbs"]), "bf16_tflops": float(m["bf16_tflops"]),
+                "bf16_tflops_sustained": float(m.get("bf16_tflops_sustained", m["bf16_tflops"]))}, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(ROOT, "latent_compressed_expert_gb300", "csrc", "*"))):
+        with open(p, "rb") as f:
+            h.update(os.path.basename(p).encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(stage: str):
+    """DRAM bytes per launch of a stage's kernel from a committed ncu summary, if it was
+    captured from the current kernel sources; else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        t = json.load(f)
+    if t.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    s = t.get("stages", {}).get(stage)
+    return None if s is None else float(s["dram_bytes_per_launch"])
+
+
+# ----------------------------------------------------------------------------------------
+# clocks during the timed region
+# ----------------------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        sm, mx, reasons = [], [], set()
+        for l in getattr(self, "lines", []):
+            parts = [p.strip() for p in l.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------------------
+# the CPU oracle on a bounded sample (reported baseline, and the reference arm)
+# ----------------------------------------------------------------------------------------
+def oracle_step(oracle, wh, x_rows, K):
+    """The whole layer on a sub-batch of tokens, thresholds solved over that sub-batch."""
+    return oracle.forward(wh, x_rows, K, residual=x_rows, tau="batch")
+
+
+def host_weights(w):
+    return {k: v.detach().cpu() for k, v in w.items()}
+
+
+def time_oracle(sh, wh, x_host, n_tokens, reps=1):
+    import oracle
+    oracle.build()
+    t0 = time.perf_counter()
+    done = 0
+    for r in range(reps):
+        s = (r * n_tokens) % max(1, sh.T - n_tokens)
+        oracle_step(oracle, wh, x_host[s:s + n_tokens].contiguous(), sh.K)
+        done += n_tokens
+    dt = time.perf_counter() - t0
+    return done / dt, dt, oracle.num_threads()
+
+
+# ----------------------------------------------------------------------------------------
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v: float, world: int) -> float:
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64,
+                     device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def make_inputs(sh, dev, rank):
+    gain = synth.outlier_router_gain(sh, OUTLIER_FRAC, OUTLIER_SCALE)
+    w = synth.make_weights(sh, SEED, device=dev, router_gain=gain)
+    x = synth.make_x(sh, SEED + 1000 * rank, device=dev, outlier_frac=OUTLIER_FRAC,
+                     outlier_scale=OUTLIER_SCALE)
+    return w, x
+
+
+def workload_config(sh, world):
+    return {"workload": f"K3 Stable Latent MoE layer, prefill: T={sh.T} tokens, d={sh.d}, "
+                        f"latent {sh.L}, E={sh.E} routed top-{sh.K}, {sh.S} shared experts "
+                        f"(I_s={sh.Is}), routed I={sh.I}; in-batch Quantile-Balancing "
+                        f"thresholds; x~N(0,1) with 0.1% of elements x1000; residual = x",
+            "tokens_per_gpu": sh.T, "global_tokens": sh.T * world,
+            "l2": "inputs larger than L2: 10.2 GB of weights streamed per step",
+            "parallelism": f"replicas x{world}, independent batches"}
+
+
+def run_reference(args):
+    world, rank, _ = dist_setup(args.gpus)
+    if rank != 0:
+        return 0
+    sh = synth.PREFILL
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    w, x = make_inputs(sh, dev, 0)
+    wh = host_weights(w)
+    xh = x.cpu()
+    del w, x
+    import oracle
+    oracle.build()
+    # size each step so that warmup + steps take about 2-3 minutes on this host
+    rate, _, _ = time_oracle(sh, wh, xh, 2)
+    n = int(max(1, min(64, rate * 150.0 / max(1, args.steps + args.warmup))))
+    for i in range(args.warmup):
+        oracle_step(oracle, wh, xh[i * n:(i + 1) * n].contiguous(), sh.K)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        s = (i * n) % (sh.T - n)
+        oracle_step(oracle, wh, xh[s:s + n].contiguous(), sh.K)
+    dt = time.perf_counter() - t0
+    value = n * args.steps / dt
+    cores = oracle.num_threads()
+    sample = (f"{n} tokens of the {sh.T}-token batch per step through the whole layer, "
+              f"thresholds solved over those tokens (cost is linear in tokens)")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * dt / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(sh, 1),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    world, rank, local = dist_setup(args.gpus)
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA GPU (the layer has no CPU path)")
+    dev = torch.device("cuda", local)
+    sh = synth.PREFILL
+    w, x = make_inputs(sh, dev, rank)
+    layer = lmoe.Layer(sh, w)
+    y = torch.empty_like(x)
+    stream = torch.cuda.current_stream()
+
+    # warm-up (also learns how many experts a step touches)
+    for _ in range(args.warmup):
+        _, dbg = layer.forward(x, residual=x, y=y, debug=True)
+    torch.cuda.synchronize()
+    if layer.device_error() != 0:
+        raise RuntimeError("device-side error during warm-up")
+    counts = dbg["counts"].cpu().numpy()
+    touched = int((counts > 0).sum())
+    launches_per_step = layer.last_kernel_launches
+
+    # ---- timed region: device-resident inputs
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(lmoe.NUM_STAGES + 1)]
+           for _ in range(args.steps)]
+    for e in evs:  # create the events outside the timed region
+        for ev in e:
+            ev.record(stream)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    barrier(world)
+    with ClockSampler(local) as clk:
+        torch.cuda.synchronize()
+        start.record(stream)
+        for i in range(args.steps):
+            layer.forward(x, residual=x, y=y, stage_events=evs[i])
+        end.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    ms = start.elapsed_time(end)
+    if layer.device_error() != 0:
+        raise RuntimeError("device-side error in the timed region")
+    ms_max = max_over_ranks(ms, world)
+    stage_ms = {name: float(np.mean([evs[i][s].elapsed_time(evs[i][s + 1])
+                                     for i in range(args.steps)]))
+                for s, name in enumerate(lmoe.STAGES)}
+
+    # ---- end to end through the public API with host buffers
+    x_host = x.cpu().pin_memory()
+    y_host = torch.empty_like(x_host).pin_memory()
+    x_dev = torch.empty_like(x)
+    for _ in range(max(1, args.warmup)):
+        layer.forward_host(x_host, y_host, x_dev, y)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    barrier(world)
+    e0.record(stream)
+    for _ in range(args.steps):
+        layer.forward_host(x_host, y_host, x_dev, y)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
+
+    T = sh.T
+    value = world * T * args.steps / (ms_max / 1e3)
+    e2e_value = world * T * args.steps / (e2e_ms / 1e3)
+    peaks, peak_src = load_peaks()
+    flop, nbytes = layer_work(sh, touched)
+    step_s = ms_max / 1e3 / args.steps
+    work = stage_work(sh, touched)
+    dom = max(stage_ms, key=stage_ms.get)
+    dw = work[dom]
+    t_s = stage_ms[dom] / 1e3
+    t_flop = dw["flop"] / (peaks["bf16_tflops_sustained"] * 1e12)
+    t_byte = dw["bytes"] / (peaks["hbm_gbs"] * 1e9)
+    if t_flop >= t_byte:
+        roof = {"bound": "tensor", "achieved": dw["flop"] / t_s / 1e12,
+                "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s"}
+    else:
+        roof = {"bound": "hbm", "achieved": dw["bytes"] / t_s / 1e9, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = ncu_traffic(dom)
+    roof["kernel"] = dom
+    roof["peak_source"] = f"{peak_src} ({'bf16 sustained' if roof['bound'] == 'tensor' else 'HBM copy'})"
+    roof["algorithmic"] = {"flop": dw["flop"], "bytes": dw["bytes"]}
+
+    stages = {}
+    for name in lmoe.STAGES:
+        sw_ = work[name]
+        t = stage_ms[name] / 1e3
+        stages[name] = {"ms": round(stage_ms[name], 4),
+                        "tflops": round(sw_["flop"] / t / 1e12, 1) if t > 0 and sw_["flop"] else None,
+                        "gbs": round(sw_["bytes"] / t / 1e9, 1) if t > 0 else None}
+
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded; random-init weights of the K3 layer shape)",
+            "config": workload_config(sh, world),
+            "tflops": flop / step_s / 1e12,
+            "frac_bf16_peak": flop / step_s / 1e12 / peaks["bf16_tflops_sustained"],
+            "layer_roofline_ms": 1e3 * max(flop / (peaks["bf16_tflops_sustained"] * 1e12),
+                                           nbytes / (peaks["hbm_gbs"] * 1e9)),
+            "experts_touched": touched,
+            "roofline": roof, "stages": stages,
+            "clocks": clk.summary(),
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": x.numel() * 2,
+                    "d2h_bytes_per_step": y.numel() * 2},
+            "gpu_launches": launches_per_step * args.steps}
+
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        wh = host_weights(w)
+        xh = x.cpu()
+        rate, dt, cores = time_oracle(sh, wh, xh, args.cpu_tokens)
+        line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
+                                "sample": f"{args.cpu_tokens} of the {T} tokens through the whole "
+                                          f"layer (fp64), thresholds over that sub-batch; "
+                                          f"{dt:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-tokens", type=int, default=128,
+                    help="tokens in the timed CPU-oracle sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
+    return run_reference(args) if args.impl == "reference" else run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -85,7 +85,21 @@ typedef struct lmoe_weights {
   const void *w_sdown;   /* [S, d, Is]  shared experts, down projection */
 } lmoe_weights;
 
-/* Optional routing inputs and debug outputs of lmoe_forward.  Any member may be NULL. */
+/* Stages of lmoe_forward, in launch order (for lmoe_io.stage_events). */
+enum lmoe_stage {
+  LMOE_STAGE_LATENT_SHARED = 0, /* x . [W_down ; W_shared_gate/value]^T, SiTU on the shared part */
+  LMOE_STAGE_ROUTER = 1,        /* router logits (skipped when logits_in is given) */
+  LMOE_STAGE_THRESHOLDS = 2,    /* in-batch Quantile-Balancing thresholds (when solved) */
+  LMOE_STAGE_ROUTE = 3,         /* top-K selection and gates */
+  LMOE_STAGE_DISPATCH = 4,      /* expert segments and the permuted latent */
+  LMOE_STAGE_EXPERT_GATE_UP = 5,/* grouped gate/value GEMM with SiTU-GLU */
+  LMOE_STAGE_EXPERT_DOWN = 6,   /* grouped down-projection GEMM */
+  LMOE_STAGE_COMBINE = 7,       /* gate-weighted aggregation + RMSNorm */
+  LMOE_STAGE_OUTPUT = 8,        /* up-projection + shared down-projection + residual */
+  LMOE_NUM_STAGES = 9
+};
+
+/* Optional routing inputs and debug outputs of lmoe_forward.  Any pointer may be NULL. */
 typedef struct lmoe_io {
   const float *tau_in;   /* [E] thresholds to route against (e.g. from a prefill batch) */
   int balance;           /* used when tau_in == NULL: 1 = solve thresholds from this batch
@@ -97,6 +111,10 @@ typedef struct lmoe_io {
   int32_t *idx_out;      /* [T, K] selected experts, slot order */
   float *gate_out;       /* [T, K] gates */
   int32_t *counts_out;   /* [E] tokens routed to each expert */
+  void **stage_events;   /* host array of LMOE_NUM_STAGES + 1 cudaEvent_t handles, or NULL:
+                            event i is recorded on the stream before stage i, the last one
+                            after the final stage (skipped stages record back to back) */
+  int kernel_launches;   /* out: number of kernels this call launched */
 } lmoe_io;
 
 /* Bytes of the packed weight buffer for `dims` (0 if the dims are invalid). */
@@ -145,7 +163,8 @@ int lmoe_route(const float *logits, const float *tau, int T, int E, int K, int32
  *   y        [T, d] bf16 output (may not alias x or residual)
  *   workspace, ws_bytes >= lmoe_workspace_bytes(dims), 256-byte aligned; its contents are
  *            scratch between calls (its first word carries the device error flag)
- *   io       routing options and debug outputs, or NULL (= in-batch thresholds)
+ *   io       routing options and debug outputs, or NULL (= in-batch thresholds); only
+ *            io->kernel_launches is written
  * Supported shapes: d, L, I, Is multiples of 64; 1 <= K <= min(E, 32); E <= 4096 and a
  * multiple of 16;
  * L <= 16384; T * K < 2^31.  T == 0 is a no-op.
@@ -155,7 +174,7 @@ int lmoe_route(const float *logits, const float *tau, int T, int E, int K, int32
  * Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE_TOO_SMALL, CUDA. */
 int lmoe_forward(const lmoe_dims *dims, const void *packed, const void *x,
                  const void *residual, void *y, void *workspace, size_t ws_bytes,
-                 const lmoe_io *io, void *stream);
+                 lmoe_io *io, void *stream);
 
 /* Building block of lmoe_forward, exposed for verification: C = A . B^T on the tensor
  * cores (tcgen05, fp32 accumulation in TMEM), with A [M, Kd] and B [N, Kd] bf16 row-major

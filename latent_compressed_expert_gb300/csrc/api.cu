@@ -214,7 +214,8 @@ int lmoe_last_device_error(void* workspace) {
 }
 
 int lmoe_forward(const lmoe_dims* dims, const void* packed, const void* x, const void* residual,
-                 void* y, void* workspace, size_t ws_bytes, const lmoe_io* io, void* stream_) {
+                 void* y, void* workspace, size_t ws_bytes, lmoe_io* io, void* stream_) {
+  if (io) io->kernel_launches = 0;
   int rc = dims_supported(dims);
   if (rc != LMOE_OK) return rc;
   const lmoe_dims D = *dims;
@@ -234,6 +235,14 @@ int lmoe_forward(const lmoe_dims* dims, const void* packed, const void* x, const
 
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   using bf = __nv_bfloat16;
+  int launches = 0;
+  // stage boundary: optional timing event; counts the kernels of the stage just finished
+  auto mark = [&](int stage_done_next, int kernels) -> bool {
+    launches += kernels;
+    if (!opt.stage_events) return true;
+    cudaEvent_t ev = static_cast<cudaEvent_t>(opt.stage_events[stage_done_next]);
+    return ev == nullptr || cudaEventRecord(ev, stream) == cudaSuccess;
+  };
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   const uint8_t* pk = static_cast<const uint8_t*>(packed);
   const PackedLayout P = packed_layout(D);
@@ -245,6 +254,7 @@ int lmoe_forward(const lmoe_dims* dims, const void* packed, const void* x, const
   const int T = D.T, TK = D.T * D.K;
 
   if (cudaMemsetAsync(err, 0, sizeof(uint32_t), stream) != cudaSuccess) return LMOE_ERR_CUDA;
+  if (!mark(LMOE_STAGE_LATENT_SHARED, 0)) return LMOE_ERR_CUDA;
 
   // 1. x . [W_down ; W_shared_gate/value]^T: latent (bf16) and SiTU(shared) into zh[:, L:]
   {
@@ -262,6 +272,7 @@ int lmoe_forward(const lmoe_dims* dims, const void* packed, const void* x, const
     rc = launch_gemm(x, T, D.d, pk + P.w1, static_cast<uint64_t>(g.N), D.d, g, stream);
     if (rc != LMOE_OK) return rc;
   }
+  if (!mark(LMOE_STAGE_ROUTER, 1)) return LMOE_ERR_CUDA;
   // 2. router logits = lat . W_r^T (fp32), unless the caller supplies them
   const float* logits = opt.logits_in;
   if (!logits) {
@@ -275,7 +286,9 @@ int lmoe_forward(const lmoe_dims* dims, const void* packed, const void* x, const
     rc = launch_gemm(lat, T, D.L, pk + P.wr, static_cast<uint64_t>(D.E), D.L, g, stream);
     if (rc != LMOE_OK) return rc;
     logits = g.outf;
+    launches += 1;
   }
+  if (!mark(LMOE_STAGE_THRESHOLDS, 0)) return LMOE_ERR_CUDA;
   // 3. thresholds
   const float* tau = opt.tau_in;
   if (!tau && opt.balance) {
@@ -285,12 +298,15 @@ int lmoe_forward(const lmoe_dims* dims, const void* packed, const void* x, const
     rc = launch_thresholds(logits, T, D.E, k, t, stream);
     if (rc != LMOE_OK) return rc;
     tau = t;
+    launches += 1;
   }
+  if (!mark(LMOE_STAGE_ROUTE, 0)) return LMOE_ERR_CUDA;
   // 4. top-K routing
   int32_t* idx = reinterpret_cast<int32_t*>(ws + W.idx);
   float* gate = reinterpret_cast<float*>(ws + W.gate);
   rc = launch_route(logits, tau, T, D.E, D.K, idx, gate, nullptr, stream);
   if (rc != LMOE_OK) return rc;
+  if (!mark(LMOE_STAGE_DISPATCH, 1)) return LMOE_ERR_CUDA;
   // 5. dispatch into expert-contiguous segments
   int32_t* offsets = reinterpret_cast<int32_t*>(ws + W.offsets);
   int32_t* mt_off = reinterpret_cast<int32_t*>(ws + W.mt_off);
@@ -300,6 +316,7 @@ int lmoe_forward(const lmoe_dims* dims, const void* packed, const void* x, const
                        reinterpret_cast<uint32_t*>(ws + W.base), offsets, mt_off, inv, lat_p,
                        opt.counts_out, err, stream);
   if (rc != LMOE_OK) return rc;
+  if (!mark(LMOE_STAGE_EXPERT_GATE_UP, 3)) return LMOE_ERR_CUDA;
   // 6. grouped gate/value GEMM with SiTU-GLU: h = SiTU(lat_p . W_gu[e]^T)
   bf* h = reinterpret_cast<bf*>(ws + W.h);
   {
@@ -317,6 +334,7 @@ int lmoe_forward(const lmoe_dims* dims, const void* packed, const void* x, const
                      static_cast<uint64_t>(D.E) * 2 * D.I, D.L, g, stream);
     if (rc != LMOE_OK) return rc;
   }
+  if (!mark(LMOE_STAGE_EXPERT_DOWN, 1)) return LMOE_ERR_CUDA;
   // 7. grouped down GEMM: o = h . W_ed[e]^T
   bf* o = reinterpret_cast<bf*>(ws + W.o);
   {
@@ -334,10 +352,12 @@ int lmoe_forward(const lmoe_dims* dims, const void* packed, const void* x, const
                      static_cast<uint64_t>(D.E) * D.L, D.I, g, stream);
     if (rc != LMOE_OK) return rc;
   }
+  if (!mark(LMOE_STAGE_COMBINE, 1)) return LMOE_ERR_CUDA;
   // 8. gate-weighted combine + RMSNorm -> zh[:, :L]
   rc = launch_combine(o, gate, inv, reinterpret_cast<const float*>(pk + P.gamma), T, D.K, D.L,
                       D.eps, zh, ldz, stream);
   if (rc != LMOE_OK) return rc;
+  if (!mark(LMOE_STAGE_OUTPUT, 1)) return LMOE_ERR_CUDA;
   // 9. y = residual + [z | hs] . [W_up | W_sd]^T
   {
     GemmArgs g = gemm_defaults(err, D.c);
@@ -352,6 +372,8 @@ int lmoe_forward(const lmoe_dims* dims, const void* packed, const void* x, const
     rc = launch_gemm(zh, T, ldz, pk + P.w2, static_cast<uint64_t>(D.d), ldz, g, stream);
     if (rc != LMOE_OK) return rc;
   }
+  if (!mark(LMOE_NUM_STAGES, 1)) return LMOE_ERR_CUDA;
+  if (io) io->kernel_launches = launches;
   // debug outputs
   auto copy = [&](void* dst, const void* src, size_t bytes) {
     return cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, stream) == cudaSuccess;

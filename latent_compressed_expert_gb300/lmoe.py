@@ -38,7 +38,14 @@ class Weights(ctypes.Structure):
 
 class IO(ctypes.Structure):
     _fields_ = [("tau_in", _vp), ("balance", _i), ("logits_in", _vp), ("logits_out", _vp),
-                ("tau_out", _vp), ("idx_out", _vp), ("gate_out", _vp), ("counts_out", _vp)]
+                ("tau_out", _vp), ("idx_out", _vp), ("gate_out", _vp), ("counts_out", _vp),
+                ("stage_events", ctypes.POINTER(_vp)), ("kernel_launches", _i)]
+
+
+# enum lmoe_stage
+STAGES = ["latent_shared", "router", "thresholds", "route", "dispatch", "expert_gate_up",
+          "expert_down", "combine", "output"]
+NUM_STAGES = len(STAGES)
 
 
 SIGNATURES = {
@@ -211,7 +218,11 @@ class Layer:
 
     def forward(self, x: torch.Tensor, residual: torch.Tensor | None = None, y=None,
                 tau: torch.Tensor | None = None, balance: bool = True,
-                logits_in: torch.Tensor | None = None, debug: bool = False, stream=None):
+                logits_in: torch.Tensor | None = None, debug: bool = False, stream=None,
+                stage_events=None):
+        """One lmoe_forward call.  stage_events: optional list of NUM_STAGES + 1
+        torch.cuda.Event(enable_timing=True) recorded at the stage boundaries.  After the
+        call, ``self.last_kernel_launches`` holds the number of kernels it launched."""
         sh = self.shape
         T = x.shape[0]
         if T > self.max_tokens:
@@ -243,9 +254,20 @@ class Layer:
             io.idx_out = _ptr(dbg["idx"])
             io.gate_out = _ptr(dbg["gate"])
             io.counts_out = _ptr(dbg["counts"])
+        if stage_events is not None:
+            if len(stage_events) != NUM_STAGES + 1:
+                raise ValueError(f"lmoe: need {NUM_STAGES + 1} stage events")
+            handles = []
+            for ev in stage_events:
+                if not ev.cuda_event:      # torch creates its events lazily
+                    ev.record(torch.cuda.current_stream() if stream is None else stream)
+                handles.append(ev.cuda_event)
+            arr = (_vp * len(handles))(*handles)
+            io.stage_events = ctypes.cast(arr, ctypes.POINTER(_vp))
         _check(load().lmoe_forward(ctypes.byref(dims), _ptr(self.packed), _ptr(x), _ptr(residual),
                                    _ptr(y), _ptr(self.workspace), self.ws_bytes,
                                    ctypes.byref(io), _stream(stream)), "lmoe_forward")
+        self.last_kernel_launches = io.kernel_launches
         return (y, dbg) if debug else y
 
     def forward_host(self, x_host: torch.Tensor, y_host: torch.Tensor, x_dev: torch.Tensor,

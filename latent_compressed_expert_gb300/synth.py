@@ -103,7 +103,8 @@ def make_weights(sh: LayerShape, seed: int, device="cpu", hot_row_frac: float = 
     w["w_up"] = _normal((sh.d, sh.L), sh.L ** -0.5, _gen(seed, "w_up", device), device, bf)
     w["w_sgate"] = _normal((sh.S, sh.Is, sh.d), sh.d ** -0.5, _gen(seed, "w_sgate", device), device, bf)
     w["w_svalue"] = _normal((sh.S, sh.Is, sh.d), sh.d ** -0.5, _gen(seed, "w_svalue", device), device, bf)
-    w["w_sdown"] = _normal((sh.S, sh.d, sh.Is), sh.Is ** -0.5, _gen(seed, "w_sdown", device), device, bf)
+    w["w_sdown"] = _normal((sh.S, sh.d, sh.Is), max(sh.Is, 1) ** -0.5, _gen(seed, "w_sdown", device),
+                           device, bf)
     if hot_row_frac > 0.0:
         for name in ("w_gate", "w_value", "w_sgate", "w_svalue"):
             t = w[name]
