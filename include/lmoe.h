@@ -184,6 +184,31 @@ int lmoe_forward(const lmoe_dims *dims, const void *packed, const void *x,
 int lmoe_gemm_bf16(const void *A, const void *B, float *C, int M, int N, int Kd,
                    uint32_t *dev_flag, void *stream);
 
+/* Size in bytes of the fixed device array that lmoe_forward_noalloc uses as its workspace. */
+#define LMOE_NOALLOC_SCRATCH_BYTES (24u << 20)
+
+/* lmoe_forward for callers that cannot allocate device memory.  The pages have no
+ * counterpart to this entry point: it concerns how the library is called, not the layer.
+ * Who needs it: code that may not call cudaMalloc at the point where it runs the layer -- a
+ * plug-in whose host framework owns all device memory through its own pool and gives
+ * extensions no raw allocations, a serving loop in which an allocation would synchronise
+ * the device and stall the other streams, a deployment whose memory is fixed when the
+ * process starts.  Arguments and results are those of lmoe_forward without the workspace.
+ * Scratch: a LMOE_NOALLOC_SCRATCH_BYTES (24 MiB) array in the library's device image,
+ * reserved on every GPU that loads the library until the process exits.  It covers a K3
+ * decode batch of up to 92 tokens (64 tokens need 16.6 MiB).  When lmoe_workspace_bytes(dims)
+ * exceeds it, the call returns LMOE_ERR_WORKSPACE_TOO_SMALL and enqueues nothing.
+ * Set-up: the first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call before any stream
+ * capture.  No call allocates or frees memory.
+ * Sharing: every call on a device uses the same array, which keeps the last call's
+ * contents; each call clears what must start at zero.  Calls whose work overlaps on the
+ * GPU (different streams, or host threads without ordering between them) race on the array
+ * and corrupt each other's results: serialise them.  A device-side time-out is recorded in
+ * the array and cannot be read back with lmoe_last_device_error. */
+int lmoe_forward_noalloc(const lmoe_dims *dims, const void *packed, const void *x,
+                         const void *residual, void *y, lmoe_io *io, void *stream);
+
 /* Synchronously read and clear the device error flag that lmoe_forward's kernels write
  * into `workspace`.  Every device-side wait is bounded (2 s by default; the environment
  * variable LMOE_WAIT_LIMIT_MS overrides it), and LMOE_FAULT_INJECT=stall makes the first

@@ -57,6 +57,8 @@ SIGNATURES = {
     "lmoe_forward": (_i, [ctypes.POINTER(Dims), _vp, _vp, _vp, _vp, _vp, _sz, ctypes.POINTER(IO),
                           _vp]),
     "lmoe_gemm_bf16": (_i, [_vp, _vp, _vp, _i, _i, _i, _vp, _vp]),
+    "lmoe_forward_noalloc": (_i, [ctypes.POINTER(Dims), _vp, _vp, _vp, _vp, ctypes.POINTER(IO),
+                                  _vp]),
     "lmoe_last_device_error": (_i, [_vp]),
     "lmoe_error_string": (ctypes.c_char_p, [_i]),
     "lmoe_version": (ctypes.c_char_p, []),
