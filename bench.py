@@ -216,31 +216,86 @@ def max_over_ranks(v: float, world: int) -> float:
     return float(t.item())
 
 
-def make_inputs(sh, dev, rank):
-    gain = synth.outlier_router_gain(sh, OUTLIER_FRAC, OUTLIER_SCALE)
+SMALL = synth.LayerShape("small", T=1024, d=7168, L=3584, E=128, K=16, I=512, S=2, Is=2048)
+SHAPES = {"prefill": synth.PREFILL, "decode": synth.DECODE, "e64": synth.E64,
+          "skew": synth.SKEW, "small": SMALL}
+DESCRIPTIONS = {
+    "prefill": "K3 Stable Latent MoE layer, prefill: in-batch Quantile-Balancing thresholds; "
+               "x~N(0,1) with 0.1% of elements x1000; residual = x",
+    "decode": "K3 layer, decode: thresholds from a 8192-token prefill batch of the same "
+              "layer passed in; x~N(0,1); residual = x",
+    "e64": "K3 widths with a reduced pool (E=64, top-4): in-batch thresholds; x~N(0,1); "
+           "residual = x",
+    "skew": "K3 layer, skewed router: router logits supplied with a per-expert Zipf(1.1) "
+            "bias (router GEMM not in the step), in-batch thresholds; x~N(0,1); residual = x",
+    "small": "K3 widths, 128 experts, T=1024 (profiling case: ~128 tokens per expert as "
+             "in prefill, a few GB on the device); x as in prefill",
+}
+
+
+class Workload:
+    """Inputs and routing arguments of one bench configuration."""
+
+    def __init__(self, name, dev, rank):
+        self.name = name
+        self.sh = sh = SHAPES[name]
+        outliers = name in ("prefill", "small")
+        gain = synth.outlier_router_gain(sh, OUTLIER_FRAC, OUTLIER_SCALE) if outliers else 1.0
+        self.w = synth.make_weights(sh, SEED, device=dev, router_gain=gain)
+        self.x = synth.make_x(sh, SEED + 1000 * rank, device=dev,
+                              outlier_frac=OUTLIER_FRAC if outliers else 0.0,
+                              outlier_scale=OUTLIER_SCALE)
+        self.layer = lmoe.Layer(sh, self.w, max_tokens=max(sh.T, 8192 if name == "decode" else 0))
+        self.kwargs = {}
+        self.extra = {}
+        if name == "decode":
+            # thresholds of a prefill batch through the same layer
+            xp = synth.make_x(sh, SEED + 7, device=dev, T=8192)
+            _, dbg = self.layer.forward(xp, debug=True)
+            self.kwargs["tau"] = dbg["tau"].clone()
+            del xp, dbg
+        if name == "skew":
+            _, dbg = self.layer.forward(self.x, debug=True, balance=False)
+            bias = synth.make_logits(1, sh.E, SEED, device=dev, zipf_s=1.1) - \
+                synth.make_logits(1, sh.E, SEED, device=dev)
+            self.kwargs["logits_in"] = (dbg["logits"] + bias).contiguous()
+            _, plain = self.layer.forward(self.x, debug=True, balance=False,
+                                          logits_in=self.kwargs["logits_in"])
+            fair = sh.T * sh.K / sh.E
+            c0 = plain["counts"].float()
+            self.extra["load_before"] = {"max_over_mean": float(c0.max() / fair),
+                                         "min_over_mean": float(c0.min() / fair)}
+            del dbg, plain
+
+    def forward(self, **kw):
+        return self.layer.forward(self.x, residual=self.x, **self.kwargs, **kw)
+
+    def config(self, world):
+        sh = self.sh
+        return {"workload": f"{DESCRIPTIONS[self.name]}. T={sh.T} tokens, d={sh.d}, "
+                            f"latent {sh.L}, E={sh.E} routed top-{sh.K}, {sh.S} shared experts "
+                            f"(I_s={sh.Is}), routed I={sh.I}",
+                "shape": self.name, "tokens_per_gpu": sh.T, "global_tokens": sh.T * world,
+                "l2": "inputs larger than L2: the expert weights streamed per step exceed it",
+                "parallelism": f"replicas x{world}, independent batches"}
+
+
+def make_inputs(sh, dev, rank, outliers=True):
+    """The same weights and x that Workload draws (for the CPU-only reference arm)."""
+    gain = synth.outlier_router_gain(sh, OUTLIER_FRAC, OUTLIER_SCALE) if outliers else 1.0
     w = synth.make_weights(sh, SEED, device=dev, router_gain=gain)
-    x = synth.make_x(sh, SEED + 1000 * rank, device=dev, outlier_frac=OUTLIER_FRAC,
-                     outlier_scale=OUTLIER_SCALE)
+    x = synth.make_x(sh, SEED + 1000 * rank, device=dev,
+                     outlier_frac=OUTLIER_FRAC if outliers else 0.0, outlier_scale=OUTLIER_SCALE)
     return w, x
-
-
-def workload_config(sh, world):
-    return {"workload": f"K3 Stable Latent MoE layer, prefill: T={sh.T} tokens, d={sh.d}, "
-                        f"latent {sh.L}, E={sh.E} routed top-{sh.K}, {sh.S} shared experts "
-                        f"(I_s={sh.Is}), routed I={sh.I}; in-batch Quantile-Balancing "
-                        f"thresholds; x~N(0,1) with 0.1% of elements x1000; residual = x",
-            "tokens_per_gpu": sh.T, "global_tokens": sh.T * world,
-            "l2": "inputs larger than L2: 10.2 GB of weights streamed per step",
-            "parallelism": f"replicas x{world}, independent batches"}
 
 
 def run_reference(args):
     world, rank, _ = dist_setup(args.gpus)
     if rank != 0:
         return 0
-    sh = synth.PREFILL
+    sh = SHAPES[args.shape]
     dev = "cuda" if torch.cuda.is_available() else "cpu"
-    w, x = make_inputs(sh, dev, 0)
+    w, x = make_inputs(sh, dev, 0, outliers=args.shape in ("prefill", "small"))
     wh = host_weights(w)
     xh = x.cpu()
     del w, x
@@ -264,7 +319,10 @@ def run_reference(args):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * dt / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": workload_config(sh, 1),
+            "config": {"workload": f"{DESCRIPTIONS[args.shape]}. T={sh.T} tokens, d={sh.d}, "
+                                   f"latent {sh.L}, E={sh.E} routed top-{sh.K}, {sh.S} shared "
+                                   f"experts (I_s={sh.Is}), routed I={sh.I}",
+                       "shape": args.shape, "tokens_per_gpu": sh.T, "global_tokens": sh.T},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
@@ -278,15 +336,14 @@ def run_ours(args):
     if not torch.cuda.is_available():
         raise RuntimeError("bench.py needs a CUDA GPU (the layer has no CPU path)")
     dev = torch.device("cuda", local)
-    sh = synth.PREFILL
-    w, x = make_inputs(sh, dev, rank)
-    layer = lmoe.Layer(sh, w)
+    wl = Workload(args.shape, dev, rank)
+    sh, layer, x, w = wl.sh, wl.layer, wl.x, wl.w
     y = torch.empty_like(x)
     stream = torch.cuda.current_stream()
 
     # warm-up (also learns how many experts a step touches)
     for _ in range(args.warmup):
-        _, dbg = layer.forward(x, residual=x, y=y, debug=True)
+        _, dbg = wl.forward(y=y, debug=True)
     torch.cuda.synchronize()
     if layer.device_error() != 0:
         raise RuntimeError("device-side error during warm-up")
@@ -307,7 +364,7 @@ def run_ours(args):
         torch.cuda.synchronize()
         start.record(stream)
         for i in range(args.steps):
-            layer.forward(x, residual=x, y=y, stage_events=evs[i])
+            wl.forward(y=y, stage_events=evs[i])
         end.record(stream)
         torch.cuda.synchronize()
     barrier(world)
@@ -324,13 +381,13 @@ def run_ours(args):
     y_host = torch.empty_like(x_host).pin_memory()
     x_dev = torch.empty_like(x)
     for _ in range(max(1, args.warmup)):
-        layer.forward_host(x_host, y_host, x_dev, y)
+        layer.forward_host(x_host, y_host, x_dev, y, **wl.kwargs)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     barrier(world)
     e0.record(stream)
     for _ in range(args.steps):
-        layer.forward_host(x_host, y_host, x_dev, y)
+        layer.forward_host(x_host, y_host, x_dev, y, **wl.kwargs)
     e1.record(stream)
     torch.cuda.synchronize()
     barrier(world)
@@ -372,7 +429,7 @@ def run_ours(args):
             "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded; random-init weights of the K3 layer shape)",
-            "config": workload_config(sh, world),
+            "config": wl.config(world),
             "tflops": flop / step_s / 1e12,
             "frac_bf16_peak": flop / step_s / 1e12 / peaks["bf16_tflops_sustained"],
             "layer_roofline_ms": 1e3 * max(flop / (peaks["bf16_tflops_sustained"] * 1e12),
@@ -384,6 +441,13 @@ def run_ours(args):
                     "d2h_bytes_per_step": y.numel() * 2},
             "gpu_launches": launches_per_step * args.steps}
 
+    if wl.name == "skew":
+        fair = sh.T * sh.K / sh.E
+        line["load"] = {"before_balancing": wl.extra["load_before"],
+                        "after_balancing": {"max_over_mean": float(counts.max() / fair),
+                                            "min_over_mean": float(counts.min() / fair)}}
+    if wl.name == "decode":
+        line["decode_weight_gbs"] = layer_work(sh, touched)[1] / step_s / 1e9
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         wh = host_weights(w)
         xh = x.cpu()
@@ -406,6 +470,8 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--shape", choices=sorted(SHAPES), default="prefill",
+                    help="workload (prefill is the headline; the others are extra lines)")
     ap.add_argument("--cpu-tokens", type=int, default=128,
                     help="tokens in the timed CPU-oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")

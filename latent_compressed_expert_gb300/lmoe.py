@@ -273,11 +273,13 @@ class Layer:
         return (y, dbg) if debug else y
 
     def forward_host(self, x_host: torch.Tensor, y_host: torch.Tensor, x_dev: torch.Tensor,
-                     y_dev: torch.Tensor, residual_from_x: bool = True, stream=None):
+                     y_dev: torch.Tensor, residual_from_x: bool = True, stream=None, **kw):
         """End-to-end call from host memory: copy x (pinned host) to the device, run the
-        layer, copy y back to pinned host memory; all on one stream, asynchronous."""
+        layer, copy y back to pinned host memory; all on one stream, asynchronous.  Extra
+        keyword arguments (tau, balance, logits_in) go to ``forward``."""
         x_dev.copy_(x_host, non_blocking=True)
-        self.forward(x_dev, residual=x_dev if residual_from_x else None, y=y_dev, stream=stream)
+        self.forward(x_dev, residual=x_dev if residual_from_x else None, y=y_dev, stream=stream,
+                     **kw)
         y_host.copy_(y_dev, non_blocking=True)
         return y_host
 
