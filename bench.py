@@ -185,16 +185,19 @@ def time_oracle(sh, wh, x_host, n_tokens, reps=1):
 
 
 # ----------------------------------------------------------------------------------------
-def dist_setup(n_gpus):
+def dist_setup(n_gpus, backend=None):
+    """Rank, world size and local rank from the torchrun environment; one GPU per rank."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if world > 1:
         import torch.distributed as dist
-        backend = "nccl" if torch.cuda.is_available() else "gloo"
-        if torch.cuda.is_available():
+        if backend is None:
+            backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
             torch.cuda.set_device(local)
-        dist.init_process_group(backend=backend)
+        if not dist.is_initialized():
+            dist.init_process_group(backend=backend)
     elif torch.cuda.is_available():
         torch.cuda.set_device(0)
     return world, rank, local
@@ -210,8 +213,8 @@ def max_over_ranks(v: float, world: int) -> float:
     if world == 1:
         return v
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64,
-                     device="cuda" if torch.cuda.is_available() else "cpu")
+    on_gpu = dist.get_backend() == "nccl"
+    t = torch.tensor([v], dtype=torch.float64, device="cuda" if on_gpu else "cpu")
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 

@@ -1,0 +1,43 @@
+"""Failure detection without a GPU fault: a device-side wait is made to run out (the first
+GEMM waits on an mbarrier that nothing arrives on), every role of that kernel gives up
+within the wait limit, frees its tensor memory and returns; the host reads the time-out
+from the workspace flag, and the next call on the same context is correct again."""
+import numpy as np
+import pytest
+import torch
+
+import gpu_helpers as H
+from latent_compressed_expert_gb300 import lmoe, synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from latent_compressed_expert_gb300 import build
+    build.build()
+    lmoe.load()
+    return torch.device("cuda:0")
+
+
+def test_stalled_wait_reports_timeout_and_context_recovers(dev, oracle_mod, monkeypatch):
+    sh = synth.TINY
+    w = synth.make_weights(sh, seed=9)
+    layer = lmoe.Layer(sh, {k: v.to(dev) for k, v in w.items()})
+    x = synth.make_x(sh, seed=9)
+    xd = x.to(dev)
+    logits = synth.make_logits(sh.T, sh.E, seed=9)
+    monkeypatch.setenv("LMOE_WAIT_LIMIT_MS", "200")
+    monkeypatch.setenv("LMOE_FAULT_INJECT", "stall")
+    layer.forward(xd, residual=xd, logits_in=logits.to(dev))
+    torch.cuda.synchronize()
+    assert layer.device_error() == lmoe.LMOE_ERR_DEVICE_TIMEOUT
+    assert layer.device_error() == lmoe.LMOE_OK  # reading clears the flag
+    monkeypatch.delenv("LMOE_FAULT_INJECT")
+    y = layer.forward(xd, residual=xd, logits_in=logits.to(dev))
+    torch.cuda.synchronize()
+    assert layer.device_error() == lmoe.LMOE_OK
+    ref = oracle_mod.forward(w, x, sh.K, residual=x, tau="batch", logits_in=logits.numpy())
+    H.assert_close(y.float().cpu().numpy(), ref.y, "after-timeout")
