@@ -72,7 +72,7 @@ WorkspaceLayout workspace_layout(const lmoe_dims& D) {
   W.masks = take(nb * D.E * 4);
   W.base = take(nb * D.E * 4);
   W.offsets = take((static_cast<size_t>(D.E) + 1) * 4);
-  W.mt_off = take((static_cast<size_t>(D.E) + 1) * 4);
+  W.ct_off = take((static_cast<size_t>(D.E) + 1) * 4);
   W.inv = take(TK * 4);
   W.lat_p = take(TK * D.L * 2);
   W.h = take(TK * D.I * 2);
@@ -309,47 +309,49 @@ int lmoe_forward(const lmoe_dims* dims, const void* packed, const void* x, const
   if (!mark(LMOE_STAGE_DISPATCH, 1)) return LMOE_ERR_CUDA;
   // 5. dispatch into expert-contiguous segments
   int32_t* offsets = reinterpret_cast<int32_t*>(ws + W.offsets);
-  int32_t* mt_off = reinterpret_cast<int32_t*>(ws + W.mt_off);
+  int32_t* ct_off = reinterpret_cast<int32_t*>(ws + W.ct_off);
   int32_t* inv = reinterpret_cast<int32_t*>(ws + W.inv);
   bf* lat_p = reinterpret_cast<bf*>(ws + W.lat_p);
   rc = launch_dispatch(idx, lat, T, D.E, D.K, D.L, reinterpret_cast<uint32_t*>(ws + W.masks),
-                       reinterpret_cast<uint32_t*>(ws + W.base), offsets, mt_off, inv, lat_p,
+                       reinterpret_cast<uint32_t*>(ws + W.base), offsets, ct_off, inv, lat_p,
                        opt.counts_out, err, stream);
   if (rc != LMOE_OK) return rc;
   if (!mark(LMOE_STAGE_EXPERT_GATE_UP, 3)) return LMOE_ERR_CUDA;
-  // 6. grouped gate/value GEMM with SiTU-GLU: h = SiTU(lat_p . W_gu[e]^T)
+  // 6. routed gate/value GEMM with SiTU-GLU: h = SiTU(lat_p . W_gu[e]^T) per expert
   bf* h = reinterpret_cast<bf*>(ws + W.h);
   {
-    GemmArgs g = gemm_defaults(err, D.c);
-    g.grouped = 1;
+    GroupedArgs g{};
     g.E = D.E;
-    g.seg_off = offsets;
-    g.mt_off = mt_off;
-    g.N = 2 * D.I;
+    g.M_w = 2 * D.I;
     g.Kd = D.L;
+    g.seg_off = offsets;
+    g.ct_off = ct_off;
     g.epi = EPI_SITU;
-    g.out1 = h;
-    g.ld1 = D.I;
-    rc = launch_gemm(lat_p, static_cast<uint64_t>(TK), D.L, pk + P.wgu,
-                     static_cast<uint64_t>(D.E) * 2 * D.I, D.L, g, stream);
+    g.out = h;
+    g.ldo = D.I;
+    g.c = D.c;
+    g.err = err;
+    g.timeout_ns = wait_limit_ns();
+    rc = launch_grouped_gemm(pk + P.wgu, D.L, lat_p, static_cast<uint64_t>(TK), D.L, g, stream);
     if (rc != LMOE_OK) return rc;
   }
   if (!mark(LMOE_STAGE_EXPERT_DOWN, 1)) return LMOE_ERR_CUDA;
-  // 7. grouped down GEMM: o = h . W_ed[e]^T
+  // 7. routed down GEMM: o = h . W_ed[e]^T per expert
   bf* o = reinterpret_cast<bf*>(ws + W.o);
   {
-    GemmArgs g = gemm_defaults(err, D.c);
-    g.grouped = 1;
+    GroupedArgs g{};
     g.E = D.E;
-    g.seg_off = offsets;
-    g.mt_off = mt_off;
-    g.N = D.L;
+    g.M_w = D.L;
     g.Kd = D.I;
+    g.seg_off = offsets;
+    g.ct_off = ct_off;
     g.epi = EPI_BF16;
-    g.out0 = o;
-    g.ld0 = D.L;
-    rc = launch_gemm(h, static_cast<uint64_t>(TK), D.I, pk + P.wed,
-                     static_cast<uint64_t>(D.E) * D.L, D.I, g, stream);
+    g.out = o;
+    g.ldo = D.L;
+    g.c = D.c;
+    g.err = err;
+    g.timeout_ns = wait_limit_ns();
+    rc = launch_grouped_gemm(pk + P.wed, D.I, h, static_cast<uint64_t>(TK), D.I, g, stream);
     if (rc != LMOE_OK) return rc;
   }
   if (!mark(LMOE_STAGE_COMBINE, 1)) return LMOE_ERR_CUDA;

@@ -31,6 +31,11 @@ constexpr int GLU_GROUP = 16;
 // Tokens per block in the dispatch (permute) kernels: one 32-bit mask word per expert.
 constexpr int DISPATCH_TOKENS = 32;
 
+// Largest token count (MMA N) of one routed-expert GEMM tile; an expert's token rows are cut
+// into chunks of at most this many.  192 covers the K3 prefill load (146 on average, under
+// 1.2x that at most with Quantile-Balancing thresholds) in one chunk.
+constexpr int GROUPED_TOKN = 192;
+
 __host__ __device__ inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 __device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {

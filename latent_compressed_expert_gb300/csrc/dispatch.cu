@@ -42,11 +42,12 @@ dispatch_mask_kernel(const int32_t* __restrict__ idx, int T, int E, int K,
 }
 
 // One CTA: base[b][e] = picks of expert e in blocks < b; offsets = exclusive scan of the
-// counts over experts; mt_off = exclusive scan of ceil(count / 128) (GEMM row tiles).
+// counts over experts; ct_off = exclusive scan of ceil(count / GROUPED_TOKN) (the token
+// chunks of the routed-expert GEMMs).
 __global__ void __launch_bounds__(1024)
 dispatch_scan_kernel(const uint32_t* __restrict__ masks, int nb, int E, int TK,
                      uint32_t* __restrict__ base, int32_t* __restrict__ offsets,
-                     int32_t* __restrict__ mt_off, int32_t* __restrict__ counts_out) {
+                     int32_t* __restrict__ ct_off, int32_t* __restrict__ counts_out) {
   __shared__ int32_t warp_cnt[32], warp_mt[32];
   __shared__ int32_t carry_cnt, carry_mt;
   if (threadIdx.x == 0) {
@@ -80,7 +81,7 @@ dispatch_scan_kernel(const uint32_t* __restrict__ masks, int nb, int E, int TK,
       }
       if (counts_out) counts_out[e] = cnt;
     }
-    const int mt = static_cast<int>(ceil_div(cnt, BLOCK_M));
+    const int mt = static_cast<int>(ceil_div(cnt, GROUPED_TOKN));
     // block-wide exclusive scans of cnt and mt
     int ic = cnt, im = mt;
     for (int o = 1; o < 32; o <<= 1) {
@@ -117,7 +118,7 @@ dispatch_scan_kernel(const uint32_t* __restrict__ masks, int nb, int E, int TK,
     const int before_m = (warp > 0 ? warp_mt[warp - 1] : 0) + (im - mt);
     if (e < E) {
       offsets[e] = carry_cnt + before_c;
-      mt_off[e] = carry_mt + before_m;
+      ct_off[e] = carry_mt + before_m;
     }
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -128,7 +129,7 @@ dispatch_scan_kernel(const uint32_t* __restrict__ masks, int nb, int E, int TK,
   }
   if (threadIdx.x == 0) {
     offsets[E] = carry_cnt;  // == T*K when every index was valid
-    mt_off[E] = carry_mt;
+    ct_off[E] = carry_mt;
     (void)TK;
   }
 }
@@ -238,7 +239,7 @@ combine_rmsnorm_kernel(const __nv_bfloat16* __restrict__ o, const float* __restr
 
 // ------------------------------------------------------------------------------------
 int launch_dispatch(const int32_t* idx, const __nv_bfloat16* lat, int T, int E, int K, int L,
-                    uint32_t* masks, uint32_t* base, int32_t* offsets, int32_t* mt_off,
+                    uint32_t* masks, uint32_t* base, int32_t* offsets, int32_t* ct_off,
                     int32_t* inv, __nv_bfloat16* lat_p, int32_t* counts_out, uint32_t* err,
                     cudaStream_t stream) {
   const int nb = static_cast<int>(ceil_div(T, DISPATCH_TOKENS));
@@ -247,7 +248,7 @@ int launch_dispatch(const int32_t* idx, const __nv_bfloat16* lat, int T, int E, 
     dispatch_mask_kernel<<<nb, 256, msmem, stream>>>(idx, T, E, K, masks, err);
     if (cudaGetLastError() != cudaSuccess) return LMOE_ERR_CUDA;
   }
-  dispatch_scan_kernel<<<1, 1024, 0, stream>>>(masks, nb, E, T * K, base, offsets, mt_off,
+  dispatch_scan_kernel<<<1, 1024, 0, stream>>>(masks, nb, E, T * K, base, offsets, ct_off,
                                                counts_out);
   if (cudaGetLastError() != cudaSuccess) return LMOE_ERR_CUDA;
   if (nb > 0) {

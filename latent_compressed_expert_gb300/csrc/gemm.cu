@@ -12,10 +12,8 @@
 //               bf16 / fp32 store, SiTU-GLU on interleaved gate/value columns, residual add),
 //               then release the accumulator ("tmem_empty") so the MMA of the tile after
 //               next can start while this one is written out.
-// Grouped mode runs one GEMM per expert segment: A rows are the expert's contiguous rows
-// of the permuted activations (segment offsets produced on the device), B rows the
-// expert's weight slice; tiles are enumerated from a device-side prefix sum of row-tile
-// counts, so no count ever travels back to the host.
+// This kernel serves the dense contractions (x-side GEMM, router, output GEMM); the routed
+// experts' GEMMs are in gemm_grouped.cu.
 //
 // Every wait is bounded (globaltimer); on time-out a role records an error bit in global
 // memory, raises a shared abort flag that makes the other roles give up too, waits for
@@ -57,45 +55,21 @@ struct TileCoord {
 };
 
 template <int BN>
-__device__ __forceinline__ TileCoord decode_tile(const GemmArgs& g, int nt, int mt_dense,
-                                                 int tile) {
+__device__ __forceinline__ TileCoord decode_tile(const GemmArgs& g, int nt, int mt, int tile) {
+  // groups of RASTER_GROUP_M row tiles sweep all column tiles, rows fastest, so the CTAs in
+  // flight share a few A row-panels and B column-panels in L2
+  const int span = RASTER_GROUP_M * nt;
+  const int grp = tile / span;
+  const int first_m = grp * RASTER_GROUP_M;
+  const int gm = min(RASTER_GROUP_M, mt - first_m);
+  const int local = tile - grp * span;
+  const int m = first_m + local % gm;
+  const int n = local / gm;
   TileCoord c;
-  if (!g.grouped) {
-    // groups of RASTER_GROUP_M row tiles sweep all column tiles, rows fastest, so the
-    // CTAs in flight share a few A row-panels and B column-panels in L2
-    const int span = RASTER_GROUP_M * nt;
-    const int grp = tile / span;
-    const int first_m = grp * RASTER_GROUP_M;
-    const int gm = min(RASTER_GROUP_M, mt_dense - first_m);
-    const int local = tile - grp * span;
-    const int m = first_m + local % gm;
-    const int n = local / gm;
-    c.a_row = m * BLOCK_M;
-    c.row_end = g.M;
-    c.b_row = n * BN;
-    c.n0 = n * BN;
-  } else {
-    // tiles of expert e occupy [mt_off[e] * nt, mt_off[e+1] * nt); rows fastest so the
-    // row tiles of one expert that share a weight slice run side by side
-    const int q = tile / nt;
-    int lo = 0, hi = g.E;  // mt_off[lo] <= q < mt_off[hi]
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (__ldg(g.mt_off + mid) <= q)
-        lo = mid;
-      else
-        hi = mid;
-    }
-    const int e = lo;
-    const int mt0 = __ldg(g.mt_off + e);
-    const int mte = __ldg(g.mt_off + e + 1) - mt0;
-    const int local = tile - mt0 * nt;
-    const int n = local / mte, m = local % mte;
-    c.a_row = __ldg(g.seg_off + e) + m * BLOCK_M;
-    c.row_end = __ldg(g.seg_off + e + 1);
-    c.b_row = e * g.N + n * BN;
-    c.n0 = n * BN;
-  }
+  c.a_row = m * BLOCK_M;
+  c.row_end = g.M;
+  c.b_row = n * BN;
+  c.n0 = n * BN;
   return c;
 }
 
@@ -235,8 +209,8 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA,
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nt = (g.N + BN - 1) / BN;
   const int nk = g.Kd / BLOCK_K;
-  const int mt_dense = g.grouped ? 0 : (g.M + BLOCK_M - 1) / BLOCK_M;
-  const int total = g.grouped ? __ldg(g.mt_off + g.E) * nt : mt_dense * nt;
+  const int mt_dense = (g.M + BLOCK_M - 1) / BLOCK_M;
+  const int total = mt_dense * nt;
   const uint64_t limit = g.timeout_ns;
 
   if (threadIdx.x == 0) {
@@ -431,10 +405,8 @@ static int launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArg
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return LMOE_ERR_CUDA;
   int grid = sms;
-  if (!g.grouped) {
-    const int64_t tiles = ceil_div(g.M, BLOCK_M) * ceil_div(g.N, BN);
-    if (tiles < grid) grid = static_cast<int>(tiles);
-  }
+  const int64_t tiles = ceil_div(g.M, BLOCK_M) * ceil_div(g.N, BN);
+  if (tiles < grid) grid = static_cast<int>(tiles);
   if (grid <= 0) return LMOE_OK;
   gemm_tcgen05_kernel<BN><<<grid, GEMM_THREADS, C::SMEM_BYTES, stream>>>(ta, tb, g);
   return cudaGetLastError() == cudaSuccess ? LMOE_OK : LMOE_ERR_CUDA;
@@ -446,7 +418,7 @@ int launch_gemm(const void* A, uint64_t a_rows, int a_ld, const void* B, uint64_
   const bool glu = g.epi == EPI_SITU || g.epi == EPI_SPLIT;
   if (g.N % (glu ? 32 : 16) != 0 || (g.epi == EPI_SPLIT && g.split % 32 != 0))
     return LMOE_ERR_UNSUPPORTED;
-  if (!g.grouped && g.M == 0) return LMOE_OK;
+  if (g.M == 0) return LMOE_OK;
   const int bn = (g.N % 256 == 0) ? 256 : 128;
   CUtensorMap ta, tb;
   if (!make_tmap_bf16(&ta, A, a_rows, static_cast<uint64_t>(g.Kd), static_cast<uint64_t>(a_ld),

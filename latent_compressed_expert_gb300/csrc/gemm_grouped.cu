@@ -1,0 +1,305 @@
+// gemm_grouped.cu -- the routed experts' GEMMs, one small GEMM per expert segment, on the
+// 5th-generation tensor cores with the operands swapped ("swap-AB"):
+//
+//   out[tok, r] = sum_k act[tok, k] * W[e][r, k]     for the tokens tok routed to expert e
+//
+// computed as D[r, tok] = W[e][r, :] . act[tok, :]^T, so that the expert's weight rows fill
+// the MMA's M = 128 dimension and its tokens form N (a multiple of 32, at most TOKN).  An
+// expert sees ~T*K/E tokens (146 at the K3 prefill shape, ~1 at decode): as N they cost no
+// padded MMA rows, and every weight byte is staged into shared memory exactly once while
+// the expert's few token rows are re-read from L2.
+//
+// Tiles: for each expert e, its token rows are cut into chunks of at most TOKN; each
+// (expert, chunk) pair has M_w / 128 weight row-tiles, enumerated fastest so that the tiles
+// sharing a token chunk run on neighbouring SMs at the same time.  The chunk counts come
+// from a device-side prefix sum; nothing returns to the host.
+//
+// Roles as in gemm.cu: warp 0 TMA producer (one 128 x 64 weight box + one 32 x 64 box per 32
+// tokens), warp 1 TMEM owner and single-thread tcgen05.mma issuer (instruction descriptor
+// with the tile's N built at run time), warps 2-5 epilogue.  In the epilogue a thread owns
+// one weight row (one output feature) and walks the tokens, so a warp writes 32 consecutive
+// features of one token row per store.  Gate/value epilogue (SiTU-GLU): weight rows are
+// interleaved 16 gate / 16 value, so lanes l and l+16 hold the gate and value of the same
+// feature and meet through one shuffle.
+#include "common.cuh"
+#include "kernels.cuh"
+#include "ptx.cuh"
+
+namespace lmoe {
+
+struct GroupedCfg {
+  static constexpr int TOKN = GROUPED_TOKN;               // max tokens (N) per tile
+  static constexpr int BOX_T = 32;                        // token rows per TMA box
+  static constexpr int A_BYTES = BLOCK_M * BLOCK_K * 2;   // 16 KB of weights
+  static constexpr int B_BYTES = TOKN * BLOCK_K * 2;      // up to 24 KB of activations
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES = 5;
+  static constexpr int ACC_COLS = 256;                    // TMEM columns between accumulators
+  static constexpr int TMEM_COLS = 512;
+  static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
+  static constexpr int NUM_BARS = 2 * STAGES + 5;
+  static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
+  static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;
+  static_assert(TOKN % BOX_T == 0 && TOKN % 16 == 0 && TOKN <= 256, "UMMA N range");
+  static_assert(TOKN <= ACC_COLS && 2 * ACC_COLS <= TMEM_COLS, "two accumulators");
+  static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "1024-aligned tiles");
+  static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+};
+
+constexpr int GROUPED_THREADS = 192;
+
+struct GTile {
+  int w_row;    // first weight row (packed [E * M_w, Kd])
+  int r0;       // first weight row within the expert (output feature)
+  int tok0;     // first token row (permuted order)
+  int ntok;     // valid token rows in this tile (1..TOKN)
+  int npad;     // ntok rounded up to BOX_T
+};
+
+__device__ __forceinline__ GTile decode_gtile(const GroupedArgs& g, int mt, int tile) {
+  const int q = tile / mt;  // global (expert, chunk) index
+  int lo = 0, hi = g.E;     // ct_off[lo] <= q < ct_off[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(g.ct_off + mid) <= q)
+      lo = mid;
+    else
+      hi = mid;
+  }
+  const int e = lo;
+  const int chunk = q - __ldg(g.ct_off + e);
+  const int m = tile - q * mt;
+  GTile t;
+  t.r0 = m * BLOCK_M;
+  t.w_row = e * g.M_w + t.r0;
+  t.tok0 = __ldg(g.seg_off + e) + chunk * GroupedCfg::TOKN;
+  const int end = __ldg(g.seg_off + e + 1);
+  t.ntok = min(GroupedCfg::TOKN, end - t.tok0);
+  t.npad = (t.ntok + GroupedCfg::BOX_T - 1) / GroupedCfg::BOX_T * GroupedCfg::BOX_T;
+  return t;
+}
+
+__device__ __forceinline__ void graise(const GroupedArgs& g, volatile int* abort_flag,
+                                       uint32_t code) {
+  *abort_flag = 1;
+  atomicOr(g.err, code);
+}
+
+__device__ __forceinline__ bool gwait_drain(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = ptx::globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 0u && ptx::globaltimer_ns() - t0 > limit_ns) return false;
+  }
+}
+
+// SiTU-GLU, as in the dense epilogue: silu(c tanh(g/c)) * c tanh(v/c).
+__device__ __forceinline__ float situ_g(float g, float v, float c, float inv_c) {
+  const float gc = c * ptx::tanh_approx(g * inv_c);
+  const float vc = c * ptx::tanh_approx(v * inv_c);
+  return __fdividef(gc, 1.0f + __expf(fminf(-gc, 80.0f))) * vc;
+}
+
+__global__ void __launch_bounds__(GROUPED_THREADS, 1)
+grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
+                    const __grid_constant__ CUtensorMap tmX, const GroupedArgs g) {
+  using C = GroupedCfg;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = ptx::smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
+  uint64_t* empty = full + C::STAGES;
+  uint64_t* tfull = empty + C::STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::MISC_OFF);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int mt = (g.M_w + BLOCK_M - 1) / BLOCK_M;
+  const int nk = g.Kd / BLOCK_K;
+  const int total = __ldg(g.ct_off + g.E) * mt;
+  const uint64_t limit = g.timeout_ns;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      ptx::mbar_init(&full[s], 1);
+      ptx::mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      ptx::mbar_init(&tfull[a], 1);
+      ptx::mbar_init(&tempty[a], 128);
+    }
+    ptx::mbar_init(drain, 1);
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::prefetch_tmap(&tmW);
+    ptx::prefetch_tmap(&tmX);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(tmem_slot, C::TMEM_COLS);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ TMA producer
+      uint32_t it = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+        const GTile t = decode_gtile(g, mt, tile);
+        const int nbox = t.npad / C::BOX_T;
+        const uint32_t bytes = C::A_BYTES + static_cast<uint32_t>(nbox) * C::BOX_T * BLOCK_K * 2;
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int s = static_cast<int>(it % C::STAGES);
+          const uint32_t ph = (it / C::STAGES) & 1u;
+          if (!ptx::mbar_wait(&empty[s], ph ^ 1u, abort_flag, limit)) {
+            graise(g, abort_flag, DEVERR_TIMEOUT_PRODUCER);
+            ok = false;
+            break;
+          }
+          uint8_t* sa = smem + s * C::STAGE_BYTES;
+          uint8_t* sb = sa + C::A_BYTES;
+          ptx::mbar_arrive_expect_tx(&full[s], bytes);
+          ptx::tma_load_2d(sa, &tmW, &full[s], kb * BLOCK_K, t.w_row);
+          for (int b = 0; b < nbox; ++b)
+            ptx::tma_load_2d(sb + b * C::BOX_T * BLOCK_K * 2, &tmX, &full[s], kb * BLOCK_K,
+                             t.tok0 + b * C::BOX_T);
+        }
+      }
+      const uint32_t first = it > static_cast<uint32_t>(C::STAGES) ? it - C::STAGES : 0u;
+      for (uint32_t j = first; j < it; ++j) {
+        if (!gwait_drain(&full[j % C::STAGES], (j / C::STAGES) & 1u, limit)) {
+          graise(g, abort_flag, DEVERR_TIMEOUT_DRAIN);
+          break;
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ MMA issuer
+      uint32_t it = 0;
+      int lt = 0;
+      for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++lt) {
+        const GTile t = decode_gtile(g, mt, tile);
+        const uint32_t idesc = ptx::idesc_bf16_f32(BLOCK_M, t.npad);
+        const int acc = lt & 1;
+        const uint32_t aph = static_cast<uint32_t>(lt >> 1) & 1u;
+        if (!ptx::mbar_wait(&tempty[acc], aph ^ 1u, abort_flag, limit)) {
+          graise(g, abort_flag, DEVERR_TIMEOUT_MMA);
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * C::ACC_COLS);
+        bool ok = true;
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int s = static_cast<int>(it % C::STAGES);
+          const uint32_t ph = (it / C::STAGES) & 1u;
+          if (!ptx::mbar_wait(&full[s], ph, abort_flag, limit)) {
+            graise(g, abort_flag, DEVERR_TIMEOUT_MMA);
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t sa = ptx::smem_u32(smem + s * C::STAGE_BYTES);
+          const uint32_t sb = sa + C::A_BYTES;
+#pragma unroll
+          for (int k = 0; k < BLOCK_K / 16; ++k)
+            ptx::umma_bf16(d_tmem, ptx::smem_desc_sw128(sa + k * 32),
+                           ptx::smem_desc_sw128(sb + k * 32), idesc, (kb | k) != 0 ? 1u : 0u);
+          ptx::umma_commit(&empty[s]);
+        }
+        if (!ok) break;
+        ptx::umma_commit(&tfull[acc]);
+      }
+      ptx::umma_commit(drain);
+      if (!gwait_drain(drain, 0u, limit)) graise(g, abort_flag, DEVERR_TIMEOUT_DRAIN);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue (warps 2..5)
+    const int q = warp & 3;
+    const float c = g.c, inv_c = 1.0f / g.c;
+    int lt = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++lt) {
+      const int acc = lt & 1;
+      const uint32_t aph = static_cast<uint32_t>(lt >> 1) & 1u;
+      const bool got = ptx::mbar_wait(&tfull[acc], aph, abort_flag, limit);
+      if (!__all_sync(0xffffffffu, got)) {
+        if (lane == 0) graise(g, abort_flag, DEVERR_TIMEOUT_EPILOGUE);
+        break;
+      }
+      ptx::tc_fence_after();
+      const GTile t = decode_gtile(g, mt, tile);
+      const int r = t.r0 + q * 32 + lane;  // weight row of this thread within the expert
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                             static_cast<uint32_t>(acc * C::ACC_COLS);
+      const bool row_ok = r < g.M_w;  // the last weight tile of an expert may be partial
+#pragma unroll 1
+      for (int ch = 0; ch * 32 < t.npad; ++ch) {
+        float v[32];
+        ptx::tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(ch * 32), v);
+        const int nv = min(32, t.ntok - ch * 32);
+        __nv_bfloat16* orow = g.out + static_cast<size_t>(t.tok0 + ch * 32) * g.ldo;
+        if (g.epi == EPI_SITU) {
+          // rows r (gate, lanes 0..15) and r + 16 (value, lanes 16..31) of one 32-row group
+          const int f = ((t.r0 + q * 32) >> 1) + (lane & 15);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const float val = __shfl_xor_sync(0xffffffffu, v[j], 16);
+            if (lane < 16 && j < nv)
+              orow[static_cast<size_t>(j) * g.ldo + f] =
+                  __float2bfloat16_rn(situ_g(v[j], val, c, inv_c));
+          }
+        } else {
+          if (row_ok) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (j < nv) orow[static_cast<size_t>(j) * g.ldo + r] = __float2bfloat16_rn(v[j]);
+          }
+        }
+      }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(&tempty[acc]);
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
+}
+
+int launch_grouped_gemm(const void* W, int w_ld, const void* X, uint64_t x_rows, int x_ld,
+                        const GroupedArgs& g, cudaStream_t stream) {
+  using C = GroupedCfg;
+  if (g.M_w <= 0 || g.Kd % BLOCK_K != 0 || g.Kd <= 0 || x_rows == 0) return LMOE_ERR_UNSUPPORTED;
+  if (g.epi != EPI_SITU && g.epi != EPI_BF16) return LMOE_ERR_UNSUPPORTED;
+  if (g.epi == EPI_SITU && g.M_w % BLOCK_M != 0) return LMOE_ERR_UNSUPPORTED;
+  CUtensorMap tw, tx;
+  if (!make_tmap_bf16(&tw, W, static_cast<uint64_t>(g.E) * g.M_w, static_cast<uint64_t>(g.Kd),
+                      static_cast<uint64_t>(w_ld), BLOCK_M) ||
+      !make_tmap_bf16(&tx, X, x_rows, static_cast<uint64_t>(g.Kd), static_cast<uint64_t>(x_ld),
+                      C::BOX_T))
+    return LMOE_ERR_CUDA;
+  if (cudaFuncSetAttribute(grouped_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           C::SMEM_BYTES) != cudaSuccess)
+    return LMOE_ERR_CUDA;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return LMOE_ERR_CUDA;
+  grouped_gemm_kernel<<<sms, GROUPED_THREADS, C::SMEM_BYTES, stream>>>(tw, tx, g);
+  return cudaGetLastError() == cudaSuccess ? LMOE_OK : LMOE_ERR_CUDA;
+}
+
+}  // namespace lmoe

@@ -15,7 +15,7 @@ struct PackedLayout {
 
 // Offsets (bytes) of the forward workspace; every buffer 256-aligned.
 struct WorkspaceLayout {
-  size_t err, lat, logits, tau, idx, gate, masks, base, offsets, mt_off, inv, lat_p, h, o, zh,
+  size_t err, lat, logits, tau, idx, gate, masks, base, offsets, ct_off, inv, lat_p, h, o, zh,
       total;
 };
 
@@ -32,13 +32,9 @@ enum EpiMode : int {
 };
 
 struct GemmArgs {
-  int M;                  // dense: rows of A and of the output
-  int N;                  // output columns (per group), multiple of 32
+  int M;                  // rows of A and of the output
+  int N;                  // output columns
   int Kd;                 // reduction length, multiple of 64
-  int grouped;            // 0: dense; 1: one problem per expert segment
-  int E;                  // groups
-  const int32_t* seg_off; // [E+1] first row of each segment (grouped)
-  const int32_t* mt_off;  // [E+1] prefix sum of the segments' 128-row tile counts
   int epi;
   int split;
   __nv_bfloat16* out0;
@@ -56,6 +52,25 @@ struct GemmArgs {
                           // on, so every role runs into its bounded wait and aborts
 };
 
+// Routed-expert GEMMs (gemm_grouped.cu): out[tok, r] = act[tok, :] . W[e][r, :] for the
+// token rows of each expert segment, weight rows on the MMA's M side.
+struct GroupedArgs {
+  int E;                  // experts
+  int M_w;                // weight rows per expert (2I for gate/value, L for down)
+  int Kd;                 // reduction length (L for gate/value, I for down), multiple of 64
+  const int32_t* seg_off; // [E+1] first token row of each expert's segment
+  const int32_t* ct_off;  // [E+1] prefix sum of ceil(count / GROUPED_TOKN)
+  int epi;                // EPI_SITU (gate/value, M_w = 2I) or EPI_BF16
+  __nv_bfloat16* out;     // [rows, ldo] token-major output
+  int ldo;
+  float c;
+  uint32_t* err;
+  unsigned long long timeout_ns;
+};
+
+int launch_grouped_gemm(const void* W, int w_ld, const void* X, uint64_t x_rows, int x_ld,
+                        const GroupedArgs& g, cudaStream_t stream);
+
 // Encodes a 2-D bf16 row-major [rows, cols] (row stride ld elements) TMA map with a
 // 64 x box_rows box and the 128-byte swizzle.  Returns false on failure.
 bool make_tmap_bf16(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint64_t ld,
@@ -69,7 +84,7 @@ int launch_route(const float* logits, const float* tau, int T, int E, int K, int
 int launch_thresholds(const float* logits, int T, int E, int k, float* tau,
                       cudaStream_t stream);
 int launch_dispatch(const int32_t* idx, const __nv_bfloat16* lat, int T, int E, int K, int L,
-                    uint32_t* masks, uint32_t* base, int32_t* offsets, int32_t* mt_off,
+                    uint32_t* masks, uint32_t* base, int32_t* offsets, int32_t* ct_off,
                     int32_t* inv, __nv_bfloat16* lat_p, int32_t* counts_out, uint32_t* err,
                     cudaStream_t stream);
 int launch_combine(const __nv_bfloat16* o, const float* gate, const int32_t* inv,
