@@ -239,7 +239,7 @@ DESCRIPTIONS = {
 class Workload:
     """Inputs and routing arguments of one bench configuration."""
 
-    def __init__(self, name, dev, rank):
+    def __init__(self, name, dev, rank, overlap=False, shared_sms=0):
         self.name = name
         self.sh = sh = SHAPES[name]
         outliers = name in ("prefill", "small")
@@ -248,7 +248,8 @@ class Workload:
         self.x = synth.make_x(sh, SEED + 1000 * rank, device=dev,
                               outlier_frac=OUTLIER_FRAC if outliers else 0.0,
                               outlier_scale=OUTLIER_SCALE)
-        self.layer = lmoe.Layer(sh, self.w, max_tokens=max(sh.T, 8192 if name == "decode" else 0))
+        self.layer = lmoe.Layer(sh, self.w, max_tokens=max(sh.T, 8192 if name == "decode" else 0),
+                                overlap=overlap, shared_sms=shared_sms)
         self.kwargs = {}
         self.extra = {}
         if name == "decode":
@@ -280,7 +281,9 @@ class Workload:
                             f"(I_s={sh.Is}), routed I={sh.I}",
                 "shape": self.name, "tokens_per_gpu": sh.T, "global_tokens": sh.T * world,
                 "l2": "inputs larger than L2: the expert weights streamed per step exceed it",
-                "parallelism": f"replicas x{world}, independent batches"}
+                "parallelism": f"replicas x{world}, independent batches",
+                "shared_experts": "in line" if not self.layer.overlap else
+                                  f"second stream, {self.layer.shared_sms or 'default'} SMs"}
 
 
 def make_inputs(sh, dev, rank, outliers=True):
@@ -339,7 +342,7 @@ def run_ours(args):
     if not torch.cuda.is_available():
         raise RuntimeError("bench.py needs a CUDA GPU (the layer has no CPU path)")
     dev = torch.device("cuda", local)
-    wl = Workload(args.shape, dev, rank)
+    wl = Workload(args.shape, dev, rank, overlap=args.overlap, shared_sms=args.shared_sms)
     sh, layer, x, w = wl.sh, wl.layer, wl.x, wl.w
     y = torch.empty_like(x)
     stream = torch.cuda.current_stream()
@@ -478,6 +481,10 @@ def main():
     ap.add_argument("--cpu-tokens", type=int, default=128,
                     help="tokens in the timed CPU-oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--overlap", action="store_true",
+                    help="run the shared experts on a second stream beside the routed path")
+    ap.add_argument("--shared-sms", type=int, default=0,
+                    help="SMs for the shared experts when they overlap (0: library default)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
     return run_reference(args) if args.impl == "reference" else run_ours(args)

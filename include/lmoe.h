@@ -115,7 +115,17 @@ typedef struct lmoe_io {
                             event i is recorded on the stream before stage i, the last one
                             after the final stage (skipped stages record back to back) */
   int kernel_launches;   /* out: number of kernels this call launched */
+  void *aux_stream;      /* optional second cudaStream_t: with it (and T >= LMOE_OVERLAP_MIN_T)
+                            the shared experts run on it, on shared_sms SMs, while the routed
+                            path runs on `stream` on the others; `stream` waits for it before
+                            the output GEMM, so the call stays ordered on `stream` */
+  void *aux_events[2];   /* two cudaEvent_t handles (fork, join), required with aux_stream */
+  int shared_sms;        /* SMs for the shared experts while they overlap (0: a third) */
 } lmoe_io;
+
+/* Batches at least this large run the shared experts concurrently when lmoe_io.aux_stream is
+ * given; the workspace of such batches holds their fp32 output [T, d]. */
+#define LMOE_OVERLAP_MIN_T 512
 
 /* Bytes of the packed weight buffer for `dims` (0 if the dims are invalid). */
 size_t lmoe_packed_bytes(const lmoe_dims *dims);
@@ -196,7 +206,7 @@ int lmoe_gemm_bf16(const void *A, const void *B, float *C, int M, int N, int Kd,
  * process starts.  Arguments and results are those of lmoe_forward without the workspace.
  * Scratch: a LMOE_NOALLOC_SCRATCH_BYTES (24 MiB) array in the library's device image,
  * reserved on every GPU that loads the library until the process exits.  It covers a K3
- * decode batch of up to 92 tokens (64 tokens need 16.6 MiB).  When lmoe_workspace_bytes(dims)
+ * decode batch of up to 91 tokens (64 tokens need 16.8 MiB).  When lmoe_workspace_bytes(dims)
  * exceeds it, the call returns LMOE_ERR_WORKSPACE_TOO_SMALL and enqueues nothing.
  * Set-up: the first call on each device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call before any stream

@@ -66,6 +66,7 @@ WorkspaceLayout workspace_layout(const lmoe_dims& D) {
   W.err = take(256);
   W.lat = take(T * D.L * 2);
   W.logits = take(T * D.E * 4);
+  W.logits_t = take(T * D.E * 4);
   W.tau = take(static_cast<size_t>(D.E) * 4);
   W.idx = take(TK * 4);
   W.gate = take(TK * 4);
@@ -78,6 +79,8 @@ WorkspaceLayout workspace_layout(const lmoe_dims& D) {
   W.h = take(TK * D.I * 2);
   W.o = take(TK * D.L * 2);
   W.zh = take(T * (D.L + shared_width(D)) * 2);
+  // fp32 shared-expert output, used when the shared experts run beside the routed path
+  W.ys = take(D.T >= LMOE_OVERLAP_MIN_T && shared_width(D) > 0 ? T * D.d * 4 : 0);
   W.total = off;
   return W;
 }
@@ -170,7 +173,8 @@ int lmoe_thresholds(const float* logits, int T, int E, int K, int k_rank, float*
     const int64_t f = static_cast<int64_t>(T) * K / E;
     k = static_cast<int>(f < 1 ? 1 : (f > T ? T : f));
   }
-  return launch_thresholds(logits, T, E, k, tau, static_cast<cudaStream_t>(stream));
+  // token-major input: each expert's column is read with stride E
+  return launch_thresholds(logits, T, E, E, 1, k, tau, static_cast<cudaStream_t>(stream));
 }
 
 int lmoe_route(const float* logits, const float* tau, int T, int E, int K, int32_t* idx,
@@ -256,8 +260,30 @@ int lmoe_forward(const lmoe_dims* dims, const void* packed, const void* x, const
   if (cudaMemsetAsync(err, 0, sizeof(uint32_t), stream) != cudaSuccess) return LMOE_ERR_CUDA;
   if (!mark(LMOE_STAGE_LATENT_SHARED, 0)) return LMOE_ERR_CUDA;
 
-  // 1. x . [W_down ; W_shared_gate/value]^T: latent (bf16) and SiTU(shared) into zh[:, L:]
+  int dev_sms = 0;
   {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&dev_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return LMOE_ERR_CUDA;
+  }
+  // Overlap: the shared experts (pure tensor work) run on an auxiliary stream on
+  // `shared_ctas` SMs while the routed path (bandwidth-bound expert GEMMs) runs on the rest.
+  const bool overlap = opt.aux_stream != nullptr && opt.aux_events[0] != nullptr &&
+                       opt.aux_events[1] != nullptr && sw > 0 && T >= LMOE_OVERLAP_MIN_T;
+  cudaStream_t aux = static_cast<cudaStream_t>(opt.aux_stream);
+  int shared_ctas = 0, routed_ctas = 0;
+  float* ys = nullptr;
+  if (overlap) {
+    shared_ctas = opt.shared_sms > 0 ? opt.shared_sms : dev_sms / 3;
+    if (shared_ctas >= dev_sms) shared_ctas = dev_sms / 3;
+    if (shared_ctas < 1) shared_ctas = 1;
+    routed_ctas = dev_sms - shared_ctas;
+    ys = reinterpret_cast<float*>(ws + W.ys);
+  }
+
+  if (!overlap) {
+    // 1. x . [W_down ; W_shared_gate/value]^T: latent (bf16) and SiTU(shared) into zh[:, L:]
     GemmArgs g = gemm_defaults(err, D.c);
     g.M = T;
     g.N = D.L + 2 * sw;
@@ -271,10 +297,63 @@ int lmoe_forward(const lmoe_dims* dims, const void* packed, const void* x, const
     g.inject_stall = inject_stall() ? 1 : 0;
     rc = launch_gemm(x, T, D.d, pk + P.w1, static_cast<uint64_t>(g.N), D.d, g, stream);
     if (rc != LMOE_OK) return rc;
+    launches += 1;
+  } else {
+    cudaEvent_t ev_fork = static_cast<cudaEvent_t>(opt.aux_events[0]);
+    cudaEvent_t ev_join = static_cast<cudaEvent_t>(opt.aux_events[1]);
+    if (cudaEventRecord(ev_fork, stream) != cudaSuccess ||
+        cudaStreamWaitEvent(aux, ev_fork, 0) != cudaSuccess)
+      return LMOE_ERR_CUDA;
+    // aux 1: hs = SiTU(x . W_shared_gate/value^T) -> zh[:, L:]
+    {
+      GemmArgs g = gemm_defaults(err, D.c);
+      g.M = T;
+      g.N = 2 * sw;
+      g.Kd = D.d;
+      g.epi = EPI_SITU;
+      g.out1 = zh + D.L;
+      g.ld1 = ldz;
+      g.max_ctas = shared_ctas;
+      rc = launch_gemm(x, T, D.d, pk + P.w1 + static_cast<size_t>(D.L) * D.d * 2,
+                       static_cast<uint64_t>(2 * sw), D.d, g, aux);
+      if (rc != LMOE_OK) return rc;
+    }
+    // aux 2: ys = hs . W_shared_down^T (fp32)
+    {
+      GemmArgs g = gemm_defaults(err, D.c);
+      g.M = T;
+      g.N = D.d;
+      g.Kd = sw;
+      g.epi = EPI_F32;
+      g.outf = ys;
+      g.ldf = D.d;
+      g.max_ctas = shared_ctas;
+      rc = launch_gemm(zh + D.L, T, ldz, pk + P.w2 + static_cast<size_t>(D.L) * 2,
+                       static_cast<uint64_t>(D.d), ldz, g, aux);
+      if (rc != LMOE_OK) return rc;
+    }
+    if (cudaEventRecord(ev_join, aux) != cudaSuccess) return LMOE_ERR_CUDA;
+    // main 1: lat = x . W_down^T
+    {
+      GemmArgs g = gemm_defaults(err, D.c);
+      g.M = T;
+      g.N = D.L;
+      g.Kd = D.d;
+      g.epi = EPI_BF16;
+      g.out0 = lat;
+      g.ld0 = D.L;
+      g.max_ctas = routed_ctas;
+      g.inject_stall = inject_stall() ? 1 : 0;
+      rc = launch_gemm(x, T, D.d, pk + P.w1, static_cast<uint64_t>(D.L), D.d, g, stream);
+      if (rc != LMOE_OK) return rc;
+    }
+    launches += 3;
   }
-  if (!mark(LMOE_STAGE_ROUTER, 1)) return LMOE_ERR_CUDA;
+  if (!mark(LMOE_STAGE_ROUTER, 0)) return LMOE_ERR_CUDA;
   // 2. router logits = lat . W_r^T (fp32), unless the caller supplies them
   const float* logits = opt.logits_in;
+  float* logits_t = reinterpret_cast<float*>(ws + W.logits_t);  // expert-major copy
+  const bool solve_tau = !opt.tau_in && opt.balance;
   if (!logits) {
     GemmArgs g = gemm_defaults(err, D.c);
     g.M = T;
@@ -283,19 +362,28 @@ int lmoe_forward(const lmoe_dims* dims, const void* packed, const void* x, const
     g.epi = EPI_F32;
     g.outf = reinterpret_cast<float*>(ws + W.logits);
     g.ldf = D.E;
+    g.max_ctas = routed_ctas;
+    if (solve_tau) {
+      g.outf_t = logits_t;
+      g.ldt = T;
+    }
     rc = launch_gemm(lat, T, D.L, pk + P.wr, static_cast<uint64_t>(D.E), D.L, g, stream);
     if (rc != LMOE_OK) return rc;
     logits = g.outf;
+    launches += 1;
+  } else if (solve_tau) {
+    rc = launch_transpose_f32(logits, T, D.E, logits_t, stream);
+    if (rc != LMOE_OK) return rc;
     launches += 1;
   }
   if (!mark(LMOE_STAGE_THRESHOLDS, 0)) return LMOE_ERR_CUDA;
   // 3. thresholds
   const float* tau = opt.tau_in;
-  if (!tau && opt.balance) {
+  if (solve_tau) {
     float* t = reinterpret_cast<float*>(ws + W.tau);
     const int64_t f = static_cast<int64_t>(T) * D.K / D.E;
     const int k = static_cast<int>(f < 1 ? 1 : (f > T ? T : f));
-    rc = launch_thresholds(logits, T, D.E, k, t, stream);
+    rc = launch_thresholds(logits_t, T, D.E, 1, T, k, t, stream);
     if (rc != LMOE_OK) return rc;
     tau = t;
     launches += 1;
@@ -332,6 +420,7 @@ int lmoe_forward(const lmoe_dims* dims, const void* packed, const void* x, const
     g.c = D.c;
     g.err = err;
     g.timeout_ns = wait_limit_ns();
+    g.max_ctas = routed_ctas;
     rc = launch_grouped_gemm(pk + P.wgu, D.L, lat_p, static_cast<uint64_t>(TK), D.L, g, stream);
     if (rc != LMOE_OK) return rc;
   }
@@ -351,6 +440,7 @@ int lmoe_forward(const lmoe_dims* dims, const void* packed, const void* x, const
     g.c = D.c;
     g.err = err;
     g.timeout_ns = wait_limit_ns();
+    g.max_ctas = routed_ctas;
     rc = launch_grouped_gemm(pk + P.wed, D.I, h, static_cast<uint64_t>(TK), D.I, g, stream);
     if (rc != LMOE_OK) return rc;
   }
@@ -360,18 +450,28 @@ int lmoe_forward(const lmoe_dims* dims, const void* packed, const void* x, const
                       D.eps, zh, ldz, stream);
   if (rc != LMOE_OK) return rc;
   if (!mark(LMOE_STAGE_OUTPUT, 1)) return LMOE_ERR_CUDA;
-  // 9. y = residual + [z | hs] . [W_up | W_sd]^T
+  // 9. y = residual + [z | hs] . [W_up | W_sd]^T   (overlap: y = residual + z . W_up^T + ys)
   {
     GemmArgs g = gemm_defaults(err, D.c);
     g.M = T;
     g.N = D.d;
-    g.Kd = ldz;
     g.epi = EPI_RESID;
     g.out0 = static_cast<bf*>(y);
     g.ld0 = D.d;
     g.resid = static_cast<const bf*>(residual);
     g.ldr = D.d;
-    rc = launch_gemm(zh, T, ldz, pk + P.w2, static_cast<uint64_t>(D.d), ldz, g, stream);
+    if (!overlap) {
+      g.Kd = ldz;
+      rc = launch_gemm(zh, T, ldz, pk + P.w2, static_cast<uint64_t>(D.d), ldz, g, stream);
+    } else {
+      if (cudaStreamWaitEvent(stream, static_cast<cudaEvent_t>(opt.aux_events[1]), 0) !=
+          cudaSuccess)
+        return LMOE_ERR_CUDA;
+      g.Kd = D.L;
+      g.addf = ys;
+      g.lda = D.d;
+      rc = launch_gemm(zh, T, ldz, pk + P.w2, static_cast<uint64_t>(D.d), ldz, g, stream);
+    }
     if (rc != LMOE_OK) return rc;
   }
   if (!mark(LMOE_NUM_STAGES, 1)) return LMOE_ERR_CUDA;

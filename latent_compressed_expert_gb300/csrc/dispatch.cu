@@ -135,40 +135,48 @@ dispatch_scan_kernel(const uint32_t* __restrict__ masks, int nb, int E, int TK,
 }
 
 // Scatter + gather: inv[t*K + j] = row of (t, j) in the permuted order, and
-// lat_p[row, :] = lat[t, :].  One CTA per block of 32 tokens; a warp copies one row.
+// lat_p[row, :] = lat[t, :].  One warp per (token, slot) pair; each lane keeps up to eight
+// 16-byte loads in flight before their stores.
 __global__ void __launch_bounds__(256)
 dispatch_scatter_kernel(const int32_t* __restrict__ idx, const uint32_t* __restrict__ masks,
                         const uint32_t* __restrict__ base, const int32_t* __restrict__ offsets,
                         const __nv_bfloat16* __restrict__ lat, int T, int E, int K, int L,
                         int32_t* __restrict__ inv, __nv_bfloat16* __restrict__ lat_p) {
-  const int b = blockIdx.x;
-  const int t0 = b * DISPATCH_TOKENS;
-  const int ntok = min(DISPATCH_TOKENS, T - t0);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nwarps = blockDim.x >> 5;
-  const int vec_per_row = L / 8;  // 16-byte vectors
-  for (int p = warp; p < ntok * K; p += nwarps) {
-    const int tl = p / K;
-    const int t = t0 + tl;
-    const int e = __ldg(idx + static_cast<size_t>(t0) * K + p);
-    if (e < 0 || e >= E) continue;  // flagged by the mask kernel
-    const size_t me = static_cast<size_t>(b) * E + e;
-    const int row = __ldg(offsets + e) + static_cast<int>(__ldg(base + me)) +
-                    __popc(__ldg(masks + me) & ((1u << tl) - 1u));
-    if (lane == 0) inv[static_cast<size_t>(t0) * K + p] = row;
-    const uint4* src = reinterpret_cast<const uint4*>(lat + static_cast<size_t>(t) * L);
-    uint4* dst = reinterpret_cast<uint4*>(lat_p + static_cast<size_t>(row) * L);
-    for (int v = lane; v < vec_per_row; v += 32) dst[v] = __ldg(src + v);
+  const int lane = threadIdx.x & 31;
+  const int64_t p = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  if (p >= static_cast<int64_t>(T) * K) return;
+  const int t = static_cast<int>(p / K);
+  const int b = t / DISPATCH_TOKENS, tl = t % DISPATCH_TOKENS;
+  const int e = __ldg(idx + p);
+  if (e < 0 || e >= E) return;  // flagged by the mask kernel
+  const size_t me = static_cast<size_t>(b) * E + e;
+  const int row = __ldg(offsets + e) + static_cast<int>(__ldg(base + me)) +
+                  __popc(__ldg(masks + me) & ((1u << tl) - 1u));
+  if (lane == 0) inv[p] = row;
+  const uint4* src = reinterpret_cast<const uint4*>(lat + static_cast<size_t>(t) * L);
+  uint4* dst = reinterpret_cast<uint4*>(lat_p + static_cast<size_t>(row) * L);
+  const int nvec = L / 8;
+  constexpr int B = 8;
+  for (int v0 = lane; v0 < nvec; v0 += B * 32) {
+    uint4 r[B];
+#pragma unroll
+    for (int i = 0; i < B; ++i)
+      if (v0 + i * 32 < nvec) r[i] = __ldg(src + v0 + i * 32);
+#pragma unroll
+    for (int i = 0; i < B; ++i)
+      if (v0 + i * 32 < nvec) dst[v0 + i * 32] = r[i];
   }
 }
 
 // Combine + RMSNorm: one CTA per token, each thread owns 8 consecutive latent features
-// (a 16-byte vector) for up to COMBINE_MAX_VEC vectors.  u accumulates the K expert rows in
+// (a 16-byte vector), for up to COMBINE_MAX_VEC vectors (L <= 16384).  u accumulates the K expert rows in
 // fp32 in slot order; the sum of squares is reduced in a fixed tree, so the result does not
 // depend on scheduling.
-constexpr int COMBINE_MAX_VEC = 2;
+constexpr int COMBINE_MAX_VEC = 4;
+constexpr int COMBINE_MAX_THREADS = 512;
+constexpr int COMBINE_BATCH = 4;  // row loads issued together
 
-__global__ void __launch_bounds__(1024)
+__global__ void __launch_bounds__(COMBINE_MAX_THREADS)
 combine_rmsnorm_kernel(const __nv_bfloat16* __restrict__ o, const float* __restrict__ gate,
                        const int32_t* __restrict__ inv, const float* __restrict__ gamma,
                        int T, int K, int L, float eps, __nv_bfloat16* __restrict__ z,
@@ -191,16 +199,25 @@ combine_rmsnorm_kernel(const __nv_bfloat16* __restrict__ o, const float* __restr
 #pragma unroll
     for (int i = 0; i < 8; ++i) u[c][i] = 0.0f;
     if (v < nvec) {
-      for (int j = 0; j < K; ++j) {
-        const uint4 raw =
-            __ldg(reinterpret_cast<const uint4*>(o + static_cast<size_t>(rows[j]) * L) + v);
-        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
-        const float g = gates[j];
+      // the loads of COMBINE_BATCH rows are issued before their sums, in slot order
+      for (int j0 = 0; j0 < K; j0 += COMBINE_BATCH) {
+        uint4 raw[COMBINE_BATCH];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float2 f = __bfloat1622float2(h[i]);
-          u[c][2 * i] = fmaf(g, f.x, u[c][2 * i]);
-          u[c][2 * i + 1] = fmaf(g, f.y, u[c][2 * i + 1]);
+        for (int jj = 0; jj < COMBINE_BATCH; ++jj)
+          if (j0 + jj < K)
+            raw[jj] = __ldg(reinterpret_cast<const uint4*>(o + static_cast<size_t>(rows[j0 + jj]) * L) + v);
+#pragma unroll
+        for (int jj = 0; jj < COMBINE_BATCH; ++jj) {
+          if (j0 + jj < K) {
+            const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw[jj]);
+            const float g = gates[j0 + jj];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const float2 f = __bfloat1622float2(h[i]);
+              u[c][2 * i] = fmaf(g, f.x, u[c][2 * i]);
+              u[c][2 * i + 1] = fmaf(g, f.y, u[c][2 * i + 1]);
+            }
+          }
         }
       }
 #pragma unroll
@@ -252,8 +269,9 @@ int launch_dispatch(const int32_t* idx, const __nv_bfloat16* lat, int T, int E, 
                                                counts_out);
   if (cudaGetLastError() != cudaSuccess) return LMOE_ERR_CUDA;
   if (nb > 0) {
-    dispatch_scatter_kernel<<<nb, 256, 0, stream>>>(idx, masks, base, offsets, lat, T, E, K, L,
-                                                    inv, lat_p);
+    const int64_t warps = static_cast<int64_t>(T) * K;
+    dispatch_scatter_kernel<<<static_cast<unsigned>(ceil_div(warps, 8)), 256, 0, stream>>>(
+        idx, masks, base, offsets, lat, T, E, K, L, inv, lat_p);
     if (cudaGetLastError() != cudaSuccess) return LMOE_ERR_CUDA;
   }
   return LMOE_OK;
@@ -264,7 +282,8 @@ int launch_combine(const __nv_bfloat16* o, const float* gate, const int32_t* inv
                    int ldz, cudaStream_t stream) {
   if (T == 0) return LMOE_OK;
   const int nvec = L / 8;
-  const int threads = static_cast<int>(ceil_div(nvec < 1024 ? nvec : 1024, 32) * 32);
+  const int threads = static_cast<int>(
+      ceil_div(nvec < COMBINE_MAX_THREADS ? nvec : COMBINE_MAX_THREADS, 32) * 32);
   if (nvec > COMBINE_MAX_VEC * threads) return LMOE_ERR_UNSUPPORTED;
   combine_rmsnorm_kernel<<<T, threads, 0, stream>>>(o, gate, inv, gamma, T, K, L, eps, z, ldz);
   return cudaGetLastError() == cudaSuccess ? LMOE_OK : LMOE_ERR_CUDA;

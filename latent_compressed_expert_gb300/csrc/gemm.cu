@@ -136,6 +136,10 @@ __device__ __forceinline__ void epilogue_store(const GemmArgs& g, int row, int c
 #pragma unroll
       for (int q = 0; q < 8; ++q)
         o[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+      if (g.outf_t) {  // a warp's 32 rows are consecutive: 128-byte runs per column
+#pragma unroll
+        for (int i = 0; i < 32; ++i) g.outf_t[static_cast<size_t>(col0 + i) * g.ldt + r] = v[i];
+      }
       break;
     }
     case EPI_SITU:
@@ -149,6 +153,17 @@ __device__ __forceinline__ void epilogue_store(const GemmArgs& g, int row, int c
       break;
     case EPI_RESID:
     default: {
+      if (g.addf) {
+        const float4* ap = reinterpret_cast<const float4*>(g.addf + r * g.lda + col0);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const float4 a = __ldg(ap + q);
+          v[4 * q] += a.x;
+          v[4 * q + 1] += a.y;
+          v[4 * q + 2] += a.z;
+          v[4 * q + 3] += a.w;
+        }
+      }
       if (g.resid) {
         const uint4* rp = reinterpret_cast<const uint4*>(g.resid + r * g.ldr + col0);
 #pragma unroll
@@ -179,11 +194,14 @@ __device__ __forceinline__ void epilogue_store_partial(const GemmArgs& g, int ro
     const int col = col0 + i;
     if (g.epi == EPI_F32) {
       g.outf[r * g.ldf + col] = v[i];
+      if (g.outf_t) g.outf_t[static_cast<size_t>(col) * g.ldt + r] = v[i];
     } else if (g.epi == EPI_BF16) {
       g.out0[r * g.ld0 + col] = __float2bfloat16_rn(v[i]);
     } else if (g.epi == EPI_RESID) {
-      const float rv = g.resid ? __bfloat162float(g.resid[r * g.ldr + col]) : 0.0f;
-      g.out0[r * g.ld0 + col] = __float2bfloat16_rn(v[i] + rv);
+      float t = v[i];
+      if (g.addf) t += g.addf[r * g.lda + col];
+      if (g.resid) t += __bfloat162float(g.resid[r * g.ldr + col]);
+      g.out0[r * g.ld0 + col] = __float2bfloat16_rn(t);
     }
   }
 }
@@ -404,7 +422,7 @@ static int launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArg
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return LMOE_ERR_CUDA;
-  int grid = sms;
+  int grid = (g.max_ctas > 0 && g.max_ctas < sms) ? g.max_ctas : sms;
   const int64_t tiles = ceil_div(g.M, BLOCK_M) * ceil_div(g.N, BN);
   if (tiles < grid) grid = static_cast<int>(tiles);
   if (grid <= 0) return LMOE_OK;

@@ -175,6 +175,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
                              t.tok0 + b * C::BOX_T);
         }
       }
+      // every issued copy must land before the CTA may exit
       const uint32_t first = it > static_cast<uint32_t>(C::STAGES) ? it - C::STAGES : 0u;
       for (uint32_t j = first; j < it; ++j) {
         if (!gwait_drain(&full[j % C::STAGES], (j / C::STAGES) & 1u, limit)) {
@@ -298,7 +299,8 @@ int launch_grouped_gemm(const void* W, int w_ld, const void* X, uint64_t x_rows,
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return LMOE_ERR_CUDA;
-  grouped_gemm_kernel<<<sms, GROUPED_THREADS, C::SMEM_BYTES, stream>>>(tw, tx, g);
+  const int grid = (g.max_ctas > 0 && g.max_ctas < sms) ? g.max_ctas : sms;
+  grouped_gemm_kernel<<<grid, GROUPED_THREADS, C::SMEM_BYTES, stream>>>(tw, tx, g);
   return cudaGetLastError() == cudaSuccess ? LMOE_OK : LMOE_ERR_CUDA;
 }
 

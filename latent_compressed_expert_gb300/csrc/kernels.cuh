@@ -15,8 +15,8 @@ struct PackedLayout {
 
 // Offsets (bytes) of the forward workspace; every buffer 256-aligned.
 struct WorkspaceLayout {
-  size_t err, lat, logits, tau, idx, gate, masks, base, offsets, ct_off, inv, lat_p, h, o, zh,
-      total;
+  size_t err, lat, logits, logits_t, tau, idx, gate, masks, base, offsets, ct_off, inv, lat_p,
+      h, o, zh, ys, total;
 };
 
 PackedLayout packed_layout(const lmoe_dims& D);
@@ -43,8 +43,13 @@ struct GemmArgs {
   int ld1;
   float* outf;
   int ldf;
+  float* outf_t;          // EPI_F32: optional transposed copy, outf_t[c * ldt + r]
+  int ldt;
   const __nv_bfloat16* resid;
   int ldr;
+  const float* addf;      // EPI_RESID: optional fp32 addend addf[r * lda + c]
+  int lda;
+  int max_ctas;           // persistent grid limit (0: one CTA per SM)
   float c;                // SiTU cap
   uint32_t* err;          // device error flag (never null)
   unsigned long long timeout_ns;
@@ -66,6 +71,7 @@ struct GroupedArgs {
   float c;
   uint32_t* err;
   unsigned long long timeout_ns;
+  int max_ctas;           // persistent grid limit (0: one CTA per SM)
 };
 
 int launch_grouped_gemm(const void* W, int w_ld, const void* X, uint64_t x_rows, int x_ld,
@@ -81,8 +87,12 @@ int launch_gemm(const void* A, uint64_t a_rows, int a_ld, const void* B, uint64_
 
 int launch_route(const float* logits, const float* tau, int T, int E, int K, int32_t* idx,
                  float* gate, float* scores_out, cudaStream_t stream);
-int launch_thresholds(const float* logits, int T, int E, int k, float* tau,
-                      cudaStream_t stream);
+// Thresholds from logits stored with element (t, e) at z[t * stride_t + e * stride_e]
+// (stride_t = 1, stride_e = T is the fast, expert-major layout).
+int launch_thresholds(const float* z, int T, int E, int64_t stride_t, int64_t stride_e, int k,
+                      float* tau, cudaStream_t stream);
+// out[E, T] = in[T, E]^T (fp32).
+int launch_transpose_f32(const float* in, int T, int E, float* out, cudaStream_t stream);
 int launch_dispatch(const int32_t* idx, const __nv_bfloat16* lat, int T, int E, int K, int L,
                     uint32_t* masks, uint32_t* base, int32_t* offsets, int32_t* ct_off,
                     int32_t* inv, __nv_bfloat16* lat_p, int32_t* counts_out, uint32_t* err,

@@ -58,8 +58,9 @@ __device__ __forceinline__ uint32_t order_key(float a) {
 // ------------------------------------------------------------------------------------
 // Top-K routing: one warp per token.  The warp writes the token's keys a = fl32(s - tau)
 // into shared memory, then K times takes the largest remaining key (ties to the lower
-// expert id) with two warp reductions.  Each lane keeps its own best candidate and only
-// the lane that lost its candidate rescans its share of the experts.
+// expert id) with two warp reductions.  Each lane keeps its best and second-best candidate,
+// so a lane whose best is taken promotes its runner-up and only rescans its share of the
+// experts when it loses a second time.
 // ------------------------------------------------------------------------------------
 constexpr int ROUTE_WARPS = 4;
 
@@ -74,38 +75,67 @@ route_kernel(const float* __restrict__ logits, const float* __restrict__ tau, in
   if (t >= T) return;
   const float* zrow = logits + static_cast<size_t>(t) * E;
 
-  for (int e = lane; e < E; e += 32) {
-    const float s = score_sigmoid(__ldg(zrow + e));
-    if (scores_out) scores_out[static_cast<size_t>(t) * E + e] = s;
-    const float a = tau ? __fsub_rn(s, __ldg(tau + e)) : s;
-    keys[e] = order_key(a);
+  // eight independent logit loads in flight per lane before their keys are computed
+  constexpr int B = 8;
+  for (int e0 = lane; e0 < E; e0 += B * 32) {
+    float zv[B], tv[B];
+#pragma unroll
+    for (int i = 0; i < B; ++i) {
+      const int e = e0 + i * 32;
+      zv[i] = e < E ? __ldg(zrow + e) : 0.0f;
+      tv[i] = (tau && e < E) ? __ldg(tau + e) : 0.0f;
+    }
+#pragma unroll
+    for (int i = 0; i < B; ++i) {
+      const int e = e0 + i * 32;
+      if (e < E) {
+        const float s = score_sigmoid(zv[i]);
+        if (scores_out) scores_out[static_cast<size_t>(t) * E + e] = s;
+        const float a = tau ? __fsub_rn(s, tv[i]) : s;
+        keys[e] = order_key(a);
+      }
+    }
   }
   __syncwarp();
 
-  // lane-local best among e = lane, lane + 32, ...
-  auto lane_best = [&](uint32_t& bk, int& be) {
-    bk = 0u;
-    be = 0x7fffffff;
+  // best (b1) and runner-up (b2) among e = lane, lane + 32, ...; key 0 = none.  The scan is
+  // ascending in e and replaces only on a strictly larger key, so equal keys keep the lower e.
+  uint32_t b1k = 0u, b2k = 0u;
+  int b1e = 0x7fffffff, b2e = 0x7fffffff;
+  auto rescan = [&]() {
+    b1k = 0u;
+    b2k = 0u;
+    b1e = b2e = 0x7fffffff;
     for (int e = lane; e < E; e += 32) {
       const uint32_t k = keys[e];
-      if (k > bk) {  // strictly greater keeps the lower e on ties (ascending scan)
-        bk = k;
-        be = e;
+      if (k > b1k) {
+        b2k = b1k;
+        b2e = b1e;
+        b1k = k;
+        b1e = e;
+      } else if (k > b2k) {
+        b2k = k;
+        b2e = e;
       }
     }
   };
-  uint32_t bk;
-  int be;
-  lane_best(bk, be);
+  rescan();
   int my_idx = 0;  // lane j keeps the j-th winner
   for (int j = 0; j < K; ++j) {
-    const uint32_t mk = __reduce_max_sync(0xffffffffu, bk);
+    const uint32_t mk = __reduce_max_sync(0xffffffffu, b1k);
     const int we = static_cast<int>(
-        __reduce_min_sync(0xffffffffu, bk == mk ? static_cast<uint32_t>(be) : 0xffffffffu));
+        __reduce_min_sync(0xffffffffu, b1k == mk ? static_cast<uint32_t>(b1e) : 0xffffffffu));
     if (lane == j) my_idx = we;
     if (lane == (we & 31)) {
       keys[we] = 0u;  // below every real key
-      lane_best(bk, be);
+      if (b2k != 0u) {
+        b1k = b2k;
+        b1e = b2e;
+        b2k = 0u;  // runner-up unknown now: rescan if this lane wins again
+        b2e = 0x7fffffff;
+      } else {
+        rescan();
+      }
     }
     __syncwarp();
   }
@@ -120,48 +150,79 @@ route_kernel(const float* __restrict__ logits, const float* __restrict__ tau, in
 }
 
 // ------------------------------------------------------------------------------------
-// Quantile-Balancing thresholds: one CTA per expert column.  The scores of the column
-// (non-negative, so their fp32 bit patterns are ordered like their values) are staged in
-// shared memory when they fit, then the k-th largest is found by a three-pass radix
-// select over bits [31:21], [20:10], [9:0] with shared-memory histograms.
+// Quantile-Balancing thresholds: one CTA per expert.  The scores of the expert's column
+// (non-negative, so their fp32 bit patterns order like their values, and below 2^30) are
+// staged in shared memory when they fit; the k-th largest is then found by a radix select
+// over bits [29:18], [17:9], [8:0].  After a pass whose selected bin holds at most
+// TH_CAND keys, those keys are compacted and the remaining passes read only them (for the
+// fair-share rank that is ~2 % of the column).  Histograms use shared-memory atomics.
 // ------------------------------------------------------------------------------------
-constexpr int TH_THREADS = 512;
-constexpr int TH_BINS = 2048;
+constexpr int TH_THREADS = 256;
+constexpr int TH_BINS = 4096;
+constexpr int TH_CAND = 4096;
 constexpr int TH_SMEM_MAX_T = 32768;
 
 __global__ void __launch_bounds__(TH_THREADS)
-thresholds_kernel(const float* __restrict__ logits, int T, int E, int k,
-                  float* __restrict__ tau) {
+thresholds_kernel(const float* __restrict__ z, int T, int64_t stride_t, int64_t stride_e,
+                  int k, float* __restrict__ tau) {
   extern __shared__ uint32_t th_smem[];
-  uint32_t* hist = th_smem;                  // [TH_BINS]
-  uint32_t* ctl = th_smem + TH_BINS;         // [0] = digit, [1] = new k
-  uint32_t* vals = th_smem + TH_BINS + 32;   // [T] when staged
+  uint32_t* hist = th_smem;                       // [TH_BINS]
+  uint32_t* ctl = th_smem + TH_BINS;              // [0] digit, [1] new k, [2] candidates
+  uint32_t* cand = th_smem + TH_BINS + 32;        // [TH_CAND]
+  uint32_t* vals = cand + TH_CAND;                // [T] when staged
   const int e = blockIdx.x;
+  const int lane = threadIdx.x & 31;
+  const float* col = z + static_cast<int64_t>(e) * stride_e;
   const bool staged = T <= TH_SMEM_MAX_T;
   if (staged) {
-    for (int t = threadIdx.x; t < T; t += TH_THREADS)
-      vals[t] = __float_as_uint(score_sigmoid(__ldg(logits + static_cast<size_t>(t) * E + e)));
+    // eight independent loads in flight per thread before their scores are computed
+    constexpr int B = 8;
+    for (int t0 = threadIdx.x; t0 < T; t0 += B * TH_THREADS) {
+      float zv[B];
+#pragma unroll
+      for (int i = 0; i < B; ++i) {
+        const int t = t0 + i * TH_THREADS;
+        zv[i] = t < T ? __ldg(col + t * stride_t) : 0.0f;
+      }
+#pragma unroll
+      for (int i = 0; i < B; ++i) {
+        const int t = t0 + i * TH_THREADS;
+        if (t < T) vals[t] = __float_as_uint(score_sigmoid(zv[i]));
+      }
+    }
   }
+  // source of the keys: the full column (staged or re-read), or the compacted candidates
+  bool from_cand = false;
+  int n = T;
+  auto key_at = [&](int i) -> uint32_t {
+    if (from_cand) return cand[i];
+    return staged ? vals[i] : __float_as_uint(score_sigmoid(__ldg(col + i * stride_t)));
+  };
   uint32_t prefix = 0u, mask = 0u;
   int krem = k;
-#pragma unroll
+#pragma unroll 1
   for (int pass = 0; pass < 3; ++pass) {
-    const int sh = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
-    const uint32_t dm = pass == 2 ? 0x3FFu : 0x7FFu;
-    for (int b = threadIdx.x; b < TH_BINS; b += TH_THREADS) hist[b] = 0u;
+    const int sh = pass == 0 ? 18 : (pass == 1 ? 9 : 0);
+    const uint32_t dm = pass == 0 ? 0xFFFu : 0x1FFu;
+    const int nbins = static_cast<int>(dm) + 1;
+    for (int b = threadIdx.x; b < nbins; b += TH_THREADS) hist[b] = 0u;
     __syncthreads();
-    for (int t = threadIdx.x; t < T; t += TH_THREADS) {
-      const uint32_t key =
-          staged ? vals[t]
-                 : __float_as_uint(score_sigmoid(__ldg(logits + static_cast<size_t>(t) * E + e)));
-      if ((key & mask) == prefix) atomicAdd(&hist[(key >> sh) & dm], 1u);
+    const int n_round = (n + 31) & ~31;  // whole warps iterate together
+    for (int i = threadIdx.x; i < n_round; i += TH_THREADS) {
+      uint32_t key = 0u;
+      bool in = false;
+      if (i < n) {
+        key = key_at(i);
+        in = (key & mask) == prefix;
+      }
+      if (in) atomicAdd(&hist[(key >> sh) & dm], 1u);
     }
     __syncthreads();
     if (threadIdx.x < 32) {
-      // lane l owns bins [64 l, 64 l + 64); count of keys in bins above lane l's range
-      const int lane = threadIdx.x;
-      uint32_t mine = 0u;
-      for (int b = 0; b < 64; ++b) mine += hist[lane * 64 + b];
+      // lane l owns bins [per l, per l + per); counts of the bins above its range
+      const int per = nbins / 32;
+      uint32_t mine = 0u;  // each lane starts at a different bank
+      for (int b = 0; b < per; ++b) mine += hist[lane * per + ((b + lane) & (per - 1))];
       uint32_t incl = mine;  // inclusive suffix sum over lanes >= lane
       for (int o = 1; o < 32; o <<= 1) {
         const uint32_t v = __shfl_down_sync(0xffffffffu, incl, o);
@@ -170,11 +231,12 @@ thresholds_kernel(const float* __restrict__ logits, int T, int E, int k,
       const uint32_t above = incl - mine;
       if (above < static_cast<uint32_t>(krem) && static_cast<uint32_t>(krem) <= incl) {
         uint32_t cum = above;
-        for (int b = 63; b >= 0; --b) {
-          const uint32_t h = hist[lane * 64 + b];
+        for (int b = per - 1; b >= 0; --b) {
+          const uint32_t h = hist[lane * per + b];
           if (cum + h >= static_cast<uint32_t>(krem)) {
-            ctl[0] = static_cast<uint32_t>(lane * 64 + b);
+            ctl[0] = static_cast<uint32_t>(lane * per + b);
             ctl[1] = static_cast<uint32_t>(krem) - cum;
+            ctl[2] = h;
             break;
           }
           cum += h;
@@ -182,12 +244,52 @@ thresholds_kernel(const float* __restrict__ logits, int T, int E, int k,
       }
     }
     __syncthreads();
-    prefix |= ctl[0] << sh;
+    const uint32_t digit = ctl[0];
+    const uint32_t in_bin = ctl[2];
+    prefix |= digit << sh;
     mask |= dm << sh;
     krem = static_cast<int>(ctl[1]);
+    if (pass < 2 && !from_cand && in_bin <= static_cast<uint32_t>(TH_CAND)) {
+      // compact the keys of the selected bin (warp-aggregated appends)
+      if (threadIdx.x == 0) ctl[3] = 0u;
+      __syncthreads();
+      for (int i = threadIdx.x; i < n_round; i += TH_THREADS) {
+        uint32_t key = 0u;
+        bool in = false;
+        if (i < n) {
+          key = key_at(i);
+          in = (key & mask) == prefix;
+        }
+        const uint32_t bal = __ballot_sync(0xffffffffu, in);
+        uint32_t base = 0u;
+        if (lane == 0 && bal) base = atomicAdd(&ctl[3], static_cast<uint32_t>(__popc(bal)));
+        base = __shfl_sync(0xffffffffu, base, 0);
+        if (in) cand[base + __popc(bal & ((1u << lane) - 1u))] = key;
+      }
+      __syncthreads();
+      from_cand = true;
+      n = static_cast<int>(ctl[3]);
+    }
     __syncthreads();
   }
   if (threadIdx.x == 0) tau[e] = __uint_as_float(prefix);
+}
+
+// out[E, T] = in[T, E]^T through 32 x 32 shared-memory tiles.
+__global__ void __launch_bounds__(256)
+transpose_f32_kernel(const float* __restrict__ in, int T, int E, float* __restrict__ out) {
+  __shared__ float tile[32][33];
+  const int e0 = blockIdx.x * 32, t0 = blockIdx.y * 32;
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8
+  for (int i = ty; i < 32; i += 8) {
+    const int t = t0 + i, e = e0 + tx;
+    if (t < T && e < E) tile[i][tx] = __ldg(in + static_cast<size_t>(t) * E + e);
+  }
+  __syncthreads();
+  for (int i = ty; i < 32; i += 8) {
+    const int e = e0 + i, t = t0 + tx;
+    if (t < T && e < E) out[static_cast<size_t>(e) * T + t] = tile[tx][i];
+  }
 }
 
 // ------------------------------------------------------------------------------------
@@ -208,16 +310,24 @@ int launch_route(const float* logits, const float* tau, int T, int E, int K, int
   return cudaGetLastError() == cudaSuccess ? LMOE_OK : LMOE_ERR_CUDA;
 }
 
-int launch_thresholds(const float* logits, int T, int E, int k, float* tau,
-                      cudaStream_t stream) {
+int launch_thresholds(const float* z, int T, int E, int64_t stride_t, int64_t stride_e, int k,
+                      float* tau, cudaStream_t stream) {
   if (T == 0) return LMOE_OK;
-  const size_t smem = (TH_BINS + 32 + (T <= TH_SMEM_MAX_T ? T : 0)) * sizeof(uint32_t);
+  const size_t smem =
+      (TH_BINS + 32 + TH_CAND + (T <= TH_SMEM_MAX_T ? T : 0)) * sizeof(uint32_t);
   if (smem > 48 * 1024) {
     if (cudaFuncSetAttribute(thresholds_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
       return LMOE_ERR_CUDA;
   }
-  thresholds_kernel<<<E, TH_THREADS, smem, stream>>>(logits, T, E, k, tau);
+  thresholds_kernel<<<E, TH_THREADS, smem, stream>>>(z, T, stride_t, stride_e, k, tau);
+  return cudaGetLastError() == cudaSuccess ? LMOE_OK : LMOE_ERR_CUDA;
+}
+
+int launch_transpose_f32(const float* in, int T, int E, float* out, cudaStream_t stream) {
+  if (T == 0) return LMOE_OK;
+  const dim3 grid(static_cast<unsigned>(ceil_div(E, 32)), static_cast<unsigned>(ceil_div(T, 32)));
+  transpose_f32_kernel<<<grid, 256, 0, stream>>>(in, T, E, out);
   return cudaGetLastError() == cudaSuccess ? LMOE_OK : LMOE_ERR_CUDA;
 }
 

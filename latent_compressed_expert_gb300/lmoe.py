@@ -39,7 +39,11 @@ class Weights(ctypes.Structure):
 class IO(ctypes.Structure):
     _fields_ = [("tau_in", _vp), ("balance", _i), ("logits_in", _vp), ("logits_out", _vp),
                 ("tau_out", _vp), ("idx_out", _vp), ("gate_out", _vp), ("counts_out", _vp),
-                ("stage_events", ctypes.POINTER(_vp)), ("kernel_launches", _i)]
+                ("stage_events", ctypes.POINTER(_vp)), ("kernel_launches", _i),
+                ("aux_stream", _vp), ("aux_events", _vp * 2), ("shared_sms", _i)]
+
+
+OVERLAP_MIN_T = 512  # LMOE_OVERLAP_MIN_T
 
 
 # enum lmoe_stage
@@ -209,7 +213,12 @@ class Layer:
     """One Stable Latent MoE layer on the device: packed weights + a workspace sized for up
     to ``max_tokens`` tokens.  ``forward`` is one lmoe_forward call."""
 
-    def __init__(self, shape, weights: dict, max_tokens: int | None = None, stream=None):
+    def __init__(self, shape, weights: dict, max_tokens: int | None = None, stream=None,
+                 overlap: bool = False, shared_sms: int = 0):
+        """overlap: run the shared experts on an auxiliary stream beside the routed path for
+        batches of at least OVERLAP_MIN_T tokens (shared_sms SMs for them; 0 = a third).
+        Off by default: the routed expert GEMMs are limited per SM, so the SMs lent to the
+        shared experts slow them down more than the concurrency gains."""
         self.shape = shape
         self.max_tokens = shape.T if max_tokens is None else max_tokens
         self.dims = dims_of(shape, T=self.max_tokens)
@@ -217,6 +226,15 @@ class Layer:
         self.packed = pack_weights(self.dims, weights, stream)
         self.ws_bytes = workspace_bytes(self.dims)
         self.workspace = torch.empty(self.ws_bytes, dtype=torch.uint8, device=self.device)
+        self.overlap = overlap
+        self.shared_sms = shared_sms
+        self.aux_stream = torch.cuda.Stream(device=self.device) if overlap else None
+        self.aux_events = []
+        if overlap:
+            for _ in range(2):
+                ev = torch.cuda.Event()
+                ev.record(torch.cuda.current_stream(self.device))  # create the event now
+                self.aux_events.append(ev)
 
     def forward(self, x: torch.Tensor, residual: torch.Tensor | None = None, y=None,
                 tau: torch.Tensor | None = None, balance: bool = True,
@@ -237,6 +255,11 @@ class Layer:
         dims = dims_of(sh, T=T)
         io = IO()
         io.balance = 1 if balance else 0
+        if self.overlap and T >= OVERLAP_MIN_T and T <= self.max_tokens:
+            io.aux_stream = ctypes.c_void_p(self.aux_stream.cuda_stream)
+            io.aux_events[0] = self.aux_events[0].cuda_event
+            io.aux_events[1] = self.aux_events[1].cuda_event
+            io.shared_sms = self.shared_sms
         dbg = {}
         if tau is not None:
             _expect(tau, torch.float32, (sh.E,), "tau")

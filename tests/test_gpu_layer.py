@@ -310,3 +310,23 @@ def test_skew_router_given_logits(dev, oracle_mod):
     wh = H.weights_to_host(w)
     ref = H.oracle_rows(oracle_mod, wh, x[rows].cpu(), idx[rows], gate[rows], None)
     H.assert_close(y[rows].float().cpu().numpy(), ref, "skew")
+
+
+@pytest.mark.parametrize("overlap", [False, True])
+def test_shared_overlap_and_serial_paths(dev, oracle_mod, overlap):
+    """Batches of at least 512 tokens may run the shared experts on a second stream (fp32
+    partial added in the output GEMM's epilogue); both paths match the oracle and route
+    identically."""
+    sh = H.mid_shape()
+    w = synth.make_weights(sh, seed=5)
+    layer = lmoe.Layer(sh, {k: v.to(dev) for k, v in w.items()}, overlap=overlap, shared_sms=40)
+    x = synth.make_x(sh, seed=5)
+    logits = synth.make_logits(sh.T, sh.E, seed=5)
+    xd = x.to(dev)
+    y, dbg = layer.forward(xd, residual=xd, logits_in=logits.to(dev), debug=True)
+    torch.cuda.synchronize()
+    assert layer.device_error() == 0
+    assert layer.last_kernel_launches == (13 if overlap else 11)
+    ref = oracle_mod.forward(w, x, sh.K, residual=x, tau="batch", logits_in=logits.numpy())
+    assert np.array_equal(dbg["idx"].cpu().numpy(), ref.idx)
+    H.assert_close(y.float().cpu().numpy(), ref.y, f"mid/overlap={overlap}")
