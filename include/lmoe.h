@@ -206,7 +206,7 @@ int lmoe_gemm_bf16(const void *A, const void *B, float *C, int M, int N, int Kd,
  * process starts.  Arguments and results are those of lmoe_forward without the workspace.
  * Scratch: a LMOE_NOALLOC_SCRATCH_BYTES (24 MiB) array in the library's device image,
  * reserved on every GPU that loads the library until the process exits.  It covers a K3
- * decode batch of up to 91 tokens (64 tokens need 16.8 MiB).  When lmoe_workspace_bytes(dims)
+ * decode batch of up to 155 tokens (64 tokens need 9.9 MiB).  When lmoe_workspace_bytes(dims)
  * exceeds it, the call returns LMOE_ERR_WORKSPACE_TOO_SMALL and enqueues nothing.
  * Set-up: the first call on each device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call before any stream

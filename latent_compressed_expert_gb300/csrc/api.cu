@@ -75,7 +75,7 @@ WorkspaceLayout workspace_layout(const lmoe_dims& D) {
   W.offsets = take((static_cast<size_t>(D.E) + 1) * 4);
   W.ct_off = take((static_cast<size_t>(D.E) + 1) * 4);
   W.inv = take(TK * 4);
-  W.lat_p = take(TK * D.L * 2);
+  W.src_tok = take(TK * 4);
   W.h = take(TK * D.I * 2);
   W.o = take(TK * D.L * 2);
   W.zh = take(T * (D.L + shared_width(D)) * 2);
@@ -399,13 +399,14 @@ int lmoe_forward(const lmoe_dims* dims, const void* packed, const void* x, const
   int32_t* offsets = reinterpret_cast<int32_t*>(ws + W.offsets);
   int32_t* ct_off = reinterpret_cast<int32_t*>(ws + W.ct_off);
   int32_t* inv = reinterpret_cast<int32_t*>(ws + W.inv);
-  bf* lat_p = reinterpret_cast<bf*>(ws + W.lat_p);
-  rc = launch_dispatch(idx, lat, T, D.E, D.K, D.L, reinterpret_cast<uint32_t*>(ws + W.masks),
-                       reinterpret_cast<uint32_t*>(ws + W.base), offsets, ct_off, inv, lat_p,
+  int32_t* src_tok = reinterpret_cast<int32_t*>(ws + W.src_tok);
+  rc = launch_dispatch(idx, T, D.E, D.K, reinterpret_cast<uint32_t*>(ws + W.masks),
+                       reinterpret_cast<uint32_t*>(ws + W.base), offsets, ct_off, inv, src_tok,
                        opt.counts_out, err, stream);
   if (rc != LMOE_OK) return rc;
   if (!mark(LMOE_STAGE_EXPERT_GATE_UP, 3)) return LMOE_ERR_CUDA;
-  // 6. routed gate/value GEMM with SiTU-GLU: h = SiTU(lat_p . W_gu[e]^T) per expert
+  // 6. routed gate/value GEMM with SiTU-GLU: h = SiTU(lat[src_tok] . W_gu[e]^T) per expert,
+  //    the latent rows gathered inside the GEMM
   bf* h = reinterpret_cast<bf*>(ws + W.h);
   {
     GroupedArgs g{};
@@ -414,6 +415,9 @@ int lmoe_forward(const lmoe_dims* dims, const void* packed, const void* x, const
     g.Kd = D.L;
     g.seg_off = offsets;
     g.ct_off = ct_off;
+    g.gather = src_tok;
+    g.x = lat;
+    g.ldx = D.L;
     g.epi = EPI_SITU;
     g.out = h;
     g.ldo = D.I;
@@ -421,7 +425,7 @@ int lmoe_forward(const lmoe_dims* dims, const void* packed, const void* x, const
     g.err = err;
     g.timeout_ns = wait_limit_ns();
     g.max_ctas = routed_ctas;
-    rc = launch_grouped_gemm(pk + P.wgu, D.L, lat_p, static_cast<uint64_t>(TK), D.L, g, stream);
+    rc = launch_grouped_gemm(pk + P.wgu, D.L, lat, static_cast<uint64_t>(T), D.L, g, stream);
     if (rc != LMOE_OK) return rc;
   }
   if (!mark(LMOE_STAGE_EXPERT_DOWN, 1)) return LMOE_ERR_CUDA;

@@ -1,5 +1,6 @@
-// dispatch.cu -- token dispatch into expert-contiguous segments, and the gate-weighted
-// aggregation fused with RMSNorm.
+// dispatch.cu -- token dispatch into expert-contiguous segments (indices only: the routed
+// gate/value GEMM gathers the latent rows itself), and the gate-weighted aggregation fused
+// with RMSNorm.
 //
 // Sources: "The 2.8-Trillion-Parameter Problem: Why Bigger Models Break the Old Playbook"
 // ("Part 1 of Inside Kimi K3", Towards AI article): each selected expert receives the
@@ -134,16 +135,14 @@ dispatch_scan_kernel(const uint32_t* __restrict__ masks, int nb, int E, int TK,
   }
 }
 
-// Scatter + gather: inv[t*K + j] = row of (t, j) in the permuted order, and
-// lat_p[row, :] = lat[t, :].  One warp per (token, slot) pair; each lane keeps up to eight
-// 16-byte loads in flight before their stores.
+// Scatter: inv[t*K + j] = row of (t, j) in the permuted order, and src_tok[row] = t (the
+// routed gate/value GEMM gathers the latent rows through it).  One thread per pair.
 __global__ void __launch_bounds__(256)
 dispatch_scatter_kernel(const int32_t* __restrict__ idx, const uint32_t* __restrict__ masks,
                         const uint32_t* __restrict__ base, const int32_t* __restrict__ offsets,
-                        const __nv_bfloat16* __restrict__ lat, int T, int E, int K, int L,
-                        int32_t* __restrict__ inv, __nv_bfloat16* __restrict__ lat_p) {
-  const int lane = threadIdx.x & 31;
-  const int64_t p = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+                        int T, int E, int K, int32_t* __restrict__ inv,
+                        int32_t* __restrict__ src_tok) {
+  const int64_t p = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (p >= static_cast<int64_t>(T) * K) return;
   const int t = static_cast<int>(p / K);
   const int b = t / DISPATCH_TOKENS, tl = t % DISPATCH_TOKENS;
@@ -152,20 +151,8 @@ dispatch_scatter_kernel(const int32_t* __restrict__ idx, const uint32_t* __restr
   const size_t me = static_cast<size_t>(b) * E + e;
   const int row = __ldg(offsets + e) + static_cast<int>(__ldg(base + me)) +
                   __popc(__ldg(masks + me) & ((1u << tl) - 1u));
-  if (lane == 0) inv[p] = row;
-  const uint4* src = reinterpret_cast<const uint4*>(lat + static_cast<size_t>(t) * L);
-  uint4* dst = reinterpret_cast<uint4*>(lat_p + static_cast<size_t>(row) * L);
-  const int nvec = L / 8;
-  constexpr int B = 8;
-  for (int v0 = lane; v0 < nvec; v0 += B * 32) {
-    uint4 r[B];
-#pragma unroll
-    for (int i = 0; i < B; ++i)
-      if (v0 + i * 32 < nvec) r[i] = __ldg(src + v0 + i * 32);
-#pragma unroll
-    for (int i = 0; i < B; ++i)
-      if (v0 + i * 32 < nvec) dst[v0 + i * 32] = r[i];
-  }
+  inv[p] = row;
+  src_tok[row] = t;
 }
 
 // Combine + RMSNorm: one CTA per token, each thread owns 8 consecutive latent features
@@ -255,10 +242,9 @@ combine_rmsnorm_kernel(const __nv_bfloat16* __restrict__ o, const float* __restr
 }
 
 // ------------------------------------------------------------------------------------
-int launch_dispatch(const int32_t* idx, const __nv_bfloat16* lat, int T, int E, int K, int L,
-                    uint32_t* masks, uint32_t* base, int32_t* offsets, int32_t* ct_off,
-                    int32_t* inv, __nv_bfloat16* lat_p, int32_t* counts_out, uint32_t* err,
-                    cudaStream_t stream) {
+int launch_dispatch(const int32_t* idx, int T, int E, int K, uint32_t* masks, uint32_t* base,
+                    int32_t* offsets, int32_t* ct_off, int32_t* inv, int32_t* src_tok,
+                    int32_t* counts_out, uint32_t* err, cudaStream_t stream) {
   const int nb = static_cast<int>(ceil_div(T, DISPATCH_TOKENS));
   const size_t msmem = static_cast<size_t>(E) * sizeof(uint32_t);
   if (nb > 0) {
@@ -269,9 +255,9 @@ int launch_dispatch(const int32_t* idx, const __nv_bfloat16* lat, int T, int E, 
                                                counts_out);
   if (cudaGetLastError() != cudaSuccess) return LMOE_ERR_CUDA;
   if (nb > 0) {
-    const int64_t warps = static_cast<int64_t>(T) * K;
-    dispatch_scatter_kernel<<<static_cast<unsigned>(ceil_div(warps, 8)), 256, 0, stream>>>(
-        idx, masks, base, offsets, lat, T, E, K, L, inv, lat_p);
+    const int64_t pairs = static_cast<int64_t>(T) * K;
+    dispatch_scatter_kernel<<<static_cast<unsigned>(ceil_div(pairs, 256)), 256, 0, stream>>>(
+        idx, masks, base, offsets, T, E, K, inv, src_tok);
     if (cudaGetLastError() != cudaSuccess) return LMOE_ERR_CUDA;
   }
   return LMOE_OK;

@@ -16,7 +16,7 @@
 //
 // Roles as in gemm.cu: warp 0 TMA producer (one 128 x 64 weight box + one 32 x 64 box per 32
 // tokens), warp 1 TMEM owner and single-thread tcgen05.mma issuer (instruction descriptor
-// with the tile's N built at run time), warps 2-5 epilogue.  In the epilogue a thread owns
+// with the tile's N built at run time), warps 2-5 epilogue, warps 6-9 row gatherers.  In the epilogue a thread owns
 // one weight row (one output feature) and walks the tokens, so a warp writes 32 consecutive
 // features of one token row per store.  Gate/value epilogue (SiTU-GLU): weight rows are
 // interleaved 16 gate / 16 value, so lanes l and l+16 hold the gate and value of the same
@@ -46,7 +46,12 @@ struct GroupedCfg {
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
 
-constexpr int GROUPED_THREADS = 192;
+// warp 0 TMA producer, warp 1 MMA, warps 2..5 epilogue, warps 6..9 row gatherers (used when
+// the activation rows are gathered through an index, idle otherwise)
+constexpr int GROUPED_EPI_WARPS = 4;
+constexpr int GROUPED_GATHER_WARPS = 4;
+constexpr int GROUPED_GATHER_THREADS = GROUPED_GATHER_WARPS * 32;
+constexpr int GROUPED_THREADS = (2 + GROUPED_EPI_WARPS + GROUPED_GATHER_WARPS) * 32;
 
 struct GTile {
   int w_row;    // first weight row (packed [E * M_w, Kd])
@@ -124,13 +129,16 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
   const uint64_t limit = g.timeout_ns;
 
   if (threadIdx.x == 0) {
+    // a stage is full once the TMA bytes have landed and, when rows are gathered, every
+    // gathering thread's copies have landed too
+    const uint32_t full_count = 1u + (g.gather ? GROUPED_GATHER_THREADS : 0u);
     for (int s = 0; s < C::STAGES; ++s) {
-      ptx::mbar_init(&full[s], 1);
+      ptx::mbar_init(&full[s], full_count);
       ptx::mbar_init(&empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(&tfull[a], 1);
-      ptx::mbar_init(&tempty[a], 128);
+      ptx::mbar_init(&tempty[a], GROUPED_EPI_WARPS * 32);
     }
     ptx::mbar_init(drain, 1);
     *abort_flag = 0;
@@ -156,7 +164,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
         const GTile t = decode_gtile(g, mt, tile);
-        const int nbox = t.npad / C::BOX_T;
+        const int nbox = g.gather ? 0 : t.npad / C::BOX_T;
         const uint32_t bytes = C::A_BYTES + static_cast<uint32_t>(nbox) * C::BOX_T * BLOCK_K * 2;
         for (int kb = 0; kb < nk; ++kb, ++it) {
           const int s = static_cast<int>(it % C::STAGES);
@@ -210,6 +218,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
             break;
           }
           ptx::tc_fence_after();
+          if (g.gather) ptx::fence_proxy_async_smem();  // rows written by cp.async
           const uint32_t sa = ptx::smem_u32(smem + s * C::STAGE_BYTES);
           const uint32_t sb = sa + C::A_BYTES;
 #pragma unroll
@@ -224,9 +233,49 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
       ptx::umma_commit(drain);
       if (!gwait_drain(drain, 0u, limit)) graise(g, abort_flag, DEVERR_TIMEOUT_DRAIN);
     }
+  } else if (warp >= 2 + GROUPED_EPI_WARPS) {
+    // ------------------------------------------------------------ row gatherers (warps 6..9)
+    // Thread gt copies 16-byte chunk (gt & 7) of rows gt/8 + 16 j of each stage's token
+    // tile, from the activation row src = gather[permuted row], into the 128-byte-swizzled
+    // K-major layout the MMA reads; its arrival on the stage's barrier fires when they land.
+    if (g.gather) {
+      const int gt = threadIdx.x - (2 + GROUPED_EPI_WARPS) * 32;
+      const int chunk = gt & 7;
+      constexpr int J = C::TOKN / 16;  // rows per thread
+      uint32_t it = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+        const GTile t = decode_gtile(g, mt, tile);
+        const __nv_bfloat16* src[J];
+#pragma unroll
+        for (int j = 0; j < J; ++j) {
+          const int row = (gt >> 3) + 16 * j;
+          const int tok = t.tok0 + (row < t.ntok ? row : t.ntok - 1);  // pad: a valid row
+          src[j] = g.x + static_cast<size_t>(__ldg(g.gather + tok)) * g.ldx + chunk * 8;
+        }
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int s = static_cast<int>(it % C::STAGES);
+          const uint32_t ph = (it / C::STAGES) & 1u;
+          if (!ptx::mbar_wait(&empty[s], ph ^ 1u, abort_flag, limit)) {
+            graise(g, abort_flag, DEVERR_TIMEOUT_PRODUCER);
+            ok = false;
+            break;
+          }
+          const uint32_t sb = ptx::smem_u32(smem + s * C::STAGE_BYTES + C::A_BYTES);
+#pragma unroll
+          for (int j = 0; j < J; ++j) {
+            const int row = (gt >> 3) + 16 * j;
+            if (row < t.npad)
+              ptx::cp_async_16(sb + row * 128 + ((chunk ^ (row & 7)) << 4), src[j] + kb * BLOCK_K);
+          }
+          ptx::cp_async_mbar_arrive_noinc(&full[s]);
+        }
+      }
+      ptx::cp_async_wait_all();
+    }
   } else {
     // ------------------------------------------------------------ epilogue (warps 2..5)
-    const int q = warp & 3;
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
     const float c = g.c, inv_c = 1.0f / g.c;
     int lt = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++lt) {

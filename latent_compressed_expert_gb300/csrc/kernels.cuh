@@ -15,7 +15,7 @@ struct PackedLayout {
 
 // Offsets (bytes) of the forward workspace; every buffer 256-aligned.
 struct WorkspaceLayout {
-  size_t err, lat, logits, logits_t, tau, idx, gate, masks, base, offsets, ct_off, inv, lat_p,
+  size_t err, lat, logits, logits_t, tau, idx, gate, masks, base, offsets, ct_off, inv, src_tok,
       h, o, zh, ys, total;
 };
 
@@ -65,6 +65,10 @@ struct GroupedArgs {
   int Kd;                 // reduction length (L for gate/value, I for down), multiple of 64
   const int32_t* seg_off; // [E+1] first token row of each expert's segment
   const int32_t* ct_off;  // [E+1] prefix sum of ceil(count / GROUPED_TOKN)
+  const int32_t* gather;  // [rows] source row of each permuted row, or null: then the
+                          // activation rows are the permuted rows themselves (TMA boxes)
+  const __nv_bfloat16* x; // gathered activations [*, ldx] (with gather)
+  int ldx;
   int epi;                // EPI_SITU (gate/value, M_w = 2I) or EPI_BF16
   __nv_bfloat16* out;     // [rows, ldo] token-major output
   int ldo;
@@ -93,10 +97,9 @@ int launch_thresholds(const float* z, int T, int E, int64_t stride_t, int64_t st
                       float* tau, cudaStream_t stream);
 // out[E, T] = in[T, E]^T (fp32).
 int launch_transpose_f32(const float* in, int T, int E, float* out, cudaStream_t stream);
-int launch_dispatch(const int32_t* idx, const __nv_bfloat16* lat, int T, int E, int K, int L,
-                    uint32_t* masks, uint32_t* base, int32_t* offsets, int32_t* ct_off,
-                    int32_t* inv, __nv_bfloat16* lat_p, int32_t* counts_out, uint32_t* err,
-                    cudaStream_t stream);
+int launch_dispatch(const int32_t* idx, int T, int E, int K, uint32_t* masks, uint32_t* base,
+                    int32_t* offsets, int32_t* ct_off, int32_t* inv, int32_t* src_tok,
+                    int32_t* counts_out, uint32_t* err, cudaStream_t stream);
 int launch_combine(const __nv_bfloat16* o, const float* gate, const int32_t* inv,
                    const float* gamma, int T, int K, int L, float eps, __nv_bfloat16* z,
                    int ldz, cudaStream_t stream);

@@ -67,7 +67,7 @@ def test_noalloc_matches_forward_with_workspace(lib, decode_layer, which):
 
 
 def test_noalloc_refuses_batches_beyond_its_array(lib, decode_layer):
-    T = 256  # needs ~67 MiB of scratch at the K3 widths
+    T = 256  # needs ~39 MiB of scratch at the K3 widths
     assert lmoe.workspace_bytes(lmoe.dims_of(synth.DECODE, T=T)) > lmoe_scratch_bytes()
     x = synth.make_x(synth.DECODE, seed=5, device="cuda", T=T)
     y = torch.full_like(x, 7.0)
