@@ -55,7 +55,9 @@ def test_size_queries(lib):
     weights = (sh.L * sh.d + sh.E * sh.L + 3 * sh.E * sh.I * sh.L + sh.d * sh.L
                + 3 * sh.S * sh.Is * sh.d) * 2 + sh.L * 4
     assert weights <= pb <= weights + 6 * 1024
-    assert lmoe.workspace_bytes(d) > sh.T * sh.K * sh.L * 2 * 2  # lat_p and o dominate
+    # the expert outputs o [T*K, L] dominate; the permuted latent is never materialised
+    o_bytes = sh.T * sh.K * sh.L * 2
+    assert o_bytes < lmoe.workspace_bytes(d) < 2 * o_bytes
     # T = 0 is valid and small
     assert 0 < lmoe.workspace_bytes(lmoe.dims_of(synth.PREFILL, T=0)) < 1 << 20
 
