@@ -45,8 +45,9 @@ PackedLayout packed_layout(const lmoe_dims& D) {
   const size_t sw = static_cast<size_t>(shared_width(D));
   P.w1 = take((static_cast<size_t>(D.L) + 2 * sw) * D.d * 2);
   P.wr = take(static_cast<size_t>(D.E) * D.L * 2);
-  P.wgu = take(static_cast<size_t>(D.E) * 2 * D.I * D.L * 2);
-  P.wed = take(static_cast<size_t>(D.E) * D.L * D.I * 2);
+  // expert weights in 128-row tiles (the last row tile of an expert zero-padded)
+  P.wgu = take(static_cast<size_t>(D.E) * ceil_div(2 * D.I, BLOCK_M) * BLOCK_M * D.L * 2);
+  P.wed = take(static_cast<size_t>(D.E) * ceil_div(D.L, BLOCK_M) * BLOCK_M * D.I * 2);
   P.w2 = take(static_cast<size_t>(D.d) * (D.L + sw) * 2);
   P.gamma = take(static_cast<size_t>(D.L) * 4);
   P.total = off;
@@ -425,7 +426,7 @@ int lmoe_forward(const lmoe_dims* dims, const void* packed, const void* x, const
     g.err = err;
     g.timeout_ns = wait_limit_ns();
     g.max_ctas = routed_ctas;
-    rc = launch_grouped_gemm(pk + P.wgu, D.L, lat, static_cast<uint64_t>(T), D.L, g, stream);
+    rc = launch_grouped_gemm(pk + P.wgu, lat, static_cast<uint64_t>(T), D.L, g, stream);
     if (rc != LMOE_OK) return rc;
   }
   if (!mark(LMOE_STAGE_EXPERT_DOWN, 1)) return LMOE_ERR_CUDA;
@@ -445,7 +446,7 @@ int lmoe_forward(const lmoe_dims* dims, const void* packed, const void* x, const
     g.err = err;
     g.timeout_ns = wait_limit_ns();
     g.max_ctas = routed_ctas;
-    rc = launch_grouped_gemm(pk + P.wed, D.I, h, static_cast<uint64_t>(TK), D.I, g, stream);
+    rc = launch_grouped_gemm(pk + P.wed, h, static_cast<uint64_t>(TK), D.I, g, stream);
     if (rc != LMOE_OK) return rc;
   }
   if (!mark(LMOE_STAGE_COMBINE, 1)) return LMOE_ERR_CUDA;

@@ -14,8 +14,8 @@
 // sharing a token chunk run on neighbouring SMs at the same time.  The chunk counts come
 // from a device-side prefix sum; nothing returns to the host.
 //
-// Roles as in gemm.cu: warp 0 TMA producer (one 128 x 64 weight box + one 32 x 64 box per 32
-// tokens), warp 1 TMEM owner and single-thread tcgen05.mma issuer (instruction descriptor
+// Roles as in gemm.cu: warp 0 TMA producer (one 128 x 64 weight box, a contiguous 16 KB tile
+// of the packed weights, + one 32 x 64 box per 32 tokens), warp 1 TMEM owner and single-thread tcgen05.mma issuer (instruction descriptor
 // with the tile's N built at run time), warps 2-5 epilogue, warps 6-9 row gatherers.  In the epilogue a thread owns
 // one weight row (one output feature) and walks the tokens, so a warp writes 32 consecutive
 // features of one token row per store.  Gate/value epilogue (SiTU-GLU): weight rows are
@@ -54,7 +54,7 @@ constexpr int GROUPED_GATHER_THREADS = GROUPED_GATHER_WARPS * 32;
 constexpr int GROUPED_THREADS = (2 + GROUPED_EPI_WARPS + GROUPED_GATHER_WARPS) * 32;
 
 struct GTile {
-  int w_row;    // first weight row (packed [E * M_w, Kd])
+  int w_row;    // row coordinate of the tile's first 128 x 64 weight box (tiled layout)
   int r0;       // first weight row within the expert (output feature)
   int tok0;     // first token row (permuted order)
   int ntok;     // valid token rows in this tile (1..TOKN)
@@ -76,7 +76,7 @@ __device__ __forceinline__ GTile decode_gtile(const GroupedArgs& g, int mt, int 
   const int m = tile - q * mt;
   GTile t;
   t.r0 = m * BLOCK_M;
-  t.w_row = e * g.M_w + t.r0;
+  t.w_row = (e * mt + m) * (g.Kd / BLOCK_K) * BLOCK_M;
   t.tok0 = __ldg(g.seg_off + e) + chunk * GroupedCfg::TOKN;
   const int end = __ldg(g.seg_off + e + 1);
   t.ntok = min(GroupedCfg::TOKN, end - t.tok0);
@@ -177,7 +177,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
           uint8_t* sa = smem + s * C::STAGE_BYTES;
           uint8_t* sb = sa + C::A_BYTES;
           ptx::mbar_arrive_expect_tx(&full[s], bytes);
-          ptx::tma_load_2d(sa, &tmW, &full[s], kb * BLOCK_K, t.w_row);
+          ptx::tma_load_2d(sa, &tmW, &full[s], 0, t.w_row + kb * BLOCK_M);
           for (int b = 0; b < nbox; ++b)
             ptx::tma_load_2d(sb + b * C::BOX_T * BLOCK_K * 2, &tmX, &full[s], kb * BLOCK_K,
                              t.tok0 + b * C::BOX_T);
@@ -329,15 +329,16 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
   }
 }
 
-int launch_grouped_gemm(const void* W, int w_ld, const void* X, uint64_t x_rows, int x_ld,
+int launch_grouped_gemm(const void* W, const void* X, uint64_t x_rows, int x_ld,
                         const GroupedArgs& g, cudaStream_t stream) {
   using C = GroupedCfg;
   if (g.M_w <= 0 || g.Kd % BLOCK_K != 0 || g.Kd <= 0 || x_rows == 0) return LMOE_ERR_UNSUPPORTED;
   if (g.epi != EPI_SITU && g.epi != EPI_BF16) return LMOE_ERR_UNSUPPORTED;
   if (g.epi == EPI_SITU && g.M_w % BLOCK_M != 0) return LMOE_ERR_UNSUPPORTED;
   CUtensorMap tw, tx;
-  if (!make_tmap_bf16(&tw, W, static_cast<uint64_t>(g.E) * g.M_w, static_cast<uint64_t>(g.Kd),
-                      static_cast<uint64_t>(w_ld), BLOCK_M) ||
+  const uint64_t w_rows = static_cast<uint64_t>(g.E) * ceil_div(g.M_w, BLOCK_M) *
+                          (g.Kd / BLOCK_K) * BLOCK_M;  // tiled: rows of 64 bf16
+  if (!make_tmap_bf16(&tw, W, w_rows, BLOCK_K, BLOCK_K, BLOCK_M) ||
       !make_tmap_bf16(&tx, X, x_rows, static_cast<uint64_t>(g.Kd), static_cast<uint64_t>(x_ld),
                       C::BOX_T))
     return LMOE_ERR_CUDA;

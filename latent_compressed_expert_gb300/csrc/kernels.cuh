@@ -78,7 +78,8 @@ struct GroupedArgs {
   int max_ctas;           // persistent grid limit (0: one CTA per SM)
 };
 
-int launch_grouped_gemm(const void* W, int w_ld, const void* X, uint64_t x_rows, int x_ld,
+// W: the experts' weights in 128 x 64 tiles ordered (expert, row tile, column tile).
+int launch_grouped_gemm(const void* W, const void* X, uint64_t x_rows, int x_ld,
                         const GroupedArgs& g, cudaStream_t stream);
 
 // Encodes a 2-D bf16 row-major [rows, cols] (row stride ld elements) TMA map with a

@@ -4,10 +4,15 @@
 //                        interleaved in groups of 16 (16 gate rows of features f..f+15, then
 //                        the 16 value rows of the same features), features ordered s*Is + i
 //   Wr  [E, L]           router, unchanged
-//   Wgu [E, 2 I, L]      per expert, gate/value rows interleaved in groups of 16 likewise
-//   Wed [E, L, I]        routed down-projections, unchanged
+//   Wgu                  per expert, gate/value rows interleaved in groups of 16 likewise,
+//                        stored as tiles (below)
+//   Wed                  routed down-projections, stored as tiles (below)
 //   W2  [d, L + S Is]    row n = [ W_up[n, :] | W_sd[0][n, :] | ... | W_sd[S-1][n, :] ]
 //   gamma [L] fp32
+// Tiled expert weights: an expert's [M_w, Kd] matrix is cut into 128-row x 64-column tiles,
+// ordered (expert, row tile, column tile), each stored as 128 consecutive rows of 64 bf16
+// (16 KB, contiguous); rows past M_w in the last row tile are zero.  Every box the routed
+// GEMMs load is then one contiguous 16 KB read.
 // The interleave lets one 32-column slice of a GEMM accumulator hold 16 gate and the 16
 // matching value pre-activations, so SiTU-GLU is applied in the GEMM epilogue.  The two
 // shared experts then form one GLU of width S*Is, and the shared down-projection is
@@ -18,7 +23,7 @@
 
 namespace lmoe {
 
-enum PackJob : int { PACK_W1 = 0, PACK_WGU = 1, PACK_W2 = 2 };
+enum PackJob : int { PACK_W1 = 0, PACK_W2 = 2 };
 
 struct PackArgs {
   int job;
@@ -52,13 +57,6 @@ __global__ void __launch_bounds__(256) pack_kernel(const PackArgs p) {
         const __nv_bfloat16* src = (w < GLU_GROUP ? p.g : p.v) + static_cast<size_t>(f) * p.d;
         copy_row(drow, src, p.d);
       }
-    } else if (p.job == PACK_WGU) {
-      const int e = r / (2 * p.I), rr = r % (2 * p.I);
-      const int grp = rr / (2 * GLU_GROUP), w = rr % (2 * GLU_GROUP);
-      const int f = grp * GLU_GROUP + (w % GLU_GROUP);
-      const __nv_bfloat16* src =
-          (w < GLU_GROUP ? p.g : p.v) + (static_cast<size_t>(e) * p.I + f) * p.L;
-      copy_row(drow, src, p.L);
     } else {  // PACK_W2, row n of the output width d
       copy_row(drow, p.a + static_cast<size_t>(r) * p.L, p.L);
       for (int s = 0; s < p.S; ++s)
@@ -66,6 +64,48 @@ __global__ void __launch_bounds__(256) pack_kernel(const PackArgs p) {
                  p.sd + (static_cast<size_t>(s) * p.d + r) * p.Is, p.Is);
     }
   }
+}
+
+// Tiled expert weights.  glu = 1: rows are the gate/value interleave of w_g / w_v
+// ([E, M_w / 2, Kd] each); glu = 0: rows of w ([E, M_w, Kd]).  One thread per 16-byte chunk.
+__global__ void __launch_bounds__(256)
+pack_tiled_kernel(__nv_bfloat16* __restrict__ dst, const __nv_bfloat16* __restrict__ w,
+                  const __nv_bfloat16* __restrict__ w_g, const __nv_bfloat16* __restrict__ w_v,
+                  int glu, int E, int M_w, int Kd) {
+  const int mt = (M_w + BLOCK_M - 1) / BLOCK_M, nk = Kd / BLOCK_K;
+  const int64_t chunks = static_cast<int64_t>(E) * mt * nk * BLOCK_M * (BLOCK_K / 8);
+  for (int64_t c = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; c < chunks;
+       c += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t row = c >> 3;  // 8 chunks of 16 B per 64-column row
+    const int ch = static_cast<int>(c & 7);
+    const int r = static_cast<int>(row % BLOCK_M);
+    const int64_t tile = row / BLOCK_M;
+    const int kb = static_cast<int>(tile % nk);
+    const int64_t em = tile / nk;
+    const int m = static_cast<int>(em % mt);
+    const int e = static_cast<int>(em / mt);
+    const int lr = m * BLOCK_M + r;  // row within the expert
+    uint4 val = make_uint4(0u, 0u, 0u, 0u);
+    if (lr < M_w) {
+      const __nv_bfloat16* src;
+      if (glu) {
+        const int grp = lr / (2 * GLU_GROUP), wi = lr % (2 * GLU_GROUP);
+        const int f = grp * GLU_GROUP + (wi % GLU_GROUP);
+        src = (wi < GLU_GROUP ? w_g : w_v) + (static_cast<size_t>(e) * (M_w / 2) + f) * Kd;
+      } else {
+        src = w + (static_cast<size_t>(e) * M_w + lr) * Kd;
+      }
+      val = __ldg(reinterpret_cast<const uint4*>(src + kb * BLOCK_K) + ch);
+    }
+    reinterpret_cast<uint4*>(dst)[c] = val;
+  }
+}
+
+static int run_pack_tiled(__nv_bfloat16* dst, const __nv_bfloat16* w, const __nv_bfloat16* w_g,
+                          const __nv_bfloat16* w_v, int glu, int E, int M_w, int Kd,
+                          cudaStream_t stream) {
+  pack_tiled_kernel<<<4096, 256, 0, stream>>>(dst, w, w_g, w_v, glu, E, M_w, Kd);
+  return cudaGetLastError() == cudaSuccess ? LMOE_OK : LMOE_ERR_CUDA;
 }
 
 static int run_pack(const PackArgs& a, cudaStream_t stream) {
@@ -95,13 +135,13 @@ int launch_pack(const lmoe_dims& D, const lmoe_weights& w, const PackedLayout& P
   a.v = static_cast<const bf*>(w.w_svalue);
   if ((rc = run_pack(a, stream)) != LMOE_OK) return rc;
 
-  a.job = PACK_WGU;
-  a.rows = D.E * 2 * D.I;
-  a.cols = D.L;
-  a.dst = reinterpret_cast<bf*>(base + P.wgu);
-  a.g = static_cast<const bf*>(w.w_gate);
-  a.v = static_cast<const bf*>(w.w_value);
-  if ((rc = run_pack(a, stream)) != LMOE_OK) return rc;
+  if ((rc = run_pack_tiled(reinterpret_cast<bf*>(base + P.wgu), nullptr,
+                           static_cast<const bf*>(w.w_gate), static_cast<const bf*>(w.w_value), 1,
+                           D.E, 2 * D.I, D.L, stream)) != LMOE_OK)
+    return rc;
+  if ((rc = run_pack_tiled(reinterpret_cast<bf*>(base + P.wed), static_cast<const bf*>(w.w_edown),
+                           nullptr, nullptr, 0, D.E, D.L, D.I, stream)) != LMOE_OK)
+    return rc;
 
   a.job = PACK_W2;
   a.rows = D.d;
@@ -112,9 +152,6 @@ int launch_pack(const lmoe_dims& D, const lmoe_weights& w, const PackedLayout& P
   if ((rc = run_pack(a, stream)) != LMOE_OK) return rc;
 
   if (cudaMemcpyAsync(base + P.wr, w.w_router, static_cast<size_t>(D.E) * D.L * 2,
-                      cudaMemcpyDeviceToDevice, stream) != cudaSuccess)
-    return LMOE_ERR_CUDA;
-  if (cudaMemcpyAsync(base + P.wed, w.w_edown, static_cast<size_t>(D.E) * D.L * D.I * 2,
                       cudaMemcpyDeviceToDevice, stream) != cudaSuccess)
     return LMOE_ERR_CUDA;
   if (cudaMemcpyAsync(base + P.gamma, w.gamma, static_cast<size_t>(D.L) * 4,
