@@ -52,9 +52,11 @@ def stage_work(sh, touched: int, residual: bool = True) -> dict:
         "router": (2.0 * T * L * E, (T * L + E * L) * bf + T * E * f4),
         "thresholds": (0.0, T * E * f4 + E * f4),
         "route": (0.0, T * E * f4 + E * f4 + T * K * 8),
-        "dispatch": (0.0, T * K * 4 + T * L * bf + T * K * L * bf + T * K * 4),
+        # indices only: idx read, per-block masks/bases, inv and source-token written
+        "dispatch": (0.0, T * K * 4 * 3 + 2 * ((T + 31) // 32) * E * 4),
+        # the latent rows are gathered inside the GEMM: read once (L2 serves the repeats)
         "expert_gate_up": (2.0 * T * K * L * 2 * I,
-                           touched * 2 * I * L * bf + T * K * L * bf + T * K * I * bf),
+                           touched * 2 * I * L * bf + T * L * bf + T * K * I * bf),
         "expert_down": (2.0 * T * K * I * L, touched * L * I * bf + T * K * (I + L) * bf),
         "combine": (0.0, T * K * L * bf + T * K * 8 + T * L * bf + L * f4),
         "output": (2.0 * T * (L + sw) * d,
