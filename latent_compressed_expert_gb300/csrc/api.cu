@@ -426,6 +426,7 @@ int lmoe_forward(const lmoe_dims* dims, const void* packed, const void* x, const
     g.err = err;
     g.timeout_ns = wait_limit_ns();
     g.max_ctas = routed_ctas;
+    g.mean_tokens = static_cast<int>(static_cast<int64_t>(TK) / D.E);
     rc = launch_grouped_gemm(pk + P.wgu, lat, static_cast<uint64_t>(T), D.L, g, stream);
     if (rc != LMOE_OK) return rc;
   }
@@ -446,6 +447,7 @@ int lmoe_forward(const lmoe_dims* dims, const void* packed, const void* x, const
     g.err = err;
     g.timeout_ns = wait_limit_ns();
     g.max_ctas = routed_ctas;
+    g.mean_tokens = static_cast<int>(static_cast<int64_t>(TK) / D.E);
     rc = launch_grouped_gemm(pk + P.wed, h, static_cast<uint64_t>(TK), D.I, g, stream);
     if (rc != LMOE_OK) return rc;
   }

@@ -34,7 +34,10 @@ constexpr int DISPATCH_TOKENS = 32;
 // Largest token count (MMA N) of one routed-expert GEMM tile; an expert's token rows are cut
 // into chunks of at most this many.  192 covers the K3 prefill load (146 on average, under
 // 1.2x that at most with Quantile-Balancing thresholds) in one chunk.
-constexpr int GROUPED_TOKN = 192;
+#ifndef LMOE_GROUPED_TOKN
+#define LMOE_GROUPED_TOKN 192
+#endif
+constexpr int GROUPED_TOKN = LMOE_GROUPED_TOKN;
 
 __host__ __device__ inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 

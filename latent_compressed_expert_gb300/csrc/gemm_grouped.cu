@@ -27,13 +27,25 @@
 
 namespace lmoe {
 
+constexpr int GROUPED_BOX_T = 32;  // token rows per TMA box / padding granule of N
+
+// Pipeline depth (shared-memory stages of one weight box + one token tile).  Measured at
+// the K3 shapes: the gate/value GEMM (long K, gathered rows) is fastest with the deepest ring
+// that fits (1.19 ms at 5 stages vs 1.28 at 4, prefill); the down GEMM (K = 512, writing the
+// expert outputs) with one stage less when experts see many tokens (0.75 ms at 4 vs 0.82 at
+// 5, prefill) but not at decode (~1 token per expert: 0.37 ms at 5 vs 0.39 at 4).
+constexpr int GROUPED_STAGES_DEEP = 5;
+constexpr int GROUPED_STAGES_SHALLOW = 4;
+constexpr int GROUPED_SHALLOW_MIN_TOKENS = 32;
+
+template <int STAGES_>
 struct GroupedCfg {
   static constexpr int TOKN = GROUPED_TOKN;               // max tokens (N) per tile
-  static constexpr int BOX_T = 32;                        // token rows per TMA box
+  static constexpr int BOX_T = GROUPED_BOX_T;             // token rows per TMA box
   static constexpr int A_BYTES = BLOCK_M * BLOCK_K * 2;   // 16 KB of weights
   static constexpr int B_BYTES = TOKN * BLOCK_K * 2;      // up to 24 KB of activations
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES = 5;
+  static constexpr int STAGES = STAGES_;
   static constexpr int ACC_COLS = 256;                    // TMEM columns between accumulators
   static constexpr int TMEM_COLS = 512;
   static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
@@ -77,10 +89,10 @@ __device__ __forceinline__ GTile decode_gtile(const GroupedArgs& g, int mt, int 
   GTile t;
   t.r0 = m * BLOCK_M;
   t.w_row = (e * mt + m) * (g.Kd / BLOCK_K) * BLOCK_M;
-  t.tok0 = __ldg(g.seg_off + e) + chunk * GroupedCfg::TOKN;
+  t.tok0 = __ldg(g.seg_off + e) + chunk * GROUPED_TOKN;
   const int end = __ldg(g.seg_off + e + 1);
-  t.ntok = min(GroupedCfg::TOKN, end - t.tok0);
-  t.npad = (t.ntok + GroupedCfg::BOX_T - 1) / GroupedCfg::BOX_T * GroupedCfg::BOX_T;
+  t.ntok = min(GROUPED_TOKN, end - t.tok0);
+  t.npad = (t.ntok + GROUPED_BOX_T - 1) / GROUPED_BOX_T * GROUPED_BOX_T;
   return t;
 }
 
@@ -106,10 +118,11 @@ __device__ __forceinline__ float situ_g(float g, float v, float c, float inv_c) 
   return __fdividef(gc, 1.0f + __expf(fminf(-gc, 80.0f))) * vc;
 }
 
+template <int STAGES_>
 __global__ void __launch_bounds__(GROUPED_THREADS, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
                     const __grid_constant__ CUtensorMap tmX, const GroupedArgs g) {
-  using C = GroupedCfg;
+  using C = GroupedCfg<STAGES_>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = ptx::smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -160,6 +173,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------ TMA producer
+      const uint64_t w_policy = ptx::l2_policy_evict_first();  // for weights read once
       uint32_t it = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
@@ -177,7 +191,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
           uint8_t* sa = smem + s * C::STAGE_BYTES;
           uint8_t* sb = sa + C::A_BYTES;
           ptx::mbar_arrive_expect_tx(&full[s], bytes);
-          ptx::tma_load_2d(sa, &tmW, &full[s], 0, t.w_row + kb * BLOCK_M);
+          if (g.evict_first)
+            ptx::tma_load_2d_hint(sa, &tmW, &full[s], 0, t.w_row + kb * BLOCK_M, w_policy);
+          else
+            ptx::tma_load_2d(sa, &tmW, &full[s], 0, t.w_row + kb * BLOCK_M);
           for (int b = 0; b < nbox; ++b)
             ptx::tma_load_2d(sb + b * C::BOX_T * BLOCK_K * 2, &tmX, &full[s], kb * BLOCK_K,
                              t.tok0 + b * C::BOX_T);
@@ -329,9 +346,24 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
   }
 }
 
+template <int STAGES_>
+static int launch_grouped_stages(const CUtensorMap& tw, const CUtensorMap& tx,
+                                 const GroupedArgs& g, cudaStream_t stream) {
+  using C = GroupedCfg<STAGES_>;
+  if (cudaFuncSetAttribute(grouped_gemm_kernel<STAGES_>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) != cudaSuccess)
+    return LMOE_ERR_CUDA;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return LMOE_ERR_CUDA;
+  const int grid = (g.max_ctas > 0 && g.max_ctas < sms) ? g.max_ctas : sms;
+  grouped_gemm_kernel<STAGES_><<<grid, GROUPED_THREADS, C::SMEM_BYTES, stream>>>(tw, tx, g);
+  return cudaGetLastError() == cudaSuccess ? LMOE_OK : LMOE_ERR_CUDA;
+}
+
 int launch_grouped_gemm(const void* W, const void* X, uint64_t x_rows, int x_ld,
                         const GroupedArgs& g, cudaStream_t stream) {
-  using C = GroupedCfg;
   if (g.M_w <= 0 || g.Kd % BLOCK_K != 0 || g.Kd <= 0 || x_rows == 0) return LMOE_ERR_UNSUPPORTED;
   if (g.epi != EPI_SITU && g.epi != EPI_BF16) return LMOE_ERR_UNSUPPORTED;
   if (g.epi == EPI_SITU && g.M_w % BLOCK_M != 0) return LMOE_ERR_UNSUPPORTED;
@@ -340,18 +372,17 @@ int launch_grouped_gemm(const void* W, const void* X, uint64_t x_rows, int x_ld,
                           (g.Kd / BLOCK_K) * BLOCK_M;  // tiled: rows of 64 bf16
   if (!make_tmap_bf16(&tw, W, w_rows, BLOCK_K, BLOCK_K, BLOCK_M) ||
       !make_tmap_bf16(&tx, X, x_rows, static_cast<uint64_t>(g.Kd), static_cast<uint64_t>(x_ld),
-                      C::BOX_T))
+                      GROUPED_BOX_T))
     return LMOE_ERR_CUDA;
-  if (cudaFuncSetAttribute(grouped_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           C::SMEM_BYTES) != cudaSuccess)
-    return LMOE_ERR_CUDA;
-  int dev = 0, sms = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-    return LMOE_ERR_CUDA;
-  const int grid = (g.max_ctas > 0 && g.max_ctas < sms) ? g.max_ctas : sms;
-  grouped_gemm_kernel<<<grid, GROUPED_THREADS, C::SMEM_BYTES, stream>>>(tw, tx, g);
-  return cudaGetLastError() == cudaSuccess ? LMOE_OK : LMOE_ERR_CUDA;
+  const bool shallow = g.epi != EPI_SITU && g.mean_tokens >= GROUPED_SHALLOW_MIN_TOKENS;
+  // Each weight byte is read exactly once: marking it evict-first keeps the token rows, which
+  // every weight row tile of an expert re-reads, in L2 (gate/value 1.20 -> 1.11 ms at the K3
+  // prefill shape).  The down GEMM at prefill measured no gain (its output write-back shares
+  // L2), so it keeps the default policy there.
+  GroupedArgs ga = g;
+  ga.evict_first = (g.epi == EPI_SITU || !shallow) ? 1 : 0;
+  return shallow ? launch_grouped_stages<GROUPED_STAGES_SHALLOW>(tw, tx, ga, stream)
+                 : launch_grouped_stages<GROUPED_STAGES_DEEP>(tw, tx, ga, stream);
 }
 
 }  // namespace lmoe

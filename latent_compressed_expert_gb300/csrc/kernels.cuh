@@ -76,6 +76,8 @@ struct GroupedArgs {
   uint32_t* err;
   unsigned long long timeout_ns;
   int max_ctas;           // persistent grid limit (0: one CTA per SM)
+  int mean_tokens;        // average tokens per expert (T*K/E): picks the pipeline depth
+  int evict_first;        // set by the launcher: weights loaded with an L2 evict-first policy
 };
 
 // W: the experts' weights in 128 x 64 tiles ordered (expert, row tile, column tile).
