@@ -9,7 +9,9 @@ outliers); in-batch Quantile-Balancing thresholds; residual = x.  Synthetic data
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
 Prints one JSON line (rank 0).  Under torchrun each rank runs its own batch on its own GPU
-(weak scaling, no collective on the data path); the time is the max over ranks.
+(weak scaling); the time is the max over ranks.  By default each rank solves its own
+thresholds (no collective on the data path); ``--qb global`` solves one set over all
+ranks' batches (router phase, all-gather of threshold candidates, experts phase).
 ``--impl reference`` times the CPU oracle (the only reference there is) on host cores.
 """
 from __future__ import annotations
@@ -84,27 +86,42 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_source_hash() -> str:
+# The source files that define each stage's kernel and its launch configuration (the
+# launcher sits in the kernel's own .cu), plus the headers every kernel includes.
+_COMMON_SRC = ("common.cuh", "kernels.cuh", "ptx.cuh", "lmoe.h")
+STAGE_SOURCES = {
+    "latent_shared": ("gemm.cu",), "router": ("gemm.cu",), "output": ("gemm.cu",),
+    "thresholds": ("routing.cu",), "route": ("routing.cu",), "dispatch": ("dispatch.cu",),
+    "expert_gate_up": ("gemm_grouped.cu",), "expert_down": ("gemm_grouped.cu",),
+    "combine": ("dispatch.cu",),
+}
+
+
+def kernel_source_hash(stage: str) -> str:
+    """Hash of the sources of one stage's kernel: a stored ncu figure is valid while it
+    matches."""
     h = hashlib.sha256()
-    for p in sorted(glob.glob(os.path.join(ROOT, "latent_compressed_expert_gb300", "csrc", "*"))):
-        with open(p, "rb") as f:
-            h.update(os.path.basename(p).encode())
+    for name in sorted(STAGE_SOURCES[stage] + _COMMON_SRC):
+        path = os.path.join(ROOT, "include" if name.endswith(".h") else
+                            os.path.join("latent_compressed_expert_gb300", "csrc"), name)
+        with open(path, "rb") as f:
+            h.update(name.encode())
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
 def ncu_traffic(stage: str):
     """DRAM bytes per launch of a stage's kernel from a committed ncu summary, if it was
-    captured from the current kernel sources; else None."""
+    captured from the current sources of that kernel; else None."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         t = json.load(f)
-    if t.get("kernel_source_hash") != kernel_source_hash():
-        return None
     s = t.get("stages", {}).get(stage)
-    return None if s is None else float(s["dram_bytes_per_launch"])
+    if s is None or s.get("kernel_source_hash") != kernel_source_hash(stage):
+        return None
+    return float(s["dram_bytes_per_launch"])
 
 
 # ----------------------------------------------------------------------------------------
@@ -241,8 +258,9 @@ DESCRIPTIONS = {
 class Workload:
     """Inputs and routing arguments of one bench configuration."""
 
-    def __init__(self, name, dev, rank, overlap=False, shared_sms=0):
+    def __init__(self, name, dev, rank, overlap=False, shared_sms=0, qb="local", world=1):
         self.name = name
+        self.qb = qb
         self.sh = sh = SHAPES[name]
         outliers = name in ("prefill", "small")
         gain = synth.outlier_router_gain(sh, OUTLIER_FRAC, OUTLIER_SCALE) if outliers else 1.0
@@ -254,6 +272,11 @@ class Workload:
                                 overlap=overlap, shared_sms=shared_sms)
         self.kwargs = {}
         self.extra = {}
+        if qb == "global":
+            if name not in ("prefill", "e64", "small"):
+                raise ValueError("--qb global applies to the in-batch-threshold workloads")
+            # thresholds over all ranks' batches together (all-gather of candidates)
+            self.kwargs["global_tokens"] = sh.T * world
         if name == "decode":
             # thresholds of a prefill batch through the same layer
             xp = synth.make_x(sh, SEED + 7, device=dev, T=8192)
@@ -274,6 +297,8 @@ class Workload:
             del dbg, plain
 
     def forward(self, **kw):
+        if self.qb == "global":
+            return self.layer.forward_global(self.x, residual=self.x, **self.kwargs, **kw)
         return self.layer.forward(self.x, residual=self.x, **self.kwargs, **kw)
 
     def config(self, world):
@@ -283,7 +308,10 @@ class Workload:
                             f"(I_s={sh.Is}), routed I={sh.I}",
                 "shape": self.name, "tokens_per_gpu": sh.T, "global_tokens": sh.T * world,
                 "l2": "inputs larger than L2: the expert weights streamed per step exceed it",
-                "parallelism": f"replicas x{world}, independent batches",
+                "parallelism": f"replicas x{world}, independent batches" if self.qb == "local"
+                               else f"data parallel x{world}, Quantile-Balancing thresholds over "
+                                    f"the {sh.T * world}-token global batch (all-gather of "
+                                    f"per-rank candidates)",
                 "shared_experts": "in line" if not self.layer.overlap else
                                   f"second stream, {self.layer.shared_sms or 'default'} SMs"}
 
@@ -344,7 +372,8 @@ def run_ours(args):
     if not torch.cuda.is_available():
         raise RuntimeError("bench.py needs a CUDA GPU (the layer has no CPU path)")
     dev = torch.device("cuda", local)
-    wl = Workload(args.shape, dev, rank, overlap=args.overlap, shared_sms=args.shared_sms)
+    wl = Workload(args.shape, dev, rank, overlap=args.overlap, shared_sms=args.shared_sms,
+                  qb=args.qb, world=world)
     sh, layer, x, w = wl.sh, wl.layer, wl.x, wl.w
     y = torch.empty_like(x)
     stream = torch.cuda.current_stream()
@@ -389,13 +418,13 @@ def run_ours(args):
     y_host = torch.empty_like(x_host).pin_memory()
     x_dev = torch.empty_like(x)
     for _ in range(max(1, args.warmup)):
-        layer.forward_host(x_host, y_host, x_dev, y, **wl.kwargs)
+        layer.forward_host(x_host, y_host, x_dev, y, qb=wl.qb, **wl.kwargs)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     barrier(world)
     e0.record(stream)
     for _ in range(args.steps):
-        layer.forward_host(x_host, y_host, x_dev, y, **wl.kwargs)
+        layer.forward_host(x_host, y_host, x_dev, y, qb=wl.qb, **wl.kwargs)
     e1.record(stream)
     torch.cuda.synchronize()
     barrier(world)
@@ -487,6 +516,9 @@ def main():
                     help="run the shared experts on a second stream beside the routed path")
     ap.add_argument("--shared-sms", type=int, default=0,
                     help="SMs for the shared experts when they overlap (0: library default)")
+    ap.add_argument("--qb", choices=["local", "global"], default="local",
+                    help="thresholds per rank's batch (local) or over all ranks' batches "
+                         "(global: router phase, all-gather of candidates, experts phase)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
     return run_reference(args) if args.impl == "reference" else run_ours(args)

@@ -91,7 +91,7 @@ enum lmoe_stage {
   LMOE_STAGE_ROUTER = 1,        /* router logits (skipped when logits_in is given) */
   LMOE_STAGE_THRESHOLDS = 2,    /* in-batch Quantile-Balancing thresholds (when solved) */
   LMOE_STAGE_ROUTE = 3,         /* top-K selection and gates */
-  LMOE_STAGE_DISPATCH = 4,      /* expert segments and the permuted latent */
+  LMOE_STAGE_DISPATCH = 4,      /* expert segments: token indices per expert */
   LMOE_STAGE_EXPERT_GATE_UP = 5,/* grouped gate/value GEMM with SiTU-GLU */
   LMOE_STAGE_EXPERT_DOWN = 6,   /* grouped down-projection GEMM */
   LMOE_STAGE_COMBINE = 7,       /* gate-weighted aggregation + RMSNorm */
@@ -121,7 +121,25 @@ typedef struct lmoe_io {
                             the output GEMM, so the call stays ordered on `stream` */
   void *aux_events[2];   /* two cudaEvent_t handles (fork, join), required with aux_stream */
   int shared_sms;        /* SMs for the shared experts while they overlap (0: a third) */
+  int phase;             /* LMOE_PHASE_*: the whole layer (0), or one of its two halves */
+  float *cand_out;       /* LMOE_PHASE_ROUTER only: [cand_k, E] threshold candidates of this
+                            batch, as lmoe_threshold_candidates writes them */
+  int cand_k;            /* rank the candidates serve (required with cand_out, >= 1) */
 } lmoe_io;
+
+/* lmoe_io.phase.  The layer splits where its only cross-batch quantity, the thresholds, is
+ * needed: a batch spread over several ranks solves one threshold set over all of them by
+ * running LMOE_PHASE_ROUTER on each rank (with cand_out), exchanging the candidates (an
+ * all-gather), reducing them with lmoe_thresholds, and running LMOE_PHASE_EXPERTS with the
+ * result as tau_in.  LMOE_PHASE_EXPERTS continues from the workspace that a
+ * LMOE_PHASE_ROUTER call with the same dims, packed weights, io->logits_in, io->aux_stream
+ * and io->aux_events left on the same stream; it does not read x (which may be NULL).
+ * Together the two phases compute what LMOE_PHASE_ALL computes. */
+enum lmoe_phase {
+  LMOE_PHASE_ALL = 0,      /* stages LATENT_SHARED .. OUTPUT */
+  LMOE_PHASE_ROUTER = 1,   /* stages LATENT_SHARED and ROUTER (+ candidates) */
+  LMOE_PHASE_EXPERTS = 2   /* stages THRESHOLDS .. OUTPUT */
+};
 
 /* Batches at least this large run the shared experts concurrently when lmoe_io.aux_stream is
  * given; the workspace of such batches holds their fp32 output [T, d]. */
@@ -152,6 +170,21 @@ size_t lmoe_workspace_bytes(const lmoe_dims *dims);
  * Errors: INVALID_ARG for null pointers or T < 0, E < 1, K < 1, k_rank > T. */
 int lmoe_thresholds(const float *logits, int T, int E, int K, int k_rank, float *tau,
                     void *stream);
+
+/* Threshold candidates of one part of a batch that is spread over several ranks.
+ * [IK3] Quantile Balancing passage: the threshold is read off the distribution of the
+ * scores of the whole step's batch; the pages do not say how a batch split across devices
+ * obtains it.  Reading: the k largest scores of a column over the whole batch lie among the
+ * k largest of each part, so each part contributes those.  Column e of cand receives the
+ * logits of the min(k, T) tokens with the largest scores s = sigmoid(logit) of expert e
+ * (scores above the min(k, T)-th largest first, then tokens whose score equals it, each
+ * group in token order), and rows T..k-1, when T < k, receive -FLT_MAX (the lowest score).
+ * Stacking the candidates of all parts as [parts * k, E] and calling lmoe_thresholds on
+ * them with k_rank = k gives, bit for bit, the thresholds of the whole batch.
+ *   logits [T, E] fp32 (read), cand [k, E] fp32 (written).  T == 0 fills cand with -FLT_MAX.
+ * Errors: INVALID_ARG for null pointers, T < 0, E < 1, k < 1. */
+int lmoe_threshold_candidates(const float *logits, int T, int E, int k, float *cand,
+                              void *stream);
 
 /* Top-K routing.  [TPP] Technical Details: a lightweight router selects 16 of 896 routed
  * experts per token; [SU]: Quantile Balancing replaces the predecessor's bias updates.

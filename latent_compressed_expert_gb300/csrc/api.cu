@@ -178,6 +178,13 @@ int lmoe_thresholds(const float* logits, int T, int E, int K, int k_rank, float*
   return launch_thresholds(logits, T, E, E, 1, k, tau, static_cast<cudaStream_t>(stream));
 }
 
+int lmoe_threshold_candidates(const float* logits, int T, int E, int k, float* cand,
+                              void* stream) {
+  if (T < 0 || E < 1 || k < 1 || !cand || (T > 0 && !logits)) return LMOE_ERR_INVALID_ARG;
+  // token-major input: each expert's column is read with stride E
+  return launch_candidates(logits, T, E, E, 1, k, cand, E, static_cast<cudaStream_t>(stream));
+}
+
 int lmoe_route(const float* logits, const float* tau, int T, int E, int K, int32_t* idx,
                float* gate, float* scores_out, void* stream) {
   if (T < 0 || E < 1 || K < 1) return LMOE_ERR_INVALID_ARG;
@@ -224,17 +231,28 @@ int lmoe_forward(const lmoe_dims* dims, const void* packed, const void* x, const
   int rc = dims_supported(dims);
   if (rc != LMOE_OK) return rc;
   const lmoe_dims D = *dims;
-  if (D.T == 0) return LMOE_OK;
-  if (!packed || !x || !y || !workspace) return LMOE_ERR_INVALID_ARG;
-  if (!aligned16(packed) || !aligned16(x) || !aligned16(y) || !aligned16(workspace) ||
-      (residual && !aligned16(residual)))
-    return LMOE_ERR_INVALID_ARG;
-  if (y == x || (residual && y == residual)) return LMOE_ERR_INVALID_ARG;
-  const WorkspaceLayout W = workspace_layout(D);
-  if (ws_bytes < W.total) return LMOE_ERR_WORKSPACE_TOO_SMALL;
   lmoe_io opt{};
   opt.balance = 1;
   if (io) opt = *io;
+  if (opt.phase < LMOE_PHASE_ALL || opt.phase > LMOE_PHASE_EXPERTS) return LMOE_ERR_INVALID_ARG;
+  // front: latent/shared GEMM and router; back: thresholds through the output GEMM
+  const bool front = opt.phase != LMOE_PHASE_EXPERTS;
+  const bool back = opt.phase != LMOE_PHASE_ROUTER;
+  if (opt.cand_out && (opt.phase != LMOE_PHASE_ROUTER || opt.cand_k < 1))
+    return LMOE_ERR_INVALID_ARG;
+  if (D.T == 0) {
+    if (opt.cand_out)
+      return launch_candidates(nullptr, 0, D.E, D.E, 1, opt.cand_k, opt.cand_out, D.E,
+                               static_cast<cudaStream_t>(stream_));
+    return LMOE_OK;
+  }
+  if (!packed || !workspace || (front && !x) || (back && !y)) return LMOE_ERR_INVALID_ARG;
+  if (!aligned16(packed) || !aligned16(workspace) || (front && !aligned16(x)) ||
+      (back && !aligned16(y)) || (residual && !aligned16(residual)))
+    return LMOE_ERR_INVALID_ARG;
+  if (back && ((x && y == x) || (residual && y == residual))) return LMOE_ERR_INVALID_ARG;
+  const WorkspaceLayout W = workspace_layout(D);
+  if (ws_bytes < W.total) return LMOE_ERR_WORKSPACE_TOO_SMALL;
   if ((opt.tau_in && !aligned16(opt.tau_in)) || (opt.logits_in && !aligned16(opt.logits_in)))
     return LMOE_ERR_INVALID_ARG;
 
@@ -258,8 +276,9 @@ int lmoe_forward(const lmoe_dims* dims, const void* packed, const void* x, const
   const int ldz = D.L + sw;
   const int T = D.T, TK = D.T * D.K;
 
-  if (cudaMemsetAsync(err, 0, sizeof(uint32_t), stream) != cudaSuccess) return LMOE_ERR_CUDA;
-  if (!mark(LMOE_STAGE_LATENT_SHARED, 0)) return LMOE_ERR_CUDA;
+  if (front && cudaMemsetAsync(err, 0, sizeof(uint32_t), stream) != cudaSuccess)
+    return LMOE_ERR_CUDA;
+  if (front && !mark(LMOE_STAGE_LATENT_SHARED, 0)) return LMOE_ERR_CUDA;
 
   int dev_sms = 0;
   {
@@ -283,7 +302,9 @@ int lmoe_forward(const lmoe_dims* dims, const void* packed, const void* x, const
     ys = reinterpret_cast<float*>(ws + W.ys);
   }
 
-  if (!overlap) {
+  if (!front) {
+    // LMOE_PHASE_EXPERTS: the latent, shared activations and logits are in the workspace
+  } else if (!overlap) {
     // 1. x . [W_down ; W_shared_gate/value]^T: latent (bf16) and SiTU(shared) into zh[:, L:]
     GemmArgs g = gemm_defaults(err, D.c);
     g.M = T;
@@ -350,12 +371,23 @@ int lmoe_forward(const lmoe_dims* dims, const void* packed, const void* x, const
     }
     launches += 3;
   }
-  if (!mark(LMOE_STAGE_ROUTER, 0)) return LMOE_ERR_CUDA;
+  if (front && !mark(LMOE_STAGE_ROUTER, 0)) return LMOE_ERR_CUDA;
   // 2. router logits = lat . W_r^T (fp32), unless the caller supplies them
-  const float* logits = opt.logits_in;
+  const float* logits =
+      opt.logits_in ? opt.logits_in : reinterpret_cast<const float*>(ws + W.logits);
   float* logits_t = reinterpret_cast<float*>(ws + W.logits_t);  // expert-major copy
   const bool solve_tau = !opt.tau_in && opt.balance;
-  if (!logits) {
+  // who needs the expert-major copy: in-batch thresholds of a whole-layer call, or the
+  // candidates of a router phase (an experts phase makes its own when it solves thresholds)
+  const bool want_t =
+      (opt.phase == LMOE_PHASE_ALL && solve_tau) || (opt.phase == LMOE_PHASE_ROUTER && opt.cand_out);
+  if (!front) {
+    if (solve_tau) {
+      rc = launch_transpose_f32(logits, T, D.E, logits_t, stream);
+      if (rc != LMOE_OK) return rc;
+      launches += 1;
+    }
+  } else if (!opt.logits_in) {
     GemmArgs g = gemm_defaults(err, D.c);
     g.M = T;
     g.N = D.E;
@@ -364,18 +396,33 @@ int lmoe_forward(const lmoe_dims* dims, const void* packed, const void* x, const
     g.outf = reinterpret_cast<float*>(ws + W.logits);
     g.ldf = D.E;
     g.max_ctas = routed_ctas;
-    if (solve_tau) {
+    if (want_t) {
       g.outf_t = logits_t;
       g.ldt = T;
     }
     rc = launch_gemm(lat, T, D.L, pk + P.wr, static_cast<uint64_t>(D.E), D.L, g, stream);
     if (rc != LMOE_OK) return rc;
-    logits = g.outf;
     launches += 1;
-  } else if (solve_tau) {
+  } else if (want_t) {
     rc = launch_transpose_f32(logits, T, D.E, logits_t, stream);
     if (rc != LMOE_OK) return rc;
     launches += 1;
+  }
+  auto copy = [&](void* dst, const void* src, size_t bytes) {
+    return cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, stream) == cudaSuccess;
+  };
+  if (!back) {
+    // LMOE_PHASE_ROUTER ends here, with the candidates this batch contributes
+    if (opt.cand_out) {
+      rc = launch_candidates(logits_t, T, D.E, 1, T, opt.cand_k, opt.cand_out, D.E, stream);
+      if (rc != LMOE_OK) return rc;
+      launches += 1;
+    }
+    if (!mark(LMOE_STAGE_THRESHOLDS, 0)) return LMOE_ERR_CUDA;
+    if (io) io->kernel_launches = launches;
+    if (opt.logits_out && !copy(opt.logits_out, logits, static_cast<size_t>(T) * D.E * 4))
+      return LMOE_ERR_CUDA;
+    return LMOE_OK;
   }
   if (!mark(LMOE_STAGE_THRESHOLDS, 0)) return LMOE_ERR_CUDA;
   // 3. thresholds
@@ -484,9 +531,6 @@ int lmoe_forward(const lmoe_dims* dims, const void* packed, const void* x, const
   if (!mark(LMOE_NUM_STAGES, 1)) return LMOE_ERR_CUDA;
   if (io) io->kernel_launches = launches;
   // debug outputs
-  auto copy = [&](void* dst, const void* src, size_t bytes) {
-    return cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, stream) == cudaSuccess;
-  };
   if (opt.logits_out && !copy(opt.logits_out, logits, static_cast<size_t>(T) * D.E * 4))
     return LMOE_ERR_CUDA;
   if (opt.tau_out) {

@@ -98,6 +98,10 @@ int launch_route(const float* logits, const float* tau, int T, int E, int K, int
 // (stride_t = 1, stride_e = T is the fast, expert-major layout).
 int launch_thresholds(const float* z, int T, int E, int64_t stride_t, int64_t stride_e, int k,
                       float* tau, cudaStream_t stream);
+// Per expert, the logits of the min(k, T) largest scores (rows of cand, stride ldc), then
+// -FLT_MAX up to row k.
+int launch_candidates(const float* z, int T, int E, int64_t stride_t, int64_t stride_e, int k,
+                      float* cand, int64_t ldc, cudaStream_t stream);
 // out[E, T] = in[T, E]^T (fp32).
 int launch_transpose_f32(const float* in, int T, int E, float* out, cudaStream_t stream);
 int launch_dispatch(const int32_t* idx, int T, int E, int K, uint32_t* masks, uint32_t* base,

@@ -11,6 +11,8 @@
 // Every decision here is taken in fp32 with explicitly rounded operations (__fmul_rn,
 // __fadd_rn, __fmaf_rn, __fdiv_rn), so that no contraction or approximation changes a
 // result bit: a CPU evaluation of the same sequence of IEEE operations agrees exactly.
+#include <cfloat>
+
 #include "common.cuh"
 #include "kernels.cuh"
 
@@ -162,18 +164,22 @@ constexpr int TH_BINS = 4096;
 constexpr int TH_CAND = 4096;
 constexpr int TH_SMEM_MAX_T = 32768;
 
-__global__ void __launch_bounds__(TH_THREADS)
-thresholds_kernel(const float* __restrict__ z, int T, int64_t stride_t, int64_t stride_e,
-                  int k, float* __restrict__ tau) {
-  extern __shared__ uint32_t th_smem[];
+struct KthResult {
+  uint32_t key;  // score bits of the k-th largest score of the column
+  int above;     // number of scores strictly greater than it (< k)
+};
+
+// k-th largest score (1 <= k <= T) of column `col` (T logits, stride stride_t).  Called by
+// all TH_THREADS threads of the CTA; `th_smem` is the layout launch_thresholds sizes.  When
+// the column is staged, vals[0..T) keeps the score bits on return.
+__device__ __forceinline__ KthResult select_kth_score(const float* __restrict__ col, int T,
+                                                     int64_t stride_t, int k,
+                                                     uint32_t* th_smem, bool staged) {
   uint32_t* hist = th_smem;                       // [TH_BINS]
-  uint32_t* ctl = th_smem + TH_BINS;              // [0] digit, [1] new k, [2] candidates
+  uint32_t* ctl = th_smem + TH_BINS;              // [0] digit, [1] new k, [2] in bin, [3] count
   uint32_t* cand = th_smem + TH_BINS + 32;        // [TH_CAND]
   uint32_t* vals = cand + TH_CAND;                // [T] when staged
-  const int e = blockIdx.x;
   const int lane = threadIdx.x & 31;
-  const float* col = z + static_cast<int64_t>(e) * stride_e;
-  const bool staged = T <= TH_SMEM_MAX_T;
   if (staged) {
     // eight independent loads in flight per thread before their scores are computed
     constexpr int B = 8;
@@ -272,7 +278,89 @@ thresholds_kernel(const float* __restrict__ z, int T, int64_t stride_t, int64_t 
     }
     __syncthreads();
   }
-  if (threadIdx.x == 0) tau[e] = __uint_as_float(prefix);
+  // after the last pass the selected bin is one key value; krem of its copies complete k
+  KthResult r;
+  r.key = prefix;
+  r.above = k - krem;
+  return r;
+}
+
+__global__ void __launch_bounds__(TH_THREADS)
+thresholds_kernel(const float* __restrict__ z, int T, int64_t stride_t, int64_t stride_e,
+                  int k, float* __restrict__ tau) {
+  extern __shared__ uint32_t th_smem[];
+  const int e = blockIdx.x;
+  const KthResult r = select_kth_score(z + static_cast<int64_t>(e) * stride_e, T, stride_t, k,
+                                       th_smem, T <= TH_SMEM_MAX_T);
+  if (threadIdx.x == 0) tau[e] = __uint_as_float(r.key);
+}
+
+// Threshold candidates of one batch: column e of cand ([k, E], row stride ldc) receives the
+// logits of the min(k, T) tokens with the largest scores of expert e -- first those whose
+// score is above the min(k, T)-th largest, then tokens whose score equals it, both in token
+// order -- and rows T..k-1 (when T < k) receive -FLT_MAX, whose score is the lowest any
+// logit has.  The k-th largest score of the union of several batches' candidates is the
+// k-th largest score of the union of the batches.
+__global__ void __launch_bounds__(TH_THREADS)
+candidates_kernel(const float* __restrict__ z, int T, int64_t stride_t, int64_t stride_e,
+                  int k, float* __restrict__ cand, int64_t ldc) {
+  extern __shared__ uint32_t th_smem[];
+  __shared__ uint32_t wsum[2][TH_THREADS / 32];
+  __shared__ uint32_t run[2];
+  const int e = blockIdx.x;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const float* col = z + static_cast<int64_t>(e) * stride_e;
+  const int kk = k < T ? k : T;
+  if (kk > 0) {
+  const bool staged = T <= TH_SMEM_MAX_T;
+  const KthResult r = select_kth_score(col, T, stride_t, kk, th_smem, staged);
+  const uint32_t* vals = th_smem + TH_BINS + 32 + TH_CAND;
+  const int take_eq = kk - r.above;  // copies of the k-th score to emit
+  if (threadIdx.x == 0) run[0] = run[1] = 0u;
+  __syncthreads();
+  // ordered compaction, TH_THREADS tokens per round: warp ballots, then a scan of the
+  // warps' counts; run[] carries the counts of earlier rounds
+  for (int t0 = 0; t0 < T; t0 += TH_THREADS) {
+    const int t = t0 + threadIdx.x;
+    bool gt = false, eq = false;
+    if (t < T) {
+      const uint32_t key =
+          staged ? vals[t] : __float_as_uint(score_sigmoid(__ldg(col + t * stride_t)));
+      gt = key > r.key;
+      eq = key == r.key;
+    }
+    const uint32_t bg = __ballot_sync(0xffffffffu, gt), be = __ballot_sync(0xffffffffu, eq);
+    if (lane == 0) {
+      wsum[0][warp] = __popc(bg);
+      wsum[1][warp] = __popc(be);
+    }
+    __syncthreads();
+    uint32_t pg = run[0], pe = run[1];
+    for (int w = 0; w < warp; ++w) {
+      pg += wsum[0][w];
+      pe += wsum[1][w];
+    }
+    const uint32_t below = (1u << lane) - 1u;
+    pg += __popc(bg & below);
+    pe += __popc(be & below);
+    if (gt) cand[static_cast<int64_t>(pg) * ldc + e] = __ldg(col + t * stride_t);
+    if (eq && pe < static_cast<uint32_t>(take_eq))
+      cand[static_cast<int64_t>(r.above + pe) * ldc + e] = __ldg(col + t * stride_t);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      uint32_t sg = 0u, se = 0u;
+      for (int w = 0; w < TH_THREADS / 32; ++w) {
+        sg += wsum[0][w];
+        se += wsum[1][w];
+      }
+      run[0] += sg;
+      run[1] += se;
+    }
+    __syncthreads();
+  }
+  }
+  for (int j = kk + threadIdx.x; j < k; j += TH_THREADS)
+    cand[static_cast<int64_t>(j) * ldc + e] = -FLT_MAX;
 }
 
 // out[E, T] = in[T, E]^T through 32 x 32 shared-memory tiles.
@@ -321,6 +409,20 @@ int launch_thresholds(const float* z, int T, int E, int64_t stride_t, int64_t st
       return LMOE_ERR_CUDA;
   }
   thresholds_kernel<<<E, TH_THREADS, smem, stream>>>(z, T, stride_t, stride_e, k, tau);
+  return cudaGetLastError() == cudaSuccess ? LMOE_OK : LMOE_ERR_CUDA;
+}
+
+int launch_candidates(const float* z, int T, int E, int64_t stride_t, int64_t stride_e, int k,
+                      float* cand, int64_t ldc, cudaStream_t stream) {
+  if (E == 0 || k == 0) return LMOE_OK;
+  const size_t smem =
+      (TH_BINS + 32 + TH_CAND + (T <= TH_SMEM_MAX_T ? T : 0)) * sizeof(uint32_t);
+  if (smem > 48 * 1024) {
+    if (cudaFuncSetAttribute(candidates_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess)
+      return LMOE_ERR_CUDA;
+  }
+  candidates_kernel<<<E, TH_THREADS, smem, stream>>>(z, T, stride_t, stride_e, k, cand, ldc);
   return cudaGetLastError() == cudaSuccess ? LMOE_OK : LMOE_ERR_CUDA;
 }
 

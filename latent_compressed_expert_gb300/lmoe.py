@@ -40,10 +40,14 @@ class IO(ctypes.Structure):
     _fields_ = [("tau_in", _vp), ("balance", _i), ("logits_in", _vp), ("logits_out", _vp),
                 ("tau_out", _vp), ("idx_out", _vp), ("gate_out", _vp), ("counts_out", _vp),
                 ("stage_events", ctypes.POINTER(_vp)), ("kernel_launches", _i),
-                ("aux_stream", _vp), ("aux_events", _vp * 2), ("shared_sms", _i)]
+                ("aux_stream", _vp), ("aux_events", _vp * 2), ("shared_sms", _i),
+                ("phase", _i), ("cand_out", _vp), ("cand_k", _i)]
 
 
 OVERLAP_MIN_T = 512  # LMOE_OVERLAP_MIN_T
+
+# enum lmoe_phase
+PHASE_ALL, PHASE_ROUTER, PHASE_EXPERTS = 0, 1, 2
 
 
 # enum lmoe_stage
@@ -57,6 +61,7 @@ SIGNATURES = {
     "lmoe_pack_weights": (_i, [ctypes.POINTER(Dims), ctypes.POINTER(Weights), _vp, _sz, _vp]),
     "lmoe_workspace_bytes": (_sz, [ctypes.POINTER(Dims)]),
     "lmoe_thresholds": (_i, [_vp, _i, _i, _i, _i, _vp, _vp]),
+    "lmoe_threshold_candidates": (_i, [_vp, _i, _i, _i, _vp, _vp]),
     "lmoe_route": (_i, [_vp, _vp, _i, _i, _i, _vp, _vp, _vp, _vp]),
     "lmoe_forward": (_i, [ctypes.POINTER(Dims), _vp, _vp, _vp, _vp, _vp, _sz, ctypes.POINTER(IO),
                           _vp]),
@@ -177,6 +182,45 @@ def thresholds(logits: torch.Tensor, K: int, k_rank: int = 0, stream=None) -> to
     return tau
 
 
+def fair_share_rank(T: int, K: int, E: int) -> int:
+    """The threshold's rank among a column's T scores: max(1, floor(T*K/E)), at most T."""
+    return max(1, min(T, (T * K) // E)) if T > 0 else 1
+
+
+def threshold_candidates(logits: torch.Tensor, k: int, stream=None) -> torch.Tensor:
+    """[k, E] candidates this batch contributes to thresholds solved over several batches
+    (lmoe_threshold_candidates)."""
+    T, E = logits.shape
+    _expect(logits, torch.float32, (T, E), "logits")
+    cand = torch.empty((k, E), dtype=torch.float32, device=logits.device)
+    _check(load().lmoe_threshold_candidates(_ptr(logits), T, E, k, _ptr(cand), _stream(stream)),
+           "lmoe_threshold_candidates")
+    return cand
+
+
+def gather_candidates(cand: torch.Tensor, group=None) -> torch.Tensor:
+    """All-gather every rank's [k, E] candidates into [world * k, E], rank order: the one
+    exchange of a batch spread over ranks.  torch.distributed moves the bytes."""
+    import torch.distributed as dist
+    if not dist.is_initialized() or dist.get_world_size(group) == 1:
+        return cand
+    world = dist.get_world_size(group)
+    parts = [torch.empty_like(cand) for _ in range(world)]
+    dist.all_gather(parts, cand.contiguous(), group=group)
+    return torch.cat(parts, dim=0)
+
+
+def global_token_count(T: int, device, group=None) -> int:
+    """Sum of the ranks' batch sizes."""
+    import torch.distributed as dist
+    if not dist.is_initialized():
+        return T
+    dev = device if dist.get_backend(group) == "nccl" else "cpu"
+    t = torch.tensor([T], dtype=torch.int64, device=dev)
+    dist.all_reduce(t, group=group)
+    return int(t.item())
+
+
 def route(logits: torch.Tensor, tau, K: int, want_scores: bool = False, stream=None):
     """Returns (idx int32 [T,K], gate fp32 [T,K]) and, with want_scores, scores [T,E]."""
     T, E = logits.shape
@@ -239,10 +283,13 @@ class Layer:
     def forward(self, x: torch.Tensor, residual: torch.Tensor | None = None, y=None,
                 tau: torch.Tensor | None = None, balance: bool = True,
                 logits_in: torch.Tensor | None = None, debug: bool = False, stream=None,
-                stage_events=None):
+                stage_events=None, phase: int = PHASE_ALL, cand_k: int = 0):
         """One lmoe_forward call.  stage_events: optional list of NUM_STAGES + 1
         torch.cuda.Event(enable_timing=True) recorded at the stage boundaries.  After the
-        call, ``self.last_kernel_launches`` holds the number of kernels it launched."""
+        call, ``self.last_kernel_launches`` holds the number of kernels it launched.
+        phase: PHASE_ALL, or one half of the layer: PHASE_ROUTER (returns the [cand_k, E]
+        threshold candidates when cand_k > 0, else None) then PHASE_EXPERTS (x gives the
+        batch size only)."""
         sh = self.shape
         T = x.shape[0]
         if T > self.max_tokens:
@@ -255,6 +302,12 @@ class Layer:
         dims = dims_of(sh, T=T)
         io = IO()
         io.balance = 1 if balance else 0
+        io.phase = phase
+        cand = None
+        if phase == PHASE_ROUTER and cand_k > 0:
+            cand = torch.empty((cand_k, sh.E), dtype=torch.float32, device=x.device)
+            io.cand_out = _ptr(cand)
+            io.cand_k = cand_k
         if self.overlap and T >= OVERLAP_MIN_T and T <= self.max_tokens:
             io.aux_stream = ctypes.c_void_p(self.aux_stream.cuda_stream)
             io.aux_events[0] = self.aux_events[0].cuda_event
@@ -293,16 +346,46 @@ class Layer:
                                    _ptr(y), _ptr(self.workspace), self.ws_bytes,
                                    ctypes.byref(io), _stream(stream)), "lmoe_forward")
         self.last_kernel_launches = io.kernel_launches
+        if phase == PHASE_ROUTER:
+            return (cand, dbg) if debug else cand
         return (y, dbg) if debug else y
 
+    def forward_global(self, x: torch.Tensor, residual: torch.Tensor | None = None, y=None,
+                       group=None, global_tokens: int | None = None, debug: bool = False,
+                       stage_events=None):
+        """The layer on this rank's part of a batch spread over the ranks of ``group``, with
+        one set of Quantile-Balancing thresholds solved over the whole batch: router phase
+        with candidates, all-gather of the candidates, lmoe_thresholds on them, experts
+        phase.  Runs on the current stream (the collectives order against it)."""
+        sh = self.shape
+        T = x.shape[0]
+        Tg = global_token_count(T, x.device, group) if global_tokens is None else global_tokens
+        k = fair_share_rank(Tg, sh.K, sh.E)
+        r = self.forward(x, phase=PHASE_ROUTER, cand_k=k, debug=debug, stage_events=stage_events)
+        launches = self.last_kernel_launches
+        cand, dbg0 = r if debug else (r, None)
+        tau = thresholds(gather_candidates(cand, group), sh.K, k_rank=k)
+        out = self.forward(x, residual, y, tau=tau, phase=PHASE_EXPERTS, debug=debug,
+                           stage_events=stage_events)
+        self.last_kernel_launches += launches + 1
+        if debug:
+            out[1]["logits"] = dbg0["logits"]
+            out[1]["candidates"] = cand
+        return out
+
     def forward_host(self, x_host: torch.Tensor, y_host: torch.Tensor, x_dev: torch.Tensor,
-                     y_dev: torch.Tensor, residual_from_x: bool = True, stream=None, **kw):
+                     y_dev: torch.Tensor, residual_from_x: bool = True, stream=None,
+                     qb: str = "local", **kw):
         """End-to-end call from host memory: copy x (pinned host) to the device, run the
         layer, copy y back to pinned host memory; all on one stream, asynchronous.  Extra
-        keyword arguments (tau, balance, logits_in) go to ``forward``."""
+        keyword arguments go to ``forward`` (tau, balance, logits_in), or, with
+        qb="global", to ``forward_global`` (group, global_tokens)."""
         x_dev.copy_(x_host, non_blocking=True)
-        self.forward(x_dev, residual=x_dev if residual_from_x else None, y=y_dev, stream=stream,
-                     **kw)
+        resid = x_dev if residual_from_x else None
+        if qb == "global":
+            self.forward_global(x_dev, resid, y=y_dev, **kw)
+        else:
+            self.forward(x_dev, residual=resid, y=y_dev, stream=stream, **kw)
         y_host.copy_(y_dev, non_blocking=True)
         return y_host
 

@@ -128,3 +128,38 @@ def test_binding_refuses_cpu_tensors(lib):
     logits = torch.zeros(4, 16)
     with pytest.raises(ValueError):
         lmoe.route(logits, None, 4)
+
+
+@no_gpu
+def test_phase_and_candidate_argument_checks(lib):
+    d = lmoe.dims_of(synth.TINY)
+    fake = ctypes.c_void_p(0x1000)
+    ws = lmoe.workspace_bytes(d)
+
+    def fwd(x, y, **fields):
+        io = lmoe.IO()
+        io.balance = 1
+        for k, v in fields.items():
+            setattr(io, k, v)
+        return lib.lmoe_forward(ctypes.byref(d), fake, x, None, y, ctypes.c_void_p(0x4000), ws,
+                                ctypes.byref(io), None)
+
+    assert fwd(fake, ctypes.c_void_p(0x2000), phase=3) == lmoe.LMOE_ERR_INVALID_ARG
+    assert fwd(fake, ctypes.c_void_p(0x2000), phase=-1) == lmoe.LMOE_ERR_INVALID_ARG
+    # candidates only come out of the router phase, and need their rank
+    assert fwd(fake, ctypes.c_void_p(0x2000), cand_out=0x5000, cand_k=4) \
+        == lmoe.LMOE_ERR_INVALID_ARG
+    assert fwd(fake, None, phase=lmoe.PHASE_ROUTER, cand_out=0x5000, cand_k=0) \
+        == lmoe.LMOE_ERR_INVALID_ARG
+    assert fwd(fake, None, phase=lmoe.PHASE_EXPERTS, cand_out=0x5000, cand_k=4) \
+        == lmoe.LMOE_ERR_INVALID_ARG
+    # the router phase needs x, the experts phase needs y
+    assert fwd(None, None, phase=lmoe.PHASE_ROUTER) == lmoe.LMOE_ERR_INVALID_ARG
+    assert fwd(None, None, phase=lmoe.PHASE_EXPERTS) == lmoe.LMOE_ERR_INVALID_ARG
+    # lmoe_threshold_candidates
+    c = lib.lmoe_threshold_candidates
+    assert c(None, 10, 8, 4, fake, None) == lmoe.LMOE_ERR_INVALID_ARG   # logits missing
+    assert c(fake, 10, 8, 4, None, None) == lmoe.LMOE_ERR_INVALID_ARG   # cand missing
+    assert c(fake, 10, 8, 0, fake, None) == lmoe.LMOE_ERR_INVALID_ARG   # k < 1
+    assert c(fake, 10, 0, 4, fake, None) == lmoe.LMOE_ERR_INVALID_ARG   # E < 1
+    assert c(fake, -1, 8, 4, fake, None) == lmoe.LMOE_ERR_INVALID_ARG   # T < 0
