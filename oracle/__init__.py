@@ -17,6 +17,9 @@ the layer defines them:
     ys     = sum_s SiTU-FFN_s(x)                       shared experts at full width
     y      = residual + z_n . W_up^T + ys
 
+The routed experts also have an e4m3 variant (``routed_fp8``, ``forward(expert_fp8=True)``):
+per-row quantisation of both GEMM operands, defined in the C source.
+
 Parity status: every function is pinned by the CPU tests in ``tests/test_oracle_*.py``
 (closed forms, library special cases, brute force on tiny inputs, invariants).
 """
@@ -68,6 +71,14 @@ def _load():
         lib.oracle_situ.restype = ctypes.c_double
         lib.oracle_situ.argtypes = [ctypes.c_double] * 3
         lib.oracle_num_threads.restype = ctypes.c_int
+        lib.oracle_e4m3_decode.restype = ctypes.c_double
+        lib.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
+        lib.oracle_e4m3_encode.restype = ctypes.c_uint8
+        lib.oracle_e4m3_encode.argtypes = [ctypes.c_float]
+        lib.oracle_bf16_round.restype = ctypes.c_float
+        lib.oracle_bf16_round.argtypes = [ctypes.c_double]
+        for name in ("oracle_quantize_rows", "oracle_routed_fp8"):
+            getattr(lib, name).restype = None
         for name in ("oracle_latent", "oracle_router_logits", "oracle_scores",
                      "oracle_thresholds", "oracle_route", "oracle_situ_vec",
                      "oracle_routed", "oracle_shared", "oracle_output"):
@@ -193,6 +204,86 @@ def routed(lat, idx, gate, w_gate, w_value, w_edown, gamma, c=100.0, eps=1e-6):
     return z
 
 
+_u8_p = ctypes.POINTER(ctypes.c_uint8)
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    """Values of e4m3 codes (uint8 array) as float64."""
+    lib = _load()
+    table = np.array([lib.oracle_e4m3_decode(i) for i in range(256)], dtype=np.float64)
+    return table[np.asarray(codes, dtype=np.uint8)]
+
+
+def e4m3_encode(x) -> np.ndarray:
+    """Nearest e4m3 codes (ties to even, saturating at 448) of fp32 values."""
+    lib = _load()
+    xf = np.asarray(x, dtype=np.float32)
+    return np.array([lib.oracle_e4m3_encode(float(v)) for v in xf.ravel()],
+                    dtype=np.uint8).reshape(xf.shape)
+
+
+def bf16_round(x) -> np.ndarray:
+    """fp64 values rounded to the nearest bf16 (ties to even), as float32."""
+    lib = _load()
+    xd = np.asarray(x, dtype=np.float64)
+    return np.array([lib.oracle_bf16_round(float(v)) for v in xd.ravel()],
+                    dtype=np.float32).reshape(xd.shape)
+
+
+def quantize_rows(x):
+    """Per-row e4m3 quantisation of fp32 rows [rows, cols]: (codes uint8, scales fp32),
+    with x ~ decode(codes) * scale."""
+    xf = np.ascontiguousarray(x, dtype=np.float32)
+    rows, cols = xf.shape
+    codes = np.empty((rows, cols), dtype=np.uint8)
+    scales = np.empty(rows, dtype=np.float32)
+    if rows:
+        _load().oracle_quantize_rows(ctypes.c_longlong(rows), cols, _p(xf, _flt_p),
+                                     _p(codes, _u8_p), _p(scales, _flt_p))
+    return codes, scales
+
+
+def _bf16_values(w) -> np.ndarray:
+    """bf16 weights (torch tensor or uint16 bits) as float32 values."""
+    u = _u16(w)
+    return (u.astype(np.uint32) << 16).view(np.float32)
+
+
+def quantize_expert_weights(w_gate, w_value, w_edown) -> dict:
+    """The routed experts' weights quantised row by row (one row = one output feature of
+    one expert): qg, qv [E, I, L] + sg, sv [E, I]; qd [E, L, I] + sd [E, L]."""
+    out = {}
+    for name, w in (("g", w_gate), ("v", w_value), ("d", w_edown)):
+        v = _bf16_values(w)
+        E, R, C = v.shape
+        q, s = quantize_rows(v.reshape(E * R, C))
+        out["q" + name] = q.reshape(E, R, C)
+        out["s" + name] = s.reshape(E, R)
+    return out
+
+
+def routed_fp8(lat, idx, gate, wq: dict, gamma, c=100.0, eps=1e-6):
+    """Routed experts with e4m3 operands (weights from quantize_expert_weights)."""
+    lat = np.ascontiguousarray(lat, dtype=np.float64)
+    idx = np.ascontiguousarray(idx, dtype=np.int32)
+    gate = np.ascontiguousarray(gate, dtype=np.float32)
+    gamma = np.ascontiguousarray(gamma, dtype=np.float32)
+    qg, qv, qd = (np.ascontiguousarray(wq[k]) for k in ("qg", "qv", "qd"))
+    sg, sv, sd = (np.ascontiguousarray(wq[k], dtype=np.float32) for k in ("sg", "sv", "sd"))
+    n, L = lat.shape
+    E, I, L2 = qg.shape
+    K = idx.shape[1]
+    assert L2 == L and qv.shape == qg.shape and qd.shape == (E, L, I)
+    assert sg.shape == sv.shape == (E, I) and sd.shape == (E, L)
+    assert n == 0 or (idx.min() >= 0 and idx.max() < E)
+    z = np.empty((n, L), dtype=np.float64)
+    _load().oracle_routed_fp8(n, L, E, K, I, _p(lat, _dbl_p), _p(idx, _i32_p),
+                              _p(gate, _flt_p), _p(qg, _u8_p), _p(sg, _flt_p), _p(qv, _u8_p),
+                              _p(sv, _flt_p), _p(qd, _u8_p), _p(sd, _flt_p), _p(gamma, _flt_p),
+                              ctypes.c_double(c), ctypes.c_double(eps), _p(z, _dbl_p))
+    return z
+
+
 def shared(x, w_sgate, w_svalue, w_sdown, c=100.0):
     x = _u16(x)
     w_sgate, w_svalue, w_sdown = _u16(w_sgate), _u16(w_svalue), _u16(w_sdown)
@@ -237,7 +328,7 @@ class OracleResult:
 
 
 def forward(w: dict, x, K: int, residual=None, tau="batch", logits_in=None, c=100.0,
-            eps=1e-6) -> OracleResult:
+            eps=1e-6, expert_fp8: bool = False) -> OracleResult:
     """The whole layer on the rows of ``x``.
 
     w: dict of weights (bf16 tensors or uint16 bit arrays, fp32 gamma) with keys w_down,
@@ -245,6 +336,7 @@ def forward(w: dict, x, K: int, residual=None, tau="batch", logits_in=None, c=10
     tau: "batch" -> thresholds solved over the rows of x (k = fair_share_rank);
          None -> plain top-K without balancing; an array -> those thresholds.
     logits_in: fp32 [n, E] router logits to route on instead of the computed ones.
+    expert_fp8: routed experts with e4m3 operands (``routed_fp8``).
     """
     xs = _u16(x)
     n = xs.shape[0]
@@ -265,7 +357,11 @@ def forward(w: dict, x, K: int, residual=None, tau="batch", logits_in=None, c=10
     gamma = w["gamma"]
     if hasattr(gamma, "detach"):
         gamma = gamma.detach().float().cpu().numpy()
-    z = routed(lat, idx, gate, w["w_gate"], w["w_value"], w["w_edown"], gamma, c, eps)
+    if expert_fp8:
+        wq = quantize_expert_weights(w["w_gate"], w["w_value"], w["w_edown"])
+        z = routed_fp8(lat, idx, gate, wq, gamma, c, eps)
+    else:
+        z = routed(lat, idx, gate, w["w_gate"], w["w_value"], w["w_edown"], gamma, c, eps)
     ys = shared(xs, w["w_sgate"], w["w_svalue"], w["w_sdown"], c)
     y = output(z, ys, w["w_up"], residual)
     return OracleResult(y=y, lat=lat, logits=lg, tau=tau_v, idx=idx, gate=gate, z=z, ys=ys)

@@ -333,3 +333,143 @@ void oracle_output(int n, int d, int L, const double *z, const double *ys,
     }
   }
 }
+
+/* ------------------------------------------------------------------------------------ */
+/* FP8 (e4m3) variant of the routed experts.  [SU] Stable LatentMoE bullet: SiTU-GLU
+ * soft-caps the outliers that would otherwise blow up the BF16/FP8 dynamic range, i.e. the
+ * routed experts are meant to run in FP8.  The pages give no quantisation recipe; the
+ * reading used here (stated once, followed by both sides):
+ *   - e4m3: 1 sign, 4 exponent (bias 7), 3 mantissa bits; subnormal step 2^-9; largest
+ *     finite 448; the code S.1111.111 is NaN; no infinities;
+ *   - rounding to e4m3: to nearest, ties to an even mantissa; magnitudes above 448 (and
+ *     infinities) saturate to 448; NaN -> NaN;
+ *   - a row x (fp32 values) is quantised with one scale: amax = max |x|,
+ *     s = fl32(amax / 448) (s = 1 when that is 0), q = e4m3(fl32(x / s)); x ~ q * s;
+ *   - the routed GEMMs take quantised rows on both sides: each weight row (one output
+ *     feature of one expert) and each activation row (the bf16 latent of a token; the
+ *     bf16 SiTU output of one (token, expert) pair); products are summed and the sum is
+ *     multiplied by both rows' scales.                                                      */
+
+/* e4m3 code -> value (exact in double). */
+double oracle_e4m3_decode(uint8_t c) {
+  const int s = c >> 7, e = (c >> 3) & 15, m = c & 7;
+  double v;
+  if (e == 15 && m == 7) return NAN;
+  if (e == 0)
+    v = ldexp((double)m, -9);
+  else
+    v = ldexp((double)(8 + m), e - 10);
+  return s ? -v : v;
+}
+
+/* fp32 -> nearest e4m3 code, ties to even, saturating. */
+uint8_t oracle_e4m3_encode(float x) {
+  if (isnan(x)) return 0x7F;
+  const uint8_t sign = signbit(x) ? 0x80 : 0x00;
+  double a = fabs((double)x);
+  if (a >= 448.0) return sign | 0x7E;
+  uint8_t code;
+  if (a < ldexp(1.0, -6)) {
+    /* subnormal range: multiples of 2^-9; 8 * 2^-9 is the smallest normal, code 0x08 */
+    double q = nearbyint(a * 512.0); /* exact scaling; default rounding is to nearest even */
+    code = (uint8_t)q;
+  } else {
+    int ex;
+    frexp(a, &ex);  /* a = f * 2^ex, f in [0.5, 1) -> a in [2^(ex-1), 2^ex) */
+    const int E = ex - 1;
+    double q = nearbyint(ldexp(a, 3 - E)); /* in [8, 16]: 8 + mantissa, 16 = next binade */
+    int Ef = E, mq = (int)q;
+    if (mq == 16) {
+      Ef += 1;
+      mq = 8;
+    }
+    if (Ef > 8 || (Ef == 8 && mq > 14)) return sign | 0x7E; /* rounded past 448 */
+    code = (uint8_t)(((Ef + 7) << 3) | (mq - 8));
+  }
+  return sign | code;
+}
+
+/* Quantise `rows` rows of `cols` fp32 values each: codes [rows, cols], scales [rows]. */
+void oracle_quantize_rows(long long rows, int cols, const float *x, uint8_t *codes,
+                          float *scales) {
+#pragma omp parallel for schedule(static)
+  for (long long r = 0; r < rows; ++r) {
+    const float *xr = x + (size_t)r * cols;
+    float amax = 0.0f;
+    for (int i = 0; i < cols; ++i) {
+      const float a = fabsf(xr[i]);
+      if (a > amax) amax = a;
+    }
+    float s = amax / 448.0f;
+    if (!(s > 0.0f)) s = 1.0f;
+    scales[r] = s;
+    for (int i = 0; i < cols; ++i) codes[(size_t)r * cols + i] = oracle_e4m3_encode(xr[i] / s);
+  }
+}
+
+/* double -> nearest bf16 value (ties to even), returned as the exact fp32 it is. */
+float oracle_bf16_round(double x) {
+  if (isnan(x) || isinf(x) || x == 0.0) return (float)x;
+  int ex;
+  frexp(x, &ex); /* |x| in [2^(ex-1), 2^ex) */
+  double q = nearbyint(ldexp(x, 8 - ex)); /* 8 significant bits */
+  return (float)ldexp(q, ex - 8);
+}
+
+/* Routed experts with e4m3 operands, aggregation and RMSNorm (the fp8 reading above).
+ * Weights arrive quantised: qg, qv [E, I, L] with sg, sv [E, I]; qd [E, L, I] with sd [E, L].
+ * The latent row of a token is rounded to bf16 and quantised; the SiTU output of each
+ * (token, expert) pair is rounded to bf16 and quantised; everything else is fp64.
+ *   g_i = sg_i * s_lat * sum_l dq(qg_il) dq(q_lat_l)     (v likewise)
+ *   h_i = SiTU(g_i, v_i);  q_h, s_h = quantise(bf16(h))
+ *   o_l = sd_l * s_h * sum_i dq(qd_li) dq(q_h_i);  u = sum_j gate_j o_j;  z = RMSNorm(u)   */
+void oracle_routed_fp8(int n, int L, int E, int K, int I, const double *lat,
+                       const int32_t *idx, const float *gate, const uint8_t *qg,
+                       const float *sg, const uint8_t *qv, const float *sv,
+                       const uint8_t *qd, const float *sd, const float *gamma, double c,
+                       double eps, double *z) {
+  (void)E;
+  double dq[256];
+  for (int i = 0; i < 256; ++i) dq[i] = oracle_e4m3_decode((uint8_t)i);
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int t = 0; t < n; ++t) {
+    double *u = (double *)calloc((size_t)L, sizeof(double));
+    float *row = (float *)malloc(sizeof(float) * (size_t)(L > I ? L : I));
+    uint8_t *ql = (uint8_t *)malloc((size_t)L);
+    uint8_t *qh = (uint8_t *)malloc((size_t)I);
+    float s_lat, s_h;
+    for (int l = 0; l < L; ++l) row[l] = oracle_bf16_round(lat[(size_t)t * L + l]);
+    oracle_quantize_rows(1, L, row, ql, &s_lat);
+    for (int j = 0; j < K; ++j) {
+      const int e = idx[(size_t)t * K + j];
+      const double g = (double)gate[(size_t)t * K + j];
+      for (int i = 0; i < I; ++i) {
+        const size_t wr = (size_t)e * I + i;
+        double ag = 0.0, av = 0.0;
+        for (int l = 0; l < L; ++l) {
+          ag += dq[qg[wr * L + l]] * dq[ql[l]];
+          av += dq[qv[wr * L + l]] * dq[ql[l]];
+        }
+        ag *= (double)sg[wr] * (double)s_lat;
+        av *= (double)sv[wr] * (double)s_lat;
+        row[i] = oracle_bf16_round(oracle_situ(ag, av, c));
+      }
+      oracle_quantize_rows(1, I, row, qh, &s_h);
+      for (int l = 0; l < L; ++l) {
+        const size_t wr = (size_t)e * L + l;
+        double o = 0.0;
+        for (int i = 0; i < I; ++i) o += dq[qd[wr * I + i]] * dq[qh[i]];
+        u[l] += g * o * (double)sd[wr] * (double)s_h;
+      }
+    }
+    double ms = 0.0;
+    for (int l = 0; l < L; ++l) ms += u[l] * u[l];
+    ms /= (double)L;
+    const double inv = 1.0 / sqrt(ms + eps);
+    for (int l = 0; l < L; ++l) z[(size_t)t * L + l] = (double)gamma[l] * u[l] * inv;
+    free(u);
+    free(row);
+    free(ql);
+    free(qh);
+  }
+}
