@@ -44,10 +44,11 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # ----------------------------------------------------------------------------------------
 # algorithmic work of each stage (what the method must read/write/compute at minimum)
 # ----------------------------------------------------------------------------------------
-def stage_work(sh, touched: int, residual: bool = True) -> dict:
+def stage_work(sh, touched: int, residual: bool = True, fp8: bool = False) -> dict:
     T, d, L, E, K, I, S, Is = sh.T, sh.d, sh.L, sh.E, sh.K, sh.I, sh.S, sh.Is
     sw = S * Is
     bf, f4 = 2, 4
+    TK = T * K
     w = {
         "latent_shared": (2.0 * T * d * (L + 2 * sw),
                           (T * d + (L + 2 * sw) * d + T * L + T * sw) * bf),
@@ -64,15 +65,25 @@ def stage_work(sh, touched: int, residual: bool = True) -> dict:
         "output": (2.0 * T * (L + sw) * d,
                    (T * (L + sw) + d * (L + sw) + T * d * (2 if residual else 1)) * bf),
     }
+    if fp8:
+        # e4m3 operands: one byte per weight plus a scale per row; the stage also quantises
+        # its activation rows (bf16 read, codes + scale written) before the GEMM reads them
+        w["expert_gate_up"] = (2.0 * TK * L * 2 * I,
+                               touched * 2 * I * (L + f4) + T * L * bf + T * (L + f4)
+                               + T * L + TK * I * bf)
+        w["expert_down"] = (2.0 * TK * I * L,
+                            TK * I * bf + TK * (I + f4) + touched * L * (I + f4) + TK * I
+                            + TK * L * bf)
     return {k: {"flop": v[0], "bytes": float(v[1])} for k, v in w.items()}
 
 
-def layer_work(sh, touched: int) -> tuple[float, float]:
+def layer_work(sh, touched: int, fp8: bool = False) -> tuple[float, float]:
     """FLOP of the layer (461.5 MFLOP per token at the K3 shape) and its algorithmic bytes:
     every touched weight once, x and the residual read, y written."""
     T, d, L, E, K, I, S, Is = sh.T, sh.d, sh.L, sh.E, sh.K, sh.I, sh.S, sh.Is
     flop_tok = 2.0 * (d * L + L * E + K * (L * 2 * I + I * L) + 3 * S * Is * d + L * d)
-    wbytes = (L * d + E * L + touched * 3 * I * L + L * d + 3 * S * Is * d) * 2 + L * 4
+    routed = touched * 3 * I * L * (1 if fp8 else 2) + (touched * (2 * I + L) * 4 if fp8 else 0)
+    wbytes = (L * d + E * L + L * d + 3 * S * Is * d) * 2 + routed + L * 4
     return flop_tok * T, float(wbytes + 3 * T * d * 2)
 
 
@@ -110,15 +121,16 @@ def kernel_source_hash(stage: str) -> str:
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(stage: str):
+def ncu_traffic(stage: str, table: str = "stages"):
     """DRAM bytes per launch of a stage's kernel from a committed ncu summary, if it was
-    captured from the current sources of that kernel; else None."""
+    captured from the current sources of that kernel; else None.  table: "stages" (bf16
+    routed experts) or "stages_fp8"."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         t = json.load(f)
-    s = t.get("stages", {}).get(stage)
+    s = t.get(table, {}).get(stage)
     if s is None or s.get("kernel_source_hash") != kernel_source_hash(stage):
         return None
     return float(s["dram_bytes_per_launch"])
@@ -239,8 +251,11 @@ def max_over_ranks(v: float, world: int) -> float:
 
 
 SMALL = synth.LayerShape("small", T=1024, d=7168, L=3584, E=128, K=16, I=512, S=2, Is=2048)
+# the K3 routing shape (T=8192, E=896, top-16) with narrow widths: the threshold, top-K and
+# dispatch kernels run at full size on a device footprint of well under 1 GB
+ROUTING = synth.LayerShape("routing", T=8192, d=512, L=256, E=896, K=16, I=64, S=2, Is=128)
 SHAPES = {"prefill": synth.PREFILL, "decode": synth.DECODE, "e64": synth.E64,
-          "skew": synth.SKEW, "small": SMALL}
+          "skew": synth.SKEW, "small": SMALL, "routing": ROUTING}
 DESCRIPTIONS = {
     "prefill": "K3 Stable Latent MoE layer, prefill: in-batch Quantile-Balancing thresholds; "
                "x~N(0,1) with 0.1% of elements x1000; residual = x",
@@ -252,15 +267,20 @@ DESCRIPTIONS = {
             "bias (router GEMM not in the step), in-batch thresholds; x~N(0,1); residual = x",
     "small": "K3 widths, 128 experts, T=1024 (profiling case: ~128 tokens per expert as "
              "in prefill, a few GB on the device); x as in prefill",
+    "routing": "K3 routing shape with narrow widths (profiling case for the threshold, "
+               "top-K and dispatch kernels at T=8192, E=896, top-16); x~N(0,1); in-batch "
+               "thresholds",
 }
 
 
 class Workload:
     """Inputs and routing arguments of one bench configuration."""
 
-    def __init__(self, name, dev, rank, overlap=False, shared_sms=0, qb="local", world=1):
+    def __init__(self, name, dev, rank, overlap=False, shared_sms=0, qb="local", world=1,
+                 expert_fp8=False):
         self.name = name
         self.qb = qb
+        self.fp8 = expert_fp8
         self.sh = sh = SHAPES[name]
         outliers = name in ("prefill", "small")
         gain = synth.outlier_router_gain(sh, OUTLIER_FRAC, OUTLIER_SCALE) if outliers else 1.0
@@ -269,11 +289,11 @@ class Workload:
                               outlier_frac=OUTLIER_FRAC if outliers else 0.0,
                               outlier_scale=OUTLIER_SCALE)
         self.layer = lmoe.Layer(sh, self.w, max_tokens=max(sh.T, 8192 if name == "decode" else 0),
-                                overlap=overlap, shared_sms=shared_sms)
+                                overlap=overlap, shared_sms=shared_sms, expert_fp8=expert_fp8)
         self.kwargs = {}
         self.extra = {}
         if qb == "global":
-            if name not in ("prefill", "e64", "small"):
+            if name not in ("prefill", "e64", "small", "routing"):
                 raise ValueError("--qb global applies to the in-batch-threshold workloads")
             # thresholds over all ranks' batches together (all-gather of candidates)
             self.kwargs["global_tokens"] = sh.T * world
@@ -313,7 +333,9 @@ class Workload:
                                     f"the {sh.T * world}-token global batch (all-gather of "
                                     f"per-rank candidates)",
                 "shared_experts": "in line" if not self.layer.overlap else
-                                  f"second stream, {self.layer.shared_sms or 'default'} SMs"}
+                                  f"second stream, {self.layer.shared_sms or 'default'} SMs",
+                "routed_experts": "e4m3 operands, one fp32 scale per row" if self.fp8
+                                  else "bf16"}
 
 
 def make_inputs(sh, dev, rank, outliers=True):
@@ -373,7 +395,7 @@ def run_ours(args):
         raise RuntimeError("bench.py needs a CUDA GPU (the layer has no CPU path)")
     dev = torch.device("cuda", local)
     wl = Workload(args.shape, dev, rank, overlap=args.overlap, shared_sms=args.shared_sms,
-                  qb=args.qb, world=world)
+                  qb=args.qb, world=world, expert_fp8=args.experts == "fp8")
     sh, layer, x, w = wl.sh, wl.layer, wl.x, wl.w
     y = torch.empty_like(x)
     stream = torch.cuda.current_stream()
@@ -434,9 +456,9 @@ def run_ours(args):
     value = world * T * args.steps / (ms_max / 1e3)
     e2e_value = world * T * args.steps / (e2e_ms / 1e3)
     peaks, peak_src = load_peaks()
-    flop, nbytes = layer_work(sh, touched)
+    flop, nbytes = layer_work(sh, touched, fp8=wl.fp8)
     step_s = ms_max / 1e3 / args.steps
-    work = stage_work(sh, touched)
+    work = stage_work(sh, touched, fp8=wl.fp8)
     dom = max(stage_ms, key=stage_ms.get)
     dw = work[dom]
     t_s = stage_ms[dom] / 1e3
@@ -449,7 +471,7 @@ def run_ours(args):
         roof = {"bound": "hbm", "achieved": dw["bytes"] / t_s / 1e9, "peak": peaks["hbm_gbs"],
                 "unit": "GB/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = ncu_traffic(dom)
+    roof["traffic"] = ncu_traffic(dom, "stages_fp8" if wl.fp8 else "stages")
     roof["kernel"] = dom
     roof["peak_source"] = f"{peak_src} ({'bf16 sustained' if roof['bound'] == 'tensor' else 'HBM copy'})"
     roof["algorithmic"] = {"flop": dw["flop"], "bytes": dw["bytes"]}
@@ -464,7 +486,8 @@ def run_ours(args):
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16, routed experts e4m3" if wl.fp8 else "bf16",
             "data": "synthetic (seeded; random-init weights of the K3 layer shape)",
             "config": wl.config(world),
             "tflops": flop / step_s / 1e12,
@@ -484,7 +507,7 @@ def run_ours(args):
                         "after_balancing": {"max_over_mean": float(counts.max() / fair),
                                             "min_over_mean": float(counts.min() / fair)}}
     if wl.name == "decode":
-        line["decode_weight_gbs"] = layer_work(sh, touched)[1] / step_s / 1e9
+        line["decode_weight_gbs"] = layer_work(sh, touched, fp8=wl.fp8)[1] / step_s / 1e9
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         wh = host_weights(w)
         xh = x.cpu()
@@ -516,6 +539,8 @@ def main():
                     help="run the shared experts on a second stream beside the routed path")
     ap.add_argument("--shared-sms", type=int, default=0,
                     help="SMs for the shared experts when they overlap (0: library default)")
+    ap.add_argument("--experts", choices=["bf16", "fp8"], default="bf16",
+                    help="routed-expert GEMM operands: bf16, or e4m3 with per-row scales")
     ap.add_argument("--qb", choices=["local", "global"], default="local",
                     help="thresholds per rank's batch (local) or over all ranks' batches "
                          "(global: router phase, all-gather of candidates, experts phase)")

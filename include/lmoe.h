@@ -69,7 +69,20 @@ typedef struct lmoe_dims {
   int Is;     /* shared expert intermediate size */
   float c;    /* SiTU-GLU cap (100 for K3) */
   float eps;  /* RMSNorm epsilon (1e-6) */
+  int expert_fp8; /* 0: routed experts in bf16; 1: routed experts with e4m3 operands (see
+                     below); fixes the packed layout, so pack and forward must agree */
 } lmoe_dims;
+
+/* Routed experts in FP8 (lmoe_dims.expert_fp8 = 1).  [SU] Stable LatentMoE bullet:
+ * SiTU-GLU soft-caps the outliers that would otherwise blow up the BF16/FP8 dynamic range,
+ * i.e. the routed experts are meant to run in FP8; the pages give no recipe.  Reading: both
+ * operands of the two routed GEMMs are e4m3 (OCP E4M3: ties to even, saturating at 448)
+ * with one fp32 scale per row -- per output feature of each expert's weights (quantised
+ * by lmoe_pack_weights), per token for the latent, per (token, expert) pair for the SiTU
+ * output -- s = amax/448 and code = e4m3(x/s), every step an IEEE fp32 operation; the GEMM
+ * accumulates in fp32 and multiplies its sum by both scales.  The latent and the SiTU
+ * output are quantised from their bf16 values.  The dense GEMMs, routing, combine and
+ * RMSNorm are unchanged.  Requires L and I multiples of 128. */
 
 /* Unpacked weights as a caller holds them (device pointers, bf16 unless stated). */
 typedef struct lmoe_weights {
@@ -208,8 +221,8 @@ int lmoe_route(const float *logits, const float *tau, int T, int E, int K, int32
  *            scratch between calls (its first word carries the device error flag)
  *   io       routing options and debug outputs, or NULL (= in-batch thresholds); only
  *            io->kernel_launches is written
- * Supported shapes: d, L, I, Is multiples of 64; 1 <= K <= min(E, 32); E <= 4096 and a
- * multiple of 16;
+ * Supported shapes: d, L, I, Is multiples of 64 (L and I of 128 with expert_fp8);
+ * 1 <= K <= min(E, 32); E <= 4096 and a multiple of 16;
  * L <= 16384; T * K < 2^31.  T == 0 is a no-op.
  * Arithmetic: bf16 operands on the tensor cores with fp32 accumulation; the latent, the
  * expert intermediates and the normalised latent are rounded to bf16 between GEMMs;
@@ -226,6 +239,13 @@ int lmoe_forward(const lmoe_dims *dims, const void *packed, const void *x,
  * error bits as the forward workspace's flag if a device-side wait runs out. */
 int lmoe_gemm_bf16(const void *A, const void *B, float *C, int M, int N, int Kd,
                    uint32_t *dev_flag, void *stream);
+
+/* Building block of the FP8 routed experts, exposed for verification: per-row e4m3
+ * quantisation of x [rows, cols] bf16 (row-major, cols a multiple of 16, 16-byte aligned)
+ * into codes [rows, cols] and scales [rows] fp32, by the recipe stated at lmoe_dims.
+ * Errors: INVALID_ARG (null pointers, rows < 0), UNSUPPORTED (cols). */
+int lmoe_quantize_e4m3(const void *x, long long rows, int cols, uint8_t *codes, float *scales,
+                       void *stream);
 
 /* Size in bytes of the fixed device array that lmoe_forward_noalloc uses as its workspace. */
 #define LMOE_NOALLOC_SCRATCH_BYTES (24u << 20)

@@ -16,6 +16,7 @@ static bool dims_ok(const lmoe_dims* D) {
       D->Is < 0)
     return false;
   if (!(D->c > 0.0f) || !(D->eps >= 0.0f)) return false;
+  if (D->expert_fp8 != 0 && D->expert_fp8 != 1) return false;
   return true;
 }
 
@@ -25,6 +26,7 @@ static int dims_supported(const lmoe_dims* D) {
   if (D->S > 0 && (D->Is <= 0 || D->Is % 64)) return LMOE_ERR_UNSUPPORTED;
   if (D->K > D->E || D->K > 32 || D->E > 4096 || D->E % 16) return LMOE_ERR_UNSUPPORTED;
   if (D->L > 16384) return LMOE_ERR_UNSUPPORTED;
+  if (D->expert_fp8 && (D->L % 128 || D->I % 128)) return LMOE_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(D->T) * D->K >= (int64_t{1} << 31)) return LMOE_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(D->E) * 2 * D->I >= (int64_t{1} << 31) ||
       static_cast<int64_t>(D->E) * D->L >= (int64_t{1} << 31))
@@ -45,11 +47,20 @@ PackedLayout packed_layout(const lmoe_dims& D) {
   const size_t sw = static_cast<size_t>(shared_width(D));
   P.w1 = take((static_cast<size_t>(D.L) + 2 * sw) * D.d * 2);
   P.wr = take(static_cast<size_t>(D.E) * D.L * 2);
-  // expert weights in 128-row tiles (the last row tile of an expert zero-padded)
-  P.wgu = take(static_cast<size_t>(D.E) * ceil_div(2 * D.I, BLOCK_M) * BLOCK_M * D.L * 2);
-  P.wed = take(static_cast<size_t>(D.E) * ceil_div(D.L, BLOCK_M) * BLOCK_M * D.I * 2);
+  // expert weights in 128-row tiles (the last row tile of an expert zero-padded): bf16, or
+  // e4m3 codes (one byte each) with one fp32 scale per row
+  const size_t eb = D.expert_fp8 ? 1 : 2;
+  const size_t rows_gu = static_cast<size_t>(D.E) * ceil_div(2 * D.I, BLOCK_M) * BLOCK_M;
+  const size_t rows_ed = static_cast<size_t>(D.E) * ceil_div(D.L, BLOCK_M) * BLOCK_M;
+  P.wgu = take(rows_gu * D.L * eb);
+  P.wed = take(rows_ed * D.I * eb);
   P.w2 = take(static_cast<size_t>(D.d) * (D.L + sw) * 2);
   P.gamma = take(static_cast<size_t>(D.L) * 4);
+  P.sgu = P.sed = 0;
+  if (D.expert_fp8) {
+    P.sgu = take(rows_gu * 4);
+    P.sed = take(rows_ed * 4);
+  }
   P.total = off;
   return P;
 }
@@ -64,7 +75,7 @@ WorkspaceLayout workspace_layout(const lmoe_dims& D) {
   };
   const size_t T = static_cast<size_t>(D.T), TK = T * D.K;
   const size_t nb = static_cast<size_t>(ceil_div(D.T, DISPATCH_TOKENS));
-  W.err = take(256);
+  W.err = take(256);  // word 0: device error flag; word 1: dispatch scan completion counter
   W.lat = take(T * D.L * 2);
   W.logits = take(T * D.E * 4);
   W.logits_t = take(T * D.E * 4);
@@ -82,6 +93,13 @@ WorkspaceLayout workspace_layout(const lmoe_dims& D) {
   W.zh = take(T * (D.L + shared_width(D)) * 2);
   // fp32 shared-expert output, used when the shared experts run beside the routed path
   W.ys = take(D.T >= LMOE_OVERLAP_MIN_T && shared_width(D) > 0 ? T * D.d * 4 : 0);
+  W.lat8 = W.slat = W.h8 = W.sh = 0;
+  if (D.expert_fp8) {
+    W.lat8 = take(T * D.L);
+    W.slat = take(T * 4);
+    W.h8 = take(TK * D.I);
+    W.sh = take(TK * 4);
+  }
   W.total = off;
   return W;
 }
@@ -176,6 +194,16 @@ int lmoe_thresholds(const float* logits, int T, int E, int K, int k_rank, float*
   }
   // token-major input: each expert's column is read with stride E
   return launch_thresholds(logits, T, E, E, 1, k, tau, static_cast<cudaStream_t>(stream));
+}
+
+int lmoe_quantize_e4m3(const void* x, long long rows, int cols, uint8_t* codes, float* scales,
+                       void* stream) {
+  if (rows < 0 || cols <= 0) return LMOE_ERR_INVALID_ARG;
+  if (rows == 0) return LMOE_OK;
+  if (!x || !codes || !scales) return LMOE_ERR_INVALID_ARG;
+  if (cols % 16 || !aligned16(x) || !aligned16(codes)) return LMOE_ERR_UNSUPPORTED;
+  return launch_quantize_rows(static_cast<const __nv_bfloat16*>(x), rows, cols, cols, codes,
+                              cols, scales, static_cast<cudaStream_t>(stream));
 }
 
 int lmoe_threshold_candidates(const float* logits, int T, int E, int k, float* cand,
@@ -456,6 +484,7 @@ int lmoe_forward(const lmoe_dims* dims, const void* packed, const void* x, const
   // 6. routed gate/value GEMM with SiTU-GLU: h = SiTU(lat[src_tok] . W_gu[e]^T) per expert,
   //    the latent rows gathered inside the GEMM
   bf* h = reinterpret_cast<bf*>(ws + W.h);
+  const bool fp8 = D.expert_fp8 != 0;
   {
     GroupedArgs g{};
     g.E = D.E;
@@ -466,6 +495,20 @@ int lmoe_forward(const lmoe_dims* dims, const void* packed, const void* x, const
     g.gather = src_tok;
     g.x = lat;
     g.ldx = D.L;
+    const void* xop = lat;
+    if (fp8) {
+      // e4m3 latent rows (one scale per token), gathered like the bf16 rows
+      uint8_t* lat8 = ws + W.lat8;
+      float* slat = reinterpret_cast<float*>(ws + W.slat);
+      rc = launch_quantize_rows(lat, T, D.L, D.L, lat8, D.L, slat, stream);
+      if (rc != LMOE_OK) return rc;
+      launches += 1;
+      g.fp8 = 1;
+      g.x = reinterpret_cast<const bf*>(lat8);
+      g.w_scale = reinterpret_cast<const float*>(pk + P.sgu);
+      g.x_scale = slat;
+      xop = lat8;
+    }
     g.epi = EPI_SITU;
     g.out = h;
     g.ldo = D.I;
@@ -474,7 +517,7 @@ int lmoe_forward(const lmoe_dims* dims, const void* packed, const void* x, const
     g.timeout_ns = wait_limit_ns();
     g.max_ctas = routed_ctas;
     g.mean_tokens = static_cast<int>(static_cast<int64_t>(TK) / D.E);
-    rc = launch_grouped_gemm(pk + P.wgu, lat, static_cast<uint64_t>(T), D.L, g, stream);
+    rc = launch_grouped_gemm(pk + P.wgu, xop, static_cast<uint64_t>(T), D.L, g, stream);
     if (rc != LMOE_OK) return rc;
   }
   if (!mark(LMOE_STAGE_EXPERT_DOWN, 1)) return LMOE_ERR_CUDA;
@@ -495,7 +538,20 @@ int lmoe_forward(const lmoe_dims* dims, const void* packed, const void* x, const
     g.timeout_ns = wait_limit_ns();
     g.max_ctas = routed_ctas;
     g.mean_tokens = static_cast<int>(static_cast<int64_t>(TK) / D.E);
-    rc = launch_grouped_gemm(pk + P.wed, h, static_cast<uint64_t>(TK), D.I, g, stream);
+    const void* xop = h;
+    if (fp8) {
+      // e4m3 SiTU outputs, one scale per (token, expert) row
+      uint8_t* h8 = ws + W.h8;
+      float* sh = reinterpret_cast<float*>(ws + W.sh);
+      rc = launch_quantize_rows(h, TK, D.I, D.I, h8, D.I, sh, stream);
+      if (rc != LMOE_OK) return rc;
+      launches += 1;
+      g.fp8 = 1;
+      g.w_scale = reinterpret_cast<const float*>(pk + P.sed);
+      g.x_scale = sh;
+      xop = h8;
+    }
+    rc = launch_grouped_gemm(pk + P.wed, xop, static_cast<uint64_t>(TK), D.I, g, stream);
     if (rc != LMOE_OK) return rc;
   }
   if (!mark(LMOE_STAGE_COMBINE, 1)) return LMOE_ERR_CUDA;

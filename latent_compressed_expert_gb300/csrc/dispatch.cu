@@ -21,9 +21,11 @@ namespace lmoe {
 // masks[b][e] bit i <=> token 32 b + i selected expert e.
 __global__ void __launch_bounds__(256)
 dispatch_mask_kernel(const int32_t* __restrict__ idx, int T, int E, int K,
-                     uint32_t* __restrict__ masks, uint32_t* __restrict__ err) {
+                     uint32_t* __restrict__ masks, uint32_t* __restrict__ err,
+                     uint32_t* __restrict__ done) {
   extern __shared__ uint32_t m_smem[];
   const int b = blockIdx.x;
+  if (b == 0 && threadIdx.x == 0) *done = 0u;  // completion counter of the column scan
   for (int e = threadIdx.x; e < E; e += blockDim.x) m_smem[e] = 0u;
   __syncthreads();
   const int t0 = b * DISPATCH_TOKENS;
@@ -42,96 +44,101 @@ dispatch_mask_kernel(const int32_t* __restrict__ idx, int T, int E, int K,
     masks[static_cast<size_t>(b) * E + e] = m_smem[e];
 }
 
-// One CTA: base[b][e] = picks of expert e in blocks < b; offsets = exclusive scan of the
-// counts over experts; ct_off = exclusive scan of ceil(count / GROUPED_TOKN) (the token
-// chunks of the routed-expert GEMMs).
-__global__ void __launch_bounds__(1024)
-dispatch_scan_kernel(const uint32_t* __restrict__ masks, int nb, int E, int TK,
+// Column scan: base[b][e] = picks of expert e in blocks < b, and the expert's count.  A CTA
+// owns 32 experts (one per lane, so every mask row is read as one 128-byte line); its 8 warps
+// split the blocks into strips: each thread sums its strip, the strips' sums are scanned
+// across the warps, and a second pass over the strip writes the bases.  The counts go to
+// offsets[e]; the last CTA to finish (a fence and an atomic counter that the mask kernel
+// zeroed, no waiting) turns them into the exclusive scans offsets (rows) and ct_off (token
+// chunks of the routed-expert GEMMs, ceil(count / GROUPED_TOKN)).
+constexpr int SCAN_WARPS = 8;
+constexpr int SCAN_THREADS = SCAN_WARPS * 32;
+
+__global__ void __launch_bounds__(SCAN_THREADS)
+dispatch_scan_kernel(const uint32_t* __restrict__ masks, int nb, int E,
                      uint32_t* __restrict__ base, int32_t* __restrict__ offsets,
-                     int32_t* __restrict__ ct_off, int32_t* __restrict__ counts_out) {
-  __shared__ int32_t warp_cnt[32], warp_mt[32];
-  __shared__ int32_t carry_cnt, carry_mt;
-  if (threadIdx.x == 0) {
-    carry_cnt = 0;
-    carry_mt = 0;
+                     int32_t* __restrict__ ct_off, int32_t* __restrict__ counts_out,
+                     uint32_t* __restrict__ done) {
+  __shared__ uint32_t part[SCAN_WARPS][32];
+  __shared__ int32_t wsum[2][SCAN_WARPS];
+  __shared__ bool last;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int e = blockIdx.x * 32 + lane;
+  const int per = (nb + SCAN_WARPS - 1) / SCAN_WARPS;
+  const int b0 = warp * per, b1 = min(nb, b0 + per);
+  uint32_t sum = 0u;
+  if (e < E) {
+#pragma unroll 4
+    for (int b = b0; b < b1; ++b) sum += __popc(__ldg(masks + static_cast<size_t>(b) * E + e));
+  }
+  part[warp][lane] = sum;
+  __syncthreads();
+  uint32_t run = 0u, total = 0u;
+  for (int w = 0; w < SCAN_WARPS; ++w) {
+    const uint32_t v = part[w][lane];
+    run += w < warp ? v : 0u;
+    total += v;
+  }
+  if (e < E) {
+    for (int b = b0; b < b1; ++b) {
+      const size_t me = static_cast<size_t>(b) * E + e;
+      base[me] = run;
+      run += __popc(__ldg(masks + me));
+    }
+    if (warp == 0) {
+      offsets[e] = static_cast<int32_t>(total);
+      if (counts_out) counts_out[e] = static_cast<int32_t>(total);
+    }
+  }
+  // the last CTA scans the counts of all experts
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) last = atomicAdd(done, 1u) == gridDim.x - 1;
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  const int eper = (E + SCAN_THREADS - 1) / SCAN_THREADS;
+  const int e0 = threadIdx.x * eper, e1 = min(E, e0 + eper);
+  int32_t c_rows = 0, c_chunks = 0;
+  for (int i = e0; i < e1; ++i) {
+    const int32_t c = __ldcg(offsets + i);
+    c_rows += c;
+    c_chunks += static_cast<int32_t>(ceil_div(c, GROUPED_TOKN));
+  }
+  int32_t ir = c_rows, ic = c_chunks;  // inclusive scans within the warp
+  for (int o = 1; o < 32; o <<= 1) {
+    const int32_t vr = __shfl_up_sync(0xffffffffu, ir, o);
+    const int32_t vc = __shfl_up_sync(0xffffffffu, ic, o);
+    if (lane >= o) {
+      ir += vr;
+      ic += vc;
+    }
+  }
+  if (lane == 31) {
+    wsum[0][warp] = ir;
+    wsum[1][warp] = ic;
   }
   __syncthreads();
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  for (int e0 = 0; e0 < E; e0 += blockDim.x) {
-    const int e = e0 + threadIdx.x;
-    int cnt = 0;
-    if (e < E) {
-      int b = 0;
-      for (; b + 4 <= nb; b += 4) {
-        const uint32_t m0 = __ldg(masks + static_cast<size_t>(b) * E + e);
-        const uint32_t m1 = __ldg(masks + static_cast<size_t>(b + 1) * E + e);
-        const uint32_t m2 = __ldg(masks + static_cast<size_t>(b + 2) * E + e);
-        const uint32_t m3 = __ldg(masks + static_cast<size_t>(b + 3) * E + e);
-        base[static_cast<size_t>(b) * E + e] = cnt;
-        cnt += __popc(m0);
-        base[static_cast<size_t>(b + 1) * E + e] = cnt;
-        cnt += __popc(m1);
-        base[static_cast<size_t>(b + 2) * E + e] = cnt;
-        cnt += __popc(m2);
-        base[static_cast<size_t>(b + 3) * E + e] = cnt;
-        cnt += __popc(m3);
-      }
-      for (; b < nb; ++b) {
-        base[static_cast<size_t>(b) * E + e] = cnt;
-        cnt += __popc(__ldg(masks + static_cast<size_t>(b) * E + e));
-      }
-      if (counts_out) counts_out[e] = cnt;
-    }
-    const int mt = static_cast<int>(ceil_div(cnt, GROUPED_TOKN));
-    // block-wide exclusive scans of cnt and mt
-    int ic = cnt, im = mt;
-    for (int o = 1; o < 32; o <<= 1) {
-      const int vc = __shfl_up_sync(0xffffffffu, ic, o);
-      const int vm = __shfl_up_sync(0xffffffffu, im, o);
-      if (lane >= o) {
-        ic += vc;
-        im += vm;
-      }
-    }
-    if (lane == 31) {
-      warp_cnt[warp] = ic;
-      warp_mt[warp] = im;
-    }
-    __syncthreads();
-    if (warp == 0) {
-      const int nw = blockDim.x >> 5;
-      int wc = lane < nw ? warp_cnt[lane] : 0, wm = lane < nw ? warp_mt[lane] : 0;
-      for (int o = 1; o < 32; o <<= 1) {
-        const int vc = __shfl_up_sync(0xffffffffu, wc, o);
-        const int vm = __shfl_up_sync(0xffffffffu, wm, o);
-        if (lane >= o) {
-          wc += vc;
-          wm += vm;
-        }
-      }
-      if (lane < nw) {
-        warp_cnt[lane] = wc;  // inclusive over warps
-        warp_mt[lane] = wm;
-      }
-    }
-    __syncthreads();
-    const int before_c = (warp > 0 ? warp_cnt[warp - 1] : 0) + (ic - cnt);
-    const int before_m = (warp > 0 ? warp_mt[warp - 1] : 0) + (im - mt);
-    if (e < E) {
-      offsets[e] = carry_cnt + before_c;
-      ct_off[e] = carry_mt + before_m;
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      carry_cnt += warp_cnt[(blockDim.x >> 5) - 1];
-      carry_mt += warp_mt[(blockDim.x >> 5) - 1];
-    }
-    __syncthreads();
+  int32_t pr = ir - c_rows, pc = ic - c_chunks;
+  int32_t tr = 0, tc = 0;
+  for (int w = 0; w < SCAN_WARPS; ++w) {
+    pr += w < warp ? wsum[0][w] : 0;
+    pc += w < warp ? wsum[1][w] : 0;
+    tr += wsum[0][w];
+    tc += wsum[1][w];
+  }
+  // every count was read above: the exclusive scans overwrite them in place
+  __syncthreads();
+  for (int i = e0; i < e1; ++i) {
+    const int32_t c = __ldcg(offsets + i);
+    offsets[i] = pr;
+    ct_off[i] = pc;
+    pr += c;
+    pc += static_cast<int32_t>(ceil_div(c, GROUPED_TOKN));
   }
   if (threadIdx.x == 0) {
-    offsets[E] = carry_cnt;  // == T*K when every index was valid
-    ct_off[E] = carry_mt;
-    (void)TK;
+    offsets[E] = tr;  // == T*K when every index was valid
+    ct_off[E] = tc;
   }
 }
 
@@ -247,12 +254,15 @@ int launch_dispatch(const int32_t* idx, int T, int E, int K, uint32_t* masks, ui
                     int32_t* counts_out, uint32_t* err, cudaStream_t stream) {
   const int nb = static_cast<int>(ceil_div(T, DISPATCH_TOKENS));
   const size_t msmem = static_cast<size_t>(E) * sizeof(uint32_t);
+  uint32_t* done = err + 1;  // the word after the error flag
   if (nb > 0) {
-    dispatch_mask_kernel<<<nb, 256, msmem, stream>>>(idx, T, E, K, masks, err);
+    dispatch_mask_kernel<<<nb, 256, msmem, stream>>>(idx, T, E, K, masks, err, done);
     if (cudaGetLastError() != cudaSuccess) return LMOE_ERR_CUDA;
+  } else if (cudaMemsetAsync(done, 0, sizeof(uint32_t), stream) != cudaSuccess) {
+    return LMOE_ERR_CUDA;
   }
-  dispatch_scan_kernel<<<1, 1024, 0, stream>>>(masks, nb, E, T * K, base, offsets, ct_off,
-                                               counts_out);
+  dispatch_scan_kernel<<<static_cast<unsigned>(ceil_div(E, 32)), SCAN_THREADS, 0, stream>>>(
+      masks, nb, E, base, offsets, ct_off, counts_out, done);
   if (cudaGetLastError() != cudaSuccess) return LMOE_ERR_CUDA;
   if (nb > 0) {
     const int64_t pairs = static_cast<int64_t>(T) * K;

@@ -48,7 +48,9 @@ struct GroupedCfg {
   static constexpr int STAGES = STAGES_;
   static constexpr int ACC_COLS = 256;                    // TMEM columns between accumulators
   static constexpr int TMEM_COLS = 512;
-  static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
+  static constexpr int EPI_OFF = STAGES * STAGE_BYTES;   // per epilogue warp 32 x 32 bf16
+  static constexpr int EPI_BYTES = 4 * 32 * 32 * 2;
+  static constexpr int BAR_OFF = EPI_OFF + EPI_BYTES;
   static constexpr int NUM_BARS = 2 * STAGES + 5;
   static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
   static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;
@@ -66,6 +68,7 @@ constexpr int GROUPED_GATHER_THREADS = GROUPED_GATHER_WARPS * 32;
 constexpr int GROUPED_THREADS = (2 + GROUPED_EPI_WARPS + GROUPED_GATHER_WARPS) * 32;
 
 struct GTile {
+  int e;        // expert
   int w_row;    // row coordinate of the tile's first 128 x 64 weight box (tiled layout)
   int r0;       // first weight row within the expert (output feature)
   int tok0;     // first token row (permuted order)
@@ -87,6 +90,7 @@ __device__ __forceinline__ GTile decode_gtile(const GroupedArgs& g, int mt, int 
   const int chunk = q - __ldg(g.ct_off + e);
   const int m = tile - q * mt;
   GTile t;
+  t.e = e;
   t.r0 = m * BLOCK_M;
   t.w_row = (e * mt + m) * (g.Kd / BLOCK_K) * BLOCK_M;
   t.tok0 = __ldg(g.seg_off + e) + chunk * GROUPED_TOKN;
@@ -118,7 +122,33 @@ __device__ __forceinline__ float situ_g(float g, float v, float c, float inv_c) 
   return __fdividef(gc, 1.0f + __expf(fminf(-gc, 80.0f))) * vc;
 }
 
-template <int STAGES_>
+// tanh to ~2^-20 relative: below |x| = 1/4 its odd Taylor polynomial through x^9 (the next
+// term, 1382/155925 x^11, is < 1.5e-8 of tanh there), above it (1 - e) / (1 + e) with
+// e = exp(-2|x|), where the subtraction loses no significant bits.
+// Both branches are evaluated and one is selected: a warp vote to skip the exponential
+// measured slower (it serialises the unrolled epilogue loop).
+__device__ __forceinline__ float tanh_close(float x) {
+  const float ax = fabsf(x);
+  const float x2 = x * x;
+  float p = fmaf(x2, 62.0f / 2835.0f, -17.0f / 315.0f);
+  p = fmaf(x2, p, 2.0f / 15.0f);
+  p = fmaf(x2, p, -1.0f / 3.0f);
+  p = fmaf(x2 * x, p, x);
+  const float e = __expf(-2.0f * ax);
+  const float t = copysignf(__fdividef(1.0f - e, 1.0f + e), x);
+  return ax < 0.25f ? p : t;
+}
+
+// SiTU-GLU for the FP8 path, which quantises h next: an e4m3 code moves when its input
+// moves by 2^-4 relative, so h must carry little more error than the fp32 GEMM sums
+// themselves (the MUFU tanh approximation, ~2^-11, would move ~1 % of the codes).
+__device__ __forceinline__ float situ_close(float g, float v, float c, float inv_c) {
+  const float gc = c * tanh_close(g * inv_c);
+  const float vc = c * tanh_close(v * inv_c);
+  return __fdividef(gc, 1.0f + __expf(fminf(-gc, 80.0f))) * vc;
+}
+
+template <int STAGES_, bool FP8>
 __global__ void __launch_bounds__(GROUPED_THREADS, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
                     const __grid_constant__ CUtensorMap tmX, const GroupedArgs g) {
@@ -134,6 +164,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
   uint64_t* drain = tempty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 4);
+  __nv_bfloat16* epi_stage = reinterpret_cast<__nv_bfloat16*>(smem + C::EPI_OFF);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int mt = (g.M_w + BLOCK_M - 1) / BLOCK_M;
@@ -216,7 +247,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
       int lt = 0;
       for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++lt) {
         const GTile t = decode_gtile(g, mt, tile);
-        const uint32_t idesc = ptx::idesc_bf16_f32(BLOCK_M, t.npad);
+        const uint32_t idesc = FP8 ? ptx::idesc_e4m3_f32(BLOCK_M, t.npad)
+                                   : ptx::idesc_bf16_f32(BLOCK_M, t.npad);
         const int acc = lt & 1;
         const uint32_t aph = static_cast<uint32_t>(lt >> 1) & 1u;
         if (!ptx::mbar_wait(&tempty[acc], aph ^ 1u, abort_flag, limit)) {
@@ -239,9 +271,14 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
           const uint32_t sa = ptx::smem_u32(smem + s * C::STAGE_BYTES);
           const uint32_t sb = sa + C::A_BYTES;
 #pragma unroll
-          for (int k = 0; k < BLOCK_K / 16; ++k)
-            ptx::umma_bf16(d_tmem, ptx::smem_desc_sw128(sa + k * 32),
-                           ptx::smem_desc_sw128(sb + k * 32), idesc, (kb | k) != 0 ? 1u : 0u);
+          for (int k = 0; k < BLOCK_K / 16; ++k) {  // 32 bytes of K per instruction
+            if constexpr (FP8)
+              ptx::umma_e4m3(d_tmem, ptx::smem_desc_sw128(sa + k * 32),
+                             ptx::smem_desc_sw128(sb + k * 32), idesc, (kb | k) != 0 ? 1u : 0u);
+            else
+              ptx::umma_bf16(d_tmem, ptx::smem_desc_sw128(sa + k * 32),
+                             ptx::smem_desc_sw128(sb + k * 32), idesc, (kb | k) != 0 ? 1u : 0u);
+          }
           ptx::umma_commit(&empty[s]);
         }
         if (!ok) break;
@@ -298,14 +335,32 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++lt) {
       const int acc = lt & 1;
       const uint32_t aph = static_cast<uint32_t>(lt >> 1) & 1u;
+      // the tile and, with fp8, its scales are fetched before the accumulator is ready, so
+      // their load latency hides under the tile's MMAs
+      const GTile t = decode_gtile(g, mt, tile);
+      const int r = t.r0 + q * 32 + lane;  // weight row of this thread within the expert
+      constexpr int NCH = C::TOKN / 32;    // token chunks of a tile
+      float w_s = 1.0f;
+      float x_s[NCH];                      // lane l: scale of token 32 c + l of the tile
+#pragma unroll
+      for (int c = 0; c < NCH; ++c) x_s[c] = 0.0f;
+      if constexpr (FP8) {
+        w_s = __ldg(g.w_scale + static_cast<size_t>(t.e) * mt * BLOCK_M + r);
+        int src[NCH];
+#pragma unroll
+        for (int c = 0; c < NCH; ++c) {
+          const int p = t.tok0 + c * 32 + lane;
+          src[c] = (c * 32 + lane < t.ntok) ? (g.gather ? __ldg(g.gather + p) : p) : -1;
+        }
+#pragma unroll
+        for (int c = 0; c < NCH; ++c) x_s[c] = src[c] >= 0 ? __ldg(g.x_scale + src[c]) : 0.0f;
+      }
       const bool got = ptx::mbar_wait(&tfull[acc], aph, abort_flag, limit);
       if (!__all_sync(0xffffffffu, got)) {
         if (lane == 0) graise(g, abort_flag, DEVERR_TIMEOUT_EPILOGUE);
         break;
       }
       ptx::tc_fence_after();
-      const GTile t = decode_gtile(g, mt, tile);
-      const int r = t.r0 + q * 32 + lane;  // weight row of this thread within the expert
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                              static_cast<uint32_t>(acc * C::ACC_COLS);
       const bool row_ok = r < g.M_w;  // the last weight tile of an expert may be partial
@@ -314,23 +369,49 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
         float v[32];
         ptx::tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(ch * 32), v);
         const int nv = min(32, t.ntok - ch * 32);
+        if constexpr (FP8) {
+          float xs = x_s[0];  // this chunk's scales (a register select, no local memory)
+#pragma unroll
+          for (int c = 1; c < NCH; ++c) xs = ch == c ? x_s[c] : xs;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = v[j] * w_s * __shfl_sync(0xffffffffu, xs, j);
+        }
         __nv_bfloat16* orow = g.out + static_cast<size_t>(t.tok0 + ch * 32) * g.ldo;
         if (g.epi == EPI_SITU) {
           // rows r (gate, lanes 0..15) and r + 16 (value, lanes 16..31) of one 32-row group
+          // hold feature f; lanes 0..15 evaluate it for the even tokens, lanes 16..31 for
+          // the odd ones, so every SiTU evaluation uses the whole warp
           const int f = ((t.r0 + q * 32) >> 1) + (lane & 15);
+          const bool hi = lane >= 16;
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const float val = __shfl_xor_sync(0xffffffffu, v[j], 16);
-            if (lane < 16 && j < nv)
-              orow[static_cast<size_t>(j) * g.ldo + f] =
-                  __float2bfloat16_rn(situ_g(v[j], val, c, inv_c));
+          for (int jp = 0; jp < 16; ++jp) {
+            const float x0 = __shfl_xor_sync(0xffffffffu, v[2 * jp], 16);
+            const float x1 = __shfl_xor_sync(0xffffffffu, v[2 * jp + 1], 16);
+            const float gv = hi ? x1 : v[2 * jp];       // gate of token 2jp (+1 on hi lanes)
+            const float vv = hi ? v[2 * jp + 1] : x0;   // value of the same token
+            const int j = 2 * jp + (hi ? 1 : 0);
+            // padding tokens hold finite values (a repeated valid row, or a zero scale)
+            const float hv = FP8 ? situ_close(gv, vv, c, inv_c) : situ_g(gv, vv, c, inv_c);
+            if (j < nv) orow[static_cast<size_t>(j) * g.ldo + f] = __float2bfloat16_rn(hv);
           }
-        } else {
-          if (row_ok) {
+        } else if (row_ok) {
+          // through shared memory: the warp's 32 rows x 32 tokens become, per token, four
+          // 16-byte pieces of its output row, so a store instruction writes 8 tokens' rows
+          // instead of one
+          __nv_bfloat16* st = epi_stage + (warp - 2) * (32 * 32);
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (j < nv) orow[static_cast<size_t>(j) * g.ldo + r] = __float2bfloat16_rn(v[j]);
+          for (int j = 0; j < 32; ++j) st[j * 32 + lane] = __float2bfloat16_rn(v[j]);
+          __syncwarp();
+          const int piece = lane & 3;
+#pragma unroll
+          for (int j0 = 0; j0 < 32; j0 += 8) {
+            const int j = j0 + (lane >> 2);
+            const uint4 val = *reinterpret_cast<const uint4*>(st + j * 32 + piece * 8);
+            if (j < nv)
+              *reinterpret_cast<uint4*>(orow + static_cast<size_t>(j) * g.ldo + t.r0 + q * 32 +
+                                        piece * 8) = val;
           }
+          __syncwarp();
         }
       }
       ptx::tc_fence_before();
@@ -346,11 +427,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
   }
 }
 
-template <int STAGES_>
+template <int STAGES_, bool FP8>
 static int launch_grouped_stages(const CUtensorMap& tw, const CUtensorMap& tx,
                                  const GroupedArgs& g, cudaStream_t stream) {
   using C = GroupedCfg<STAGES_>;
-  if (cudaFuncSetAttribute(grouped_gemm_kernel<STAGES_>,
+  if (cudaFuncSetAttribute(grouped_gemm_kernel<STAGES_, FP8>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) != cudaSuccess)
     return LMOE_ERR_CUDA;
   int dev = 0, sms = 0;
@@ -358,20 +439,30 @@ static int launch_grouped_stages(const CUtensorMap& tw, const CUtensorMap& tx,
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return LMOE_ERR_CUDA;
   const int grid = (g.max_ctas > 0 && g.max_ctas < sms) ? g.max_ctas : sms;
-  grouped_gemm_kernel<STAGES_><<<grid, GROUPED_THREADS, C::SMEM_BYTES, stream>>>(tw, tx, g);
+  grouped_gemm_kernel<STAGES_, FP8><<<grid, GROUPED_THREADS, C::SMEM_BYTES, stream>>>(tw, tx, g);
   return cudaGetLastError() == cudaSuccess ? LMOE_OK : LMOE_ERR_CUDA;
 }
 
 int launch_grouped_gemm(const void* W, const void* X, uint64_t x_rows, int x_ld,
                         const GroupedArgs& g, cudaStream_t stream) {
-  if (g.M_w <= 0 || g.Kd % BLOCK_K != 0 || g.Kd <= 0 || x_rows == 0) return LMOE_ERR_UNSUPPORTED;
+  const int kgran = g.fp8 ? 2 * BLOCK_K : BLOCK_K;  // elements per 128-byte K-block
+  if (g.M_w <= 0 || g.Kd % kgran != 0 || g.Kd <= 0 || x_rows == 0) return LMOE_ERR_UNSUPPORTED;
   if (g.epi != EPI_SITU && g.epi != EPI_BF16) return LMOE_ERR_UNSUPPORTED;
   if (g.epi == EPI_SITU && g.M_w % BLOCK_M != 0) return LMOE_ERR_UNSUPPORTED;
+  if (g.fp8 && (!g.w_scale || !g.x_scale || x_ld % 2 != 0)) return LMOE_ERR_INVALID_ARG;
+  // From here on the kernel counts K in units of 2 bytes: an e4m3 row of Kd codes is
+  // addressed as Kd / 2 bf16-sized pairs, so tiles, boxes, swizzle and the gather offsets
+  // are the same bytes for both operand types.
+  GroupedArgs ga = g;
+  const int kd = g.fp8 ? g.Kd / 2 : g.Kd;
+  const int ld = g.fp8 ? x_ld / 2 : x_ld;
+  ga.Kd = kd;
+  if (g.fp8) ga.ldx = g.ldx / 2;
   CUtensorMap tw, tx;
   const uint64_t w_rows = static_cast<uint64_t>(g.E) * ceil_div(g.M_w, BLOCK_M) *
-                          (g.Kd / BLOCK_K) * BLOCK_M;  // tiled: rows of 64 bf16
+                          (kd / BLOCK_K) * BLOCK_M;  // tiled: rows of 128 bytes
   if (!make_tmap_bf16(&tw, W, w_rows, BLOCK_K, BLOCK_K, BLOCK_M) ||
-      !make_tmap_bf16(&tx, X, x_rows, static_cast<uint64_t>(g.Kd), static_cast<uint64_t>(x_ld),
+      !make_tmap_bf16(&tx, X, x_rows, static_cast<uint64_t>(kd), static_cast<uint64_t>(ld),
                       GROUPED_BOX_T))
     return LMOE_ERR_CUDA;
   const bool shallow = g.epi != EPI_SITU && g.mean_tokens >= GROUPED_SHALLOW_MIN_TOKENS;
@@ -379,10 +470,12 @@ int launch_grouped_gemm(const void* W, const void* X, uint64_t x_rows, int x_ld,
   // every weight row tile of an expert re-reads, in L2 (gate/value 1.20 -> 1.11 ms at the K3
   // prefill shape).  The down GEMM at prefill measured no gain (its output write-back shares
   // L2), so it keeps the default policy there.
-  GroupedArgs ga = g;
   ga.evict_first = (g.epi == EPI_SITU || !shallow) ? 1 : 0;
-  return shallow ? launch_grouped_stages<GROUPED_STAGES_SHALLOW>(tw, tx, ga, stream)
-                 : launch_grouped_stages<GROUPED_STAGES_DEEP>(tw, tx, ga, stream);
+  if (g.fp8)
+    return shallow ? launch_grouped_stages<GROUPED_STAGES_SHALLOW, true>(tw, tx, ga, stream)
+                   : launch_grouped_stages<GROUPED_STAGES_DEEP, true>(tw, tx, ga, stream);
+  return shallow ? launch_grouped_stages<GROUPED_STAGES_SHALLOW, false>(tw, tx, ga, stream)
+                 : launch_grouped_stages<GROUPED_STAGES_DEEP, false>(tw, tx, ga, stream);
 }
 
 }  // namespace lmoe

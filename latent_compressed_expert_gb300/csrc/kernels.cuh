@@ -11,12 +11,14 @@ namespace lmoe {
 // Offsets (bytes) of the pieces of the packed weight buffer; every piece 1024-aligned.
 struct PackedLayout {
   size_t w1, wr, wgu, wed, w2, gamma, total;
+  size_t sgu, sed;  // e4m3 experts: per-row scales of wgu / wed
 };
 
 // Offsets (bytes) of the forward workspace; every buffer 256-aligned.
 struct WorkspaceLayout {
   size_t err, lat, logits, logits_t, tau, idx, gate, masks, base, offsets, ct_off, inv, src_tok,
       h, o, zh, ys, total;
+  size_t lat8, slat, h8, sh;  // e4m3 experts: quantised latent and SiTU output, row scales
 };
 
 PackedLayout packed_layout(const lmoe_dims& D);
@@ -63,6 +65,7 @@ struct GroupedArgs {
   int E;                  // experts
   int M_w;                // weight rows per expert (2I for gate/value, L for down)
   int Kd;                 // reduction length (L for gate/value, I for down), multiple of 64
+                          // (of 128 with fp8)
   const int32_t* seg_off; // [E+1] first token row of each expert's segment
   const int32_t* ct_off;  // [E+1] prefix sum of ceil(count / GROUPED_TOKN)
   const int32_t* gather;  // [rows] source row of each permuted row, or null: then the
@@ -78,9 +81,16 @@ struct GroupedArgs {
   int max_ctas;           // persistent grid limit (0: one CTA per SM)
   int mean_tokens;        // average tokens per expert (T*K/E): picks the pipeline depth
   int evict_first;        // set by the launcher: weights loaded with an L2 evict-first policy
+  // e4m3 operands: W and x hold codes, Kd and ldx count codes, a K-block is 128 codes (the
+  // same 128 bytes per row as 64 bf16); the accumulator is multiplied by the weight row's
+  // and the activation row's scale in the epilogue
+  int fp8;
+  const float* w_scale;   // [E * ceil(M_w / 128) * 128] per weight row
+  const float* x_scale;   // per activation row, indexed like the rows (through gather)
 };
 
-// W: the experts' weights in 128 x 64 tiles ordered (expert, row tile, column tile).
+// W: the experts' weights in tiles of 128 rows x 128 bytes (64 bf16 or 128 e4m3 codes),
+// ordered (expert, row tile, column tile).
 int launch_grouped_gemm(const void* W, const void* X, uint64_t x_rows, int x_ld,
                         const GroupedArgs& g, cudaStream_t stream);
 
@@ -110,6 +120,13 @@ int launch_dispatch(const int32_t* idx, int T, int E, int K, uint32_t* masks, ui
 int launch_combine(const __nv_bfloat16* o, const float* gate, const int32_t* inv,
                    const float* gamma, int T, int K, int L, float eps, __nv_bfloat16* z,
                    int ldz, cudaStream_t stream);
+// Per-row e4m3 quantisation of bf16 rows (cols % 16 == 0): codes [rows, ldq], scales [rows].
+int launch_quantize_rows(const __nv_bfloat16* x, int64_t rows, int cols, int64_t ldx,
+                         uint8_t* q, int64_t ldq, float* scales, cudaStream_t stream);
+// Expert weights -> e4m3 tiles of 128 rows x 128 codes + per-row scales (see quant.cu).
+int launch_pack_tiled_e4m3(uint8_t* dst, float* scales, const __nv_bfloat16* w,
+                           const __nv_bfloat16* w_g, const __nv_bfloat16* w_v, int glu, int E,
+                           int M_w, int Kd, cudaStream_t stream);
 int launch_pack(const lmoe_dims& D, const lmoe_weights& w, const PackedLayout& P, uint8_t* base,
                 cudaStream_t stream);
 

@@ -7,6 +7,8 @@
 //   Wgu                  per expert, gate/value rows interleaved in groups of 16 likewise,
 //                        stored as tiles (below)
 //   Wed                  routed down-projections, stored as tiles (below)
+//   (expert_fp8: Wgu and Wed hold e4m3 codes in tiles of 128 rows x 128 codes, the same
+//   16 KB, plus one fp32 scale per row in Sgu / Sed; see quant.cu)
 //   W2  [d, L + S Is]    row n = [ W_up[n, :] | W_sd[0][n, :] | ... | W_sd[S-1][n, :] ]
 //   gamma [L] fp32
 // Tiled expert weights: an expert's [M_w, Kd] matrix is cut into 128-row x 64-column tiles,
@@ -135,13 +137,26 @@ int launch_pack(const lmoe_dims& D, const lmoe_weights& w, const PackedLayout& P
   a.v = static_cast<const bf*>(w.w_svalue);
   if ((rc = run_pack(a, stream)) != LMOE_OK) return rc;
 
-  if ((rc = run_pack_tiled(reinterpret_cast<bf*>(base + P.wgu), nullptr,
-                           static_cast<const bf*>(w.w_gate), static_cast<const bf*>(w.w_value), 1,
-                           D.E, 2 * D.I, D.L, stream)) != LMOE_OK)
-    return rc;
-  if ((rc = run_pack_tiled(reinterpret_cast<bf*>(base + P.wed), static_cast<const bf*>(w.w_edown),
-                           nullptr, nullptr, 0, D.E, D.L, D.I, stream)) != LMOE_OK)
-    return rc;
+  if (D.expert_fp8) {
+    if ((rc = launch_pack_tiled_e4m3(base + P.wgu, reinterpret_cast<float*>(base + P.sgu),
+                                     nullptr, static_cast<const bf*>(w.w_gate),
+                                     static_cast<const bf*>(w.w_value), 1, D.E, 2 * D.I, D.L,
+                                     stream)) != LMOE_OK)
+      return rc;
+    if ((rc = launch_pack_tiled_e4m3(base + P.wed, reinterpret_cast<float*>(base + P.sed),
+                                     static_cast<const bf*>(w.w_edown), nullptr, nullptr, 0, D.E,
+                                     D.L, D.I, stream)) != LMOE_OK)
+      return rc;
+  } else {
+    if ((rc = run_pack_tiled(reinterpret_cast<bf*>(base + P.wgu), nullptr,
+                             static_cast<const bf*>(w.w_gate), static_cast<const bf*>(w.w_value),
+                             1, D.E, 2 * D.I, D.L, stream)) != LMOE_OK)
+      return rc;
+    if ((rc = run_pack_tiled(reinterpret_cast<bf*>(base + P.wed),
+                             static_cast<const bf*>(w.w_edown), nullptr, nullptr, 0, D.E, D.L,
+                             D.I, stream)) != LMOE_OK)
+      return rc;
+  }
 
   a.job = PACK_W2;
   a.rows = D.d;

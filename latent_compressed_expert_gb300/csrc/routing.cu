@@ -163,6 +163,7 @@ constexpr int TH_THREADS = 256;
 constexpr int TH_BINS = 4096;
 constexpr int TH_CAND = 4096;
 constexpr int TH_SMEM_MAX_T = 32768;
+static_assert(512 % TH_THREADS == 0 && TH_THREADS / 32 <= 8, "bin ranges and warp sums");
 
 struct KthResult {
   uint32_t key;  // score bits of the k-th largest score of the column
@@ -176,7 +177,8 @@ __device__ __forceinline__ KthResult select_kth_score(const float* __restrict__ 
                                                      int64_t stride_t, int k,
                                                      uint32_t* th_smem, bool staged) {
   uint32_t* hist = th_smem;                       // [TH_BINS]
-  uint32_t* ctl = th_smem + TH_BINS;              // [0] digit, [1] new k, [2] in bin, [3] count
+  uint32_t* ctl = th_smem + TH_BINS;              // [0] digit, [1] new k, [2] in bin,
+                                                  // [3] count, [8..16) warp sums
   uint32_t* cand = th_smem + TH_BINS + 32;        // [TH_CAND]
   uint32_t* vals = cand + TH_CAND;                // [T] when staged
   const int lane = threadIdx.x & 31;
@@ -224,23 +226,30 @@ __device__ __forceinline__ KthResult select_kth_score(const float* __restrict__ 
       if (in) atomicAdd(&hist[(key >> sh) & dm], 1u);
     }
     __syncthreads();
-    if (threadIdx.x < 32) {
-      // lane l owns bins [per l, per l + per); counts of the bins above its range
-      const int per = nbins / 32;
-      uint32_t mine = 0u;  // each lane starts at a different bank
-      for (int b = 0; b < per; ++b) mine += hist[lane * per + ((b + lane) & (per - 1))];
-      uint32_t incl = mine;  // inclusive suffix sum over lanes >= lane
+    {
+      // thread i owns bins [per i, per i + per); a block-wide suffix sum gives the count
+      // above its range, and the one thread whose range holds the krem-th key finds its bin
+      const int per = nbins / TH_THREADS;
+      const int warp = threadIdx.x >> 5;
+      const int b0 = threadIdx.x * per;
+      uint32_t mine = 0u;  // neighbouring lanes start at different banks
+      for (int b = 0; b < per; ++b) mine += hist[b0 + ((b + lane) & (per - 1))];
+      uint32_t incl = mine;  // inclusive suffix sum over the lanes >= lane of this warp
       for (int o = 1; o < 32; o <<= 1) {
         const uint32_t v = __shfl_down_sync(0xffffffffu, incl, o);
         if (lane + o < 32) incl += v;
       }
-      const uint32_t above = incl - mine;
-      if (above < static_cast<uint32_t>(krem) && static_cast<uint32_t>(krem) <= incl) {
+      if (lane == 0) ctl[8 + warp] = incl;  // warp total
+      __syncthreads();
+      uint32_t above_w = 0u;  // keys in the warps above this one
+      for (int w = warp + 1; w < TH_THREADS / 32; ++w) above_w += ctl[8 + w];
+      const uint32_t above = above_w + incl - mine;
+      if (above < static_cast<uint32_t>(krem) && static_cast<uint32_t>(krem) <= above + mine) {
         uint32_t cum = above;
         for (int b = per - 1; b >= 0; --b) {
-          const uint32_t h = hist[lane * per + b];
+          const uint32_t h = hist[b0 + b];
           if (cum + h >= static_cast<uint32_t>(krem)) {
-            ctl[0] = static_cast<uint32_t>(lane * per + b);
+            ctl[0] = static_cast<uint32_t>(b0 + b);
             ctl[1] = static_cast<uint32_t>(krem) - cum;
             ctl[2] = h;
             break;

@@ -28,7 +28,7 @@ _vp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_
 
 class Dims(ctypes.Structure):
     _fields_ = [("T", _i), ("d", _i), ("L", _i), ("E", _i), ("K", _i), ("I", _i), ("S", _i),
-                ("Is", _i), ("c", _f), ("eps", _f)]
+                ("Is", _i), ("c", _f), ("eps", _f), ("expert_fp8", _i)]
 
 
 class Weights(ctypes.Structure):
@@ -62,6 +62,7 @@ SIGNATURES = {
     "lmoe_workspace_bytes": (_sz, [ctypes.POINTER(Dims)]),
     "lmoe_thresholds": (_i, [_vp, _i, _i, _i, _i, _vp, _vp]),
     "lmoe_threshold_candidates": (_i, [_vp, _i, _i, _i, _vp, _vp]),
+    "lmoe_quantize_e4m3": (_i, [_vp, ctypes.c_longlong, _i, _vp, _vp, _vp]),
     "lmoe_route": (_i, [_vp, _vp, _i, _i, _i, _vp, _vp, _vp, _vp]),
     "lmoe_forward": (_i, [ctypes.POINTER(Dims), _vp, _vp, _vp, _vp, _vp, _sz, ctypes.POINTER(IO),
                           _vp]),
@@ -128,14 +129,15 @@ def _expect(t, dtype, shape, name):
                          f"{tuple(t.shape)}")
 
 
-def make_dims(T, d, L, E, K, I, S, Is, c=100.0, eps=1e-6) -> Dims:
-    return Dims(T, d, L, E, K, I, S, Is, c, eps)
+def make_dims(T, d, L, E, K, I, S, Is, c=100.0, eps=1e-6, expert_fp8=False) -> Dims:
+    return Dims(T, d, L, E, K, I, S, Is, c, eps, 1 if expert_fp8 else 0)
 
 
-def dims_of(shape, T=None) -> Dims:
+def dims_of(shape, T=None, expert_fp8=False) -> Dims:
     """Dims from an object with T, d, L, E, K, I, S, Is (and optionally c, eps)."""
     return make_dims(shape.T if T is None else T, shape.d, shape.L, shape.E, shape.K, shape.I,
-                     shape.S, shape.Is, getattr(shape, "c", 100.0), getattr(shape, "eps", 1e-6))
+                     shape.S, shape.Is, getattr(shape, "c", 100.0), getattr(shape, "eps", 1e-6),
+                     expert_fp8)
 
 
 def packed_bytes(dims: Dims) -> int:
@@ -180,6 +182,17 @@ def thresholds(logits: torch.Tensor, K: int, k_rank: int = 0, stream=None) -> to
     _check(load().lmoe_thresholds(_ptr(logits), T, E, K, k_rank, _ptr(tau), _stream(stream)),
            "lmoe_thresholds")
     return tau
+
+
+def quantize_e4m3(x: torch.Tensor, stream=None):
+    """Per-row e4m3 codes (uint8) and fp32 scales of bf16 rows (lmoe_quantize_e4m3)."""
+    rows, cols = x.shape
+    _expect(x, torch.bfloat16, (rows, cols), "x")
+    codes = torch.empty((rows, cols), dtype=torch.uint8, device=x.device)
+    scales = torch.empty(rows, dtype=torch.float32, device=x.device)
+    _check(load().lmoe_quantize_e4m3(_ptr(x), rows, cols, _ptr(codes), _ptr(scales),
+                                     _stream(stream)), "lmoe_quantize_e4m3")
+    return codes, scales
 
 
 def fair_share_rank(T: int, K: int, E: int) -> int:
@@ -258,14 +271,16 @@ class Layer:
     to ``max_tokens`` tokens.  ``forward`` is one lmoe_forward call."""
 
     def __init__(self, shape, weights: dict, max_tokens: int | None = None, stream=None,
-                 overlap: bool = False, shared_sms: int = 0):
+                 overlap: bool = False, shared_sms: int = 0, expert_fp8: bool = False):
         """overlap: run the shared experts on an auxiliary stream beside the routed path for
         batches of at least OVERLAP_MIN_T tokens (shared_sms SMs for them; 0 = a third).
         Off by default: the routed expert GEMMs are limited per SM, so the SMs lent to the
-        shared experts slow them down more than the concurrency gains."""
+        shared experts slow them down more than the concurrency gains.
+        expert_fp8: routed experts with e4m3 operands (weights quantised when packed)."""
         self.shape = shape
+        self.expert_fp8 = expert_fp8
         self.max_tokens = shape.T if max_tokens is None else max_tokens
-        self.dims = dims_of(shape, T=self.max_tokens)
+        self.dims = dims_of(shape, T=self.max_tokens, expert_fp8=expert_fp8)
         self.device = weights["w_down"].device
         self.packed = pack_weights(self.dims, weights, stream)
         self.ws_bytes = workspace_bytes(self.dims)
@@ -299,7 +314,7 @@ class Layer:
             _expect(residual, torch.bfloat16, (T, sh.d), "residual")
         if y is None:
             y = torch.empty((T, sh.d), dtype=torch.bfloat16, device=x.device)
-        dims = dims_of(sh, T=T)
+        dims = dims_of(sh, T=T, expert_fp8=self.expert_fp8)
         io = IO()
         io.balance = 1 if balance else 0
         io.phase = phase

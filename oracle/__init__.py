@@ -77,6 +77,8 @@ def _load():
         lib.oracle_e4m3_encode.argtypes = [ctypes.c_float]
         lib.oracle_bf16_round.restype = ctypes.c_float
         lib.oracle_bf16_round.argtypes = [ctypes.c_double]
+        lib.oracle_bf16_tie_distance.restype = ctypes.c_double
+        lib.oracle_bf16_tie_distance.argtypes = [ctypes.c_double]
         for name in ("oracle_quantize_rows", "oracle_routed_fp8"):
             getattr(lib, name).restype = None
         for name in ("oracle_latent", "oracle_router_logits", "oracle_scores",
@@ -262,8 +264,20 @@ def quantize_expert_weights(w_gate, w_value, w_edown) -> dict:
     return out
 
 
-def routed_fp8(lat, idx, gate, wq: dict, gamma, c=100.0, eps=1e-6):
-    """Routed experts with e4m3 operands (weights from quantize_expert_weights)."""
+def bf16_tie_distance(x) -> np.ndarray:
+    """Relative distance of each value from the nearest bf16 rounding tie."""
+    lib = _load()
+    xd = np.asarray(x, dtype=np.float64)
+    return np.array([lib.oracle_bf16_tie_distance(float(v)) for v in xd.ravel()]).reshape(xd.shape)
+
+
+def routed_fp8(lat, idx, gate, wq: dict, gamma, c=100.0, eps=1e-6, tie_margin=2.0 ** -16,
+               return_ties=False):
+    """Routed experts with e4m3 operands (weights from quantize_expert_weights).
+    return_ties: also return, per token, how many of its quantised rows (its latent and its
+    K SiTU outputs) have a scale that hinges on a bf16 rounding near-tie (relative distance
+    below tie_margin): there an evaluation that differs in the last fp32 bits may quantise
+    the whole row differently."""
     lat = np.ascontiguousarray(lat, dtype=np.float64)
     idx = np.ascontiguousarray(idx, dtype=np.int32)
     gate = np.ascontiguousarray(gate, dtype=np.float32)
@@ -277,11 +291,13 @@ def routed_fp8(lat, idx, gate, wq: dict, gamma, c=100.0, eps=1e-6):
     assert sg.shape == sv.shape == (E, I) and sd.shape == (E, L)
     assert n == 0 or (idx.min() >= 0 and idx.max() < E)
     z = np.empty((n, L), dtype=np.float64)
+    ties = np.zeros(n, dtype=np.int32)
     _load().oracle_routed_fp8(n, L, E, K, I, _p(lat, _dbl_p), _p(idx, _i32_p),
                               _p(gate, _flt_p), _p(qg, _u8_p), _p(sg, _flt_p), _p(qv, _u8_p),
                               _p(sv, _flt_p), _p(qd, _u8_p), _p(sd, _flt_p), _p(gamma, _flt_p),
-                              ctypes.c_double(c), ctypes.c_double(eps), _p(z, _dbl_p))
-    return z
+                              ctypes.c_double(c), ctypes.c_double(eps), _p(z, _dbl_p),
+                              _p(ties, _i32_p), ctypes.c_double(tie_margin))
+    return (z, ties) if return_ties else z
 
 
 def shared(x, w_sgate, w_svalue, w_sdown, c=100.0):
@@ -325,6 +341,7 @@ class OracleResult:
     gate: np.ndarray         # [n, K] fp32
     z: np.ndarray            # [n, L] fp64 normalised aggregated latent
     ys: np.ndarray           # [n, d] fp64 shared-expert output
+    scale_ties: np.ndarray | None = None  # expert_fp8: per token, rows quantised at a near-tie
 
 
 def forward(w: dict, x, K: int, residual=None, tau="batch", logits_in=None, c=100.0,
@@ -357,11 +374,13 @@ def forward(w: dict, x, K: int, residual=None, tau="batch", logits_in=None, c=10
     gamma = w["gamma"]
     if hasattr(gamma, "detach"):
         gamma = gamma.detach().float().cpu().numpy()
+    ties = None
     if expert_fp8:
         wq = quantize_expert_weights(w["w_gate"], w["w_value"], w["w_edown"])
-        z = routed_fp8(lat, idx, gate, wq, gamma, c, eps)
+        z, ties = routed_fp8(lat, idx, gate, wq, gamma, c, eps, return_ties=True)
     else:
         z = routed(lat, idx, gate, w["w_gate"], w["w_value"], w["w_edown"], gamma, c, eps)
     ys = shared(xs, w["w_sgate"], w["w_svalue"], w["w_sdown"], c)
     y = output(z, ys, w["w_up"], residual)
-    return OracleResult(y=y, lat=lat, logits=lg, tau=tau_v, idx=idx, gate=gate, z=z, ys=ys)
+    return OracleResult(y=y, lat=lat, logits=lg, tau=tau_v, idx=idx, gate=gate, z=z, ys=ys,
+                        scale_ties=ties)

@@ -416,6 +416,36 @@ float oracle_bf16_round(double x) {
   return (float)ldexp(q, ex - 8);
 }
 
+/* Relative distance of x from the nearest bf16 rounding tie (the midpoint between two
+ * neighbouring bf16 values).  Small values mean that a slightly different evaluation of x
+ * may round to the other neighbour. */
+double oracle_bf16_tie_distance(double x) {
+  if (x == 0.0 || isnan(x) || isinf(x)) return INFINITY;
+  int ex;
+  frexp(x, &ex);
+  const double ulp = ldexp(1.0, ex - 8);          /* bf16 spacing at |x| */
+  const double a = fabs(x);
+  const double lo = floor(a / ulp) * ulp;          /* bf16 neighbour below |x| */
+  return fabs(a - (lo + 0.5 * ulp)) / a;
+}
+
+/* 1 when the scale of a row of values (quantised from their bf16 roundings) depends on a
+ * near-tie: some element within 2^-6 of the row's largest bf16 magnitude lies within
+ * `margin` (relative) of a bf16 rounding tie, so that an evaluation of the row that differs
+ * in the last fp32 bits may pick another amax, another scale, and other codes. */
+static int scale_near_tie(const double *x, int n, double margin) {
+  float amax = 0.0f;
+  for (int i = 0; i < n; ++i) {
+    const float a = fabsf(oracle_bf16_round(x[i]));
+    if (a > amax) amax = a;
+  }
+  for (int i = 0; i < n; ++i)
+    if (fabs(x[i]) >= (double)amax * (1.0 - ldexp(1.0, -6)) &&
+        oracle_bf16_tie_distance(x[i]) < margin)
+      return 1;
+  return 0;
+}
+
 /* Routed experts with e4m3 operands, aggregation and RMSNorm (the fp8 reading above).
  * Weights arrive quantised: qg, qv [E, I, L] with sg, sv [E, I]; qd [E, L, I] with sd [E, L].
  * The latent row of a token is rounded to bf16 and quantised; the SiTU output of each
@@ -427,7 +457,7 @@ void oracle_routed_fp8(int n, int L, int E, int K, int I, const double *lat,
                        const int32_t *idx, const float *gate, const uint8_t *qg,
                        const float *sg, const uint8_t *qv, const float *sv,
                        const uint8_t *qd, const float *sd, const float *gamma, double c,
-                       double eps, double *z) {
+                       double eps, double *z, int32_t *scale_ties, double tie_margin) {
   (void)E;
   double dq[256];
   for (int i = 0; i < 256; ++i) dq[i] = oracle_e4m3_decode((uint8_t)i);
@@ -435,9 +465,11 @@ void oracle_routed_fp8(int n, int L, int E, int K, int I, const double *lat,
   for (int t = 0; t < n; ++t) {
     double *u = (double *)calloc((size_t)L, sizeof(double));
     float *row = (float *)malloc(sizeof(float) * (size_t)(L > I ? L : I));
+    double *hx = (double *)malloc(sizeof(double) * (size_t)I);
     uint8_t *ql = (uint8_t *)malloc((size_t)L);
     uint8_t *qh = (uint8_t *)malloc((size_t)I);
     float s_lat, s_h;
+    int ties = scale_near_tie(lat + (size_t)t * L, L, tie_margin);
     for (int l = 0; l < L; ++l) row[l] = oracle_bf16_round(lat[(size_t)t * L + l]);
     oracle_quantize_rows(1, L, row, ql, &s_lat);
     for (int j = 0; j < K; ++j) {
@@ -452,8 +484,10 @@ void oracle_routed_fp8(int n, int L, int E, int K, int I, const double *lat,
         }
         ag *= (double)sg[wr] * (double)s_lat;
         av *= (double)sv[wr] * (double)s_lat;
-        row[i] = oracle_bf16_round(oracle_situ(ag, av, c));
+        hx[i] = oracle_situ(ag, av, c);
+        row[i] = oracle_bf16_round(hx[i]);
       }
+      ties += scale_near_tie(hx, I, tie_margin);
       oracle_quantize_rows(1, I, row, qh, &s_h);
       for (int l = 0; l < L; ++l) {
         const size_t wr = (size_t)e * L + l;
@@ -467,8 +501,10 @@ void oracle_routed_fp8(int n, int L, int E, int K, int I, const double *lat,
     ms /= (double)L;
     const double inv = 1.0 / sqrt(ms + eps);
     for (int l = 0; l < L; ++l) z[(size_t)t * L + l] = (double)gamma[l] * u[l] * inv;
+    if (scale_ties) scale_ties[t] = ties;
     free(u);
     free(row);
+    free(hx);
     free(ql);
     free(qh);
   }

@@ -62,6 +62,23 @@ def test_size_queries(lib):
     assert 0 < lmoe.workspace_bytes(lmoe.dims_of(synth.PREFILL, T=0)) < 1 << 20
 
 
+def test_fp8_size_queries(lib):
+    sh = synth.PREFILL
+    d16 = lmoe.dims_of(sh)
+    d8 = lmoe.dims_of(sh, expert_fp8=True)
+    routed = sh.E * 3 * sh.I * sh.L
+    # the routed experts take one byte per weight plus a fp32 scale per row
+    scales = sh.E * (2 * sh.I + sh.L) * 4
+    assert lmoe.packed_bytes(d16) - lmoe.packed_bytes(d8) == pytest.approx(routed - scales,
+                                                                         abs=8 * 1024)
+    # the workspace adds the quantised latent and SiTU output with their scales
+    extra = sh.T * (sh.L + 4) + sh.T * sh.K * (sh.I + 4)
+    assert lmoe.workspace_bytes(d8) - lmoe.workspace_bytes(d16) == pytest.approx(extra,
+                                                                                abs=2048)
+    # FP8 needs L and I in multiples of 128 (one 128-byte K-block of codes)
+    assert lmoe.packed_bytes(lmoe.dims_of(synth.TINY, expert_fp8=True)) == 0
+
+
 @no_gpu
 @pytest.mark.parametrize("field,value,code", [
     ("d", 100, lmoe.LMOE_ERR_UNSUPPORTED),    # not a multiple of 64
@@ -163,3 +180,9 @@ def test_phase_and_candidate_argument_checks(lib):
     assert c(fake, 10, 8, 0, fake, None) == lmoe.LMOE_ERR_INVALID_ARG   # k < 1
     assert c(fake, 10, 0, 4, fake, None) == lmoe.LMOE_ERR_INVALID_ARG   # E < 1
     assert c(fake, -1, 8, 4, fake, None) == lmoe.LMOE_ERR_INVALID_ARG   # T < 0
+    # lmoe_quantize_e4m3
+    q = lib.lmoe_quantize_e4m3
+    assert q(None, 4, 16, fake, fake, None) == lmoe.LMOE_ERR_INVALID_ARG
+    assert q(fake, -1, 16, fake, fake, None) == lmoe.LMOE_ERR_INVALID_ARG
+    assert q(fake, 4, 24, fake, fake, None) == lmoe.LMOE_ERR_UNSUPPORTED  # cols % 16
+    assert q(None, 0, 16, None, None, None) == lmoe.LMOE_OK

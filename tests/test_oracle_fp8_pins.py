@@ -165,3 +165,28 @@ def test_routed_fp8_error_is_that_of_a_3_bit_mantissa(oracle_mod):
     assert np.array_equal(r16.idx, r8.idx)             # routing is not quantised
     rel = np.sqrt(np.mean((r8.z - r16.z) ** 2)) / np.sqrt(np.mean(r16.z ** 2))
     assert 1e-3 < rel < 0.1, rel
+
+
+def test_bf16_tie_distance(oracle_mod):
+    d = oracle_mod.bf16_tie_distance(np.array([1.0, 1.0 + 2.0 ** -8, -(1.0 + 2.0 ** -8),
+                                               1.75 + 2.0 ** -8, 3.0 + 2.0 ** -7]))
+    assert d[0] == pytest.approx(2.0 ** -8)          # a bf16 value: half a spacing away
+    assert d[1] == 0.0 and d[2] == 0.0 and d[3] == 0.0 and d[4] == 0.0   # exact ties
+
+
+def test_routed_fp8_flags_scales_set_at_a_near_tie(oracle_mod):
+    """A token whose latent amax sits on a bf16 rounding tie is flagged; the others are
+    not (their rows are exact e4m3 multiples of a power of two, far from any tie)."""
+    rng = np.random.default_rng(6)
+    n, L, E, K, I = 6, 64, 4, 2, 1
+    lat = _exact_rows(rng, n, L, -8)
+    lat[2, 0] = 1.75 + 2.0 ** -8                    # amax at the midpoint of two bf16 values
+    wg = _exact_rows(rng, E * I, L, -9).reshape(E, I, L)
+    wv = _exact_rows(rng, E * I, L, -10).reshape(E, I, L)
+    wd = np.ones((E, L, I))
+    idx = np.stack([rng.choice(E, K, replace=False) for _ in range(n)]).astype(np.int32)
+    gate = np.full((n, K), 0.5, dtype=np.float32)
+    wq = oracle_mod.quantize_expert_weights(_bf16(wg), _bf16(wv), _bf16(wd))
+    _, ties = oracle_mod.routed_fp8(lat, idx, gate, wq, np.ones(L, np.float32),
+                                    return_ties=True)
+    assert ties.tolist() == [0, 0, 1, 0, 0, 0]
