@@ -471,7 +471,8 @@ def run_ours(args):
         roof = {"bound": "hbm", "achieved": dw["bytes"] / t_s / 1e9, "peak": peaks["hbm_gbs"],
                 "unit": "GB/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = ncu_traffic(dom, "stages_fp8" if wl.fp8 else "stages")
+    roof["traffic"] = ncu_traffic(dom, "stages_fp8" if wl.fp8 and dom.startswith("expert")
+                                  else "stages")
     roof["kernel"] = dom
     roof["peak_source"] = f"{peak_src} ({'bf16 sustained' if roof['bound'] == 'tensor' else 'HBM copy'})"
     roof["algorithmic"] = {"flop": dw["flop"], "bytes": dw["bytes"]}
