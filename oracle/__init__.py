@@ -71,6 +71,7 @@ def _load():
         lib.oracle_situ.restype = ctypes.c_double
         lib.oracle_situ.argtypes = [ctypes.c_double] * 3
         lib.oracle_num_threads.restype = ctypes.c_int
+        lib.oracle_sigmoid_decreases.restype = None
         lib.oracle_e4m3_decode.restype = ctypes.c_double
         lib.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
         lib.oracle_e4m3_encode.restype = ctypes.c_uint8
@@ -113,6 +114,14 @@ def num_threads() -> int:
 
 def sigmoid32(z: float) -> float:
     return float(_load().oracle_sigmoid32(ctypes.c_float(z)))
+
+
+def sigmoid_decreases() -> tuple[int, int]:
+    """(steps down by one ulp, larger steps down) of the routing score between consecutive
+    fp32 inputs, over all of [-88, 88]."""
+    a, b = ctypes.c_longlong(), ctypes.c_longlong()
+    _load().oracle_sigmoid_decreases(ctypes.byref(a), ctypes.byref(b))
+    return int(a.value), int(b.value)
 
 
 def scores(logits: np.ndarray) -> np.ndarray:

@@ -144,6 +144,39 @@ float oracle_sigmoid32(float z) {
   return 1.0f / den;
 }
 
+/* Decreases of the routing score between consecutive fp32 inputs, over every fp32 value in
+ * [-88, 88] in increasing order (outside it the clamp makes the score constant): *one_ulp
+ * counts steps down by exactly one ulp, *more counts larger ones.  The sequence of fp32
+ * roundings is not monotone everywhere, so the k-th largest score of a set of logits need
+ * not be the score of its k-th largest logit: selections are made on the scores. */
+void oracle_sigmoid_decreases(long long *one_ulp, long long *more) {
+  const uint32_t NEG = 0xC2B00000u; /* -88.0f */
+  const uint32_t POS = 0x42B00000u; /* +88.0f */
+  const long long nneg = (long long)(NEG - 0x80000000u) + 1; /* -88 ... -0 */
+  const long long n = nneg + (long long)POS + 1;               /* ... +0 ... +88 */
+  long long c1 = 0, c2 = 0;
+#pragma omp parallel for schedule(static) reduction(+ : c1, c2)
+  for (long long c = 0; c < 4096; ++c) {
+    const long long i0 = n * c / 4096, i1 = n * (c + 1) / 4096;
+    float prev = 0.0f;
+    for (long long i = (i0 > 0 ? i0 - 1 : 0); i < i1; ++i) {
+      const uint32_t bits = i < nneg ? NEG - (uint32_t)i : (uint32_t)(i - nneg);
+      float z;
+      memcpy(&z, &bits, 4);
+      const float sc = oracle_sigmoid32(z);
+      if (i >= i0 && i > 0 && sc < prev) {
+        if (nextafterf(sc, 2.0f) == prev)
+          ++c1;
+        else
+          ++c2;
+      }
+      prev = sc;
+    }
+  }
+  *one_ulp = c1;
+  *more = c2;
+}
+
 void oracle_scores(long long count, const float *logits, float *scores) {
 #pragma omp parallel for schedule(static)
   for (long long i = 0; i < count; ++i) scores[i] = oracle_sigmoid32(logits[i]);

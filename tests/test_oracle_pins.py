@@ -64,6 +64,17 @@ def test_sigmoid_symmetry_and_monotone(oracle_mod):
         assert np.all(np.diff(ss.astype(np.float64)) >= 0.0), centre
 
 
+def test_sigmoid_is_monotone_up_to_one_ulp_over_all_fp32(oracle_mod):
+    """Every fp32 input in [-88, 88], in increasing order (2.24e9 values; outside the clamp
+    the score is constant).  The score never steps down by more than one ulp, and it does
+    step down by one ulp in a few hundred places (the roundings of the polynomial and the
+    division): a selection by score is not a selection by logit, which is why thresholds,
+    candidates and top-K all compare the scores themselves."""
+    one, more = oracle_mod.sigmoid_decreases()
+    assert more == 0
+    assert 0 < one < 10_000, one
+
+
 # ----------------------------------------------------------------------------------------
 # Quantile-Balancing thresholds
 # ----------------------------------------------------------------------------------------
