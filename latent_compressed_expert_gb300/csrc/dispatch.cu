@@ -25,6 +25,8 @@ dispatch_mask_kernel(const int32_t* __restrict__ idx, int T, int E, int K,
                      uint32_t* __restrict__ done) {
   extern __shared__ uint32_t m_smem[];
   const int b = blockIdx.x;
+  pdl_wait();
+  pdl_launch_dependents();
   if (b == 0 && threadIdx.x == 0) *done = 0u;  // completion counter of the column scan
   for (int e = threadIdx.x; e < E; e += blockDim.x) m_smem[e] = 0u;
   __syncthreads();
@@ -62,6 +64,8 @@ dispatch_scan_kernel(const uint32_t* __restrict__ masks, int nb, int E,
   __shared__ uint32_t part[SCAN_WARPS][32];
   __shared__ int32_t wsum[2][SCAN_WARPS];
   __shared__ bool last;
+  pdl_wait();
+  pdl_launch_dependents();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int e = blockIdx.x * 32 + lane;
   const int per = (nb + SCAN_WARPS - 1) / SCAN_WARPS;
@@ -149,6 +153,8 @@ dispatch_scatter_kernel(const int32_t* __restrict__ idx, const uint32_t* __restr
                         const uint32_t* __restrict__ base, const int32_t* __restrict__ offsets,
                         int T, int E, int K, int32_t* __restrict__ inv,
                         int32_t* __restrict__ src_tok) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int64_t p = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (p >= static_cast<int64_t>(T) * K) return;
   const int t = static_cast<int>(p / K);
@@ -178,6 +184,8 @@ combine_rmsnorm_kernel(const __nv_bfloat16* __restrict__ o, const float* __restr
   __shared__ int32_t rows[32];
   __shared__ float gates[32];
   __shared__ float warp_ss[32];
+  pdl_wait();
+  pdl_launch_dependents();
   const int t = blockIdx.x;
   if (threadIdx.x < K) {
     rows[threadIdx.x] = __ldg(inv + static_cast<size_t>(t) * K + threadIdx.x);
@@ -256,19 +264,20 @@ int launch_dispatch(const int32_t* idx, int T, int E, int K, uint32_t* masks, ui
   const size_t msmem = static_cast<size_t>(E) * sizeof(uint32_t);
   uint32_t* done = err + 1;  // the word after the error flag
   if (nb > 0) {
-    dispatch_mask_kernel<<<nb, 256, msmem, stream>>>(idx, T, E, K, masks, err, done);
-    if (cudaGetLastError() != cudaSuccess) return LMOE_ERR_CUDA;
+    if (launch_pdl(dispatch_mask_kernel, nb, 256, msmem, stream, idx, T, E, K, masks, err, done) !=
+        cudaSuccess)
+      return LMOE_ERR_CUDA;
   } else if (cudaMemsetAsync(done, 0, sizeof(uint32_t), stream) != cudaSuccess) {
     return LMOE_ERR_CUDA;
   }
-  dispatch_scan_kernel<<<static_cast<unsigned>(ceil_div(E, 32)), SCAN_THREADS, 0, stream>>>(
-      masks, nb, E, base, offsets, ct_off, counts_out, done);
-  if (cudaGetLastError() != cudaSuccess) return LMOE_ERR_CUDA;
+  if (launch_pdl(dispatch_scan_kernel, static_cast<unsigned>(ceil_div(E, 32)), SCAN_THREADS, 0,
+                 stream, masks, nb, E, base, offsets, ct_off, counts_out, done) != cudaSuccess)
+    return LMOE_ERR_CUDA;
   if (nb > 0) {
     const int64_t pairs = static_cast<int64_t>(T) * K;
-    dispatch_scatter_kernel<<<static_cast<unsigned>(ceil_div(pairs, 256)), 256, 0, stream>>>(
-        idx, masks, base, offsets, T, E, K, inv, src_tok);
-    if (cudaGetLastError() != cudaSuccess) return LMOE_ERR_CUDA;
+    if (launch_pdl(dispatch_scatter_kernel, static_cast<unsigned>(ceil_div(pairs, 256)), 256, 0,
+                   stream, idx, masks, base, offsets, T, E, K, inv, src_tok) != cudaSuccess)
+      return LMOE_ERR_CUDA;
   }
   return LMOE_OK;
 }
@@ -281,8 +290,10 @@ int launch_combine(const __nv_bfloat16* o, const float* gate, const int32_t* inv
   const int threads = static_cast<int>(
       ceil_div(nvec < COMBINE_MAX_THREADS ? nvec : COMBINE_MAX_THREADS, 32) * 32);
   if (nvec > COMBINE_MAX_VEC * threads) return LMOE_ERR_UNSUPPORTED;
-  combine_rmsnorm_kernel<<<T, threads, 0, stream>>>(o, gate, inv, gamma, T, K, L, eps, z, ldz);
-  return cudaGetLastError() == cudaSuccess ? LMOE_OK : LMOE_ERR_CUDA;
+  return launch_pdl(combine_rmsnorm_kernel, T, threads, 0, stream, o, gate, inv, gamma, T, K, L,
+                    eps, z, ldz) == cudaSuccess
+             ? LMOE_OK
+             : LMOE_ERR_CUDA;
 }
 
 }  // namespace lmoe

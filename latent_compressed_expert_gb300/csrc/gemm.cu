@@ -257,6 +257,8 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA,
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  pdl_wait();  // from here on: the previous kernel's outputs are visible
+  pdl_launch_dependents();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -426,8 +428,10 @@ static int launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArg
   const int64_t tiles = ceil_div(g.M, BLOCK_M) * ceil_div(g.N, BN);
   if (tiles < grid) grid = static_cast<int>(tiles);
   if (grid <= 0) return LMOE_OK;
-  gemm_tcgen05_kernel<BN><<<grid, GEMM_THREADS, C::SMEM_BYTES, stream>>>(ta, tb, g);
-  return cudaGetLastError() == cudaSuccess ? LMOE_OK : LMOE_ERR_CUDA;
+  return launch_pdl(gemm_tcgen05_kernel<BN>, grid, GEMM_THREADS, C::SMEM_BYTES, stream, ta, tb, g) ==
+                 cudaSuccess
+             ? LMOE_OK
+             : LMOE_ERR_CUDA;
 }
 
 int launch_gemm(const void* A, uint64_t a_rows, int a_ld, const void* B, uint64_t b_rows,

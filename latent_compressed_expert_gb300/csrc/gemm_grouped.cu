@@ -169,7 +169,6 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int mt = (g.M_w + BLOCK_M - 1) / BLOCK_M;
   const int nk = g.Kd / BLOCK_K;
-  const int total = __ldg(g.ct_off + g.E) * mt;
   const uint64_t limit = g.timeout_ns;
 
   if (threadIdx.x == 0) {
@@ -200,6 +199,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  pdl_wait();  // from here on: the previous kernel's outputs (segments, rows) are visible
+  pdl_launch_dependents();
+  const int total = __ldg(g.ct_off + g.E) * mt;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -439,8 +441,10 @@ static int launch_grouped_stages(const CUtensorMap& tw, const CUtensorMap& tx,
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return LMOE_ERR_CUDA;
   const int grid = (g.max_ctas > 0 && g.max_ctas < sms) ? g.max_ctas : sms;
-  grouped_gemm_kernel<STAGES_, FP8><<<grid, GROUPED_THREADS, C::SMEM_BYTES, stream>>>(tw, tx, g);
-  return cudaGetLastError() == cudaSuccess ? LMOE_OK : LMOE_ERR_CUDA;
+  return launch_pdl(grouped_gemm_kernel<STAGES_, FP8>, grid, GROUPED_THREADS, C::SMEM_BYTES,
+                    stream, tw, tx, g) == cudaSuccess
+             ? LMOE_OK
+             : LMOE_ERR_CUDA;
 }
 
 int launch_grouped_gemm(const void* W, const void* X, uint64_t x_rows, int x_ld,

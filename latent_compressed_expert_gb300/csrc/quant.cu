@@ -52,6 +52,8 @@ __device__ __forceinline__ float warp_max(float v) {
 __global__ void __launch_bounds__(QUANT_WARPS * 32)
 quantize_rows_kernel(const __nv_bfloat16* __restrict__ x, int64_t rows, int cols, int64_t ldx,
                      uint8_t* __restrict__ q, int64_t ldq, float* __restrict__ scales) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int64_t r = static_cast<int64_t>(blockIdx.x) * QUANT_WARPS + (threadIdx.x >> 5);
   if (r >= rows) return;
@@ -87,9 +89,10 @@ int launch_quantize_rows(const __nv_bfloat16* x, int64_t rows, int cols, int64_t
   if (rows == 0) return LMOE_OK;
   if (cols <= 0 || cols % 16 || ldx % 8 || ldq % 16) return LMOE_ERR_UNSUPPORTED;
   const int64_t grid = ceil_div(rows, QUANT_WARPS);
-  quantize_rows_kernel<<<static_cast<unsigned>(grid), QUANT_WARPS * 32, 0, stream>>>(
-      x, rows, cols, ldx, q, ldq, scales);
-  return cudaGetLastError() == cudaSuccess ? LMOE_OK : LMOE_ERR_CUDA;
+  return launch_pdl(quantize_rows_kernel, static_cast<unsigned>(grid), QUANT_WARPS * 32, 0, stream,
+                    x, rows, cols, ldx, q, ldq, scales) == cudaSuccess
+             ? LMOE_OK
+             : LMOE_ERR_CUDA;
 }
 
 // Expert weights -> e4m3 tiles of 128 rows x 128 codes (16 KB, ordered (expert, row tile,

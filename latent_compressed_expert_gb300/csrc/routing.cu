@@ -71,6 +71,9 @@ route_kernel(const float* __restrict__ logits, const float* __restrict__ tau, in
              int K, int32_t* __restrict__ idx, float* __restrict__ gate,
              float* __restrict__ scores_out) {
   extern __shared__ uint32_t route_smem[];
+  pdl_wait();
+  pdl_launch_dependents();
+
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint32_t* keys = route_smem + static_cast<size_t>(warp) * E;
   const int t = blockIdx.x * ROUTE_WARPS + warp;
@@ -298,6 +301,9 @@ __global__ void __launch_bounds__(TH_THREADS)
 thresholds_kernel(const float* __restrict__ z, int T, int64_t stride_t, int64_t stride_e,
                   int k, float* __restrict__ tau) {
   extern __shared__ uint32_t th_smem[];
+  pdl_wait();
+  pdl_launch_dependents();
+
   const int e = blockIdx.x;
   const KthResult r = select_kth_score(z + static_cast<int64_t>(e) * stride_e, T, stride_t, k,
                                        th_smem, T <= TH_SMEM_MAX_T);
@@ -314,6 +320,9 @@ __global__ void __launch_bounds__(TH_THREADS)
 candidates_kernel(const float* __restrict__ z, int T, int64_t stride_t, int64_t stride_e,
                   int k, float* __restrict__ cand, int64_t ldc) {
   extern __shared__ uint32_t th_smem[];
+  pdl_wait();
+  pdl_launch_dependents();
+
   __shared__ uint32_t wsum[2][TH_THREADS / 32];
   __shared__ uint32_t run[2];
   const int e = blockIdx.x;
@@ -376,6 +385,9 @@ candidates_kernel(const float* __restrict__ z, int T, int64_t stride_t, int64_t 
 __global__ void __launch_bounds__(256)
 transpose_f32_kernel(const float* __restrict__ in, int T, int E, float* __restrict__ out) {
   __shared__ float tile[32][33];
+  pdl_wait();
+  pdl_launch_dependents();
+
   const int e0 = blockIdx.x * 32, t0 = blockIdx.y * 32;
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8
   for (int i = ty; i < 32; i += 8) {
@@ -402,9 +414,10 @@ int launch_route(const float* logits, const float* tau, int T, int E, int K, int
       return LMOE_ERR_CUDA;
   }
   const int grid = static_cast<int>(ceil_div(T, ROUTE_WARPS));
-  route_kernel<<<grid, ROUTE_WARPS * 32, smem, stream>>>(logits, tau, T, E, K, idx, gate,
-                                                         scores_out);
-  return cudaGetLastError() == cudaSuccess ? LMOE_OK : LMOE_ERR_CUDA;
+  return launch_pdl(route_kernel, grid, ROUTE_WARPS * 32, smem, stream, logits, tau, T, E, K, idx,
+                    gate, scores_out) == cudaSuccess
+             ? LMOE_OK
+             : LMOE_ERR_CUDA;
 }
 
 int launch_thresholds(const float* z, int T, int E, int64_t stride_t, int64_t stride_e, int k,
@@ -417,8 +430,10 @@ int launch_thresholds(const float* z, int T, int E, int64_t stride_t, int64_t st
                              static_cast<int>(smem)) != cudaSuccess)
       return LMOE_ERR_CUDA;
   }
-  thresholds_kernel<<<E, TH_THREADS, smem, stream>>>(z, T, stride_t, stride_e, k, tau);
-  return cudaGetLastError() == cudaSuccess ? LMOE_OK : LMOE_ERR_CUDA;
+  return launch_pdl(thresholds_kernel, E, TH_THREADS, smem, stream, z, T, stride_t, stride_e, k,
+                    tau) == cudaSuccess
+             ? LMOE_OK
+             : LMOE_ERR_CUDA;
 }
 
 int launch_candidates(const float* z, int T, int E, int64_t stride_t, int64_t stride_e, int k,
@@ -431,15 +446,18 @@ int launch_candidates(const float* z, int T, int E, int64_t stride_t, int64_t st
                              static_cast<int>(smem)) != cudaSuccess)
       return LMOE_ERR_CUDA;
   }
-  candidates_kernel<<<E, TH_THREADS, smem, stream>>>(z, T, stride_t, stride_e, k, cand, ldc);
-  return cudaGetLastError() == cudaSuccess ? LMOE_OK : LMOE_ERR_CUDA;
+  return launch_pdl(candidates_kernel, E, TH_THREADS, smem, stream, z, T, stride_t, stride_e, k,
+                    cand, ldc) == cudaSuccess
+             ? LMOE_OK
+             : LMOE_ERR_CUDA;
 }
 
 int launch_transpose_f32(const float* in, int T, int E, float* out, cudaStream_t stream) {
   if (T == 0) return LMOE_OK;
   const dim3 grid(static_cast<unsigned>(ceil_div(E, 32)), static_cast<unsigned>(ceil_div(T, 32)));
-  transpose_f32_kernel<<<grid, 256, 0, stream>>>(in, T, E, out);
-  return cudaGetLastError() == cudaSuccess ? LMOE_OK : LMOE_ERR_CUDA;
+  return launch_pdl(transpose_f32_kernel, grid, 256, 0, stream, in, T, E, out) == cudaSuccess
+             ? LMOE_OK
+             : LMOE_ERR_CUDA;
 }
 
 }  // namespace lmoe
