@@ -80,7 +80,8 @@ def _load():
         lib.oracle_bf16_round.argtypes = [ctypes.c_double]
         lib.oracle_bf16_tie_distance.restype = ctypes.c_double
         lib.oracle_bf16_tie_distance.argtypes = [ctypes.c_double]
-        for name in ("oracle_quantize_rows", "oracle_routed_fp8"):
+        for name in ("oracle_quantize_rows", "oracle_routed_fp8", "oracle_tau_ema",
+                     "oracle_load_stats_update"):
             getattr(lib, name).restype = None
         for name in ("oracle_latent", "oracle_router_logits", "oracle_scores",
                      "oracle_thresholds", "oracle_route", "oracle_situ_vec",
@@ -154,6 +155,27 @@ def thresholds(logits: np.ndarray, k: int) -> np.ndarray:
     tau = np.empty(E, dtype=np.float32)
     _load().oracle_thresholds(T, E, int(k), _p(lg, _flt_p), _p(tau, _flt_p))
     return tau
+
+
+def tau_ema(tau_ema_prev, tau_step, beta: float, first: bool = False) -> np.ndarray:
+    """One step of the streaming thresholds: fma(beta, prev - step, step) in fp32."""
+    step = np.ascontiguousarray(tau_step, dtype=np.float32)
+    out = (np.array(step) if tau_ema_prev is None
+           else np.ascontiguousarray(tau_ema_prev, dtype=np.float32).copy())
+    _load().oracle_tau_ema(len(step), ctypes.c_float(beta), 1 if first else 0,
+                           _p(step, _flt_p), _p(out, _flt_p))
+    return out
+
+
+def load_stats_update(acc, counts) -> np.ndarray:
+    """Accumulate one step's per-expert counts into the 64-bit counters (4 + 4E)."""
+    c = np.ascontiguousarray(counts, dtype=np.int32)
+    E = len(c)
+    a = (np.zeros(4 + 4 * E, dtype=np.uint64) if acc is None
+         else np.ascontiguousarray(acc, dtype=np.uint64).copy())
+    _load().oracle_load_stats_update(E, _p(c, _i32_p),
+                                     a.ctypes.data_as(ctypes.POINTER(ctypes.c_ulonglong)))
+    return a
 
 
 def route(logits: np.ndarray, tau, K: int):

@@ -542,3 +542,40 @@ void oracle_routed_fp8(int n, int L, int E, int K, int I, const double *lat,
     free(qh);
   }
 }
+
+/* ------------------------------------------------------------------------------------ */
+/* Streaming thresholds.  [IK3] Quantile Balancing passage: thresholds are read off the
+ * distribution of the router scores at each step.  A threshold that persists across steps
+ * (for decode batches too small to carry a quantile, or to damp step-to-step noise) is the
+ * exponential moving average of the per-step thresholds -- a reading; the pages do not
+ * name one.  In fp32, one subtraction and one fused multiply-add:
+ *   tau_ema <- fma(beta, tau_ema - tau_step, tau_step)   (= beta tau_ema + (1-beta) tau_step)
+ * and on the first step tau_ema <- tau_step.                                              */
+void oracle_tau_ema(int E, float beta, int first, const float *tau_step, float *tau_ema) {
+  for (int e = 0; e < E; ++e)
+    tau_ema[e] = first ? tau_step[e] : fmaf(beta, tau_ema[e] - tau_step[e], tau_step[e]);
+}
+
+/* Load statistics over steps ([IK3]: the balancing exists so that no expert sits idle while
+ * a few monopolise the traffic).  acc, 64-bit counters (4 + 4E), updated from one step's
+ * per-expert token counts:
+ *   acc[0] steps, acc[1] routed pairs, acc[2] sum over steps of max_e count,
+ *   acc[3] largest count of any expert in any step,
+ *   acc[4 + e] sum of counts of e, acc[4 + E + e] sum of squared counts of e,
+ *   acc[4 + 2E + e] steps in which e received no token, acc[4 + 3E + e] largest count of e. */
+void oracle_load_stats_update(int E, const int32_t *counts, unsigned long long *acc) {
+  unsigned long long pairs = 0, mx = 0;
+  for (int e = 0; e < E; ++e) {
+    const unsigned long long c = (unsigned long long)counts[e];
+    pairs += c;
+    if (c > mx) mx = c;
+    acc[4 + e] += c;
+    acc[4 + E + e] += c * c;
+    acc[4 + 2 * E + e] += c == 0 ? 1 : 0;
+    if (c > acc[4 + 3 * E + e]) acc[4 + 3 * E + e] = c;
+  }
+  acc[0] += 1;
+  acc[1] += pairs;
+  acc[2] += mx;
+  if (mx > acc[3]) acc[3] = mx;
+}

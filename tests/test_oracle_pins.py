@@ -419,3 +419,45 @@ def test_all_experts_without_balancing_is_dense_moe(oracle_mod):
     ref = _dense_masked(oracle_mod, r.lat, idx_all, G.astype(np.float32), w)
     assert np.allclose(r.z, ref, rtol=1e-6, atol=1e-6)
     assert sorted(r.idx[0].tolist()) == list(range(sh.E))
+
+
+# ----------------------------------------------------------------------------------------
+# streaming thresholds and load statistics
+# ----------------------------------------------------------------------------------------
+def test_tau_ema_limits_and_convergence(oracle_mod):
+    rng = np.random.default_rng(7)
+    a = rng.uniform(0.3, 0.9, 50).astype(np.float32)
+    b = rng.uniform(0.3, 0.9, 50).astype(np.float32)
+    assert np.array_equal(oracle_mod.tau_ema(a, b, 0.0), b)             # beta 0: this step
+    assert np.array_equal(oracle_mod.tau_ema(a, b, 1.0), a)             # beta 1: frozen
+    assert np.array_equal(oracle_mod.tau_ema(a, b, 0.9, first=True), b)  # initialisation
+    # a constant step threshold is approached geometrically: |t_n - b| <= beta^n |t_0 - b|
+    t = a.copy()
+    for n in range(1, 40):
+        t = oracle_mod.tau_ema(t, b, 0.75)
+        bound = 0.75 ** n * np.abs(a.astype(np.float64) - b) + n * 2.0 ** -24
+        assert np.all(np.abs(t.astype(np.float64) - b) <= bound)
+    # between the two: a convex combination
+    m = oracle_mod.tau_ema(a, b, 0.3).astype(np.float64)
+    assert np.all(m >= np.minimum(a, b) - 1e-7) and np.all(m <= np.maximum(a, b) + 1e-7)
+
+
+def test_load_stats_accumulate_counts(oracle_mod):
+    rng = np.random.default_rng(8)
+    E = 16
+    steps = [rng.integers(0, 20, E) for _ in range(5)]
+    steps[2][3] = 0
+    acc = None
+    for c in steps:
+        acc = oracle_mod.load_stats_update(acc, c)
+    S = np.array(steps, dtype=np.int64)
+    assert acc[0] == 5 and acc[1] == S.sum() and acc[2] == S.max(1).sum() and acc[3] == S.max()
+    assert np.array_equal(acc[4:4 + E], S.sum(0))
+    assert np.array_equal(acc[4 + E:4 + 2 * E], (S * S).sum(0))
+    assert np.array_equal(acc[4 + 2 * E:4 + 3 * E], (S == 0).sum(0))
+    assert np.array_equal(acc[4 + 3 * E:], S.max(0))
+    # invariants: pairs are conserved, the per-step maximum bounds the mean, and the largest
+    # count of any expert is the largest per-expert maximum
+    assert acc[4:4 + E].sum() == acc[1]
+    assert acc[3] * acc[0] >= acc[2] and acc[3] == acc[4 + 3 * E:].max()
+    assert np.all(acc[4 + E:4 + 2 * E] * acc[0] >= acc[4:4 + E] ** 2)  # Cauchy-Schwarz
