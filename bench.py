@@ -254,8 +254,10 @@ SMALL = synth.LayerShape("small", T=1024, d=7168, L=3584, E=128, K=16, I=512, S=
 # the K3 routing shape (T=8192, E=896, top-16) with narrow widths: the threshold, top-K and
 # dispatch kernels run at full size on a device footprint of well under 1 GB
 ROUTING = synth.LayerShape("routing", T=8192, d=512, L=256, E=896, K=16, I=64, S=2, Is=128)
+# the alternative pool the pages weigh against 896 / top-16: 448 experts, 8 per token
+POOL448 = synth.LayerShape("pool448", T=8192, d=7168, L=3584, E=448, K=8, I=512, S=2, Is=2048)
 SHAPES = {"prefill": synth.PREFILL, "decode": synth.DECODE, "e64": synth.E64,
-          "skew": synth.SKEW, "small": SMALL, "routing": ROUTING}
+          "skew": synth.SKEW, "small": SMALL, "routing": ROUTING, "pool448": POOL448}
 DESCRIPTIONS = {
     "prefill": "K3 Stable Latent MoE layer, prefill: in-batch Quantile-Balancing thresholds; "
                "x~N(0,1) with 0.1% of elements x1000; residual = x",
@@ -267,6 +269,9 @@ DESCRIPTIONS = {
             "bias (router GEMM not in the step), in-batch thresholds; x~N(0,1); residual = x",
     "small": "K3 widths, 128 experts, T=1024 (profiling case: ~128 tokens per expert as "
              "in prefill, a few GB on the device); x as in prefill",
+    "pool448": "K3 widths with the alternative pool of 448 routed experts, top-8 (the same "
+               "1/56 activation ratio, half the routed FLOPs); x as in prefill; in-batch "
+               "thresholds",
     "routing": "K3 routing shape with narrow widths (profiling case for the threshold, "
                "top-K and dispatch kernels at T=8192, E=896, top-16); x~N(0,1); in-batch "
                "thresholds",
@@ -282,7 +287,7 @@ class Workload:
         self.qb = qb
         self.fp8 = expert_fp8
         self.sh = sh = SHAPES[name]
-        outliers = name in ("prefill", "small")
+        outliers = name in ("prefill", "small", "pool448")
         gain = synth.outlier_router_gain(sh, OUTLIER_FRAC, OUTLIER_SCALE) if outliers else 1.0
         self.w = synth.make_weights(sh, SEED, device=dev, router_gain=gain)
         self.x = synth.make_x(sh, SEED + 1000 * rank, device=dev,
@@ -293,7 +298,7 @@ class Workload:
         self.kwargs = {}
         self.extra = {}
         if qb == "global":
-            if name not in ("prefill", "e64", "small", "routing"):
+            if name not in ("prefill", "e64", "small", "routing", "pool448"):
                 raise ValueError("--qb global applies to the in-batch-threshold workloads")
             # thresholds over all ranks' batches together (all-gather of candidates)
             self.kwargs["global_tokens"] = sh.T * world
@@ -502,8 +507,11 @@ def run_ours(args):
                     "d2h_bytes_per_step": y.numel() * 2},
             "gpu_launches": launches_per_step * args.steps}
 
+    fair = sh.T * sh.K / sh.E
+    line["load"] = {"max_over_mean": float(counts.max() / fair),
+                    "min_over_mean": float(counts.min() / fair),
+                    "idle_experts": int((counts == 0).sum())}
     if wl.name == "skew":
-        fair = sh.T * sh.K / sh.E
         line["load"] = {"before_balancing": wl.extra["load_before"],
                         "after_balancing": {"max_over_mean": float(counts.max() / fair),
                                             "min_over_mean": float(counts.min() / fair)}}

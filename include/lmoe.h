@@ -138,6 +138,14 @@ typedef struct lmoe_io {
   float *cand_out;       /* LMOE_PHASE_ROUTER only: [cand_k, E] threshold candidates of this
                             batch, as lmoe_threshold_candidates writes them */
   int cand_k;            /* rank the candidates serve (required with cand_out, >= 1) */
+  float *tau_ema;        /* [E] streaming thresholds, in/out, or NULL.  With tau_in == NULL
+                            and balance == 1: the batch's thresholds are solved, folded into
+                            tau_ema by lmoe_tau_ema (ema_beta, ema_first), and the batch is
+                            routed against the updated tau_ema (tau_out receives it) */
+  float ema_beta;        /* weight of the previous tau_ema, in [0, 1] */
+  int ema_first;         /* 1: this step initialises tau_ema to the batch's thresholds */
+  unsigned long long *load_stats; /* counters updated with this step's per-expert token
+                            counts, as lmoe_load_stats_update does, or NULL */
 } lmoe_io;
 
 /* lmoe_io.phase.  The layer splits where its only cross-batch quantity, the thresholds, is
@@ -198,6 +206,26 @@ int lmoe_thresholds(const float *logits, int T, int E, int K, int k_rank, float 
  * Errors: INVALID_ARG for null pointers, T < 0, E < 1, k < 1. */
 int lmoe_threshold_candidates(const float *logits, int T, int E, int k, float *cand,
                               void *stream);
+
+/* Streaming thresholds.  [IK3] Quantile Balancing passage: the thresholds are read off the
+ * distribution of the router scores at each step; the pages name no cross-step rule.
+ * Reading: a threshold that persists across steps (decode batches are too small to carry a
+ * quantile) is the exponential moving average of the per-step thresholds, in fp32:
+ *   tau_ema[e] = first ? tau_step[e] : fma(beta, tau_ema[e] - tau_step[e], tau_step[e]).
+ *   tau_step [E] (read), tau_ema [E] (read and written).
+ * Errors: INVALID_ARG for null pointers, E < 0, beta outside [0, 1]. */
+int lmoe_tau_ema(const float *tau_step, float *tau_ema, int E, float beta, int first,
+                 void *stream);
+
+/* Load statistics over steps ([IK3]: balancing keeps experts from sitting idle while a few
+ * take the traffic).  Adds one step's per-expert token counts [E] to the caller's 64-bit
+ * counters acc [4 + 4E] (zero them before the first step):
+ *   acc[0] steps, acc[1] routed (token, expert) pairs, acc[2] sum over steps of the largest
+ *   count, acc[3] largest count of any expert in any step; for each expert e: acc[4 + e] sum
+ *   of its counts, acc[4 + E + e] sum of their squares, acc[4 + 2E + e] steps in which it
+ *   received no token, acc[4 + 3E + e] its largest count.
+ * Errors: INVALID_ARG for null pointers or E < 1. */
+int lmoe_load_stats_update(const int32_t *counts, int E, unsigned long long *acc, void *stream);
 
 /* Top-K routing.  [TPP] Technical Details: a lightweight router selects 16 of 896 routed
  * experts per token; [SU]: Quantile Balancing replaces the predecessor's bias updates.

@@ -206,6 +206,20 @@ int lmoe_quantize_e4m3(const void* x, long long rows, int cols, uint8_t* codes, 
                               cols, scales, static_cast<cudaStream_t>(stream));
 }
 
+int lmoe_tau_ema(const float* tau_step, float* tau_ema, int E, float beta, int first,
+                 void* stream) {
+  if (E < 0 || !(beta >= 0.0f && beta <= 1.0f)) return LMOE_ERR_INVALID_ARG;
+  if (E == 0) return LMOE_OK;
+  if (!tau_step || !tau_ema) return LMOE_ERR_INVALID_ARG;
+  return launch_tau_ema(tau_step, tau_ema, E, beta, first ? 1 : 0,
+                        static_cast<cudaStream_t>(stream));
+}
+
+int lmoe_load_stats_update(const int32_t* counts, int E, unsigned long long* acc, void* stream) {
+  if (E < 1 || !counts || !acc) return LMOE_ERR_INVALID_ARG;
+  return launch_load_stats(counts, nullptr, E, acc, static_cast<cudaStream_t>(stream));
+}
+
 int lmoe_threshold_candidates(const float* logits, int T, int E, int k, float* cand,
                               void* stream) {
   if (T < 0 || E < 1 || k < 1 || !cand || (T > 0 && !logits)) return LMOE_ERR_INVALID_ARG;
@@ -283,6 +297,7 @@ int lmoe_forward(const lmoe_dims* dims, const void* packed, const void* x, const
   if (ws_bytes < W.total) return LMOE_ERR_WORKSPACE_TOO_SMALL;
   if ((opt.tau_in && !aligned16(opt.tau_in)) || (opt.logits_in && !aligned16(opt.logits_in)))
     return LMOE_ERR_INVALID_ARG;
+  if (opt.tau_ema && !(opt.ema_beta >= 0.0f && opt.ema_beta <= 1.0f)) return LMOE_ERR_INVALID_ARG;
 
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   using bf = __nv_bfloat16;
@@ -463,6 +478,13 @@ int lmoe_forward(const lmoe_dims* dims, const void* packed, const void* x, const
     if (rc != LMOE_OK) return rc;
     tau = t;
     launches += 1;
+    if (opt.tau_ema) {
+      // streaming thresholds: fold this batch's in, route against the result
+      rc = launch_tau_ema(t, opt.tau_ema, D.E, opt.ema_beta, opt.ema_first ? 1 : 0, stream);
+      if (rc != LMOE_OK) return rc;
+      tau = opt.tau_ema;
+      launches += 1;
+    }
   }
   if (!mark(LMOE_STAGE_ROUTE, 0)) return LMOE_ERR_CUDA;
   // 4. top-K routing
@@ -480,6 +502,11 @@ int lmoe_forward(const lmoe_dims* dims, const void* packed, const void* x, const
                        reinterpret_cast<uint32_t*>(ws + W.base), offsets, ct_off, inv, src_tok,
                        opt.counts_out, err, stream);
   if (rc != LMOE_OK) return rc;
+  if (opt.load_stats) {
+    rc = launch_load_stats(nullptr, offsets, D.E, opt.load_stats, stream);
+    if (rc != LMOE_OK) return rc;
+    launches += 1;
+  }
   if (!mark(LMOE_STAGE_EXPERT_GATE_UP, 3)) return LMOE_ERR_CUDA;
   // 6. routed gate/value GEMM with SiTU-GLU: h = SiTU(lat[src_tok] . W_gu[e]^T) per expert,
   //    the latent rows gathered inside the GEMM

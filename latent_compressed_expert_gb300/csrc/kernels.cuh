@@ -120,6 +120,12 @@ int launch_dispatch(const int32_t* idx, int T, int E, int K, uint32_t* masks, ui
 int launch_combine(const __nv_bfloat16* o, const float* gate, const int32_t* inv,
                    const float* gamma, int T, int K, int L, float eps, __nv_bfloat16* z,
                    int ldz, cudaStream_t stream);
+// Streaming thresholds: tau_ema = first ? tau_step : fma(beta, tau_ema - tau_step, tau_step).
+int launch_tau_ema(const float* tau_step, float* tau_ema, int E, float beta, int first,
+                   cudaStream_t stream);
+// Load counters (layout at lmoe_load_stats_update) from counts, or from segment offsets.
+int launch_load_stats(const int32_t* counts, const int32_t* offsets, int E,
+                      unsigned long long* acc, cudaStream_t stream);
 // Per-row e4m3 quantisation of bf16 rows (cols % 16 == 0): codes [rows, ldq], scales [rows].
 int launch_quantize_rows(const __nv_bfloat16* x, int64_t rows, int cols, int64_t ldx,
                          uint8_t* q, int64_t ldq, float* scales, cudaStream_t stream);

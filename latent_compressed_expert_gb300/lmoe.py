@@ -41,7 +41,8 @@ class IO(ctypes.Structure):
                 ("tau_out", _vp), ("idx_out", _vp), ("gate_out", _vp), ("counts_out", _vp),
                 ("stage_events", ctypes.POINTER(_vp)), ("kernel_launches", _i),
                 ("aux_stream", _vp), ("aux_events", _vp * 2), ("shared_sms", _i),
-                ("phase", _i), ("cand_out", _vp), ("cand_k", _i)]
+                ("phase", _i), ("cand_out", _vp), ("cand_k", _i),
+                ("tau_ema", _vp), ("ema_beta", _f), ("ema_first", _i), ("load_stats", _vp)]
 
 
 OVERLAP_MIN_T = 512  # LMOE_OVERLAP_MIN_T
@@ -63,6 +64,8 @@ SIGNATURES = {
     "lmoe_thresholds": (_i, [_vp, _i, _i, _i, _i, _vp, _vp]),
     "lmoe_threshold_candidates": (_i, [_vp, _i, _i, _i, _vp, _vp]),
     "lmoe_quantize_e4m3": (_i, [_vp, ctypes.c_longlong, _i, _vp, _vp, _vp]),
+    "lmoe_tau_ema": (_i, [_vp, _vp, _i, _f, _i, _vp]),
+    "lmoe_load_stats_update": (_i, [_vp, _i, _vp, _vp]),
     "lmoe_route": (_i, [_vp, _vp, _i, _i, _i, _vp, _vp, _vp, _vp]),
     "lmoe_forward": (_i, [ctypes.POINTER(Dims), _vp, _vp, _vp, _vp, _vp, _sz, ctypes.POINTER(IO),
                           _vp]),
@@ -195,6 +198,42 @@ def quantize_e4m3(x: torch.Tensor, stream=None):
     return codes, scales
 
 
+def tau_ema(tau_step: torch.Tensor, tau_ema_: torch.Tensor, beta: float, first: bool = False,
+            stream=None) -> torch.Tensor:
+    """Fold one step's thresholds into the streaming thresholds, in place (lmoe_tau_ema)."""
+    E = tau_step.shape[0]
+    _expect(tau_step, torch.float32, (E,), "tau_step")
+    _expect(tau_ema_, torch.float32, (E,), "tau_ema")
+    _check(load().lmoe_tau_ema(_ptr(tau_step), _ptr(tau_ema_), E, beta, 1 if first else 0,
+                               _stream(stream)), "lmoe_tau_ema")
+    return tau_ema_
+
+
+class LoadStats:
+    """64-bit per-expert load counters on the device (layout at lmoe_load_stats_update),
+    updated by ``Layer.forward(load_stats=...)`` or ``update(counts)``."""
+
+    def __init__(self, E: int, device):
+        self.E = E
+        self.acc = torch.zeros(4 + 4 * E, dtype=torch.int64, device=device)
+
+    def update(self, counts: torch.Tensor, stream=None):
+        _expect(counts, torch.int32, (self.E,), "counts")
+        _check(load().lmoe_load_stats_update(_ptr(counts), self.E, _ptr(self.acc),
+                                             _stream(stream)), "lmoe_load_stats_update")
+
+    def summary(self) -> dict:
+        a = self.acc.cpu().numpy().astype(float)
+        E, steps = self.E, max(a[0], 1.0)
+        mean = a[1] / steps / E                     # tokens per expert per step
+        per = a[4:4 + E] / steps
+        return {"steps": int(a[0]), "fair_share": mean,
+                "mean_max_over_mean": a[2] / steps / mean if mean else None,
+                "worst_max_over_mean": a[3] / mean if mean else None,
+                "expert_cv": float(per.std() / per.mean()) if per.mean() else None,
+                "idle_expert_steps": int(a[4 + 2 * E:4 + 3 * E].sum())}
+
+
 def fair_share_rank(T: int, K: int, E: int) -> int:
     """The threshold's rank among a column's T scores: max(1, floor(T*K/E)), at most T."""
     return max(1, min(T, (T * K) // E)) if T > 0 else 1
@@ -298,13 +337,17 @@ class Layer:
     def forward(self, x: torch.Tensor, residual: torch.Tensor | None = None, y=None,
                 tau: torch.Tensor | None = None, balance: bool = True,
                 logits_in: torch.Tensor | None = None, debug: bool = False, stream=None,
-                stage_events=None, phase: int = PHASE_ALL, cand_k: int = 0):
+                stage_events=None, phase: int = PHASE_ALL, cand_k: int = 0,
+                tau_ema: torch.Tensor | None = None, ema_beta: float = 0.9,
+                ema_first: bool = False, load_stats: "LoadStats | None" = None):
         """One lmoe_forward call.  stage_events: optional list of NUM_STAGES + 1
         torch.cuda.Event(enable_timing=True) recorded at the stage boundaries.  After the
         call, ``self.last_kernel_launches`` holds the number of kernels it launched.
         phase: PHASE_ALL, or one half of the layer: PHASE_ROUTER (returns the [cand_k, E]
         threshold candidates when cand_k > 0, else None) then PHASE_EXPERTS (x gives the
-        batch size only)."""
+        batch size only).  tau_ema: [E] streaming thresholds, updated in place with this
+        batch's (ema_beta, ema_first) and routed against.  load_stats: a LoadStats that this
+        step's per-expert counts are added to."""
         sh = self.shape
         T = x.shape[0]
         if T > self.max_tokens:
@@ -335,6 +378,13 @@ class Layer:
         if logits_in is not None:
             _expect(logits_in, torch.float32, (T, sh.E), "logits_in")
             io.logits_in = _ptr(logits_in)
+        if tau_ema is not None:
+            _expect(tau_ema, torch.float32, (sh.E,), "tau_ema")
+            io.tau_ema = _ptr(tau_ema)
+            io.ema_beta = ema_beta
+            io.ema_first = 1 if ema_first else 0
+        if load_stats is not None:
+            io.load_stats = _ptr(load_stats.acc)
         if debug:
             dev = x.device
             dbg["logits"] = torch.empty((T, sh.E), dtype=torch.float32, device=dev)

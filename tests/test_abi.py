@@ -186,3 +186,11 @@ def test_phase_and_candidate_argument_checks(lib):
     assert q(fake, -1, 16, fake, fake, None) == lmoe.LMOE_ERR_INVALID_ARG
     assert q(fake, 4, 24, fake, fake, None) == lmoe.LMOE_ERR_UNSUPPORTED  # cols % 16
     assert q(None, 0, 16, None, None, None) == lmoe.LMOE_OK
+    # streaming thresholds and load statistics
+    assert lib.lmoe_tau_ema(fake, fake, 8, 1.5, 0, None) == lmoe.LMOE_ERR_INVALID_ARG
+    assert lib.lmoe_tau_ema(None, fake, 8, 0.5, 0, None) == lmoe.LMOE_ERR_INVALID_ARG
+    assert lib.lmoe_tau_ema(None, None, 0, 0.5, 0, None) == lmoe.LMOE_OK
+    assert lib.lmoe_load_stats_update(fake, 0, fake, None) == lmoe.LMOE_ERR_INVALID_ARG
+    assert lib.lmoe_load_stats_update(None, 8, fake, None) == lmoe.LMOE_ERR_INVALID_ARG
+    assert fwd(fake, ctypes.c_void_p(0x2000), tau_ema=0x6000, ema_beta=2.0) \
+        == lmoe.LMOE_ERR_INVALID_ARG
