@@ -80,8 +80,9 @@ def _load():
         lib.oracle_bf16_round.argtypes = [ctypes.c_double]
         lib.oracle_bf16_tie_distance.restype = ctypes.c_double
         lib.oracle_bf16_tie_distance.argtypes = [ctypes.c_double]
+        lib.oracle_ep_dispatch.restype = ctypes.c_longlong
         for name in ("oracle_quantize_rows", "oracle_routed_fp8", "oracle_tau_ema",
-                     "oracle_load_stats_update"):
+                     "oracle_load_stats_update", "oracle_ep_combine"):
             getattr(lib, name).restype = None
         for name in ("oracle_latent", "oracle_router_logits", "oracle_scores",
                      "oracle_thresholds", "oracle_route", "oracle_situ_vec",
@@ -176,6 +177,52 @@ def load_stats_update(acc, counts) -> np.ndarray:
     _load().oracle_load_stats_update(E, _p(c, _i32_p),
                                      a.ctypes.data_as(ctypes.POINTER(ctypes.c_ulonglong)))
     return a
+
+
+_u32_p = ctypes.POINTER(ctypes.c_uint32)
+
+
+def ep_dispatch(idx, E: int, R: int, rows=None) -> dict:
+    """Expert-parallel dispatch over R ranks: the (token, rank) pairs in (rank, token) order,
+    their slot masks, and (with rows, bf16 [T, W]) the rows each pair carries."""
+    idx = np.ascontiguousarray(idx, dtype=np.int32)
+    T, K = idx.shape
+    assert E % R == 0
+    rr = None if rows is None else _u16(rows)
+    W = 0 if rr is None else rr.shape[1]
+    pmax = T * min(K, R)
+    off = np.zeros(R + 1, dtype=np.int32)
+    tok = np.zeros(pmax, dtype=np.int32)
+    slots = np.zeros(pmax, dtype=np.uint32)
+    srows = np.zeros((pmax, max(W, 1)), dtype=np.uint16)
+    P = _load().oracle_ep_dispatch(T, K, E, R, _p(idx, _i32_p), W,
+                                   None if rr is None else _p(rr, _u16_p), _p(off, _i32_p),
+                                   _p(tok, _i32_p), _p(slots, _u32_p),
+                                   None if rr is None else _p(srows, _u16_p))
+    out = {"P": int(P), "send_off": off, "send_tok": tok[:P], "send_slots": slots[:P]}
+    if rr is not None:
+        out["send_rows"] = srows[:P, :W]
+    return out
+
+
+def ep_combine(disp: dict, inv, gate, o, T: int):
+    """Expert-parallel combine: per pair the bf16 gate-weighted sum of its slots' output rows
+    (o: bf16 [T*K, W], rows addressed through inv [T, K]), then per token the fp32 sum of its
+    pairs' rows in rank order.  Returns (part uint16 [P, W], u fp32 [T, W])."""
+    inv = np.ascontiguousarray(inv, dtype=np.int32)
+    gate = np.ascontiguousarray(gate, dtype=np.float32)
+    ou = _u16(o)
+    K = inv.shape[1]
+    W = ou.shape[1]
+    P = disp["P"]
+    tok = np.ascontiguousarray(disp["send_tok"], dtype=np.int32)
+    slots = np.ascontiguousarray(disp["send_slots"], dtype=np.uint32)
+    part = np.zeros((P, W), dtype=np.uint16)
+    u = np.zeros((T, W), dtype=np.float32)
+    _load().oracle_ep_combine(T, K, ctypes.c_longlong(P), _p(tok, _i32_p), _p(slots, _u32_p),
+                              _p(inv, _i32_p), _p(gate, _flt_p), W, _p(ou, _u16_p),
+                              _p(part, _u16_p), _p(u, _flt_p))
+    return part, u
 
 
 def route(logits: np.ndarray, tau, K: int):

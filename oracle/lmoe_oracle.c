@@ -579,3 +579,72 @@ void oracle_load_stats_update(int E, const int32_t *counts, unsigned long long *
   acc[2] += mx;
   if (mx > acc[3]) acc[3] = mx;
 }
+
+/* ------------------------------------------------------------------------------------ */
+/* Expert-parallel dispatch and combine (the pages' layout, on one device).  [IK3] Stable
+ * LatentMoE and communication passages: experts live on different GPUs, each selected
+ * expert receives the token's (latent) vector, and the outputs travel back to be combined;
+ * compressing before the trip halves the bytes.  [TPP] Technical Details: 7168 -> 3584.
+ * Readings: R ranks host the E experts in equal contiguous blocks (expert e on rank
+ * e / (E/R)); a token's row travels once to every rank hosting at least one of its experts
+ * (with the mask of its slots served there); the expert side returns one row per such
+ * (token, rank) pair, the gate-weighted sum of its slots' outputs; the source sums the
+ * returned rows. */
+
+/* Dispatch: pairs (token, rank) in (rank, token) order.  send_off [R + 1], send_tok [P],
+ * send_slots [P] (bit j: slot j of the token goes to that rank), send_rows [P, W] (copies of
+ * the token's row, bf16 bits).  Returns P. */
+long long oracle_ep_dispatch(int T, int K, int E, int R, const int32_t *idx, int W,
+                             const uint16_t *rows, int32_t *send_off, int32_t *send_tok,
+                             uint32_t *send_slots, uint16_t *send_rows) {
+  const int per = E / R;
+  long long p = 0;
+  for (int r = 0; r < R; ++r) {
+    send_off[r] = (int32_t)p;
+    for (int t = 0; t < T; ++t) {
+      uint32_t slots = 0;
+      for (int j = 0; j < K; ++j)
+        if (idx[(size_t)t * K + j] / per == r) slots |= 1u << j;
+      if (!slots) continue;
+      send_tok[p] = t;
+      send_slots[p] = slots;
+      if (send_rows) memcpy(send_rows + (size_t)p * W, rows + (size_t)t * W, sizeof(uint16_t) * W);
+      ++p;
+    }
+  }
+  send_off[R] = (int32_t)p;
+  return p;
+}
+
+/* Combine, expert side: for each pair p, part[p] = bf16(sum over its slots j, ascending, of
+ * gate[t, j] * o_j accumulated in fp32 by fused multiply-adds), where o_j is the row
+ * o[inv[t, j]] (bf16 bits).  Source side: u[t] = sum over its pairs in rank order of the
+ * returned rows, in fp32. */
+static uint16_t f32_to_bf16_rn(float f) {
+  uint32_t u;
+  memcpy(&u, &f, 4);
+  if ((u & 0x7F800000u) == 0x7F800000u) return (uint16_t)(u >> 16 | ((u & 0xFFFF) ? 0x40 : 0));
+  u += 0x7FFFu + ((u >> 16) & 1u);
+  return (uint16_t)(u >> 16);
+}
+
+void oracle_ep_combine(int T, int K, long long P, const int32_t *send_tok,
+                       const uint32_t *send_slots, const int32_t *inv, const float *gate,
+                       int W, const uint16_t *o, uint16_t *part, float *u) {
+  for (long long p = 0; p < P; ++p) {
+    const int t = send_tok[p];
+    for (int w = 0; w < W; ++w) {
+      float acc = 0.0f;
+      for (int j = 0; j < K; ++j)
+        if (send_slots[p] >> j & 1u)
+          acc = fmaf(gate[(size_t)t * K + j], (float)bf(o[(size_t)inv[(size_t)t * K + j] * W + w]),
+                     acc);
+      part[(size_t)p * W + w] = f32_to_bf16_rn(acc);
+    }
+  }
+  for (size_t i = 0; i < (size_t)T * W; ++i) u[i] = 0.0f;
+  for (long long p = 0; p < P; ++p) { /* pairs are in rank order, so each u[t] sums ranks in order */
+    const int t = send_tok[p];
+    for (int w = 0; w < W; ++w) u[(size_t)t * W + w] += (float)bf(part[(size_t)p * W + w]);
+  }
+}

@@ -461,3 +461,68 @@ def test_load_stats_accumulate_counts(oracle_mod):
     assert acc[4:4 + E].sum() == acc[1]
     assert acc[3] * acc[0] >= acc[2] and acc[3] == acc[4 + 3 * E:].max()
     assert np.all(acc[4 + E:4 + 2 * E] * acc[0] >= acc[4:4 + E] ** 2)  # Cauchy-Schwarz
+
+
+# ----------------------------------------------------------------------------------------
+# expert-parallel dispatch and combine
+# ----------------------------------------------------------------------------------------
+def _ep_case(seed, T=40, K=6, E=48):
+    rng = np.random.default_rng(seed)
+    idx = np.stack([rng.choice(E, K, replace=False) for _ in range(T)]).astype(np.int32)
+    return rng, idx
+
+
+@pytest.mark.parametrize("R", [1, 4, 8, 48])
+def test_ep_dispatch_pairs(oracle_mod, R):
+    rng, idx = _ep_case(11)
+    T, K = idx.shape
+    E = 48
+    rows = torch.randn(T, 16).to(torch.bfloat16)
+    d = oracle_mod.ep_dispatch(idx, E, R, rows)
+    per = E // R
+    ranks = idx // per
+    # one pair per (token, distinct rank), in (rank, token) order
+    assert d["P"] == sum(len(set(ranks[t])) for t in range(T))
+    keys = [(int(r), int(t)) for r in range(R) for t in range(T) if r in set(ranks[t])]
+    got = [(r, int(t)) for r in range(R) for t in d["send_tok"][d["send_off"][r]:d["send_off"][r + 1]]]
+    assert got == keys
+    # every slot of every token goes to exactly one pair, the one of its expert's rank
+    seen = np.zeros((T, K), dtype=int)
+    for r in range(R):
+        for p in range(d["send_off"][r], d["send_off"][r + 1]):
+            t, sl = d["send_tok"][p], int(d["send_slots"][p])
+            for j in range(K):
+                if sl >> j & 1:
+                    assert ranks[t, j] == r
+                    seen[t, j] += 1
+    assert np.all(seen == 1)
+    # rows are copies of the token's row
+    assert np.array_equal(d["send_rows"], rows.view(torch.int16).numpy().view(np.uint16)[d["send_tok"]])
+    if R == 1:
+        assert d["P"] == T
+    if R == E:
+        assert d["P"] == T * K
+
+
+def test_ep_combine_sums_to_the_gated_mixture(oracle_mod):
+    """Summed over ranks, the returned rows give sum_j gate_j o_j: exactly so with one rank
+    (one fma chain over all slots, then one bf16 rounding), and within the bf16 rounding of
+    each rank's partial otherwise."""
+    rng, idx = _ep_case(12)
+    T, K = idx.shape
+    E, W = 48, 24
+    gate = rng.uniform(0.05, 0.3, (T, K)).astype(np.float32)
+    inv = rng.permutation(T * K).reshape(T, K).astype(np.int32)
+    o = torch.randn(T * K, W).to(torch.bfloat16)
+    of = o.float().numpy().astype(np.float64)
+    exact = np.einsum("tk,tkw->tw", gate.astype(np.float64), of[inv])
+    for R in (1, 4, 48):
+        d = oracle_mod.ep_dispatch(idx, E, R)
+        part, u = oracle_mod.ep_combine(d, inv, gate, o, T)
+        pf = (part.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+        bound = np.zeros((T, W))
+        for p in range(d["P"]):
+            bound[d["send_tok"][p]] += np.abs(pf[p]) * 2.0 ** -8 + 1e-6
+        assert np.all(np.abs(u - exact) <= bound + 1e-5 * np.abs(exact)), R
+        if R == 1:
+            assert np.array_equal(u, pf.astype(np.float32))
