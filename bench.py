@@ -533,13 +533,79 @@ def run_ours(args):
     return 0
 
 
+def run_ep(args):
+    """Expert-parallel dispatch and combine, packed and unpacked on one GPU, at the K3 prefill
+    routing shape over R ranks: the bytes that would cross the interconnect per token with
+    latent rows (L = 3584) against hidden rows (d = 7168), and the pack/unpack kernels' time.
+    The transfer itself is not run (one GPU)."""
+    world, rank, local = dist_setup(args.gpus)
+    dev = torch.device("cuda", local)
+    sh, R = synth.PREFILL, args.ep_ranks
+    T, K, E = sh.T, sh.K, sh.E
+    logits = synth.make_logits(T, E, SEED + rank, device=dev)
+    tau = lmoe.thresholds(logits, K)
+    idx, gate = lmoe.route(logits, tau, K)
+    # expert outputs in expert-segment order, as the routed GEMMs leave them
+    order = np.argsort(idx.cpu().numpy().ravel(), kind="stable")
+    inv = torch.from_numpy(np.argsort(order).astype(np.int32).reshape(T, K)).to(dev)
+    res = {}
+    for name, W in (("latent", sh.L), ("hidden", sh.d)):
+        rows = synth.make_x(synth.LayerShape("ep", T=T, d=W, L=W, E=E, K=K, I=64, S=0, Is=0),
+                            SEED + rank, device=dev)
+        o = synth.make_x(synth.LayerShape("ep", T=T * K, d=W, L=W, E=E, K=K, I=64, S=0, Is=0),
+                         SEED + 1 + rank, device=dev)
+        for _ in range(args.warmup):
+            d = lmoe.ep_dispatch(idx, E, R, rows)
+            lmoe.ep_combine(idx, d, inv, gate, o)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        torch.cuda.synchronize()
+        barrier(world)
+        t_disp = t_comb = 0.0
+        for _ in range(args.steps):
+            ev[0].record()
+            d = lmoe.ep_dispatch(idx, E, R, rows)
+            ev[1].record()
+            lmoe.ep_combine(idx, d, inv, gate, o)
+            ev[2].record()
+            torch.cuda.synchronize()
+            t_disp += ev[0].elapsed_time(ev[1])
+            t_comb += ev[1].elapsed_time(ev[2])
+        barrier(world)
+        P = int(d["send_off"][R].item())
+        res[name] = {"width": W, "pairs_per_token": P / T,
+                     "interconnect_bytes_per_token": {"dispatch": P * W * 2 / T,
+                                                       "combine": P * W * 2 / T},
+                     "dispatch_ms": max_over_ranks(t_disp / args.steps, world),
+                     "combine_ms": max_over_ranks(t_comb / args.steps, world)}
+    lat = res["latent"]
+    ms = lat["dispatch_ms"] + lat["combine_ms"]
+    line = {"metric": "EP dispatch+combine pack/unpack tokens/s (latent rows)",
+            "value": world * T / (ms / 1e3), "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded logits and rows)",
+            "config": {"workload": f"K3 prefill routing (T={T}, E={E}, top-{K}, in-batch "
+                                   f"thresholds) over {R} ranks of {E // R} experts; rows of the "
+                                   f"latent ({sh.L}) and of the hidden state ({sh.d})",
+                       "ranks": R, "transfer": "not run (one GPU): buffers are what would cross "
+                                               "the interconnect"},
+            "latent": lat, "hidden": res["hidden"],
+            "byte_ratio_hidden_over_latent": (res["hidden"]["interconnect_bytes_per_token"]
+                                              ["dispatch"] /
+                                              lat["interconnect_bytes_per_token"]["dispatch"]),
+            "gpu_launches": 5 * args.steps}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--shape", choices=sorted(SHAPES), default="prefill",
+    ap.add_argument("--shape", choices=sorted(SHAPES) + ["ep"], default="prefill",
                     help="workload (prefill is the headline; the others are extra lines)")
     ap.add_argument("--cpu-tokens", type=int, default=128,
                     help="tokens in the timed CPU-oracle sample")
@@ -548,6 +614,8 @@ def main():
                     help="run the shared experts on a second stream beside the routed path")
     ap.add_argument("--shared-sms", type=int, default=0,
                     help="SMs for the shared experts when they overlap (0: library default)")
+    ap.add_argument("--ep-ranks", type=int, default=8,
+                    help="--shape ep: ranks the experts are spread over")
     ap.add_argument("--experts", choices=["bf16", "fp8"], default="bf16",
                     help="routed-expert GEMM operands: bf16, or e4m3 with per-row scales")
     ap.add_argument("--qb", choices=["local", "global"], default="local",
@@ -555,7 +623,13 @@ def main():
                          "(global: router phase, all-gather of candidates, experts phase)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
-    return run_reference(args) if args.impl == "reference" else run_ours(args)
+    if args.impl == "reference":
+        if args.shape == "ep":
+            print(json.dumps({"impl": "reference", "unavailable": "the oracle arm times the layer; "
+                              "--shape ep measures pack/unpack kernels only"}), flush=True)
+            return 0
+        return run_reference(args)
+    return run_ep(args) if args.shape == "ep" else run_ours(args)
 
 
 if __name__ == "__main__":

@@ -227,6 +227,38 @@ int lmoe_tau_ema(const float *tau_step, float *tau_ema, int E, float beta, int f
  * Errors: INVALID_ARG for null pointers or E < 1. */
 int lmoe_load_stats_update(const int32_t *counts, int E, unsigned long long *acc, void *stream);
 
+/* Expert-parallel dispatch and combine, packed and unpacked on one device.  [IK3] Stable
+ * LatentMoE and communication passages: the routed experts live on different GPUs, each
+ * selected expert receives the token's vector and the outputs travel back to be combined;
+ * projecting to the latent first halves the bytes ([TPP] Technical Details: 7168 -> 3584).
+ * Readings: R ranks host the E experts in equal contiguous blocks (expert e on rank
+ * e / (E/R)); a token's row travels once to every rank hosting at least one of its K
+ * experts; the (token, rank) pairs are laid out by rank, then token.  The buffers below are
+ * what would cross the interconnect; the transfer (an all-to-all) is not part of the library.
+ * Requires 1 <= K <= 32, 1 <= R <= 64, E % R == 0.
+ *
+ * lmoe_ep_workspace_bytes: scratch (device) that dispatch fills and combine reads again.
+ * lmoe_ep_dispatch: idx [T, K] int32 (read); rows [T, W] bf16 or NULL (then only the layout);
+ *   outputs send_off [R + 1] (pair offsets per rank; P = send_off[R] <= T * min(K, R)),
+ *   send_tok [P] (token of each pair), send_slots [P] (bit j: the token's slot j is served
+ *   on that rank), send_rows [T * min(K, R), W] bf16 (row of each pair).  W % 8 == 0,
+ *   16-byte-aligned rows.  Slots whose index is outside [0, E) go to no rank.
+ * lmoe_ep_combine: the expert side sums, for every pair, gate[t, j] * o[inv[t, j]] over its
+ *   slots j in ascending order by fp32 fused multiply-adds and rounds to bf16 into part [P, W];
+ *   the source side adds a token's pairs in rank order in fp32 into u [T, W].  o [*, W] bf16
+ *   (the experts' outputs, one row per (token, slot) at inv [T, K]), gate [T, K] fp32, and
+ *   send_off / send_tok / send_slots / ws from lmoe_ep_dispatch with the same idx.
+ * Errors: INVALID_ARG (null pointers, negative sizes, W, alignment), UNSUPPORTED (K, R, E),
+ *   WORKSPACE_TOO_SMALL. */
+size_t lmoe_ep_workspace_bytes(int T, int K, int E, int R);
+int lmoe_ep_dispatch(const int32_t *idx, int T, int K, int E, int R, const void *rows, int W,
+                     void *send_rows, int32_t *send_off, int32_t *send_tok,
+                     uint32_t *send_slots, void *ws, size_t ws_bytes, void *stream);
+int lmoe_ep_combine(const int32_t *idx, int T, int K, int E, int R, const int32_t *send_off,
+                    const int32_t *send_tok, const uint32_t *send_slots, const int32_t *inv,
+                    const float *gate, const void *o, int W, void *part, float *u,
+                    const void *ws, void *stream);
+
 /* Top-K routing.  [TPP] Technical Details: a lightweight router selects 16 of 896 routed
  * experts per token; [SU]: Quantile Balancing replaces the predecessor's bias updates.
  * Readings: s = sigmoid(logits) evaluated in fp32 by a fixed sequence of IEEE operations

@@ -220,6 +220,50 @@ int lmoe_load_stats_update(const int32_t* counts, int E, unsigned long long* acc
   return launch_load_stats(counts, nullptr, E, acc, static_cast<cudaStream_t>(stream));
 }
 
+static int ep_args_ok(int T, int K, int E, int R) {
+  if (T < 0 || K < 1 || E < 1 || R < 1) return LMOE_ERR_INVALID_ARG;
+  if (K > 32 || R > 64 || E % R) return LMOE_ERR_UNSUPPORTED;
+  return LMOE_OK;
+}
+
+size_t lmoe_ep_workspace_bytes(int T, int K, int E, int R) {
+  if (ep_args_ok(T, K, E, R) != LMOE_OK) return 0;
+  return ep_workspace_bytes(T, R) + 256;
+}
+
+int lmoe_ep_dispatch(const int32_t* idx, int T, int K, int E, int R, const void* rows, int W,
+                     void* send_rows, int32_t* send_off, int32_t* send_tok, uint32_t* send_slots,
+                     void* ws, size_t ws_bytes, void* stream) {
+  int rc = ep_args_ok(T, K, E, R);
+  if (rc != LMOE_OK) return rc;
+  if (!send_off || (T > 0 && (!idx || !send_tok || !send_slots || !ws))) return LMOE_ERR_INVALID_ARG;
+  if (rows && (!send_rows || W <= 0 || W % 8 || !aligned16(rows) || !aligned16(send_rows)))
+    return LMOE_ERR_INVALID_ARG;
+  if (ws_bytes < ep_workspace_bytes(T, R)) return LMOE_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (T == 0)
+    return cudaMemsetAsync(send_off, 0, sizeof(int32_t) * (R + 1), st) == cudaSuccess
+               ? LMOE_OK
+               : LMOE_ERR_CUDA;
+  return launch_ep_dispatch(idx, T, K, E, R, rows, rows ? W : 0, send_rows, send_off, send_tok,
+                            send_slots, ws, st);
+}
+
+int lmoe_ep_combine(const int32_t* idx, int T, int K, int E, int R, const int32_t* send_off,
+                    const int32_t* send_tok, const uint32_t* send_slots, const int32_t* inv,
+                    const float* gate, const void* o, int W, void* part, float* u,
+                    const void* ws, void* stream) {
+  int rc = ep_args_ok(T, K, E, R);
+  if (rc != LMOE_OK) return rc;
+  if (T == 0) return LMOE_OK;
+  if (!idx || !send_off || !send_tok || !send_slots || !inv || !gate || !o || !part || !u || !ws)
+    return LMOE_ERR_INVALID_ARG;
+  if (W <= 0 || W % 8 || !aligned16(o) || !aligned16(part) || !aligned16(u))
+    return LMOE_ERR_INVALID_ARG;
+  return launch_ep_combine(idx, T, K, E, R, send_off, send_tok, send_slots, inv, gate, o, W, part,
+                           u, ws, static_cast<cudaStream_t>(stream));
+}
+
 int lmoe_threshold_candidates(const float* logits, int T, int E, int k, float* cand,
                               void* stream) {
   if (T < 0 || E < 1 || k < 1 || !cand || (T > 0 && !logits)) return LMOE_ERR_INVALID_ARG;

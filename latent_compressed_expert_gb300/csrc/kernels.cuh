@@ -126,6 +126,15 @@ int launch_tau_ema(const float* tau_step, float* tau_ema, int E, float beta, int
 // Load counters (layout at lmoe_load_stats_update) from counts, or from segment offsets.
 int launch_load_stats(const int32_t* counts, const int32_t* offsets, int E,
                       unsigned long long* acc, cudaStream_t stream);
+// Expert-parallel dispatch / combine over R ranks (see ep.cu); ws: ep_workspace_bytes.
+size_t ep_workspace_bytes(int T, int R);
+int launch_ep_dispatch(const int32_t* idx, int T, int K, int E, int R, const void* rows, int W,
+                       void* send_rows, int32_t* send_off, int32_t* send_tok,
+                       uint32_t* send_slots, void* ws, cudaStream_t stream);
+int launch_ep_combine(const int32_t* idx, int T, int K, int E, int R, const int32_t* send_off,
+                      const int32_t* send_tok, const uint32_t* send_slots, const int32_t* inv,
+                      const float* gate, const void* o, int W, void* part, float* u,
+                      const void* ws, cudaStream_t stream);
 // Per-row e4m3 quantisation of bf16 rows (cols % 16 == 0): codes [rows, ldq], scales [rows].
 int launch_quantize_rows(const __nv_bfloat16* x, int64_t rows, int cols, int64_t ldx,
                          uint8_t* q, int64_t ldq, float* scales, cudaStream_t stream);

@@ -65,6 +65,10 @@ SIGNATURES = {
     "lmoe_threshold_candidates": (_i, [_vp, _i, _i, _i, _vp, _vp]),
     "lmoe_quantize_e4m3": (_i, [_vp, ctypes.c_longlong, _i, _vp, _vp, _vp]),
     "lmoe_tau_ema": (_i, [_vp, _vp, _i, _f, _i, _vp]),
+    "lmoe_ep_workspace_bytes": (_sz, [_i, _i, _i, _i]),
+    "lmoe_ep_dispatch": (_i, [_vp, _i, _i, _i, _i, _vp, _i, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "lmoe_ep_combine": (_i, [_vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _vp,
+                             _vp, _vp]),
     "lmoe_load_stats_update": (_i, [_vp, _i, _vp, _vp]),
     "lmoe_route": (_i, [_vp, _vp, _i, _i, _i, _vp, _vp, _vp, _vp]),
     "lmoe_forward": (_i, [ctypes.POINTER(Dims), _vp, _vp, _vp, _vp, _vp, _sz, ctypes.POINTER(IO),
@@ -232,6 +236,50 @@ class LoadStats:
                 "worst_max_over_mean": a[3] / mean if mean else None,
                 "expert_cv": float(per.std() / per.mean()) if per.mean() else None,
                 "idle_expert_steps": int(a[4 + 2 * E:4 + 3 * E].sum())}
+
+
+def ep_dispatch(idx: torch.Tensor, E: int, R: int, rows: torch.Tensor | None = None,
+                stream=None) -> dict:
+    """Expert-parallel dispatch over R ranks (lmoe_ep_dispatch): pair offsets per rank, the
+    token and slot mask of each pair, and (with rows, bf16 [T, W]) each pair's row."""
+    T, K = idx.shape
+    _expect(idx, torch.int32, (T, K), "idx")
+    dev = idx.device
+    pmax = T * min(K, R)
+    W = 0
+    if rows is not None:
+        W = rows.shape[1]
+        _expect(rows, torch.bfloat16, (T, W), "rows")
+    ws_bytes = int(load().lmoe_ep_workspace_bytes(T, K, E, R))
+    if ws_bytes == 0:
+        raise LmoeError(LMOE_ERR_UNSUPPORTED, "lmoe_ep_workspace_bytes")
+    d = {"ws": torch.empty(ws_bytes, dtype=torch.uint8, device=dev),
+         "send_off": torch.empty(R + 1, dtype=torch.int32, device=dev),
+         "send_tok": torch.empty(pmax, dtype=torch.int32, device=dev),
+         "send_slots": torch.empty(pmax, dtype=torch.int32, device=dev),
+         "send_rows": torch.empty((pmax, W), dtype=torch.bfloat16, device=dev) if W else None,
+         "E": E, "R": R}
+    _check(load().lmoe_ep_dispatch(_ptr(idx), T, K, E, R, _ptr(rows), W, _ptr(d["send_rows"]),
+                                   _ptr(d["send_off"]), _ptr(d["send_tok"]), _ptr(d["send_slots"]),
+                                   _ptr(d["ws"]), ws_bytes, _stream(stream)), "lmoe_ep_dispatch")
+    return d
+
+
+def ep_combine(idx: torch.Tensor, disp: dict, inv: torch.Tensor, gate: torch.Tensor,
+               o: torch.Tensor, stream=None):
+    """Expert-parallel combine (lmoe_ep_combine): (part bf16 [pairs, W], u fp32 [T, W])."""
+    T, K = idx.shape
+    W = o.shape[1]
+    _expect(o, torch.bfloat16, (o.shape[0], W), "o")
+    _expect(inv, torch.int32, (T, K), "inv")
+    _expect(gate, torch.float32, (T, K), "gate")
+    part = torch.empty((T * min(K, disp["R"]), W), dtype=torch.bfloat16, device=o.device)
+    u = torch.empty((T, W), dtype=torch.float32, device=o.device)
+    _check(load().lmoe_ep_combine(_ptr(idx), T, K, disp["E"], disp["R"], _ptr(disp["send_off"]),
+                                  _ptr(disp["send_tok"]), _ptr(disp["send_slots"]), _ptr(inv),
+                                  _ptr(gate), _ptr(o), W, _ptr(part), _ptr(u), _ptr(disp["ws"]),
+                                  _stream(stream)), "lmoe_ep_combine")
+    return part, u
 
 
 def fair_share_rank(T: int, K: int, E: int) -> int:
