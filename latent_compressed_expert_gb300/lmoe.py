@@ -504,3 +504,59 @@ class Layer:
 
     def device_error(self) -> int:
         return last_device_error(self.workspace)
+
+
+class HostPipeline:
+    """The layer on batches that live in pinned host memory, overlapped across batches.
+
+    Each ``submit`` copies x to the device on an upload stream, runs the layer on the
+    compute stream, and copies y back on a download stream, all asynchronous; with ``depth``
+    device buffer pairs, batch i+1's upload and batch i-1's download run while batch i
+    computes.  Events order every reuse: an x buffer is overwritten only after the forward
+    that read it, a y buffer only after its download.  The forward calls themselves stay in
+    order on one stream, so the layer's workspace is shared safely.  ``synchronize`` waits
+    for every submitted batch."""
+
+    def __init__(self, layer: "Layer", depth: int = 2):
+        self.layer = layer
+        self.depth = depth
+        T, d = layer.max_tokens, layer.shape.d
+        dev = layer.device
+        self.x = [torch.empty((T, d), dtype=torch.bfloat16, device=dev) for _ in range(depth)]
+        self.y = [torch.empty((T, d), dtype=torch.bfloat16, device=dev) for _ in range(depth)]
+        self.up = torch.cuda.Stream(device=dev)
+        self.compute = torch.cuda.Stream(device=dev)
+        self.down = torch.cuda.Stream(device=dev)
+        self.uploaded = [torch.cuda.Event() for _ in range(depth)]
+        self.computed = [torch.cuda.Event() for _ in range(depth)]
+        self.downloaded = [torch.cuda.Event() for _ in range(depth)]
+        self.used = [False] * depth
+        self.n = 0
+
+    def submit(self, x_host: torch.Tensor, y_host: torch.Tensor, residual_from_x: bool = True,
+               **kw):
+        """Enqueue one batch: x_host [T, d] bf16 pinned in, y_host pinned out.  Extra keyword
+        arguments go to ``Layer.forward``."""
+        k = self.n % self.depth
+        T = x_host.shape[0]
+        xd, yd = self.x[k][:T], self.y[k][:T]
+        if self.used[k]:
+            self.up.wait_event(self.computed[k])        # the forward that read x[k] is done
+            self.compute.wait_event(self.downloaded[k])  # y[k] has been read back
+        with torch.cuda.stream(self.up):
+            xd.copy_(x_host, non_blocking=True)
+            self.uploaded[k].record(self.up)
+        self.compute.wait_event(self.uploaded[k])
+        self.layer.forward(xd, residual=xd if residual_from_x else None, y=yd,
+                           stream=self.compute, **kw)
+        self.computed[k].record(self.compute)
+        self.down.wait_event(self.computed[k])
+        with torch.cuda.stream(self.down):
+            y_host.copy_(yd, non_blocking=True)
+            self.downloaded[k].record(self.down)
+        self.used[k] = True
+        self.n += 1
+
+    def synchronize(self):
+        for s in (self.up, self.compute, self.down):
+            s.synchronize()
