@@ -628,7 +628,7 @@ int lmoe_forward(const lmoe_dims* dims, const void* packed, const void* x, const
   if (!mark(LMOE_STAGE_COMBINE, 1)) return LMOE_ERR_CUDA;
   // 8. gate-weighted combine + RMSNorm -> zh[:, :L]
   rc = launch_combine(o, gate, inv, reinterpret_cast<const float*>(pk + P.gamma), T, D.K, D.L,
-                      D.eps, zh, ldz, stream);
+                      D.eps, zh, ldz, err, wait_limit_ns(), stream);
   if (rc != LMOE_OK) return rc;
   if (!mark(LMOE_STAGE_OUTPUT, 1)) return LMOE_ERR_CUDA;
   // 9. y = residual + [z | hs] . [W_up | W_sd]^T   (overlap: y = residual + z . W_up^T + ys)

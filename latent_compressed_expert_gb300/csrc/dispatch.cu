@@ -15,6 +15,7 @@
 // plus the popcount of the lower mask bits.
 #include "common.cuh"
 #include "kernels.cuh"
+#include "ptx.cuh"
 
 namespace lmoe {
 
@@ -256,6 +257,106 @@ combine_rmsnorm_kernel(const __nv_bfloat16* __restrict__ o, const float* __restr
   }
 }
 
+// Combine + RMSNorm with the token's K expert rows staged in shared memory by 1-D bulk
+// copies: one thread issues the K copies on one mbarrier, so a CTA has all K rows in
+// flight at once (K * L * 2 bytes; two CTAs per SM when that is at most COMBINE_BULK_MAX).
+// Then each thread sums its 8-feature vectors over the slots in slot order, the sum of
+// squares is reduced in the same fixed tree as above, and z is written.  The wait on the
+// copies is bounded; on time-out the CTA records the error bit and writes nothing.
+constexpr int COMBINE_BULK_MAX = 114688;  // bytes of staged rows per CTA (16 x 3584 bf16)
+__global__ void __launch_bounds__(COMBINE_MAX_THREADS)
+combine_bulk_kernel(const __nv_bfloat16* __restrict__ o, const float* __restrict__ gate,
+                    const int32_t* __restrict__ inv, const float* __restrict__ gamma, int T,
+                    int K, int L, float eps, __nv_bfloat16* __restrict__ z, int ldz,
+                    uint32_t* __restrict__ err, unsigned long long timeout_ns) {
+  extern __shared__ __align__(128) uint8_t cb_smem[];
+  __shared__ float gates[32];
+  __shared__ float warp_ss[32];
+  __shared__ __align__(8) uint64_t bar;
+  const int t = blockIdx.x;
+  const uint32_t row_bytes = static_cast<uint32_t>(L) * 2;
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(&bar, 1);
+    ptx::fence_mbar_init();
+  }
+  __syncthreads();
+  pdl_wait();
+  pdl_launch_dependents();
+  if (threadIdx.x == 0) {
+    ptx::mbar_arrive_expect_tx(&bar, row_bytes * static_cast<uint32_t>(K));
+    for (int j = 0; j < K; ++j) {
+      const int row = __ldg(inv + static_cast<size_t>(t) * K + j);
+      ptx::bulk_load(cb_smem + static_cast<size_t>(j) * row_bytes,
+                     o + static_cast<size_t>(row) * L, row_bytes, &bar);
+    }
+  }
+  if (threadIdx.x < K) gates[threadIdx.x] = __ldg(gate + static_cast<size_t>(t) * K + threadIdx.x);
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) abort_flag = 0;
+  __syncthreads();
+  // every thread waits on the copies; the wait is bounded
+  const bool ok = ptx::mbar_wait(&bar, 0u, &abort_flag, timeout_ns);
+  if (!__syncthreads_and(ok ? 1 : 0)) {
+    if (threadIdx.x == 0) atomicOr(err, DEVERR_TIMEOUT_EPILOGUE);
+    // copies still in flight must land before the CTA exits (bounded again)
+    ptx::mbar_wait(&bar, 0u, &abort_flag, timeout_ns);
+    return;
+  }
+  const int nvec = L / 8;
+  const uint4* rows = reinterpret_cast<const uint4*>(cb_smem);
+  float u[COMBINE_MAX_VEC][8];
+  float ss = 0.0f;
+#pragma unroll
+  for (int c = 0; c < COMBINE_MAX_VEC; ++c) {
+    const int v = threadIdx.x + c * blockDim.x;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) u[c][i] = 0.0f;
+    if (v < nvec) {
+      for (int j = 0; j < K; ++j) {
+        const uint4 raw = rows[static_cast<size_t>(j) * nvec + v];
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
+        const float g = gates[j];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 f = __bfloat1622float2(h[i]);
+          u[c][2 * i] = fmaf(g, f.x, u[c][2 * i]);
+          u[c][2 * i + 1] = fmaf(g, f.y, u[c][2 * i + 1]);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) ss = fmaf(u[c][i], u[c][i], ss);
+    }
+  }
+  for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) warp_ss[warp] = ss;
+  __syncthreads();
+  if (warp == 0) {
+    const int nw = (blockDim.x + 31) >> 5;
+    float v = lane < nw ? warp_ss[lane] : 0.0f;
+    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    if (lane == 0) warp_ss[0] = v;
+  }
+  __syncthreads();
+  const float inv_rms = rsqrtf(warp_ss[0] / static_cast<float>(L) + eps);
+#pragma unroll
+  for (int c = 0; c < COMBINE_MAX_VEC; ++c) {
+    const int v = threadIdx.x + c * blockDim.x;
+    if (v < nvec) {
+      const float4 g0 = __ldg(reinterpret_cast<const float4*>(gamma) + 2 * v);
+      const float4 g1 = __ldg(reinterpret_cast<const float4*>(gamma) + 2 * v + 1);
+      const float gm[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+      uint4 out;
+      __nv_bfloat162* ob = reinterpret_cast<__nv_bfloat162*>(&out);
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        ob[i] = __floats2bfloat162_rn(u[c][2 * i] * inv_rms * gm[2 * i],
+                                      u[c][2 * i + 1] * inv_rms * gm[2 * i + 1]);
+      reinterpret_cast<uint4*>(z + static_cast<size_t>(t) * ldz)[v] = out;
+    }
+  }
+}
+
 // ------------------------------------------------------------------------------------
 int launch_dispatch(const int32_t* idx, int T, int E, int K, uint32_t* masks, uint32_t* base,
                     int32_t* offsets, int32_t* ct_off, int32_t* inv, int32_t* src_tok,
@@ -284,12 +385,22 @@ int launch_dispatch(const int32_t* idx, int T, int E, int K, uint32_t* masks, ui
 
 int launch_combine(const __nv_bfloat16* o, const float* gate, const int32_t* inv,
                    const float* gamma, int T, int K, int L, float eps, __nv_bfloat16* z,
-                   int ldz, cudaStream_t stream) {
+                   int ldz, uint32_t* err, unsigned long long timeout_ns, cudaStream_t stream) {
   if (T == 0) return LMOE_OK;
   const int nvec = L / 8;
   const int threads = static_cast<int>(
       ceil_div(nvec < COMBINE_MAX_THREADS ? nvec : COMBINE_MAX_THREADS, 32) * 32);
   if (nvec > COMBINE_MAX_VEC * threads) return LMOE_ERR_UNSUPPORTED;
+  const size_t staged = static_cast<size_t>(K) * L * 2;
+  if (staged <= static_cast<size_t>(COMBINE_BULK_MAX)) {
+    if (cudaFuncSetAttribute(combine_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(staged)) != cudaSuccess)
+      return LMOE_ERR_CUDA;
+    return launch_pdl(combine_bulk_kernel, T, threads, staged, stream, o, gate, inv, gamma, T, K,
+                      L, eps, z, ldz, err, timeout_ns) == cudaSuccess
+               ? LMOE_OK
+               : LMOE_ERR_CUDA;
+  }
   return launch_pdl(combine_rmsnorm_kernel, T, threads, 0, stream, o, gate, inv, gamma, T, K, L,
                     eps, z, ldz) == cudaSuccess
              ? LMOE_OK

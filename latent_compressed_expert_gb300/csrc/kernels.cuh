@@ -119,7 +119,7 @@ int launch_dispatch(const int32_t* idx, int T, int E, int K, uint32_t* masks, ui
                     int32_t* counts_out, uint32_t* err, cudaStream_t stream);
 int launch_combine(const __nv_bfloat16* o, const float* gate, const int32_t* inv,
                    const float* gamma, int T, int K, int L, float eps, __nv_bfloat16* z,
-                   int ldz, cudaStream_t stream);
+                   int ldz, uint32_t* err, unsigned long long timeout_ns, cudaStream_t stream);
 // Streaming thresholds: tau_ema = first ? tau_step : fma(beta, tau_ema - tau_step, tau_step).
 int launch_tau_ema(const float* tau_step, float* tau_ema, int E, float beta, int first,
                    cudaStream_t stream);
