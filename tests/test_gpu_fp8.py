@@ -161,3 +161,27 @@ def test_prefill_fp8_sampled_tokens(dev, oracle_mod):
     stable = ties == 0
     assert stable.sum() >= len(rows) // 2, ties
     assert_close_fp8(y[rows].float().cpu().numpy()[stable], ref[stable], tag="prefill/fp8")
+
+
+@pytest.mark.parametrize("T", [1, 7, 64])
+def test_fp8_small_batches_every_token(dev, oracle_mod, T):
+    """Decode-sized batches (about one token per expert, ragged token tiles) with thresholds
+    passed in, as decode runs: every token against the oracle's FP8 path."""
+    sh = synth.LayerShape("d8", T=T, d=1024, L=512, E=64, K=8, I=256, S=2, Is=512)
+    w = synth.make_weights(sh, seed=71)
+    wd = {k: v.to(dev) for k, v in w.items()}
+    layer = lmoe.Layer(sh, wd, expert_fp8=True)
+    x = synth.make_x(sh, seed=72)
+    logits = synth.make_logits(T, sh.E, seed=73)
+    tau = torch.from_numpy(oracle_mod.thresholds(synth.make_logits(4096, sh.E, seed=74).numpy(),
+                                                 oracle_mod.fair_share_rank(4096, sh.K, sh.E)))
+    y, dbg = layer.forward(x.to(dev), residual=x.to(dev), logits_in=logits.to(dev),
+                           tau=tau.to(dev), debug=True)
+    torch.cuda.synchronize()
+    assert layer.device_error() == 0
+    ref = oracle_mod.forward(w, x, sh.K, residual=x, tau=tau.numpy(), logits_in=logits.numpy(),
+                             expert_fp8=True)
+    assert np.array_equal(dbg["idx"].cpu().numpy(), ref.idx)
+    stable = ref.scale_ties == 0
+    if stable.any():
+        assert_close_fp8(y.float().cpu().numpy()[stable], ref.y[stable], tag=f"fp8/T{T}")
