@@ -49,7 +49,7 @@ struct GroupedCfg {
   static constexpr int ACC_COLS = 256;                    // TMEM columns between accumulators
   static constexpr int TMEM_COLS = 512;
   static constexpr int EPI_OFF = STAGES * STAGE_BYTES;   // per epilogue warp 32 x 32 bf16
-  static constexpr int EPI_BYTES = 4 * 32 * 32 * 2;
+  static constexpr int EPI_BYTES = 8 * 32 * 32 * 2;
   static constexpr int BAR_OFF = EPI_OFF + EPI_BYTES;
   static constexpr int NUM_BARS = 2 * STAGES + 5;
   static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
@@ -181,7 +181,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
     }
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(&tfull[a], 1);
-      ptx::mbar_init(&tempty[a], GROUPED_EPI_WARPS * 32);
+      // with e4m3 operands and nothing gathered, warps 6..9 join the epilogue
+      ptx::mbar_init(&tempty[a],
+                     ((FP8 && !g.gather) ? 2 * GROUPED_EPI_WARPS : GROUPED_EPI_WARPS) * 32);
     }
     ptx::mbar_init(drain, 1);
     *abort_flag = 0;
@@ -289,7 +291,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
       ptx::umma_commit(drain);
       if (!gwait_drain(drain, 0u, limit)) graise(g, abort_flag, DEVERR_TIMEOUT_DRAIN);
     }
-  } else if (warp >= 2 + GROUPED_EPI_WARPS) {
+  } else if (warp >= 2 + GROUPED_EPI_WARPS && (g.gather || !FP8)) {
     // ------------------------------------------------------------ row gatherers (warps 6..9)
     // Thread gt copies 16-byte chunk (gt & 7) of rows gt/8 + 16 j of each stage's token
     // tile, from the activation row src = gather[permuted row], into the 128-byte-swizzled
@@ -330,8 +332,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
       ptx::cp_async_wait_all();
     }
   } else {
-    // ------------------------------------------------------------ epilogue (warps 2..5)
+    // ------------------------------------------------------------ epilogue (warps 2..5, and
+    // 6..9 for the e4m3 down GEMM: two warps per TMEM lane quarter, even and odd chunks).
+    // Its mainloop is half as long as the bf16 one, so the output stores bound it; the bf16
+    // down GEMM measured slower with the second group (its warps only poll)
     const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int egroups = (FP8 && !g.gather) ? 2 : 1;
+    const int eg = (warp - 2) / GROUPED_EPI_WARPS;
     const float c = g.c, inv_c = 1.0f / g.c;
     int lt = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++lt) {
@@ -367,7 +374,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
                              static_cast<uint32_t>(acc * C::ACC_COLS);
       const bool row_ok = r < g.M_w;  // the last weight tile of an expert may be partial
 #pragma unroll 1
-      for (int ch = 0; ch * 32 < t.npad; ++ch) {
+      for (int ch = eg; ch * 32 < t.npad; ch += egroups) {
         float v[32];
         ptx::tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(ch * 32), v);
         const int nv = min(32, t.ntok - ch * 32);
