@@ -17,6 +17,9 @@ the layer defines them:
     ys     = sum_s SiTU-FFN_s(x)                       shared experts at full width
     y      = residual + z_n . W_up^T + ys
 
+``backward.py`` differentiates the routed branch (PyTorch fp64 autodiff of a plain
+re-statement, pinned to this forward and to finite differences).
+
 The routed experts also have an e4m3 variant (``routed_fp8``, ``forward(expert_fp8=True)``):
 per-row quantisation of both GEMM operands, defined in the C source.
 
