@@ -300,6 +300,30 @@ int lmoe_forward(const lmoe_dims *dims, const void *packed, const void *x,
 int lmoe_gemm_bf16(const void *A, const void *B, float *C, int M, int N, int Kd,
                    uint32_t *dev_flag, void *stream);
 
+/* Backward pass of the routed-expert branch.  [IK3] stabilizers passage: SiTU-GLU and the
+ * RMSNorm after aggregation were introduced to keep training of the routed branch stable.
+ * For the branch  h_j = SiTU(lat W_g[e_j]^T, lat W_v[e_j]^T),  o_j = h_j W_ed[e_j]^T,
+ * u = sum_j g_j o_j,  z = gamma u / sqrt(mean(u^2) + eps),  and dz = dLoss/dz, computes
+ * dLoss/d(lat, gates, gamma, W_g, W_v, W_ed).  Routing is a discrete choice and is held fixed.
+ * It continues from the workspace of the lmoe_forward call (same dims, packed weights and
+ * stream) that produced z: the latent, the routing, the SiTU outputs and the expert outputs
+ * are read from there; the gate/value pre-activations are recomputed.  Operands of the
+ * GEMMs are bf16 with fp32 accumulation, like the forward's.  bf16 routed experts only.
+ *   lmoe_pack_backward_weights: transposed tiled copies of the expert weights into
+ *     packed_bwd (lmoe_packed_backward_bytes; from the same unpacked weights as the forward).
+ *   lmoe_routed_backward: dz [T, L] fp32 in; dlat [T, L], dgate [T, K], dgamma [L],
+ *     dw_gu [E, 2I, L] (rows 0..I-1: W_g, rows I..2I-1: W_v) and dw_ed [E, L, I], all fp32,
+ *     out; bwd_ws: lmoe_routed_backward_workspace_bytes of device scratch.
+ * Errors: INVALID_ARG, UNSUPPORTED (expert_fp8), WORKSPACE_TOO_SMALL, CUDA. */
+size_t lmoe_packed_backward_bytes(const lmoe_dims *dims);
+int lmoe_pack_backward_weights(const lmoe_dims *dims, const lmoe_weights *w, void *packed_bwd,
+                               size_t bytes, void *stream);
+size_t lmoe_routed_backward_workspace_bytes(const lmoe_dims *dims);
+int lmoe_routed_backward(const lmoe_dims *dims, const void *packed, const void *packed_bwd,
+                         void *workspace, size_t ws_bytes, const float *dz, float *dlat,
+                         float *dgate, float *dgamma, float *dw_gu, float *dw_ed, void *bwd_ws,
+                         size_t bwd_ws_bytes, void *stream);
+
 /* Building block of the FP8 routed experts, exposed for verification: per-row e4m3
  * quantisation of x [rows, cols] bf16 (row-major, cols a multiple of 16, 16-byte aligned)
  * into codes [rows, cols] and scales [rows] fp32, by the recipe stated at lmoe_dims.

@@ -132,6 +132,57 @@ static GemmArgs gemm_defaults(uint32_t* err, float c) {
   return g;
 }
 
+// Backward of the routed branch: transposed expert weights and scratch.
+struct BwdPacked {
+  size_t wgu_t, wed_t, total;
+};
+static BwdPacked bwd_packed_layout(const lmoe_dims& D) {
+  BwdPacked B{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off += align_up(bytes, 1024);
+    return o;
+  };
+  B.wgu_t = take(static_cast<size_t>(D.E) * ceil_div(D.L, BLOCK_M) * BLOCK_M * 2 * D.I * 2);
+  B.wed_t = take(static_cast<size_t>(D.E) * ceil_div(D.I, BLOCK_M) * BLOCK_M * D.L * 2);
+  B.total = off;
+  return B;
+}
+
+struct BwdLayout {
+  size_t u, r, dout, dh, pre, dgv, dlatp, kseg, part, rowmap, dout_t, h_t, dgv_t, latp_t, total;
+  int64_t qmax;  // columns of the padded, transposed operands of the weight gradients
+};
+static BwdLayout bwd_layout(const lmoe_dims& D) {
+  BwdLayout B{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off += align_up(bytes > 0 ? bytes : 1, 256);
+    return o;
+  };
+  const size_t T = static_cast<size_t>(D.T), TK = T * D.K, L = D.L, I = D.I;
+  B.qmax = static_cast<int64_t>(ceil_div(static_cast<int64_t>(TK) + 64 * D.E, 64) * 64);
+  const size_t q = static_cast<size_t>(B.qmax);
+  B.u = take(T * L * 4);
+  B.r = take(T * 4);
+  B.dout = take(TK * L * 2);
+  B.dh = take(TK * I * 2);
+  B.pre = take(TK * 2 * I * 2);
+  B.dgv = take(TK * 2 * I * 2);
+  B.dlatp = take(TK * L * 2);
+  B.kseg = take((static_cast<size_t>(D.E) + 1) * 4);
+  B.part = take(64 * L * 4);
+  B.rowmap = take(2 * I * 4);
+  B.dout_t = take(L * q * 2);
+  B.h_t = take(I * q * 2);
+  B.dgv_t = take(2 * I * q * 2);
+  B.latp_t = take(L * q * 2);
+  B.total = off;
+  return B;
+}
+
 }  // namespace lmoe
 
 using namespace lmoe;
@@ -296,6 +347,178 @@ int lmoe_gemm_bf16(const void* A, const void* B, float* C, int M, int N, int Kd,
   g.ldf = N;
   return launch_gemm(A, static_cast<uint64_t>(M), Kd, B, static_cast<uint64_t>(N), Kd, g,
                      static_cast<cudaStream_t>(stream));
+}
+
+size_t lmoe_packed_backward_bytes(const lmoe_dims* dims) {
+  if (dims_supported(dims) != LMOE_OK || dims->expert_fp8) return 0;
+  return bwd_packed_layout(*dims).total;
+}
+
+int lmoe_pack_backward_weights(const lmoe_dims* dims, const lmoe_weights* w, void* packed_bwd,
+                               size_t bytes, void* stream) {
+  const int rc = dims_supported(dims);
+  if (rc != LMOE_OK) return rc;
+  if (dims->expert_fp8) return LMOE_ERR_UNSUPPORTED;
+  if (!w || !packed_bwd || !w->w_gate || !w->w_value || !w->w_edown || !aligned16(packed_bwd))
+    return LMOE_ERR_INVALID_ARG;
+  const BwdPacked B = bwd_packed_layout(*dims);
+  if (bytes < B.total) return LMOE_ERR_WORKSPACE_TOO_SMALL;
+  uint8_t* base = static_cast<uint8_t*>(packed_bwd);
+  return launch_pack_backward(*dims, *w, reinterpret_cast<__nv_bfloat16*>(base + B.wgu_t),
+                              reinterpret_cast<__nv_bfloat16*>(base + B.wed_t),
+                              static_cast<cudaStream_t>(stream));
+}
+
+size_t lmoe_routed_backward_workspace_bytes(const lmoe_dims* dims) {
+  if (dims_supported(dims) != LMOE_OK || dims->expert_fp8) return 0;
+  return bwd_layout(*dims).total;
+}
+
+int lmoe_routed_backward(const lmoe_dims* dims, const void* packed, const void* packed_bwd,
+                         void* workspace, size_t ws_bytes, const float* dz, float* dlat,
+                         float* dgate, float* dgamma, float* dw_gu, float* dw_ed, void* bwd_ws,
+                         size_t bwd_ws_bytes, void* stream_) {
+  int rc = dims_supported(dims);
+  if (rc != LMOE_OK) return rc;
+  const lmoe_dims D = *dims;
+  if (D.expert_fp8) return LMOE_ERR_UNSUPPORTED;
+  if (!packed || !packed_bwd || !workspace || !dz || !dlat || !dgate || !dgamma || !dw_gu ||
+      !dw_ed || !bwd_ws)
+    return LMOE_ERR_INVALID_ARG;
+  const void* ptrs[] = {packed, packed_bwd, workspace, dz, dlat, dgamma, dw_gu, dw_ed, bwd_ws};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return LMOE_ERR_INVALID_ARG;
+  const WorkspaceLayout W = workspace_layout(D);
+  const BwdLayout B = bwd_layout(D);
+  if (ws_bytes < W.total || bwd_ws_bytes < B.total) return LMOE_ERR_WORKSPACE_TOO_SMALL;
+  if (D.T == 0) return LMOE_OK;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  using bf = __nv_bfloat16;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint8_t* bw = static_cast<uint8_t*>(bwd_ws);
+  const uint8_t* pk = static_cast<const uint8_t*>(packed);
+  const uint8_t* pb = static_cast<const uint8_t*>(packed_bwd);
+  const PackedLayout P = packed_layout(D);
+  const BwdPacked PB = bwd_packed_layout(D);
+  const int T = D.T, K = D.K, L = D.L, I = D.I, E = D.E, TK = T * K;
+  uint32_t* err = reinterpret_cast<uint32_t*>(ws + W.err);
+  const int32_t* offsets = reinterpret_cast<const int32_t*>(ws + W.offsets);
+  const int32_t* ct_off = reinterpret_cast<const int32_t*>(ws + W.ct_off);
+  const int32_t* inv = reinterpret_cast<const int32_t*>(ws + W.inv);
+  const int32_t* src_tok = reinterpret_cast<const int32_t*>(ws + W.src_tok);
+  const bf* lat = reinterpret_cast<const bf*>(ws + W.lat);
+  const bf* h = reinterpret_cast<const bf*>(ws + W.h);
+  bf* dout = reinterpret_cast<bf*>(bw + B.dout);
+  bf* dh = reinterpret_cast<bf*>(bw + B.dh);
+  bf* pre = reinterpret_cast<bf*>(bw + B.pre);
+  bf* dgv = reinterpret_cast<bf*>(bw + B.dgv);
+  bf* dlatp = reinterpret_cast<bf*>(bw + B.dlatp);
+  int32_t* kseg = reinterpret_cast<int32_t*>(bw + B.kseg);
+  int32_t* rowmap = reinterpret_cast<int32_t*>(bw + B.rowmap);
+  const int64_t q = B.qmax;
+
+  // 1-2. RMSNorm and combine backward: du, do_j, dg_j; dgamma
+  if ((rc = launch_combine_bwd(reinterpret_cast<const bf*>(ws + W.o),
+                               reinterpret_cast<const float*>(ws + W.gate), inv,
+                               reinterpret_cast<const float*>(pk + P.gamma), dz, T, K, L, D.eps,
+                               dout, dgate, reinterpret_cast<float*>(bw + B.u),
+                               reinterpret_cast<float*>(bw + B.r), stream)) != LMOE_OK ||
+      (rc = launch_dgamma(dz, reinterpret_cast<const float*>(bw + B.u),
+                          reinterpret_cast<const float*>(bw + B.r), T, L,
+                          reinterpret_cast<float*>(bw + B.part), dgamma, stream)) != LMOE_OK)
+    return rc;
+  auto grouped = [&](int M_w, int Kd, const int32_t* gather, const bf* x, int ldx, int epi,
+                     bf* out, int ldo) {
+    GroupedArgs g{};
+    g.E = E;
+    g.M_w = M_w;
+    g.Kd = Kd;
+    g.seg_off = offsets;
+    g.ct_off = ct_off;
+    g.gather = gather;
+    g.x = x;
+    g.ldx = ldx;
+    g.epi = epi;
+    g.out = out;
+    g.ldo = ldo;
+    g.c = D.c;
+    g.err = err;
+    g.timeout_ns = wait_limit_ns();
+    g.mean_tokens = static_cast<int>(static_cast<int64_t>(TK) / E);
+    return g;
+  };
+  // 3. dh = do . W_ed (per expert, weights transposed)
+  {
+    GroupedArgs g = grouped(I, L, nullptr, nullptr, 0, EPI_BF16, dh, I);
+    if ((rc = launch_grouped_gemm(pb + PB.wed_t, dout, static_cast<uint64_t>(TK), L, g, stream)) !=
+        LMOE_OK)
+      return rc;
+  }
+  // 4. gate/value pre-activations again (interleaved rows), 5. through SiTU
+  {
+    GroupedArgs g = grouped(2 * I, L, src_tok, lat, L, EPI_BF16, pre, 2 * I);
+    if ((rc = launch_grouped_gemm(pk + P.wgu, lat, static_cast<uint64_t>(T), L, g, stream)) !=
+        LMOE_OK)
+      return rc;
+  }
+  if ((rc = launch_situ_bwd(pre, dh, TK, I, D.c, dgv, stream)) != LMOE_OK) return rc;
+  // 6. dlat_p = dgv . W_gu (per expert, weights transposed), 7. summed over the slots
+  {
+    GroupedArgs g = grouped(L, 2 * I, nullptr, nullptr, 0, EPI_BF16, dlatp, L);
+    if ((rc = launch_grouped_gemm(pb + PB.wgu_t, dgv, static_cast<uint64_t>(TK), 2 * I, g,
+                                  stream)) != LMOE_OK)
+      return rc;
+  }
+  if ((rc = launch_slot_sum(dlatp, inv, T, K, L, dlat, stream)) != LMOE_OK) return rc;
+  // 8-9. weight gradients reduce over each expert's tokens: token-contiguous copies, each
+  // expert's range padded to 64 with zeros
+  if ((rc = launch_pad_scan(offsets, E, kseg, stream)) != LMOE_OK ||
+      (rc = launch_rowmap(I, rowmap, stream)) != LMOE_OK ||
+      (rc = launch_transpose_pad(dout, L, nullptr, L, offsets, kseg, E, q, q,
+                                 reinterpret_cast<bf*>(bw + B.dout_t), stream)) != LMOE_OK ||
+      (rc = launch_transpose_pad(h, I, nullptr, I, offsets, kseg, E, q, q,
+                                 reinterpret_cast<bf*>(bw + B.h_t), stream)) != LMOE_OK ||
+      (rc = launch_transpose_pad(dgv, 2 * I, nullptr, 2 * I, offsets, kseg, E, q, q,
+                                 reinterpret_cast<bf*>(bw + B.dgv_t), stream)) != LMOE_OK ||
+      (rc = launch_transpose_pad(lat, L, src_tok, L, offsets, kseg, E, q, q,
+                                 reinterpret_cast<bf*>(bw + B.latp_t), stream)) != LMOE_OK)
+    return rc;
+  // 10. dW_ed[e] = do_e^T h_e   [L, I];  11. dW_gu[e] = dgv_e^T lat_e   [2I, L] (gate rows,
+  // then value rows)
+  {
+    GemmArgs g = gemm_defaults(err, D.c);
+    g.M = L;
+    g.N = I;
+    g.Kd = static_cast<int>(q);
+    g.epi = EPI_F32;
+    g.outf = dw_ed;
+    g.ldf = I;
+    g.groups = E;
+    g.kseg = kseg;
+    g.group_stride = static_cast<long long>(L) * I;
+    if ((rc = launch_gemm(bw + B.dout_t, static_cast<uint64_t>(L), static_cast<int>(q),
+                          bw + B.h_t, static_cast<uint64_t>(I), static_cast<int>(q), g,
+                          stream)) != LMOE_OK)
+      return rc;
+  }
+  {
+    GemmArgs g = gemm_defaults(err, D.c);
+    g.M = 2 * I;
+    g.N = L;
+    g.Kd = static_cast<int>(q);
+    g.epi = EPI_F32;
+    g.outf = dw_gu;
+    g.ldf = L;
+    g.groups = E;
+    g.kseg = kseg;
+    g.group_stride = static_cast<long long>(2 * I) * L;
+    g.row_map = rowmap;
+    if ((rc = launch_gemm(bw + B.dgv_t, static_cast<uint64_t>(2 * I), static_cast<int>(q),
+                          bw + B.latp_t, static_cast<uint64_t>(L), static_cast<int>(q), g,
+                          stream)) != LMOE_OK)
+      return rc;
+  }
+  return LMOE_OK;
 }
 
 int lmoe_last_device_error(void* workspace) {

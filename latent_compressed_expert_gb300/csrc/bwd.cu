@@ -1,0 +1,390 @@
+// bwd.cu -- backward pass of the routed-expert branch (element-wise and layout kernels).
+//
+// "Part 1 of Inside Kimi K3" (Towards AI article, stabilizers passage): SiTU-GLU and the
+// RMSNorm after expert aggregation were introduced to keep training of the routed branch
+// stable.  For the branch  h = SiTU(lat W_g^T, lat W_v^T),  o = h W_ed^T,  u = sum_j g_j o_j,
+// z = gamma u r  with  r = (mean(u^2) + eps)^-1/2,  and an incoming dz:
+//   a = gamma * dz,   du = r a - u r^3 <u, a> / L,   dgamma = sum_t dz u r,
+//   do_j = g_j du,    dg_j = <du, o_j>,
+//   dh -> through SiTU: with G = c tanh(g/c), V = c tanh(v/c), s = sigmoid(G):
+//     dg_pre = dh V s (1 + G (1 - s)) (1 - (G/c)^2),   dv_pre = dh G s (1 - (V/c)^2),
+// and the GEMMs (dgrad on transposed expert weights, wgrad as per-expert reductions over the
+// expert's tokens) run in gemm_grouped.cu / gemm.cu.  Routing is a discrete choice and is
+// held fixed.
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace lmoe {
+
+constexpr int BWD_MAX_VEC = 4;
+constexpr int BWD_THREADS = 512;
+
+__device__ __forceinline__ void bf8_to_f(const uint4& u, float (&f)[8]) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+__device__ __forceinline__ uint4 f_to_bf8(const float (&f)[8]) {
+  uint32_t w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+    w[i] = *reinterpret_cast<const uint32_t*>(&h);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// Block-wide sum of one value per thread, in a fixed tree (warps, then warp 0).
+__device__ __forceinline__ float block_sum(float v, float* red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  __syncthreads();
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  if (warp == 0) {
+    const int nw = (blockDim.x + 31) >> 5;
+    float x = lane < nw ? red[lane] : 0.0f;
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    if (lane == 0) red[32] = x;
+  }
+  __syncthreads();
+  return red[32];
+}
+
+// One CTA per token: u and r exactly as the forward's combine computed them (fp32 fma in
+// slot order, the same tree for the sum of squares), then du, do_j (bf16, at the permuted
+// row of (t, j)) and dg_j; u and r are kept for dgamma.
+__global__ void __launch_bounds__(BWD_THREADS)
+combine_bwd_kernel(const __nv_bfloat16* __restrict__ o, const float* __restrict__ gate,
+                   const int32_t* __restrict__ inv, const float* __restrict__ gamma,
+                   const float* __restrict__ dz, int K, int L, float eps,
+                   __nv_bfloat16* __restrict__ dout, float* __restrict__ dgate,
+                   float* __restrict__ u_out, float* __restrict__ r_out) {
+  __shared__ int32_t rows[32];
+  __shared__ float gates[32];
+  __shared__ float red[33];
+  __shared__ float dgs[32][33];
+  pdl_wait();
+  pdl_launch_dependents();
+  const int t = blockIdx.x;
+  if (threadIdx.x < K) {
+    rows[threadIdx.x] = __ldg(inv + static_cast<size_t>(t) * K + threadIdx.x);
+    gates[threadIdx.x] = __ldg(gate + static_cast<size_t>(t) * K + threadIdx.x);
+  }
+  __syncthreads();
+  const int nvec = L / 8;
+  float u[BWD_MAX_VEC][8];
+  float ss = 0.0f;
+#pragma unroll
+  for (int c = 0; c < BWD_MAX_VEC; ++c) {
+    const int v = threadIdx.x + c * blockDim.x;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) u[c][i] = 0.0f;
+    if (v < nvec) {
+      for (int j = 0; j < K; ++j) {
+        float f[8];
+        bf8_to_f(__ldg(reinterpret_cast<const uint4*>(o + static_cast<size_t>(rows[j]) * L) + v), f);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) u[c][i] = fmaf(gates[j], f[i], u[c][i]);
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) ss = fmaf(u[c][i], u[c][i], ss);
+    }
+  }
+  const float r = rsqrtf(block_sum(ss, red) / static_cast<float>(L) + eps);
+  // <u, gamma dz>
+  float ua = 0.0f;
+  float a[BWD_MAX_VEC][8];
+#pragma unroll
+  for (int c = 0; c < BWD_MAX_VEC; ++c) {
+    const int v = threadIdx.x + c * blockDim.x;
+    if (v < nvec) {
+      const float4* dzp = reinterpret_cast<const float4*>(dz + static_cast<size_t>(t) * L) + 2 * v;
+      const float4* gp = reinterpret_cast<const float4*>(gamma) + 2 * v;
+      const float4 d0 = __ldg(dzp), d1 = __ldg(dzp + 1), g0 = __ldg(gp), g1 = __ldg(gp + 1);
+      const float dd[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
+      const float gg[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        a[c][i] = gg[i] * dd[i];
+        ua = fmaf(u[c][i], a[c][i], ua);
+      }
+      float4* up = reinterpret_cast<float4*>(u_out + static_cast<size_t>(t) * L) + 2 * v;
+      up[0] = make_float4(u[c][0], u[c][1], u[c][2], u[c][3]);
+      up[1] = make_float4(u[c][4], u[c][5], u[c][6], u[c][7]);
+    }
+  }
+  const float coef = block_sum(ua, red) * r * r * r / static_cast<float>(L);
+  if (threadIdx.x == 0) r_out[t] = r;
+  // du, then do_j = g_j du and the per-thread parts of dg_j = <du, o_j>
+  float dg[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) dg[j] = 0.0f;
+#pragma unroll
+  for (int c = 0; c < BWD_MAX_VEC; ++c) {
+    const int v = threadIdx.x + c * blockDim.x;
+    if (v < nvec) {
+      float du[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) du[i] = r * a[c][i] - u[c][i] * coef;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        if (j < K) {
+          float f[8], d[8];
+          bf8_to_f(__ldg(reinterpret_cast<const uint4*>(o + static_cast<size_t>(rows[j]) * L) + v), f);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            d[i] = gates[j] * du[i];
+            dg[j] = fmaf(du[i], f[i], dg[j]);
+          }
+          reinterpret_cast<uint4*>(dout + static_cast<size_t>(rows[j]) * L)[v] = f_to_bf8(d);
+        }
+      }
+    }
+  }
+  // dg_j: warp sums, then one fixed-order sum over the warps
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    float x = dg[j];
+    for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+    if (lane == 0) dgs[warp][j] = x;
+  }
+  __syncthreads();
+  if (threadIdx.x < K) {
+    float s = 0.0f;
+    for (int w = 0; w < static_cast<int>((blockDim.x + 31) >> 5); ++w) s += dgs[w][threadIdx.x];
+    dgate[static_cast<size_t>(t) * K + threadIdx.x] = s;
+  }
+}
+
+// dgamma[l] = sum_t dz[t, l] u[t, l] r[t], in two fixed-order passes: BWD_CHUNKS row chunks,
+// then the chunks.
+constexpr int BWD_CHUNKS = 64;
+
+__global__ void __launch_bounds__(256)
+colsum_kernel(const float* __restrict__ dz, const float* __restrict__ u,
+              const float* __restrict__ r, int T, int L, float* __restrict__ part) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int l = blockIdx.x * blockDim.x + threadIdx.x;
+  const int chunk = blockIdx.y;
+  if (l >= L) return;
+  const int per = (T + BWD_CHUNKS - 1) / BWD_CHUNKS;
+  const int t0 = chunk * per, t1 = min(T, t0 + per);
+  float s = 0.0f;
+  for (int t = t0; t < t1; ++t) {
+    const size_t i = static_cast<size_t>(t) * L + l;
+    s = fmaf(__ldg(dz + i) * __ldg(u + i), __ldg(r + t), s);
+  }
+  part[static_cast<size_t>(chunk) * L + l] = s;
+}
+
+__global__ void __launch_bounds__(256)
+colsum_final_kernel(const float* __restrict__ part, int L, float* __restrict__ dgamma) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int l = blockIdx.x * blockDim.x + threadIdx.x;
+  if (l >= L) return;
+  float s = 0.0f;
+  for (int c = 0; c < BWD_CHUNKS; ++c) s += part[static_cast<size_t>(c) * L + l];
+  dgamma[l] = s;
+}
+
+// SiTU-GLU backward on the interleaved gate/value layout: row p of pre / dgv holds, for each
+// group of GLU_GROUP features, GLU_GROUP gate then GLU_GROUP value pre-activations.
+__global__ void __launch_bounds__(256)
+situ_bwd_kernel(const __nv_bfloat16* __restrict__ pre, const __nv_bfloat16* __restrict__ dh,
+                int64_t rows, int I, float c, __nv_bfloat16* __restrict__ dgv) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int64_t n = rows * I;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t p = i / I;
+    const int f = static_cast<int>(i % I);
+    const int grp = f / GLU_GROUP, w = f % GLU_GROUP;
+    const size_t gi = static_cast<size_t>(p) * 2 * I + grp * 2 * GLU_GROUP + w;
+    const size_t vi = gi + GLU_GROUP;
+    const float g = __bfloat162float(pre[gi]), v = __bfloat162float(pre[vi]);
+    const float d = __bfloat162float(dh[static_cast<size_t>(p) * I + f]);
+    const float tg = tanhf(g / c), tv = tanhf(v / c);
+    const float G = c * tg, V = c * tv;
+    const float s = 1.0f / (1.0f + expf(-G));
+    const float dG = d * V * s * (1.0f + G * (1.0f - s));
+    const float dV = d * G * s;
+    dgv[gi] = __float2bfloat16_rn(dG * (1.0f - tg * tg));
+    dgv[vi] = __float2bfloat16_rn(dV * (1.0f - tv * tv));
+  }
+}
+
+// dlat[t] = sum_j x[inv[t, j]] in slot order (fp32).
+__global__ void __launch_bounds__(BWD_THREADS)
+slot_sum_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ inv, int K,
+                int L, float* __restrict__ out) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int t = blockIdx.x;
+  const int nvec = L / 8;
+  for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int j = 0; j < K; ++j) {
+      float f[8];
+      const int row = __ldg(inv + static_cast<size_t>(t) * K + j);
+      bf8_to_f(__ldg(reinterpret_cast<const uint4*>(x + static_cast<size_t>(row) * L) + v), f);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] += f[i];
+    }
+    float4* o = reinterpret_cast<float4*>(out + static_cast<size_t>(t) * L) + 2 * v;
+    o[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    o[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+  }
+}
+
+// kseg[e] = sum over e' < e of the expert's token count rounded up to 64 (one CTA).
+__global__ void __launch_bounds__(1024)
+pad_scan_kernel(const int32_t* __restrict__ offsets, int E, int32_t* __restrict__ kseg) {
+  __shared__ int32_t wsum[32];
+  pdl_wait();
+  pdl_launch_dependents();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int per = (E + 1023) / 1024;
+  const int e0 = threadIdx.x * per, e1 = min(E, e0 + per);
+  int32_t mine = 0;
+  for (int e = e0; e < e1; ++e) mine += (offsets[e + 1] - offsets[e] + 63) / 64 * 64;
+  int32_t incl = mine;
+  for (int o = 1; o < 32; o <<= 1) {
+    const int32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) wsum[warp] = incl;
+  __syncthreads();
+  int32_t before = incl - mine;
+  for (int w = 0; w < warp; ++w) before += wsum[w];
+  for (int e = e0; e < e1; ++e) {
+    kseg[e] = before;
+    before += (offsets[e + 1] - offsets[e] + 63) / 64 * 64;
+  }
+  if (threadIdx.x == 1023) kseg[E] = before;
+}
+
+// XT[w, q] for q < kseg[E]: column q of expert e's padded range is its token
+// p = offsets[e] + (q - kseg[e]) (row gather[p] of x, or row p), or zero past the expert's
+// tokens.  32 x 32 tiles through shared memory.
+__global__ void __launch_bounds__(256)
+transpose_pad_kernel(const __nv_bfloat16* __restrict__ x, int64_t ldx,
+                     const int32_t* __restrict__ gather, int W, const int32_t* __restrict__ offsets,
+                     const int32_t* __restrict__ kseg, int E, int64_t ldt,
+                     __nv_bfloat16* __restrict__ xt) {
+  __shared__ __nv_bfloat16 tile[32][34];
+  pdl_wait();
+  pdl_launch_dependents();
+  const int w0 = blockIdx.x * 32;
+  const int64_t q0 = static_cast<int64_t>(blockIdx.y) * 32;
+  const int qtot = __ldg(kseg + E);
+  if (q0 >= qtot) return;
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8
+  for (int i = ty; i < 32; i += 8) {
+    const int64_t q = q0 + i;
+    __nv_bfloat16 val = __float2bfloat16_rn(0.0f);
+    if (q < qtot && w0 + tx < W) {
+      int lo = 0, hi = E;  // kseg[lo] <= q < kseg[hi]
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (__ldg(kseg + mid) <= q) lo = mid; else hi = mid;
+      }
+      const int64_t p = __ldg(offsets + lo) + (q - __ldg(kseg + lo));
+      if (p < __ldg(offsets + lo + 1)) {
+        const int64_t src = gather ? __ldg(gather + p) : p;
+        val = x[src * ldx + w0 + tx];
+      }
+    }
+    tile[i][tx] = val;
+  }
+  __syncthreads();
+  for (int i = ty; i < 32; i += 8) {
+    const int w = w0 + i;
+    const int64_t q = q0 + tx;
+    if (w < W && q < qtot) xt[static_cast<int64_t>(w) * ldt + q] = tile[tx][i];
+  }
+}
+
+// Output row of each packed gate/value row (interleaved in groups of GLU_GROUP): gate
+// feature f -> row f, value feature f -> row I + f.
+__global__ void rowmap_kernel(int I, int32_t* __restrict__ map) {
+  for (int k = blockIdx.x * blockDim.x + threadIdx.x; k < 2 * I; k += gridDim.x * blockDim.x) {
+    const int grp = k / (2 * GLU_GROUP), wi = k % (2 * GLU_GROUP);
+    const int f = grp * GLU_GROUP + (wi % GLU_GROUP);
+    map[k] = wi < GLU_GROUP ? f : I + f;
+  }
+}
+
+int launch_rowmap(int I, int32_t* map, cudaStream_t stream) {
+  rowmap_kernel<<<static_cast<unsigned>(ceil_div(2 * I, 256)), 256, 0, stream>>>(I, map);
+  return cudaGetLastError() == cudaSuccess ? LMOE_OK : LMOE_ERR_CUDA;
+}
+
+// ------------------------------------------------------------------------------------
+int launch_combine_bwd(const __nv_bfloat16* o, const float* gate, const int32_t* inv,
+                       const float* gamma, const float* dz, int T, int K, int L, float eps,
+                       __nv_bfloat16* dout, float* dgate, float* u, float* r,
+                       cudaStream_t stream) {
+  if (T == 0) return LMOE_OK;
+  const int nvec = L / 8;
+  const int threads = static_cast<int>(ceil_div(nvec < BWD_THREADS ? nvec : BWD_THREADS, 32) * 32);
+  if (nvec > BWD_MAX_VEC * threads || K > 32) return LMOE_ERR_UNSUPPORTED;
+  return launch_pdl(combine_bwd_kernel, T, threads, 0, stream, o, gate, inv, gamma, dz, K, L, eps,
+                    dout, dgate, u, r) == cudaSuccess
+             ? LMOE_OK
+             : LMOE_ERR_CUDA;
+}
+
+int launch_dgamma(const float* dz, const float* u, const float* r, int T, int L, float* part,
+                  float* dgamma, cudaStream_t stream) {
+  const dim3 grid(static_cast<unsigned>(ceil_div(L, 256)), BWD_CHUNKS);
+  if (launch_pdl(colsum_kernel, grid, 256, 0, stream, dz, u, r, T, L, part) != cudaSuccess ||
+      launch_pdl(colsum_final_kernel, static_cast<unsigned>(ceil_div(L, 256)), 256, 0, stream,
+                 static_cast<const float*>(part), L, dgamma) != cudaSuccess)
+    return LMOE_ERR_CUDA;
+  return LMOE_OK;
+}
+
+int launch_situ_bwd(const __nv_bfloat16* pre, const __nv_bfloat16* dh, int64_t rows, int I,
+                    float c, __nv_bfloat16* dgv, cudaStream_t stream) {
+  if (rows == 0) return LMOE_OK;
+  const int64_t n = rows * I;
+  const unsigned grid = static_cast<unsigned>(ceil_div(n, 256) < 65535 * 16 ? ceil_div(n, 256) : 65535 * 16);
+  return launch_pdl(situ_bwd_kernel, grid, 256, 0, stream, pre, dh, rows, I, c, dgv) == cudaSuccess
+             ? LMOE_OK
+             : LMOE_ERR_CUDA;
+}
+
+int launch_slot_sum(const __nv_bfloat16* x, const int32_t* inv, int T, int K, int L, float* out,
+                    cudaStream_t stream) {
+  if (T == 0) return LMOE_OK;
+  return launch_pdl(slot_sum_kernel, T, BWD_THREADS, 0, stream, x, inv, K, L, out) == cudaSuccess
+             ? LMOE_OK
+             : LMOE_ERR_CUDA;
+}
+
+int launch_pad_scan(const int32_t* offsets, int E, int32_t* kseg, cudaStream_t stream) {
+  return launch_pdl(pad_scan_kernel, 1, 1024, 0, stream, offsets, E, kseg) == cudaSuccess
+             ? LMOE_OK
+             : LMOE_ERR_CUDA;
+}
+
+int launch_transpose_pad(const __nv_bfloat16* x, int64_t ldx, const int32_t* gather, int W,
+                         const int32_t* offsets, const int32_t* kseg, int E, int64_t qmax,
+                         int64_t ldt, __nv_bfloat16* xt, cudaStream_t stream) {
+  const dim3 grid(static_cast<unsigned>(ceil_div(W, 32)), static_cast<unsigned>(ceil_div(qmax, 32)));
+  return launch_pdl(transpose_pad_kernel, grid, 256, 0, stream, x, ldx, gather, W, offsets, kseg,
+                    E, ldt, xt) == cudaSuccess
+             ? LMOE_OK
+             : LMOE_ERR_CUDA;
+}
+
+}  // namespace lmoe

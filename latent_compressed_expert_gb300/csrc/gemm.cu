@@ -52,10 +52,18 @@ struct TileCoord {
   int row_end;  // rows >= row_end are not part of this problem
   int b_row;    // first row of B
   int n0;       // first output column
+  int grp;      // grouped-K mode: the group; else 0
+  int k0;       // first column of A and B reduced over
+  int nk;       // 64-wide K-blocks reduced over
 };
 
 template <int BN>
 __device__ __forceinline__ TileCoord decode_tile(const GemmArgs& g, int nt, int mt, int tile) {
+  int kgroup = 0;
+  if (g.groups > 0) {  // grouped-K: groups outermost, then the raster below
+    kgroup = tile / (mt * nt);
+    tile -= kgroup * mt * nt;
+  }
   // groups of RASTER_GROUP_M row tiles sweep all column tiles, rows fastest, so the CTAs in
   // flight share a few A row-panels and B column-panels in L2
   const int span = RASTER_GROUP_M * nt;
@@ -70,6 +78,14 @@ __device__ __forceinline__ TileCoord decode_tile(const GemmArgs& g, int nt, int 
   c.row_end = g.M;
   c.b_row = n * BN;
   c.n0 = n * BN;
+  c.grp = kgroup;
+  if (g.groups > 0) {
+    c.k0 = __ldg(g.kseg + kgroup);
+    c.nk = (__ldg(g.kseg + kgroup + 1) - c.k0) / BLOCK_K;
+  } else {
+    c.k0 = 0;
+    c.nk = g.Kd / BLOCK_K;
+  }
   return c;
 }
 
@@ -226,9 +242,8 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA,
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nt = (g.N + BN - 1) / BN;
-  const int nk = g.Kd / BLOCK_K;
   const int mt_dense = (g.M + BLOCK_M - 1) / BLOCK_M;
-  const int total = mt_dense * nt;
+  const int total = mt_dense * nt * (g.groups > 0 ? g.groups : 1);
   const uint64_t limit = g.timeout_ns;
 
   if (threadIdx.x == 0) {
@@ -267,7 +282,7 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA,
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
         const TileCoord tc = decode_tile<BN>(g, nt, mt_dense, tile);
-        for (int kb = 0; kb < nk; ++kb, ++it) {
+        for (int kb = 0; kb < tc.nk; ++kb, ++it) {
           const int s = static_cast<int>(it % C::STAGES);
           const uint32_t ph = (it / C::STAGES) & 1u;
           if (!ptx::mbar_wait(&empty[s], ph ^ 1u, abort_flag, limit)) {
@@ -277,8 +292,8 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA,
           }
           uint8_t* sa = smem + s * C::STAGE_BYTES;
           ptx::mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
-          ptx::tma_load_2d(sa, &tmA, &full[s], kb * BLOCK_K, tc.a_row);
-          ptx::tma_load_2d(sa + C::A_BYTES, &tmB, &full[s], kb * BLOCK_K, tc.b_row);
+          ptx::tma_load_2d(sa, &tmA, &full[s], tc.k0 + kb * BLOCK_K, tc.a_row);
+          ptx::tma_load_2d(sa + C::A_BYTES, &tmB, &full[s], tc.k0 + kb * BLOCK_K, tc.b_row);
         }
       }
       // every issued copy must land before the CTA may exit
@@ -309,8 +324,9 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA,
         }
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        const int nkt = g.groups > 0 ? decode_tile<BN>(g, nt, mt_dense, tile).nk : g.Kd / BLOCK_K;
         bool ok = true;
-        for (int kb = 0; kb < nk; ++kb, ++it) {
+        for (int kb = 0; kb < nkt; ++kb, ++it) {
           const int s = static_cast<int>(it % C::STAGES);
           const uint32_t ph = (it / C::STAGES) & 1u;
           if (!ptx::mbar_wait(&full[s], ph, abort_flag, limit)) {
@@ -358,6 +374,31 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA,
         const int col0 = tc.n0 + ch * 32;
         if (col0 >= g.N) break;  // uniform across the warp
         float v[32];
+        if (g.groups > 0) {
+          // grouped-K: an empty reduction range is a zero product
+          if (tc.nk > 0) {
+            ptx::tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(ch * 32), v);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+          }
+          if (row_ok) {
+            const int orow = g.row_map ? __ldg(g.row_map + row) : row;
+            float* o = g.outf + tc.grp * g.group_stride + static_cast<size_t>(orow) * g.ldf + col0;
+            const int nvalid = min(32, g.N - col0);
+            if (nvalid == 32) {
+#pragma unroll
+              for (int q4 = 0; q4 < 8; ++q4)
+                reinterpret_cast<float4*>(o)[q4] =
+                    make_float4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]);
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                if (i < nvalid) o[i] = v[i];
+            }
+          }
+          continue;
+        }
         ptx::tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(ch * 32), v);
         if (row_ok) {
           if (col0 + 32 <= g.N)

@@ -57,6 +57,13 @@ struct GemmArgs {
   unsigned long long timeout_ns;
   int inject_stall;       // test hook: the MMA role first waits on a barrier nobody arrives
                           // on, so every role runs into its bounded wait and aborts
+  // Grouped-K mode (groups > 0): `groups` independent products, group q reducing over the
+  // columns [kseg[q], kseg[q + 1]) of A and B (multiples of 64; an empty range gives zeros);
+  // EPI_F32 only, group q's output at outf + q * group_stride, output row row_map[r] (or r)
+  int groups;
+  const int32_t* kseg;
+  long long group_stride;
+  const int32_t* row_map;
 };
 
 // Routed-expert GEMMs (gemm_grouped.cu): out[tok, r] = act[tok, :] . W[e][r, :] for the
@@ -135,6 +142,24 @@ int launch_ep_combine(const int32_t* idx, int T, int K, int E, int R, const int3
                       const int32_t* send_tok, const uint32_t* send_slots, const int32_t* inv,
                       const float* gate, const void* o, int W, void* part, float* u,
                       const void* ws, cudaStream_t stream);
+// Transposed tiled expert weights for the backward pass (pack.cu).
+int launch_pack_backward(const lmoe_dims& D, const lmoe_weights& w, __nv_bfloat16* wgu_t,
+                         __nv_bfloat16* wed_t, cudaStream_t stream);
+// Backward of the routed branch (bwd.cu).
+int launch_combine_bwd(const __nv_bfloat16* o, const float* gate, const int32_t* inv,
+                       const float* gamma, const float* dz, int T, int K, int L, float eps,
+                       __nv_bfloat16* dout, float* dgate, float* u, float* r, cudaStream_t stream);
+int launch_dgamma(const float* dz, const float* u, const float* r, int T, int L, float* part,
+                  float* dgamma, cudaStream_t stream);
+int launch_situ_bwd(const __nv_bfloat16* pre, const __nv_bfloat16* dh, int64_t rows, int I,
+                    float c, __nv_bfloat16* dgv, cudaStream_t stream);
+int launch_slot_sum(const __nv_bfloat16* x, const int32_t* inv, int T, int K, int L, float* out,
+                    cudaStream_t stream);
+int launch_pad_scan(const int32_t* offsets, int E, int32_t* kseg, cudaStream_t stream);
+int launch_rowmap(int I, int32_t* map, cudaStream_t stream);
+int launch_transpose_pad(const __nv_bfloat16* x, int64_t ldx, const int32_t* gather, int W,
+                         const int32_t* offsets, const int32_t* kseg, int E, int64_t qmax,
+                         int64_t ldt, __nv_bfloat16* xt, cudaStream_t stream);
 // Per-row e4m3 quantisation of bf16 rows (cols % 16 == 0): codes [rows, ldq], scales [rows].
 int launch_quantize_rows(const __nv_bfloat16* x, int64_t rows, int cols, int64_t ldx,
                          uint8_t* q, int64_t ldq, float* scales, cudaStream_t stream);

@@ -103,6 +103,59 @@ pack_tiled_kernel(__nv_bfloat16* __restrict__ dst, const __nv_bfloat16* __restri
   }
 }
 
+// Transposed tiled expert weights for the backward pass, same tile order as above.
+// glu = 1: per expert [M_w = L rows, Kd = 2I cols], col k is packed gate/value row k
+// (interleave of w_g / w_v [E, Kd/2, M_w]), element (r, k) = W_{g|v}[e][f(k)][r];
+// glu = 0: per expert [M_w = I rows, Kd = L cols], element (r, k) = w[e][k][r] (w [E, Kd, M_w]).
+__global__ void __launch_bounds__(256)
+pack_tiled_t_kernel(__nv_bfloat16* __restrict__ dst, const __nv_bfloat16* __restrict__ w,
+                    const __nv_bfloat16* __restrict__ w_g, const __nv_bfloat16* __restrict__ w_v,
+                    int glu, int E, int M_w, int Kd) {
+  const int mt = (M_w + BLOCK_M - 1) / BLOCK_M, nk = Kd / BLOCK_K;
+  const int64_t chunks = static_cast<int64_t>(E) * mt * nk * BLOCK_M * (BLOCK_K / 8);
+  for (int64_t c = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; c < chunks;
+       c += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t row = c >> 3;
+    const int ch = static_cast<int>(c & 7);
+    const int rr = static_cast<int>(row % BLOCK_M);
+    const int64_t tile = row / BLOCK_M;
+    const int kb = static_cast<int>(tile % nk);
+    const int64_t em = tile / nk;
+    const int m = static_cast<int>(em % mt);
+    const int e = static_cast<int>(em / mt);
+    const int r = m * BLOCK_M + rr;
+    __nv_bfloat16 v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int k = kb * BLOCK_K + ch * 8 + i;
+      __nv_bfloat16 x = __float2bfloat16_rn(0.0f);
+      if (r < M_w) {
+        if (glu) {
+          const int grp = k / (2 * GLU_GROUP), wi = k % (2 * GLU_GROUP);
+          const int f = grp * GLU_GROUP + (wi % GLU_GROUP);
+          x = (wi < GLU_GROUP ? w_g : w_v)[(static_cast<size_t>(e) * (Kd / 2) + f) * M_w + r];
+        } else {
+          x = w[(static_cast<size_t>(e) * Kd + k) * M_w + r];
+        }
+      }
+      v[i] = x;
+    }
+    reinterpret_cast<uint4*>(dst)[c] = *reinterpret_cast<const uint4*>(v);
+  }
+}
+
+int launch_pack_backward(const lmoe_dims& D, const lmoe_weights& w, __nv_bfloat16* wgu_t,
+                         __nv_bfloat16* wed_t, cudaStream_t stream) {
+  pack_tiled_t_kernel<<<8192, 256, 0, stream>>>(wgu_t, nullptr,
+                                                static_cast<const __nv_bfloat16*>(w.w_gate),
+                                                static_cast<const __nv_bfloat16*>(w.w_value), 1,
+                                                D.E, D.L, 2 * D.I);
+  if (cudaGetLastError() != cudaSuccess) return LMOE_ERR_CUDA;
+  pack_tiled_t_kernel<<<8192, 256, 0, stream>>>(wed_t, static_cast<const __nv_bfloat16*>(w.w_edown),
+                                                nullptr, nullptr, 0, D.E, D.I, D.L);
+  return cudaGetLastError() == cudaSuccess ? LMOE_OK : LMOE_ERR_CUDA;
+}
+
 static int run_pack_tiled(__nv_bfloat16* dst, const __nv_bfloat16* w, const __nv_bfloat16* w_g,
                           const __nv_bfloat16* w_v, int glu, int E, int M_w, int Kd,
                           cudaStream_t stream) {

@@ -65,6 +65,12 @@ SIGNATURES = {
     "lmoe_threshold_candidates": (_i, [_vp, _i, _i, _i, _vp, _vp]),
     "lmoe_quantize_e4m3": (_i, [_vp, ctypes.c_longlong, _i, _vp, _vp, _vp]),
     "lmoe_tau_ema": (_i, [_vp, _vp, _i, _f, _i, _vp]),
+    "lmoe_packed_backward_bytes": (_sz, [ctypes.POINTER(Dims)]),
+    "lmoe_pack_backward_weights": (_i, [ctypes.POINTER(Dims), ctypes.POINTER(Weights), _vp, _sz,
+                                        _vp]),
+    "lmoe_routed_backward_workspace_bytes": (_sz, [ctypes.POINTER(Dims)]),
+    "lmoe_routed_backward": (_i, [ctypes.POINTER(Dims), _vp, _vp, _vp, _sz, _vp, _vp, _vp, _vp,
+                                  _vp, _vp, _vp, _sz, _vp]),
     "lmoe_ep_workspace_bytes": (_sz, [_i, _i, _i, _i]),
     "lmoe_ep_dispatch": (_i, [_vp, _i, _i, _i, _i, _vp, _i, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "lmoe_ep_combine": (_i, [_vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _vp,
@@ -504,6 +510,45 @@ class Layer:
 
     def device_error(self) -> int:
         return last_device_error(self.workspace)
+
+    def enable_backward(self, weights: dict, stream=None):
+        """Pack the transposed expert weights and allocate the scratch of ``backward``."""
+        D = self.dims
+        nb = int(load().lmoe_packed_backward_bytes(ctypes.byref(D)))
+        if nb == 0:
+            raise LmoeError(LMOE_ERR_UNSUPPORTED, "lmoe_packed_backward_bytes")
+        self.packed_bwd = torch.empty(nb, dtype=torch.uint8, device=self.device)
+        W = Weights(*[_ptr(weights.get(n)) for n, _ in Weights._fields_])
+        _check(load().lmoe_pack_backward_weights(ctypes.byref(D), ctypes.byref(W),
+                                                 _ptr(self.packed_bwd), nb, _stream(stream)),
+               "lmoe_pack_backward_weights")
+        self.bwd_bytes = int(load().lmoe_routed_backward_workspace_bytes(ctypes.byref(D)))
+        self.bwd_ws = torch.empty(self.bwd_bytes, dtype=torch.uint8, device=self.device)
+
+    def backward(self, dz: torch.Tensor, stream=None) -> dict:
+        """Gradients of the routed branch for the batch of the last ``forward`` call
+        (lmoe_routed_backward): dz [T, L] fp32 -> dlat, dgate, dgamma, dw_gate, dw_value,
+        dw_edown (fp32)."""
+        sh = self.shape
+        T = dz.shape[0]
+        _expect(dz, torch.float32, (T, sh.L), "dz")
+        dims = dims_of(sh, T=T, expert_fp8=self.expert_fp8)
+        dev = dz.device
+        f = torch.float32
+        out = {"dlat": torch.empty((T, sh.L), dtype=f, device=dev),
+               "dgate": torch.empty((T, sh.K), dtype=f, device=dev),
+               "dgamma": torch.empty(sh.L, dtype=f, device=dev),
+               "dw_gu": torch.empty((sh.E, 2 * sh.I, sh.L), dtype=f, device=dev),
+               "dw_edown": torch.empty((sh.E, sh.L, sh.I), dtype=f, device=dev)}
+        bwd_bytes = int(load().lmoe_routed_backward_workspace_bytes(ctypes.byref(dims)))
+        _check(load().lmoe_routed_backward(
+            ctypes.byref(dims), _ptr(self.packed), _ptr(self.packed_bwd), _ptr(self.workspace),
+            self.ws_bytes, _ptr(dz), _ptr(out["dlat"]), _ptr(out["dgate"]), _ptr(out["dgamma"]),
+            _ptr(out["dw_gu"]), _ptr(out["dw_edown"]), _ptr(self.bwd_ws), bwd_bytes,
+            _stream(stream)), "lmoe_routed_backward")
+        out["dw_gate"] = out["dw_gu"][:, :sh.I]
+        out["dw_value"] = out["dw_gu"][:, sh.I:]
+        return out
 
 
 class HostPipeline:
