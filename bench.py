@@ -549,6 +549,61 @@ def run_ours(args):
     return 0
 
 
+def run_backward(args):
+    """The routed branch's backward pass (lmoe_routed_backward) after each forward step, at
+    the K3 prefill workload: the forward is timed as in the headline, the backward alone
+    with CUDA events around it."""
+    world, rank, local = dist_setup(args.gpus)
+    dev = torch.device("cuda", local)
+    wl = Workload(args.shape, dev, rank)
+    sh, layer, x = wl.sh, wl.layer, wl.x
+    layer.enable_backward(wl.w)
+    y = torch.empty_like(x)
+    dz = torch.randn(sh.T, sh.L, generator=torch.Generator(device=dev).manual_seed(SEED),
+                     device=dev)
+    for _ in range(args.warmup):
+        wl.forward(y=y)
+        layer.backward(dz)
+    torch.cuda.synchronize()
+    if layer.device_error() != 0:
+        raise RuntimeError("device-side error during warm-up")
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        for i in range(args.steps):
+            ev[i][0].record()
+            wl.forward(y=y)
+            ev[i][1].record()
+            layer.backward(dz)
+            ev[i][2].record()
+        torch.cuda.synchronize()
+    barrier(world)
+    fwd_launches = layer.last_kernel_launches
+    fwd = max_over_ranks(float(np.mean([e[0].elapsed_time(e[1]) for e in ev])), world)
+    bwd = max_over_ranks(float(np.mean([e[1].elapsed_time(e[2]) for e in ev])), world)
+    TK = sh.T * sh.K
+    flop = 16.0 * TK * sh.L * sh.I      # dgrad x2, recomputed gate/value, wgrad x2
+    grad_bytes = 4.0 * sh.E * 3 * sh.I * sh.L
+    peaks, _ = load_peaks()
+    line = {"metric": "routed-branch backward tokens/s (K3 prefill)",
+            "value": world * sh.T / (bwd / 1e3), "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": bwd,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded; random-init weights of the K3 layer shape; dz ~ N(0,1))",
+            "config": {"workload": wl.config(world)["workload"],
+                       "backward": "routed branch: dlat, dgate, dgamma, dW_g, dW_v, dW_ed (fp32)"},
+            "forward_ms": fwd, "backward_ms": bwd,
+            "backward_tflops": flop / (bwd / 1e3) / 1e12,
+            "weight_gradient_bytes": grad_bytes,
+            "weight_gradient_write_ms_at_hbm_peak": grad_bytes / (peaks["hbm_gbs"] * 1e9) * 1e3,
+            "clocks": clk.summary(),
+            "gpu_launches": (fwd_launches + layer.BACKWARD_LAUNCHES) * args.steps}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
 def run_ep(args):
     """Expert-parallel dispatch and combine, packed and unpacked on one GPU, at the K3 prefill
     routing shape over R ranks: the bytes that would cross the interconnect per token with
@@ -630,6 +685,8 @@ def main():
                     help="run the shared experts on a second stream beside the routed path")
     ap.add_argument("--shared-sms", type=int, default=0,
                     help="SMs for the shared experts when they overlap (0: library default)")
+    ap.add_argument("--backward", action="store_true",
+                    help="time the routed branch's backward pass after each forward step")
     ap.add_argument("--ep-ranks", type=int, default=8,
                     help="--shape ep: ranks the experts are spread over")
     ap.add_argument("--experts", choices=["bf16", "fp8"], default="bf16",
@@ -645,6 +702,8 @@ def main():
                               "--shape ep measures pack/unpack kernels only"}), flush=True)
             return 0
         return run_reference(args)
+    if args.backward:
+        return run_backward(args)
     return run_ep(args) if args.shape == "ep" else run_ours(args)
 
 

@@ -274,42 +274,61 @@ pad_scan_kernel(const int32_t* __restrict__ offsets, int E, int32_t* __restrict_
 
 // XT[w, q] for q < kseg[E]: column q of expert e's padded range is its token
 // p = offsets[e] + (q - kseg[e]) (row gather[p] of x, or row p), or zero past the expert's
-// tokens.  32 x 32 tiles through shared memory.
+// tokens.  Every expert's range starts on a multiple of 64, so one 64 x 64 tile lies in one
+// expert: one lookup per CTA, 16-byte row loads into shared memory, and 16-byte stores of
+// eight consecutive q of one output row (a warp reads 32 consecutive w of one tile row).
+constexpr int TP_TILE = 64;
+constexpr int TP_PITCH = TP_TILE + 8;  // bf16 per shared row; keeps 16-byte row stores aligned
+
 __global__ void __launch_bounds__(256)
 transpose_pad_kernel(const __nv_bfloat16* __restrict__ x, int64_t ldx,
                      const int32_t* __restrict__ gather, int W, const int32_t* __restrict__ offsets,
                      const int32_t* __restrict__ kseg, int E, int64_t ldt,
                      __nv_bfloat16* __restrict__ xt) {
-  __shared__ __nv_bfloat16 tile[32][34];
+  __shared__ __align__(16) __nv_bfloat16 tile[TP_TILE][TP_PITCH];
+  __shared__ int64_t row_src[TP_TILE];
   pdl_wait();
   pdl_launch_dependents();
-  const int w0 = blockIdx.x * 32;
-  const int64_t q0 = static_cast<int64_t>(blockIdx.y) * 32;
+  const int w0 = blockIdx.y * TP_TILE;
+  const int64_t q0 = static_cast<int64_t>(blockIdx.x) * TP_TILE;
   const int qtot = __ldg(kseg + E);
   if (q0 >= qtot) return;
-  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8
-  for (int i = ty; i < 32; i += 8) {
-    const int64_t q = q0 + i;
-    __nv_bfloat16 val = __float2bfloat16_rn(0.0f);
-    if (q < qtot && w0 + tx < W) {
-      int lo = 0, hi = E;  // kseg[lo] <= q < kseg[hi]
-      while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (__ldg(kseg + mid) <= q) lo = mid; else hi = mid;
-      }
-      const int64_t p = __ldg(offsets + lo) + (q - __ldg(kseg + lo));
-      if (p < __ldg(offsets + lo + 1)) {
-        const int64_t src = gather ? __ldg(gather + p) : p;
-        val = x[src * ldx + w0 + tx];
-      }
+  if (threadIdx.x < TP_TILE) {
+    int lo = 0, hi = E;  // kseg[lo] <= q0 < kseg[hi]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (__ldg(kseg + mid) <= q0) lo = mid; else hi = mid;
     }
-    tile[i][tx] = val;
+    const int64_t p = __ldg(offsets + lo) + (q0 + threadIdx.x - __ldg(kseg + lo));
+    row_src[threadIdx.x] =
+        p < __ldg(offsets + lo + 1) ? (gather ? static_cast<int64_t>(__ldg(gather + p)) : p) : -1;
   }
   __syncthreads();
-  for (int i = ty; i < 32; i += 8) {
-    const int w = w0 + i;
-    const int64_t q = q0 + tx;
-    if (w < W && q < qtot) xt[static_cast<int64_t>(w) * ldt + q] = tile[tx][i];
+  const int c = threadIdx.x & 7;  // 16-byte chunk of a 64-wide row
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int r = (threadIdx.x >> 3) + 32 * i;
+    const int64_t src = row_src[r];
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (src >= 0 && w0 + 8 * c < W)
+      v = __ldg(reinterpret_cast<const uint4*>(x + src * ldx + w0 + 8 * c));
+    *reinterpret_cast<uint4*>(&tile[r][8 * c]) = v;
+  }
+  __syncthreads();
+  const int lane = threadIdx.x & 31, qc = threadIdx.x >> 5;  // q chunk per warp
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int wl = lane + 32 * i;
+    if (w0 + wl >= W || q0 + 8 * qc >= qtot) continue;
+    uint32_t pk[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t lo = __bfloat16_as_ushort(tile[8 * qc + 2 * j][wl]);
+      const uint32_t hi = __bfloat16_as_ushort(tile[8 * qc + 2 * j + 1][wl]);
+      pk[j] = lo | (hi << 16);
+    }
+    *reinterpret_cast<uint4*>(xt + static_cast<int64_t>(w0 + wl) * ldt + q0 + 8 * qc) =
+        make_uint4(pk[0], pk[1], pk[2], pk[3]);
   }
 }
 
@@ -380,7 +399,13 @@ int launch_pad_scan(const int32_t* offsets, int E, int32_t* kseg, cudaStream_t s
 int launch_transpose_pad(const __nv_bfloat16* x, int64_t ldx, const int32_t* gather, int W,
                          const int32_t* offsets, const int32_t* kseg, int E, int64_t qmax,
                          int64_t ldt, __nv_bfloat16* xt, cudaStream_t stream) {
-  const dim3 grid(static_cast<unsigned>(ceil_div(W, 32)), static_cast<unsigned>(ceil_div(qmax, 32)));
+  // 16-byte rows and stores; padded ranges are whole tiles
+  if (W % 8 || ldx % 8 || ldt % 8 || qmax % TP_TILE || (reinterpret_cast<uintptr_t>(x) & 15) ||
+      (reinterpret_cast<uintptr_t>(xt) & 15))
+    return LMOE_ERR_UNSUPPORTED;
+  if (ceil_div(W, TP_TILE) > 65535) return LMOE_ERR_UNSUPPORTED;
+  const dim3 grid(static_cast<unsigned>(qmax / TP_TILE),
+                  static_cast<unsigned>(ceil_div(W, TP_TILE)));
   return launch_pdl(transpose_pad_kernel, grid, 256, 0, stream, x, ldx, gather, W, offsets, kseg,
                     E, ldt, xt) == cudaSuccess
              ? LMOE_OK

@@ -38,7 +38,10 @@ struct GemmCfg {
   static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
   static constexpr int NUM_BARS = 2 * STAGES + 6;
   static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
-  static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;  // + slack for 1024 alignment
+  // grouped-K epilogue staging: 32 rows x 32 fp32 per epilogue warp
+  static constexpr int EPI_OFF = (MISC_OFF + 16 + 127) / 128 * 128;
+  static constexpr int EPI_BYTES = 4 * 32 * 32 * 4;
+  static constexpr int SMEM_BYTES = EPI_OFF + EPI_BYTES + 1024;  // + slack for 1024 alignment
   static constexpr uint32_t IDESC = ptx::idesc_bf16_f32(BLOCK_M, BN);
   static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "tiles must stay 1024-aligned");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
@@ -353,6 +356,7 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA,
   } else {
     // ------------------------------------------------------------ epilogue (warps 2..5)
     const int q = warp & 3;  // TMEM lane quarter this warp may access
+    float* stage = reinterpret_cast<float*>(smem + C::EPI_OFF) + q * 32 * 32;
     const float c = g.c, inv_c = 1.0f / g.c;
     int lt = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++lt) {
@@ -367,6 +371,7 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA,
       const TileCoord tc = decode_tile<BN>(g, nt, mt_dense, tile);
       const int row = tc.a_row + q * 32 + lane;
       const bool row_ok = row < tc.row_end;
+      const int orow = (g.groups > 0 && row_ok) ? (g.row_map ? __ldg(g.row_map + row) : row) : 0;
       const uint32_t tbase =
           tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
 #pragma unroll 1
@@ -382,21 +387,27 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA,
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = 0.0f;
           }
-          if (row_ok) {
-            const int orow = g.row_map ? __ldg(g.row_map + row) : row;
-            float* o = g.outf + tc.grp * g.group_stride + static_cast<size_t>(orow) * g.ldf + col0;
-            const int nvalid = min(32, g.N - col0);
-            if (nvalid == 32) {
+          // Through this warp's staging buffer (16-byte chunks XOR-swizzled by row), so that
+          // each store instruction writes four whole 128-byte row segments instead of one
+          // 16-byte piece of 32 rows.
 #pragma unroll
-              for (int q4 = 0; q4 < 8; ++q4)
-                reinterpret_cast<float4*>(o)[q4] =
-                    make_float4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]);
-            } else {
+          for (int j = 0; j < 8; ++j)
+            reinterpret_cast<float4*>(stage + lane * 32)[j ^ (lane & 7)] =
+                make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+          __syncwarp();
+          const int nvalid = min(32, g.N - col0);  // a multiple of 16
+          const int c4 = lane & 7;
+          float* og = g.outf + tc.grp * g.group_stride + col0 + 4 * c4;
 #pragma unroll
-              for (int i = 0; i < 32; ++i)
-                if (i < nvalid) o[i] = v[i];
-            }
+          for (int it = 0; it < 8; ++it) {
+            const int r = 4 * it + (lane >> 3);
+            const int orow_r = __shfl_sync(0xffffffffu, orow, r);
+            const bool ok_r = __shfl_sync(0xffffffffu, row_ok ? 1 : 0, r) != 0;
+            if (ok_r && 4 * c4 < nvalid)
+              *reinterpret_cast<float4*>(og + static_cast<size_t>(orow_r) * g.ldf) =
+                  reinterpret_cast<const float4*>(stage + r * 32)[c4 ^ (r & 7)];
           }
+          __syncwarp();
           continue;
         }
         ptx::tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(ch * 32), v);
@@ -466,7 +477,8 @@ static int launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArg
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return LMOE_ERR_CUDA;
   int grid = (g.max_ctas > 0 && g.max_ctas < sms) ? g.max_ctas : sms;
-  const int64_t tiles = ceil_div(g.M, BLOCK_M) * ceil_div(g.N, BN);
+  const int64_t tiles =
+      ceil_div(g.M, BLOCK_M) * ceil_div(g.N, BN) * (g.groups > 0 ? g.groups : 1);
   if (tiles < grid) grid = static_cast<int>(tiles);
   if (grid <= 0) return LMOE_OK;
   return launch_pdl(gemm_tcgen05_kernel<BN>, grid, GEMM_THREADS, C::SMEM_BYTES, stream, ta, tb, g) ==

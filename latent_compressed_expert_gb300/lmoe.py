@@ -525,6 +525,11 @@ class Layer:
         self.bwd_bytes = int(load().lmoe_routed_backward_workspace_bytes(ctypes.byref(D)))
         self.bwd_ws = torch.empty(self.bwd_bytes, dtype=torch.uint8, device=self.device)
 
+    # kernels one lmoe_routed_backward call launches: combine backward, two dgamma passes,
+    # three grouped GEMMs, SiTU backward, slot sum, pad scan, row map, four transposes and
+    # two grouped-K weight-gradient GEMMs
+    BACKWARD_LAUNCHES = 15
+
     def backward(self, dz: torch.Tensor, stream=None) -> dict:
         """Gradients of the routed branch for the batch of the last ``forward`` call
         (lmoe_routed_backward): dz [T, L] fp32 -> dlat, dgate, dgamma, dw_gate, dw_value,
