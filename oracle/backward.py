@@ -1,6 +1,9 @@
 """Backward pass of the routed-expert branch -- TEST INFRASTRUCTURE ONLY (the product path
 never imports this module).
 
+Two functions: ``routed_backward`` for the routed branch alone (from dz at the RMSNorm output),
+and ``layer_backward`` for the whole layer (from dy at the layer output).
+
 The branch, as the forward oracle (``lmoe_oracle.c``, ``oracle_routed``) defines it, for a
 token t with selected experts e_j and gates g_j (routing is a discrete choice and is held
 fixed; the gates carry gradient):
@@ -63,3 +66,65 @@ def routed_backward(lat, idx, gate, w_gate, w_value, w_edown, gamma, dz, c=100.0
     return {"z": z.detach().numpy(), "dlat": lat_t.grad.numpy(), "dgate": gate_t.grad.numpy(),
             "dgamma": gam_t.grad.numpy(), "dw_gate": wg.grad.numpy(),
             "dw_value": wv.grad.numpy(), "dw_edown": wed.grad.numpy()}
+
+
+def _f64(a) -> torch.Tensor:
+    """A float64 copy of a tensor, a bf16 bit array (int16/uint16) or a float array."""
+    if isinstance(a, torch.Tensor):
+        return a.detach().to(torch.float64).cpu().clone()
+    a = np.asarray(a)
+    if a.dtype in (np.int16, np.uint16):
+        return _bf16_values(a)
+    return torch.as_tensor(a.astype(np.float64))
+
+
+def _situ(g, v, c):
+    gc = c * torch.tanh(g / c)
+    return gc * torch.sigmoid(gc) * (c * torch.tanh(v / c))
+
+
+def layer_forward_t(x, idx, w: dict, c=100.0, eps=1e-6, gate=None):
+    """The whole layer without its residual term, in float64 torch ops, with routing held at
+    ``idx`` (the forward oracle's ``latent``, ``router_logits``, ``route``, ``routed``,
+    ``shared`` and ``output``):
+        lat = x W_down^T,  logits = lat W_r^T,  s = sigmoid(logits),
+        g_j = s[e_j] / sum_i s[e_i]   (the selected experts),
+        z = routed branch (see the module docstring),
+        hs_s = SiTU-GLU(x W_sg[s]^T, x W_sv[s]^T),  y = z W_up^T + sum_s hs_s W_sd[s]^T.
+    ``gate`` replaces the computed gates when given (to pin the rest of the restatement to
+    the C oracle, which takes fp32 gates).  Returns (y, {"lat", "logits", "gate", "z"})."""
+    idx_t = torch.as_tensor(np.asarray(idx), dtype=torch.long)
+    lat = x @ w["w_down"].T
+    logits = lat @ w["w_router"].T
+    if gate is None:
+        s = torch.sigmoid(torch.gather(logits, 1, idx_t))
+        gate = s / s.sum(1, keepdim=True)
+    z = routed_forward_t(lat, idx, gate, w["w_gate"], w["w_value"], w["w_edown"], w["gamma"],
+                         c, eps)
+    y = z @ w["w_up"].T
+    if w["w_sgate"].shape[0] > 0:
+        G = torch.einsum("td,sid->tsi", x, w["w_sgate"])
+        V = torch.einsum("td,sid->tsi", x, w["w_svalue"])
+        y = y + torch.einsum("tsi,sdi->td", _situ(G, V, c), w["w_sdown"])
+    return y, {"lat": lat, "logits": logits, "gate": gate, "z": z}
+
+
+LAYER_WEIGHTS = ("w_down", "w_router", "w_gate", "w_value", "w_edown", "w_up", "w_sgate",
+                 "w_svalue", "w_sdown")
+
+
+def layer_backward(x, idx, w: dict, dy, c=100.0, eps=1e-6) -> dict:
+    """Gradients of sum(dy * y) for the layer (``layer_forward_t``) with respect to x (through
+    the latent and the shared experts; the residual adds dy itself), gamma and every weight,
+    in float64: keys dx, dgamma and "d" + weight name (dw_down [L, d], dw_router [E, L],
+    dw_gate, dw_value, dw_edown, dw_up [d, L], dw_sgate, dw_svalue, dw_sdown); "y" is the
+    forward value.  x, dy: [n, d]; weights bf16 tensors or bit arrays, gamma fp32."""
+    xt = _f64(x).requires_grad_(True)
+    wt = {k: _f64(w[k]).requires_grad_(True) for k in LAYER_WEIGHTS + ("gamma",)}
+    y, _ = layer_forward_t(xt, idx, wt, c, eps)
+    y.backward(torch.as_tensor(np.asarray(dy, dtype=np.float64)))
+    out = {"y": y.detach().numpy(), "dx": xt.grad.numpy(), "dgamma": wt["gamma"].grad.numpy()}
+    for k in LAYER_WEIGHTS:
+        g = wt[k].grad  # None for weights the forward does not reach (no shared experts)
+        out["d" + k] = g.numpy() if g is not None else np.zeros(tuple(wt[k].shape))
+    return out

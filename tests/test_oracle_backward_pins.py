@@ -85,3 +85,66 @@ def test_gradients_equal_finite_differences(oracle_mod, c):
     # (gamma enters the C oracle as fp32, which would round the perturbation away)
     fd = (loss(lat, gate, a, wgf, wvf, wdf) - loss(lat, gate, b, wgf, wvf, wdf)) / (2 * h)
     assert fd == pytest.approx(g["dgamma"][l], rel=1e-5, abs=1e-7)
+
+
+# --- the whole layer (layer_backward) ---------------------------------------------------
+
+def _layer_case(S, seed=5, T=7):
+    sh = synth.LayerShape("tiny_bwd", T=T, d=48, L=32, E=8, K=3, I=16, S=S, Is=16 if S else 0)
+    w = synth.make_weights(sh, seed=seed)
+    w["gamma"] = torch.linspace(0.6, 1.4, sh.L)
+    x = synth.make_x(sh, seed=seed + 1)
+    return sh, w, x
+
+
+@pytest.mark.parametrize("S", [2, 0])
+def test_layer_restatement_equals_c_oracle(oracle_mod, S):
+    """With the C oracle's routing and fp32 gates the restated layer reproduces its output,
+    latent and logits; the restatement's own fp64 gates match route's fp32 gates to within
+    the fp32 sigmoid's error."""
+    import oracle.backward as B
+    sh, w, x = _layer_case(S)
+    r = oracle_mod.forward(w, x, sh.K, residual=None, tau="batch")
+    w64 = {k: B._f64(v) for k, v in w.items()}
+    x64 = B._f64(x)
+    y, parts = B.layer_forward_t(x64, r.idx, w64, gate=torch.as_tensor(r.gate.astype(np.float64)))
+    rms = float(np.sqrt(np.mean(r.y ** 2)))
+    assert np.allclose(y.numpy(), r.y, rtol=1e-10, atol=1e-10 * rms)
+    assert np.allclose(parts["lat"].numpy(), r.lat, rtol=1e-12, atol=1e-12)
+    lg = parts["logits"].numpy()
+    assert np.all(np.abs(lg - r.logits) <= 2.0 ** -24 * np.abs(lg) + 1e-30)
+    _, own = B.layer_forward_t(x64, r.idx, w64)
+    assert np.allclose(own["gate"].numpy(), r.gate, rtol=2e-6, atol=0)
+
+
+@pytest.mark.parametrize("S,c", [(2, 100.0), (2, 2.0), (0, 100.0)])
+def test_layer_gradients_equal_finite_differences(S, c):
+    """Central differences of the restated layer (routing held fixed) on a few entries of x,
+    gamma and every weight."""
+    import oracle.backward as B
+    sh, w, x = _layer_case(S, seed=11)
+    rng = np.random.default_rng(12)
+    idx = np.stack([rng.choice(sh.E, sh.K, replace=False) for _ in range(sh.T)]).astype(np.int32)
+    dy = rng.standard_normal((sh.T, sh.d))
+    g = B.layer_backward(x, idx, w, dy, c=c)
+    base = {k: B._f64(v) for k, v in w.items()}
+    base["x"] = B._f64(x)
+    key = {"x": "dx", "gamma": "dgamma"}
+
+    def loss(vals):
+        wd = {k: v for k, v in vals.items() if k != "x"}
+        y, _ = B.layer_forward_t(vals["x"], idx, wd, c=c)
+        return float(torch.sum(torch.as_tensor(dy) * y))
+
+    h = 1e-6
+    names = ["x", "gamma"] + [n for n in B.LAYER_WEIGHTS if base[n].numel() > 0]
+    for name in names:
+        for _ in range(3):
+            ix = tuple(int(rng.integers(s)) for s in base[name].shape)
+            a, b = dict(base), dict(base)
+            a[name] = base[name].clone()
+            b[name] = base[name].clone()
+            a[name][ix] += h
+            b[name][ix] -= h
+            fd = (loss(a) - loss(b)) / (2 * h)
+            assert fd == pytest.approx(g[key.get(name, "d" + name)][ix], rel=1e-5, abs=1e-7), name
