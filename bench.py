@@ -550,20 +550,28 @@ def run_ours(args):
 
 
 def run_backward(args):
-    """The routed branch's backward pass (lmoe_routed_backward) after each forward step, at
-    the K3 prefill workload: the forward is timed as in the headline, the backward alone
-    with CUDA events around it."""
+    """The backward pass after each forward step, at the K3 prefill workload: the whole layer
+    (lmoe_backward, from dy) or the routed branch alone (lmoe_routed_backward, from dz).  The
+    forward is timed as in the headline, the backward alone with CUDA events around it."""
     world, rank, local = dist_setup(args.gpus)
     dev = torch.device("cuda", local)
     wl = Workload(args.shape, dev, rank)
     sh, layer, x = wl.sh, wl.layer, wl.x
     layer.enable_backward(wl.w)
+    whole = args.backward == "layer"
     y = torch.empty_like(x)
-    dz = torch.randn(sh.T, sh.L, generator=torch.Generator(device=dev).manual_seed(SEED),
-                     device=dev)
+    gen = torch.Generator(device=dev).manual_seed(SEED)
+    if whole:
+        grad = torch.randn(sh.T, sh.d, generator=gen, device=dev).to(torch.bfloat16)
+        step_bwd = lambda: layer.backward_layer(x, grad)  # noqa: E731
+        bwd_launches = layer.layer_backward_launches()
+    else:
+        grad = torch.randn(sh.T, sh.L, generator=gen, device=dev)
+        step_bwd = lambda: layer.backward(grad)  # noqa: E731
+        bwd_launches = layer.BACKWARD_LAUNCHES
     for _ in range(args.warmup):
         wl.forward(y=y)
-        layer.backward(dz)
+        step_bwd()
     torch.cuda.synchronize()
     if layer.device_error() != 0:
         raise RuntimeError("device-side error during warm-up")
@@ -575,30 +583,40 @@ def run_backward(args):
             ev[i][0].record()
             wl.forward(y=y)
             ev[i][1].record()
-            layer.backward(dz)
+            step_bwd()
             ev[i][2].record()
         torch.cuda.synchronize()
     barrier(world)
     fwd_launches = layer.last_kernel_launches
     fwd = max_over_ranks(float(np.mean([e[0].elapsed_time(e[1]) for e in ev])), world)
     bwd = max_over_ranks(float(np.mean([e[1].elapsed_time(e[2]) for e in ev])), world)
-    TK = sh.T * sh.K
-    flop = 16.0 * TK * sh.L * sh.I      # dgrad x2, recomputed gate/value, wgrad x2
-    grad_bytes = 4.0 * sh.E * 3 * sh.I * sh.L
+    T, TK, L, I, E, d = sh.T, sh.T * sh.K, sh.L, sh.I, sh.E, sh.d
+    sw = sh.S * sh.Is
+    # routed: dgrad x2, recomputed gate/value, wgrad x2 (2 flop per multiply-add each)
+    flop = 16.0 * TK * L * I
+    grad_bytes = 4.0 * E * 3 * I * L
+    if whole:
+        # dz/dhs, dx, router dgrad, shared recompute; dW_out, dW_in, dW_router
+        flop += 2.0 * T * d * (L + sw) * 2 + 2.0 * T * (L + 2 * sw) * d * 2 \
+            + 2.0 * T * E * L * 2 + 2.0 * T * d * 2 * sw
+        grad_bytes += 4.0 * (d * (L + sw) + (L + 2 * sw) * d + E * L)
     peaks, _ = load_peaks()
-    line = {"metric": "routed-branch backward tokens/s (K3 prefill)",
+    what = "layer" if whole else "routed-branch"
+    line = {"metric": f"{what} backward tokens/s (K3 prefill)",
             "value": world * sh.T / (bwd / 1e3), "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": bwd,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-            "data": "synthetic (seeded; random-init weights of the K3 layer shape; dz ~ N(0,1))",
+            "data": "synthetic (seeded; random-init weights of the K3 layer shape; "
+                    + ("dy" if whole else "dz") + " ~ N(0,1))",
             "config": {"workload": wl.config(world)["workload"],
-                       "backward": "routed branch: dlat, dgate, dgamma, dW_g, dW_v, dW_ed (fp32)"},
+                       "backward": "whole layer: dx and every weight's gradient (fp32)" if whole
+                       else "routed branch: dlat, dgate, dgamma, dW_g, dW_v, dW_ed (fp32)"},
             "forward_ms": fwd, "backward_ms": bwd,
             "backward_tflops": flop / (bwd / 1e3) / 1e12,
             "weight_gradient_bytes": grad_bytes,
             "weight_gradient_write_ms_at_hbm_peak": grad_bytes / (peaks["hbm_gbs"] * 1e9) * 1e3,
             "clocks": clk.summary(),
-            "gpu_launches": (fwd_launches + layer.BACKWARD_LAUNCHES) * args.steps}
+            "gpu_launches": (fwd_launches + bwd_launches) * args.steps}
     if rank == 0:
         print(json.dumps(line), flush=True)
     return 0
@@ -685,8 +703,9 @@ def main():
                     help="run the shared experts on a second stream beside the routed path")
     ap.add_argument("--shared-sms", type=int, default=0,
                     help="SMs for the shared experts when they overlap (0: library default)")
-    ap.add_argument("--backward", action="store_true",
-                    help="time the routed branch's backward pass after each forward step")
+    ap.add_argument("--backward", nargs="?", const="layer", choices=("layer", "routed"),
+                    help="time the backward pass after each forward step: the whole layer "
+                         "(lmoe_backward, the default) or the routed branch alone")
     ap.add_argument("--ep-ranks", type=int, default=8,
                     help="--shape ep: ranks the experts are spread over")
     ap.add_argument("--experts", choices=["bf16", "fp8"], default="bf16",

@@ -309,20 +309,48 @@ int lmoe_gemm_bf16(const void *A, const void *B, float *C, int M, int N, int Kd,
  * stream) that produced z: the latent, the routing, the SiTU outputs and the expert outputs
  * are read from there; the gate/value pre-activations are recomputed.  Operands of the
  * GEMMs are bf16 with fp32 accumulation, like the forward's.  bf16 routed experts only.
- *   lmoe_pack_backward_weights: transposed tiled copies of the expert weights into
- *     packed_bwd (lmoe_packed_backward_bytes; from the same unpacked weights as the forward).
+ *   lmoe_pack_backward_weights: transposed copies of the weights into packed_bwd
+ *     (lmoe_packed_backward_bytes): the expert weights in tiles, from the same unpacked
+ *     weights w as the forward's packing, and the dense weights, from `packed` (the
+ *     forward's packed buffer, filled by lmoe_pack_weights with the same dims).
  *   lmoe_routed_backward: dz [T, L] fp32 in; dlat [T, L], dgate [T, K], dgamma [L],
  *     dw_gu [E, 2I, L] (rows 0..I-1: W_g, rows I..2I-1: W_v) and dw_ed [E, L, I], all fp32,
  *     out; bwd_ws: lmoe_routed_backward_workspace_bytes of device scratch.
  * Errors: INVALID_ARG, UNSUPPORTED (expert_fp8), WORKSPACE_TOO_SMALL, CUDA. */
 size_t lmoe_packed_backward_bytes(const lmoe_dims *dims);
-int lmoe_pack_backward_weights(const lmoe_dims *dims, const lmoe_weights *w, void *packed_bwd,
-                               size_t bytes, void *stream);
+int lmoe_pack_backward_weights(const lmoe_dims *dims, const lmoe_weights *w, const void *packed,
+                               void *packed_bwd, size_t bytes, void *stream);
 size_t lmoe_routed_backward_workspace_bytes(const lmoe_dims *dims);
 int lmoe_routed_backward(const lmoe_dims *dims, const void *packed, const void *packed_bwd,
                          void *workspace, size_t ws_bytes, const float *dz, float *dlat,
                          float *dgate, float *dgamma, float *dw_gu, float *dw_ed, void *bwd_ws,
                          size_t bwd_ws_bytes, void *stream);
+
+/* Backward pass of the whole layer (the same passages; the layer as lmoe_forward computes
+ * it).  Given dy = dLoss/dy [T, d] bf16 for the lmoe_forward call whose workspace is passed
+ * (same dims, packed weights and stream), computes, all fp32:
+ *   dx [T, d]: the gradient reaching x through the latent (x W_down^T) and the shared
+ *     experts.  The residual term adds dy itself, which dx does not include.
+ *   dgamma [L];
+ *   dw_in [L + 2 S Is, d]: rows 0..L-1 dW_down; then row L + s Is + i for shared expert s's
+ *     gate row i; then row L + S Is + s Is + i for its value row i;
+ *   dw_router [E, L];
+ *   dw_gu [E, 2I, L] and dw_ed [E, L, I] as lmoe_routed_backward;
+ *   dw_out [d, L + S Is]: columns 0..L-1 dW_up, columns L + s Is + i dW_sd[s][:, i].
+ * The router's part: the gates g_j = s_j / sum_i s_i of the selected experts carry gradient
+ * to their scores s = sigmoid(logit), and from there to the latent and W_r; the selection
+ * (thresholds and top-K) is held fixed.  logits: the fp32 [T, E] router logits the forward
+ * routed on -- required when the forward was given lmoe_io.logits_in, else NULL (the ones
+ * it computed into the workspace).  x: the forward's input [T, d] bf16.
+ * bwd_ws: lmoe_backward_workspace_bytes of device scratch.  bf16 routed experts only.
+ * Errors: INVALID_ARG (null or misaligned pointers), UNSUPPORTED (expert_fp8),
+ * WORKSPACE_TOO_SMALL, CUDA. */
+size_t lmoe_backward_workspace_bytes(const lmoe_dims *dims);
+int lmoe_backward(const lmoe_dims *dims, const void *packed, const void *packed_bwd,
+                  void *workspace, size_t ws_bytes, const void *x, const float *logits,
+                  const void *dy, float *dx, float *dgamma, float *dw_in, float *dw_router,
+                  float *dw_gu, float *dw_ed, float *dw_out, void *bwd_ws, size_t bwd_ws_bytes,
+                  void *stream);
 
 /* Building block of the FP8 routed experts, exposed for verification: per-row e4m3
  * quantisation of x [rows, cols] bf16 (row-major, cols a multiple of 16, 16-byte aligned)

@@ -134,8 +134,11 @@ static GemmArgs gemm_defaults(uint32_t* err, float c) {
 
 // Backward of the routed branch: transposed expert weights and scratch.
 struct BwdPacked {
-  size_t wgu_t, wed_t, total;
+  size_t wgu_t, wed_t;       // expert weights transposed, in 128-row tiles
+  size_t wout_t, wr_t, wls_t;  // dense weights transposed (whole-layer backward)
+  size_t total;
 };
+static int pad64(int n) { return (n + 63) / 64 * 64; }
 static BwdPacked bwd_packed_layout(const lmoe_dims& D) {
   BwdPacked B{};
   size_t off = 0;
@@ -146,6 +149,10 @@ static BwdPacked bwd_packed_layout(const lmoe_dims& D) {
   };
   B.wgu_t = take(static_cast<size_t>(D.E) * ceil_div(D.L, BLOCK_M) * BLOCK_M * 2 * D.I * 2);
   B.wed_t = take(static_cast<size_t>(D.E) * ceil_div(D.I, BLOCK_M) * BLOCK_M * D.L * 2);
+  const size_t sw = static_cast<size_t>(D.S > 0 ? D.S * D.Is : 0);
+  B.wout_t = take((D.L + sw) * D.d * 2);                       // [L + sw, d]
+  B.wr_t = take(static_cast<size_t>(D.L) * pad64(D.E) * 2);      // [L, E padded to 64]
+  B.wls_t = take(static_cast<size_t>(D.d) * (D.L + 2 * sw) * 2);  // [d, L + 2 sw]
   B.total = off;
   return B;
 }
@@ -183,9 +190,209 @@ static BwdLayout bwd_layout(const lmoe_dims& D) {
   return B;
 }
 
+// The whole layer's backward adds these buffers after the routed branch's.
+struct LayerBwdLayout {
+  size_t dz, dhs, dgate, dlogit, dlat_r, dlat, dcat, pre_s, seg1, rowmap_s, dy_t, zh_t, dlogit_t,
+      lat_t, dcat_t, x_t, total;
+  int Tq, Ep, sw, wc, wz;  // T and E padded to 64; shared width; widths of dcat and zh
+};
+static LayerBwdLayout layer_bwd_layout(const lmoe_dims& D) {
+  LayerBwdLayout B{};
+  size_t off = bwd_layout(D).total;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off += align_up(bytes > 0 ? bytes : 1, 256);
+    return o;
+  };
+  B.Tq = pad64(D.T);
+  B.Ep = pad64(D.E);
+  B.sw = D.S > 0 ? D.S * D.Is : 0;
+  B.wc = D.L + 2 * B.sw;
+  B.wz = D.L + B.sw;
+  const size_t T = static_cast<size_t>(D.T), Tq = static_cast<size_t>(B.Tq), L = D.L;
+  B.dz = take(T * L * 4);
+  B.dhs = take(T * B.sw * 2);
+  B.dgate = take(T * D.K * 4);
+  B.dlogit = take(T * B.Ep * 2);
+  B.dlat_r = take(T * L * 4);
+  B.dlat = take(T * L * 4);
+  B.dcat = take(T * B.wc * 2);
+  B.pre_s = take(T * 2 * B.sw * 2);
+  B.seg1 = take(2 * 4);
+  B.rowmap_s = take(static_cast<size_t>(B.wc) * 4);
+  B.dy_t = take(static_cast<size_t>(D.d) * Tq * 2);
+  B.zh_t = take(static_cast<size_t>(B.wz) * Tq * 2);
+  B.dlogit_t = take(static_cast<size_t>(B.Ep) * Tq * 2);
+  B.lat_t = take(L * Tq * 2);
+  B.dcat_t = take(static_cast<size_t>(B.wc) * Tq * 2);
+  B.x_t = take(static_cast<size_t>(D.d) * Tq * 2);
+  B.total = off;
+  return B;
+}
+
+// The routed branch's backward in two halves, shared by lmoe_routed_backward and
+// lmoe_backward (which runs the router's backward between them).
+struct RoutedBwd {
+  lmoe_dims D;
+  const uint8_t* pk;  // packed forward weights
+  const uint8_t* pb;  // packed transposed weights
+  uint8_t* ws;        // forward workspace (the batch's routing and activations)
+  uint8_t* bw;        // backward workspace
+  PackedLayout P;
+  BwdPacked PB;
+  WorkspaceLayout W;
+  BwdLayout B;
+  cudaStream_t stream;
+};
+
+// 1-2. RMSNorm and combine backward (du, do_j, dgate_j), then dgamma.
+static int routed_bwd_front(const RoutedBwd& R, const float* dz, float* dgate, float* dgamma) {
+  using bf = __nv_bfloat16;
+  const lmoe_dims& D = R.D;
+  int rc = launch_combine_bwd(reinterpret_cast<const bf*>(R.ws + R.W.o),
+                              reinterpret_cast<const float*>(R.ws + R.W.gate),
+                              reinterpret_cast<const int32_t*>(R.ws + R.W.inv),
+                              reinterpret_cast<const float*>(R.pk + R.P.gamma), dz, D.T, D.K, D.L,
+                              D.eps, reinterpret_cast<bf*>(R.bw + R.B.dout), dgate,
+                              reinterpret_cast<float*>(R.bw + R.B.u),
+                              reinterpret_cast<float*>(R.bw + R.B.r), R.stream);
+  if (rc != LMOE_OK) return rc;
+  return launch_dgamma(dz, reinterpret_cast<const float*>(R.bw + R.B.u),
+                       reinterpret_cast<const float*>(R.bw + R.B.r), D.T, D.L,
+                       reinterpret_cast<float*>(R.bw + R.B.part), dgamma, R.stream);
+}
+
+
 }  // namespace lmoe
 
 using namespace lmoe;
+
+// 3-11. dgrad through the experts (dlat, plus `dlat_add` when given, also copied to bf16
+// into dlat_b with row stride ldb when given), then the expert weight gradients.
+static int routed_bwd_back(const RoutedBwd& R, const float* dlat_add, float* dlat,
+                           __nv_bfloat16* dlat_b, int64_t ldb, float* dw_gu, float* dw_ed) {
+  using bf = __nv_bfloat16;
+  const lmoe_dims& D = R.D;
+  const int T = D.T, K = D.K, L = D.L, I = D.I, E = D.E, TK = T * K;
+  const WorkspaceLayout& W = R.W;
+  const BwdLayout& B = R.B;
+  const PackedLayout& P = R.P;
+  const BwdPacked& PB = R.PB;
+  const uint8_t* pk = R.pk;
+  const uint8_t* pb = R.pb;
+  uint8_t* ws = R.ws;
+  uint8_t* bw = R.bw;
+  cudaStream_t stream = R.stream;
+  uint32_t* err = reinterpret_cast<uint32_t*>(ws + W.err);
+  const int32_t* offsets = reinterpret_cast<const int32_t*>(ws + W.offsets);
+  const int32_t* ct_off = reinterpret_cast<const int32_t*>(ws + W.ct_off);
+  const int32_t* inv = reinterpret_cast<const int32_t*>(ws + W.inv);
+  const int32_t* src_tok = reinterpret_cast<const int32_t*>(ws + W.src_tok);
+  const bf* lat = reinterpret_cast<const bf*>(ws + W.lat);
+  const bf* h = reinterpret_cast<const bf*>(ws + W.h);
+  bf* dout = reinterpret_cast<bf*>(bw + B.dout);
+  bf* dh = reinterpret_cast<bf*>(bw + B.dh);
+  bf* pre = reinterpret_cast<bf*>(bw + B.pre);
+  bf* dgv = reinterpret_cast<bf*>(bw + B.dgv);
+  bf* dlatp = reinterpret_cast<bf*>(bw + B.dlatp);
+  int32_t* kseg = reinterpret_cast<int32_t*>(bw + B.kseg);
+  int32_t* rowmap = reinterpret_cast<int32_t*>(bw + B.rowmap);
+  const int64_t q = B.qmax;
+  int rc;
+  auto grouped = [&](int M_w, int Kd, const int32_t* gather, const bf* x, int ldx, int epi,
+                     bf* out, int ldo) {
+    GroupedArgs g{};
+    g.E = E;
+    g.M_w = M_w;
+    g.Kd = Kd;
+    g.seg_off = offsets;
+    g.ct_off = ct_off;
+    g.gather = gather;
+    g.x = x;
+    g.ldx = ldx;
+    g.epi = epi;
+    g.out = out;
+    g.ldo = ldo;
+    g.c = D.c;
+    g.err = err;
+    g.timeout_ns = wait_limit_ns();
+    g.mean_tokens = static_cast<int>(static_cast<int64_t>(TK) / E);
+    return g;
+  };
+  // 3. dh = do . W_ed (per expert, weights transposed)
+  {
+    GroupedArgs g = grouped(I, L, nullptr, nullptr, 0, EPI_BF16, dh, I);
+    if ((rc = launch_grouped_gemm(pb + PB.wed_t, dout, static_cast<uint64_t>(TK), L, g, stream)) !=
+        LMOE_OK)
+      return rc;
+  }
+  // 4. gate/value pre-activations again (interleaved rows), 5. through SiTU
+  {
+    GroupedArgs g = grouped(2 * I, L, src_tok, lat, L, EPI_BF16, pre, 2 * I);
+    if ((rc = launch_grouped_gemm(pk + P.wgu, lat, static_cast<uint64_t>(T), L, g, stream)) !=
+        LMOE_OK)
+      return rc;
+  }
+  if ((rc = launch_situ_bwd(pre, dh, TK, I, D.c, dgv, 2 * I, stream)) != LMOE_OK) return rc;
+  // 6. dlat_p = dgv . W_gu (per expert, weights transposed), 7. summed over the slots
+  {
+    GroupedArgs g = grouped(L, 2 * I, nullptr, nullptr, 0, EPI_BF16, dlatp, L);
+    if ((rc = launch_grouped_gemm(pb + PB.wgu_t, dgv, static_cast<uint64_t>(TK), 2 * I, g,
+                                  stream)) != LMOE_OK)
+      return rc;
+  }
+  if ((rc = launch_slot_sum(dlatp, inv, T, K, L, dlat_add, dlat, dlat_b, ldb, stream)) != LMOE_OK) return rc;
+  // 8-9. weight gradients reduce over each expert's tokens: token-contiguous copies, each
+  // expert's range padded to 64 with zeros
+  if ((rc = launch_pad_scan(offsets, E, kseg, stream)) != LMOE_OK ||
+      (rc = launch_rowmap(I, 0, rowmap, nullptr, 0, stream)) != LMOE_OK ||
+      (rc = launch_transpose_pad(dout, L, nullptr, L, offsets, kseg, E, q, q,
+                                 reinterpret_cast<bf*>(bw + B.dout_t), stream)) != LMOE_OK ||
+      (rc = launch_transpose_pad(h, I, nullptr, I, offsets, kseg, E, q, q,
+                                 reinterpret_cast<bf*>(bw + B.h_t), stream)) != LMOE_OK ||
+      (rc = launch_transpose_pad(dgv, 2 * I, nullptr, 2 * I, offsets, kseg, E, q, q,
+                                 reinterpret_cast<bf*>(bw + B.dgv_t), stream)) != LMOE_OK ||
+      (rc = launch_transpose_pad(lat, L, src_tok, L, offsets, kseg, E, q, q,
+                                 reinterpret_cast<bf*>(bw + B.latp_t), stream)) != LMOE_OK)
+    return rc;
+  // 10. dW_ed[e] = do_e^T h_e   [L, I];  11. dW_gu[e] = dgv_e^T lat_e   [2I, L] (gate rows,
+  // then value rows)
+  {
+    GemmArgs g = gemm_defaults(err, D.c);
+    g.M = L;
+    g.N = I;
+    g.Kd = static_cast<int>(q);
+    g.epi = EPI_F32;
+    g.outf = dw_ed;
+    g.ldf = I;
+    g.groups = E;
+    g.kseg = kseg;
+    g.group_stride = static_cast<long long>(L) * I;
+    if ((rc = launch_gemm(bw + B.dout_t, static_cast<uint64_t>(L), static_cast<int>(q),
+                          bw + B.h_t, static_cast<uint64_t>(I), static_cast<int>(q), g,
+                          stream)) != LMOE_OK)
+      return rc;
+  }
+  {
+    GemmArgs g = gemm_defaults(err, D.c);
+    g.M = 2 * I;
+    g.N = L;
+    g.Kd = static_cast<int>(q);
+    g.epi = EPI_F32;
+    g.outf = dw_gu;
+    g.ldf = L;
+    g.groups = E;
+    g.kseg = kseg;
+    g.group_stride = static_cast<long long>(2 * I) * L;
+    g.row_map = rowmap;
+    if ((rc = launch_gemm(bw + B.dgv_t, static_cast<uint64_t>(2 * I), static_cast<int>(q),
+                          bw + B.latp_t, static_cast<uint64_t>(L), static_cast<int>(q), g,
+                          stream)) != LMOE_OK)
+      return rc;
+  }
+  return LMOE_OK;
+}
+
 
 extern "C" {
 
@@ -354,19 +561,37 @@ size_t lmoe_packed_backward_bytes(const lmoe_dims* dims) {
   return bwd_packed_layout(*dims).total;
 }
 
-int lmoe_pack_backward_weights(const lmoe_dims* dims, const lmoe_weights* w, void* packed_bwd,
-                               size_t bytes, void* stream) {
-  const int rc = dims_supported(dims);
-  if (rc != LMOE_OK) return rc;
-  if (dims->expert_fp8) return LMOE_ERR_UNSUPPORTED;
-  if (!w || !packed_bwd || !w->w_gate || !w->w_value || !w->w_edown || !aligned16(packed_bwd))
+int lmoe_pack_backward_weights(const lmoe_dims* dims, const lmoe_weights* w, const void* packed,
+                               void* packed_bwd, size_t bytes, void* stream) {
+  const int rc0 = dims_supported(dims);
+  if (rc0 != LMOE_OK) return rc0;
+  const lmoe_dims D = *dims;
+  if (D.expert_fp8) return LMOE_ERR_UNSUPPORTED;
+  if (!w || !packed || !packed_bwd || !w->w_gate || !w->w_value || !w->w_edown ||
+      !aligned16(packed) || !aligned16(packed_bwd))
     return LMOE_ERR_INVALID_ARG;
-  const BwdPacked B = bwd_packed_layout(*dims);
+  const BwdPacked B = bwd_packed_layout(D);
   if (bytes < B.total) return LMOE_ERR_WORKSPACE_TOO_SMALL;
+  using bf = __nv_bfloat16;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint8_t* base = static_cast<uint8_t*>(packed_bwd);
-  return launch_pack_backward(*dims, *w, reinterpret_cast<__nv_bfloat16*>(base + B.wgu_t),
-                              reinterpret_cast<__nv_bfloat16*>(base + B.wed_t),
-                              static_cast<cudaStream_t>(stream));
+  const uint8_t* pk = static_cast<const uint8_t*>(packed);
+  const PackedLayout P = packed_layout(D);
+  const int sw = shared_width(D), wz = D.L + sw, wc = D.L + 2 * sw, Ep = pad64(D.E);
+  int rc = launch_pack_backward(D, *w, reinterpret_cast<bf*>(base + B.wgu_t),
+                                reinterpret_cast<bf*>(base + B.wed_t), st);
+  // dense weights: [W_up | W_sd] [d, L + sw] -> [L + sw, d]; W_r [E, L] -> [L, E padded];
+  // [W_down ; shared gate/value] [L + 2 sw, d] -> [d, L + 2 sw]
+  if (rc == LMOE_OK)
+    rc = launch_transpose_pad(reinterpret_cast<const bf*>(pk + P.w2), wz, nullptr, wz, nullptr,
+                              nullptr, D.d, D.d, D.d, reinterpret_cast<bf*>(base + B.wout_t), st);
+  if (rc == LMOE_OK)
+    rc = launch_transpose_pad(reinterpret_cast<const bf*>(pk + P.wr), D.L, nullptr, D.L, nullptr,
+                              nullptr, D.E, Ep, Ep, reinterpret_cast<bf*>(base + B.wr_t), st);
+  if (rc == LMOE_OK)
+    rc = launch_transpose_pad(reinterpret_cast<const bf*>(pk + P.w1), D.d, nullptr, D.d, nullptr,
+                              nullptr, wc, wc, wc, reinterpret_cast<bf*>(base + B.wls_t), st);
+  return rc;
 }
 
 size_t lmoe_routed_backward_workspace_bytes(const lmoe_dims* dims) {
@@ -388,136 +613,158 @@ int lmoe_routed_backward(const lmoe_dims* dims, const void* packed, const void* 
   const void* ptrs[] = {packed, packed_bwd, workspace, dz, dlat, dgamma, dw_gu, dw_ed, bwd_ws};
   for (const void* p : ptrs)
     if (!aligned16(p)) return LMOE_ERR_INVALID_ARG;
-  const WorkspaceLayout W = workspace_layout(D);
-  const BwdLayout B = bwd_layout(D);
-  if (ws_bytes < W.total || bwd_ws_bytes < B.total) return LMOE_ERR_WORKSPACE_TOO_SMALL;
+  RoutedBwd R{};
+  R.D = D;
+  R.W = workspace_layout(D);
+  R.B = bwd_layout(D);
+  if (ws_bytes < R.W.total || bwd_ws_bytes < R.B.total) return LMOE_ERR_WORKSPACE_TOO_SMALL;
   if (D.T == 0) return LMOE_OK;
-  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
-  using bf = __nv_bfloat16;
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  uint8_t* bw = static_cast<uint8_t*>(bwd_ws);
-  const uint8_t* pk = static_cast<const uint8_t*>(packed);
-  const uint8_t* pb = static_cast<const uint8_t*>(packed_bwd);
-  const PackedLayout P = packed_layout(D);
-  const BwdPacked PB = bwd_packed_layout(D);
-  const int T = D.T, K = D.K, L = D.L, I = D.I, E = D.E, TK = T * K;
-  uint32_t* err = reinterpret_cast<uint32_t*>(ws + W.err);
-  const int32_t* offsets = reinterpret_cast<const int32_t*>(ws + W.offsets);
-  const int32_t* ct_off = reinterpret_cast<const int32_t*>(ws + W.ct_off);
-  const int32_t* inv = reinterpret_cast<const int32_t*>(ws + W.inv);
-  const int32_t* src_tok = reinterpret_cast<const int32_t*>(ws + W.src_tok);
-  const bf* lat = reinterpret_cast<const bf*>(ws + W.lat);
-  const bf* h = reinterpret_cast<const bf*>(ws + W.h);
-  bf* dout = reinterpret_cast<bf*>(bw + B.dout);
-  bf* dh = reinterpret_cast<bf*>(bw + B.dh);
-  bf* pre = reinterpret_cast<bf*>(bw + B.pre);
-  bf* dgv = reinterpret_cast<bf*>(bw + B.dgv);
-  bf* dlatp = reinterpret_cast<bf*>(bw + B.dlatp);
-  int32_t* kseg = reinterpret_cast<int32_t*>(bw + B.kseg);
-  int32_t* rowmap = reinterpret_cast<int32_t*>(bw + B.rowmap);
-  const int64_t q = B.qmax;
+  R.pk = static_cast<const uint8_t*>(packed);
+  R.pb = static_cast<const uint8_t*>(packed_bwd);
+  R.ws = static_cast<uint8_t*>(workspace);
+  R.bw = static_cast<uint8_t*>(bwd_ws);
+  R.P = packed_layout(D);
+  R.PB = bwd_packed_layout(D);
+  R.stream = static_cast<cudaStream_t>(stream_);
+  if ((rc = routed_bwd_front(R, dz, dgate, dgamma)) != LMOE_OK) return rc;
+  return routed_bwd_back(R, nullptr, dlat, nullptr, 0, dw_gu, dw_ed);
+}
 
-  // 1-2. RMSNorm and combine backward: du, do_j, dg_j; dgamma
-  if ((rc = launch_combine_bwd(reinterpret_cast<const bf*>(ws + W.o),
-                               reinterpret_cast<const float*>(ws + W.gate), inv,
-                               reinterpret_cast<const float*>(pk + P.gamma), dz, T, K, L, D.eps,
-                               dout, dgate, reinterpret_cast<float*>(bw + B.u),
-                               reinterpret_cast<float*>(bw + B.r), stream)) != LMOE_OK ||
-      (rc = launch_dgamma(dz, reinterpret_cast<const float*>(bw + B.u),
-                          reinterpret_cast<const float*>(bw + B.r), T, L,
-                          reinterpret_cast<float*>(bw + B.part), dgamma, stream)) != LMOE_OK)
-    return rc;
-  auto grouped = [&](int M_w, int Kd, const int32_t* gather, const bf* x, int ldx, int epi,
-                     bf* out, int ldo) {
-    GroupedArgs g{};
-    g.E = E;
-    g.M_w = M_w;
+size_t lmoe_backward_workspace_bytes(const lmoe_dims* dims) {
+  if (dims_supported(dims) != LMOE_OK || dims->expert_fp8) return 0;
+  return layer_bwd_layout(*dims).total;
+}
+
+int lmoe_backward(const lmoe_dims* dims, const void* packed, const void* packed_bwd,
+                  void* workspace, size_t ws_bytes, const void* x, const float* logits,
+                  const void* dy, float* dx, float* dgamma, float* dw_in, float* dw_router,
+                  float* dw_gu, float* dw_ed, float* dw_out, void* bwd_ws, size_t bwd_ws_bytes,
+                  void* stream_) {
+  int rc = dims_supported(dims);
+  if (rc != LMOE_OK) return rc;
+  const lmoe_dims D = *dims;
+  if (D.expert_fp8) return LMOE_ERR_UNSUPPORTED;
+  if (!packed || !packed_bwd || !workspace || !x || !dy || !dx || !dgamma || !dw_in ||
+      !dw_router || !dw_gu || !dw_ed || !dw_out || !bwd_ws)
+    return LMOE_ERR_INVALID_ARG;
+  const void* ptrs[] = {packed, packed_bwd, workspace, x, dy, dx, dgamma, dw_in, dw_router,
+                        dw_gu, dw_ed, dw_out, bwd_ws};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return LMOE_ERR_INVALID_ARG;
+  RoutedBwd R{};
+  R.D = D;
+  R.W = workspace_layout(D);
+  R.B = bwd_layout(D);
+  const LayerBwdLayout LB = layer_bwd_layout(D);
+  if (ws_bytes < R.W.total || bwd_ws_bytes < LB.total) return LMOE_ERR_WORKSPACE_TOO_SMALL;
+  if (D.T == 0) return LMOE_OK;
+  using bf = __nv_bfloat16;
+  R.pk = static_cast<const uint8_t*>(packed);
+  R.pb = static_cast<const uint8_t*>(packed_bwd);
+  R.ws = static_cast<uint8_t*>(workspace);
+  R.bw = static_cast<uint8_t*>(bwd_ws);
+  R.P = packed_layout(D);
+  R.PB = bwd_packed_layout(D);
+  R.stream = static_cast<cudaStream_t>(stream_);
+  cudaStream_t stream = R.stream;
+  const uint8_t* pk = R.pk;
+  const uint8_t* pb = R.pb;
+  uint8_t* ws = R.ws;
+  uint8_t* bw = R.bw;
+  const int T = D.T, L = D.L, E = D.E, d = D.d;
+  const int sw = LB.sw, wc = LB.wc, wz = LB.wz, Tq = LB.Tq, Ep = LB.Ep;
+  uint32_t* err = reinterpret_cast<uint32_t*>(ws + R.W.err);
+  const bf* xb = static_cast<const bf*>(x);
+  const bf* dyb = static_cast<const bf*>(dy);
+  const bf* lat = reinterpret_cast<const bf*>(ws + R.W.lat);
+  const bf* zh = reinterpret_cast<const bf*>(ws + R.W.zh);
+  const float* z = logits ? logits : reinterpret_cast<const float*>(ws + R.W.logits);
+  float* dz = reinterpret_cast<float*>(bw + LB.dz);
+  bf* dhs = reinterpret_cast<bf*>(bw + LB.dhs);
+  float* dgate = reinterpret_cast<float*>(bw + LB.dgate);
+  bf* dlogit = reinterpret_cast<bf*>(bw + LB.dlogit);
+  float* dlat_r = reinterpret_cast<float*>(bw + LB.dlat_r);
+  bf* dcat = reinterpret_cast<bf*>(bw + LB.dcat);
+  bf* pre_s = reinterpret_cast<bf*>(bw + LB.pre_s);
+  int32_t* seg1 = reinterpret_cast<int32_t*>(bw + LB.seg1);
+  int32_t* rowmap_s = reinterpret_cast<int32_t*>(bw + LB.rowmap_s);
+  // C[M, N] = A[M, Kd] . B[N, Kd]^T, fp32 or bf16 out
+  auto dense = [&](const void* A, int M, int a_ld, const void* Bm, int N, int b_ld, int Kd,
+                   int epi, void* out, int ld) {
+    GemmArgs g = gemm_defaults(err, D.c);
+    g.M = M;
+    g.N = N;
     g.Kd = Kd;
-    g.seg_off = offsets;
-    g.ct_off = ct_off;
-    g.gather = gather;
-    g.x = x;
-    g.ldx = ldx;
     g.epi = epi;
-    g.out = out;
-    g.ldo = ldo;
-    g.c = D.c;
-    g.err = err;
-    g.timeout_ns = wait_limit_ns();
-    g.mean_tokens = static_cast<int>(static_cast<int64_t>(TK) / E);
-    return g;
+    if (epi == EPI_F32) {
+      g.outf = static_cast<float*>(out);
+      g.ldf = ld;
+    } else {
+      g.out0 = static_cast<bf*>(out);
+      g.ld0 = ld;
+    }
+    return launch_gemm(A, static_cast<uint64_t>(M), a_ld, Bm, static_cast<uint64_t>(N), b_ld, g,
+                       stream);
   };
-  // 3. dh = do . W_ed (per expert, weights transposed)
-  {
-    GroupedArgs g = grouped(I, L, nullptr, nullptr, 0, EPI_BF16, dh, I);
-    if ((rc = launch_grouped_gemm(pb + PB.wed_t, dout, static_cast<uint64_t>(TK), L, g, stream)) !=
-        LMOE_OK)
-      return rc;
-  }
-  // 4. gate/value pre-activations again (interleaved rows), 5. through SiTU
-  {
-    GroupedArgs g = grouped(2 * I, L, src_tok, lat, L, EPI_BF16, pre, 2 * I);
-    if ((rc = launch_grouped_gemm(pk + P.wgu, lat, static_cast<uint64_t>(T), L, g, stream)) !=
-        LMOE_OK)
-      return rc;
-  }
-  if ((rc = launch_situ_bwd(pre, dh, TK, I, D.c, dgv, stream)) != LMOE_OK) return rc;
-  // 6. dlat_p = dgv . W_gu (per expert, weights transposed), 7. summed over the slots
-  {
-    GroupedArgs g = grouped(L, 2 * I, nullptr, nullptr, 0, EPI_BF16, dlatp, L);
-    if ((rc = launch_grouped_gemm(pb + PB.wgu_t, dgv, static_cast<uint64_t>(TK), 2 * I, g,
-                                  stream)) != LMOE_OK)
-      return rc;
-  }
-  if ((rc = launch_slot_sum(dlatp, inv, T, K, L, dlat, stream)) != LMOE_OK) return rc;
-  // 8-9. weight gradients reduce over each expert's tokens: token-contiguous copies, each
-  // expert's range padded to 64 with zeros
-  if ((rc = launch_pad_scan(offsets, E, kseg, stream)) != LMOE_OK ||
-      (rc = launch_rowmap(I, rowmap, stream)) != LMOE_OK ||
-      (rc = launch_transpose_pad(dout, L, nullptr, L, offsets, kseg, E, q, q,
-                                 reinterpret_cast<bf*>(bw + B.dout_t), stream)) != LMOE_OK ||
-      (rc = launch_transpose_pad(h, I, nullptr, I, offsets, kseg, E, q, q,
-                                 reinterpret_cast<bf*>(bw + B.h_t), stream)) != LMOE_OK ||
-      (rc = launch_transpose_pad(dgv, 2 * I, nullptr, 2 * I, offsets, kseg, E, q, q,
-                                 reinterpret_cast<bf*>(bw + B.dgv_t), stream)) != LMOE_OK ||
-      (rc = launch_transpose_pad(lat, L, src_tok, L, offsets, kseg, E, q, q,
-                                 reinterpret_cast<bf*>(bw + B.latp_t), stream)) != LMOE_OK)
+  // weight gradient dW[M, N] = At[M, Tq] . Bt[N, Tq]^T over the padded token axis (one group)
+  auto wgrad = [&](const bf* At, int M, const bf* Bt, int N, float* out, const int32_t* row_map) {
+    GemmArgs g = gemm_defaults(err, D.c);
+    g.M = M;
+    g.N = N;
+    g.Kd = Tq;
+    g.epi = EPI_F32;
+    g.outf = out;
+    g.ldf = N;
+    g.groups = 1;
+    g.kseg = seg1;
+    g.row_map = row_map;
+    return launch_gemm(At, static_cast<uint64_t>(M), Tq, Bt, static_cast<uint64_t>(N), Tq, g,
+                       stream);
+  };
+  auto tr = [&](const bf* src, int width, size_t off) {
+    return launch_transpose_pad(src, width, nullptr, width, nullptr, nullptr, T, Tq, Tq,
+                                reinterpret_cast<bf*>(bw + off), stream);
+  };
+  // output rows of dw_in (shared gate/value rows de-interleaved), and the one-group range
+  if ((rc = launch_rowmap(sw, L, rowmap_s, seg1, Tq, stream)) != LMOE_OK) return rc;
+  // 1. [dz | dhs] = dy . [W_up | W_sd]  (dz fp32 for the RMSNorm backward, dhs bf16)
+  if ((rc = dense(dyb, T, d, pb + R.PB.wout_t, L, d, d, EPI_F32, dz, L)) != LMOE_OK) return rc;
+  if (sw > 0 && (rc = dense(dyb, T, d, pb + R.PB.wout_t + static_cast<size_t>(L) * d * 2, sw, d,
+                            d, EPI_BF16, dhs, sw)) != LMOE_OK)
     return rc;
-  // 10. dW_ed[e] = do_e^T h_e   [L, I];  11. dW_gu[e] = dgv_e^T lat_e   [2I, L] (gate rows,
-  // then value rows)
-  {
-    GemmArgs g = gemm_defaults(err, D.c);
-    g.M = L;
-    g.N = I;
-    g.Kd = static_cast<int>(q);
-    g.epi = EPI_F32;
-    g.outf = dw_ed;
-    g.ldf = I;
-    g.groups = E;
-    g.kseg = kseg;
-    g.group_stride = static_cast<long long>(L) * I;
-    if ((rc = launch_gemm(bw + B.dout_t, static_cast<uint64_t>(L), static_cast<int>(q),
-                          bw + B.h_t, static_cast<uint64_t>(I), static_cast<int>(q), g,
-                          stream)) != LMOE_OK)
+  // 2. routed branch, first half: dout, dgate, dgamma
+  if ((rc = routed_bwd_front(R, dz, dgate, dgamma)) != LMOE_OK) return rc;
+  // 3. router: dlogit, then its latent gradient dlat_r = dlogit . W_r
+  if ((rc = launch_router_bwd(z, E, reinterpret_cast<const int32_t*>(ws + R.W.idx),
+                              reinterpret_cast<const float*>(ws + R.W.gate), dgate, T, D.K,
+                              dlogit, Ep, stream)) != LMOE_OK ||
+      (rc = dense(dlogit, T, Ep, pb + R.PB.wr_t, L, Ep, Ep, EPI_F32, dlat_r, L)) != LMOE_OK)
+    return rc;
+  // 4. routed branch, second half: dlat = routed + router parts, bf16 into dcat[:, :L];
+  // expert weight gradients
+  if ((rc = routed_bwd_back(R, dlat_r, reinterpret_cast<float*>(bw + LB.dlat), dcat, wc, dw_gu,
+                            dw_ed)) != LMOE_OK)
+    return rc;
+  // 5. shared experts: gate/value pre-activations again, SiTU backward into dcat[:, L:]
+  if (sw > 0) {
+    if ((rc = dense(xb, T, d, pk + R.P.w1 + static_cast<size_t>(L) * d * 2, 2 * sw, d, d,
+                    EPI_BF16, pre_s, 2 * sw)) != LMOE_OK ||
+        (rc = launch_situ_bwd(pre_s, dhs, T, sw, D.c, dcat + L, wc, stream)) != LMOE_OK)
       return rc;
   }
-  {
-    GemmArgs g = gemm_defaults(err, D.c);
-    g.M = 2 * I;
-    g.N = L;
-    g.Kd = static_cast<int>(q);
-    g.epi = EPI_F32;
-    g.outf = dw_gu;
-    g.ldf = L;
-    g.groups = E;
-    g.kseg = kseg;
-    g.group_stride = static_cast<long long>(2 * I) * L;
-    g.row_map = rowmap;
-    if ((rc = launch_gemm(bw + B.dgv_t, static_cast<uint64_t>(2 * I), static_cast<int>(q),
-                          bw + B.latp_t, static_cast<uint64_t>(L), static_cast<int>(q), g,
-                          stream)) != LMOE_OK)
-      return rc;
-  }
+  // 6. dx = [dlat | dgv_shared] . [W_down ; W_shared_gate/value]
+  if ((rc = dense(dcat, T, wc, pb + R.PB.wls_t, d, wc, wc, EPI_F32, dx, d)) != LMOE_OK) return rc;
+  // 7. dense weight gradients over the tokens: transposed, zero-padded copies, then
+  // dw_out = dy^T [z | hs], dw_router = dlogit^T lat, dw_in = [dlat | dgv_s]^T x
+  if ((rc = tr(dyb, d, LB.dy_t)) != LMOE_OK || (rc = tr(zh, wz, LB.zh_t)) != LMOE_OK ||
+      (rc = tr(dlogit, Ep, LB.dlogit_t)) != LMOE_OK || (rc = tr(lat, L, LB.lat_t)) != LMOE_OK ||
+      (rc = tr(dcat, wc, LB.dcat_t)) != LMOE_OK || (rc = tr(xb, d, LB.x_t)) != LMOE_OK)
+    return rc;
+  auto at = [&](size_t off) { return reinterpret_cast<const bf*>(bw + off); };
+  if ((rc = wgrad(at(LB.dy_t), d, at(LB.zh_t), wz, dw_out, nullptr)) != LMOE_OK ||
+      (rc = wgrad(at(LB.dlogit_t), E, at(LB.lat_t), L, dw_router, nullptr)) != LMOE_OK ||
+      (rc = wgrad(at(LB.dcat_t), wc, at(LB.x_t), d, dw_in, rowmap_s)) != LMOE_OK)
+    return rc;
   return LMOE_OK;
 }
 

@@ -199,7 +199,7 @@ colsum_final_kernel(const float* __restrict__ part, int L, float* __restrict__ d
 // group of GLU_GROUP features, GLU_GROUP gate then GLU_GROUP value pre-activations.
 __global__ void __launch_bounds__(256)
 situ_bwd_kernel(const __nv_bfloat16* __restrict__ pre, const __nv_bfloat16* __restrict__ dh,
-                int64_t rows, int I, float c, __nv_bfloat16* __restrict__ dgv) {
+                int64_t rows, int I, float c, __nv_bfloat16* __restrict__ dgv, int64_t ldo) {
   pdl_wait();
   pdl_launch_dependents();
   const int64_t n = rows * I;
@@ -217,21 +217,30 @@ situ_bwd_kernel(const __nv_bfloat16* __restrict__ pre, const __nv_bfloat16* __re
     const float s = 1.0f / (1.0f + expf(-G));
     const float dG = d * V * s * (1.0f + G * (1.0f - s));
     const float dV = d * G * s;
-    dgv[gi] = __float2bfloat16_rn(dG * (1.0f - tg * tg));
-    dgv[vi] = __float2bfloat16_rn(dV * (1.0f - tv * tv));
+    const size_t go = static_cast<size_t>(p) * ldo + grp * 2 * GLU_GROUP + w;
+    dgv[go] = __float2bfloat16_rn(dG * (1.0f - tg * tg));
+    dgv[go + GLU_GROUP] = __float2bfloat16_rn(dV * (1.0f - tv * tv));
   }
 }
 
-// dlat[t] = sum_j x[inv[t, j]] in slot order (fp32).
+// dlat[t] = add[t] + sum_j x[inv[t, j]] in slot order (fp32; add optional), and optionally
+// its bf16 copy into row t of outb (row stride ldb).
 __global__ void __launch_bounds__(BWD_THREADS)
 slot_sum_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ inv, int K,
-                int L, float* __restrict__ out) {
+                int L, const float* __restrict__ add, float* __restrict__ out,
+                __nv_bfloat16* __restrict__ outb, int64_t ldb) {
   pdl_wait();
   pdl_launch_dependents();
   const int t = blockIdx.x;
   const int nvec = L / 8;
   for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    if (add) {
+      const float4* a4 = reinterpret_cast<const float4*>(add + static_cast<size_t>(t) * L) + 2 * v;
+      const float4 a0 = __ldg(a4), a1 = __ldg(a4 + 1);
+      acc[0] = a0.x; acc[1] = a0.y; acc[2] = a0.z; acc[3] = a0.w;
+      acc[4] = a1.x; acc[5] = a1.y; acc[6] = a1.z; acc[7] = a1.w;
+    }
     for (int j = 0; j < K; ++j) {
       float f[8];
       const int row = __ldg(inv + static_cast<size_t>(t) * K + j);
@@ -242,6 +251,16 @@ slot_sum_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__
     float4* o = reinterpret_cast<float4*>(out + static_cast<size_t>(t) * L) + 2 * v;
     o[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
     o[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    if (outb) {
+      uint32_t pk[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const __nv_bfloat162 h2 = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
+        pk[i] = *reinterpret_cast<const uint32_t*>(&h2);
+      }
+      *reinterpret_cast<uint4*>(outb + static_cast<size_t>(t) * ldb + 8 * v) =
+          make_uint4(pk[0], pk[1], pk[2], pk[3]);
+    }
   }
 }
 
@@ -274,7 +293,8 @@ pad_scan_kernel(const int32_t* __restrict__ offsets, int E, int32_t* __restrict_
 
 // XT[w, q] for q < kseg[E]: column q of expert e's padded range is its token
 // p = offsets[e] + (q - kseg[e]) (row gather[p] of x, or row p), or zero past the expert's
-// tokens.  Every expert's range starts on a multiple of 64, so one 64 x 64 tile lies in one
+// tokens.  Without offsets the rows form one segment: XT[w, q] = x[q, w] for q < E (the row
+// count), zero up to the grid's last column.  Every expert's range starts on a multiple of 64, so one 64 x 64 tile lies in one
 // expert: one lookup per CTA, 16-byte row loads into shared memory, and 16-byte stores of
 // eight consecutive q of one output row (a warp reads 32 consecutive w of one tile row).
 constexpr int TP_TILE = 64;
@@ -291,9 +311,12 @@ transpose_pad_kernel(const __nv_bfloat16* __restrict__ x, int64_t ldx,
   pdl_launch_dependents();
   const int w0 = blockIdx.y * TP_TILE;
   const int64_t q0 = static_cast<int64_t>(blockIdx.x) * TP_TILE;
-  const int qtot = __ldg(kseg + E);
+  const int64_t qtot = offsets ? __ldg(kseg + E) : static_cast<int64_t>(gridDim.x) * TP_TILE;
   if (q0 >= qtot) return;
-  if (threadIdx.x < TP_TILE) {
+  if (threadIdx.x < TP_TILE && !offsets) {
+    const int64_t q = q0 + threadIdx.x;
+    row_src[threadIdx.x] = q < E ? (gather ? static_cast<int64_t>(__ldg(gather + q)) : q) : -1;
+  } else if (threadIdx.x < TP_TILE) {
     int lo = 0, hi = E;  // kseg[lo] <= q0 < kseg[hi]
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
@@ -332,18 +355,32 @@ transpose_pad_kernel(const __nv_bfloat16* __restrict__ x, int64_t ldx,
   }
 }
 
-// Output row of each packed gate/value row (interleaved in groups of GLU_GROUP): gate
-// feature f -> row f, value feature f -> row I + f.
-__global__ void rowmap_kernel(int I, int32_t* __restrict__ map) {
-  for (int k = blockIdx.x * blockDim.x + threadIdx.x; k < 2 * I; k += gridDim.x * blockDim.x) {
-    const int grp = k / (2 * GLU_GROUP), wi = k % (2 * GLU_GROUP);
+// Output row of each packed row: rows below `base` keep their place; the 2I gate/value rows
+// after them (interleaved in groups of GLU_GROUP) go to base + f (gate feature f) and
+// base + I + f (value feature f).  With `seg`, also writes the one-group range {0, seg_len}.
+__global__ void rowmap_kernel(int I, int base, int32_t* __restrict__ map,
+                              int32_t* __restrict__ seg, int seg_len) {
+  const int i0 = blockIdx.x * blockDim.x + threadIdx.x;
+  if (seg && i0 == 0) {
+    seg[0] = 0;
+    seg[1] = seg_len;
+  }
+  for (int k = i0; k < base + 2 * I; k += gridDim.x * blockDim.x) {
+    if (k < base) {
+      map[k] = k;
+      continue;
+    }
+    const int kk = k - base;
+    const int grp = kk / (2 * GLU_GROUP), wi = kk % (2 * GLU_GROUP);
     const int f = grp * GLU_GROUP + (wi % GLU_GROUP);
-    map[k] = wi < GLU_GROUP ? f : I + f;
+    map[k] = base + (wi < GLU_GROUP ? f : I + f);
   }
 }
 
-int launch_rowmap(int I, int32_t* map, cudaStream_t stream) {
-  rowmap_kernel<<<static_cast<unsigned>(ceil_div(2 * I, 256)), 256, 0, stream>>>(I, map);
+int launch_rowmap(int I, int base, int32_t* map, int32_t* seg, int seg_len, cudaStream_t stream) {
+  const int n = base + 2 * I > 1 ? base + 2 * I : 1;
+  rowmap_kernel<<<static_cast<unsigned>(ceil_div(n, 256)), 256, 0, stream>>>(I, base, map, seg,
+                                                                              seg_len);
   return cudaGetLastError() == cudaSuccess ? LMOE_OK : LMOE_ERR_CUDA;
 }
 
@@ -373,19 +410,23 @@ int launch_dgamma(const float* dz, const float* u, const float* r, int T, int L,
 }
 
 int launch_situ_bwd(const __nv_bfloat16* pre, const __nv_bfloat16* dh, int64_t rows, int I,
-                    float c, __nv_bfloat16* dgv, cudaStream_t stream) {
+                    float c, __nv_bfloat16* dgv, int64_t ldo, cudaStream_t stream) {
   if (rows == 0) return LMOE_OK;
   const int64_t n = rows * I;
   const unsigned grid = static_cast<unsigned>(ceil_div(n, 256) < 65535 * 16 ? ceil_div(n, 256) : 65535 * 16);
-  return launch_pdl(situ_bwd_kernel, grid, 256, 0, stream, pre, dh, rows, I, c, dgv) == cudaSuccess
+  return launch_pdl(situ_bwd_kernel, grid, 256, 0, stream, pre, dh, rows, I, c, dgv, ldo) ==
+                 cudaSuccess
              ? LMOE_OK
              : LMOE_ERR_CUDA;
 }
 
-int launch_slot_sum(const __nv_bfloat16* x, const int32_t* inv, int T, int K, int L, float* out,
+int launch_slot_sum(const __nv_bfloat16* x, const int32_t* inv, int T, int K, int L,
+                    const float* add, float* out, __nv_bfloat16* outb, int64_t ldb,
                     cudaStream_t stream) {
   if (T == 0) return LMOE_OK;
-  return launch_pdl(slot_sum_kernel, T, BWD_THREADS, 0, stream, x, inv, K, L, out) == cudaSuccess
+  if (outb && (ldb % 8 || (reinterpret_cast<uintptr_t>(outb) & 15))) return LMOE_ERR_UNSUPPORTED;
+  return launch_pdl(slot_sum_kernel, T, BWD_THREADS, 0, stream, x, inv, K, L, add, out, outb,
+                    ldb) == cudaSuccess
              ? LMOE_OK
              : LMOE_ERR_CUDA;
 }
@@ -400,6 +441,7 @@ int launch_transpose_pad(const __nv_bfloat16* x, int64_t ldx, const int32_t* gat
                          const int32_t* offsets, const int32_t* kseg, int E, int64_t qmax,
                          int64_t ldt, __nv_bfloat16* xt, cudaStream_t stream) {
   // 16-byte rows and stores; padded ranges are whole tiles
+  if (!offsets && qmax < E) return LMOE_ERR_INVALID_ARG;  // one segment of E rows
   if (W % 8 || ldx % 8 || ldt % 8 || qmax % TP_TILE || (reinterpret_cast<uintptr_t>(x) & 15) ||
       (reinterpret_cast<uintptr_t>(xt) & 15))
     return LMOE_ERR_UNSUPPORTED;

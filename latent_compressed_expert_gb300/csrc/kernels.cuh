@@ -152,11 +152,16 @@ int launch_combine_bwd(const __nv_bfloat16* o, const float* gate, const int32_t*
 int launch_dgamma(const float* dz, const float* u, const float* r, int T, int L, float* part,
                   float* dgamma, cudaStream_t stream);
 int launch_situ_bwd(const __nv_bfloat16* pre, const __nv_bfloat16* dh, int64_t rows, int I,
-                    float c, __nv_bfloat16* dgv, cudaStream_t stream);
-int launch_slot_sum(const __nv_bfloat16* x, const int32_t* inv, int T, int K, int L, float* out,
+                    float c, __nv_bfloat16* dgv, int64_t ldo, cudaStream_t stream);
+int launch_slot_sum(const __nv_bfloat16* x, const int32_t* inv, int T, int K, int L,
+                    const float* add, float* out, __nv_bfloat16* outb, int64_t ldb,
                     cudaStream_t stream);
 int launch_pad_scan(const int32_t* offsets, int E, int32_t* kseg, cudaStream_t stream);
-int launch_rowmap(int I, int32_t* map, cudaStream_t stream);
+int launch_rowmap(int I, int base, int32_t* map, int32_t* seg, int seg_len, cudaStream_t stream);
+// Router backward: dz [T, ldo] bf16 from the logits z [T, ldz], routing and dgate.
+int launch_router_bwd(const float* z, int64_t ldz, const int32_t* idx, const float* gate,
+                      const float* dgate, int T, int K, __nv_bfloat16* dz, int ldo,
+                      cudaStream_t stream);
 int launch_transpose_pad(const __nv_bfloat16* x, int64_t ldx, const int32_t* gather, int W,
                          const int32_t* offsets, const int32_t* kseg, int E, int64_t qmax,
                          int64_t ldt, __nv_bfloat16* xt, cudaStream_t stream);

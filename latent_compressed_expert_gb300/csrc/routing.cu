@@ -452,6 +452,53 @@ int launch_candidates(const float* z, int T, int E, int64_t stride_t, int64_t st
              : LMOE_ERR_CUDA;
 }
 
+// Router backward.  Token t selected experts e_j with scores s_j = sigmoid(z[t, e_j]) and
+// gates g_j = s_j / S, S the sum of the selected scores.  Given dg_j:
+//   ds_j = (dg_j - sum_i g_i dg_i) / S,   dz[t, e_j] = ds_j s_j (1 - s_j),
+// and dz[t, e] = 0 for the experts not selected.  One warp per token; the bf16 output row
+// has ldo >= E columns, the ones past E zero.
+__global__ void __launch_bounds__(256)
+router_bwd_kernel(const float* __restrict__ z, int64_t ldz, const int32_t* __restrict__ idx,
+                  const float* __restrict__ gate, const float* __restrict__ dgate, int T, int K,
+                  __nv_bfloat16* __restrict__ dz, int ldo) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (t >= T) return;
+  __nv_bfloat16* row = dz + static_cast<size_t>(t) * ldo;
+  for (int v = lane; v < ldo / 8; v += 32)
+    reinterpret_cast<uint4*>(row)[v] = make_uint4(0u, 0u, 0u, 0u);
+  float s = 0.0f, g = 0.0f, dg = 0.0f;
+  int e = 0;
+  if (lane < K) {
+    const size_t j = static_cast<size_t>(t) * K + lane;
+    e = __ldg(idx + j);
+    s = score_sigmoid(__ldg(z + static_cast<size_t>(t) * ldz + e));
+    g = __ldg(gate + j);
+    dg = __ldg(dgate + j);
+  }
+  float S = s, dot = g * dg;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    S += __shfl_xor_sync(0xffffffffu, S, o);
+    dot += __shfl_xor_sync(0xffffffffu, dot, o);
+  }
+  __syncwarp();  // the zero fill above lands before the scattered entries
+  if (lane < K) row[e] = __float2bfloat16_rn((dg - dot) / S * s * (1.0f - s));
+}
+
+int launch_router_bwd(const float* z, int64_t ldz, const int32_t* idx, const float* gate,
+                      const float* dgate, int T, int K, __nv_bfloat16* dz, int ldo,
+                      cudaStream_t stream) {
+  if (T == 0) return LMOE_OK;
+  if (K > 32 || ldo % 8 || (reinterpret_cast<uintptr_t>(dz) & 15)) return LMOE_ERR_UNSUPPORTED;
+  return launch_pdl(router_bwd_kernel, static_cast<unsigned>(ceil_div(T, 8)), 256, 0, stream, z,
+                    ldz, idx, gate, dgate, T, K, dz, ldo) == cudaSuccess
+             ? LMOE_OK
+             : LMOE_ERR_CUDA;
+}
+
 int launch_transpose_f32(const float* in, int T, int E, float* out, cudaStream_t stream) {
   if (T == 0) return LMOE_OK;
   const dim3 grid(static_cast<unsigned>(ceil_div(E, 32)), static_cast<unsigned>(ceil_div(T, 32)));

@@ -66,8 +66,11 @@ SIGNATURES = {
     "lmoe_quantize_e4m3": (_i, [_vp, ctypes.c_longlong, _i, _vp, _vp, _vp]),
     "lmoe_tau_ema": (_i, [_vp, _vp, _i, _f, _i, _vp]),
     "lmoe_packed_backward_bytes": (_sz, [ctypes.POINTER(Dims)]),
-    "lmoe_pack_backward_weights": (_i, [ctypes.POINTER(Dims), ctypes.POINTER(Weights), _vp, _sz,
-                                        _vp]),
+    "lmoe_pack_backward_weights": (_i, [ctypes.POINTER(Dims), ctypes.POINTER(Weights), _vp, _vp,
+                                        _sz, _vp]),
+    "lmoe_backward_workspace_bytes": (_sz, [ctypes.POINTER(Dims)]),
+    "lmoe_backward": (_i, [ctypes.POINTER(Dims), _vp, _vp, _vp, _sz, _vp, _vp, _vp, _vp, _vp,
+                           _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "lmoe_routed_backward_workspace_bytes": (_sz, [ctypes.POINTER(Dims)]),
     "lmoe_routed_backward": (_i, [ctypes.POINTER(Dims), _vp, _vp, _vp, _sz, _vp, _vp, _vp, _vp,
                                   _vp, _vp, _vp, _sz, _vp]),
@@ -512,7 +515,8 @@ class Layer:
         return last_device_error(self.workspace)
 
     def enable_backward(self, weights: dict, stream=None):
-        """Pack the transposed expert weights and allocate the scratch of ``backward``."""
+        """Pack the transposed weights and allocate the scratch of ``backward`` and
+        ``backward_layer``."""
         D = self.dims
         nb = int(load().lmoe_packed_backward_bytes(ctypes.byref(D)))
         if nb == 0:
@@ -520,15 +524,16 @@ class Layer:
         self.packed_bwd = torch.empty(nb, dtype=torch.uint8, device=self.device)
         W = Weights(*[_ptr(weights.get(n)) for n, _ in Weights._fields_])
         _check(load().lmoe_pack_backward_weights(ctypes.byref(D), ctypes.byref(W),
-                                                 _ptr(self.packed_bwd), nb, _stream(stream)),
+                                                 _ptr(self.packed), _ptr(self.packed_bwd), nb,
+                                                 _stream(stream)),
                "lmoe_pack_backward_weights")
-        self.bwd_bytes = int(load().lmoe_routed_backward_workspace_bytes(ctypes.byref(D)))
+        self.bwd_bytes = int(load().lmoe_backward_workspace_bytes(ctypes.byref(D)))
         self.bwd_ws = torch.empty(self.bwd_bytes, dtype=torch.uint8, device=self.device)
 
     # kernels one lmoe_routed_backward call launches: combine backward, two dgamma passes,
     # three grouped GEMMs, SiTU backward, slot sum, pad scan, row map, four transposes and
     # two grouped-K weight-gradient GEMMs
-    BACKWARD_LAUNCHES = 15
+    BACKWARD_LAUNCHES = 16
 
     def backward(self, dz: torch.Tensor, stream=None) -> dict:
         """Gradients of the routed branch for the batch of the last ``forward`` call
@@ -553,6 +558,56 @@ class Layer:
             _stream(stream)), "lmoe_routed_backward")
         out["dw_gate"] = out["dw_gu"][:, :sh.I]
         out["dw_value"] = out["dw_gu"][:, sh.I:]
+        return out
+
+    def layer_backward_launches(self) -> int:
+        """Kernels one lmoe_backward call launches: the routed branch's, plus the row map of
+        dw_in, the dz GEMM (and the dhs GEMM), router backward and its GEMM, (the shared
+        experts' GEMM and SiTU backward), the dx GEMM, six transposes and three
+        weight-gradient GEMMs; the parenthesised ones only with shared experts."""
+        shared = 3 if self.shape.S > 0 else 0
+        return self.BACKWARD_LAUNCHES + 1 + 1 + 2 + 1 + 6 + 3 + shared
+
+    def backward_layer(self, x: torch.Tensor, dy: torch.Tensor, logits=None,
+                       stream=None) -> dict:
+        """Gradients of the whole layer for the batch of the last ``forward`` call
+        (lmoe_backward): x [T, d] bf16 (that call's input), dy [T, d] bf16 ->
+        dx (through the latent and the shared experts; the residual adds dy), dgamma and
+        every weight's gradient, fp32, in the weights' own shapes (dw_up, dw_sdown and the
+        shared gate/value gradients are views into the packed gradient buffers).  logits:
+        the fp32 [T, E] logits the forward routed on, when it was given ``logits_in``."""
+        sh = self.shape
+        T = x.shape[0]
+        _expect(x, torch.bfloat16, (T, sh.d), "x")
+        _expect(dy, torch.bfloat16, (T, sh.d), "dy")
+        if logits is not None:
+            _expect(logits, torch.float32, (T, sh.E), "logits")
+        dims = dims_of(sh, T=T, expert_fp8=self.expert_fp8)
+        dev = x.device
+        f = torch.float32
+        S, Is, L, d = sh.S, sh.Is, sh.L, sh.d
+        sw = S * Is
+        out = {"dx": torch.empty((T, d), dtype=f, device=dev),
+               "dgamma": torch.empty(L, dtype=f, device=dev),
+               "dw_in": torch.empty((L + 2 * sw, d), dtype=f, device=dev),
+               "dw_router": torch.empty((sh.E, L), dtype=f, device=dev),
+               "dw_gu": torch.empty((sh.E, 2 * sh.I, L), dtype=f, device=dev),
+               "dw_edown": torch.empty((sh.E, L, sh.I), dtype=f, device=dev),
+               "dw_out": torch.empty((d, L + sw), dtype=f, device=dev)}
+        bwd_bytes = int(load().lmoe_backward_workspace_bytes(ctypes.byref(dims)))
+        _check(load().lmoe_backward(
+            ctypes.byref(dims), _ptr(self.packed), _ptr(self.packed_bwd), _ptr(self.workspace),
+            self.ws_bytes, _ptr(x), _ptr(logits), _ptr(dy), _ptr(out["dx"]),
+            _ptr(out["dgamma"]), _ptr(out["dw_in"]), _ptr(out["dw_router"]), _ptr(out["dw_gu"]),
+            _ptr(out["dw_edown"]), _ptr(out["dw_out"]), _ptr(self.bwd_ws), bwd_bytes,
+            _stream(stream)), "lmoe_backward")
+        out["dw_down"] = out["dw_in"][:L]
+        out["dw_sgate"] = out["dw_in"][L:L + sw].view(S, Is, d)
+        out["dw_svalue"] = out["dw_in"][L + sw:].view(S, Is, d)
+        out["dw_gate"] = out["dw_gu"][:, :sh.I]
+        out["dw_value"] = out["dw_gu"][:, sh.I:]
+        out["dw_up"] = out["dw_out"][:, :L]
+        out["dw_sdown"] = out["dw_out"][:, L:].unflatten(1, (S, Is)).permute(1, 0, 2)
         return out
 
 

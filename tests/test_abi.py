@@ -194,3 +194,48 @@ def test_phase_and_candidate_argument_checks(lib):
     assert lib.lmoe_load_stats_update(None, 8, fake, None) == lmoe.LMOE_ERR_INVALID_ARG
     assert fwd(fake, ctypes.c_void_p(0x2000), tau_ema=0x6000, ema_beta=2.0) \
         == lmoe.LMOE_ERR_INVALID_ARG
+
+
+def test_backward_size_queries(lib):
+    sh = synth.PREFILL
+    d = lmoe.dims_of(sh)
+    routed = lib.lmoe_routed_backward_workspace_bytes(ctypes.byref(d))
+    layer = lib.lmoe_backward_workspace_bytes(ctypes.byref(d))
+    # the layer's scratch extends the routed branch's by its dense buffers
+    sw = sh.S * sh.Is
+    dense_t = 2 * sh.T * (2 * sh.d + 3 * sh.L + 3 * sw + sh.E)   # six transposed copies
+    assert routed + dense_t < layer < routed + 3 * dense_t
+    # the transposed pack holds every routed and dense weight once (bf16)
+    pb = lib.lmoe_packed_backward_bytes(ctypes.byref(d))
+    weights = 2 * (3 * sh.E * sh.I * sh.L + (sh.L + sw) * sh.d + sh.L * sh.E
+                   + sh.d * (sh.L + 2 * sw))
+    assert weights <= pb <= weights + 8 * 1024 * 1024
+    d8 = lmoe.dims_of(sh, expert_fp8=True)
+    assert lib.lmoe_backward_workspace_bytes(ctypes.byref(d8)) == 0
+
+
+@no_gpu
+def test_backward_argument_checks(lib):
+    d = lmoe.dims_of(synth.TINY)
+    fake = ctypes.c_void_p(0x1000)
+    ws = lmoe.workspace_bytes(d)
+    bw = lib.lmoe_backward_workspace_bytes(ctypes.byref(d))
+    f = lib.lmoe_backward
+
+    def call(dims=d, x=fake, dy=fake, ws_bytes=ws, bw_bytes=bw, dx=fake):
+        return f(ctypes.byref(dims), fake, fake, fake, ws_bytes, x, None, dy, dx, fake, fake,
+                 fake, fake, fake, fake, fake, bw_bytes, None)
+
+    assert call(x=None) == lmoe.LMOE_ERR_INVALID_ARG
+    assert call(dy=None) == lmoe.LMOE_ERR_INVALID_ARG
+    assert call(dx=ctypes.c_void_p(0x1004)) == lmoe.LMOE_ERR_INVALID_ARG   # misaligned
+    assert call(bw_bytes=bw - 1) == lmoe.LMOE_ERR_WORKSPACE_TOO_SMALL
+    assert call(ws_bytes=ws - 1) == lmoe.LMOE_ERR_WORKSPACE_TOO_SMALL
+    assert call(dims=lmoe.dims_of(synth.TINY, T=0), ws_bytes=1 << 30, bw_bytes=1 << 30) \
+        == lmoe.LMOE_OK
+    d8 = lmoe.dims_of(synth.PREFILL, expert_fp8=True)
+    assert call(dims=d8) == lmoe.LMOE_ERR_UNSUPPORTED
+    # the transposed pack needs the forward's packed buffer
+    W = lmoe.Weights()
+    assert lib.lmoe_pack_backward_weights(ctypes.byref(d), ctypes.byref(W), None, fake, 1 << 30,
+                                          None) == lmoe.LMOE_ERR_INVALID_ARG

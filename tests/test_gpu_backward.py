@@ -79,3 +79,38 @@ def test_routed_backward_matches_oracle(dev, oracle_mod, shape):
     unused = np.setdiff1d(np.arange(sh.E), np.unique(idx))
     if len(unused):
         assert float(g["dw_edown"][torch.as_tensor(unused)].abs().max()) == 0.0
+
+
+LAYER_KEYS = ("dx", "dgamma", "dw_down", "dw_router", "dw_gate", "dw_value", "dw_edown", "dw_up",
+              "dw_sgate", "dw_svalue", "dw_sdown")
+
+
+@pytest.mark.parametrize("shape", [
+    synth.LayerShape("b1", T=256, d=512, L=256, E=32, K=4, I=128, S=2, Is=128),
+    synth.LayerShape("b2", T=300, d=512, L=384, E=16, K=6, I=192, S=0, Is=0),  # ragged tiles
+])
+def test_layer_backward_matches_oracle(dev, oracle_mod, shape):
+    """lmoe_backward against the oracle's whole-layer backward.  The GPU routes on the
+    oracle's own fp32 logits (logits_in), so the selection is shared and the gates are those
+    of lat W_r^T on both sides."""
+    import oracle.backward as B
+    sh = shape
+    w = synth.make_weights(sh, seed=91)
+    w["gamma"] = torch.linspace(0.6, 1.4, sh.L)
+    wd = {k: v.to(dev) for k, v in w.items()}
+    layer = lmoe.Layer(sh, wd)
+    layer.enable_backward(wd)
+    x = synth.make_x(sh, seed=92)
+    r = oracle_mod.forward(w, x, sh.K, residual=None)
+    logits = torch.as_tensor(r.logits).to(dev)
+    xd = x.to(dev)
+    _, dbg = layer.forward(xd, residual=xd, logits_in=logits, debug=True)
+    assert np.array_equal(dbg["idx"].cpu().numpy(), r.idx)
+    dy = torch.randn(sh.T, sh.d, generator=torch.Generator().manual_seed(93)).to(torch.bfloat16)
+    g = layer.backward_layer(xd, dy.to(dev), logits=logits)
+    torch.cuda.synchronize()
+    assert layer.device_error() == 0
+    ref = B.layer_backward(x, r.idx, w, dy.double().numpy())
+    keys = [k for k in LAYER_KEYS if ref[k].size > 0]
+    stats = {k: _stats(g[k].cpu().numpy(), ref[k]) for k in keys}
+    assert all(_ok(v) for v in stats.values()), (sh.name, stats)
