@@ -564,13 +564,11 @@ def run_backward(args):
     if whole:
         grad = torch.randn(sh.T, sh.d, generator=gen, device=dev).to(torch.bfloat16)
         step_bwd = lambda: layer.backward_layer(x, grad)  # noqa: E731
-        bwd_launches = layer.layer_backward_launches()
     else:
         grad = torch.randn(sh.T, sh.L, generator=gen, device=dev)
         step_bwd = lambda: layer.backward(grad)  # noqa: E731
-        bwd_launches = layer.BACKWARD_LAUNCHES
     for _ in range(args.warmup):
-        wl.forward(y=y)
+        wl.forward(y=y, train=True)
         step_bwd()
     torch.cuda.synchronize()
     if layer.device_error() != 0:
@@ -581,19 +579,22 @@ def run_backward(args):
     with ClockSampler(local) as clk:
         for i in range(args.steps):
             ev[i][0].record()
-            wl.forward(y=y)
+            wl.forward(y=y, train=True)  # a training step keeps the routed pre-activations
             ev[i][1].record()
             step_bwd()
             ev[i][2].record()
         torch.cuda.synchronize()
     barrier(world)
     fwd_launches = layer.last_kernel_launches
+    bwd_launches = (layer.layer_backward_launches(sh.T) if whole
+                    else layer.backward_launches(sh.T))
     fwd = max_over_ranks(float(np.mean([e[0].elapsed_time(e[1]) for e in ev])), world)
     bwd = max_over_ranks(float(np.mean([e[1].elapsed_time(e[2]) for e in ev])), world)
     T, TK, L, I, E, d = sh.T, sh.T * sh.K, sh.L, sh.I, sh.E, sh.d
     sw = sh.S * sh.Is
-    # routed: dgrad x2, recomputed gate/value, wgrad x2 (2 flop per multiply-add each)
-    flop = 16.0 * TK * L * I
+    # routed: dgrad x2, wgrad x2 (2 flop per multiply-add each; the forward keeps the
+    # gate/value pre-activations, so none are recomputed)
+    flop = 12.0 * TK * L * I
     grad_bytes = 4.0 * E * 3 * I * L
     if whole:
         # dz/dhs, dx, router dgrad, shared recompute; dW_out, dW_in, dW_router
@@ -610,7 +611,8 @@ def run_backward(args):
                     + ("dy" if whole else "dz") + " ~ N(0,1))",
             "config": {"workload": wl.config(world)["workload"],
                        "backward": "whole layer: dx and every weight's gradient (fp32)" if whole
-                       else "routed branch: dlat, dgate, dgamma, dW_g, dW_v, dW_ed (fp32)"},
+                       else "routed branch: dlat, dgate, dgamma, dW_g, dW_v, dW_ed (fp32)",
+                       "forward": "training step (keeps the routed pre-activations)"},
             "forward_ms": fwd, "backward_ms": bwd,
             "backward_tflops": flop / (bwd / 1e3) / 1e12,
             "weight_gradient_bytes": grad_bytes,

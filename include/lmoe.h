@@ -146,6 +146,10 @@ typedef struct lmoe_io {
   int ema_first;         /* 1: this step initialises tau_ema to the batch's thresholds */
   unsigned long long *load_stats; /* counters updated with this step's per-expert token
                             counts, as lmoe_load_stats_update does, or NULL */
+  void *save_pre;        /* [T*K, 2I] bf16, or NULL: a training step also stores the routed
+                            experts' gate/value pre-activations here (slot order; per slot,
+                            groups of 16 gate then 16 value features), so that the backward
+                            need not recompute them.  bf16 routed experts only. */
 } lmoe_io;
 
 /* lmoe_io.phase.  The layer splits where its only cross-batch quantity, the thresholds, is
@@ -313,7 +317,9 @@ int lmoe_gemm_bf16(const void *A, const void *B, float *C, int M, int N, int Kd,
  *     (lmoe_packed_backward_bytes): the expert weights in tiles, from the same unpacked
  *     weights w as the forward's packing, and the dense weights, from `packed` (the
  *     forward's packed buffer, filled by lmoe_pack_weights with the same dims).
- *   lmoe_routed_backward: dz [T, L] fp32 in; dlat [T, L], dgate [T, K], dgamma [L],
+ *   lmoe_routed_backward: dz [T, L] fp32 in; pre: the forward's lmoe_io.save_pre buffer,
+ *     or NULL (the pre-activations are then recomputed from the latent and W_g, W_v);
+ *     dlat [T, L], dgate [T, K], dgamma [L],
  *     dw_gu [E, 2I, L] (rows 0..I-1: W_g, rows I..2I-1: W_v) and dw_ed [E, L, I], all fp32,
  *     out; bwd_ws: lmoe_routed_backward_workspace_bytes of device scratch.
  * Errors: INVALID_ARG, UNSUPPORTED (expert_fp8), WORKSPACE_TOO_SMALL, CUDA. */
@@ -322,7 +328,8 @@ int lmoe_pack_backward_weights(const lmoe_dims *dims, const lmoe_weights *w, con
                                void *packed_bwd, size_t bytes, void *stream);
 size_t lmoe_routed_backward_workspace_bytes(const lmoe_dims *dims);
 int lmoe_routed_backward(const lmoe_dims *dims, const void *packed, const void *packed_bwd,
-                         void *workspace, size_t ws_bytes, const float *dz, float *dlat,
+                         void *workspace, size_t ws_bytes, const float *dz, const void *pre,
+                         float *dlat,
                          float *dgate, float *dgamma, float *dw_gu, float *dw_ed, void *bwd_ws,
                          size_t bwd_ws_bytes, void *stream);
 
@@ -341,14 +348,15 @@ int lmoe_routed_backward(const lmoe_dims *dims, const void *packed, const void *
  * to their scores s = sigmoid(logit), and from there to the latent and W_r; the selection
  * (thresholds and top-K) is held fixed.  logits: the fp32 [T, E] router logits the forward
  * routed on -- required when the forward was given lmoe_io.logits_in, else NULL (the ones
- * it computed into the workspace).  x: the forward's input [T, d] bf16.
+ * it computed into the workspace).  x: the forward's input [T, d] bf16.  pre: as for
+ * lmoe_routed_backward.
  * bwd_ws: lmoe_backward_workspace_bytes of device scratch.  bf16 routed experts only.
  * Errors: INVALID_ARG (null or misaligned pointers), UNSUPPORTED (expert_fp8),
  * WORKSPACE_TOO_SMALL, CUDA. */
 size_t lmoe_backward_workspace_bytes(const lmoe_dims *dims);
 int lmoe_backward(const lmoe_dims *dims, const void *packed, const void *packed_bwd,
                   void *workspace, size_t ws_bytes, const void *x, const float *logits,
-                  const void *dy, float *dx, float *dgamma, float *dw_in, float *dw_router,
+                  const void *dy, const void *pre, float *dx, float *dgamma, float *dw_in, float *dw_router,
                   float *dw_gu, float *dw_ed, float *dw_out, void *bwd_ws, size_t bwd_ws_bytes,
                   void *stream);
 

@@ -158,8 +158,7 @@ static BwdPacked bwd_packed_layout(const lmoe_dims& D) {
 }
 
 struct BwdLayout {
-  size_t u, r, dout, dh, pre, dgv, dlatp, kseg, part, rowmap, dout_t, h_t, dgv_t, latp_t, total;
-  int64_t qmax;  // columns of the padded, transposed operands of the weight gradients
+  size_t u, r, dout, dh, pre, dgv, dlatp, part, rowmap, latp, total;
 };
 static BwdLayout bwd_layout(const lmoe_dims& D) {
   BwdLayout B{};
@@ -170,8 +169,6 @@ static BwdLayout bwd_layout(const lmoe_dims& D) {
     return o;
   };
   const size_t T = static_cast<size_t>(D.T), TK = T * D.K, L = D.L, I = D.I;
-  B.qmax = static_cast<int64_t>(ceil_div(static_cast<int64_t>(TK) + 64 * D.E, 64) * 64);
-  const size_t q = static_cast<size_t>(B.qmax);
   B.u = take(T * L * 4);
   B.r = take(T * 4);
   B.dout = take(TK * L * 2);
@@ -179,22 +176,17 @@ static BwdLayout bwd_layout(const lmoe_dims& D) {
   B.pre = take(TK * 2 * I * 2);
   B.dgv = take(TK * 2 * I * 2);
   B.dlatp = take(TK * L * 2);
-  B.kseg = take((static_cast<size_t>(D.E) + 1) * 4);
   B.part = take(64 * L * 4);
   B.rowmap = take(2 * I * 4);
-  B.dout_t = take(L * q * 2);
-  B.h_t = take(I * q * 2);
-  B.dgv_t = take(2 * I * q * 2);
-  B.latp_t = take(L * q * 2);
+  B.latp = take(TK * L * 2);
   B.total = off;
   return B;
 }
 
 // The whole layer's backward adds these buffers after the routed branch's.
 struct LayerBwdLayout {
-  size_t dz, dhs, dgate, dlogit, dlat_r, dlat, dcat, pre_s, seg1, rowmap_s, dy_t, zh_t, dlogit_t,
-      lat_t, dcat_t, x_t, total;
-  int Tq, Ep, sw, wc, wz;  // T and E padded to 64; shared width; widths of dcat and zh
+  size_t dz, dhs, dgate, dlogit, dlat_r, dlat, dcat, pre_s, seg1, rowmap_s, total;
+  int Ep, sw, wc, wz;  // E padded to 64; shared width; widths of dcat and zh
 };
 static LayerBwdLayout layer_bwd_layout(const lmoe_dims& D) {
   LayerBwdLayout B{};
@@ -204,12 +196,11 @@ static LayerBwdLayout layer_bwd_layout(const lmoe_dims& D) {
     off += align_up(bytes > 0 ? bytes : 1, 256);
     return o;
   };
-  B.Tq = pad64(D.T);
   B.Ep = pad64(D.E);
   B.sw = D.S > 0 ? D.S * D.Is : 0;
   B.wc = D.L + 2 * B.sw;
   B.wz = D.L + B.sw;
-  const size_t T = static_cast<size_t>(D.T), Tq = static_cast<size_t>(B.Tq), L = D.L;
+  const size_t T = static_cast<size_t>(D.T), L = D.L;
   B.dz = take(T * L * 4);
   B.dhs = take(T * B.sw * 2);
   B.dgate = take(T * D.K * 4);
@@ -220,12 +211,6 @@ static LayerBwdLayout layer_bwd_layout(const lmoe_dims& D) {
   B.pre_s = take(T * 2 * B.sw * 2);
   B.seg1 = take(2 * 4);
   B.rowmap_s = take(static_cast<size_t>(B.wc) * 4);
-  B.dy_t = take(static_cast<size_t>(D.d) * Tq * 2);
-  B.zh_t = take(static_cast<size_t>(B.wz) * Tq * 2);
-  B.dlogit_t = take(static_cast<size_t>(B.Ep) * Tq * 2);
-  B.lat_t = take(L * Tq * 2);
-  B.dcat_t = take(static_cast<size_t>(B.wc) * Tq * 2);
-  B.x_t = take(static_cast<size_t>(D.d) * Tq * 2);
   B.total = off;
   return B;
 }
@@ -243,6 +228,7 @@ struct RoutedBwd {
   WorkspaceLayout W;
   BwdLayout B;
   cudaStream_t stream;
+  const __nv_bfloat16* pre;  // the forward's saved pre-activations, or null: recompute
 };
 
 // 1-2. RMSNorm and combine backward (du, do_j, dgate_j), then dgamma.
@@ -295,9 +281,7 @@ static int routed_bwd_back(const RoutedBwd& R, const float* dlat_add, float* dla
   bf* pre = reinterpret_cast<bf*>(bw + B.pre);
   bf* dgv = reinterpret_cast<bf*>(bw + B.dgv);
   bf* dlatp = reinterpret_cast<bf*>(bw + B.dlatp);
-  int32_t* kseg = reinterpret_cast<int32_t*>(bw + B.kseg);
   int32_t* rowmap = reinterpret_cast<int32_t*>(bw + B.rowmap);
-  const int64_t q = B.qmax;
   int rc;
   auto grouped = [&](int M_w, int Kd, const int32_t* gather, const bf* x, int ldx, int epi,
                      bf* out, int ldo) {
@@ -326,14 +310,17 @@ static int routed_bwd_back(const RoutedBwd& R, const float* dlat_add, float* dla
         LMOE_OK)
       return rc;
   }
-  // 4. gate/value pre-activations again (interleaved rows), 5. through SiTU
-  {
+  // 4. gate/value pre-activations (interleaved rows): the forward's, or computed again;
+  // 5. through SiTU
+  const bf* pre_in = R.pre;
+  if (!pre_in) {
     GroupedArgs g = grouped(2 * I, L, src_tok, lat, L, EPI_BF16, pre, 2 * I);
     if ((rc = launch_grouped_gemm(pk + P.wgu, lat, static_cast<uint64_t>(T), L, g, stream)) !=
         LMOE_OK)
       return rc;
+    pre_in = pre;
   }
-  if ((rc = launch_situ_bwd(pre, dh, TK, I, D.c, dgv, 2 * I, stream)) != LMOE_OK) return rc;
+  if ((rc = launch_situ_bwd(pre_in, dh, TK, I, D.c, dgv, 2 * I, stream)) != LMOE_OK) return rc;
   // 6. dlat_p = dgv . W_gu (per expert, weights transposed), 7. summed over the slots
   {
     GroupedArgs g = grouped(L, 2 * I, nullptr, nullptr, 0, EPI_BF16, dlatp, L);
@@ -342,34 +329,25 @@ static int routed_bwd_back(const RoutedBwd& R, const float* dlat_add, float* dla
       return rc;
   }
   if ((rc = launch_slot_sum(dlatp, inv, T, K, L, dlat_add, dlat, dlat_b, ldb, stream)) != LMOE_OK) return rc;
-  // 8-9. weight gradients reduce over each expert's tokens: token-contiguous copies, each
-  // expert's range padded to 64 with zeros
-  if ((rc = launch_pad_scan(offsets, E, kseg, stream)) != LMOE_OK ||
-      (rc = launch_rowmap(I, 0, rowmap, nullptr, 0, stream)) != LMOE_OK ||
-      (rc = launch_transpose_pad(dout, L, nullptr, L, offsets, kseg, E, q, q,
-                                 reinterpret_cast<bf*>(bw + B.dout_t), stream)) != LMOE_OK ||
-      (rc = launch_transpose_pad(h, I, nullptr, I, offsets, kseg, E, q, q,
-                                 reinterpret_cast<bf*>(bw + B.h_t), stream)) != LMOE_OK ||
-      (rc = launch_transpose_pad(dgv, 2 * I, nullptr, 2 * I, offsets, kseg, E, q, q,
-                                 reinterpret_cast<bf*>(bw + B.dgv_t), stream)) != LMOE_OK ||
-      (rc = launch_transpose_pad(lat, L, src_tok, L, offsets, kseg, E, q, q,
-                                 reinterpret_cast<bf*>(bw + B.latp_t), stream)) != LMOE_OK)
+  // 8. the latent rows in slot order (the weight gradient's B operand); output rows of the
+  // packed gate/value rows
+  bf* latp = reinterpret_cast<bf*>(bw + B.latp);
+  if ((rc = launch_gather_rows(lat, L, src_tok, TK, L, latp, L, stream)) != LMOE_OK ||
+      (rc = launch_rowmap(I, 0, rowmap, nullptr, 0, stream)) != LMOE_OK)
     return rc;
-  // 10. dW_ed[e] = do_e^T h_e   [L, I];  11. dW_gu[e] = dgv_e^T lat_e   [2I, L] (gate rows,
-  // then value rows)
+  // 9. dW_ed[e] = do_e^T h_e   [L, I];  10. dW_gu[e] = dgv_e^T lat_e   [2I, L] (gate rows,
+  // then value rows): each over its expert's slot rows, operands read token-major
   {
     GemmArgs g = gemm_defaults(err, D.c);
     g.M = L;
     g.N = I;
-    g.Kd = static_cast<int>(q);
     g.epi = EPI_F32;
     g.outf = dw_ed;
     g.ldf = I;
     g.groups = E;
-    g.kseg = kseg;
+    g.kseg = offsets;
     g.group_stride = static_cast<long long>(L) * I;
-    if ((rc = launch_gemm(bw + B.dout_t, static_cast<uint64_t>(L), static_cast<int>(q),
-                          bw + B.h_t, static_cast<uint64_t>(I), static_cast<int>(q), g,
+    if ((rc = launch_gemm(dout, static_cast<uint64_t>(TK), L, h, static_cast<uint64_t>(TK), I, g,
                           stream)) != LMOE_OK)
       return rc;
   }
@@ -377,17 +355,15 @@ static int routed_bwd_back(const RoutedBwd& R, const float* dlat_add, float* dla
     GemmArgs g = gemm_defaults(err, D.c);
     g.M = 2 * I;
     g.N = L;
-    g.Kd = static_cast<int>(q);
     g.epi = EPI_F32;
     g.outf = dw_gu;
     g.ldf = L;
     g.groups = E;
-    g.kseg = kseg;
+    g.kseg = offsets;
     g.group_stride = static_cast<long long>(2 * I) * L;
     g.row_map = rowmap;
-    if ((rc = launch_gemm(bw + B.dgv_t, static_cast<uint64_t>(2 * I), static_cast<int>(q),
-                          bw + B.latp_t, static_cast<uint64_t>(L), static_cast<int>(q), g,
-                          stream)) != LMOE_OK)
+    if ((rc = launch_gemm(dgv, static_cast<uint64_t>(TK), 2 * I, latp, static_cast<uint64_t>(TK),
+                          L, g, stream)) != LMOE_OK)
       return rc;
   }
   return LMOE_OK;
@@ -583,14 +559,14 @@ int lmoe_pack_backward_weights(const lmoe_dims* dims, const lmoe_weights* w, con
   // dense weights: [W_up | W_sd] [d, L + sw] -> [L + sw, d]; W_r [E, L] -> [L, E padded];
   // [W_down ; shared gate/value] [L + 2 sw, d] -> [d, L + 2 sw]
   if (rc == LMOE_OK)
-    rc = launch_transpose_pad(reinterpret_cast<const bf*>(pk + P.w2), wz, nullptr, wz, nullptr,
-                              nullptr, D.d, D.d, D.d, reinterpret_cast<bf*>(base + B.wout_t), st);
+    rc = launch_transpose_rows(reinterpret_cast<const bf*>(pk + P.w2), wz, wz, D.d, D.d, D.d,
+                               reinterpret_cast<bf*>(base + B.wout_t), st);
   if (rc == LMOE_OK)
-    rc = launch_transpose_pad(reinterpret_cast<const bf*>(pk + P.wr), D.L, nullptr, D.L, nullptr,
-                              nullptr, D.E, Ep, Ep, reinterpret_cast<bf*>(base + B.wr_t), st);
+    rc = launch_transpose_rows(reinterpret_cast<const bf*>(pk + P.wr), D.L, D.L, D.E, Ep, Ep,
+                               reinterpret_cast<bf*>(base + B.wr_t), st);
   if (rc == LMOE_OK)
-    rc = launch_transpose_pad(reinterpret_cast<const bf*>(pk + P.w1), D.d, nullptr, D.d, nullptr,
-                              nullptr, wc, wc, wc, reinterpret_cast<bf*>(base + B.wls_t), st);
+    rc = launch_transpose_rows(reinterpret_cast<const bf*>(pk + P.w1), D.d, D.d, wc, wc, wc,
+                               reinterpret_cast<bf*>(base + B.wls_t), st);
   return rc;
 }
 
@@ -600,7 +576,8 @@ size_t lmoe_routed_backward_workspace_bytes(const lmoe_dims* dims) {
 }
 
 int lmoe_routed_backward(const lmoe_dims* dims, const void* packed, const void* packed_bwd,
-                         void* workspace, size_t ws_bytes, const float* dz, float* dlat,
+                         void* workspace, size_t ws_bytes, const float* dz, const void* pre,
+                         float* dlat,
                          float* dgate, float* dgamma, float* dw_gu, float* dw_ed, void* bwd_ws,
                          size_t bwd_ws_bytes, void* stream_) {
   int rc = dims_supported(dims);
@@ -626,6 +603,8 @@ int lmoe_routed_backward(const lmoe_dims* dims, const void* packed, const void* 
   R.P = packed_layout(D);
   R.PB = bwd_packed_layout(D);
   R.stream = static_cast<cudaStream_t>(stream_);
+  if (pre && !aligned16(pre)) return LMOE_ERR_INVALID_ARG;
+  R.pre = static_cast<const __nv_bfloat16*>(pre);
   if ((rc = routed_bwd_front(R, dz, dgate, dgamma)) != LMOE_OK) return rc;
   return routed_bwd_back(R, nullptr, dlat, nullptr, 0, dw_gu, dw_ed);
 }
@@ -637,7 +616,8 @@ size_t lmoe_backward_workspace_bytes(const lmoe_dims* dims) {
 
 int lmoe_backward(const lmoe_dims* dims, const void* packed, const void* packed_bwd,
                   void* workspace, size_t ws_bytes, const void* x, const float* logits,
-                  const void* dy, float* dx, float* dgamma, float* dw_in, float* dw_router,
+                  const void* dy, const void* pre, float* dx, float* dgamma, float* dw_in,
+                  float* dw_router,
                   float* dw_gu, float* dw_ed, float* dw_out, void* bwd_ws, size_t bwd_ws_bytes,
                   void* stream_) {
   int rc = dims_supported(dims);
@@ -649,6 +629,7 @@ int lmoe_backward(const lmoe_dims* dims, const void* packed, const void* packed_
     return LMOE_ERR_INVALID_ARG;
   const void* ptrs[] = {packed, packed_bwd, workspace, x, dy, dx, dgamma, dw_in, dw_router,
                         dw_gu, dw_ed, dw_out, bwd_ws};
+  if (pre && !aligned16(pre)) return LMOE_ERR_INVALID_ARG;
   for (const void* p : ptrs)
     if (!aligned16(p)) return LMOE_ERR_INVALID_ARG;
   RoutedBwd R{};
@@ -666,13 +647,14 @@ int lmoe_backward(const lmoe_dims* dims, const void* packed, const void* packed_
   R.P = packed_layout(D);
   R.PB = bwd_packed_layout(D);
   R.stream = static_cast<cudaStream_t>(stream_);
+  R.pre = static_cast<const __nv_bfloat16*>(pre);
   cudaStream_t stream = R.stream;
   const uint8_t* pk = R.pk;
   const uint8_t* pb = R.pb;
   uint8_t* ws = R.ws;
   uint8_t* bw = R.bw;
   const int T = D.T, L = D.L, E = D.E, d = D.d;
-  const int sw = LB.sw, wc = LB.wc, wz = LB.wz, Tq = LB.Tq, Ep = LB.Ep;
+  const int sw = LB.sw, wc = LB.wc, wz = LB.wz, Ep = LB.Ep;
   uint32_t* err = reinterpret_cast<uint32_t*>(ws + R.W.err);
   const bf* xb = static_cast<const bf*>(x);
   const bf* dyb = static_cast<const bf*>(dy);
@@ -706,27 +688,23 @@ int lmoe_backward(const lmoe_dims* dims, const void* packed, const void* packed_
     return launch_gemm(A, static_cast<uint64_t>(M), a_ld, Bm, static_cast<uint64_t>(N), b_ld, g,
                        stream);
   };
-  // weight gradient dW[M, N] = At[M, Tq] . Bt[N, Tq]^T over the padded token axis (one group)
-  auto wgrad = [&](const bf* At, int M, const bf* Bt, int N, float* out, const int32_t* row_map) {
+  // weight gradient dW[M, N] = A^T B over the T token rows of A [T, M] and B [T, N]
+  auto wgrad = [&](const bf* Am, int M, int a_ld, const bf* Bm, int N, int b_ld, float* out,
+                   const int32_t* row_map) {
     GemmArgs g = gemm_defaults(err, D.c);
     g.M = M;
     g.N = N;
-    g.Kd = Tq;
     g.epi = EPI_F32;
     g.outf = out;
     g.ldf = N;
     g.groups = 1;
     g.kseg = seg1;
     g.row_map = row_map;
-    return launch_gemm(At, static_cast<uint64_t>(M), Tq, Bt, static_cast<uint64_t>(N), Tq, g,
+    return launch_gemm(Am, static_cast<uint64_t>(T), a_ld, Bm, static_cast<uint64_t>(T), b_ld, g,
                        stream);
   };
-  auto tr = [&](const bf* src, int width, size_t off) {
-    return launch_transpose_pad(src, width, nullptr, width, nullptr, nullptr, T, Tq, Tq,
-                                reinterpret_cast<bf*>(bw + off), stream);
-  };
   // output rows of dw_in (shared gate/value rows de-interleaved), and the one-group range
-  if ((rc = launch_rowmap(sw, L, rowmap_s, seg1, Tq, stream)) != LMOE_OK) return rc;
+  if ((rc = launch_rowmap(sw, L, rowmap_s, seg1, T, stream)) != LMOE_OK) return rc;
   // 1. [dz | dhs] = dy . [W_up | W_sd]  (dz fp32 for the RMSNorm backward, dhs bf16)
   if ((rc = dense(dyb, T, d, pb + R.PB.wout_t, L, d, d, EPI_F32, dz, L)) != LMOE_OK) return rc;
   if (sw > 0 && (rc = dense(dyb, T, d, pb + R.PB.wout_t + static_cast<size_t>(L) * d * 2, sw, d,
@@ -754,16 +732,11 @@ int lmoe_backward(const lmoe_dims* dims, const void* packed, const void* packed_
   }
   // 6. dx = [dlat | dgv_shared] . [W_down ; W_shared_gate/value]
   if ((rc = dense(dcat, T, wc, pb + R.PB.wls_t, d, wc, wc, EPI_F32, dx, d)) != LMOE_OK) return rc;
-  // 7. dense weight gradients over the tokens: transposed, zero-padded copies, then
-  // dw_out = dy^T [z | hs], dw_router = dlogit^T lat, dw_in = [dlat | dgv_s]^T x
-  if ((rc = tr(dyb, d, LB.dy_t)) != LMOE_OK || (rc = tr(zh, wz, LB.zh_t)) != LMOE_OK ||
-      (rc = tr(dlogit, Ep, LB.dlogit_t)) != LMOE_OK || (rc = tr(lat, L, LB.lat_t)) != LMOE_OK ||
-      (rc = tr(dcat, wc, LB.dcat_t)) != LMOE_OK || (rc = tr(xb, d, LB.x_t)) != LMOE_OK)
-    return rc;
-  auto at = [&](size_t off) { return reinterpret_cast<const bf*>(bw + off); };
-  if ((rc = wgrad(at(LB.dy_t), d, at(LB.zh_t), wz, dw_out, nullptr)) != LMOE_OK ||
-      (rc = wgrad(at(LB.dlogit_t), E, at(LB.lat_t), L, dw_router, nullptr)) != LMOE_OK ||
-      (rc = wgrad(at(LB.dcat_t), wc, at(LB.x_t), d, dw_in, rowmap_s)) != LMOE_OK)
+  // 7. dense weight gradients over the tokens: dw_out = dy^T [z | hs],
+  // dw_router = dlogit^T lat, dw_in = [dlat | dgv_s]^T x
+  if ((rc = wgrad(dyb, d, d, zh, wz, wz, dw_out, nullptr)) != LMOE_OK ||
+      (rc = wgrad(dlogit, E, Ep, lat, L, L, dw_router, nullptr)) != LMOE_OK ||
+      (rc = wgrad(dcat, wc, wc, xb, d, d, dw_in, rowmap_s)) != LMOE_OK)
     return rc;
   return LMOE_OK;
 }
@@ -812,6 +785,7 @@ int lmoe_forward(const lmoe_dims* dims, const void* packed, const void* x, const
   if ((opt.tau_in && !aligned16(opt.tau_in)) || (opt.logits_in && !aligned16(opt.logits_in)))
     return LMOE_ERR_INVALID_ARG;
   if (opt.tau_ema && !(opt.ema_beta >= 0.0f && opt.ema_beta <= 1.0f)) return LMOE_ERR_INVALID_ARG;
+  if (opt.save_pre && (D.expert_fp8 || !aligned16(opt.save_pre))) return LMOE_ERR_INVALID_ARG;
 
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   using bf = __nv_bfloat16;
@@ -1053,6 +1027,8 @@ int lmoe_forward(const lmoe_dims* dims, const void* packed, const void* x, const
     g.epi = EPI_SITU;
     g.out = h;
     g.ldo = D.I;
+    g.pre = static_cast<bf*>(opt.save_pre);
+    g.ldp = 2 * D.I;
     g.c = D.c;
     g.err = err;
     g.timeout_ns = wait_limit_ns();

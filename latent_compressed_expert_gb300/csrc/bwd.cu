@@ -264,77 +264,27 @@ slot_sum_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__
   }
 }
 
-// kseg[e] = sum over e' < e of the expert's token count rounded up to 64 (one CTA).
-__global__ void __launch_bounds__(1024)
-pad_scan_kernel(const int32_t* __restrict__ offsets, int E, int32_t* __restrict__ kseg) {
-  __shared__ int32_t wsum[32];
-  pdl_wait();
-  pdl_launch_dependents();
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int per = (E + 1023) / 1024;
-  const int e0 = threadIdx.x * per, e1 = min(E, e0 + per);
-  int32_t mine = 0;
-  for (int e = e0; e < e1; ++e) mine += (offsets[e + 1] - offsets[e] + 63) / 64 * 64;
-  int32_t incl = mine;
-  for (int o = 1; o < 32; o <<= 1) {
-    const int32_t v = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += v;
-  }
-  if (lane == 31) wsum[warp] = incl;
-  __syncthreads();
-  int32_t before = incl - mine;
-  for (int w = 0; w < warp; ++w) before += wsum[w];
-  for (int e = e0; e < e1; ++e) {
-    kseg[e] = before;
-    before += (offsets[e + 1] - offsets[e] + 63) / 64 * 64;
-  }
-  if (threadIdx.x == 1023) kseg[E] = before;
-}
-
-// XT[w, q] for q < kseg[E]: column q of expert e's padded range is its token
-// p = offsets[e] + (q - kseg[e]) (row gather[p] of x, or row p), or zero past the expert's
-// tokens.  Without offsets the rows form one segment: XT[w, q] = x[q, w] for q < E (the row
-// count), zero up to the grid's last column.  Every expert's range starts on a multiple of 64, so one 64 x 64 tile lies in one
-// expert: one lookup per CTA, 16-byte row loads into shared memory, and 16-byte stores of
-// eight consecutive q of one output row (a warp reads 32 consecutive w of one tile row).
+// XT[w, q] = x[q, w] for q < n, zero for n <= q < qmax (qmax = the grid's 64-row tiles):
+// 64 x 64 tiles through shared memory, 16-byte row loads, and 16-byte stores of eight
+// consecutive q of one output row (a warp reads 32 consecutive w of one tile row).
 constexpr int TP_TILE = 64;
 constexpr int TP_PITCH = TP_TILE + 8;  // bf16 per shared row; keeps 16-byte row stores aligned
 
 __global__ void __launch_bounds__(256)
-transpose_pad_kernel(const __nv_bfloat16* __restrict__ x, int64_t ldx,
-                     const int32_t* __restrict__ gather, int W, const int32_t* __restrict__ offsets,
-                     const int32_t* __restrict__ kseg, int E, int64_t ldt,
-                     __nv_bfloat16* __restrict__ xt) {
+transpose_rows_kernel(const __nv_bfloat16* __restrict__ x, int64_t ldx, int W, int64_t n,
+                      int64_t ldt, __nv_bfloat16* __restrict__ xt) {
   __shared__ __align__(16) __nv_bfloat16 tile[TP_TILE][TP_PITCH];
-  __shared__ int64_t row_src[TP_TILE];
   pdl_wait();
   pdl_launch_dependents();
   const int w0 = blockIdx.y * TP_TILE;
   const int64_t q0 = static_cast<int64_t>(blockIdx.x) * TP_TILE;
-  const int64_t qtot = offsets ? __ldg(kseg + E) : static_cast<int64_t>(gridDim.x) * TP_TILE;
-  if (q0 >= qtot) return;
-  if (threadIdx.x < TP_TILE && !offsets) {
-    const int64_t q = q0 + threadIdx.x;
-    row_src[threadIdx.x] = q < E ? (gather ? static_cast<int64_t>(__ldg(gather + q)) : q) : -1;
-  } else if (threadIdx.x < TP_TILE) {
-    int lo = 0, hi = E;  // kseg[lo] <= q0 < kseg[hi]
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (__ldg(kseg + mid) <= q0) lo = mid; else hi = mid;
-    }
-    const int64_t p = __ldg(offsets + lo) + (q0 + threadIdx.x - __ldg(kseg + lo));
-    row_src[threadIdx.x] =
-        p < __ldg(offsets + lo + 1) ? (gather ? static_cast<int64_t>(__ldg(gather + p)) : p) : -1;
-  }
-  __syncthreads();
   const int c = threadIdx.x & 7;  // 16-byte chunk of a 64-wide row
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
     const int r = (threadIdx.x >> 3) + 32 * i;
-    const int64_t src = row_src[r];
     uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (src >= 0 && w0 + 8 * c < W)
-      v = __ldg(reinterpret_cast<const uint4*>(x + src * ldx + w0 + 8 * c));
+    if (q0 + r < n && w0 + 8 * c < W)
+      v = __ldg(reinterpret_cast<const uint4*>(x + (q0 + r) * ldx + w0 + 8 * c));
     *reinterpret_cast<uint4*>(&tile[r][8 * c]) = v;
   }
   __syncthreads();
@@ -342,7 +292,7 @@ transpose_pad_kernel(const __nv_bfloat16* __restrict__ x, int64_t ldx,
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
     const int wl = lane + 32 * i;
-    if (w0 + wl >= W || q0 + 8 * qc >= qtot) continue;
+    if (w0 + wl >= W) continue;
     uint32_t pk[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -353,6 +303,31 @@ transpose_pad_kernel(const __nv_bfloat16* __restrict__ x, int64_t ldx,
     *reinterpret_cast<uint4*>(xt + static_cast<int64_t>(w0 + wl) * ldt + q0 + 8 * qc) =
         make_uint4(pk[0], pk[1], pk[2], pk[3]);
   }
+}
+
+// out[p, :W] = x[idx[p], :W] for p < n (16-byte pieces; W, ldx and ldo multiples of 8).
+__global__ void __launch_bounds__(256)
+gather_rows_kernel(const __nv_bfloat16* __restrict__ x, int64_t ldx,
+                   const int32_t* __restrict__ idx, int W, __nv_bfloat16* __restrict__ out,
+                   int64_t ldo) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int64_t p = blockIdx.x;
+  const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<int64_t>(__ldg(idx + p)) * ldx);
+  uint4* dst = reinterpret_cast<uint4*>(out + p * ldo);
+  for (int v = threadIdx.x; v < W / 8; v += blockDim.x) dst[v] = __ldg(src + v);
+}
+
+int launch_gather_rows(const __nv_bfloat16* x, int64_t ldx, const int32_t* idx, int64_t n, int W,
+                       __nv_bfloat16* out, int64_t ldo, cudaStream_t stream) {
+  if (n == 0) return LMOE_OK;
+  if (W % 8 || ldx % 8 || ldo % 8 || (reinterpret_cast<uintptr_t>(x) & 15) ||
+      (reinterpret_cast<uintptr_t>(out) & 15) || n > 0x7fffffff)
+    return LMOE_ERR_UNSUPPORTED;
+  return launch_pdl(gather_rows_kernel, static_cast<unsigned>(n), 256, 0, stream, x, ldx, idx, W,
+                    out, ldo) == cudaSuccess
+             ? LMOE_OK
+             : LMOE_ERR_CUDA;
 }
 
 // Output row of each packed row: rows below `base` keep their place; the 2I gate/value rows
@@ -431,25 +406,18 @@ int launch_slot_sum(const __nv_bfloat16* x, const int32_t* inv, int T, int K, in
              : LMOE_ERR_CUDA;
 }
 
-int launch_pad_scan(const int32_t* offsets, int E, int32_t* kseg, cudaStream_t stream) {
-  return launch_pdl(pad_scan_kernel, 1, 1024, 0, stream, offsets, E, kseg) == cudaSuccess
-             ? LMOE_OK
-             : LMOE_ERR_CUDA;
-}
-
-int launch_transpose_pad(const __nv_bfloat16* x, int64_t ldx, const int32_t* gather, int W,
-                         const int32_t* offsets, const int32_t* kseg, int E, int64_t qmax,
-                         int64_t ldt, __nv_bfloat16* xt, cudaStream_t stream) {
-  // 16-byte rows and stores; padded ranges are whole tiles
-  if (!offsets && qmax < E) return LMOE_ERR_INVALID_ARG;  // one segment of E rows
-  if (W % 8 || ldx % 8 || ldt % 8 || qmax % TP_TILE || (reinterpret_cast<uintptr_t>(x) & 15) ||
-      (reinterpret_cast<uintptr_t>(xt) & 15))
+int launch_transpose_rows(const __nv_bfloat16* x, int64_t ldx, int W, int64_t n, int64_t qmax,
+                          int64_t ldt, __nv_bfloat16* xt, cudaStream_t stream) {
+  if (n == 0 && qmax == 0) return LMOE_OK;
+  // 16-byte rows and stores; whole 64-row tiles
+  if (qmax < n || W % 8 || ldx % 8 || ldt % 8 || ldt < qmax || qmax % TP_TILE ||
+      (reinterpret_cast<uintptr_t>(x) & 15) || (reinterpret_cast<uintptr_t>(xt) & 15))
     return LMOE_ERR_UNSUPPORTED;
   if (ceil_div(W, TP_TILE) > 65535) return LMOE_ERR_UNSUPPORTED;
   const dim3 grid(static_cast<unsigned>(qmax / TP_TILE),
                   static_cast<unsigned>(ceil_div(W, TP_TILE)));
-  return launch_pdl(transpose_pad_kernel, grid, 256, 0, stream, x, ldx, gather, W, offsets, kseg,
-                    E, ldt, xt) == cudaSuccess
+  return launch_pdl(transpose_rows_kernel, grid, 256, 0, stream, x, ldx, W, n, ldt, xt) ==
+                 cudaSuccess
              ? LMOE_OK
              : LMOE_ERR_CUDA;
 }

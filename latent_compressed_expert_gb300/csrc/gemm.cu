@@ -43,6 +43,8 @@ struct GemmCfg {
   static constexpr int EPI_BYTES = 4 * 32 * 32 * 4;
   static constexpr int SMEM_BYTES = EPI_OFF + EPI_BYTES + 1024;  // + slack for 1024 alignment
   static constexpr uint32_t IDESC = ptx::idesc_bf16_f32(BLOCK_M, BN);
+  static constexpr uint32_t IDESC_MN = ptx::idesc_bf16_f32_mn(BLOCK_M, BN);
+  static constexpr int BOX_BYTES = 64 * BLOCK_K * 2;  // one 64 x 64 MN-major TMA box
   static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "tiles must stay 1024-aligned");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
@@ -56,8 +58,9 @@ struct TileCoord {
   int b_row;    // first row of B
   int n0;       // first output column
   int grp;      // grouped-K mode: the group; else 0
-  int k0;       // first column of A and B reduced over
+  int k0;       // first K index (column of A and B; grouped-K: their first row) reduced over
   int nk;       // 64-wide K-blocks reduced over
+  int klen;     // grouped-K: rows in the group (the last K-block may be partial)
 };
 
 template <int BN>
@@ -84,9 +87,11 @@ __device__ __forceinline__ TileCoord decode_tile(const GemmArgs& g, int nt, int 
   c.grp = kgroup;
   if (g.groups > 0) {
     c.k0 = __ldg(g.kseg + kgroup);
-    c.nk = (__ldg(g.kseg + kgroup + 1) - c.k0) / BLOCK_K;
+    c.klen = __ldg(g.kseg + kgroup + 1) - c.k0;
+    c.nk = (c.klen + BLOCK_K - 1) / BLOCK_K;
   } else {
     c.k0 = 0;
+    c.klen = g.Kd;
     c.nk = g.Kd / BLOCK_K;
   }
   return c;
@@ -295,8 +300,20 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA,
           }
           uint8_t* sa = smem + s * C::STAGE_BYTES;
           ptx::mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
-          ptx::tma_load_2d(sa, &tmA, &full[s], tc.k0 + kb * BLOCK_K, tc.a_row);
-          ptx::tma_load_2d(sa + C::A_BYTES, &tmB, &full[s], tc.k0 + kb * BLOCK_K, tc.b_row);
+          if (g.groups > 0) {
+            // MN-major: 64 K rows of 64-column boxes (rows past the operand are zero-filled)
+            const int krow = tc.k0 + kb * BLOCK_K;
+#pragma unroll
+            for (int i = 0; i < BLOCK_M / 64; ++i)
+              ptx::tma_load_2d(sa + i * C::BOX_BYTES, &tmA, &full[s], tc.a_row + 64 * i, krow);
+#pragma unroll
+            for (int i = 0; i < BN / 64; ++i)
+              ptx::tma_load_2d(sa + C::A_BYTES + i * C::BOX_BYTES, &tmB, &full[s],
+                               tc.b_row + 64 * i, krow);
+          } else {
+            ptx::tma_load_2d(sa, &tmA, &full[s], tc.k0 + kb * BLOCK_K, tc.a_row);
+            ptx::tma_load_2d(sa + C::A_BYTES, &tmB, &full[s], tc.k0 + kb * BLOCK_K, tc.b_row);
+          }
         }
       }
       // every issued copy must land before the CTA may exit
@@ -307,6 +324,65 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA,
           break;
         }
       }
+    }
+  } else if (warp == 1 && g.groups > 0) {
+    // ------------------------------------------------------------ MMA issuer, grouped-K:
+    // the whole warp waits; in a group's last K-block it zeroes A's rows past the group
+    // (another group's rows, or TMA fill), then one lane issues the MMAs
+    uint32_t it = 0;
+    int lt = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x, ++lt) {
+      const int acc = lt & 1;
+      const uint32_t aph = static_cast<uint32_t>(lt >> 1) & 1u;
+      if (!__all_sync(0xffffffffu, ptx::mbar_wait(&tempty[acc], aph ^ 1u, abort_flag, limit))) {
+        if (lane == 0) raise_error(g, abort_flag, DEVERR_TIMEOUT_MMA);
+        break;
+      }
+      ptx::tc_fence_after();
+      const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+      const TileCoord tc = decode_tile<BN>(g, nt, mt_dense, tile);
+      for (int kb = 0; kb < tc.nk; ++kb, ++it) {
+        const int s = static_cast<int>(it % C::STAGES);
+        const uint32_t ph = (it / C::STAGES) & 1u;
+        if (!__all_sync(0xffffffffu, ptx::mbar_wait(&full[s], ph, abort_flag, limit))) {
+          if (lane == 0) raise_error(g, abort_flag, DEVERR_TIMEOUT_MMA);
+          ok = false;
+          break;
+        }
+        uint8_t* sa = smem + s * C::STAGE_BYTES;
+        const int valid = tc.klen - kb * BLOCK_K;  // K rows of this block inside the group
+        if (valid < BLOCK_K) {
+          // a K row is one 128-byte line of each A box (the swizzle permutes within it)
+          const int per_box = (BLOCK_K - valid) * 8;  // 16-byte pieces
+          for (int i = lane; i < (BLOCK_M / 64) * per_box; i += 32) {
+            const int box = i / per_box, rem = i - box * per_box;
+            *reinterpret_cast<uint4*>(sa + box * C::BOX_BYTES + valid * 128 + rem * 16) =
+                make_uint4(0u, 0u, 0u, 0u);
+          }
+          ptx::fence_proxy_async_smem();  // the zeros are visible to the tensor cores
+        }
+        __syncwarp();
+        if (lane == 0) {
+          ptx::tc_fence_after();
+          const uint32_t a0 = ptx::smem_u32(sa);
+          const uint32_t b0 = a0 + C::A_BYTES;
+#pragma unroll
+          for (int k = 0; k < BLOCK_K / 16; ++k)  // 16 K rows = two 1024-byte atoms
+            ptx::umma_bf16(d_tmem, ptx::smem_desc_sw128_mn(a0 + k * 2048, C::BOX_BYTES),
+                           ptx::smem_desc_sw128_mn(b0 + k * 2048, C::BOX_BYTES), C::IDESC_MN,
+                           (kb | k) != 0 ? 1u : 0u);
+          ptx::umma_commit(&empty[s]);
+        }
+        __syncwarp();
+      }
+      if (!ok) break;
+      if (lane == 0) ptx::umma_commit(&tfull[acc]);
+    }
+    if (lane == 0) {
+      // all MMAs issued by this thread complete before TMEM is released
+      ptx::umma_commit(drain);
+      if (!wait_drain(drain, 0u, limit)) raise_error(g, abort_flag, DEVERR_TIMEOUT_DRAIN);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -327,7 +403,7 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA,
         }
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-        const int nkt = g.groups > 0 ? decode_tile<BN>(g, nt, mt_dense, tile).nk : g.Kd / BLOCK_K;
+        const int nkt = g.Kd / BLOCK_K;
         bool ok = true;
         for (int kb = 0; kb < nkt; ++kb, ++it) {
           const int s = static_cast<int>(it % C::STAGES);
@@ -489,7 +565,9 @@ static int launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArg
 
 int launch_gemm(const void* A, uint64_t a_rows, int a_ld, const void* B, uint64_t b_rows,
                 int b_ld, const GemmArgs& g, cudaStream_t stream) {
-  if (g.Kd % BLOCK_K != 0 || g.Kd <= 0 || g.N <= 0) return LMOE_ERR_UNSUPPORTED;
+  if (g.groups > 0 && (g.epi != EPI_F32 || !g.kseg)) return LMOE_ERR_INVALID_ARG;
+  if (g.groups == 0 && (g.Kd % BLOCK_K != 0 || g.Kd <= 0)) return LMOE_ERR_UNSUPPORTED;
+  if (g.N <= 0) return LMOE_ERR_UNSUPPORTED;
   const bool glu = g.epi == EPI_SITU || g.epi == EPI_SPLIT;
   if (g.N % (glu ? 32 : 16) != 0 || (g.epi == EPI_SPLIT && g.split % 32 != 0))
     return LMOE_ERR_UNSUPPORTED;
@@ -499,11 +577,19 @@ int launch_gemm(const void* A, uint64_t a_rows, int a_ld, const void* B, uint64_
   // tiles instead of 7, re-reading the latent half as often (61.9 -> 59.4 us at prefill)
   const int bn = (g.N % 256 == 0 || g.N > 512) ? 256 : 128;
   CUtensorMap ta, tb;
-  if (!make_tmap_bf16(&ta, A, a_rows, static_cast<uint64_t>(g.Kd), static_cast<uint64_t>(a_ld),
-                      BLOCK_M) ||
-      !make_tmap_bf16(&tb, B, b_rows, static_cast<uint64_t>(g.Kd), static_cast<uint64_t>(b_ld),
-                      static_cast<uint32_t>(bn)))
+  if (g.groups > 0) {
+    // MN-major: a_rows / b_rows count K rows; boxes of 64 columns x 64 rows
+    if (!make_tmap_bf16(&ta, A, a_rows, static_cast<uint64_t>(g.M), static_cast<uint64_t>(a_ld),
+                        BLOCK_K) ||
+        !make_tmap_bf16(&tb, B, b_rows, static_cast<uint64_t>(g.N), static_cast<uint64_t>(b_ld),
+                        BLOCK_K))
+      return LMOE_ERR_CUDA;
+  } else if (!make_tmap_bf16(&ta, A, a_rows, static_cast<uint64_t>(g.Kd),
+                             static_cast<uint64_t>(a_ld), BLOCK_M) ||
+             !make_tmap_bf16(&tb, B, b_rows, static_cast<uint64_t>(g.Kd),
+                             static_cast<uint64_t>(b_ld), static_cast<uint32_t>(bn))) {
     return LMOE_ERR_CUDA;
+  }
   return bn == 256 ? launch_bn<256>(ta, tb, g, stream) : launch_bn<128>(ta, tb, g, stream);
 }
 

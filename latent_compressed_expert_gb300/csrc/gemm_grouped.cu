@@ -386,7 +386,27 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
           for (int j = 0; j < 32; ++j) v[j] = v[j] * w_s * __shfl_sync(0xffffffffu, xs, j);
         }
         __nv_bfloat16* orow = g.out + static_cast<size_t>(t.tok0 + ch * 32) * g.ldo;
+        // through shared memory: the warp's 32 rows x 32 tokens become, per token, four
+        // 16-byte pieces of its output row, so a store instruction writes 8 tokens' rows
+        // instead of one
+        auto staged_store = [&](__nv_bfloat16* base, int ld) {
+          __nv_bfloat16* st = epi_stage + (warp - 2) * (32 * 32);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) st[j * 32 + lane] = __float2bfloat16_rn(v[j]);
+          __syncwarp();
+          const int piece = lane & 3;
+#pragma unroll
+          for (int j0 = 0; j0 < 32; j0 += 8) {
+            const int j = j0 + (lane >> 2);
+            const uint4 val = *reinterpret_cast<const uint4*>(st + j * 32 + piece * 8);
+            if (j < nv)
+              *reinterpret_cast<uint4*>(base + static_cast<size_t>(t.tok0 + ch * 32 + j) * ld +
+                                        t.r0 + q * 32 + piece * 8) = val;
+          }
+          __syncwarp();
+        };
         if (g.epi == EPI_SITU) {
+          if (g.pre) staged_store(g.pre, g.ldp);  // the pre-activations, for a backward pass
           // rows r (gate, lanes 0..15) and r + 16 (value, lanes 16..31) of one 32-row group
           // hold feature f; lanes 0..15 evaluate it for the even tokens, lanes 16..31 for
           // the odd ones, so every SiTU evaluation uses the whole warp
@@ -404,23 +424,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
             if (j < nv) orow[static_cast<size_t>(j) * g.ldo + f] = __float2bfloat16_rn(hv);
           }
         } else if (row_ok) {
-          // through shared memory: the warp's 32 rows x 32 tokens become, per token, four
-          // 16-byte pieces of its output row, so a store instruction writes 8 tokens' rows
-          // instead of one
-          __nv_bfloat16* st = epi_stage + (warp - 2) * (32 * 32);
-#pragma unroll
-          for (int j = 0; j < 32; ++j) st[j * 32 + lane] = __float2bfloat16_rn(v[j]);
-          __syncwarp();
-          const int piece = lane & 3;
-#pragma unroll
-          for (int j0 = 0; j0 < 32; j0 += 8) {
-            const int j = j0 + (lane >> 2);
-            const uint4 val = *reinterpret_cast<const uint4*>(st + j * 32 + piece * 8);
-            if (j < nv)
-              *reinterpret_cast<uint4*>(orow + static_cast<size_t>(j) * g.ldo + t.r0 + q * 32 +
-                                        piece * 8) = val;
-          }
-          __syncwarp();
+          staged_store(g.out, g.ldo);
         }
       }
       ptx::tc_fence_before();
@@ -461,6 +465,9 @@ int launch_grouped_gemm(const void* W, const void* X, uint64_t x_rows, int x_ld,
   if (g.epi != EPI_SITU && g.epi != EPI_BF16) return LMOE_ERR_UNSUPPORTED;
   if (g.epi == EPI_SITU && g.M_w % BLOCK_M != 0) return LMOE_ERR_UNSUPPORTED;
   if (g.fp8 && (!g.w_scale || !g.x_scale || x_ld % 2 != 0)) return LMOE_ERR_INVALID_ARG;
+  if (g.pre && (g.epi != EPI_SITU || g.ldp % 8 != 0 || g.ldp < g.M_w ||
+                (reinterpret_cast<uintptr_t>(g.pre) & 15u)))
+    return LMOE_ERR_INVALID_ARG;
   // From here on the kernel counts K in units of 2 bytes: an e4m3 row of Kd codes is
   // addressed as Kd / 2 bf16-sized pairs, so tiles, boxes, swizzle and the gather offsets
   // are the same bytes for both operand types.

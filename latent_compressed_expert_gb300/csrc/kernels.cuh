@@ -57,9 +57,12 @@ struct GemmArgs {
   unsigned long long timeout_ns;
   int inject_stall;       // test hook: the MMA role first waits on a barrier nobody arrives
                           // on, so every role runs into its bounded wait and aborts
-  // Grouped-K mode (groups > 0): `groups` independent products, group q reducing over the
-  // columns [kseg[q], kseg[q + 1]) of A and B (multiples of 64; an empty range gives zeros);
-  // EPI_F32 only, group q's output at outf + q * group_stride, output row row_map[r] (or r)
+  // Grouped-K mode (groups > 0): `groups` independent products C_q = A_q^T B_q with A and B
+  // MN-major (token-major): A [rows, M] and B [rows, N] row-major, group q reducing over the
+  // rows [kseg[q], kseg[q + 1]) (any boundaries; an empty range gives zeros; the rows of
+  // the next group that a last K-block reaches are zeroed in A's tile, so B's must be
+  // finite).  EPI_F32 only; group q's output at outf + q * group_stride, output row
+  // row_map[r] (or r).
   int groups;
   const int32_t* kseg;
   long long group_stride;
@@ -94,6 +97,9 @@ struct GroupedArgs {
   int fp8;
   const float* w_scale;   // [E * ceil(M_w / 128) * 128] per weight row
   const float* x_scale;   // per activation row, indexed like the rows (through gather)
+  // EPI_SITU: also store the bf16 pre-activations, pre[row, weight row] (row stride ldp)
+  __nv_bfloat16* pre;
+  int ldp;
 };
 
 // W: the experts' weights in tiles of 128 rows x 128 bytes (64 bf16 or 128 e4m3 codes),
@@ -156,15 +162,16 @@ int launch_situ_bwd(const __nv_bfloat16* pre, const __nv_bfloat16* dh, int64_t r
 int launch_slot_sum(const __nv_bfloat16* x, const int32_t* inv, int T, int K, int L,
                     const float* add, float* out, __nv_bfloat16* outb, int64_t ldb,
                     cudaStream_t stream);
-int launch_pad_scan(const int32_t* offsets, int E, int32_t* kseg, cudaStream_t stream);
+int launch_gather_rows(const __nv_bfloat16* x, int64_t ldx, const int32_t* idx, int64_t n, int W,
+                       __nv_bfloat16* out, int64_t ldo, cudaStream_t stream);
 int launch_rowmap(int I, int base, int32_t* map, int32_t* seg, int seg_len, cudaStream_t stream);
 // Router backward: dz [T, ldo] bf16 from the logits z [T, ldz], routing and dgate.
 int launch_router_bwd(const float* z, int64_t ldz, const int32_t* idx, const float* gate,
                       const float* dgate, int T, int K, __nv_bfloat16* dz, int ldo,
                       cudaStream_t stream);
-int launch_transpose_pad(const __nv_bfloat16* x, int64_t ldx, const int32_t* gather, int W,
-                         const int32_t* offsets, const int32_t* kseg, int E, int64_t qmax,
-                         int64_t ldt, __nv_bfloat16* xt, cudaStream_t stream);
+// xt[w, q] = x[q, w] for q < n, zero up to qmax (a multiple of 64).
+int launch_transpose_rows(const __nv_bfloat16* x, int64_t ldx, int W, int64_t n, int64_t qmax,
+                          int64_t ldt, __nv_bfloat16* xt, cudaStream_t stream);
 // Per-row e4m3 quantisation of bf16 rows (cols % 16 == 0): codes [rows, ldq], scales [rows].
 int launch_quantize_rows(const __nv_bfloat16* x, int64_t rows, int cols, int64_t ldx,
                          uint8_t* q, int64_t ldq, float* scales, cudaStream_t stream);

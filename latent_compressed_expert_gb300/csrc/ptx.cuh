@@ -223,12 +223,31 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t smem_addr) {
   return d;
 }
 
+// Shared-memory descriptor of an MN-major operand in the 128-byte swizzle: each K index is
+// one 128-byte row of 64 consecutive MN elements, 8 such rows form a 1024-byte atom (stride
+// byte offset 1024), and the next 64 MN elements start `lbo` bytes further (leading byte
+// offset).  This is the layout a TMA box of 64 elements x rows leaves with SWIZZLE_128B.
+__device__ __forceinline__ uint64_t smem_desc_sw128_mn(uint32_t smem_addr, uint32_t lbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;
+  return d;
+}
+
 // Instruction descriptor of tcgen05.mma kind::f16: fp32 accumulator (bits 4-5 = 1),
 // A and B bf16 (bits 7-9 = 1, bits 10-12 = 1), both K-major (bits 15, 16 = 0),
 // N >> 3 in bits 17-22, M >> 4 in bits 24-28.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
          (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// The same with A and B MN-major (bits 15 and 16 set).
+__host__ __device__ constexpr uint32_t idesc_bf16_f32_mn(int M, int N) {
+  return idesc_bf16_f32(M, N) | (1u << 15) | (1u << 16);
 }
 
 // Instruction descriptor of tcgen05.mma kind::f8f6f4 with A and B e4m3 (format 0 in bits

@@ -42,7 +42,8 @@ class IO(ctypes.Structure):
                 ("stage_events", ctypes.POINTER(_vp)), ("kernel_launches", _i),
                 ("aux_stream", _vp), ("aux_events", _vp * 2), ("shared_sms", _i),
                 ("phase", _i), ("cand_out", _vp), ("cand_k", _i),
-                ("tau_ema", _vp), ("ema_beta", _f), ("ema_first", _i), ("load_stats", _vp)]
+                ("tau_ema", _vp), ("ema_beta", _f), ("ema_first", _i), ("load_stats", _vp),
+                ("save_pre", _vp)]
 
 
 OVERLAP_MIN_T = 512  # LMOE_OVERLAP_MIN_T
@@ -70,10 +71,10 @@ SIGNATURES = {
                                         _sz, _vp]),
     "lmoe_backward_workspace_bytes": (_sz, [ctypes.POINTER(Dims)]),
     "lmoe_backward": (_i, [ctypes.POINTER(Dims), _vp, _vp, _vp, _sz, _vp, _vp, _vp, _vp, _vp,
-                           _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+                           _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "lmoe_routed_backward_workspace_bytes": (_sz, [ctypes.POINTER(Dims)]),
     "lmoe_routed_backward": (_i, [ctypes.POINTER(Dims), _vp, _vp, _vp, _sz, _vp, _vp, _vp, _vp,
-                                  _vp, _vp, _vp, _sz, _vp]),
+                                  _vp, _vp, _vp, _vp, _sz, _vp]),
     "lmoe_ep_workspace_bytes": (_sz, [_i, _i, _i, _i]),
     "lmoe_ep_dispatch": (_i, [_vp, _i, _i, _i, _i, _vp, _i, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "lmoe_ep_combine": (_i, [_vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _vp,
@@ -396,7 +397,8 @@ class Layer:
                 logits_in: torch.Tensor | None = None, debug: bool = False, stream=None,
                 stage_events=None, phase: int = PHASE_ALL, cand_k: int = 0,
                 tau_ema: torch.Tensor | None = None, ema_beta: float = 0.9,
-                ema_first: bool = False, load_stats: "LoadStats | None" = None):
+                ema_first: bool = False, load_stats: "LoadStats | None" = None,
+                train: bool = False):
         """One lmoe_forward call.  stage_events: optional list of NUM_STAGES + 1
         torch.cuda.Event(enable_timing=True) recorded at the stage boundaries.  After the
         call, ``self.last_kernel_launches`` holds the number of kernels it launched.
@@ -404,7 +406,9 @@ class Layer:
         threshold candidates when cand_k > 0, else None) then PHASE_EXPERTS (x gives the
         batch size only).  tau_ema: [E] streaming thresholds, updated in place with this
         batch's (ema_beta, ema_first) and routed against.  load_stats: a LoadStats that this
-        step's per-expert counts are added to."""
+        step's per-expert counts are added to.  train: also keep the routed experts'
+        pre-activations (lmoe_io.save_pre) for the next ``backward`` / ``backward_layer``
+        (needs ``enable_backward``)."""
         sh = self.shape
         T = x.shape[0]
         if T > self.max_tokens:
@@ -442,6 +446,12 @@ class Layer:
             io.ema_first = 1 if ema_first else 0
         if load_stats is not None:
             io.load_stats = _ptr(load_stats.acc)
+        self._pre_rows = None
+        if train:
+            if getattr(self, "pre_buf", None) is None:
+                raise RuntimeError("lmoe: forward(train=True) needs enable_backward() first")
+            io.save_pre = _ptr(self.pre_buf)
+            self._pre_rows = T
         if debug:
             dev = x.device
             dbg["logits"] = torch.empty((T, sh.E), dtype=torch.float32, device=dev)
@@ -528,12 +538,25 @@ class Layer:
                                                  _stream(stream)),
                "lmoe_pack_backward_weights")
         self.bwd_bytes = int(load().lmoe_backward_workspace_bytes(ctypes.byref(D)))
+        # the routed pre-activations a training forward keeps (lmoe_io.save_pre)
+        sh = self.shape
+        self.pre_buf = torch.empty((self.max_tokens * sh.K, 2 * sh.I), dtype=torch.bfloat16,
+                                   device=self.device)
         self.bwd_ws = torch.empty(self.bwd_bytes, dtype=torch.uint8, device=self.device)
 
-    # kernels one lmoe_routed_backward call launches: combine backward, two dgamma passes,
-    # three grouped GEMMs, SiTU backward, slot sum, pad scan, row map, four transposes and
-    # two grouped-K weight-gradient GEMMs
-    BACKWARD_LAUNCHES = 16
+    def backward_launches(self, T: int) -> int:
+        """Kernels one lmoe_routed_backward call for T tokens launches: combine backward, two
+        dgamma passes, two grouped dgrad GEMMs (and the pre-activation GEMM when the last
+        forward was not a training step), SiTU backward, slot sum, latent row gather, row
+        map and two grouped weight-gradient GEMMs."""
+        return 12 + (0 if getattr(self, "_pre_rows", None) == T else 1)
+
+    def _saved_pre(self, T: int):
+        """The pre-activations kept by the last forward, if it was a training step of T
+        tokens; else None (the backward recomputes them)."""
+        if getattr(self, "_pre_rows", None) == T:
+            return _ptr(self.pre_buf)
+        return None
 
     def backward(self, dz: torch.Tensor, stream=None) -> dict:
         """Gradients of the routed branch for the batch of the last ``forward`` call
@@ -553,20 +576,19 @@ class Layer:
         bwd_bytes = int(load().lmoe_routed_backward_workspace_bytes(ctypes.byref(dims)))
         _check(load().lmoe_routed_backward(
             ctypes.byref(dims), _ptr(self.packed), _ptr(self.packed_bwd), _ptr(self.workspace),
-            self.ws_bytes, _ptr(dz), _ptr(out["dlat"]), _ptr(out["dgate"]), _ptr(out["dgamma"]),
+            self.ws_bytes, _ptr(dz), self._saved_pre(T), _ptr(out["dlat"]), _ptr(out["dgate"]), _ptr(out["dgamma"]),
             _ptr(out["dw_gu"]), _ptr(out["dw_edown"]), _ptr(self.bwd_ws), bwd_bytes,
             _stream(stream)), "lmoe_routed_backward")
         out["dw_gate"] = out["dw_gu"][:, :sh.I]
         out["dw_value"] = out["dw_gu"][:, sh.I:]
         return out
 
-    def layer_backward_launches(self) -> int:
+    def layer_backward_launches(self, T: int) -> int:
         """Kernels one lmoe_backward call launches: the routed branch's, plus the row map of
-        dw_in, the dz GEMM (and the dhs GEMM), router backward and its GEMM, (the shared
-        experts' GEMM and SiTU backward), the dx GEMM, six transposes and three
-        weight-gradient GEMMs; the parenthesised ones only with shared experts."""
-        shared = 3 if self.shape.S > 0 else 0
-        return self.BACKWARD_LAUNCHES + 1 + 1 + 2 + 1 + 6 + 3 + shared
+        dw_in, the dz GEMM, router backward and its GEMM, the dx GEMM and three
+        weight-gradient GEMMs; with shared experts also the dhs GEMM, their pre-activation
+        GEMM and their SiTU backward."""
+        return self.backward_launches(T) + 8 + (3 if self.shape.S > 0 else 0)
 
     def backward_layer(self, x: torch.Tensor, dy: torch.Tensor, logits=None,
                        stream=None) -> dict:
@@ -597,7 +619,7 @@ class Layer:
         bwd_bytes = int(load().lmoe_backward_workspace_bytes(ctypes.byref(dims)))
         _check(load().lmoe_backward(
             ctypes.byref(dims), _ptr(self.packed), _ptr(self.packed_bwd), _ptr(self.workspace),
-            self.ws_bytes, _ptr(x), _ptr(logits), _ptr(dy), _ptr(out["dx"]),
+            self.ws_bytes, _ptr(x), _ptr(logits), _ptr(dy), self._saved_pre(T), _ptr(out["dx"]),
             _ptr(out["dgamma"]), _ptr(out["dw_in"]), _ptr(out["dw_router"]), _ptr(out["dw_gu"]),
             _ptr(out["dw_edown"]), _ptr(out["dw_out"]), _ptr(self.bwd_ws), bwd_bytes,
             _stream(stream)), "lmoe_backward")

@@ -201,10 +201,16 @@ def test_backward_size_queries(lib):
     d = lmoe.dims_of(sh)
     routed = lib.lmoe_routed_backward_workspace_bytes(ctypes.byref(d))
     layer = lib.lmoe_backward_workspace_bytes(ctypes.byref(d))
-    # the layer's scratch extends the routed branch's by its dense buffers
+    # the layer's scratch extends the routed branch's by its dense buffers: dz, dlat_r and
+    # dlat (fp32), dhs, the shared pre-activations, [dlat | dgv_s] and dlogit (bf16)
     sw = sh.S * sh.Is
-    dense_t = 2 * sh.T * (2 * sh.d + 3 * sh.L + 3 * sw + sh.E)   # six transposed copies
-    assert routed + dense_t < layer < routed + 3 * dense_t
+    extra = sh.T * (12 * sh.L + 2 * sw + 4 * sw + 2 * (sh.L + 2 * sw) + 2 * sh.E + 4 * sh.K)
+    assert layer - routed == pytest.approx(extra, abs=64 * 1024)
+    # the routed branch's: do, the slot-order latent and its gradient ([TK, L] bf16 each),
+    # dh [TK, I], pre-activations and their gradients [TK, 2I], plus u (fp32 [T, L])
+    TK = sh.T * sh.K
+    acts = TK * (3 * 2 * sh.L + 2 * sh.I + 2 * 2 * 2 * sh.I)
+    assert acts < routed < acts + sh.T * sh.L * 4 + 4 * 1024 * 1024
     # the transposed pack holds every routed and dense weight once (bf16)
     pb = lib.lmoe_packed_backward_bytes(ctypes.byref(d))
     weights = 2 * (3 * sh.E * sh.I * sh.L + (sh.L + sw) * sh.d + sh.L * sh.E
@@ -223,12 +229,15 @@ def test_backward_argument_checks(lib):
     f = lib.lmoe_backward
 
     def call(dims=d, x=fake, dy=fake, ws_bytes=ws, bw_bytes=bw, dx=fake):
-        return f(ctypes.byref(dims), fake, fake, fake, ws_bytes, x, None, dy, dx, fake, fake,
-                 fake, fake, fake, fake, fake, bw_bytes, None)
+        return f(ctypes.byref(dims), fake, fake, fake, ws_bytes, x, None, dy, None, dx, fake,
+                 fake, fake, fake, fake, fake, fake, bw_bytes, None)
 
     assert call(x=None) == lmoe.LMOE_ERR_INVALID_ARG
     assert call(dy=None) == lmoe.LMOE_ERR_INVALID_ARG
     assert call(dx=ctypes.c_void_p(0x1004)) == lmoe.LMOE_ERR_INVALID_ARG   # misaligned
+    assert f(ctypes.byref(d), fake, fake, fake, ws, fake, None, fake, ctypes.c_void_p(0x1002),
+             fake, fake, fake, fake, fake, fake, fake, fake, bw, None) \
+        == lmoe.LMOE_ERR_INVALID_ARG                                          # pre misaligned
     assert call(bw_bytes=bw - 1) == lmoe.LMOE_ERR_WORKSPACE_TOO_SMALL
     assert call(ws_bytes=ws - 1) == lmoe.LMOE_ERR_WORKSPACE_TOO_SMALL
     assert call(dims=lmoe.dims_of(synth.TINY, T=0), ws_bytes=1 << 30, bw_bytes=1 << 30) \

@@ -114,3 +114,25 @@ def test_layer_backward_matches_oracle(dev, oracle_mod, shape):
     keys = [k for k in LAYER_KEYS if ref[k].size > 0]
     stats = {k: _stats(g[k].cpu().numpy(), ref[k]) for k in keys}
     assert all(_ok(v) for v in stats.values()), (sh.name, stats)
+
+
+def test_saved_pre_activations_match_recompute(dev):
+    """A training forward keeps the routed pre-activations (lmoe_io.save_pre); the backward
+    that uses them equals, bit for bit, the one that recomputes them (same GEMM, same
+    accumulation order)."""
+    sh = synth.LayerShape("b1", T=256, d=512, L=256, E=32, K=4, I=128, S=2, Is=128)
+    w = synth.make_weights(sh, seed=95)
+    wd = {k: v.to(dev) for k, v in w.items()}
+    layer = lmoe.Layer(sh, wd)
+    layer.enable_backward(wd)
+    x = synth.make_x(sh, seed=96).to(dev)
+    dy = torch.randn(sh.T, sh.d, generator=torch.Generator().manual_seed(97)).to(torch.bfloat16)
+    dy = dy.to(dev)
+    layer.forward(x, residual=x)
+    g0 = {k: v.clone() for k, v in layer.backward_layer(x, dy).items()}
+    layer.forward(x, residual=x, train=True)
+    g1 = layer.backward_layer(x, dy)
+    torch.cuda.synchronize()
+    assert layer.device_error() == 0
+    for k in g0:
+        assert torch.equal(g0[k], g1[k]), k
