@@ -241,7 +241,9 @@ static int routed_bwd_front(const RoutedBwd& R, const float* dz, float* dgate, f
                               reinterpret_cast<const float*>(R.pk + R.P.gamma), dz, D.T, D.K, D.L,
                               D.eps, reinterpret_cast<bf*>(R.bw + R.B.dout), dgate,
                               reinterpret_cast<float*>(R.bw + R.B.u),
-                              reinterpret_cast<float*>(R.bw + R.B.r), R.stream);
+                              reinterpret_cast<float*>(R.bw + R.B.r),
+                              reinterpret_cast<uint32_t*>(R.ws + R.W.err), wait_limit_ns(),
+                              R.stream);
   if (rc != LMOE_OK) return rc;
   return launch_dgamma(dz, reinterpret_cast<const float*>(R.bw + R.B.u),
                        reinterpret_cast<const float*>(R.bw + R.B.r), D.T, D.L,

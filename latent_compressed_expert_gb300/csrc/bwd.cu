@@ -13,6 +13,7 @@
 // held fixed.
 #include "common.cuh"
 #include "kernels.cuh"
+#include "ptx.cuh"
 
 namespace lmoe {
 
@@ -57,37 +58,75 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
 
 // One CTA per token: u and r exactly as the forward's combine computed them (fp32 fma in
 // slot order, the same tree for the sum of squares), then du, do_j (bf16, at the permuted
-// row of (t, j)) and dg_j; u and r are kept for dgamma.
+// row of (t, j)) and dg_j; u and r are kept for dgamma.  STAGED: the token's K expert-output
+// rows are first copied into shared memory (bulk copies on one mbarrier, a bounded wait;
+// on time-out the CTA records the error bit and writes nothing), and both passes over them
+// read shared memory; else both read global memory.
+constexpr int BWD_BULK_MAX = 114688;  // bytes of staged rows per CTA (16 x 3584 bf16)
+
+template <bool STAGED, int VEC>  // VEC: 8-feature vectors per thread
 __global__ void __launch_bounds__(BWD_THREADS)
 combine_bwd_kernel(const __nv_bfloat16* __restrict__ o, const float* __restrict__ gate,
                    const int32_t* __restrict__ inv, const float* __restrict__ gamma,
                    const float* __restrict__ dz, int K, int L, float eps,
                    __nv_bfloat16* __restrict__ dout, float* __restrict__ dgate,
-                   float* __restrict__ u_out, float* __restrict__ r_out) {
+                   float* __restrict__ u_out, float* __restrict__ r_out,
+                   uint32_t* __restrict__ err, unsigned long long timeout_ns) {
+  extern __shared__ __align__(128) uint8_t cbw_smem[];
   __shared__ int32_t rows[32];
   __shared__ float gates[32];
   __shared__ float red[33];
-  __shared__ float dgs[32][33];
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  const int t = blockIdx.x;
+  if (STAGED && threadIdx.x == 0) {
+    ptx::mbar_init(&bar, 1);
+    ptx::fence_mbar_init();
+    abort_flag = 0;
+  }
+  __syncthreads();
   pdl_wait();
   pdl_launch_dependents();
-  const int t = blockIdx.x;
+  const uint32_t row_bytes = static_cast<uint32_t>(L) * 2;
   if (threadIdx.x < K) {
     rows[threadIdx.x] = __ldg(inv + static_cast<size_t>(t) * K + threadIdx.x);
     gates[threadIdx.x] = __ldg(gate + static_cast<size_t>(t) * K + threadIdx.x);
   }
   __syncthreads();
+  if (STAGED && threadIdx.x == 0) {
+    ptx::mbar_arrive_expect_tx(&bar, row_bytes * static_cast<uint32_t>(K));
+    for (int j = 0; j < K; ++j)
+      ptx::bulk_load(cbw_smem + static_cast<size_t>(j) * row_bytes,
+                     o + static_cast<size_t>(rows[j]) * L, row_bytes, &bar);
+  }
   const int nvec = L / 8;
-  float u[BWD_MAX_VEC][8];
+  // slot j's 8-feature vector v
+  auto orow = [&](int j, int v) -> uint4 {
+    if constexpr (STAGED)
+      return reinterpret_cast<const uint4*>(cbw_smem)[static_cast<size_t>(j) * nvec + v];
+    else
+      return __ldg(reinterpret_cast<const uint4*>(o + static_cast<size_t>(rows[j]) * L) + v);
+  };
+  if constexpr (STAGED) {
+    const bool ok = ptx::mbar_wait(&bar, 0u, &abort_flag, timeout_ns);
+    if (!__syncthreads_and(ok ? 1 : 0)) {
+      if (threadIdx.x == 0) atomicOr(err, DEVERR_TIMEOUT_EPILOGUE);
+      // copies still in flight must land before the CTA exits (bounded again)
+      ptx::mbar_wait(&bar, 0u, &abort_flag, timeout_ns);
+      return;
+    }
+  }
+  float u[VEC][8];
   float ss = 0.0f;
 #pragma unroll
-  for (int c = 0; c < BWD_MAX_VEC; ++c) {
+  for (int c = 0; c < VEC; ++c) {
     const int v = threadIdx.x + c * blockDim.x;
 #pragma unroll
     for (int i = 0; i < 8; ++i) u[c][i] = 0.0f;
     if (v < nvec) {
       for (int j = 0; j < K; ++j) {
         float f[8];
-        bf8_to_f(__ldg(reinterpret_cast<const uint4*>(o + static_cast<size_t>(rows[j]) * L) + v), f);
+        bf8_to_f(orow(j, v), f);
 #pragma unroll
         for (int i = 0; i < 8; ++i) u[c][i] = fmaf(gates[j], f[i], u[c][i]);
       }
@@ -98,9 +137,9 @@ combine_bwd_kernel(const __nv_bfloat16* __restrict__ o, const float* __restrict_
   const float r = rsqrtf(block_sum(ss, red) / static_cast<float>(L) + eps);
   // <u, gamma dz>
   float ua = 0.0f;
-  float a[BWD_MAX_VEC][8];
+  float a[VEC][8];
 #pragma unroll
-  for (int c = 0; c < BWD_MAX_VEC; ++c) {
+  for (int c = 0; c < VEC; ++c) {
     const int v = threadIdx.x + c * blockDim.x;
     if (v < nvec) {
       const float4* dzp = reinterpret_cast<const float4*>(dz + static_cast<size_t>(t) * L) + 2 * v;
@@ -125,7 +164,7 @@ combine_bwd_kernel(const __nv_bfloat16* __restrict__ o, const float* __restrict_
 #pragma unroll
   for (int j = 0; j < 32; ++j) dg[j] = 0.0f;
 #pragma unroll
-  for (int c = 0; c < BWD_MAX_VEC; ++c) {
+  for (int c = 0; c < VEC; ++c) {
     const int v = threadIdx.x + c * blockDim.x;
     if (v < nvec) {
       float du[8];
@@ -135,7 +174,7 @@ combine_bwd_kernel(const __nv_bfloat16* __restrict__ o, const float* __restrict_
       for (int j = 0; j < 32; ++j) {
         if (j < K) {
           float f[8], d[8];
-          bf8_to_f(__ldg(reinterpret_cast<const uint4*>(o + static_cast<size_t>(rows[j]) * L) + v), f);
+          bf8_to_f(orow(j, v), f);
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             d[i] = gates[j] * du[i];
@@ -146,8 +185,11 @@ combine_bwd_kernel(const __nv_bfloat16* __restrict__ o, const float* __restrict_
       }
     }
   }
-  // dg_j: warp sums, then one fixed-order sum over the warps
+  // dg_j: warp sums, then one fixed-order sum over the warps (in the dynamic buffer, which
+  // the staged rows no longer need: 2 CTAs of 112 KB rows fit an SM)
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  float (*dgs)[33] = reinterpret_cast<float (*)[33]>(cbw_smem);
+  if constexpr (STAGED) __syncthreads();
 #pragma unroll
   for (int j = 0; j < 32; ++j) {
     float x = dg[j];
@@ -196,30 +238,35 @@ colsum_final_kernel(const float* __restrict__ part, int L, float* __restrict__ d
 }
 
 // SiTU-GLU backward on the interleaved gate/value layout: row p of pre / dgv holds, for each
-// group of GLU_GROUP features, GLU_GROUP gate then GLU_GROUP value pre-activations.
+// group of GLU_GROUP features, GLU_GROUP gate then GLU_GROUP value pre-activations.  A thread
+// takes 8 consecutive features of one row: 16-byte loads of their gate, value and dh, and
+// 16-byte stores of both gradients.
 __global__ void __launch_bounds__(256)
 situ_bwd_kernel(const __nv_bfloat16* __restrict__ pre, const __nv_bfloat16* __restrict__ dh,
                 int64_t rows, int I, float c, __nv_bfloat16* __restrict__ dgv, int64_t ldo) {
   pdl_wait();
   pdl_launch_dependents();
-  const int64_t n = rows * I;
+  const int per_row = I / 8;
+  const int64_t n = rows * per_row;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t p = i / I;
-    const int f = static_cast<int>(i % I);
-    const int grp = f / GLU_GROUP, w = f % GLU_GROUP;
-    const size_t gi = static_cast<size_t>(p) * 2 * I + grp * 2 * GLU_GROUP + w;
-    const size_t vi = gi + GLU_GROUP;
-    const float g = __bfloat162float(pre[gi]), v = __bfloat162float(pre[vi]);
-    const float d = __bfloat162float(dh[static_cast<size_t>(p) * I + f]);
-    const float tg = tanhf(g / c), tv = tanhf(v / c);
-    const float G = c * tg, V = c * tv;
-    const float s = 1.0f / (1.0f + expf(-G));
-    const float dG = d * V * s * (1.0f + G * (1.0f - s));
-    const float dV = d * G * s;
-    const size_t go = static_cast<size_t>(p) * ldo + grp * 2 * GLU_GROUP + w;
-    dgv[go] = __float2bfloat16_rn(dG * (1.0f - tg * tg));
-    dgv[go + GLU_GROUP] = __float2bfloat16_rn(dV * (1.0f - tv * tv));
+    const int64_t p = i / per_row;
+    const int f = static_cast<int>(i - p * per_row) * 8;  // first feature
+    const int col = (f / GLU_GROUP) * 2 * GLU_GROUP + f % GLU_GROUP;  // its gate column
+    float g[8], v[8], d[8], dg[8], dv[8];
+    bf8_to_f(__ldg(reinterpret_cast<const uint4*>(pre + p * 2 * I + col)), g);
+    bf8_to_f(__ldg(reinterpret_cast<const uint4*>(pre + p * 2 * I + col + GLU_GROUP)), v);
+    bf8_to_f(__ldg(reinterpret_cast<const uint4*>(dh + p * I + f)), d);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const float tg = tanhf(g[k] / c), tv = tanhf(v[k] / c);
+      const float G = c * tg, V = c * tv;
+      const float sg = 1.0f / (1.0f + expf(-G));
+      dg[k] = d[k] * V * sg * (1.0f + G * (1.0f - sg)) * (1.0f - tg * tg);
+      dv[k] = d[k] * G * sg * (1.0f - tv * tv);
+    }
+    *reinterpret_cast<uint4*>(dgv + p * ldo + col) = f_to_bf8(dg);
+    *reinterpret_cast<uint4*>(dgv + p * ldo + col + GLU_GROUP) = f_to_bf8(dv);
   }
 }
 
@@ -362,14 +409,29 @@ int launch_rowmap(int I, int base, int32_t* map, int32_t* seg, int seg_len, cuda
 // ------------------------------------------------------------------------------------
 int launch_combine_bwd(const __nv_bfloat16* o, const float* gate, const int32_t* inv,
                        const float* gamma, const float* dz, int T, int K, int L, float eps,
-                       __nv_bfloat16* dout, float* dgate, float* u, float* r,
-                       cudaStream_t stream) {
+                       __nv_bfloat16* dout, float* dgate, float* u, float* r, uint32_t* err,
+                       unsigned long long timeout_ns, cudaStream_t stream) {
   if (T == 0) return LMOE_OK;
   const int nvec = L / 8;
   const int threads = static_cast<int>(ceil_div(nvec < BWD_THREADS ? nvec : BWD_THREADS, 32) * 32);
   if (nvec > BWD_MAX_VEC * threads || K > 32) return LMOE_ERR_UNSUPPORTED;
-  return launch_pdl(combine_bwd_kernel, T, threads, 0, stream, o, gate, inv, gamma, dz, K, L, eps,
-                    dout, dgate, u, r) == cudaSuccess
+  const size_t dgs_bytes = (BWD_THREADS / 32) * 33 * sizeof(float);
+  const size_t staged = static_cast<size_t>(K) * L * 2;
+  if (staged <= static_cast<size_t>(BWD_BULK_MAX) && nvec <= threads &&
+      !(reinterpret_cast<uintptr_t>(o) & 15)) {
+    // one vector per thread keeps the registers of two 112 KB CTAs within an SM's
+    const size_t smem = staged > dgs_bytes ? staged : dgs_bytes;
+    if (cudaFuncSetAttribute(combine_bwd_kernel<true, 1>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess)
+      return LMOE_ERR_CUDA;
+    return launch_pdl(combine_bwd_kernel<true, 1>, T, threads, smem, stream, o, gate, inv, gamma,
+                      dz, K, L, eps, dout, dgate, u, r, err, timeout_ns) == cudaSuccess
+               ? LMOE_OK
+               : LMOE_ERR_CUDA;
+  }
+  return launch_pdl(combine_bwd_kernel<false, BWD_MAX_VEC>, T, threads, dgs_bytes, stream, o, gate,
+                    inv, gamma, dz, K, L, eps, dout, dgate, u, r, err, timeout_ns) == cudaSuccess
              ? LMOE_OK
              : LMOE_ERR_CUDA;
 }
@@ -387,7 +449,10 @@ int launch_dgamma(const float* dz, const float* u, const float* r, int T, int L,
 int launch_situ_bwd(const __nv_bfloat16* pre, const __nv_bfloat16* dh, int64_t rows, int I,
                     float c, __nv_bfloat16* dgv, int64_t ldo, cudaStream_t stream) {
   if (rows == 0) return LMOE_OK;
-  const int64_t n = rows * I;
+  if (I % GLU_GROUP || ldo % 8 || (reinterpret_cast<uintptr_t>(pre) & 15) ||
+      (reinterpret_cast<uintptr_t>(dh) & 15) || (reinterpret_cast<uintptr_t>(dgv) & 15))
+    return LMOE_ERR_UNSUPPORTED;
+  const int64_t n = rows * (I / 8);
   const unsigned grid = static_cast<unsigned>(ceil_div(n, 256) < 65535 * 16 ? ceil_div(n, 256) : 65535 * 16);
   return launch_pdl(situ_bwd_kernel, grid, 256, 0, stream, pre, dh, rows, I, c, dgv, ldo) ==
                  cudaSuccess

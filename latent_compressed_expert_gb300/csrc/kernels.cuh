@@ -154,7 +154,8 @@ int launch_pack_backward(const lmoe_dims& D, const lmoe_weights& w, __nv_bfloat1
 // Backward of the routed branch (bwd.cu).
 int launch_combine_bwd(const __nv_bfloat16* o, const float* gate, const int32_t* inv,
                        const float* gamma, const float* dz, int T, int K, int L, float eps,
-                       __nv_bfloat16* dout, float* dgate, float* u, float* r, cudaStream_t stream);
+                       __nv_bfloat16* dout, float* dgate, float* u, float* r, uint32_t* err,
+                       unsigned long long timeout_ns, cudaStream_t stream);
 int launch_dgamma(const float* dz, const float* u, const float* r, int T, int L, float* part,
                   float* dgamma, cudaStream_t stream);
 int launch_situ_bwd(const __nv_bfloat16* pre, const __nv_bfloat16* dh, int64_t rows, int I,
