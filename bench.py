@@ -597,9 +597,10 @@ def run_backward(args):
     flop = 12.0 * TK * L * I
     grad_bytes = 4.0 * E * 3 * I * L
     if whole:
-        # dz/dhs, dx, router dgrad, shared recompute; dW_out, dW_in, dW_router
+        # dz/dhs and dW_out, dx and dW_in, router dgrad and dW_router (the training forward
+        # keeps the shared experts' pre-activations too)
         flop += 2.0 * T * d * (L + sw) * 2 + 2.0 * T * (L + 2 * sw) * d * 2 \
-            + 2.0 * T * E * L * 2 + 2.0 * T * d * 2 * sw
+            + 2.0 * T * E * L * 2
         grad_bytes += 4.0 * (d * (L + sw) + (L + 2 * sw) * d + E * L)
     peaks, _ = load_peaks()
     what = "layer" if whole else "routed-branch"

@@ -150,6 +150,9 @@ typedef struct lmoe_io {
                             experts' gate/value pre-activations here (slot order; per slot,
                             groups of 16 gate then 16 value features), so that the backward
                             need not recompute them.  bf16 routed experts only. */
+  void *save_pre_shared; /* [T, 2 S Is] bf16, or NULL: likewise the shared experts'
+                            pre-activations (per token, groups of 16 gate then 16 value
+                            features over the S Is concatenated features) */
 } lmoe_io;
 
 /* lmoe_io.phase.  The layer splits where its only cross-batch quantity, the thresholds, is
@@ -349,14 +352,15 @@ int lmoe_routed_backward(const lmoe_dims *dims, const void *packed, const void *
  * (thresholds and top-K) is held fixed.  logits: the fp32 [T, E] router logits the forward
  * routed on -- required when the forward was given lmoe_io.logits_in, else NULL (the ones
  * it computed into the workspace).  x: the forward's input [T, d] bf16.  pre: as for
- * lmoe_routed_backward.
+ * lmoe_routed_backward; pre_shared: the forward's lmoe_io.save_pre_shared buffer, or NULL
+ * (the shared experts' pre-activations are then recomputed from x).
  * bwd_ws: lmoe_backward_workspace_bytes of device scratch.  bf16 routed experts only.
  * Errors: INVALID_ARG (null or misaligned pointers), UNSUPPORTED (expert_fp8),
  * WORKSPACE_TOO_SMALL, CUDA. */
 size_t lmoe_backward_workspace_bytes(const lmoe_dims *dims);
 int lmoe_backward(const lmoe_dims *dims, const void *packed, const void *packed_bwd,
                   void *workspace, size_t ws_bytes, const void *x, const float *logits,
-                  const void *dy, const void *pre, float *dx, float *dgamma, float *dw_in, float *dw_router,
+                  const void *dy, const void *pre, const void *pre_shared, float *dx, float *dgamma, float *dw_in, float *dw_router,
                   float *dw_gu, float *dw_ed, float *dw_out, void *bwd_ws, size_t bwd_ws_bytes,
                   void *stream);
 

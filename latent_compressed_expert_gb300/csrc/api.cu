@@ -618,7 +618,8 @@ size_t lmoe_backward_workspace_bytes(const lmoe_dims* dims) {
 
 int lmoe_backward(const lmoe_dims* dims, const void* packed, const void* packed_bwd,
                   void* workspace, size_t ws_bytes, const void* x, const float* logits,
-                  const void* dy, const void* pre, float* dx, float* dgamma, float* dw_in,
+                  const void* dy, const void* pre, const void* pre_shared, float* dx,
+                  float* dgamma, float* dw_in,
                   float* dw_router,
                   float* dw_gu, float* dw_ed, float* dw_out, void* bwd_ws, size_t bwd_ws_bytes,
                   void* stream_) {
@@ -631,7 +632,8 @@ int lmoe_backward(const lmoe_dims* dims, const void* packed, const void* packed_
     return LMOE_ERR_INVALID_ARG;
   const void* ptrs[] = {packed, packed_bwd, workspace, x, dy, dx, dgamma, dw_in, dw_router,
                         dw_gu, dw_ed, dw_out, bwd_ws};
-  if (pre && !aligned16(pre)) return LMOE_ERR_INVALID_ARG;
+  if ((pre && !aligned16(pre)) || (pre_shared && !aligned16(pre_shared)))
+    return LMOE_ERR_INVALID_ARG;
   for (const void* p : ptrs)
     if (!aligned16(p)) return LMOE_ERR_INVALID_ARG;
   RoutedBwd R{};
@@ -725,11 +727,17 @@ int lmoe_backward(const lmoe_dims* dims, const void* packed, const void* packed_
   if ((rc = routed_bwd_back(R, dlat_r, reinterpret_cast<float*>(bw + LB.dlat), dcat, wc, dw_gu,
                             dw_ed)) != LMOE_OK)
     return rc;
-  // 5. shared experts: gate/value pre-activations again, SiTU backward into dcat[:, L:]
+  // 5. shared experts: gate/value pre-activations (the forward's, or computed again), SiTU
+  // backward into dcat[:, L:]
   if (sw > 0) {
-    if ((rc = dense(xb, T, d, pk + R.P.w1 + static_cast<size_t>(L) * d * 2, 2 * sw, d, d,
-                    EPI_BF16, pre_s, 2 * sw)) != LMOE_OK ||
-        (rc = launch_situ_bwd(pre_s, dhs, T, sw, D.c, dcat + L, wc, stream)) != LMOE_OK)
+    const bf* pre_sh = static_cast<const bf*>(pre_shared);
+    if (!pre_sh) {
+      if ((rc = dense(xb, T, d, pk + R.P.w1 + static_cast<size_t>(L) * d * 2, 2 * sw, d, d,
+                      EPI_BF16, pre_s, 2 * sw)) != LMOE_OK)
+        return rc;
+      pre_sh = pre_s;
+    }
+    if ((rc = launch_situ_bwd(pre_sh, dhs, T, sw, D.c, dcat + L, wc, stream)) != LMOE_OK)
       return rc;
   }
   // 6. dx = [dlat | dgv_shared] . [W_down ; W_shared_gate/value]
@@ -788,6 +796,7 @@ int lmoe_forward(const lmoe_dims* dims, const void* packed, const void* x, const
     return LMOE_ERR_INVALID_ARG;
   if (opt.tau_ema && !(opt.ema_beta >= 0.0f && opt.ema_beta <= 1.0f)) return LMOE_ERR_INVALID_ARG;
   if (opt.save_pre && (D.expert_fp8 || !aligned16(opt.save_pre))) return LMOE_ERR_INVALID_ARG;
+  if (opt.save_pre_shared && !aligned16(opt.save_pre_shared)) return LMOE_ERR_INVALID_ARG;
 
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   using bf = __nv_bfloat16;
@@ -849,6 +858,8 @@ int lmoe_forward(const lmoe_dims* dims, const void* packed, const void* x, const
     g.ld0 = D.L;
     g.out1 = zh + D.L;
     g.ld1 = ldz;
+    g.pre = static_cast<bf*>(opt.save_pre_shared);
+    g.ldp = 2 * sw;
     g.inject_stall = inject_stall() ? 1 : 0;
     rc = launch_gemm(x, T, D.d, pk + P.w1, static_cast<uint64_t>(g.N), D.d, g, stream);
     if (rc != LMOE_OK) return rc;
@@ -868,6 +879,8 @@ int lmoe_forward(const lmoe_dims* dims, const void* packed, const void* x, const
       g.epi = EPI_SITU;
       g.out1 = zh + D.L;
       g.ld1 = ldz;
+      g.pre = static_cast<bf*>(opt.save_pre_shared);
+      g.ldp = 2 * sw;
       g.max_ctas = shared_ctas;
       rc = launch_gemm(x, T, D.d, pk + P.w1 + static_cast<size_t>(D.L) * D.d * 2,
                        static_cast<uint64_t>(2 * sw), D.d, g, aux);

@@ -167,13 +167,16 @@ __device__ __forceinline__ void epilogue_store(const GemmArgs& g, int row, int c
       break;
     }
     case EPI_SITU:
+      if (g.pre) store_bf16x32(g.pre + r * g.ldp + col0, v);
       store_situ16(g.out1 + r * g.ld1 + col0 / 2, v, c, inv_c);
       break;
     case EPI_SPLIT:
-      if (col0 < g.split)
+      if (col0 < g.split) {
         store_bf16x32(g.out0 + r * g.ld0 + col0, v);
-      else
+      } else {
+        if (g.pre) store_bf16x32(g.pre + r * g.ldp + (col0 - g.split), v);
         store_situ16(g.out1 + r * g.ld1 + (col0 - g.split) / 2, v, c, inv_c);
+      }
       break;
     case EPI_RESID:
     default: {
@@ -566,6 +569,9 @@ static int launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArg
 int launch_gemm(const void* A, uint64_t a_rows, int a_ld, const void* B, uint64_t b_rows,
                 int b_ld, const GemmArgs& g, cudaStream_t stream) {
   if (g.groups > 0 && (g.epi != EPI_F32 || !g.kseg)) return LMOE_ERR_INVALID_ARG;
+  if (g.pre && ((g.epi != EPI_SITU && g.epi != EPI_SPLIT) || g.ldp % 8 ||
+                (reinterpret_cast<uintptr_t>(g.pre) & 15u)))
+    return LMOE_ERR_INVALID_ARG;
   if (g.groups == 0 && (g.Kd % BLOCK_K != 0 || g.Kd <= 0)) return LMOE_ERR_UNSUPPORTED;
   if (g.N <= 0) return LMOE_ERR_UNSUPPORTED;
   const bool glu = g.epi == EPI_SITU || g.epi == EPI_SPLIT;

@@ -51,6 +51,8 @@ struct GemmArgs {
   int ldr;
   const float* addf;      // EPI_RESID: optional fp32 addend addf[r * lda + c]
   int lda;
+  __nv_bfloat16* pre;     // EPI_SITU / EPI_SPLIT: optional bf16 copy of the gate/value
+  int ldp;                // pre-activations, pre[r * ldp + c] (EPI_SPLIT: c - split)
   int max_ctas;           // persistent grid limit (0: one CTA per SM)
   float c;                // SiTU cap
   uint32_t* err;          // device error flag (never null)

@@ -43,7 +43,7 @@ class IO(ctypes.Structure):
                 ("aux_stream", _vp), ("aux_events", _vp * 2), ("shared_sms", _i),
                 ("phase", _i), ("cand_out", _vp), ("cand_k", _i),
                 ("tau_ema", _vp), ("ema_beta", _f), ("ema_first", _i), ("load_stats", _vp),
-                ("save_pre", _vp)]
+                ("save_pre", _vp), ("save_pre_shared", _vp)]
 
 
 OVERLAP_MIN_T = 512  # LMOE_OVERLAP_MIN_T
@@ -71,7 +71,7 @@ SIGNATURES = {
                                         _sz, _vp]),
     "lmoe_backward_workspace_bytes": (_sz, [ctypes.POINTER(Dims)]),
     "lmoe_backward": (_i, [ctypes.POINTER(Dims), _vp, _vp, _vp, _sz, _vp, _vp, _vp, _vp, _vp,
-                           _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+                           _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "lmoe_routed_backward_workspace_bytes": (_sz, [ctypes.POINTER(Dims)]),
     "lmoe_routed_backward": (_i, [ctypes.POINTER(Dims), _vp, _vp, _vp, _sz, _vp, _vp, _vp, _vp,
                                   _vp, _vp, _vp, _vp, _sz, _vp]),
@@ -451,6 +451,8 @@ class Layer:
             if getattr(self, "pre_buf", None) is None:
                 raise RuntimeError("lmoe: forward(train=True) needs enable_backward() first")
             io.save_pre = _ptr(self.pre_buf)
+            if self.pre_shared_buf is not None:
+                io.save_pre_shared = _ptr(self.pre_shared_buf)
             self._pre_rows = T
         if debug:
             dev = x.device
@@ -542,6 +544,8 @@ class Layer:
         sh = self.shape
         self.pre_buf = torch.empty((self.max_tokens * sh.K, 2 * sh.I), dtype=torch.bfloat16,
                                    device=self.device)
+        self.pre_shared_buf = None if sh.S == 0 else torch.empty(
+            (self.max_tokens, 2 * sh.S * sh.Is), dtype=torch.bfloat16, device=self.device)
         self.bwd_ws = torch.empty(self.bwd_bytes, dtype=torch.uint8, device=self.device)
 
     def backward_launches(self, T: int) -> int:
@@ -551,12 +555,12 @@ class Layer:
         map and two grouped weight-gradient GEMMs."""
         return 12 + (0 if getattr(self, "_pre_rows", None) == T else 1)
 
-    def _saved_pre(self, T: int):
-        """The pre-activations kept by the last forward, if it was a training step of T
-        tokens; else None (the backward recomputes them)."""
-        if getattr(self, "_pre_rows", None) == T:
-            return _ptr(self.pre_buf)
-        return None
+    def _saved_pre(self, T: int, shared: bool = False):
+        """The routed (or shared) experts' pre-activations kept by the last forward, if it
+        was a training step of T tokens; else None (the backward recomputes them)."""
+        if getattr(self, "_pre_rows", None) != T:
+            return None
+        return _ptr(self.pre_shared_buf if shared else self.pre_buf)
 
     def backward(self, dz: torch.Tensor, stream=None) -> dict:
         """Gradients of the routed branch for the batch of the last ``forward`` call
@@ -586,9 +590,12 @@ class Layer:
     def layer_backward_launches(self, T: int) -> int:
         """Kernels one lmoe_backward call launches: the routed branch's, plus the row map of
         dw_in, the dz GEMM, router backward and its GEMM, the dx GEMM and three
-        weight-gradient GEMMs; with shared experts also the dhs GEMM, their pre-activation
-        GEMM and their SiTU backward."""
-        return self.backward_launches(T) + 8 + (3 if self.shape.S > 0 else 0)
+        weight-gradient GEMMs; with shared experts also the dhs GEMM and their SiTU backward,
+        and their pre-activation GEMM unless the last forward was a training step."""
+        shared = 0
+        if self.shape.S > 0:
+            shared = 2 + (0 if getattr(self, "_pre_rows", None) == T else 1)
+        return self.backward_launches(T) + 8 + shared
 
     def backward_layer(self, x: torch.Tensor, dy: torch.Tensor, logits=None,
                        stream=None) -> dict:
@@ -619,7 +626,8 @@ class Layer:
         bwd_bytes = int(load().lmoe_backward_workspace_bytes(ctypes.byref(dims)))
         _check(load().lmoe_backward(
             ctypes.byref(dims), _ptr(self.packed), _ptr(self.packed_bwd), _ptr(self.workspace),
-            self.ws_bytes, _ptr(x), _ptr(logits), _ptr(dy), self._saved_pre(T), _ptr(out["dx"]),
+            self.ws_bytes, _ptr(x), _ptr(logits), _ptr(dy), self._saved_pre(T),
+            self._saved_pre(T, shared=True), _ptr(out["dx"]),
             _ptr(out["dgamma"]), _ptr(out["dw_in"]), _ptr(out["dw_router"]), _ptr(out["dw_gu"]),
             _ptr(out["dw_edown"]), _ptr(out["dw_out"]), _ptr(self.bwd_ws), bwd_bytes,
             _stream(stream)), "lmoe_backward")

@@ -229,14 +229,14 @@ def test_backward_argument_checks(lib):
     f = lib.lmoe_backward
 
     def call(dims=d, x=fake, dy=fake, ws_bytes=ws, bw_bytes=bw, dx=fake):
-        return f(ctypes.byref(dims), fake, fake, fake, ws_bytes, x, None, dy, None, dx, fake,
-                 fake, fake, fake, fake, fake, fake, bw_bytes, None)
+        return f(ctypes.byref(dims), fake, fake, fake, ws_bytes, x, None, dy, None, None, dx,
+                 fake, fake, fake, fake, fake, fake, fake, bw_bytes, None)
 
     assert call(x=None) == lmoe.LMOE_ERR_INVALID_ARG
     assert call(dy=None) == lmoe.LMOE_ERR_INVALID_ARG
     assert call(dx=ctypes.c_void_p(0x1004)) == lmoe.LMOE_ERR_INVALID_ARG   # misaligned
     assert f(ctypes.byref(d), fake, fake, fake, ws, fake, None, fake, ctypes.c_void_p(0x1002),
-             fake, fake, fake, fake, fake, fake, fake, fake, bw, None) \
+             None, fake, fake, fake, fake, fake, fake, fake, fake, bw, None) \
         == lmoe.LMOE_ERR_INVALID_ARG                                          # pre misaligned
     assert call(bw_bytes=bw - 1) == lmoe.LMOE_ERR_WORKSPACE_TOO_SMALL
     assert call(ws_bytes=ws - 1) == lmoe.LMOE_ERR_WORKSPACE_TOO_SMALL
