@@ -36,8 +36,9 @@ def _bf16_values(w) -> torch.Tensor:
     return torch.from_numpy((u.astype(np.uint32) << 16).view(np.float32).astype(np.float64))
 
 
-def routed_forward_t(lat, idx, gate, wg, wv, wed, gamma, c=100.0, eps=1e-6):
-    """The branch in float64 torch ops (differentiable in lat, gate, gamma and weights)."""
+def routed_forward_t(lat, idx, gate, wg, wv, wed, gamma, c=100.0, eps=1e-6, keep=None):
+    """The branch in float64 torch ops (differentiable in lat, gate, gamma and weights).
+    keep: a dict that receives the expert outputs "o" [n, K, L] and their gated sum "u"."""
     n, K = idx.shape
     E, I, L = wg.shape
     idx_t = torch.as_tensor(np.asarray(idx), dtype=torch.long)
@@ -48,6 +49,8 @@ def routed_forward_t(lat, idx, gate, wg, wv, wed, gamma, c=100.0, eps=1e-6):
     h = gc * torch.sigmoid(gc) * vc
     o = torch.einsum("tki,tkli->tkl", h, wed[idx_t])
     u = (gate.unsqueeze(-1) * o).sum(1)
+    if keep is not None:
+        keep["o"], keep["u"] = o, u
     r = torch.rsqrt((u * u).mean(-1, keepdim=True) + eps)
     return gamma * u * r
 
@@ -83,7 +86,7 @@ def _situ(g, v, c):
     return gc * torch.sigmoid(gc) * (c * torch.tanh(v / c))
 
 
-def layer_forward_t(x, idx, w: dict, c=100.0, eps=1e-6, gate=None):
+def layer_forward_t(x, idx, w: dict, c=100.0, eps=1e-6, gate=None, keep=None):
     """The whole layer without its residual term, in float64 torch ops, with routing held at
     ``idx`` (the forward oracle's ``latent``, ``router_logits``, ``route``, ``routed``,
     ``shared`` and ``output``):
@@ -92,15 +95,18 @@ def layer_forward_t(x, idx, w: dict, c=100.0, eps=1e-6, gate=None):
         z = routed branch (see the module docstring),
         hs_s = SiTU-GLU(x W_sg[s]^T, x W_sv[s]^T),  y = z W_up^T + sum_s hs_s W_sd[s]^T.
     ``gate`` replaces the computed gates when given (to pin the rest of the restatement to
-    the C oracle, which takes fp32 gates).  Returns (y, {"lat", "logits", "gate", "z"})."""
+    the C oracle, which takes fp32 gates).  keep: as for ``routed_forward_t``, plus the
+    selected experts' scores "s".  Returns (y, {"lat", "logits", "gate", "z"})."""
     idx_t = torch.as_tensor(np.asarray(idx), dtype=torch.long)
     lat = x @ w["w_down"].T
     logits = lat @ w["w_router"].T
+    s = torch.sigmoid(torch.gather(logits, 1, idx_t))
     if gate is None:
-        s = torch.sigmoid(torch.gather(logits, 1, idx_t))
         gate = s / s.sum(1, keepdim=True)
+    if keep is not None:
+        keep["s"] = s
     z = routed_forward_t(lat, idx, gate, w["w_gate"], w["w_value"], w["w_edown"], w["gamma"],
-                         c, eps)
+                         c, eps, keep)
     y = z @ w["w_up"].T
     if w["w_sgate"].shape[0] > 0:
         G = torch.einsum("td,sid->tsi", x, w["w_sgate"])
@@ -113,17 +119,28 @@ LAYER_WEIGHTS = ("w_down", "w_router", "w_gate", "w_value", "w_edown", "w_up", "
                  "w_svalue", "w_sdown")
 
 
-def layer_backward(x, idx, w: dict, dy, c=100.0, eps=1e-6) -> dict:
+def layer_backward(x, idx, w: dict, dy, c=100.0, eps=1e-6, intermediates=False) -> dict:
     """Gradients of sum(dy * y) for the layer (``layer_forward_t``) with respect to x (through
     the latent and the shared experts; the residual adds dy itself), gamma and every weight,
     in float64: keys dx, dgamma and "d" + weight name (dw_down [L, d], dw_router [E, L],
     dw_gate, dw_value, dw_edown, dw_up [d, L], dw_sgate, dw_svalue, dw_sdown); "y" is the
-    forward value.  x, dy: [n, d]; weights bf16 tensors or bit arrays, gamma fp32."""
+    forward value.  x, dy: [n, d]; weights bf16 tensors or bit arrays, gamma fp32.
+    intermediates: also return du (dLoss/du, u the gated sum of the expert outputs), o, the
+    selected scores s, the gates and the latent, for error bounds."""
     xt = _f64(x).requires_grad_(True)
     wt = {k: _f64(w[k]).requires_grad_(True) for k in LAYER_WEIGHTS + ("gamma",)}
-    y, _ = layer_forward_t(xt, idx, wt, c, eps)
+    keep = {} if intermediates else None
+    y, parts = layer_forward_t(xt, idx, wt, c, eps, keep=keep)
+    if intermediates:
+        keep["u"].retain_grad()
     y.backward(torch.as_tensor(np.asarray(dy, dtype=np.float64)))
     out = {"y": y.detach().numpy(), "dx": xt.grad.numpy(), "dgamma": wt["gamma"].grad.numpy()}
+    if intermediates:
+        # for error bounds: du = dLoss/du, the expert outputs o, scores s, gates, latent
+        out.update({"du": keep["u"].grad.numpy(), "o": keep["o"].detach().numpy(),
+                    "s": keep["s"].detach().numpy(),
+                    "gate": parts["gate"].detach().numpy(),
+                    "lat": parts["lat"].detach().numpy()})
     for k in LAYER_WEIGHTS:
         g = wt[k].grad  # None for weights the forward does not reach (no shared experts)
         out["d" + k] = g.numpy() if g is not None else np.zeros(tuple(wt[k].shape))

@@ -8,7 +8,11 @@ fp32.  A gradient element is a sum of n products of two such operands (n: an exp
 for the weights, L or 2I features for the latent), so its error is at most ~2^-8 sum|terms|,
 which under sign cancellation is ~sqrt(n) times the element's typical size: per tensor the
 mean relative error is at most 1.5e-2, the RMS error at most 2.5e-2 of the tensor's RMS, and
-the largest element error at most 0.15 of it (the tail at n ~ 30-150)."""
+the largest element error at most 0.15 of it (the tail at n ~ 30-150).  With one or two
+tokens per expert an element is a single product, with no sum to average its error, and
+the gradient is a heavy-tailed outer product (largest element 15-40 times the RMS): there
+the largest error is bounded by a single product's, 2^-7 of itself, with a factor 2 of
+margin: max(0.15 RMS, 2^-6 of the largest magnitude)."""
 import numpy as np
 import pytest
 import torch
@@ -20,6 +24,7 @@ pytestmark = pytest.mark.gpu
 MEAN_REL = 1.5e-2
 RMS_REL = 2.5e-2
 MAX_REL_RMS = 0.15
+MAX_REL_PEAK = 2.0 ** -6
 
 
 @pytest.fixture(scope="module")
@@ -38,13 +43,14 @@ def _stats(got, ref):
     err = np.abs(got - ref)
     rms = float(np.sqrt(np.mean(ref * ref)))
     return {"finite": bool(np.all(np.isfinite(got))), "max_over_rms": float(err.max() / rms),
+            "max_over_peak": float(err.max() / np.abs(ref).max()),
             "rms_rel": float(np.sqrt(np.mean(err * err)) / rms),
             "mean_rel": float(err.sum() / np.abs(ref).sum())}
 
 
 def _ok(s):
     return (s["finite"] and s["mean_rel"] <= MEAN_REL and s["rms_rel"] <= RMS_REL
-            and s["max_over_rms"] <= MAX_REL_RMS)
+            and (s["max_over_rms"] <= MAX_REL_RMS or s["max_over_peak"] <= MAX_REL_PEAK))
 
 
 @pytest.mark.parametrize("shape", [
@@ -81,13 +87,43 @@ def test_routed_backward_matches_oracle(dev, oracle_mod, shape):
         assert float(g["dw_edown"][torch.as_tensor(unused)].abs().max()) == 0.0
 
 
-LAYER_KEYS = ("dx", "dgamma", "dw_down", "dw_router", "dw_gate", "dw_value", "dw_edown", "dw_up",
+LAYER_KEYS = ("dx", "dgamma", "dw_down", "dw_gate", "dw_value", "dw_edown", "dw_up",
               "dw_sgate", "dw_svalue", "dw_sdown")
+EXPERT_KEYS = ("dw_gate", "dw_value", "dw_edown")
+
+
+def _router_sigma(ref, idx, E):
+    """Standard deviation of the rounding error of each router weight-gradient element,
+    dW_r = sum_t dlogit[t]^T lat[t] with dlogit_j = (dg_j - sum_i g_i dg_i) / S * s_j (1 - s_j)
+    and dg_j = <du, o_j>.  The device computes dg_j from bf16 expert outputs o (and a du
+    that inherits their rounding): independent errors of at most 2^-9 relative per term,
+    whose variances add, so sd(dg_j) <= 2^-8 sqrt(sum_l (du_l o_jl)^2) with margin.  They
+    propagate through the normalisation (where the difference may cancel, which is why a
+    tensor-wide ratio does not bound this gradient at a few tokens) and, with the bf16
+    stores of dlogit and of the latent (2^-8 each, with margin), through the token sum."""
+    du, o, s, g, lat = ref["du"], ref["o"], ref["s"], ref["gate"], ref["lat"]
+    sd_dg = 2.0 ** -8 * np.sqrt(np.einsum("tl,tjl->tj", du * du, o * o))
+    dg = np.einsum("tl,tjl->tj", du, o)
+    S = s.sum(1, keepdims=True)
+    dl = (dg - (g * dg).sum(1, keepdims=True)) / S * s * (1.0 - s)
+    sd_dl = np.sqrt((s * (1.0 - s) / S) ** 2 * (sd_dg ** 2 + (g * g * sd_dg ** 2).sum(1, keepdims=True))
+                    + (2.0 ** -8 * dl) ** 2)
+    T = idx.shape[0]
+    sd_mat = np.zeros((T, E))
+    dl_mat = np.zeros((T, E))
+    rows = np.repeat(np.arange(T), idx.shape[1])
+    sd_mat[rows, idx.ravel()] = sd_dl.ravel()
+    dl_mat[rows, idx.ravel()] = dl.ravel()
+    return np.sqrt((sd_mat ** 2).T @ lat ** 2 + 2.0 ** -16 * (dl_mat ** 2).T @ lat ** 2)
 
 
 @pytest.mark.parametrize("shape", [
     synth.LayerShape("b1", T=256, d=512, L=256, E=32, K=4, I=128, S=2, Is=128),
     synth.LayerShape("b2", T=300, d=512, L=384, E=16, K=6, I=192, S=0, Is=0),  # ragged tiles
+    # one token, and seven: most experts get no rows, every segment and the dense weight
+    # gradients' single K-block are partial
+    synth.LayerShape("b_t1", T=1, d=512, L=256, E=32, K=4, I=128, S=2, Is=128),
+    synth.LayerShape("b_t7", T=7, d=512, L=256, E=32, K=4, I=128, S=2, Is=128),
 ])
 def test_layer_backward_matches_oracle(dev, oracle_mod, shape):
     """lmoe_backward against the oracle's whole-layer backward.  The GPU routes on the
@@ -110,10 +146,22 @@ def test_layer_backward_matches_oracle(dev, oracle_mod, shape):
     g = layer.backward_layer(xd, dy.to(dev), logits=logits)
     torch.cuda.synchronize()
     assert layer.device_error() == 0
-    ref = B.layer_backward(x, r.idx, w, dy.double().numpy())
-    keys = [k for k in LAYER_KEYS if ref[k].size > 0]
-    stats = {k: _stats(g[k].cpu().numpy(), ref[k]) for k in keys}
-    assert all(_ok(v) for v in stats.values()), (sh.name, stats)
+    ref = B.layer_backward(x, r.idx, w, dy.double().numpy(), intermediates=True)
+    # experts no token chose have exactly zero gradients; the statistics cover the others
+    # (at a few tokens most experts are idle, and their zeros would dilute the RMS)
+    used = np.unique(r.idx)
+    idle = np.setdiff1d(np.arange(sh.E), used)
+    got = {k: g[k].cpu().numpy() for k in LAYER_KEYS + ("dw_router",) if ref[k].size > 0}
+    for k in EXPERT_KEYS + ("dw_router",):
+        assert np.all(got[k][idle] == 0.0), k
+    stats = {k: _stats(got[k][used] if k in EXPERT_KEYS else got[k],
+                       ref[k][used] if k in EXPERT_KEYS else ref[k])
+             for k in LAYER_KEYS if ref[k].size > 0}
+    bad = {k: v for k, v in stats.items() if not _ok(v)}
+    assert not bad, (sh.name, bad)
+    # the router's gradient: every element within 6 standard deviations of its rounding
+    excess = np.abs(got["dw_router"] - ref["dw_router"]) - 6.0 * _router_sigma(ref, r.idx, sh.E)
+    assert excess.max() <= 1e-6 * np.abs(ref["dw_router"]).max(), (sh.name, excess.max())
 
 
 def test_saved_pre_activations_match_recompute(dev):
