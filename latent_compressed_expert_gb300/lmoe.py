@@ -553,7 +553,7 @@ class Layer:
         dgamma passes, two grouped dgrad GEMMs (and the pre-activation GEMM when the last
         forward was not a training step), SiTU backward, slot sum, latent row gather, row
         map and two grouped weight-gradient GEMMs."""
-        return 12 + (0 if getattr(self, "_pre_rows", None) == T else 1)
+        return 11 + (0 if getattr(self, "_pre_rows", None) == T else 1)
 
     def _saved_pre(self, T: int, shared: bool = False):
         """The routed (or shared) experts' pre-activations kept by the last forward, if it
