@@ -536,11 +536,15 @@ def run_ours(args):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         wh = host_weights(w)
         xh = x.cpu()
-        rate, dt, cores = time_oracle(sh, wh, xh, args.cpu_tokens)
+        n = args.cpu_tokens
+        if n <= 0:
+            # a bounded sample: about --cpu-seconds of host work, sized from a short probe
+            probe, _, _ = time_oracle(sh, wh, xh, 64)
+            n = int(min(T, max(64, probe * args.cpu_seconds)))
+        rate, dt, cores = time_oracle(sh, wh, xh, n)
         line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
-                                "sample": f"{args.cpu_tokens} of the {T} tokens through the whole "
-                                          f"layer (fp64), thresholds over that sub-batch; "
-                                          f"{dt:.1f} s"}
+                                "sample": f"{n} of the {T} tokens through the whole layer "
+                                          f"(fp64), thresholds over that sub-batch; {dt:.1f} s"}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -699,8 +703,10 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--shape", choices=sorted(SHAPES) + ["ep"], default="prefill",
                     help="workload (prefill is the headline; the others are extra lines)")
-    ap.add_argument("--cpu-tokens", type=int, default=128,
-                    help="tokens in the timed CPU-oracle sample")
+    ap.add_argument("--cpu-tokens", type=int, default=0,
+                    help="tokens in the timed CPU-oracle sample (0: sized by --cpu-seconds)")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="host time the CPU-oracle sample aims at")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--overlap", action="store_true",
                     help="run the shared experts on a second stream beside the routed path")
