@@ -256,8 +256,10 @@ SMALL = synth.LayerShape("small", T=1024, d=7168, L=3584, E=128, K=16, I=512, S=
 ROUTING = synth.LayerShape("routing", T=8192, d=512, L=256, E=896, K=16, I=64, S=2, Is=128)
 # the alternative pool the pages weigh against 896 / top-16: 448 experts, 8 per token
 POOL448 = synth.LayerShape("pool448", T=8192, d=7168, L=3584, E=448, K=8, I=512, S=2, Is=2048)
+WGRAD = synth.LayerShape("wgrad", T=584, d=7168, L=3584, E=64, K=16, I=512, S=2, Is=2048)
 SHAPES = {"prefill": synth.PREFILL, "decode": synth.DECODE, "e64": synth.E64,
-          "skew": synth.SKEW, "small": SMALL, "routing": ROUTING, "pool448": POOL448}
+          "skew": synth.SKEW, "small": SMALL, "routing": ROUTING, "pool448": POOL448,
+          "wgrad": WGRAD}
 DESCRIPTIONS = {
     "prefill": "K3 Stable Latent MoE layer, prefill: in-batch Quantile-Balancing thresholds; "
                "x~N(0,1) with 0.1% of elements x1000; residual = x",
@@ -275,6 +277,9 @@ DESCRIPTIONS = {
     "routing": "K3 routing shape with narrow widths (profiling case for the threshold, "
                "top-K and dispatch kernels at T=8192, E=896, top-16); x~N(0,1); in-batch "
                "thresholds",
+    "wgrad": "K3 widths, 64 experts, T=584 (profiling case for the backward's weight-gradient "
+             "GEMMs: 146 tokens per expert as in prefill, a few GB on the device); x as in "
+             "prefill",
 }
 
 
@@ -287,7 +292,7 @@ class Workload:
         self.qb = qb
         self.fp8 = expert_fp8
         self.sh = sh = SHAPES[name]
-        outliers = name in ("prefill", "small", "pool448")
+        outliers = name in ("prefill", "small", "pool448", "wgrad")
         gain = synth.outlier_router_gain(sh, OUTLIER_FRAC, OUTLIER_SCALE) if outliers else 1.0
         self.w = synth.make_weights(sh, SEED, device=dev, router_gain=gain)
         self.x = synth.make_x(sh, SEED + 1000 * rank, device=dev,
@@ -298,7 +303,7 @@ class Workload:
         self.kwargs = {}
         self.extra = {}
         if qb == "global":
-            if name not in ("prefill", "e64", "small", "routing", "pool448"):
+            if name not in ("prefill", "e64", "small", "routing", "pool448", "wgrad"):
                 raise ValueError("--qb global applies to the in-batch-threshold workloads")
             # thresholds over all ranks' batches together (all-gather of candidates)
             self.kwargs["global_tokens"] = sh.T * world
@@ -608,7 +613,8 @@ def run_backward(args):
         grad_bytes += 4.0 * (d * (L + sw) + (L + 2 * sw) * d + E * L)
     peaks, _ = load_peaks()
     what = "layer" if whole else "routed-branch"
-    line = {"metric": f"{what} backward tokens/s (K3 prefill)",
+    where = "K3 prefill" if args.shape == "prefill" else f"{args.shape} workload"
+    line = {"metric": f"{what} backward tokens/s ({where})",
             "value": world * sh.T / (bwd / 1e3), "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": bwd,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",

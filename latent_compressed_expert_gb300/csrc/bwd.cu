@@ -240,7 +240,8 @@ colsum_final_kernel(const float* __restrict__ part, int L, float* __restrict__ d
 // SiTU-GLU backward on the interleaved gate/value layout: row p of pre / dgv holds, for each
 // group of GLU_GROUP features, GLU_GROUP gate then GLU_GROUP value pre-activations.  A thread
 // takes 8 consecutive features of one row: 16-byte loads of their gate, value and dh, and
-// 16-byte stores of both gradients.
+// 16-byte stores of both gradients.  tanh and the exponential are the hardware approximations
+// (relative error about 2^-11, below the bf16 rounding of the operands and of the result).
 __global__ void __launch_bounds__(256)
 situ_bwd_kernel(const __nv_bfloat16* __restrict__ pre, const __nv_bfloat16* __restrict__ dh,
                 int64_t rows, int I, float c, __nv_bfloat16* __restrict__ dgv, int64_t ldo) {
@@ -257,11 +258,12 @@ situ_bwd_kernel(const __nv_bfloat16* __restrict__ pre, const __nv_bfloat16* __re
     bf8_to_f(__ldg(reinterpret_cast<const uint4*>(pre + p * 2 * I + col)), g);
     bf8_to_f(__ldg(reinterpret_cast<const uint4*>(pre + p * 2 * I + col + GLU_GROUP)), v);
     bf8_to_f(__ldg(reinterpret_cast<const uint4*>(dh + p * I + f)), d);
+    const float inv_c = 1.0f / c;
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-      const float tg = tanhf(g[k] / c), tv = tanhf(v[k] / c);
+      const float tg = ptx::tanh_approx(g[k] * inv_c), tv = ptx::tanh_approx(v[k] * inv_c);
       const float G = c * tg, V = c * tv;
-      const float sg = 1.0f / (1.0f + expf(-G));
+      const float sg = __fdividef(1.0f, 1.0f + __expf(fminf(-G, 80.0f)));
       dg[k] = d[k] * V * sg * (1.0f + G * (1.0f - sg)) * (1.0f - tg * tg);
       dv[k] = d[k] * G * sg * (1.0f - tv * tv);
     }
@@ -352,27 +354,45 @@ transpose_rows_kernel(const __nv_bfloat16* __restrict__ x, int64_t ldx, int W, i
   }
 }
 
-// out[p, :W] = x[idx[p], :W] for p < n (16-byte pieces; W, ldx and ldo multiples of 8).
-__global__ void __launch_bounds__(256)
+// out[p, :W] = x[idx[p], :W] for p < n (16-byte pieces; W, ldx and ldo multiples of 8).  One
+// warp per row; each lane issues four loads before their stores.
+constexpr int GATHER_WARPS = 8;
+
+__global__ void __launch_bounds__(32 * GATHER_WARPS)
 gather_rows_kernel(const __nv_bfloat16* __restrict__ x, int64_t ldx,
-                   const int32_t* __restrict__ idx, int W, __nv_bfloat16* __restrict__ out,
-                   int64_t ldo) {
+                   const int32_t* __restrict__ idx, int64_t n, int W,
+                   __nv_bfloat16* __restrict__ out, int64_t ldo) {
   pdl_wait();
   pdl_launch_dependents();
-  const int64_t p = blockIdx.x;
+  const int lane = threadIdx.x & 31;
+  const int64_t p = static_cast<int64_t>(blockIdx.x) * GATHER_WARPS + (threadIdx.x >> 5);
+  if (p >= n) return;
   const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<int64_t>(__ldg(idx + p)) * ldx);
   uint4* dst = reinterpret_cast<uint4*>(out + p * ldo);
-  for (int v = threadIdx.x; v < W / 8; v += blockDim.x) dst[v] = __ldg(src + v);
+  const int nv = W / 8;
+  for (int v0 = 0; v0 < nv; v0 += 4 * 32) {
+    uint4 r[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int v = v0 + k * 32 + lane;
+      if (v < nv) r[k] = __ldg(src + v);
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int v = v0 + k * 32 + lane;
+      if (v < nv) dst[v] = r[k];
+    }
+  }
 }
 
 int launch_gather_rows(const __nv_bfloat16* x, int64_t ldx, const int32_t* idx, int64_t n, int W,
                        __nv_bfloat16* out, int64_t ldo, cudaStream_t stream) {
   if (n == 0) return LMOE_OK;
   if (W % 8 || ldx % 8 || ldo % 8 || (reinterpret_cast<uintptr_t>(x) & 15) ||
-      (reinterpret_cast<uintptr_t>(out) & 15) || n > 0x7fffffff)
+      (reinterpret_cast<uintptr_t>(out) & 15) || ceil_div(n, GATHER_WARPS) > 0x7fffffff)
     return LMOE_ERR_UNSUPPORTED;
-  return launch_pdl(gather_rows_kernel, static_cast<unsigned>(n), 256, 0, stream, x, ldx, idx, W,
-                    out, ldo) == cudaSuccess
+  return launch_pdl(gather_rows_kernel, static_cast<unsigned>(ceil_div(n, GATHER_WARPS)),
+                    32 * GATHER_WARPS, 0, stream, x, ldx, idx, n, W, out, ldo) == cudaSuccess
              ? LMOE_OK
              : LMOE_ERR_CUDA;
 }
