@@ -28,19 +28,24 @@
 
 namespace lmoe {
 
-template <int BN>
+// MT: 128-row M-tiles per CTA.  MT = 2 computes a 256 x BN tile pair that shares each B
+// stage: two MMAs per K-step into the two halves of TMEM, half the B bytes per FLOP, so the
+// same shared memory covers a longer load latency.  Its single accumulator is drained
+// before the next pair starts, so it serves long reductions (dense mode only).
+template <int BN, int MT>
 struct GemmCfg {
-  static constexpr int A_BYTES = BLOCK_M * BLOCK_K * 2;
+  static constexpr int A_BYTES = BLOCK_M * BLOCK_K * 2;  // one 128-row M-tile
   static constexpr int B_BYTES = BN * BLOCK_K * 2;
-  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES = (BN == 256) ? 4 : 6;
+  static constexpr int STAGE_BYTES = MT * A_BYTES + B_BYTES;
+  static constexpr int STAGES = MT == 2 ? (BN == 256 ? 3 : 4) : (BN == 256 ? 4 : 6);
+  static constexpr int ACC = MT == 2 ? 1 : 2;  // accumulator buffers of MT x BN columns
   static constexpr int TMEM_COLS = 2 * BN;
   static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
   static constexpr int NUM_BARS = 2 * STAGES + 6;
   static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
   // grouped-K epilogue staging: 32 rows x 32 fp32 per epilogue warp
   static constexpr int EPI_OFF = (MISC_OFF + 16 + 127) / 128 * 128;
-  static constexpr int EPI_BYTES = 4 * 32 * 32 * 4;
+  static constexpr int EPI_BYTES = MT == 1 ? 4 * 32 * 32 * 4 : 0;
   static constexpr int SMEM_BYTES = EPI_OFF + EPI_BYTES + 1024;  // + slack for 1024 alignment
   static constexpr uint32_t IDESC = ptx::idesc_bf16_f32(BLOCK_M, BN);
   static constexpr uint32_t IDESC_MN = ptx::idesc_bf16_f32_mn(BLOCK_M, BN);
@@ -50,6 +55,7 @@ struct GemmCfg {
 };
 
 constexpr int GEMM_THREADS = 192;
+constexpr int GEMM_PAIR_MIN_K = 2048;  // reduction length from which tile pairs are used
 constexpr int RASTER_GROUP_M = 16;
 
 struct TileCoord {
@@ -63,7 +69,7 @@ struct TileCoord {
   int klen;     // grouped-K: rows in the group (the last K-block may be partial)
 };
 
-template <int BN>
+template <int BN, int TM = BLOCK_M>  // TM: rows of an M-tile (of a tile pair)
 __device__ __forceinline__ TileCoord decode_tile(const GemmArgs& g, int nt, int mt, int tile) {
   int kgroup = 0;
   if (g.groups > 0) {  // grouped-K: groups outermost, then the raster below
@@ -80,7 +86,7 @@ __device__ __forceinline__ TileCoord decode_tile(const GemmArgs& g, int nt, int 
   const int m = first_m + local % gm;
   const int n = local / gm;
   TileCoord c;
-  c.a_row = m * BLOCK_M;
+  c.a_row = m * TM;
   c.row_end = g.M;
   c.b_row = n * BN;
   c.n0 = n * BN;
@@ -233,11 +239,18 @@ __device__ __forceinline__ void epilogue_store_partial(const GemmArgs& g, int ro
   }
 }
 
-template <int BN>
+template <int BN, int MT>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
 gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB, const GemmArgs g) {
-  using C = GemmCfg<BN>;
+  using C = GemmCfg<BN, MT>;
+  constexpr int TM = BLOCK_M * MT;
+  if constexpr (MT != 1) {
+    if (g.groups > 0) {  // tile pairs serve the dense mode only; the launcher never does this
+      if (threadIdx.x == 0) atomicOr(g.err, DEVERR_BAD_INDEX);
+      return;
+    }
+  }
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = ptx::smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -253,7 +266,7 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA,
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nt = (g.N + BN - 1) / BN;
-  const int mt_dense = (g.M + BLOCK_M - 1) / BLOCK_M;
+  const int mt_dense = (g.M + TM - 1) / TM;
   const int total = mt_dense * nt * (g.groups > 0 ? g.groups : 1);
   const uint64_t limit = g.timeout_ns;
 
@@ -292,7 +305,7 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA,
       uint32_t it = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-        const TileCoord tc = decode_tile<BN>(g, nt, mt_dense, tile);
+        const TileCoord tc = decode_tile<BN, TM>(g, nt, mt_dense, tile);
         for (int kb = 0; kb < tc.nk; ++kb, ++it) {
           const int s = static_cast<int>(it % C::STAGES);
           const uint32_t ph = (it / C::STAGES) & 1u;
@@ -314,8 +327,12 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA,
               ptx::tma_load_2d(sa + C::A_BYTES + i * C::BOX_BYTES, &tmB, &full[s],
                                tc.b_row + 64 * i, krow);
           } else {
-            ptx::tma_load_2d(sa, &tmA, &full[s], tc.k0 + kb * BLOCK_K, tc.a_row);
-            ptx::tma_load_2d(sa + C::A_BYTES, &tmB, &full[s], tc.k0 + kb * BLOCK_K, tc.b_row);
+#pragma unroll
+            for (int i = 0; i < MT; ++i)  // rows past M are zero-filled
+              ptx::tma_load_2d(sa + i * C::A_BYTES, &tmA, &full[s], tc.k0 + kb * BLOCK_K,
+                               tc.a_row + i * BLOCK_M);
+            ptx::tma_load_2d(sa + MT * C::A_BYTES, &tmB, &full[s], tc.k0 + kb * BLOCK_K,
+                             tc.b_row);
           }
         }
       }
@@ -344,7 +361,7 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA,
       }
       ptx::tc_fence_after();
       const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-      const TileCoord tc = decode_tile<BN>(g, nt, mt_dense, tile);
+      const TileCoord tc = decode_tile<BN, TM>(g, nt, mt_dense, tile);
       for (int kb = 0; kb < tc.nk; ++kb, ++it) {
         const int s = static_cast<int>(it % C::STAGES);
         const uint32_t ph = (it / C::STAGES) & 1u;
@@ -398,8 +415,9 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA,
         stalled = true;
       }
       for (int tile = blockIdx.x; !stalled && tile < total; tile += gridDim.x, ++lt) {
-        const int acc = lt & 1;
-        const uint32_t aph = static_cast<uint32_t>(lt >> 1) & 1u;
+        const int acc = C::ACC == 2 ? (lt & 1) : 0;
+        const uint32_t aph = C::ACC == 2 ? (static_cast<uint32_t>(lt >> 1) & 1u)
+                                         : (static_cast<uint32_t>(lt) & 1u);
         if (!ptx::mbar_wait(&tempty[acc], aph ^ 1u, abort_flag, limit)) {
           raise_error(g, abort_flag, DEVERR_TIMEOUT_MMA);
           break;
@@ -418,11 +436,15 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA,
           }
           ptx::tc_fence_after();
           const uint32_t sa = ptx::smem_u32(smem + s * C::STAGE_BYTES);
-          const uint32_t sb = sa + C::A_BYTES;
+          const uint32_t sb = sa + MT * C::A_BYTES;
 #pragma unroll
           for (int k = 0; k < BLOCK_K / 16; ++k)
-            ptx::umma_bf16(d_tmem, ptx::smem_desc_sw128(sa + k * 32),
-                           ptx::smem_desc_sw128(sb + k * 32), C::IDESC, (kb | k) != 0 ? 1u : 0u);
+#pragma unroll
+            for (int i = 0; i < MT; ++i)  // M-tile i accumulates into TMEM columns i*BN..
+              ptx::umma_bf16(d_tmem + static_cast<uint32_t>(i * BN),
+                             ptx::smem_desc_sw128(sa + i * C::A_BYTES + k * 32),
+                             ptx::smem_desc_sw128(sb + k * 32), C::IDESC,
+                             (kb | k) != 0 ? 1u : 0u);
           ptx::umma_commit(&empty[s]);
         }
         if (!ok) break;
@@ -439,62 +461,68 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA,
     const float c = g.c, inv_c = 1.0f / g.c;
     int lt = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++lt) {
-      const int acc = lt & 1;
-      const uint32_t aph = static_cast<uint32_t>(lt >> 1) & 1u;
+      const int acc = C::ACC == 2 ? (lt & 1) : 0;
+      const uint32_t aph = C::ACC == 2 ? (static_cast<uint32_t>(lt >> 1) & 1u)
+                                       : (static_cast<uint32_t>(lt) & 1u);
       const bool got = ptx::mbar_wait(&tfull[acc], aph, abort_flag, limit);
       if (!__all_sync(0xffffffffu, got)) {
         if (lane == 0) raise_error(g, abort_flag, DEVERR_TIMEOUT_EPILOGUE);
         break;
       }
       ptx::tc_fence_after();
-      const TileCoord tc = decode_tile<BN>(g, nt, mt_dense, tile);
-      const int row = tc.a_row + q * 32 + lane;
-      const bool row_ok = row < tc.row_end;
-      const int orow = (g.groups > 0 && row_ok) ? (g.row_map ? __ldg(g.row_map + row) : row) : 0;
-      const uint32_t tbase =
-          tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
+      const TileCoord tc = decode_tile<BN, TM>(g, nt, mt_dense, tile);
+      // the M-tiles of the tile (two for a tile pair), at TMEM columns (acc + h) * BN
 #pragma unroll 1
-      for (int ch = 0; ch < BN / 32; ++ch) {
-        const int col0 = tc.n0 + ch * 32;
-        if (col0 >= g.N) break;  // uniform across the warp
-        float v[32];
-        if (g.groups > 0) {
-          // grouped-K: an empty reduction range is a zero product
-          if (tc.nk > 0) {
-            ptx::tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(ch * 32), v);
-          } else {
+      for (int h = 0; h < MT; ++h) {
+        const int row = tc.a_row + h * BLOCK_M + q * 32 + lane;
+        const bool row_ok = row < tc.row_end;
+        const int orow =
+            (g.groups > 0 && row_ok) ? (g.row_map ? __ldg(g.row_map + row) : row) : 0;
+        const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                               static_cast<uint32_t>((acc + h) * BN);
+#pragma unroll 1
+        for (int ch = 0; ch < BN / 32; ++ch) {
+          const int col0 = tc.n0 + ch * 32;
+          if (col0 >= g.N) break;  // uniform across the warp
+          float v[32];
+          if (g.groups > 0) {
+            // grouped-K: an empty reduction range is a zero product
+            if (tc.nk > 0) {
+              ptx::tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(ch * 32), v);
+            } else {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+              for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+            }
+            // Through this warp's staging buffer (16-byte chunks XOR-swizzled by row), so that
+            // each store instruction writes four whole 128-byte row segments instead of one
+            // 16-byte piece of 32 rows.
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              reinterpret_cast<float4*>(stage + lane * 32)[j ^ (lane & 7)] =
+                  make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+            __syncwarp();
+            const int nvalid = min(32, g.N - col0);  // a multiple of 16
+            const int c4 = lane & 7;
+            float* og = g.outf + tc.grp * g.group_stride + col0 + 4 * c4;
+#pragma unroll
+            for (int it = 0; it < 8; ++it) {
+              const int r = 4 * it + (lane >> 3);
+              const int orow_r = __shfl_sync(0xffffffffu, orow, r);
+              const bool ok_r = __shfl_sync(0xffffffffu, row_ok ? 1 : 0, r) != 0;
+              if (ok_r && 4 * c4 < nvalid)
+                *reinterpret_cast<float4*>(og + static_cast<size_t>(orow_r) * g.ldf) =
+                    reinterpret_cast<const float4*>(stage + r * 32)[c4 ^ (r & 7)];
+            }
+            __syncwarp();
+            continue;
           }
-          // Through this warp's staging buffer (16-byte chunks XOR-swizzled by row), so that
-          // each store instruction writes four whole 128-byte row segments instead of one
-          // 16-byte piece of 32 rows.
-#pragma unroll
-          for (int j = 0; j < 8; ++j)
-            reinterpret_cast<float4*>(stage + lane * 32)[j ^ (lane & 7)] =
-                make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-          __syncwarp();
-          const int nvalid = min(32, g.N - col0);  // a multiple of 16
-          const int c4 = lane & 7;
-          float* og = g.outf + tc.grp * g.group_stride + col0 + 4 * c4;
-#pragma unroll
-          for (int it = 0; it < 8; ++it) {
-            const int r = 4 * it + (lane >> 3);
-            const int orow_r = __shfl_sync(0xffffffffu, orow, r);
-            const bool ok_r = __shfl_sync(0xffffffffu, row_ok ? 1 : 0, r) != 0;
-            if (ok_r && 4 * c4 < nvalid)
-              *reinterpret_cast<float4*>(og + static_cast<size_t>(orow_r) * g.ldf) =
-                  reinterpret_cast<const float4*>(stage + r * 32)[c4 ^ (r & 7)];
+          ptx::tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(ch * 32), v);
+          if (row_ok) {
+            if (col0 + 32 <= g.N)
+              epilogue_store(g, row, col0, v, c, inv_c);
+            else
+              epilogue_store_partial(g, row, col0, g.N - col0, v);
           }
-          __syncwarp();
-          continue;
-        }
-        ptx::tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(ch * 32), v);
-        if (row_ok) {
-          if (col0 + 32 <= g.N)
-            epilogue_store(g, row, col0, v, c, inv_c);
-          else
-            epilogue_store_partial(g, row, col0, g.N - col0, v);
         }
       }
       ptx::tc_fence_before();
@@ -544,11 +572,12 @@ bool make_tmap_bf16(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t col
   return r == CUDA_SUCCESS;
 }
 
-template <int BN>
+template <int BN, int MT>
 static int launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& g,
                      cudaStream_t stream) {
-  using C = GemmCfg<BN>;
-  if (cudaFuncSetAttribute(gemm_tcgen05_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  using C = GemmCfg<BN, MT>;
+  if (cudaFuncSetAttribute(gemm_tcgen05_kernel<BN, MT>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize,
                            C::SMEM_BYTES) != cudaSuccess)
     return LMOE_ERR_CUDA;
   int dev = 0, sms = 0;
@@ -557,10 +586,11 @@ static int launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArg
     return LMOE_ERR_CUDA;
   int grid = (g.max_ctas > 0 && g.max_ctas < sms) ? g.max_ctas : sms;
   const int64_t tiles =
-      ceil_div(g.M, BLOCK_M) * ceil_div(g.N, BN) * (g.groups > 0 ? g.groups : 1);
+      ceil_div(g.M, BLOCK_M * MT) * ceil_div(g.N, BN) * (g.groups > 0 ? g.groups : 1);
   if (tiles < grid) grid = static_cast<int>(tiles);
   if (grid <= 0) return LMOE_OK;
-  return launch_pdl(gemm_tcgen05_kernel<BN>, grid, GEMM_THREADS, C::SMEM_BYTES, stream, ta, tb, g) ==
+  return launch_pdl(gemm_tcgen05_kernel<BN, MT>, grid, GEMM_THREADS, C::SMEM_BYTES, stream, ta, tb,
+                    g) ==
                  cudaSuccess
              ? LMOE_OK
              : LMOE_ERR_CUDA;
@@ -596,7 +626,18 @@ int launch_gemm(const void* A, uint64_t a_rows, int a_ld, const void* B, uint64_
                              static_cast<uint64_t>(b_ld), static_cast<uint32_t>(bn))) {
     return LMOE_ERR_CUDA;
   }
-  return bn == 256 ? launch_bn<256>(ta, tb, g, stream) : launch_bn<128>(ta, tb, g, stream);
+  // Tile pairs (two 128-row M-tiles sharing each B stage) when the problem is dense, has at
+  // least two pairs per SM and a long reduction: the pair's undivided accumulator is drained
+  // while no MMA runs, which only pays when the MMAs take far longer.
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return LMOE_ERR_CUDA;
+  const bool pairs = g.groups == 0 && g.Kd >= GEMM_PAIR_MIN_K &&
+                     ceil_div(g.M, 2 * BLOCK_M) * ceil_div(g.N, bn) >= 2 * static_cast<int64_t>(sms);
+  if (bn == 256)
+    return pairs ? launch_bn<256, 2>(ta, tb, g, stream) : launch_bn<256, 1>(ta, tb, g, stream);
+  return pairs ? launch_bn<128, 2>(ta, tb, g, stream) : launch_bn<128, 1>(ta, tb, g, stream);
 }
 
 }  // namespace lmoe

@@ -24,7 +24,10 @@ def dev():
 # ----------------------------------------------------------------------------------------
 @pytest.mark.parametrize("M,N,K", [(128, 256, 64), (200, 256, 128), (1, 16, 64), (300, 640, 448),
                                    (513, 384, 1024), (64, 896, 3584), (1000, 1280, 512),
-                                   (4096, 512, 256)])
+                                   (4096, 512, 256),
+                                   # tile pairs (two M-tiles per CTA), 256- and 128-wide tiles;
+                                   # M ragged, the last pair's second tile wholly past M
+                                   (20000, 3584, 2048), (26000, 384, 2048)])
 def test_gemm_matches_float64(dev, M, N, K):
     g = torch.Generator(device=dev).manual_seed(M * 7 + N * 3 + K)
     A = torch.randn(M, K, generator=g, device=dev).to(torch.bfloat16)
