@@ -495,8 +495,10 @@ def run_ours(args):
         roof = {"bound": "hbm", "achieved": dw["bytes"] / t_s / 1e9, "peak": peaks["hbm_gbs"],
                 "unit": "GB/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = ncu_traffic(dom, "stages_fp8" if wl.fp8 and dom.startswith("expert")
-                                  else "stages")
+    # the stored figures are captures of the prefill workload (in-batch thresholds)
+    roof["traffic"] = (ncu_traffic(dom, "stages_fp8" if wl.fp8 and dom.startswith("expert")
+                                   else "stages")
+                       if wl.name == "prefill" and wl.qb == "local" else None)
     roof["kernel"] = dom
     roof["peak_source"] = f"{peak_src} ({'bf16 sustained' if roof['bound'] == 'tensor' else 'HBM copy'})"
     roof["algorithmic"] = {"flop": dw["flop"], "bytes": dw["bytes"]}
