@@ -86,7 +86,7 @@ def _situ(g, v, c):
     return gc * torch.sigmoid(gc) * (c * torch.tanh(v / c))
 
 
-def layer_forward_t(x, idx, w: dict, c=100.0, eps=1e-6, gate=None, keep=None):
+def layer_forward_t(x, idx, w: dict, c=100.0, eps=1e-6, gate=None, keep=None, local_idx=None):
     """The whole layer without its residual term, in float64 torch ops, with routing held at
     ``idx`` (the forward oracle's ``latent``, ``router_logits``, ``route``, ``routed``,
     ``shared`` and ``output``):
@@ -96,7 +96,9 @@ def layer_forward_t(x, idx, w: dict, c=100.0, eps=1e-6, gate=None, keep=None):
         hs_s = SiTU-GLU(x W_sg[s]^T, x W_sv[s]^T),  y = z W_up^T + sum_s hs_s W_sd[s]^T.
     ``gate`` replaces the computed gates when given (to pin the rest of the restatement to
     the C oracle, which takes fp32 gates).  keep: as for ``routed_forward_t``, plus the
-    selected experts' scores "s".  Returns (y, {"lat", "logits", "gate", "z"})."""
+    selected experts' scores "s".  local_idx: when the routed weights given are only the
+    selected experts' (w_gate etc. indexed by these instead of idx).  Returns
+    (y, {"lat", "logits", "gate", "z"})."""
     idx_t = torch.as_tensor(np.asarray(idx), dtype=torch.long)
     lat = x @ w["w_down"].T
     logits = lat @ w["w_router"].T
@@ -105,8 +107,8 @@ def layer_forward_t(x, idx, w: dict, c=100.0, eps=1e-6, gate=None, keep=None):
         gate = s / s.sum(1, keepdim=True)
     if keep is not None:
         keep["s"] = s
-    z = routed_forward_t(lat, idx, gate, w["w_gate"], w["w_value"], w["w_edown"], w["gamma"],
-                         c, eps, keep)
+    z = routed_forward_t(lat, idx if local_idx is None else local_idx, gate, w["w_gate"],
+                         w["w_value"], w["w_edown"], w["gamma"], c, eps, keep)
     y = z @ w["w_up"].T
     if w["w_sgate"].shape[0] > 0:
         G = torch.einsum("td,sid->tsi", x, w["w_sgate"])
@@ -145,3 +147,33 @@ def layer_backward(x, idx, w: dict, dy, c=100.0, eps=1e-6, intermediates=False) 
         g = wt[k].grad  # None for weights the forward does not reach (no shared experts)
         out["d" + k] = g.numpy() if g is not None else np.zeros(tuple(wt[k].shape))
     return out
+
+
+def _rows_of(a, sel: np.ndarray) -> torch.Tensor:
+    """float64 copy of the rows `sel` of a weight stack (tensor or bf16 bit array)."""
+    if isinstance(a, torch.Tensor):
+        return _f64(a.index_select(0, torch.as_tensor(sel, dtype=torch.long)))
+    return _f64(np.asarray(a)[sel])
+
+
+def layer_dx_rows(x, idx, w: dict, dy, c=100.0, eps=1e-6) -> np.ndarray:
+    """dx (as ``layer_backward``) for individual tokens, one at a time.  Given the routing, a
+    token's output and its gradient depend on that token alone.  Only its K experts'
+    weights enter, so a full-size layer fits in memory.  x, dy: [n, d]; idx: [n, K]."""
+    dense = {k: _f64(w[k]) for k in ("w_down", "w_router", "gamma", "w_up", "w_sgate",
+                                     "w_svalue", "w_sdown")}
+    xs = _f64(x)
+    dys = torch.as_tensor(np.asarray(dy, dtype=np.float64))
+    idx = np.asarray(idx)
+    K = idx.shape[1]
+    local = np.arange(K)[None, :]
+    dx = np.empty(tuple(xs.shape))
+    for t in range(xs.shape[0]):
+        wt = dict(dense)
+        for k in ("w_gate", "w_value", "w_edown"):
+            wt[k] = _rows_of(w[k], idx[t])
+        xt = xs[t:t + 1].clone().requires_grad_(True)
+        y, _ = layer_forward_t(xt, idx[t:t + 1], wt, c, eps, local_idx=local)
+        y.backward(dys[t:t + 1])
+        dx[t] = xt.grad[0].numpy()
+    return dx

@@ -184,3 +184,42 @@ def test_saved_pre_activations_match_recompute(dev):
     assert layer.device_error() == 0
     for k in g0:
         assert torch.equal(g0[k], g1[k]), k
+
+
+def test_prefill_backward_sampled_tokens_and_linearity(dev, oracle_mod):
+    """The benchmark's backward at the full K3 prefill shape (T=8192, E=896, top-16, x with
+    0.1 % outliers).  The oracle computes every token's latent and logits, the in-batch
+    thresholds and the routing (bit-exact against the device on the same logits), then dx of
+    sampled tokens, one at a time.  Every weight gradient sums over thousands of tokens, so
+    at this size they are held to a property: each backward step is linear in dy and
+    doubling is exact in binary floating point, so backward(2 dy) is 2 backward(dy), bit for
+    bit, in every output."""
+    import gpu_helpers as H
+    import oracle.backward as B
+    sh = synth.PREFILL
+    gain = synth.outlier_router_gain(sh, 0.001, 1000.0)
+    w = synth.make_weights(sh, seed=4, device=dev, router_gain=gain)
+    x = synth.make_x(sh, seed=4, device=dev, outlier_frac=0.001)
+    wh = H.weights_to_host(w)
+    xh = x.cpu()
+    lat = oracle_mod.latent(xh, wh["w_down"])
+    lg32 = oracle_mod.router_logits(lat, wh["w_router"]).astype(np.float32)
+    tau = oracle_mod.thresholds(lg32, oracle_mod.fair_share_rank(sh.T, sh.K, sh.E))
+    idx, _, _ = oracle_mod.route(lg32, tau, sh.K)
+    layer = lmoe.Layer(sh, w)
+    layer.enable_backward(w)
+    logits = torch.as_tensor(lg32).to(dev)
+    _, dbg = layer.forward(x, residual=x, logits_in=logits, train=True, debug=True)
+    assert np.array_equal(dbg["idx"].cpu().numpy(), idx)
+    dy = torch.randn(sh.T, sh.d, generator=torch.Generator(device=dev).manual_seed(5),
+                     device=dev).to(torch.bfloat16)
+    g = {k: v.clone() for k, v in layer.backward_layer(x, dy, logits=logits).items()}
+    g2 = layer.backward_layer(x, dy * 2, logits=logits)
+    torch.cuda.synchronize()
+    assert layer.device_error() == 0
+    for k in ("dx", "dgamma", "dw_in", "dw_router", "dw_gu", "dw_edown", "dw_out"):
+        assert torch.equal(g2[k], 2 * g[k]), k
+    rows = np.array([0, 1, 4095, 8191] + list(np.random.default_rng(6).choice(sh.T, 2, replace=False)))
+    ref = B.layer_dx_rows(xh[rows], idx[rows], wh, dy[rows].double().cpu().numpy())
+    s = _stats(g["dx"][rows].cpu().numpy(), ref)
+    assert _ok(s), s

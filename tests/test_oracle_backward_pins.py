@@ -148,3 +148,17 @@ def test_layer_gradients_equal_finite_differences(S, c):
             b[name][ix] -= h
             fd = (loss(a) - loss(b)) / (2 * h)
             assert fd == pytest.approx(g[key.get(name, "d" + name)][ix], rel=1e-5, abs=1e-7), name
+
+
+def test_layer_dx_rows_equals_whole_batch():
+    """Token by token, with each token's experts' weights only, the restatement gives the
+    whole batch's dx (a token's gradient depends on that token alone given the routing)."""
+    import oracle.backward as B
+    sh, w, x = _layer_case(2, seed=21, T=6)
+    rng = np.random.default_rng(22)
+    idx = np.stack([rng.choice(sh.E, sh.K, replace=False) for _ in range(sh.T)]).astype(np.int32)
+    dy = rng.standard_normal((sh.T, sh.d))
+    whole = B.layer_backward(x, idx, w, dy)["dx"]
+    rows = np.array([0, 3, 5])
+    part = B.layer_dx_rows(x[rows], idx[rows], w, dy[rows])
+    assert np.allclose(part, whole[rows], rtol=1e-11, atol=1e-13)
