@@ -12,8 +12,16 @@
 //               bf16 / fp32 store, SiTU-GLU on interleaved gate/value columns, residual add),
 //               then release the accumulator ("tmem_empty") so the MMA of the tile after
 //               next can start while this one is written out.
-// This kernel serves the dense contractions (x-side GEMM, router, output GEMM); the routed
-// experts' GEMMs are in gemm_grouped.cu.
+// Tile pairs (MT = 2): a CTA computes two 128-row M-tiles that share each B stage, two MMAs
+// per K-step into the two halves of TMEM (one accumulator, drained before the next pair),
+// for long dense reductions: half the B bytes per FLOP.
+// Grouped-K mode (the backward's weight gradients): `groups` independent products, each a
+// reduction over its own range of rows of token-major operands, which the MMA reads as
+// MN-major tiles (64 x 64 TMA boxes); A's rows past a group's end are zeroed in shared
+// memory before its last K-block's MMAs.
+// This kernel serves the dense contractions (x-side GEMM, router, output GEMM, the
+// backward's dense GEMMs and weight gradients); the routed experts' forward and dgrad GEMMs
+// are in gemm_grouped.cu.
 //
 // Every wait is bounded (globaltimer); on time-out a role records an error bit in global
 // memory, raises a shared abort flag that makes the other roles give up too, waits for
