@@ -18,6 +18,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import glob
 import json
 import os
@@ -108,16 +109,20 @@ STAGE_SOURCES = {
 }
 
 
+_COMMENT = re.compile(rb"/\*.*?\*/|//[^\n]*", re.S)
+
+
 def kernel_source_hash(stage: str) -> str:
-    """Hash of the sources of one stage's kernel: a stored ncu figure is valid while it
-    matches."""
+    """Hash of the sources of one stage's kernel, comments and blank space left out: a
+    stored ncu figure is valid while it matches."""
     h = hashlib.sha256()
     for name in sorted(STAGE_SOURCES[stage] + _COMMON_SRC):
         path = os.path.join(ROOT, "include" if name.endswith(".h") else
                             os.path.join("latent_compressed_expert_gb300", "csrc"), name)
         with open(path, "rb") as f:
-            h.update(name.encode())
-            h.update(f.read())
+            code = b" ".join(_COMMENT.sub(b" ", f.read()).split())
+        h.update(name.encode())
+        h.update(code)
     return h.hexdigest()[:16]
 
 
