@@ -35,7 +35,9 @@
  *     device (a bounded wait that ran out) are read with lmoe_last_device_error after the
  *     stream has synchronised.
  *   - Inputs must be finite.  NaN router logits give an unspecified (but in-bounds)
- *     selection.
+ *     selection.  Checked mode: with LMOE_CHECK_FINITE=1 in the environment (read at each
+ *     call), lmoe_forward scans the router logits it routes on, and a NaN or infinite one
+ *     makes lmoe_last_device_error return LMOE_ERR_INVALID_ARG.
  */
 #ifndef LMOE_H
 #define LMOE_H
@@ -400,8 +402,10 @@ int lmoe_forward_noalloc(const lmoe_dims *dims, const void *packed, const void *
  * into `workspace`.  Every device-side wait is bounded (2 s by default; the environment
  * variable LMOE_WAIT_LIMIT_MS overrides it), and LMOE_FAULT_INJECT=stall makes the first
  * GEMM of a call wait on a barrier that nothing arrives on, so that this path can be
- * tested: its kernels then give up, free their tensor memory and return.  Returns LMOE_OK or LMOE_ERR_DEVICE_TIMEOUT (a bounded wait ran out;
- * the kernel returned early and y is not valid).  Call after the stream has synchronised. */
+ * tested: its kernels then give up, free their tensor memory and return.  Returns LMOE_OK,
+ * LMOE_ERR_DEVICE_TIMEOUT (a bounded wait ran out; the kernel returned early and y is not
+ * valid), or LMOE_ERR_INVALID_ARG (checked mode saw a non-finite router logit, or a device
+ * index check failed; y is not specified).  Call after the stream has synchronised. */
 int lmoe_last_device_error(void *workspace);
 
 /* Static description of a status code. */

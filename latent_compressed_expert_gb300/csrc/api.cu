@@ -124,6 +124,14 @@ static bool inject_stall() {
   return s && strcmp(s, "stall") == 0;
 }
 
+// Checked mode: LMOE_CHECK_FINITE=1 makes lmoe_forward scan the router logits; a
+// non-finite one is reported as an invalid argument by lmoe_last_device_error.  Read at
+// every call.
+static bool check_finite() {
+  const char* s = getenv("LMOE_CHECK_FINITE");
+  return s && strcmp(s, "1") == 0;
+}
+
 static GemmArgs gemm_defaults(uint32_t* err, float c) {
   GemmArgs g{};
   g.err = err;
@@ -760,7 +768,7 @@ int lmoe_last_device_error(void* workspace) {
   const uint32_t zero = 0;
   if (cudaMemcpy(workspace, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
     return LMOE_ERR_CUDA;
-  if (flag & DEVERR_BAD_INDEX) return LMOE_ERR_INVALID_ARG;
+  if (flag & (DEVERR_BAD_INDEX | DEVERR_NONFINITE)) return LMOE_ERR_INVALID_ARG;
   return LMOE_ERR_DEVICE_TIMEOUT;
 }
 
@@ -951,6 +959,12 @@ int lmoe_forward(const lmoe_dims* dims, const void* packed, const void* x, const
     launches += 1;
   } else if (want_t) {
     rc = launch_transpose_f32(logits, T, D.E, logits_t, stream);
+    if (rc != LMOE_OK) return rc;
+    launches += 1;
+  }
+  // checked mode: the logits routed on (computed or given) must be finite
+  if (front && check_finite()) {
+    rc = launch_finite_check(logits, static_cast<int64_t>(T) * D.E, err, stream);
     if (rc != LMOE_OK) return rc;
     launches += 1;
   }

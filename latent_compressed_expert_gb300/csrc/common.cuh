@@ -19,6 +19,7 @@ constexpr uint32_t DEVERR_TIMEOUT_MMA = 1u << 1;
 constexpr uint32_t DEVERR_TIMEOUT_EPILOGUE = 1u << 2;
 constexpr uint32_t DEVERR_TIMEOUT_DRAIN = 1u << 3;
 constexpr uint32_t DEVERR_BAD_INDEX = 1u << 8;
+constexpr uint32_t DEVERR_NONFINITE = 1u << 9;  // checked mode: a non-finite router logit
 
 // Tile shape of every GEMM: 128 rows (UMMA M) x BLOCK_N columns x 64 (one 128-byte
 // swizzle atom of bf16 along K).

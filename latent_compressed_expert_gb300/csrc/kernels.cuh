@@ -129,6 +129,8 @@ int launch_candidates(const float* z, int T, int E, int64_t stride_t, int64_t st
                       float* cand, int64_t ldc, cudaStream_t stream);
 // out[E, T] = in[T, E]^T (fp32).
 int launch_transpose_f32(const float* in, int T, int E, float* out, cudaStream_t stream);
+// Checked mode: sets DEVERR_NONFINITE in *err if any of p[0, n) is NaN or infinite.
+int launch_finite_check(const float* p, int64_t n, uint32_t* err, cudaStream_t stream);
 int launch_dispatch(const int32_t* idx, int T, int E, int K, uint32_t* masks, uint32_t* base,
                     int32_t* offsets, int32_t* ct_off, int32_t* inv, int32_t* src_tok,
                     int32_t* counts_out, uint32_t* err, cudaStream_t stream);

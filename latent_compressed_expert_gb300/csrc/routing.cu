@@ -499,6 +499,31 @@ int launch_router_bwd(const float* z, int64_t ldz, const int32_t* idx, const flo
              : LMOE_ERR_CUDA;
 }
 
+// Checked mode: any non-finite value among p[0, n) sets DEVERR_NONFINITE.
+__global__ void __launch_bounds__(256)
+finite_check_kernel(const float* __restrict__ p, int64_t n, uint32_t* __restrict__ err) {
+  pdl_wait();
+  pdl_launch_dependents();
+  bool bad = false;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    bad |= !isfinite(__ldg(p + i));
+  if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0) atomicOr(err, DEVERR_NONFINITE);
+}
+
+int launch_finite_check(const float* p, int64_t n, uint32_t* err, cudaStream_t stream) {
+  if (n == 0) return LMOE_OK;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return LMOE_ERR_CUDA;
+  const int64_t blocks = ceil_div(n, 256);
+  const unsigned grid = static_cast<unsigned>(blocks < 8 * sms ? blocks : 8 * sms);
+  return launch_pdl(finite_check_kernel, grid, 256, 0, stream, p, n, err) == cudaSuccess
+             ? LMOE_OK
+             : LMOE_ERR_CUDA;
+}
+
 int launch_transpose_f32(const float* in, int T, int E, float* out, cudaStream_t stream) {
   if (T == 0) return LMOE_OK;
   const dim3 grid(static_cast<unsigned>(ceil_div(E, 32)), static_cast<unsigned>(ceil_div(T, 32)));

@@ -330,3 +330,30 @@ def test_shared_overlap_and_serial_paths(dev, oracle_mod, overlap):
     ref = oracle_mod.forward(w, x, sh.K, residual=x, tau="batch", logits_in=logits.numpy())
     assert np.array_equal(dbg["idx"].cpu().numpy(), ref.idx)
     H.assert_close(y.float().cpu().numpy(), ref.y, f"mid/overlap={overlap}")
+
+
+def test_checked_mode_reports_nonfinite_logits(dev, monkeypatch):
+    """LMOE_CHECK_FINITE=1: a NaN router logit is reported as an invalid argument through
+    lmoe_last_device_error.  Without the check, NaN logits still select valid experts
+    (the score's clamp maps NaN to the lower end), so every index stays in range."""
+    sh = synth.TINY
+    w = {k: v.to(dev) for k, v in synth.make_weights(sh, seed=0).items()}
+    layer = lmoe.Layer(sh, w)
+    x = synth.make_x(sh, seed=0).to(dev)
+    logits = synth.make_logits(sh.T, sh.E, seed=0).to(dev)
+    bad = logits.clone()
+    bad[3, 5] = float("nan")
+    bad[7, 0] = float("inf")
+    monkeypatch.setenv("LMOE_CHECK_FINITE", "1")
+    layer.forward(x, residual=x, logits_in=logits)
+    torch.cuda.synchronize()
+    assert layer.device_error() == lmoe.LMOE_OK
+    layer.forward(x, residual=x, logits_in=bad)
+    torch.cuda.synchronize()
+    assert layer.device_error() == lmoe.LMOE_ERR_INVALID_ARG
+    monkeypatch.delenv("LMOE_CHECK_FINITE")
+    _, dbg = layer.forward(x, residual=x, logits_in=bad, debug=True)
+    torch.cuda.synchronize()
+    assert layer.device_error() == lmoe.LMOE_OK
+    idx = dbg["idx"].cpu().numpy()
+    assert idx.min() >= 0 and idx.max() < sh.E
