@@ -124,6 +124,8 @@ def _router_sigma(ref, idx, E):
     # gradients' single K-block are partial
     synth.LayerShape("b_t1", T=1, d=512, L=256, E=32, K=4, I=128, S=2, Is=128),
     synth.LayerShape("b_t7", T=7, d=512, L=256, E=32, K=4, I=128, S=2, Is=128),
+    # one expert per token: the gate is s/s = 1 whatever s, so the router gets no gradient
+    synth.LayerShape("b_k1", T=130, d=512, L=256, E=16, K=1, I=128, S=2, Is=128),
 ])
 def test_layer_backward_matches_oracle(dev, oracle_mod, shape):
     """lmoe_backward against the oracle's whole-layer backward.  The GPU routes on the
@@ -159,6 +161,8 @@ def test_layer_backward_matches_oracle(dev, oracle_mod, shape):
              for k in LAYER_KEYS if ref[k].size > 0}
     bad = {k: v for k, v in stats.items() if not _ok(v)}
     assert not bad, (sh.name, bad)
+    if sh.K == 1:
+        assert np.all(got["dw_router"] == 0.0)
     # the router's gradient: every element within 6 standard deviations of its rounding
     excess = np.abs(got["dw_router"] - ref["dw_router"]) - 6.0 * _router_sigma(ref, r.idx, sh.E)
     assert excess.max() <= 1e-6 * np.abs(ref["dw_router"]).max(), (sh.name, excess.max())
