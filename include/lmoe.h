@@ -186,7 +186,12 @@ size_t lmoe_packed_bytes(const lmoe_dims *dims);
 int lmoe_pack_weights(const lmoe_dims *dims, const lmoe_weights *w, void *packed,
                       size_t packed_bytes, void *stream);
 
-/* Bytes of device workspace lmoe_forward needs for `dims` (0 if the dims are invalid). */
+/* Bytes of device workspace lmoe_forward uses for `dims` (0 if the dims are invalid).  For a
+ * batch of at most 128 tokens this includes a 12 MiB region for split-K partial sums of the
+ * dense GEMMs (a single M-tile would otherwise leave most SMs idle).  lmoe_forward also runs
+ * in a workspace 12 MiB smaller, without splitting them, and only whole-layer calls
+ * (LMOE_PHASE_ALL) split: the two phases keep every token's logits and output bit-identical
+ * to those of any other batch it is part of. */
 size_t lmoe_workspace_bytes(const lmoe_dims *dims);
 
 /* Quantile-Balancing thresholds.  [IK3] Quantile Balancing passage: each step's routing
@@ -286,7 +291,8 @@ int lmoe_route(const float *logits, const float *tau, int T, int E, int K, int32
  *   packed   weights from lmoe_pack_weights for the same dims
  *   x        [T, d] bf16;  residual [T, d] bf16 or NULL (then no residual term)
  *   y        [T, d] bf16 output (may not alias x or residual)
- *   workspace, ws_bytes >= lmoe_workspace_bytes(dims), 256-byte aligned; its contents are
+ *   workspace, ws_bytes >= lmoe_workspace_bytes(dims) (less the optional split-K region for
+ *            T <= 128, see lmoe_workspace_bytes), 256-byte aligned; its contents are
  *            scratch between calls (its first word carries the device error flag)
  *   io       routing options and debug outputs, or NULL (= in-batch thresholds); only
  *            io->kernel_launches is written
@@ -385,8 +391,9 @@ int lmoe_quantize_e4m3(const void *x, long long rows, int cols, uint8_t *codes, 
  * process starts.  Arguments and results are those of lmoe_forward without the workspace.
  * Scratch: a LMOE_NOALLOC_SCRATCH_BYTES (24 MiB) array in the library's device image,
  * reserved on every GPU that loads the library until the process exits.  It covers a K3
- * decode batch of up to 155 tokens (64 tokens need 9.9 MiB).  When lmoe_workspace_bytes(dims)
- * exceeds it, the call returns LMOE_ERR_WORKSPACE_TOO_SMALL and enqueues nothing.
+ * decode batch of up to 155 tokens (64 tokens need 9.9 MiB, 21.9 MiB with the split-K
+ * region, which is used when it fits).  When the workspace without that region exceeds the
+ * array, the call returns LMOE_ERR_WORKSPACE_TOO_SMALL and enqueues nothing.
  * Set-up: the first call on each device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call before any stream
  * capture.  No call allocates or frees memory.

@@ -100,6 +100,11 @@ WorkspaceLayout workspace_layout(const lmoe_dims& D) {
     W.h8 = take(TK * D.I);
     W.sh = take(TK * 4);
   }
+  W.total_base = off;
+  // small batches: room for split-K partial sums of the dense GEMMs (optional; lmoe_forward
+  // splits only when the caller's workspace includes it)
+  W.splitk = off;
+  if (D.T > 0 && D.T <= BLOCK_M) take(SPLITK_BYTES);
   W.total = off;
   return W;
 }
@@ -604,7 +609,7 @@ int lmoe_routed_backward(const lmoe_dims* dims, const void* packed, const void* 
   R.D = D;
   R.W = workspace_layout(D);
   R.B = bwd_layout(D);
-  if (ws_bytes < R.W.total || bwd_ws_bytes < R.B.total) return LMOE_ERR_WORKSPACE_TOO_SMALL;
+  if (ws_bytes < R.W.total_base || bwd_ws_bytes < R.B.total) return LMOE_ERR_WORKSPACE_TOO_SMALL;
   if (D.T == 0) return LMOE_OK;
   R.pk = static_cast<const uint8_t*>(packed);
   R.pb = static_cast<const uint8_t*>(packed_bwd);
@@ -649,7 +654,7 @@ int lmoe_backward(const lmoe_dims* dims, const void* packed, const void* packed_
   R.W = workspace_layout(D);
   R.B = bwd_layout(D);
   const LayerBwdLayout LB = layer_bwd_layout(D);
-  if (ws_bytes < R.W.total || bwd_ws_bytes < LB.total) return LMOE_ERR_WORKSPACE_TOO_SMALL;
+  if (ws_bytes < R.W.total_base || bwd_ws_bytes < LB.total) return LMOE_ERR_WORKSPACE_TOO_SMALL;
   if (D.T == 0) return LMOE_OK;
   using bf = __nv_bfloat16;
   R.pk = static_cast<const uint8_t*>(packed);
@@ -799,7 +804,12 @@ int lmoe_forward(const lmoe_dims* dims, const void* packed, const void* x, const
     return LMOE_ERR_INVALID_ARG;
   if (back && ((x && y == x) || (residual && y == residual))) return LMOE_ERR_INVALID_ARG;
   const WorkspaceLayout W = workspace_layout(D);
-  if (ws_bytes < W.total) return LMOE_ERR_WORKSPACE_TOO_SMALL;
+  if (ws_bytes < W.total_base) return LMOE_ERR_WORKSPACE_TOO_SMALL;
+  // Small whole-layer calls split the dense GEMMs' reductions when the workspace holds the
+  // partials.  The two phases never do: a batch split across ranks then routes on logits
+  // bit-identical to the whole batch's, whatever each part's size.
+  const bool splitk =
+      W.total > W.total_base && ws_bytes >= W.total && opt.phase == LMOE_PHASE_ALL;
   if ((opt.tau_in && !aligned16(opt.tau_in)) || (opt.logits_in && !aligned16(opt.logits_in)))
     return LMOE_ERR_INVALID_ARG;
   if (opt.tau_ema && !(opt.ema_beta >= 0.0f && opt.ema_beta <= 1.0f)) return LMOE_ERR_INVALID_ARG;
@@ -823,6 +833,13 @@ int lmoe_forward(const lmoe_dims* dims, const void* packed, const void* x, const
   bf* lat = reinterpret_cast<bf*>(ws + W.lat);
   bf* zh = reinterpret_cast<bf*>(ws + W.zh);
   const int sw = shared_width(D);
+  // the dense GEMMs' split-K scratch (one GEMM at a time, in stream order)
+  auto dense_split = [&](GemmArgs& g) {
+    if (!splitk) return;
+    g.partial = reinterpret_cast<float*>(ws + W.splitk);
+    g.partial_bytes = SPLITK_BYTES;
+    g.extra_launches = &launches;
+  };
   const int ldz = D.L + sw;
   const int T = D.T, TK = D.T * D.K;
 
@@ -869,6 +886,7 @@ int lmoe_forward(const lmoe_dims* dims, const void* packed, const void* x, const
     g.pre = static_cast<bf*>(opt.save_pre_shared);
     g.ldp = 2 * sw;
     g.inject_stall = inject_stall() ? 1 : 0;
+    dense_split(g);
     rc = launch_gemm(x, T, D.d, pk + P.w1, static_cast<uint64_t>(g.N), D.d, g, stream);
     if (rc != LMOE_OK) return rc;
     launches += 1;
@@ -954,6 +972,7 @@ int lmoe_forward(const lmoe_dims* dims, const void* packed, const void* x, const
       g.outf_t = logits_t;
       g.ldt = T;
     }
+    dense_split(g);
     rc = launch_gemm(lat, T, D.L, pk + P.wr, static_cast<uint64_t>(D.E), D.L, g, stream);
     if (rc != LMOE_OK) return rc;
     launches += 1;
@@ -1118,6 +1137,7 @@ int lmoe_forward(const lmoe_dims* dims, const void* packed, const void* x, const
     g.ldr = D.d;
     if (!overlap) {
       g.Kd = ldz;
+      dense_split(g);
       rc = launch_gemm(zh, T, ldz, pk + P.w2, static_cast<uint64_t>(D.d), ldz, g, stream);
     } else {
       if (cudaStreamWaitEvent(stream, static_cast<cudaEvent_t>(opt.aux_events[1]), 0) !=

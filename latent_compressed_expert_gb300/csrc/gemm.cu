@@ -64,6 +64,7 @@ struct GemmCfg {
 
 constexpr int GEMM_THREADS = 192;
 constexpr int GEMM_PAIR_MIN_K = 2048;  // reduction length from which tile pairs are used
+constexpr int SPLITK_MIN_KB = 4;       // K-blocks per split-K slice at least
 constexpr int RASTER_GROUP_M = 16;
 
 struct TileCoord {
@@ -80,7 +81,7 @@ struct TileCoord {
 template <int BN, int TM = BLOCK_M>  // TM: rows of an M-tile (of a tile pair)
 __device__ __forceinline__ TileCoord decode_tile(const GemmArgs& g, int nt, int mt, int tile) {
   int kgroup = 0;
-  if (g.groups > 0) {  // grouped-K: groups outermost, then the raster below
+  if (g.groups > 0 || g.ksplit > 1) {  // groups (or split-K slices) outermost, then the raster
     kgroup = tile / (mt * nt);
     tile -= kgroup * mt * nt;
   }
@@ -103,6 +104,12 @@ __device__ __forceinline__ TileCoord decode_tile(const GemmArgs& g, int nt, int 
     c.k0 = __ldg(g.kseg + kgroup);
     c.klen = __ldg(g.kseg + kgroup + 1) - c.k0;
     c.nk = (c.klen + BLOCK_K - 1) / BLOCK_K;
+  } else if (g.ksplit > 1) {  // slice kgroup of the K-blocks (the launcher leaves none empty)
+    const int nkb = g.Kd / BLOCK_K;
+    const int per = (nkb + g.ksplit - 1) / g.ksplit;
+    c.k0 = kgroup * per * BLOCK_K;
+    c.nk = min(per, nkb - kgroup * per);
+    c.klen = c.nk * BLOCK_K;
   } else {
     c.k0 = 0;
     c.klen = g.Kd;
@@ -275,7 +282,8 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA,
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nt = (g.N + BN - 1) / BN;
   const int mt_dense = (g.M + TM - 1) / TM;
-  const int total = mt_dense * nt * (g.groups > 0 ? g.groups : 1);
+  const int total =
+      mt_dense * nt * (g.groups > 0 ? g.groups : 1) * (g.ksplit > 1 ? g.ksplit : 1);
   const uint64_t limit = g.timeout_ns;
 
   if (threadIdx.x == 0) {
@@ -432,7 +440,8 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA,
         }
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-        const int nkt = g.Kd / BLOCK_K;
+        const int nkt =
+            g.ksplit > 1 ? decode_tile<BN, TM>(g, nt, mt_dense, tile).nk : g.Kd / BLOCK_K;
         bool ok = true;
         for (int kb = 0; kb < nkt; ++kb, ++it) {
           const int s = static_cast<int>(it % C::STAGES);
@@ -525,6 +534,18 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA,
             continue;
           }
           ptx::tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(ch * 32), v);
+          if (g.ksplit > 1) {  // split-K: this slice's fp32 partial sums
+            if (row_ok) {
+              float4* pp = reinterpret_cast<float4*>(
+                  g.partial + (static_cast<size_t>(tc.grp) * g.M + row) * g.N + col0);
+              const int nv4 = min(32, g.N - col0) / 4;  // N is a multiple of 16
+#pragma unroll
+              for (int q4 = 0; q4 < 8; ++q4)
+                if (q4 < nv4)
+                  pp[q4] = make_float4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]);
+            }
+            continue;
+          }
           if (row_ok) {
             if (col0 + 32 <= g.N)
               epilogue_store(g, row, col0, v, c, inv_c);
@@ -543,6 +564,84 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA,
   if (warp == 1) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
+}
+
+// Split-K: out = epilogue(sum over the slices of partial[s, row, :]), each chunk's slices
+// added in a fixed order (deterministic).  Two forms:
+//   WARP = false: one thread per row and 32-column chunk adds the slices in order and applies
+//     the epilogue; for a few slices and many chunks.
+//   WARP = true: one warp per chunk.  Lane l loads 16 bytes (float4 l % 8 of the chunk) of
+//     every fourth slice from l / 8, so a warp has 32 loads in flight; a fixed shuffle tree
+//     adds the four lanes of each float4, and lane 0 gathers the chunk and applies the
+//     epilogue.  For many slices and few chunks.
+constexpr int SPLITK_WARP_MIN = 7;  // slices from which the warp form is used
+
+template <bool WARP>
+__global__ void __launch_bounds__(256) splitk_reduce_kernel(const GemmArgs g) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const float c = g.c, inv_c = 1.0f / g.c;
+  const int lane = threadIdx.x & 31;
+  const int nch = (g.N + 31) / 32;
+  const int64_t n = static_cast<int64_t>(g.M) * nch;
+  const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t w = WARP ? (tid >> 5) : tid; w < n; w += WARP ? (stride >> 5) : stride) {
+    const int row = static_cast<int>(w / nch);
+    const int col0 = static_cast<int>(w % nch) * 32;
+    const int nv4 = min(32, g.N - col0) / 4;  // N is a multiple of 16
+    float v[32];
+    if constexpr (WARP) {  // w is warp-uniform here
+      const int q4 = lane & 7;
+      float4 a = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      if (q4 < nv4) {
+        for (int sl = lane >> 3; sl < g.ksplit; sl += 4) {
+          const float4 t = __ldg(reinterpret_cast<const float4*>(
+              g.partial + (static_cast<size_t>(sl) * g.M + row) * g.N + col0) + q4);
+          a.x += t.x;
+          a.y += t.y;
+          a.z += t.z;
+          a.w += t.w;
+        }
+      }
+#pragma unroll
+      for (int o = 8; o <= 16; o <<= 1) {
+        a.x += __shfl_xor_sync(0xffffffffu, a.x, o);
+        a.y += __shfl_xor_sync(0xffffffffu, a.y, o);
+        a.z += __shfl_xor_sync(0xffffffffu, a.z, o);
+        a.w += __shfl_xor_sync(0xffffffffu, a.w, o);
+      }
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        v[4 * q] = __shfl_sync(0xffffffffu, a.x, q);
+        v[4 * q + 1] = __shfl_sync(0xffffffffu, a.y, q);
+        v[4 * q + 2] = __shfl_sync(0xffffffffu, a.z, q);
+        v[4 * q + 3] = __shfl_sync(0xffffffffu, a.w, q);
+      }
+      if (lane != 0) continue;
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+      for (int sl = 0; sl < g.ksplit; ++sl) {
+        const float4* pp = reinterpret_cast<const float4*>(
+            g.partial + (static_cast<size_t>(sl) * g.M + row) * g.N + col0);
+#pragma unroll
+        for (int q4 = 0; q4 < 8; ++q4) {
+          if (q4 < nv4) {
+            const float4 t = __ldg(pp + q4);
+            v[4 * q4] += t.x;
+            v[4 * q4 + 1] += t.y;
+            v[4 * q4 + 2] += t.z;
+            v[4 * q4 + 3] += t.w;
+          }
+        }
+      }
+    }
+    if (nv4 == 8)
+      epilogue_store(g, row, col0, v, c, inv_c);
+    else
+      epilogue_store_partial(g, row, col0, 4 * nv4, v);
   }
 }
 
@@ -593,8 +692,8 @@ static int launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArg
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return LMOE_ERR_CUDA;
   int grid = (g.max_ctas > 0 && g.max_ctas < sms) ? g.max_ctas : sms;
-  const int64_t tiles =
-      ceil_div(g.M, BLOCK_M * MT) * ceil_div(g.N, BN) * (g.groups > 0 ? g.groups : 1);
+  const int64_t tiles = ceil_div(g.M, BLOCK_M * MT) * ceil_div(g.N, BN) *
+                        (g.groups > 0 ? g.groups : 1) * (g.ksplit > 1 ? g.ksplit : 1);
   if (tiles < grid) grid = static_cast<int>(tiles);
   if (grid <= 0) return LMOE_OK;
   return launch_pdl(gemm_tcgen05_kernel<BN, MT>, grid, GEMM_THREADS, C::SMEM_BYTES, stream, ta, tb,
@@ -634,13 +733,42 @@ int launch_gemm(const void* A, uint64_t a_rows, int a_ld, const void* B, uint64_
                              static_cast<uint64_t>(b_ld), static_cast<uint32_t>(bn))) {
     return LMOE_ERR_CUDA;
   }
-  // Tile pairs (two 128-row M-tiles sharing each B stage) when the problem is dense, has at
-  // least two pairs per SM and a long reduction: the pair's undivided accumulator is drained
-  // while no MMA runs, which only pays when the MMAs take far longer.
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return LMOE_ERR_CUDA;
+  // Split-K when one M-tile's column tiles would leave most SMs idle (small batches): each
+  // slice of K-blocks is its own tile, and a second kernel adds the slices.
+  if (g.groups == 0 && g.partial && g.M <= BLOCK_M) {
+    const int64_t tiles = ceil_div(g.N, bn);
+    const int nkb = g.Kd / BLOCK_K;
+    int64_t ks = sms / tiles;
+    ks = ks < nkb / SPLITK_MIN_KB ? ks : nkb / SPLITK_MIN_KB;
+    const int64_t fit = static_cast<int64_t>(g.partial_bytes /
+                                             (static_cast<size_t>(g.M) * g.N * sizeof(float)));
+    ks = ks < fit ? ks : fit;
+    if (ks >= 2) {
+      const int per = static_cast<int>(ceil_div(nkb, ks));
+      GemmArgs gs = g;
+      gs.ksplit = static_cast<int>(ceil_div(nkb, per));  // no slice is left empty
+      const int rc = bn == 256 ? launch_bn<256, 1>(ta, tb, gs, stream)
+                               : launch_bn<128, 1>(ta, tb, gs, stream);
+      if (rc != LMOE_OK) return rc;
+      const int64_t chunks = static_cast<int64_t>(g.M) * ceil_div(g.N, 32);
+      const bool warp = gs.ksplit >= SPLITK_WARP_MIN;
+      const int64_t blocks = ceil_div(chunks, warp ? 8 : 256);
+      const unsigned grid = static_cast<unsigned>(blocks < 16 * sms ? blocks : 16 * sms);
+      if ((warp ? launch_pdl(splitk_reduce_kernel<true>, grid, 256, 0, stream, gs)
+                : launch_pdl(splitk_reduce_kernel<false>, grid, 256, 0, stream, gs)) !=
+          cudaSuccess)
+        return LMOE_ERR_CUDA;
+      if (g.extra_launches) *g.extra_launches += 1;
+      return LMOE_OK;
+    }
+  }
+  // Tile pairs (two 128-row M-tiles sharing each B stage) when the problem is dense, has at
+  // least two pairs per SM and a long reduction: the pair's undivided accumulator is drained
+  // while no MMA runs, which only pays when the MMAs take far longer.
   const bool pairs = g.groups == 0 && g.Kd >= GEMM_PAIR_MIN_K &&
                      ceil_div(g.M, 2 * BLOCK_M) * ceil_div(g.N, bn) >= 2 * static_cast<int64_t>(sms);
   if (bn == 256)

@@ -17,8 +17,11 @@ struct PackedLayout {
 // Offsets (bytes) of the forward workspace; every buffer 256-aligned.
 struct WorkspaceLayout {
   size_t err, lat, logits, logits_t, tau, idx, gate, masks, base, offsets, ct_off, inv, src_tok,
-      h, o, zh, ys, total;
+      h, o, zh, ys;
   size_t lat8, slat, h8, sh;  // e4m3 experts: quantised latent and SiTU output, row scales
+  size_t splitk;              // small batches: split-K partial sums of the dense GEMMs
+  size_t total_base;          // bytes without the split-K region (which is optional)
+  size_t total;               // bytes with it
 };
 
 PackedLayout packed_layout(const lmoe_dims& D);
@@ -69,7 +72,17 @@ struct GemmArgs {
   const int32_t* kseg;
   long long group_stride;
   const int32_t* row_map;
+  // Split-K (dense mode, set by the launcher when one M-tile leaves most SMs idle): slice s of
+  // ksplit reduces its share of the K-blocks into partial[s, M, N] (fp32), and a second kernel
+  // sums the slices in order and applies the epilogue.  partial: caller's scratch of
+  // partial_bytes, or null (no split).
+  int ksplit;
+  float* partial;
+  size_t partial_bytes;
+  int* extra_launches;    // optional: incremented by the kernels launch_gemm enqueues beyond
+                          // the GEMM itself (the split-K sum)
 };
+constexpr size_t SPLITK_BYTES = size_t{12} << 20;  // workspace for split-K partials (T <= 128)
 
 // Routed-expert GEMMs (gemm_grouped.cu): out[tok, r] = act[tok, :] . W[e][r, :] for the
 // token rows of each expert segment, weight rows on the MMA's M side.

@@ -51,9 +51,12 @@ static int noalloc_scratch_for_current_device(void** out) {
 extern "C" int lmoe_forward_noalloc(const lmoe_dims* dims, const void* packed, const void* x,
                                     const void* residual, void* y, lmoe_io* io, void* stream) {
   using namespace lmoe;
-  const size_t need = lmoe_workspace_bytes(dims);
   // invalid or unsupported dims: lmoe_forward reports which, before it enqueues anything
-  if (need == 0) return lmoe_forward(dims, packed, x, residual, y, nullptr, 0, io, stream);
+  if (lmoe_workspace_bytes(dims) == 0)
+    return lmoe_forward(dims, packed, x, residual, y, nullptr, 0, io, stream);
+  // the array must hold the base workspace; a small batch's split-K region is used when the
+  // array also has room for it
+  const size_t need = workspace_layout(*dims).total_base;
   if (need > NOALLOC_SCRATCH_BYTES) return LMOE_ERR_WORKSPACE_TOO_SMALL;
   void* scratch = nullptr;
   const int rc = noalloc_scratch_for_current_device(&scratch);

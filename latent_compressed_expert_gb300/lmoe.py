@@ -161,6 +161,16 @@ def packed_bytes(dims: Dims) -> int:
     return int(load().lmoe_packed_bytes(ctypes.byref(dims)))
 
 
+SPLITK_BYTES = 12 << 20  # the optional split-K region of lmoe_workspace_bytes (T <= 128)
+
+
+def workspace_base_bytes(dims: Dims) -> int:
+    """The smallest workspace lmoe_forward accepts: lmoe_workspace_bytes less the optional
+    split-K region of small batches."""
+    full = workspace_bytes(dims)
+    return full - SPLITK_BYTES if full and 0 < dims.T <= 128 else full
+
+
 def workspace_bytes(dims: Dims) -> int:
     return int(load().lmoe_workspace_bytes(ctypes.byref(dims)))
 

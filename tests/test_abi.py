@@ -117,9 +117,12 @@ def test_forward_argument_checks(lib):
     # y aliasing x is rejected
     assert lib.lmoe_forward(ctypes.byref(d), fake, fake, None, fake, ctypes.c_void_p(0x2000),
                             ws, None, None) == lmoe.LMOE_ERR_INVALID_ARG
-    # a workspace one byte short is rejected
+    # a workspace one byte short of the base size is rejected (the split-K region of a small
+    # batch is optional)
+    base = lmoe.workspace_base_bytes(d)
+    assert base == ws - 12 * 2 ** 20
     assert lib.lmoe_forward(ctypes.byref(d), fake, fake, None, ctypes.c_void_p(0x3000),
-                            ctypes.c_void_p(0x4000), ws - 1, None, None) \
+                            ctypes.c_void_p(0x4000), base - 1, None, None) \
         == lmoe.LMOE_ERR_WORKSPACE_TOO_SMALL
 
 
@@ -239,7 +242,7 @@ def test_backward_argument_checks(lib):
              None, fake, fake, fake, fake, fake, fake, fake, fake, bw, None) \
         == lmoe.LMOE_ERR_INVALID_ARG                                          # pre misaligned
     assert call(bw_bytes=bw - 1) == lmoe.LMOE_ERR_WORKSPACE_TOO_SMALL
-    assert call(ws_bytes=ws - 1) == lmoe.LMOE_ERR_WORKSPACE_TOO_SMALL
+    assert call(ws_bytes=lmoe.workspace_base_bytes(d) - 1) == lmoe.LMOE_ERR_WORKSPACE_TOO_SMALL
     assert call(dims=lmoe.dims_of(synth.TINY, T=0), ws_bytes=1 << 30, bw_bytes=1 << 30) \
         == lmoe.LMOE_OK
     d8 = lmoe.dims_of(synth.PREFILL, expert_fp8=True)

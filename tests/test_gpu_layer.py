@@ -357,3 +357,31 @@ def test_checked_mode_reports_nonfinite_logits(dev, monkeypatch):
     assert layer.device_error() == lmoe.LMOE_OK
     idx = dbg["idx"].cpu().numpy()
     assert idx.min() >= 0 and idx.max() < sh.E
+
+
+def test_decode_split_k_matches_unsplit(dev):
+    """A small whole-layer batch splits the dense GEMMs' reductions (the workspace includes
+    the split-K region): three more launches, outputs within the layer's tolerance of the
+    unsplit call in a workspace without the region, routing identical."""
+    sh = synth.LayerShape("k3_decode_small", T=64, d=7168, L=3584, E=128, K=16, I=512, S=2,
+                          Is=2048)
+    w = synth.make_weights(sh, seed=31, device=dev)
+    layer = lmoe.Layer(sh, w)
+    x = synth.make_x(sh, seed=32, device=dev)
+    tau = torch.zeros(sh.E, dtype=torch.float32, device=dev)
+    y1, d1 = layer.forward(x, residual=x, tau=tau, debug=True)
+    y1 = y1.clone()
+    n1 = layer.last_kernel_launches
+    full = layer.ws_bytes
+    layer.ws_bytes = lmoe.workspace_base_bytes(lmoe.dims_of(sh, T=sh.T))
+    try:
+        y2, d2 = layer.forward(x, residual=x, tau=tau, debug=True)
+        n2 = layer.last_kernel_launches
+    finally:
+        layer.ws_bytes = full
+    torch.cuda.synchronize()
+    assert layer.device_error() == 0
+    assert n1 == n2 + 3
+    assert torch.equal(d1["idx"], d2["idx"])
+    H.assert_close(y1.float().cpu().numpy(), y2.float().cpu().numpy().astype(np.float64),
+                   "decode split-K vs unsplit")
