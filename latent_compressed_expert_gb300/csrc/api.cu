@@ -79,6 +79,7 @@ WorkspaceLayout workspace_layout(const lmoe_dims& D) {
   W.lat = take(T * D.L * 2);
   W.logits = take(T * D.E * 4);
   W.logits_t = take(T * D.E * 4);
+  W.scores = take(T * D.E * 4);
   W.tau = take(static_cast<size_t>(D.E) * 4);
   W.idx = take(TK * 4);
   W.gate = take(TK * 4);
@@ -442,7 +443,7 @@ int lmoe_thresholds(const float* logits, int T, int E, int K, int k_rank, float*
     k = static_cast<int>(f < 1 ? 1 : (f > T ? T : f));
   }
   // token-major input: each expert's column is read with stride E
-  return launch_thresholds(logits, T, E, E, 1, k, tau, static_cast<cudaStream_t>(stream));
+  return launch_thresholds(logits, T, E, E, 1, k, tau, false, static_cast<cudaStream_t>(stream));
 }
 
 int lmoe_quantize_e4m3(const void* x, long long rows, int cols, uint8_t* codes, float* scales,
@@ -526,7 +527,7 @@ int lmoe_route(const float* logits, const float* tau, int T, int E, int K, int32
   if (K > E || K > 32 || E > 4096) return LMOE_ERR_UNSUPPORTED;
   if (T == 0) return LMOE_OK;
   if (!logits || !idx || !gate) return LMOE_ERR_INVALID_ARG;
-  return launch_route(logits, tau, T, E, K, idx, gate, scores_out,
+  return launch_route(logits, tau, T, E, K, idx, gate, scores_out, false,
                       static_cast<cudaStream_t>(stream));
 }
 
@@ -949,17 +950,10 @@ int lmoe_forward(const lmoe_dims* dims, const void* packed, const void* x, const
       opt.logits_in ? opt.logits_in : reinterpret_cast<const float*>(ws + W.logits);
   float* logits_t = reinterpret_cast<float*>(ws + W.logits_t);  // expert-major copy
   const bool solve_tau = !opt.tau_in && opt.balance;
-  // who needs the expert-major copy: in-batch thresholds of a whole-layer call, or the
-  // candidates of a router phase (an experts phase makes its own when it solves thresholds)
-  const bool want_t =
-      (opt.phase == LMOE_PHASE_ALL && solve_tau) || (opt.phase == LMOE_PHASE_ROUTER && opt.cand_out);
-  if (!front) {
-    if (solve_tau) {
-      rc = launch_transpose_f32(logits, T, D.E, logits_t, stream);
-      if (rc != LMOE_OK) return rc;
-      launches += 1;
-    }
-  } else if (!opt.logits_in) {
+  // the candidates of a router phase read the logits expert-major; in-batch thresholds read
+  // the scores expert-major, which the scores kernel writes into the same buffer
+  const bool want_t = opt.phase == LMOE_PHASE_ROUTER && opt.cand_out;
+  if (front && !opt.logits_in) {
     GemmArgs g = gemm_defaults(err, D.c);
     g.M = T;
     g.N = D.E;
@@ -976,7 +970,7 @@ int lmoe_forward(const lmoe_dims* dims, const void* packed, const void* x, const
     rc = launch_gemm(lat, T, D.L, pk + P.wr, static_cast<uint64_t>(D.E), D.L, g, stream);
     if (rc != LMOE_OK) return rc;
     launches += 1;
-  } else if (want_t) {
+  } else if (front && want_t) {
     rc = launch_transpose_f32(logits, T, D.E, logits_t, stream);
     if (rc != LMOE_OK) return rc;
     launches += 1;
@@ -1004,13 +998,17 @@ int lmoe_forward(const lmoe_dims* dims, const void* packed, const void* x, const
     return LMOE_OK;
   }
   if (!mark(LMOE_STAGE_THRESHOLDS, 0)) return LMOE_ERR_CUDA;
-  // 3. thresholds
+  // 3. thresholds, on scores computed once for them and the selection
   const float* tau = opt.tau_in;
+  const float* scores = reinterpret_cast<float*>(ws + W.scores);
   if (solve_tau) {
+    rc = launch_scores(logits, T, D.E, reinterpret_cast<float*>(ws + W.scores), logits_t, stream);
+    if (rc != LMOE_OK) return rc;
+    launches += 1;
     float* t = reinterpret_cast<float*>(ws + W.tau);
     const int64_t f = static_cast<int64_t>(T) * D.K / D.E;
     const int k = static_cast<int>(f < 1 ? 1 : (f > T ? T : f));
-    rc = launch_thresholds(logits_t, T, D.E, 1, T, k, t, stream);
+    rc = launch_thresholds(logits_t, T, D.E, 1, T, k, t, true, stream);
     if (rc != LMOE_OK) return rc;
     tau = t;
     launches += 1;
@@ -1026,7 +1024,8 @@ int lmoe_forward(const lmoe_dims* dims, const void* packed, const void* x, const
   // 4. top-K routing
   int32_t* idx = reinterpret_cast<int32_t*>(ws + W.idx);
   float* gate = reinterpret_cast<float*>(ws + W.gate);
-  rc = launch_route(logits, tau, T, D.E, D.K, idx, gate, nullptr, stream);
+  rc = solve_tau ? launch_route(scores, tau, T, D.E, D.K, idx, gate, nullptr, true, stream)
+                  : launch_route(logits, tau, T, D.E, D.K, idx, gate, nullptr, false, stream);
   if (rc != LMOE_OK) return rc;
   if (!mark(LMOE_STAGE_DISPATCH, 1)) return LMOE_ERR_CUDA;
   // 5. dispatch into expert-contiguous segments

@@ -16,8 +16,8 @@ struct PackedLayout {
 
 // Offsets (bytes) of the forward workspace; every buffer 256-aligned.
 struct WorkspaceLayout {
-  size_t err, lat, logits, logits_t, tau, idx, gate, masks, base, offsets, ct_off, inv, src_tok,
-      h, o, zh, ys;
+  size_t err, lat, logits, logits_t, scores, tau, idx, gate, masks, base, offsets, ct_off, inv,
+      src_tok, h, o, zh, ys;
   size_t lat8, slat, h8, sh;  // e4m3 experts: quantised latent and SiTU output, row scales
   size_t splitk;              // small batches: split-K partial sums of the dense GEMMs
   size_t total_base;          // bytes without the split-K region (which is optional)
@@ -130,12 +130,16 @@ bool make_tmap_bf16(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t col
 int launch_gemm(const void* A, uint64_t a_rows, int a_ld, const void* B, uint64_t b_rows,
                 int b_ld, const GemmArgs& args, cudaStream_t stream);
 
+// Top-K routing of [T, E] logits, or with scores of the router scores themselves.
 int launch_route(const float* logits, const float* tau, int T, int E, int K, int32_t* idx,
-                 float* gate, float* scores_out, cudaStream_t stream);
-// Thresholds from logits stored with element (t, e) at z[t * stride_t + e * stride_e]
-// (stride_t = 1, stride_e = T is the fast, expert-major layout).
+                 float* gate, float* scores_out, bool scores, cudaStream_t stream);
+// Thresholds from logits (or, with scores, router scores) stored with element (t, e) at
+// z[t * stride_t + e * stride_e] (stride_t = 1, stride_e = T is the fast, expert-major
+// layout).
 int launch_thresholds(const float* z, int T, int E, int64_t stride_t, int64_t stride_e, int k,
-                      float* tau, cudaStream_t stream);
+                      float* tau, bool scores, cudaStream_t stream);
+// Router scores of [T, E] logits z: s[T, E] and, if s_t is given, the expert-major s_t[E, T].
+int launch_scores(const float* z, int T, int E, float* s, float* s_t, cudaStream_t stream);
 // Per expert, the logits of the min(k, T) largest scores (rows of cand, stride ldc), then
 // -FLT_MAX up to row k.
 int launch_candidates(const float* z, int T, int E, int64_t stride_t, int64_t stride_e, int k,

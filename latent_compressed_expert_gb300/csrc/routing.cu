@@ -9,8 +9,9 @@
 // per-expert Top-K thresholds in place of the predecessor's bias updates).
 //
 // Every decision here is taken in fp32 with explicitly rounded operations (__fmul_rn,
-// __fadd_rn, __fmaf_rn, __fdiv_rn), so that no contraction or approximation changes a
-// result bit: a CPU evaluation of the same sequence of IEEE operations agrees exactly.
+// __fadd_rn, __fmaf_rn, __fdiv_rn, __frcp_rn), so that no contraction or approximation
+// changes a result bit: a CPU evaluation of the same sequence of IEEE operations agrees
+// exactly.
 #include <cfloat>
 
 #include "common.cuh"
@@ -46,7 +47,7 @@ __device__ __forceinline__ float score_sigmoid(float z) {
   const float s1 = __int_as_float((n1 + 127) << 23);
   const float s2 = __int_as_float((n2 + 127) << 23);
   const float e = __fmul_rn(__fmul_rn(p, s1), s2);
-  return __fdiv_rn(1.0f, __fadd_rn(1.0f, e));
+  return __frcp_rn(__fadd_rn(1.0f, e));  // correctly rounded, so equal to 1.0f / (1 + e)
 }
 
 // Order-preserving map of an fp32 value to uint32 (larger float -> larger key); -0 is
@@ -57,52 +58,16 @@ __device__ __forceinline__ uint32_t order_key(float a) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// ------------------------------------------------------------------------------------
-// Top-K routing: one warp per token.  The warp writes the token's keys a = fl32(s - tau)
-// into shared memory, then K times takes the largest remaining key (ties to the lower
-// expert id) with two warp reductions.  Each lane keeps its best and second-best candidate,
-// so a lane whose best is taken promotes its runner-up and only rescans its share of the
-// experts when it loses a second time.
-// ------------------------------------------------------------------------------------
-constexpr int ROUTE_WARPS = 4;
+// Score of a routing input: the input itself when it already is a score (SCORES), else the
+// score of a logit.
+template <bool SCORES>
+__device__ __forceinline__ float score_of(float v) {
+  return SCORES ? v : score_sigmoid(v);
+}
 
-__global__ void __launch_bounds__(ROUTE_WARPS * 32)
-route_kernel(const float* __restrict__ logits, const float* __restrict__ tau, int T, int E,
-             int K, int32_t* __restrict__ idx, float* __restrict__ gate,
-             float* __restrict__ scores_out) {
-  extern __shared__ uint32_t route_smem[];
-  pdl_wait();
-  pdl_launch_dependents();
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  uint32_t* keys = route_smem + static_cast<size_t>(warp) * E;
-  const int t = blockIdx.x * ROUTE_WARPS + warp;
-  if (t >= T) return;
-  const float* zrow = logits + static_cast<size_t>(t) * E;
-
-  // eight independent logit loads in flight per lane before their keys are computed
-  constexpr int B = 8;
-  for (int e0 = lane; e0 < E; e0 += B * 32) {
-    float zv[B], tv[B];
-#pragma unroll
-    for (int i = 0; i < B; ++i) {
-      const int e = e0 + i * 32;
-      zv[i] = e < E ? __ldg(zrow + e) : 0.0f;
-      tv[i] = (tau && e < E) ? __ldg(tau + e) : 0.0f;
-    }
-#pragma unroll
-    for (int i = 0; i < B; ++i) {
-      const int e = e0 + i * 32;
-      if (e < E) {
-        const float s = score_sigmoid(zv[i]);
-        if (scores_out) scores_out[static_cast<size_t>(t) * E + e] = s;
-        const float a = tau ? __fsub_rn(s, tv[i]) : s;
-        keys[e] = order_key(a);
-      }
-    }
-  }
-  __syncwarp();
-
+// K rounds of argmax over keys[0..E) in shared memory (consumed), ties to the lower expert
+// id: lane j returns the j-th winner (lanes >= K return 0).  Called by a whole warp.
+__device__ __forceinline__ int select_rounds(uint32_t* keys, int E, int K, int lane) {
   // best (b1) and runner-up (b2) among e = lane, lane + 32, ...; key 0 = none.  The scan is
   // ascending in e and replaces only on a strictly larger key, so equal keys keep the lower e.
   uint32_t b1k = 0u, b2k = 0u;
@@ -144,8 +109,237 @@ route_kernel(const float* __restrict__ logits, const float* __restrict__ tau, in
     }
     __syncwarp();
   }
+  return my_idx;
+}
+
+// ------------------------------------------------------------------------------------
+// Top-K routing: one warp per token.  The warp writes the token's keys a = fl32(s - tau)
+// into shared memory, then K times takes the largest remaining key (ties to the lower
+// expert id) with two warp reductions.  Each lane keeps its best and second-best candidate,
+// so a lane whose best is taken promotes its runner-up and only rescans its share of the
+// experts when it loses a second time.
+// ------------------------------------------------------------------------------------
+constexpr int ROUTE_WARPS = 4;
+
+template <bool SCORES>
+__global__ void __launch_bounds__(ROUTE_WARPS * 32)
+route_kernel(const float* __restrict__ logits, const float* __restrict__ tau, int T, int E,
+             int K, int32_t* __restrict__ idx, float* __restrict__ gate,
+             float* __restrict__ scores_out) {
+  extern __shared__ uint32_t route_smem[];
+  pdl_wait();
+  pdl_launch_dependents();
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint32_t* keys = route_smem + static_cast<size_t>(warp) * E;
+  const int t = blockIdx.x * ROUTE_WARPS + warp;
+  if (t >= T) return;
+  const float* zrow = logits + static_cast<size_t>(t) * E;
+
+  // eight independent logit loads in flight per lane before their keys are computed
+  constexpr int B = 8;
+  for (int e0 = lane; e0 < E; e0 += B * 32) {
+    float zv[B], tv[B];
+#pragma unroll
+    for (int i = 0; i < B; ++i) {
+      const int e = e0 + i * 32;
+      zv[i] = e < E ? __ldg(zrow + e) : 0.0f;
+      tv[i] = (tau && e < E) ? __ldg(tau + e) : 0.0f;
+    }
+#pragma unroll
+    for (int i = 0; i < B; ++i) {
+      const int e = e0 + i * 32;
+      if (e < E) {
+        const float s = score_of<SCORES>(zv[i]);
+        if (scores_out) scores_out[static_cast<size_t>(t) * E + e] = s;
+        const float a = tau ? __fsub_rn(s, tv[i]) : s;
+        keys[e] = order_key(a);
+      }
+    }
+  }
+  __syncwarp();
+
+  const int my_idx = select_rounds(keys, E, K, lane);
   // gates: s of the winners, fp32 sum in slot order, then one rounded division each
-  const float sj = (lane < K) ? score_sigmoid(__ldg(zrow + my_idx)) : 0.0f;
+  const float sj = (lane < K) ? score_of<SCORES>(__ldg(zrow + my_idx)) : 0.0f;
+  float sum = 0.0f;
+  for (int j = 0; j < K; ++j) sum = __fadd_rn(sum, __shfl_sync(0xffffffffu, sj, j));
+  if (lane < K) {
+    idx[static_cast<size_t>(t) * K + lane] = my_idx;
+    gate[static_cast<size_t>(t) * K + lane] = __fdiv_rn(sj, sum);
+  }
+}
+
+// ------------------------------------------------------------------------------------
+// Top-K routing, register form (E a multiple of 4 and at most 4 * 32 * RF_NQ, rows 16-byte
+// aligned): one warp per token, lane l holding the keys of experts 4(l + 32q) + c in
+// registers, the CTA's thresholds in shared memory.  The K-th largest of the lanes' maxima
+// is a lower bound B on the token's K-th largest key (K lanes each hold a key >= B).  The
+// winners, in order (larger key first, then the lower expert id), are then found among few
+// keys:
+//   - at most RF_CAND keys >= B: each is ranked against the others;
+//   - else, fewer than K keys > B (many keys equal to B, as when scores saturate at 1 and
+//     so do the thresholds): the keys > B ranked as above, then the experts whose key is B
+//     in ascending id;
+//   - else K rounds of argmax over all E keys in shared memory.
+// Each gives the same experts in the same order as K rounds of argmax.
+// ------------------------------------------------------------------------------------
+constexpr int RF_WARPS = 8;
+constexpr int RF_NQ = 8;      // float4 of logits per lane: E <= 1024
+constexpr int RF_CAND = 64;   // candidates ranked in place
+constexpr int RF_WARP_WORDS = 2 * RF_CAND + 32;  // + E words for the last form
+
+template <bool SCORES>
+__global__ void __launch_bounds__(RF_WARPS * 32, 3)
+route_reg_kernel(const float* __restrict__ logits, const float* __restrict__ tau, int T, int E,
+                 int K, int32_t* __restrict__ idx, float* __restrict__ gate,
+                 float* __restrict__ scores_out) {
+  extern __shared__ uint32_t rf_smem[];
+  pdl_wait();
+  pdl_launch_dependents();
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nq = E >> 2;
+  float4* tau_s = reinterpret_cast<float4*>(rf_smem);  // [nq] (zeros without thresholds)
+  for (int j = threadIdx.x; j < nq; j += RF_WARPS * 32)
+    tau_s[j] = tau ? __ldg(reinterpret_cast<const float4*>(tau) + j)
+                   : make_float4(0.f, 0.f, 0.f, 0.f);
+  __syncthreads();
+  uint32_t* ckey = rf_smem + E + static_cast<size_t>(warp) * (RF_WARP_WORDS + E);
+  int32_t* ce = reinterpret_cast<int32_t*>(ckey + RF_CAND);
+  int32_t* sel = ce + RF_CAND;                                  // [32] winners by slot
+  uint32_t* keys = reinterpret_cast<uint32_t*>(sel + 32);       // [E] last form
+  const int t = blockIdx.x * RF_WARPS + warp;
+  if (t >= T) return;
+  const float* zrow = logits + static_cast<size_t>(t) * E;
+
+  float4 zv[RF_NQ];
+#pragma unroll
+  for (int q = 0; q < RF_NQ; ++q) {
+    const int j = lane + 32 * q;
+    zv[q] = j < nq ? __ldg(reinterpret_cast<const float4*>(zrow) + j)
+                   : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  // keys; 0 marks no expert (every finite a has a key >= 1)
+  uint32_t key[4 * RF_NQ];
+#pragma unroll
+  for (int i = 0; i < 4 * RF_NQ; ++i) key[i] = 0u;
+  uint32_t mk = 0u;
+#pragma unroll
+  for (int q = 0; q < RF_NQ; ++q) {
+    if (32 * q >= nq) break;  // warp-uniform: no lane holds experts past this row
+    const int j = lane + 32 * q;
+    if (j < nq) {
+      const float4 tq = tau_s[j];
+      const float zz[4] = {zv[q].x, zv[q].y, zv[q].z, zv[q].w};
+      const float tt[4] = {tq.x, tq.y, tq.z, tq.w};
+      float ss[4];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        ss[c] = score_of<SCORES>(zz[c]);
+        key[4 * q + c] = order_key(tau ? __fsub_rn(ss[c], tt[c]) : ss[c]);
+        mk = key[4 * q + c] > mk ? key[4 * q + c] : mk;
+      }
+      if (scores_out)
+        reinterpret_cast<float4*>(scores_out + static_cast<size_t>(t) * E)[j] =
+            make_float4(ss[0], ss[1], ss[2], ss[3]);
+    }
+  }
+  // B = the K-th largest lane maximum: bitonic sort of the 32 maxima (ascending), lane 32 - K
+  uint32_t v = mk;
+#pragma unroll
+  for (int w = 2; w <= 32; w <<= 1) {
+#pragma unroll
+    for (int j = w >> 1; j > 0; j >>= 1) {
+      const uint32_t o = __shfl_xor_sync(0xffffffffu, v, j);
+      const bool up = (lane & w) == 0, lower = (lane & j) == 0;
+      v = (lower == up) ? (o < v ? o : v) : (o > v ? o : v);
+    }
+  }
+  const uint32_t bound = __shfl_sync(0xffffffffu, v, 32 - K);
+  int c_ge = 0, c_gt = 0;
+#pragma unroll
+  for (int i = 0; i < 4 * RF_NQ; ++i) {
+    c_ge += (key[i] != 0u && key[i] >= bound) ? 1 : 0;
+    c_gt += key[i] > bound ? 1 : 0;
+  }
+  const int n_ge = __reduce_add_sync(0xffffffffu, static_cast<unsigned>(c_ge));
+  const int n_gt = __reduce_add_sync(0xffffffffu, static_cast<unsigned>(c_gt));
+  // rank the keys >= B (strict = false) or > B (strict = true) against each other
+  auto rank_keys = [&](bool strict, int cnt, int n) {
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += u;
+    }
+    int p = incl - cnt;
+#pragma unroll
+    for (int i = 0; i < 4 * RF_NQ; ++i) {
+      if (key[i] != 0u && (strict ? key[i] > bound : key[i] >= bound)) {
+        ckey[p] = key[i];
+        ce[p] = 4 * (lane + 32 * (i >> 2)) + (i & 3);
+        ++p;
+      }
+    }
+    __syncwarp();
+    for (int m0 = lane; m0 < n; m0 += 32) {
+      const uint32_t km = ckey[m0];
+      const int em = ce[m0];
+      int rank = 0;
+      for (int m = 0; m < n; ++m) {
+        const uint32_t k2 = ckey[m];
+        rank += (k2 > km || (k2 == km && ce[m] < em)) ? 1 : 0;
+      }
+      if (rank < K) sel[rank] = em;
+    }
+  };
+  int my_idx = 0;
+  if (n_ge <= RF_CAND) {
+    rank_keys(false, c_ge, n_ge);
+    __syncwarp();
+    if (lane < K) my_idx = sel[lane];
+  } else if (n_gt < K) {
+    rank_keys(true, c_gt, n_gt);
+    // slots n_gt .. K-1: the experts whose key is B, in ascending id (row q, then lane, then c)
+    int filled = n_gt;
+#pragma unroll
+    for (int q = 0; q < RF_NQ; ++q) {
+      if (32 * q >= nq || filled >= K) break;  // warp-uniform
+      uint32_t f = 0u;
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        f |= (key[4 * q + c] != 0u && key[4 * q + c] == bound) ? (1u << c) : 0u;
+      const int cnt = __popc(f);
+      int incl = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += u;
+      }
+      int slot = filled + incl - cnt;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        if (f & (1u << c)) {
+          if (slot < K) sel[slot] = 4 * (lane + 32 * q) + c;
+          ++slot;
+        }
+      }
+      filled += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    __syncwarp();
+    if (lane < K) my_idx = sel[lane];
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4 * RF_NQ; ++i) {
+      const int j = lane + 32 * (i >> 2);
+      if (j < nq) keys[4 * j + (i & 3)] = key[i];
+    }
+    __syncwarp();
+    my_idx = select_rounds(keys, E, K, lane);
+  }
+  // gates: s of the winners, fp32 sum in slot order, then one rounded division each
+  const float sj = (lane < K) ? score_of<SCORES>(__ldg(zrow + my_idx)) : 0.0f;
   float sum = 0.0f;
   for (int j = 0; j < K; ++j) sum = __fadd_rn(sum, __shfl_sync(0xffffffffu, sj, j));
   if (lane < K) {
@@ -176,6 +370,7 @@ struct KthResult {
 // k-th largest score (1 <= k <= T) of column `col` (T logits, stride stride_t).  Called by
 // all TH_THREADS threads of the CTA; `th_smem` is the layout launch_thresholds sizes.  When
 // the column is staged, vals[0..T) keeps the score bits on return.
+template <bool SCORES>
 __device__ __forceinline__ KthResult select_kth_score(const float* __restrict__ col, int T,
                                                      int64_t stride_t, int k,
                                                      uint32_t* th_smem, bool staged) {
@@ -198,7 +393,7 @@ __device__ __forceinline__ KthResult select_kth_score(const float* __restrict__ 
 #pragma unroll
       for (int i = 0; i < B; ++i) {
         const int t = t0 + i * TH_THREADS;
-        if (t < T) vals[t] = __float_as_uint(score_sigmoid(zv[i]));
+        if (t < T) vals[t] = __float_as_uint(score_of<SCORES>(zv[i]));
       }
     }
   }
@@ -207,7 +402,7 @@ __device__ __forceinline__ KthResult select_kth_score(const float* __restrict__ 
   int n = T;
   auto key_at = [&](int i) -> uint32_t {
     if (from_cand) return cand[i];
-    return staged ? vals[i] : __float_as_uint(score_sigmoid(__ldg(col + i * stride_t)));
+    return staged ? vals[i] : __float_as_uint(score_of<SCORES>(__ldg(col + i * stride_t)));
   };
   uint32_t prefix = 0u, mask = 0u;
   int krem = k;
@@ -297,6 +492,7 @@ __device__ __forceinline__ KthResult select_kth_score(const float* __restrict__ 
   return r;
 }
 
+template <bool SCORES>
 __global__ void __launch_bounds__(TH_THREADS)
 thresholds_kernel(const float* __restrict__ z, int T, int64_t stride_t, int64_t stride_e,
                   int k, float* __restrict__ tau) {
@@ -305,9 +501,105 @@ thresholds_kernel(const float* __restrict__ z, int T, int64_t stride_t, int64_t 
   pdl_launch_dependents();
 
   const int e = blockIdx.x;
-  const KthResult r = select_kth_score(z + static_cast<int64_t>(e) * stride_e, T, stride_t, k,
+  const KthResult r = select_kth_score<SCORES>(z + static_cast<int64_t>(e) * stride_e, T, stride_t, k,
                                        th_smem, T <= TH_SMEM_MAX_T);
   if (threadIdx.x == 0) tau[e] = __uint_as_float(r.key);
+}
+
+// Quantile-Balancing thresholds for columns of at most TH_THREADS * TH_KPT tokens and
+// k <= TH_THREADS (SCORES: the columns hold router scores, not logits): one CTA per expert, thread i holding the scores of tokens i, i + 256, ...
+// in registers.  The k-th largest of the threads' maxima is a lower bound B on the column's
+// k-th largest score (k threads each hold a score >= B).  If fewer than k scores exceed B,
+// the k-th largest is B itself (the common case when the top of a column saturates at 1);
+// otherwise it is the k-th largest of the scores > B -- about 2.5 % of the column when k is
+// the fair-share rank.  Both selections are bit-by-bit searches for the largest v with
+// #{keys >= v} >= k, counted with __syncthreads_count.  More than TH_BCAND scores > B falls
+// back to the radix select over the whole column.
+constexpr int TH_KPT = 32;
+constexpr int TH_BCAND = 1024;
+static_assert(TH_BCAND <= TH_CAND && TH_BCAND % TH_THREADS == 0, "candidate buffer");
+
+template <bool SCORES>
+__global__ void __launch_bounds__(TH_THREADS)
+thresholds_bound_kernel(const float* __restrict__ z, int T, int64_t stride_t, int64_t stride_e,
+                        int k, float* __restrict__ tau) {
+  extern __shared__ uint32_t th_smem[];
+  pdl_wait();
+  pdl_launch_dependents();
+
+  uint32_t* ctl = th_smem + TH_BINS;         // [3]: count of scores > B
+  uint32_t* cand = th_smem + TH_BINS + 32;   // [TH_BCAND]
+  const int e = blockIdx.x;
+  const int lane = threadIdx.x & 31;
+  const float* col = z + static_cast<int64_t>(e) * stride_e;
+  if (threadIdx.x == 0) ctl[3] = 0u;
+
+  // score bits (non-negative, below 2^30); past T a key is 0, which no search value reaches.
+  // All the thread's logits are loaded first (one round trip), then scored in place.
+  uint32_t key[TH_KPT];
+#pragma unroll
+  for (int i = 0; i < TH_KPT; ++i) {
+    const int t = static_cast<int>(threadIdx.x) + i * TH_THREADS;
+    key[i] = t < T ? __float_as_uint(__ldg(col + t * stride_t)) : 0u;
+  }
+  uint32_t mx = 0u;
+#pragma unroll
+  for (int i = 0; i < TH_KPT; ++i) {
+    const int t = static_cast<int>(threadIdx.x) + i * TH_THREADS;
+    key[i] = t < T ? __float_as_uint(score_of<SCORES>(__uint_as_float(key[i]))) : 0u;
+    mx = key[i] > mx ? key[i] : mx;
+  }
+  // B = the k-th largest of the threads' maxima
+  uint32_t bound = 0u;
+#pragma unroll 1
+  for (int b = 29; b >= 0; --b) {
+    const uint32_t v = bound | (1u << b);
+    if (__syncthreads_count(mx >= v) >= k) bound = v;
+  }
+  // scores > B: a warp scan of the threads' counts, one shared atomic per warp
+  int cnt = 0;
+#pragma unroll
+  for (int i = 0; i < TH_KPT; ++i) cnt += key[i] > bound ? 1 : 0;
+  int incl = cnt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  uint32_t base = 0u;
+  if (lane == 31) base = atomicAdd(&ctl[3], static_cast<uint32_t>(incl));
+  base = __shfl_sync(0xffffffffu, base, 31) + static_cast<uint32_t>(incl - cnt);
+  __syncthreads();
+  const uint32_t n = ctl[3];
+  uint32_t result = bound;
+  if (n >= static_cast<uint32_t>(k) && n <= static_cast<uint32_t>(TH_BCAND)) {
+    uint32_t p = base;
+#pragma unroll
+    for (int i = 0; i < TH_KPT; ++i)
+      if (key[i] > bound) cand[p++] = key[i];
+    __syncthreads();
+    constexpr int SLOTS = TH_BCAND / TH_THREADS;
+    const int used = (static_cast<int>(n) + TH_THREADS - 1) / TH_THREADS;  // block-uniform
+    uint32_t cv[SLOTS];
+#pragma unroll
+    for (int j = 0; j < SLOTS; ++j) {
+      const uint32_t q = threadIdx.x + j * TH_THREADS;
+      cv[j] = q < n ? cand[q] : 0u;
+    }
+    result = 0u;
+#pragma unroll 1
+    for (int b = 29; b >= 0; --b) {
+      const uint32_t v = result | (1u << b);
+      int c = 0;
+#pragma unroll
+      for (int j = 0; j < SLOTS; ++j)
+        if (j < used) c += __syncthreads_count(cv[j] >= v);
+      if (c >= k) result = v;
+    }
+  } else if (n > static_cast<uint32_t>(TH_BCAND)) {
+    result = select_kth_score<SCORES>(col, T, stride_t, k, th_smem, false).key;
+  }
+  if (threadIdx.x == 0) tau[e] = __uint_as_float(result);
 }
 
 // Threshold candidates of one batch: column e of cand ([k, E], row stride ldc) receives the
@@ -331,7 +623,7 @@ candidates_kernel(const float* __restrict__ z, int T, int64_t stride_t, int64_t 
   const int kk = k < T ? k : T;
   if (kk > 0) {
   const bool staged = T <= TH_SMEM_MAX_T;
-  const KthResult r = select_kth_score(col, T, stride_t, kk, th_smem, staged);
+  const KthResult r = select_kth_score<false>(col, T, stride_t, kk, th_smem, staged);
   const uint32_t* vals = th_smem + TH_BINS + 32 + TH_CAND;
   const int take_eq = kk - r.above;  // copies of the k-th score to emit
   if (threadIdx.x == 0) run[0] = run[1] = 0u;
@@ -401,37 +693,107 @@ transpose_f32_kernel(const float* __restrict__ in, int T, int E, float* __restri
   }
 }
 
+// Router scores, each computed once: s[t, e] = score(z[t, e]) row-major for the top-K
+// selection and, when s_t is given, s_t[e, t] expert-major for the thresholds, through
+// 32 x 32 shared-memory tiles (each thread's four logits are loaded before any is scored).
+__global__ void __launch_bounds__(256)
+scores_kernel(const float* __restrict__ z, int T, int E, float* __restrict__ s,
+              float* __restrict__ s_t) {
+  __shared__ float tile[32][33];
+  pdl_wait();
+  pdl_launch_dependents();
+
+  const int e0 = blockIdx.x * 32, t0 = blockIdx.y * 32;
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8
+  const int e = e0 + tx;
+  float v[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int t = t0 + ty + 8 * i;
+    v[i] = (t < T && e < E) ? __ldg(z + static_cast<size_t>(t) * E + e) : 0.0f;
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int t = t0 + ty + 8 * i;
+    v[i] = score_sigmoid(v[i]);
+    if (t < T && e < E) s[static_cast<size_t>(t) * E + e] = v[i];
+    tile[ty + 8 * i][tx] = v[i];
+  }
+  if (!s_t) return;  // grid-uniform
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int er = e0 + ty + 8 * i, t = t0 + tx;
+    if (t < T && er < E) s_t[static_cast<size_t>(er) * T + t] = tile[tx][ty + 8 * i];
+  }
+}
+
 // ------------------------------------------------------------------------------------
 // launchers
 // ------------------------------------------------------------------------------------
 int launch_route(const float* logits, const float* tau, int T, int E, int K, int32_t* idx,
-                 float* gate, float* scores_out, cudaStream_t stream) {
+                 float* gate, float* scores_out, bool scores, cudaStream_t stream) {
   if (T == 0) return LMOE_OK;
+  auto a16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+  if (E % 4 == 0 && E <= 4 * 32 * RF_NQ && a16(logits) && (!tau || a16(tau)) &&
+      (!scores_out || a16(scores_out))) {
+    const size_t smem =
+        (E + static_cast<size_t>(RF_WARPS) * (RF_WARP_WORDS + E)) * sizeof(uint32_t);
+    const int grid = static_cast<int>(ceil_div(T, RF_WARPS));
+    auto kern = scores ? route_reg_kernel<true> : route_reg_kernel<false>;
+    return launch_pdl(kern, grid, RF_WARPS * 32, smem, stream, logits, tau, T, E, K, idx, gate,
+                      scores_out) == cudaSuccess
+               ? LMOE_OK
+               : LMOE_ERR_CUDA;
+  }
   const size_t smem = static_cast<size_t>(ROUTE_WARPS) * E * sizeof(uint32_t);
+  auto kern = scores ? route_kernel<true> : route_kernel<false>;
   if (smem > 48 * 1024) {
-    if (cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
       return LMOE_ERR_CUDA;
   }
   const int grid = static_cast<int>(ceil_div(T, ROUTE_WARPS));
-  return launch_pdl(route_kernel, grid, ROUTE_WARPS * 32, smem, stream, logits, tau, T, E, K, idx,
-                    gate, scores_out) == cudaSuccess
+  return launch_pdl(kern, grid, ROUTE_WARPS * 32, smem, stream, logits, tau, T, E, K, idx, gate,
+                    scores_out) == cudaSuccess
              ? LMOE_OK
              : LMOE_ERR_CUDA;
 }
 
 int launch_thresholds(const float* z, int T, int E, int64_t stride_t, int64_t stride_e, int k,
-                      float* tau, cudaStream_t stream) {
+                      float* tau, bool scores, cudaStream_t stream) {
   if (T == 0) return LMOE_OK;
+  if (T <= TH_THREADS * TH_KPT && k <= TH_THREADS) {
+    // bound-and-select form; its fallback uses the histogram and candidate buffers
+    const size_t smem = (TH_BINS + 32 + TH_CAND) * sizeof(uint32_t);
+    auto kern = scores ? thresholds_bound_kernel<true> : thresholds_bound_kernel<false>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess)
+      return LMOE_ERR_CUDA;
+    return launch_pdl(kern, E, TH_THREADS, smem, stream, z, T, stride_t, stride_e, k, tau) ==
+                   cudaSuccess
+               ? LMOE_OK
+               : LMOE_ERR_CUDA;
+  }
   const size_t smem =
       (TH_BINS + 32 + TH_CAND + (T <= TH_SMEM_MAX_T ? T : 0)) * sizeof(uint32_t);
+  auto kern = scores ? thresholds_kernel<true> : thresholds_kernel<false>;
   if (smem > 48 * 1024) {
-    if (cudaFuncSetAttribute(thresholds_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
       return LMOE_ERR_CUDA;
   }
-  return launch_pdl(thresholds_kernel, E, TH_THREADS, smem, stream, z, T, stride_t, stride_e, k,
-                    tau) == cudaSuccess
+  return launch_pdl(kern, E, TH_THREADS, smem, stream, z, T, stride_t, stride_e, k, tau) ==
+                 cudaSuccess
+             ? LMOE_OK
+             : LMOE_ERR_CUDA;
+}
+
+int launch_scores(const float* z, int T, int E, float* s, float* s_t, cudaStream_t stream) {
+  if (T == 0 || E == 0) return LMOE_OK;
+  if (ceil_div(T, 32) > 65535) return LMOE_ERR_UNSUPPORTED;  // grid rows
+  const dim3 grid(static_cast<unsigned>(ceil_div(E, 32)), static_cast<unsigned>(ceil_div(T, 32)));
+  return launch_pdl(scores_kernel, grid, 256, 0, stream, z, T, E, s, s_t) == cudaSuccess
              ? LMOE_OK
              : LMOE_ERR_CUDA;
 }

@@ -59,7 +59,8 @@ def _logits(T, E, kind, seed):
 ROUTE_CASES = [(64, 16, 4, "normal"), (1000, 64, 4, "ties"), (8192, 896, 16, "normal"),
                (257, 896, 16, "ties"), (1, 896, 16, "normal"), (33, 16, 16, "normal"),
                (100, 4096, 32, "normal"), (500, 896, 16, "saturated"), (2048, 448, 8, "zipf"),
-               (3, 48, 1, "normal")]
+               (3, 48, 1, "normal"), (50, 90, 8, "normal"), (700, 1024, 32, "normal"),
+               (300, 1024, 32, "ties")]
 
 
 @pytest.mark.parametrize("T,E,K,kind", ROUTE_CASES)
@@ -76,9 +77,21 @@ def test_route_bit_exact(dev, oracle_mod, T, E, K, kind):
         assert np.array_equal(gate.cpu().numpy().view(np.int32), r_gate.view(np.int32))
 
 
+def test_scores_sweep_bit_exact(dev, oracle_mod):
+    """The fixed-sequence score over 4.2 M logits spanning [-90, 90], dense near the clamp and
+    the subnormal results (z near -88) and near 0: every score bit-equal to the oracle's."""
+    parts = [np.linspace(-90.0, 90.0, 2 ** 21, dtype=np.float32),
+             np.linspace(-88.5, -86.0, 2 ** 20, dtype=np.float32),
+             np.linspace(-1.0, 1.0, 2 ** 20, dtype=np.float32)]
+    z = np.concatenate(parts).reshape(4096, 1024)
+    _, _, sc = lmoe.route(torch.from_numpy(z).to(dev), None, 1, want_scores=True)
+    _, _, r_sc = oracle_mod.route(z, None, 1)
+    assert np.array_equal(sc.cpu().numpy().view(np.int32), r_sc.view(np.int32))
+
+
 THRESH_CASES = [(64, 16, 4, 0), (8192, 896, 16, 0), (32768, 896, 16, 0), (40000, 64, 4, 0),
                 (100, 32, 4, 1), (100, 32, 4, 100), (7, 16, 16, 0), (1, 896, 16, 0),
-                (3000, 448, 8, 0)]
+                (3000, 448, 8, 0), (5000, 64, 4, 256), (5000, 64, 4, 257), (8193, 896, 16, 0)]
 
 
 @pytest.mark.parametrize("T,E,K,k_rank", THRESH_CASES)
