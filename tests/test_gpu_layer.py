@@ -120,6 +120,10 @@ EDGE_SHAPES = [
     ("no_shared", synth.LayerShape("s0", T=100, d=256, L=128, E=16, K=4, I=64, S=0, Is=0)),
     ("one_shared", synth.LayerShape("s1", T=77, d=384, L=192, E=48, K=6, I=128, S=1, Is=192)),
     ("K32", synth.LayerShape("k32", T=50, d=256, L=128, E=64, K=32, I=64, S=2, Is=64)),
+    # more than 1024 experts: the shared-memory top-K on scores
+    ("E1040", synth.LayerShape("e1040", T=300, d=256, L=128, E=1040, K=8, I=64, S=1, Is=64)),
+    # a fair-share rank above 256 at T <= 8192: the radix thresholds on scores
+    ("k300", synth.LayerShape("k300", T=2400, d=256, L=128, E=64, K=8, I=64, S=1, Is=64)),
 ]
 
 
