@@ -507,14 +507,15 @@ thresholds_kernel(const float* __restrict__ z, int T, int64_t stride_t, int64_t 
 }
 
 // Quantile-Balancing thresholds for columns of at most TH_THREADS * TH_KPT tokens and
-// k <= TH_THREADS (SCORES: the columns hold router scores, not logits): one CTA per expert, thread i holding the scores of tokens i, i + 256, ...
-// in registers.  The k-th largest of the threads' maxima is a lower bound B on the column's
-// k-th largest score (k threads each hold a score >= B).  If fewer than k scores exceed B,
-// the k-th largest is B itself (the common case when the top of a column saturates at 1);
-// otherwise it is the k-th largest of the scores > B -- about 2.5 % of the column when k is
-// the fair-share rank.  Both selections are bit-by-bit searches for the largest v with
-// #{keys >= v} >= k, counted with __syncthreads_count.  More than TH_BCAND scores > B falls
-// back to the radix select over the whole column.
+// k <= TH_THREADS (SCORES: the columns hold router scores, not logits): one CTA per expert,
+// thread i holding the scores of tokens i, i + 256, ... in registers.  The k-th largest of
+// the threads' maxima is a lower bound B on the column's k-th largest score (k threads each
+// hold a score >= B).  If fewer than k scores exceed B, the k-th largest is B itself (as
+// when the top of a column saturates at 1); otherwise it is the k-th largest of the scores
+// > B -- about 2.5 % of the column when k is the fair-share rank.  Both selections are
+// bit-by-bit searches for the largest v with #{keys >= v} >= k, counted with
+// __syncthreads_count.  More than TH_BCAND scores > B falls back to the radix select over
+// the whole column.
 constexpr int TH_KPT = 32;
 constexpr int TH_BCAND = 1024;
 static_assert(TH_BCAND <= TH_CAND && TH_BCAND % TH_THREADS == 0, "candidate buffer");
