@@ -501,8 +501,8 @@ thresholds_kernel(const float* __restrict__ z, int T, int64_t stride_t, int64_t 
   pdl_launch_dependents();
 
   const int e = blockIdx.x;
-  const KthResult r = select_kth_score<SCORES>(z + static_cast<int64_t>(e) * stride_e, T, stride_t, k,
-                                       th_smem, T <= TH_SMEM_MAX_T);
+  const KthResult r = select_kth_score<SCORES>(z + static_cast<int64_t>(e) * stride_e, T,
+                                               stride_t, k, th_smem, T <= TH_SMEM_MAX_T);
   if (threadIdx.x == 0) tau[e] = __uint_as_float(r.key);
 }
 
