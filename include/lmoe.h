@@ -155,6 +155,11 @@ typedef struct lmoe_io {
   void *save_pre_shared; /* [T, 2 S Is] bf16, or NULL: likewise the shared experts'
                             pre-activations (per token, groups of 16 gate then 16 value
                             features over the S Is concatenated features) */
+  float *y_f32_out;      /* [T, d] fp32, or NULL: the output as the up-projection's epilogue
+                            computes it in fp32 (accumulator + residual), before the store
+                            that rounds it to bf16; y is exactly this value rounded to
+                            nearest even.  For checking the arithmetic apart from the final
+                            rounding; costs one extra fp32 store of the output */
 } lmoe_io;
 
 /* lmoe_io.phase.  The layer splits where its only cross-batch quantity, the thresholds, is
@@ -205,6 +210,13 @@ size_t lmoe_workspace_bytes(const lmoe_dims *dims);
  * Errors: INVALID_ARG for null pointers or T < 0, E < 1, K < 1, k_rank > T. */
 int lmoe_thresholds(const float *logits, int T, int E, int K, int k_rank, float *tau,
                     void *stream);
+
+/* The rank k of the Quantile-Balancing threshold among a column's T scores, the fair share
+ * of tokens per expert ([IK3] Quantile Balancing passage): k = max(1, floor(T*K/E)), at
+ * most T; 0 for T == 0.  lmoe_thresholds (k_rank <= 0) and lmoe_forward use it; a batch
+ * spread over ranks passes the whole batch's T.  Returns -1 for K < 1, E < 1, T < 0 or
+ * T > 2^40.  Host function; touches no device. */
+int lmoe_fair_share_rank(long long T, int K, int E);
 
 /* Threshold candidates of one part of a batch that is spread over several ranks.
  * [IK3] Quantile Balancing passage: the threshold is read off the distribution of the
@@ -391,19 +403,29 @@ int lmoe_quantize_e4m3(const void *x, long long rows, int cols, uint8_t *codes, 
  * process starts.  Arguments and results are those of lmoe_forward without the workspace.
  * Scratch: a LMOE_NOALLOC_SCRATCH_BYTES (24 MiB) array in the library's device image,
  * reserved on every GPU that loads the library until the process exits.  It covers a K3
- * decode batch of up to 155 tokens (64 tokens need 9.9 MiB, 21.9 MiB with the split-K
+ * decode batch of up to 152 tokens (64 tokens need 10.07 MiB, or 22.07 MiB with the split-K
  * region, which is used when it fits).  When the workspace without that region exceeds the
  * array, the call returns LMOE_ERR_WORKSPACE_TOO_SMALL and enqueues nothing.
- * Set-up: the first call on each device looks up the array's device address
- * (cudaGetSymbolAddress) with that device current; make that first call before any stream
- * capture.  No call allocates or frees memory.
- * Sharing: every call on a device uses the same array, which keeps the last call's
+ * Set-up: the first call in each CUDA context looks up the array's device address in that
+ * context (cudaGetSymbolAddress, which may load the library's device code); make that first
+ * call before any stream capture.  The address is cached per context, so a second context on
+ * the same device, or the new context after cudaDeviceReset, gets its own array.  No call
+ * allocates or frees memory.
+ * Sharing: every call in a context uses the same array, which keeps the last call's
  * contents; each call clears what must start at zero.  Calls whose work overlaps on the
  * GPU (different streams, or host threads without ordering between them) race on the array
- * and corrupt each other's results: serialise them.  A device-side time-out is recorded in
- * the array and cannot be read back with lmoe_last_device_error. */
+ * and corrupt each other's results: serialise them.  A device-side error of a call (a
+ * bounded wait that ran out; checked mode's non-finite logit) is recorded in the array:
+ * read it with lmoe_noalloc_last_device_error after the stream has synchronised and before
+ * the next call, which clears it. */
 int lmoe_forward_noalloc(const lmoe_dims *dims, const void *packed, const void *x,
                          const void *residual, void *y, lmoe_io *io, void *stream);
+
+/* lmoe_last_device_error for lmoe_forward_noalloc: synchronously reads and clears the device
+ * error flag in the current context's scratch array (no counterpart in the pages either).
+ * Returns what lmoe_last_device_error returns for a workspace, or LMOE_ERR_CUDA if the
+ * array cannot be reached. */
+int lmoe_noalloc_last_device_error(void);
 
 /* Synchronously read and clear the device error flag that lmoe_forward's kernels write
  * into `workspace`.  Every device-side wait is bounded (2 s by default; the environment

@@ -432,16 +432,19 @@ int lmoe_pack_weights(const lmoe_dims* dims, const lmoe_weights* w, void* packed
                      static_cast<cudaStream_t>(stream));
 }
 
+int lmoe_fair_share_rank(long long T, int K, int E) {
+  if (K < 1 || E < 1 || T < 0 || T > (static_cast<long long>(1) << 40)) return -1;
+  if (T == 0) return 0;
+  const long long f = T * K / E;
+  return static_cast<int>(f < 1 ? 1 : (f > T ? T : f));
+}
+
 int lmoe_thresholds(const float* logits, int T, int E, int K, int k_rank, float* tau,
                     void* stream) {
   if (T < 0 || E < 1 || K < 1 || k_rank > T) return LMOE_ERR_INVALID_ARG;
   if (T == 0) return LMOE_OK;
   if (!logits || !tau) return LMOE_ERR_INVALID_ARG;
-  int k = k_rank;
-  if (k <= 0) {
-    const int64_t f = static_cast<int64_t>(T) * K / E;
-    k = static_cast<int>(f < 1 ? 1 : (f > T ? T : f));
-  }
+  const int k = k_rank > 0 ? k_rank : lmoe_fair_share_rank(T, K, E);
   // token-major input: each expert's column is read with stride E
   return launch_thresholds(logits, T, E, E, 1, k, tau, false, static_cast<cudaStream_t>(stream));
 }
@@ -816,6 +819,7 @@ int lmoe_forward(const lmoe_dims* dims, const void* packed, const void* x, const
   if (opt.tau_ema && !(opt.ema_beta >= 0.0f && opt.ema_beta <= 1.0f)) return LMOE_ERR_INVALID_ARG;
   if (opt.save_pre && (D.expert_fp8 || !aligned16(opt.save_pre))) return LMOE_ERR_INVALID_ARG;
   if (opt.save_pre_shared && !aligned16(opt.save_pre_shared)) return LMOE_ERR_INVALID_ARG;
+  if (opt.y_f32_out && !aligned16(opt.y_f32_out)) return LMOE_ERR_INVALID_ARG;
 
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   using bf = __nv_bfloat16;
@@ -1006,8 +1010,7 @@ int lmoe_forward(const lmoe_dims* dims, const void* packed, const void* x, const
     if (rc != LMOE_OK) return rc;
     launches += 1;
     float* t = reinterpret_cast<float*>(ws + W.tau);
-    const int64_t f = static_cast<int64_t>(T) * D.K / D.E;
-    const int k = static_cast<int>(f < 1 ? 1 : (f > T ? T : f));
+    const int k = lmoe_fair_share_rank(T, D.K, D.E);
     rc = launch_thresholds(logits_t, T, D.E, 1, T, k, t, true, stream);
     if (rc != LMOE_OK) return rc;
     tau = t;
@@ -1134,6 +1137,8 @@ int lmoe_forward(const lmoe_dims* dims, const void* packed, const void* x, const
     g.ld0 = D.d;
     g.resid = static_cast<const bf*>(residual);
     g.ldr = D.d;
+    g.outf = opt.y_f32_out;
+    g.ldf = D.d;
     if (!overlap) {
       g.Kd = ldz;
       dense_split(g);

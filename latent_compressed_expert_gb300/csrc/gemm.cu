@@ -226,6 +226,12 @@ __device__ __forceinline__ void epilogue_store(const GemmArgs& g, int row, int c
           }
         }
       }
+      if (g.outf) {  // the value before its rounding to bf16
+        float4* o = reinterpret_cast<float4*>(g.outf + r * g.ldf + col0);
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          o[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+      }
       store_bf16x32(g.out0 + r * g.ld0 + col0, v);
       break;
     }
@@ -249,6 +255,7 @@ __device__ __forceinline__ void epilogue_store_partial(const GemmArgs& g, int ro
       float t = v[i];
       if (g.addf) t += g.addf[r * g.lda + col];
       if (g.resid) t += __bfloat162float(g.resid[r * g.ldr + col]);
+      if (g.outf) g.outf[r * g.ldf + col] = t;
       g.out0[r * g.ld0 + col] = __float2bfloat16_rn(t);
     }
   }

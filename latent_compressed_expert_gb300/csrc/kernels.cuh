@@ -33,7 +33,8 @@ enum EpiMode : int {
   EPI_F32 = 1,    // outf[r, c] = acc
   EPI_SITU = 2,   // out1[r, c/2 + i] = bf16(SiTU(gate_i, value_i)) over 16+16 interleave
   EPI_SPLIT = 3,  // columns < split: EPI_BF16 to out0; others: EPI_SITU to out1 (c - split)
-  EPI_RESID = 4   // out0[r, c] = bf16(acc + resid[r, c]) (resid may be null)
+  EPI_RESID = 4   // out0[r, c] = bf16(acc + resid[r, c]) (resid may be null); with outf,
+                  // also outf[r, c] = acc + resid[r, c] in fp32 (the value before rounding)
 };
 
 struct GemmArgs {

@@ -12,8 +12,13 @@
 // The array below is reserved on every GPU on which this library's device code is loaded,
 // for the life of the process.  Host code cannot use the array's name as a device address
 // (in host code it names a host-side stand-in), so the device address is looked up with
-// cudaGetSymbolAddress once per device, on the first call made with that device current,
-// and cached.
+// cudaGetSymbolAddress.  The runtime loads this library's device code into each CUDA context
+// separately -- a second context on the same device, or the new primary context after
+// cudaDeviceReset, holds its own copy of the array at its own address -- so the address is
+// cached per context, keyed by the context's unique id (cuCtxGetId), which the driver never
+// hands out twice in a process.  Without those driver calls it is looked up at every call.
+#include <cuda.h>
+
 #include <mutex>
 
 #include "common.cuh"
@@ -26,23 +31,77 @@ static_assert(NOALLOC_SCRATCH_BYTES == LMOE_NOALLOC_SCRATCH_BYTES, "header and l
 
 static __device__ __align__(256) uint8_t noalloc_scratch[NOALLOC_SCRATCH_BYTES];
 
-constexpr int NOALLOC_MAX_DEVICES = 64;
-static void* noalloc_scratch_addr[NOALLOC_MAX_DEVICES];
+typedef CUresult (*ctx_get_current_fn)(CUcontext*);
+typedef CUresult (*ctx_get_id_fn)(CUcontext, unsigned long long*);
+
+struct ContextApi {
+  ctx_get_current_fn get_current = nullptr;
+  ctx_get_id_fn get_id = nullptr;
+};
+
+static const ContextApi& context_api() {
+  static ContextApi api;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      api.get_current = reinterpret_cast<ctx_get_current_fn>(p);
+    p = nullptr;
+    q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      api.get_id = reinterpret_cast<ctx_get_id_fn>(p);
+  });
+  return api;
+}
+
+// Unique id of the context current on this thread; false if there is none or it cannot be read.
+static bool current_context_id(unsigned long long* id) {
+  const ContextApi& api = context_api();
+  if (!api.get_current || !api.get_id) return false;
+  CUcontext ctx = nullptr;
+  if (api.get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return false;
+  return api.get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+constexpr int NOALLOC_CACHE = 64;
+struct ScratchEntry {
+  unsigned long long ctx_id;
+  void* addr;
+};
+static ScratchEntry noalloc_cache[NOALLOC_CACHE];
+static int noalloc_cached = 0;  // entries filled (a ring once all are)
 static std::mutex noalloc_mutex;
 
-// Device address of the array on the current device (looked up once per device).
-static int noalloc_scratch_for_current_device(void** out) {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess) return LMOE_ERR_CUDA;
-  if (dev < 0 || dev >= NOALLOC_MAX_DEVICES) return LMOE_ERR_UNSUPPORTED;
+// Device address of the array in the current context.  The first call in a context looks it
+// up (which may load this library's device code into the context); later calls in the same
+// context take it from the cache.
+static int noalloc_scratch_for_current_context(void** out) {
   std::lock_guard<std::mutex> lock(noalloc_mutex);
-  if (noalloc_scratch_addr[dev] == nullptr) {
-    void* p = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&p, noalloc_scratch);
-    if (e != cudaSuccess || p == nullptr) return LMOE_ERR_CUDA;
-    noalloc_scratch_addr[dev] = p;
+  unsigned long long id = 0;
+  if (current_context_id(&id)) {
+    const int n = noalloc_cached < NOALLOC_CACHE ? noalloc_cached : NOALLOC_CACHE;
+    for (int i = 0; i < n; ++i) {
+      if (noalloc_cache[i].ctx_id == id) {
+        *out = noalloc_cache[i].addr;
+        return LMOE_OK;
+      }
+    }
   }
-  *out = noalloc_scratch_addr[dev];
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, noalloc_scratch);
+  if (e != cudaSuccess || p == nullptr) return LMOE_ERR_CUDA;
+  // the lookup makes the device's primary context current if no context was: key by the
+  // context it resolved in
+  if (current_context_id(&id)) {
+    noalloc_cache[noalloc_cached % NOALLOC_CACHE] = ScratchEntry{id, p};
+    ++noalloc_cached;
+  }
+  *out = p;
   return LMOE_OK;
 }
 
@@ -59,9 +118,18 @@ extern "C" int lmoe_forward_noalloc(const lmoe_dims* dims, const void* packed, c
   const size_t need = workspace_layout(*dims).total_base;
   if (need > NOALLOC_SCRATCH_BYTES) return LMOE_ERR_WORKSPACE_TOO_SMALL;
   void* scratch = nullptr;
-  const int rc = noalloc_scratch_for_current_device(&scratch);
+  const int rc = noalloc_scratch_for_current_context(&scratch);
   if (rc != LMOE_OK) return rc;
   // lmoe_forward zeroes the one word that must start at zero (the device error flag) and
   // writes every other scratch buffer before reading it.
   return lmoe_forward(dims, packed, x, residual, y, scratch, NOALLOC_SCRATCH_BYTES, io, stream);
+}
+
+extern "C" int lmoe_noalloc_last_device_error(void) {
+  using namespace lmoe;
+  void* scratch = nullptr;
+  const int rc = noalloc_scratch_for_current_context(&scratch);
+  if (rc != LMOE_OK) return rc;
+  // the array's first word is the forward workspace's device error flag
+  return lmoe_last_device_error(scratch);
 }

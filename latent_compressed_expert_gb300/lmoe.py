@@ -43,7 +43,7 @@ class IO(ctypes.Structure):
                 ("aux_stream", _vp), ("aux_events", _vp * 2), ("shared_sms", _i),
                 ("phase", _i), ("cand_out", _vp), ("cand_k", _i),
                 ("tau_ema", _vp), ("ema_beta", _f), ("ema_first", _i), ("load_stats", _vp),
-                ("save_pre", _vp), ("save_pre_shared", _vp)]
+                ("save_pre", _vp), ("save_pre_shared", _vp), ("y_f32_out", _vp)]
 
 
 OVERLAP_MIN_T = 512  # LMOE_OVERLAP_MIN_T
@@ -64,6 +64,7 @@ SIGNATURES = {
     "lmoe_workspace_bytes": (_sz, [ctypes.POINTER(Dims)]),
     "lmoe_thresholds": (_i, [_vp, _i, _i, _i, _i, _vp, _vp]),
     "lmoe_threshold_candidates": (_i, [_vp, _i, _i, _i, _vp, _vp]),
+    "lmoe_fair_share_rank": (_i, [ctypes.c_longlong, _i, _i]),
     "lmoe_quantize_e4m3": (_i, [_vp, ctypes.c_longlong, _i, _vp, _vp, _vp]),
     "lmoe_tau_ema": (_i, [_vp, _vp, _i, _f, _i, _vp]),
     "lmoe_packed_backward_bytes": (_sz, [ctypes.POINTER(Dims)]),
@@ -86,6 +87,7 @@ SIGNATURES = {
     "lmoe_gemm_bf16": (_i, [_vp, _vp, _vp, _i, _i, _i, _vp, _vp]),
     "lmoe_forward_noalloc": (_i, [ctypes.POINTER(Dims), _vp, _vp, _vp, _vp, ctypes.POINTER(IO),
                                   _vp]),
+    "lmoe_noalloc_last_device_error": (_i, []),
     "lmoe_last_device_error": (_i, [_vp]),
     "lmoe_error_string": (ctypes.c_char_p, [_i]),
     "lmoe_version": (ctypes.c_char_p, []),
@@ -162,6 +164,7 @@ def packed_bytes(dims: Dims) -> int:
 
 
 SPLITK_BYTES = 12 << 20  # the optional split-K region of lmoe_workspace_bytes (T <= 128)
+NOALLOC_SCRATCH_BYTES = 24 << 20  # LMOE_NOALLOC_SCRATCH_BYTES: lmoe_forward_noalloc's array
 
 
 def workspace_base_bytes(dims: Dims) -> int:
@@ -303,8 +306,11 @@ def ep_combine(idx: torch.Tensor, disp: dict, inv: torch.Tensor, gate: torch.Ten
 
 
 def fair_share_rank(T: int, K: int, E: int) -> int:
-    """The threshold's rank among a column's T scores: max(1, floor(T*K/E)), at most T."""
-    return max(1, min(T, (T * K) // E)) if T > 0 else 1
+    """The threshold's rank among a column's T scores (lmoe_fair_share_rank)."""
+    k = int(load().lmoe_fair_share_rank(T, K, E))
+    if k < 0:
+        raise LmoeError(LMOE_ERR_INVALID_ARG, "lmoe_fair_share_rank")
+    return k
 
 
 def threshold_candidates(logits: torch.Tensor, k: int, stream=None) -> torch.Tensor:
@@ -471,6 +477,10 @@ class Layer:
             dbg["idx"] = torch.empty((T, sh.K), dtype=torch.int32, device=dev)
             dbg["gate"] = torch.empty((T, sh.K), dtype=torch.float32, device=dev)
             dbg["counts"] = torch.empty(sh.E, dtype=torch.int32, device=dev)
+            if phase != PHASE_ROUTER:
+                # the output before its bf16 store (y is this, rounded to nearest even)
+                dbg["y_f32"] = torch.empty((T, sh.d), dtype=torch.float32, device=dev)
+                io.y_f32_out = _ptr(dbg["y_f32"])
             io.logits_out = _ptr(dbg["logits"])
             io.tau_out = _ptr(dbg["tau"])
             io.idx_out = _ptr(dbg["idx"])
@@ -504,6 +514,8 @@ class Layer:
         sh = self.shape
         T = x.shape[0]
         Tg = global_token_count(T, x.device, group) if global_tokens is None else global_tokens
+        if Tg == 0:  # every rank's part is empty
+            return self.forward(x, residual, y, debug=debug)
         k = fair_share_rank(Tg, sh.K, sh.E)
         r = self.forward(x, phase=PHASE_ROUTER, cand_k=k, debug=debug, stage_events=stage_events)
         launches = self.last_kernel_launches

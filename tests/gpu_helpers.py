@@ -11,12 +11,12 @@ import torch
 from latent_compressed_expert_gb300 import synth
 
 # Output tolerance for bf16 operands with fp32 accumulation (stated for the layer):
-#   |y - y_ref| <= 2e-2 * RMS(y_ref) + ulp_bf16(y_ref)/2  elementwise, and
-#   sum |y - y_ref| / sum |y_ref| <= 5e-3.
-# The 2e-2 * RMS bound is the one stated for the computed value; the layer returns y in
-# bf16, and that final store alone moves an element by up to half a bf16 ulp of itself,
-# which exceeds 2e-2 * RMS wherever |y| > ~5 RMS (heavy-tailed outputs once pre-activations
-# hit the SiTU-GLU cap).  The half-ulp term is that store and nothing else.
+#   max |y - y_ref| <= 2e-2 * RMS(y_ref)  and  sum |y - y_ref| / sum |y_ref| <= 5e-3.
+# It is held, exactly as written, to the value the output GEMM computes in fp32 before its
+# bf16 store (lmoe_io.y_f32_out); the returned bf16 y must then be that value rounded to
+# nearest even, bit for bit, and meet the mean bound too.  (The store alone moves an element
+# by up to half a bf16 ulp of itself, which exceeds 2e-2 * RMS wherever |y| > ~5 RMS: the
+# heavy-tailed outputs once pre-activations hit the SiTU-GLU cap.)
 MAX_ERR_REL_RMS = 2e-2
 MEAN_REL_ERR = 5e-3
 
@@ -38,7 +38,33 @@ def error_stats(y, ref):
             "mean_rel_err": float(err.sum() / max(np.abs(ref).sum(), 1e-300))}
 
 
+def _np(t):
+    return t.detach().float().cpu().numpy() if isinstance(t, torch.Tensor) else np.asarray(t)
+
+
+def assert_layer_close(y, y_f32, ref, tag=""):
+    """The layer's output against the oracle's.  y: the bf16 output rows (torch); y_f32: the
+    same rows before the bf16 store (lmoe_io.y_f32_out); ref: the oracle's fp64 rows.
+    Checks the stated bound literally on y_f32, that y is y_f32 rounded to nearest even, and
+    the mean bound on y.  Returns the statistics of both."""
+    assert y.dtype == torch.bfloat16 and y_f32.dtype == torch.float32, tag
+    rounded = y_f32.to(torch.bfloat16)
+    assert torch.equal(rounded.view(torch.int16), y.view(torch.int16)), \
+        (tag, "bf16 output is not the fp32 value rounded to nearest")
+    v = _np(y_f32).astype(np.float64)
+    assert np.all(np.isfinite(v)), tag
+    s32 = error_stats(v, ref)
+    s16 = error_stats(_np(y), ref)
+    assert s32["max_err_over_rms"] <= MAX_ERR_REL_RMS, (tag, "before the store", s32)
+    assert s32["mean_rel_err"] <= MEAN_REL_ERR, (tag, "before the store", s32)
+    assert s16["mean_rel_err"] <= MEAN_REL_ERR, (tag, "bf16", s16)
+    return {"f32": s32, "bf16": s16}
+
+
 def assert_close(y, ref, tag=""):
+    """Two bf16 outputs of the device path, each rounded from its own fp32 value (split or
+    unsplit reductions, the no-allocation entry point): the stated bound plus half a bf16 ulp
+    of the reference for the rounding of y."""
     s = error_stats(y, ref)
     assert np.all(np.isfinite(np.asarray(y, dtype=np.float64))), tag
     assert s["max_excess_over_rms"] <= MAX_ERR_REL_RMS, (tag, s)

@@ -251,3 +251,62 @@ def test_backward_argument_checks(lib):
     W = lmoe.Weights()
     assert lib.lmoe_pack_backward_weights(ctypes.byref(d), ctypes.byref(W), None, fake, 1 << 30,
                                           None) == lmoe.LMOE_ERR_INVALID_ARG
+
+
+def _c_layout(struct, fields, tmp_path):
+    """sizeof and offsetof of a struct of include/lmoe.h, from a C program gcc compiles."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    body = "".join(f'  printf("%zu\\n", offsetof({struct}, {f}));\n' for f in fields)
+    src = tmp_path / "layout.c"
+    src.write_text('#include <stddef.h>\n#include <stdio.h>\n#include "lmoe.h"\n'
+                   f'int main(void) {{\n  printf("%zu\\n", sizeof({struct}));\n{body}'
+                   "  return 0;\n}\n")
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-I" + os.path.dirname(HEADER), str(src), "-o", str(exe)], check=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split()
+    return int(out[0]), [int(v) for v in out[1:]]
+
+
+@pytest.mark.parametrize("struct,cls", [("lmoe_dims", lmoe.Dims), ("lmoe_weights", lmoe.Weights),
+                                        ("lmoe_io", lmoe.IO)])
+def test_binding_structs_match_the_header(struct, cls, tmp_path):
+    """The ctypes mirrors of the header's structs have the same size and field offsets, so
+    every option reaches the library in its own field."""
+    names = [f for f, _ in cls._fields_]
+    size, offs = _c_layout(struct, names, tmp_path)
+    assert ctypes.sizeof(cls) == size
+    assert [getattr(cls, f).offset for f in names] == offs
+
+
+def test_noalloc_constants_match_the_header():
+    src = open(HEADER).read()
+    m = re.search(r"#define\s+LMOE_NOALLOC_SCRATCH_BYTES\s+\((\d+)u\s*<<\s*(\d+)\)", src)
+    assert m, "LMOE_NOALLOC_SCRATCH_BYTES not found"
+    assert lmoe.NOALLOC_SCRATCH_BYTES == int(m.group(1)) << int(m.group(2))
+    m = re.search(r"#define\s+LMOE_OVERLAP_MIN_T\s+(\d+)", src)
+    assert m and lmoe.OVERLAP_MIN_T == int(m.group(1))
+
+
+def test_noalloc_limit_is_the_documented_batch(lib):
+    """The array holds the base workspace of a K3 decode batch of up to 152 tokens, as the
+    header states; 153 tokens exceed it."""
+    fits = [T for T in range(1, 400)
+            if lmoe.workspace_base_bytes(lmoe.dims_of(synth.DECODE, T=T))
+            <= lmoe.NOALLOC_SCRATCH_BYTES]
+    assert max(fits) == 152 and fits == list(range(1, 153))
+    assert "up to 152 tokens" in open(HEADER).read()
+
+
+def test_fair_share_rank_matches_the_oracle(lib, oracle_mod):
+    """The library's rank (used by the thresholds and by a batch spread over ranks) is the
+    oracle's, pinned to the pages' fair share; invalid arguments give -1."""
+    for T in (0, 1, 7, 55, 56, 57, 64, 1000, 8192, 32768, 40000, 1 << 24):
+        for K, E in ((16, 896), (8, 448), (4, 64), (16, 16), (1, 4096), (32, 33)):
+            assert lmoe.fair_share_rank(T, K, E) == oracle_mod.fair_share_rank(T, K, E)
+    assert lib.lmoe_fair_share_rank(-1, 16, 896) == -1
+    assert lib.lmoe_fair_share_rank(100, 0, 896) == -1
+    assert lib.lmoe_fair_share_rank(100, 16, 0) == -1

@@ -36,8 +36,8 @@ def test_stalled_wait_reports_timeout_and_context_recovers(dev, oracle_mod, monk
     assert layer.device_error() == lmoe.LMOE_ERR_DEVICE_TIMEOUT
     assert layer.device_error() == lmoe.LMOE_OK  # reading clears the flag
     monkeypatch.delenv("LMOE_FAULT_INJECT")
-    y = layer.forward(xd, residual=xd, logits_in=logits.to(dev))
+    y, dbg = layer.forward(xd, residual=xd, logits_in=logits.to(dev), debug=True)
     torch.cuda.synchronize()
     assert layer.device_error() == lmoe.LMOE_OK
     ref = oracle_mod.forward(w, x, sh.K, residual=x, tau="batch", logits_in=logits.numpy())
-    H.assert_close(y.float().cpu().numpy(), ref.y, "after-timeout")
+    H.assert_layer_close(y, dbg["y_f32"], ref.y, "after-timeout")

@@ -66,7 +66,7 @@ def test_tiny_layer_with_given_logits(dev, oracle_mod, mode, with_residual):
         assert np.array_equal(dbg["tau"].cpu().numpy().view(np.int32), ref.tau.view(np.int32))
     counts = np.bincount(ref.idx.ravel(), minlength=sh.E)
     assert np.array_equal(dbg["counts"].cpu().numpy(), counts)
-    H.assert_close(y.float().cpu().numpy(), ref.y, f"tiny/{mode}/{with_residual}")
+    H.assert_layer_close(y, dbg["y_f32"], ref.y, f"tiny/{mode}/{with_residual}")
 
 
 # ----------------------------------------------------------------------------------------
@@ -105,7 +105,8 @@ def test_layer_with_own_router(dev, oracle_mod, shape_name):
     same, _ = H.routing_agrees_up_to_ties(oracle_mod, ref.logits, ref.tau,
                                           dbg["idx"].cpu().numpy(), sh.K, delta)
     assert same.mean() >= 0.9
-    H.assert_close(y.float().cpu().numpy()[same], ref.y[same], f"{shape_name}/own-router")
+    keep = torch.as_tensor(np.nonzero(same)[0], device=y.device)
+    H.assert_layer_close(y[keep], dbg["y_f32"][keep], ref.y[same], f"{shape_name}/own-router")
 
 
 # ----------------------------------------------------------------------------------------
@@ -138,7 +139,7 @@ def test_edge_shapes(dev, oracle_mod, name, sh):
     torch.cuda.synchronize()
     assert layer.device_error() == 0
     assert np.array_equal(dbg["idx"].cpu().numpy(), ref.idx)
-    H.assert_close(y.float().cpu().numpy(), ref.y, name)
+    H.assert_layer_close(y, dbg["y_f32"], ref.y, name)
 
 
 def test_empty_batch_is_a_no_op(dev):
@@ -163,11 +164,27 @@ def test_forward_is_deterministic(dev):
 # ----------------------------------------------------------------------------------------
 # full K3 widths (sampled tokens against the oracle)
 # ----------------------------------------------------------------------------------------
-def _sample_rows(T, n, seed):
+def _sample_rows(T, n, seed, y_f32=None, branch_norm=None, tails=16, total=64):
+    """Rows compared at the full shapes: the first and last four, the `tails` rows with the
+    largest |y| (from the device output: where the output is heavy-tailed) and the `tails`
+    rows with the largest routed-branch input norm (the latent: the tokens whose routed
+    pre-activations run deepest into the SiTU-GLU cap), then random rows up to `total`
+    (at least n random ones)."""
     rng = np.random.default_rng(seed)
     rows = set(range(min(4, T))) | set(range(max(0, T - 4), T))
-    rows |= set(rng.choice(T, size=min(T, n), replace=False).tolist())
+    if y_f32 is not None:
+        top = torch.topk(y_f32.abs().amax(dim=1), min(tails, T)).indices
+        rows |= set(top.cpu().numpy().tolist())
+    if branch_norm is not None:
+        rows |= set(np.argsort(-np.asarray(branch_norm))[:tails].tolist())
+    need = max(n, total - len(rows))
+    rest = np.setdiff1d(np.arange(T), np.array(sorted(rows), dtype=np.int64))
+    rows |= set(rng.choice(rest, size=min(len(rest), need), replace=False).tolist())
     return np.array(sorted(rows))
+
+
+def _rows(t, rows):
+    return t[torch.as_tensor(np.asarray(rows), device=t.device)]
 
 
 @pytest.fixture(scope="module")
@@ -182,7 +199,14 @@ def prefill(dev):
     return sh, w, layer, x
 
 
-def test_prefill_given_logits_bit_exact_routing(dev, oracle_mod, prefill):
+@pytest.fixture(scope="module")
+def prefill_latent(dev, oracle_mod, prefill):
+    """The oracle's fp64 latent of every prefill token (shared by the prefill tests)."""
+    sh, w, layer, x = prefill
+    return oracle_mod.latent(x.cpu(), w["w_down"].cpu())
+
+
+def test_prefill_given_logits_bit_exact_routing(dev, oracle_mod, prefill, prefill_latent):
     sh, w, layer, x = prefill
     logits = synth.make_logits(sh.T, sh.E, seed=12)
     y, dbg = layer.forward(x, residual=None, logits_in=logits.to(dev), debug=True)
@@ -194,14 +218,16 @@ def test_prefill_given_logits_bit_exact_routing(dev, oracle_mod, prefill):
     assert np.array_equal(dbg["tau"].cpu().numpy().view(np.int32), tau.view(np.int32))
     assert np.array_equal(dbg["idx"].cpu().numpy(), idx)
     assert np.array_equal(dbg["gate"].cpu().numpy().view(np.int32), gate.view(np.int32))
-    rows = _sample_rows(sh.T, 12, seed=0)
+    rows = _sample_rows(sh.T, 24, seed=0, y_f32=dbg["y_f32"],
+                        branch_norm=np.linalg.norm(prefill_latent, axis=1))
+    assert len(rows) >= 64
     wh = H.weights_to_host(w)
     xr = x[rows].cpu()
     ref = H.oracle_rows(oracle_mod, wh, xr, idx[rows], gate[rows], None)
-    H.assert_close(y[rows].float().cpu().numpy(), ref, "prefill/given-logits")
+    H.assert_layer_close(_rows(y, rows), _rows(dbg["y_f32"], rows), ref, "prefill/given-logits")
 
 
-def test_prefill_own_router(dev, oracle_mod, prefill):
+def test_prefill_own_router(dev, oracle_mod, prefill, prefill_latent):
     """Exactly the benchmark's call; the oracle computes all 8192 tokens' latents and logits
     (for the in-batch thresholds) and the full output of sampled tokens."""
     sh, w, layer, x = prefill
@@ -210,7 +236,7 @@ def test_prefill_own_router(dev, oracle_mod, prefill):
     assert layer.device_error() == 0
     wh = H.weights_to_host(w)
     xh = x.cpu()
-    lat = oracle_mod.latent(xh, wh["w_down"])
+    lat = prefill_latent
     lg_ref = oracle_mod.router_logits(lat, wh["w_router"])
     lg_gpu = dbg["logits"].cpu().numpy().astype(np.float64)
     bound = _logit_bound(lat, wh["w_router"])
@@ -227,10 +253,13 @@ def test_prefill_own_router(dev, oracle_mod, prefill):
     # load balance: every expert near its fair share T*K/E
     counts = dbg["counts"].cpu().numpy()
     assert counts.sum() == sh.T * sh.K
-    rows = [r for r in _sample_rows(sh.T, 16, seed=1) if same[r]]
+    cand = _sample_rows(sh.T, 32, seed=1, y_f32=dbg["y_f32"],
+                        branch_norm=np.linalg.norm(lat, axis=1), total=80)
+    rows = [r for r in cand if same[r]]
+    assert len(rows) >= 64
     _, gate_ref, _ = oracle_mod.route(lg32[rows], tau_ref, sh.K)
     ref = H.oracle_rows(oracle_mod, wh, xh[rows], idx_ref[rows], gate_ref, None)
-    H.assert_close(y[rows].float().cpu().numpy(), ref, "prefill/own-router")
+    H.assert_layer_close(_rows(y, rows), _rows(dbg["y_f32"], rows), ref, "prefill/own-router")
 
 
 def test_e64_layer(dev, oracle_mod):
@@ -254,10 +283,12 @@ def test_e64_layer(dev, oracle_mod):
     same, idx_ref = H.routing_agrees_up_to_ties(oracle_mod, lg32, tau_ref,
                                                 dbg["idx"].cpu().numpy(), sh.K, 0.5 * dz + 1e-6)
     assert same.mean() >= 0.9
-    rows = [r for r in _sample_rows(sh.T, 16, seed=2) if same[r]]
+    cand = _sample_rows(sh.T, 16, seed=2, y_f32=dbg["y_f32"],
+                        branch_norm=np.linalg.norm(lat, axis=1), tails=8, total=40)
+    rows = [r for r in cand if same[r]]
     _, gate_ref, _ = oracle_mod.route(lg32[rows], tau_ref, sh.K)
     ref = H.oracle_rows(oracle_mod, wh, xh[rows], idx_ref[rows], gate_ref, xh[rows])
-    H.assert_close(y[rows].float().cpu().numpy(), ref, "e64")
+    H.assert_layer_close(_rows(y, rows), _rows(dbg["y_f32"], rows), ref, "e64")
 
 
 def test_decode_layer(dev, oracle_mod):
@@ -286,12 +317,12 @@ def test_decode_layer(dev, oracle_mod):
     rows = np.nonzero(same)[0]
     _, gate_ref, _ = oracle_mod.route(lg32[rows], tau, sh.K)
     ref = H.oracle_rows(oracle_mod, wh, xh[rows], idx_ref[rows], gate_ref, None)
-    H.assert_close(y[rows].float().cpu().numpy(), ref, "decode")
+    H.assert_layer_close(_rows(y, rows), _rows(dbg["y_f32"], rows), ref, "decode")
 
 
 def test_skew_router_given_logits(dev, oracle_mod):
     """T=32768 with Zipf(1.1)-biased router logits: in-batch thresholds restore balance;
-    routing bit-exact, sampled outputs against the oracle."""
+    routing bit-exact, sampled outputs (the heavy tail included) against the oracle."""
     sh = synth.SKEW
     w = synth.make_weights(sh, seed=4, device=dev)
     layer = lmoe.Layer(sh, w)
@@ -310,10 +341,13 @@ def test_skew_router_given_logits(dev, oracle_mod):
     before = np.bincount(plain.ravel(), minlength=sh.E) / fair
     after = dbg["counts"].cpu().numpy() / fair
     assert before.max() > 5.0 and after.max() < 1.6
-    rows = _sample_rows(sh.T, 8, seed=3)
+    # the routed branch's input norm is the latent's, which x's row norm sets here
+    rows = _sample_rows(sh.T, 24, seed=3, y_f32=dbg["y_f32"],
+                        branch_norm=x.float().norm(dim=1).cpu().numpy())
+    assert len(rows) >= 64
     wh = H.weights_to_host(w)
     ref = H.oracle_rows(oracle_mod, wh, x[rows].cpu(), idx[rows], gate[rows], None)
-    H.assert_close(y[rows].float().cpu().numpy(), ref, "skew")
+    H.assert_layer_close(_rows(y, rows), _rows(dbg["y_f32"], rows), ref, "skew")
 
 
 @pytest.mark.parametrize("overlap", [False, True])
@@ -333,7 +367,7 @@ def test_shared_overlap_and_serial_paths(dev, oracle_mod, overlap):
     assert layer.last_kernel_launches == (13 if overlap else 11)
     ref = oracle_mod.forward(w, x, sh.K, residual=x, tau="batch", logits_in=logits.numpy())
     assert np.array_equal(dbg["idx"].cpu().numpy(), ref.idx)
-    H.assert_close(y.float().cpu().numpy(), ref.y, f"mid/overlap={overlap}")
+    H.assert_layer_close(y, dbg["y_f32"], ref.y, f"mid/overlap={overlap}")
 
 
 def test_checked_mode_reports_nonfinite_logits(dev, monkeypatch):
