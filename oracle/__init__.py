@@ -426,7 +426,7 @@ class OracleResult:
 
 
 def forward(w: dict, x, K: int, residual=None, tau="batch", logits_in=None, c=100.0,
-            eps=1e-6, expert_fp8: bool = False) -> OracleResult:
+            eps=1e-6, expert_fp8: bool = False, tie_margin: float = 2.0 ** -16) -> OracleResult:
     """The whole layer on the rows of ``x``.
 
     w: dict of weights (bf16 tensors or uint16 bit arrays, fp32 gamma) with keys w_down,
@@ -434,7 +434,8 @@ def forward(w: dict, x, K: int, residual=None, tau="batch", logits_in=None, c=10
     tau: "batch" -> thresholds solved over the rows of x (k = fair_share_rank);
          None -> plain top-K without balancing; an array -> those thresholds.
     logits_in: fp32 [n, E] router logits to route on instead of the computed ones.
-    expert_fp8: routed experts with e4m3 operands (``routed_fp8``).
+    expert_fp8: routed experts with e4m3 operands (``routed_fp8``); tie_margin is its
+    near-tie margin for ``scale_ties``.
     """
     xs = _u16(x)
     n = xs.shape[0]
@@ -458,7 +459,8 @@ def forward(w: dict, x, K: int, residual=None, tau="batch", logits_in=None, c=10
     ties = None
     if expert_fp8:
         wq = quantize_expert_weights(w["w_gate"], w["w_value"], w["w_edown"])
-        z, ties = routed_fp8(lat, idx, gate, wq, gamma, c, eps, return_ties=True)
+        z, ties = routed_fp8(lat, idx, gate, wq, gamma, c, eps, tie_margin=tie_margin,
+                             return_ties=True)
     else:
         z = routed(lat, idx, gate, w["w_gate"], w["w_value"], w["w_edown"], gamma, c, eps)
     ys = shared(xs, w["w_sgate"], w["w_svalue"], w["w_sdown"], c)

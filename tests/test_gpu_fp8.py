@@ -10,12 +10,20 @@ same experts on both sides.
 A row's scale is set by its largest bf16 value.  Where that element lies on a bf16 rounding
 near-tie, the GPU (fp32 accumulation) and the oracle (fp64) may round it differently, and
 then quantise the whole row with scales 2^-8 apart: a different, equally valid set of
-codes, and an output that moves by the e4m3 step of many elements.  Like routing near-ties,
-such tokens are decided by the last bits of the arithmetic: the oracle flags them
-(``scale_ties``), they must be rare, and outputs are compared on the others.
+codes, moving each element by at most one e4m3 step.  Every token is held to the
+elementwise bound below, near-ties included.  The oracle flags the tokens with such a row
+(``scale_ties``: the row maximum within TIE_MARGIN, relative, of a tie), and the mean and
+RMS criteria, which a scale flip would move, are checked on the others; the fraction
+flagged is reported and must stay at most MAX_EXCLUDED.
+
+TIE_MARGIN = 2^-20: the GPU's fp32 value of a row maximum agrees with the oracle's fp64
+value to well within that (measured: at the mid and decode-sized shapes, every token whose
+rows all lie further than 2^-20 from a tie has the error of an unflipped token, 3.9 % RMS at
+most, while a token at 2^-21 flipped, 8.3 %); a row is flagged with probability ~2^-11.
 """
 
-MIN_STABLE = 0.9  # fraction of tokens with no quantised row at a near-tie
+MAX_EXCLUDED = 0.01        # fraction of tokens with a quantised row at a near-tie
+TIE_MARGIN = 2.0 ** -20
 
 # Tolerance of the FP8 variant (derived, not stated by the pages).  The kernel takes its
 # quantisation decisions from fp32-accumulated values and the oracle from fp64 ones; the
@@ -31,25 +39,33 @@ FP8_MAX_ERR_REL_RMS = 2.0 ** -3
 FP8_RMS_FRACTION = 0.25
 
 
-def assert_close_fp8(y, ref8, ref16=None, tag=""):
-    """ref16 (the oracle's bf16 layer): also check the RMS criterion; it is meaningful where
-    the routed branch carries the output error, not where the dense path's bf16 rounding
-    of ~1000x outliers dwarfs the FP8 effect."""
+def assert_close_fp8(y, ref8, stable, ref16=None, tag="", max_excluded=MAX_EXCLUDED):
+    """Every token: the elementwise bound.  Tokens not at a near-tie (``stable``): the mean
+    bound, and with ref16 (the oracle's bf16 layer) the RMS criterion, which is meaningful
+    where the routed branch carries the output error, not where the dense path's bf16
+    rounding of ~1000x outliers dwarfs the FP8 effect."""
     y = np.asarray(y, dtype=np.float64)
     err = np.abs(y - ref8)
     rms = float(np.sqrt(np.mean(ref8 * ref8)))
     excess = np.maximum(err - H.half_ulp_bf16(ref8), 0.0)
-    stats = {"max_excess_over_rms": float(excess.max() / rms),
-             "mean_rel_err": float(err.sum() / np.abs(ref8).sum()),
-             "rms_err": float(np.sqrt(np.mean(err * err))),
-             "rms_fp8_vs_bf16": (float(np.sqrt(np.mean((ref8 - ref16) ** 2)))
+    es = err[stable]
+    stats = {"tokens": int(len(y)), "excluded": float(1.0 - np.mean(stable)),
+             "max_excess_over_rms": float(excess.max() / rms),
+             "max_excess_over_rms_stable": float(excess[stable].max() / rms),
+             "mean_rel_err": float(es.sum() / np.abs(ref8[stable]).sum()),
+             "rms_err": float(np.sqrt(np.mean(es * es))),
+             "rms_fp8_vs_bf16": (float(np.sqrt(np.mean((ref8[stable] - ref16[stable]) ** 2)))
                                  if ref16 is not None else None)}
+    print(f"fp8 {tag}: {stats}")
     assert np.all(np.isfinite(y)), tag
+    assert stats["excluded"] <= max_excluded, (tag, stats)
     assert stats["max_excess_over_rms"] <= FP8_MAX_ERR_REL_RMS, (tag, stats)
     assert stats["mean_rel_err"] <= H.MEAN_REL_ERR, (tag, stats)
     if ref16 is not None:
         assert stats["rms_err"] <= FP8_RMS_FRACTION * stats["rms_fp8_vs_bf16"], (tag, stats)
     return stats
+
+
 import numpy as np
 import pytest
 import torch
@@ -99,7 +115,7 @@ def _fp8_oracle_rows(oracle_mod, wh, x_rows, idx_rows, gate_rows, residual_rows=
                                             wh["w_value"][sel].contiguous(),
                                             wh["w_edown"][sel].contiguous())
     z, ties = oracle_mod.routed_fp8(lat, remap, gate_rows, wq, wh["gamma"].numpy(), c, eps,
-                                    return_ties=True)
+                                    tie_margin=TIE_MARGIN, return_ties=True)
     ys = oracle_mod.shared(x_rows, wh["w_sgate"], wh["w_svalue"], wh["w_sdown"], c)
     z16 = oracle_mod.routed(lat, remap, gate_rows, wh["w_gate"][sel].contiguous(),
                             wh["w_value"][sel].contiguous(), wh["w_edown"][sel].contiguous(),
@@ -121,14 +137,12 @@ def test_mid_layer_fp8_every_token(dev, oracle_mod):
     assert layer.device_error() == 0
     assert layer.last_kernel_launches == 13   # the bf16 layer's 11 + two quantisations
     ref = oracle_mod.forward(w, x, sh.K, residual=x, tau="batch", logits_in=logits.numpy(),
-                             expert_fp8=True)
+                             expert_fp8=True, tie_margin=TIE_MARGIN)
     assert np.array_equal(dbg["idx"].cpu().numpy(), ref.idx)
     assert np.array_equal(dbg["gate"].cpu().numpy().view(np.int32), ref.gate.view(np.int32))
     stable = ref.scale_ties == 0
-    assert stable.mean() >= MIN_STABLE, stable.mean()
     ref16 = oracle_mod.forward(w, x, sh.K, residual=x, tau="batch", logits_in=logits.numpy())
-    assert_close_fp8(y.float().cpu().numpy()[stable], ref.y[stable], ref16.y[stable],
-                     tag="mid/fp8")
+    assert_close_fp8(y.float().cpu().numpy(), ref.y, stable, ref16.y, tag="mid")
     # the FP8 layer stays near the bf16 layer: the e4m3 rounding of every operand
     y16 = lmoe.Layer(sh, wd).forward(xd, residual=xd, logits_in=logits.to(dev))
     torch.cuda.synchronize()
@@ -155,12 +169,17 @@ def test_prefill_fp8_sampled_tokens(dev, oracle_mod):
     idx, gate, _ = oracle_mod.route(lg, tau, sh.K)
     assert np.array_equal(dbg["idx"].cpu().numpy(), idx)
     rng = np.random.default_rng(4)
-    rows = np.array(sorted({0, sh.T - 1} | set(rng.choice(sh.T, 6, replace=False).tolist())))
+    top = torch.topk(y.float().abs().amax(dim=1), 4).indices.cpu().numpy().tolist()
+    rows = {0, sh.T - 1} | set(top)
+    rest = np.setdiff1d(np.arange(sh.T), np.array(sorted(rows)))
+    rows = np.array(sorted(rows | set(rng.choice(rest, 24 - len(rows), replace=False).tolist())))
     wh = H.weights_to_host(w)
     ref, _, ties = _fp8_oracle_rows(oracle_mod, wh, x[rows].cpu(), idx[rows], gate[rows], None)
+    # 24 tokens of 17 quantised rows each, a row flagged with probability ~2^-11: a flagged
+    # token is possible but rare; the cap is one token
     stable = ties == 0
-    assert stable.sum() >= len(rows) // 2, ties
-    assert_close_fp8(y[rows].float().cpu().numpy()[stable], ref[stable], tag="prefill/fp8")
+    assert_close_fp8(y[rows].float().cpu().numpy(), ref, stable, tag="prefill",
+                     max_excluded=1.0 / len(rows))
 
 
 @pytest.mark.parametrize("T", [1, 7, 64])
@@ -180,8 +199,45 @@ def test_fp8_small_batches_every_token(dev, oracle_mod, T):
     torch.cuda.synchronize()
     assert layer.device_error() == 0
     ref = oracle_mod.forward(w, x, sh.K, residual=x, tau=tau.numpy(), logits_in=logits.numpy(),
-                             expert_fp8=True)
+                             expert_fp8=True, tie_margin=TIE_MARGIN)
     assert np.array_equal(dbg["idx"].cpu().numpy(), ref.idx)
     stable = ref.scale_ties == 0
     if stable.any():
-        assert_close_fp8(y.float().cpu().numpy()[stable], ref.y[stable], tag=f"fp8/T{T}")
+        assert_close_fp8(y.float().cpu().numpy(), ref.y, stable, tag=f"T{T}",
+                         max_excluded=max(MAX_EXCLUDED, 1.0 / T))  # one token at most
+
+
+def test_fp8_forced_exact_tie(dev, oracle_mod):
+    """A token whose latent is exact in fp32 on both sides and whose largest element sits
+    exactly on a bf16 rounding tie (1 + 2^-8, between 1 and 1 + 2^-7): the oracle flags it,
+    both sides round the tie to even (1.0) and quantise the row with the same scale, and the
+    token meets every criterion although it is flagged."""
+    sh = synth.LayerShape("tie", T=8, d=256, L=128, E=16, K=4, I=128, S=1, Is=64)
+    w = synth.make_weights(sh, seed=81)
+    x = synth.make_x(sh, seed=82)
+    # token 0: x = e_0 + 2^-8 e_1, so its latent is W_down[:, 0] + 2^-8 W_down[:, 1] exactly
+    x[0] = 0
+    x[0, 0] = 1.0
+    x[0, 1] = 2.0 ** -8
+    wdn = w["w_down"].float()
+    wdn[:, 1] = 0.0
+    wdn[:, 0] = wdn[:, 0].clamp(-0.5, 0.5)
+    wdn[5, 0], wdn[5, 1] = 1.0, 1.0           # latent element 5: 1 + 2^-8, the row's largest
+    w["w_down"] = wdn.to(torch.bfloat16)
+    lat0 = w["w_down"].double()[:, 0] + 2.0 ** -8 * w["w_down"].double()[:, 1]
+    assert float(lat0.abs().max()) == 1.0 + 2.0 ** -8 and int(lat0.abs().argmax()) == 5
+    logits = synth.make_logits(sh.T, sh.E, seed=83)
+    wd = {k: v.to(dev) for k, v in w.items()}
+    layer = lmoe.Layer(sh, wd, expert_fp8=True)
+    xd = x.to(dev)
+    y, dbg = layer.forward(xd, residual=xd, logits_in=logits.to(dev), debug=True)
+    torch.cuda.synchronize()
+    assert layer.device_error() == 0
+    ref = oracle_mod.forward(w, x, sh.K, residual=x, tau="batch", logits_in=logits.numpy(),
+                             expert_fp8=True, tie_margin=TIE_MARGIN)
+    assert np.array_equal(dbg["idx"].cpu().numpy(), ref.idx)
+    assert ref.scale_ties[0] >= 1                # the forced tie is flagged
+    # token 0 compared as if it were not flagged: the tie is exact on both sides
+    stable = ref.scale_ties == 0
+    stable[0] = True
+    assert_close_fp8(y.float().cpu().numpy(), ref.y, stable, tag="forced tie", max_excluded=1.0)
