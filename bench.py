@@ -198,26 +198,63 @@ class ClockSampler:
 # ----------------------------------------------------------------------------------------
 # the CPU oracle on a bounded sample (reported baseline, and the reference arm)
 # ----------------------------------------------------------------------------------------
-def oracle_step(oracle, wh, x_rows, K):
-    """The whole layer on a sub-batch of tokens, thresholds solved over that sub-batch."""
-    return oracle.forward(wh, x_rows, K, residual=x_rows, tau="batch")
+def batch_thresholds(oracle, wh, xh, K):
+    """The batch-wide part of the layer on the host: the latent and router logits of every
+    token, and the Quantile-Balancing thresholds over the whole batch.  Returns
+    (lat, logits, tau, seconds)."""
+    t0 = time.perf_counter()
+    lat = oracle.latent(xh, wh["w_down"])
+    lg = oracle.router_logits(lat, wh["w_router"]).astype(np.float32)
+    tau = oracle.thresholds(lg, oracle.fair_share_rank(lg.shape[0], K, lg.shape[1]))
+    return lat, lg, tau, time.perf_counter() - t0
+
+
+def oracle_rest(oracle, wh, x_rows, lat_rows, lg_rows, tau, K, c=100.0, eps=1e-6):
+    """The per-token rest of the layer for some tokens, given their latent and logits and the
+    batch's thresholds: routing, routed experts, combine and RMSNorm, shared experts,
+    up-projection and residual."""
+    idx, gate, _ = oracle.route(lg_rows, tau, K)
+    z = oracle.routed(lat_rows, idx, gate, wh["w_gate"], wh["w_value"], wh["w_edown"],
+                      wh["gamma"].numpy(), c, eps)
+    ys = oracle.shared(x_rows, wh["w_sgate"], wh["w_svalue"], wh["w_sdown"], c)
+    return oracle.output(z, ys, wh["w_up"], x_rows)
+
+
+def oracle_tokens(oracle, wh, x_rows, tau, K):
+    """The whole layer's per-token work for some tokens (latent, logits, then the rest),
+    routed against thresholds solved over their whole batch."""
+    lat = oracle.latent(x_rows, wh["w_down"])
+    lg = oracle.router_logits(lat, wh["w_router"]).astype(np.float32)
+    return oracle_rest(oracle, wh, x_rows, lat, lg, tau, K)
 
 
 def host_weights(w):
     return {k: v.detach().cpu() for k, v in w.items()}
 
 
-def time_oracle(sh, wh, x_host, n_tokens, reps=1):
+SUBSET_TOKENS = 512
+
+
+def cpu_baseline(sh, wh, xh, args):
+    """The fp64 oracle on the host cores: the batch-wide stage (latent and logits of all T
+    tokens, thresholds over the batch) timed in full, and the per-token rest of the layer on
+    a fixed subset of 512 tokens; the layer's host time for the batch is the first plus the
+    second scaled by T / 512 (its cost is linear in tokens)."""
     import oracle
     oracle.build()
+    lat, lg, tau, t_batch = batch_thresholds(oracle, wh, xh, sh.K)
+    n = min(sh.T, args.cpu_tokens if args.cpu_tokens > 0 else SUBSET_TOKENS)
+    rows = np.linspace(0, sh.T - 1, n).astype(np.int64)  # fixed, spread over the batch
     t0 = time.perf_counter()
-    done = 0
-    for r in range(reps):
-        s = (r * n_tokens) % max(1, sh.T - n_tokens)
-        oracle_step(oracle, wh, x_host[s:s + n_tokens].contiguous(), sh.K)
-        done += n_tokens
-    dt = time.perf_counter() - t0
-    return done / dt, dt, oracle.num_threads()
+    oracle_rest(oracle, wh, xh[rows].contiguous(), lat[rows], lg[rows], tau, sh.K)
+    t_rest = time.perf_counter() - t0
+    t_layer = t_batch + t_rest * sh.T / n
+    return {"value": sh.T / t_layer, "unit": UNIT, "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"latent, router logits and thresholds of all {sh.T} tokens ({t_batch:.1f} s) "
+                      f"+ the rest of the layer for a fixed subset of {n} tokens "
+                      f"({t_rest:.1f} s), scaled to the batch: {t_layer:.1f} s per {sh.T}-token step",
+            "batch_stage_s": t_batch, "subset_tokens": n, "subset_rest_s": t_rest}
 
 
 # ----------------------------------------------------------------------------------------
@@ -272,8 +309,9 @@ DESCRIPTIONS = {
               "layer passed in; x~N(0,1); residual = x",
     "e64": "K3 widths with a reduced pool (E=64, top-4): in-batch thresholds; x~N(0,1); "
            "residual = x",
-    "skew": "K3 layer, skewed router: router logits supplied with a per-expert Zipf(1.1) "
-            "bias (router GEMM not in the step), in-batch thresholds; x~N(0,1); residual = x",
+    "skew": "K3 layer, skewed router: a per-expert Zipf(1.1) bias -1.1 ln(rank) added to "
+            "the router logits in the router GEMM's epilogue, in-batch thresholds; x~N(0,1); "
+            "residual = x",
     "small": "K3 widths, 128 experts, T=1024 (profiling case: ~128 tokens per expert as "
              "in prefill, a few GB on the device); x as in prefill",
     "pool448": "K3 widths with the alternative pool of 448 routed experts, top-8 (the same "
@@ -319,17 +357,17 @@ class Workload:
             self.kwargs["tau"] = dbg["tau"].clone()
             del xp, dbg
         if name == "skew":
-            _, dbg = self.layer.forward(self.x, debug=True, balance=False)
-            bias = synth.make_logits(1, sh.E, SEED, device=dev, zipf_s=1.1) - \
-                synth.make_logits(1, sh.E, SEED, device=dev)
-            self.kwargs["logits_in"] = (dbg["logits"] + bias).contiguous()
+            # the Zipf bias enters in the router GEMM's epilogue, so the step routes on
+            # biased logits it computes itself
+            self.kwargs["logit_bias"] = synth.zipf_bias(sh.E, SEED, 1.1, device=dev)
             _, plain = self.layer.forward(self.x, debug=True, balance=False,
-                                          logits_in=self.kwargs["logits_in"])
+                                          logit_bias=self.kwargs["logit_bias"])
             fair = sh.T * sh.K / sh.E
             c0 = plain["counts"].float()
             self.extra["load_before"] = {"max_over_mean": float(c0.max() / fair),
-                                         "min_over_mean": float(c0.min() / fair)}
-            del dbg, plain
+                                         "min_over_mean": float(c0.min() / fair),
+                                         "idle_experts": int((c0 == 0).sum())}
+            del plain
 
     def forward(self, **kw):
         if self.qb == "global":
@@ -363,6 +401,11 @@ def make_inputs(sh, dev, rank, outliers=True):
 
 
 def run_reference(args):
+    """The oracle (the only reference there is) on the host cores.  Set-up: the batch-wide
+    stage (latent and logits of all T tokens, thresholds over the batch), timed and
+    reported.  Each step: the whole layer's per-token work (latent, logits, routing against
+    those thresholds, experts, shared experts, output) for a sub-batch of n tokens, sized so
+    that warm-up and steps take about 2-3 minutes; value = tokens per second of those steps."""
     world, rank, _ = dist_setup(args.gpus)
     if rank != 0:
         return 0
@@ -374,20 +417,23 @@ def run_reference(args):
     del w, x
     import oracle
     oracle.build()
-    # size each step so that warmup + steps take about 2-3 minutes on this host
-    rate, _, _ = time_oracle(sh, wh, xh, 2)
+    _, _, tau, t_batch = batch_thresholds(oracle, wh, xh, sh.K)
+    t0 = time.perf_counter()
+    oracle_tokens(oracle, wh, xh[:4].contiguous(), tau, sh.K)
+    rate = 4 / (time.perf_counter() - t0)
     n = int(max(1, min(64, rate * 150.0 / max(1, args.steps + args.warmup))))
     for i in range(args.warmup):
-        oracle_step(oracle, wh, xh[i * n:(i + 1) * n].contiguous(), sh.K)
+        oracle_tokens(oracle, wh, xh[i * n:(i + 1) * n].contiguous(), tau, sh.K)
     t0 = time.perf_counter()
     for i in range(args.steps):
         s = (i * n) % (sh.T - n)
-        oracle_step(oracle, wh, xh[s:s + n].contiguous(), sh.K)
+        oracle_tokens(oracle, wh, xh[s:s + n].contiguous(), tau, sh.K)
     dt = time.perf_counter() - t0
     value = n * args.steps / dt
     cores = oracle.num_threads()
-    sample = (f"{n} tokens of the {sh.T}-token batch per step through the whole layer, "
-              f"thresholds solved over those tokens (cost is linear in tokens)")
+    sample = (f"{n} tokens of the {sh.T}-token batch per step through the whole layer's "
+              f"per-token work, routed against thresholds solved over the whole batch "
+              f"(that batch-wide stage took {t_batch:.1f} s once, before the steps)")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * dt / args.steps, "higher_is_better": True, "scaling": "weak",
@@ -397,11 +443,149 @@ def run_reference(args):
                                    f"experts (I_s={sh.Is}), routed I={sh.I}",
                        "shape": args.shape, "tokens_per_gpu": sh.T, "global_tokens": sh.T},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-                             "sample": sample},
+                             "sample": sample, "batch_stage_s": t_batch},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
+
+
+# Timed regions shorter than this are compared with the burst bf16 peak, longer ones with the
+# sustained one (a kernel timed alone vs. inside a long run under the power cap).
+BURST_REGION_S = 1.0
+
+
+def pick_peak(peaks, region_s):
+    if region_s < BURST_REGION_S:
+        return peaks["bf16_tflops"], "bf16 burst"
+    return peaks["bf16_tflops_sustained"], "bf16 sustained"
+
+
+def time_workload(wl, steps, warmup, world, local, stream):
+    """`warmup` untimed steps, then `steps` timed ones between a barrier and device
+    synchronisations, with CUDA events at every stage boundary on the launching stream and
+    nvidia-smi clock samples.  Returns the step time (max over ranks) and per-stage means."""
+    layer, x = wl.layer, wl.x
+    y = torch.empty_like(x)
+    for _ in range(warmup):  # also learns how many experts a step touches
+        _, dbg = wl.forward(y=y, debug=True)
+    torch.cuda.synchronize()
+    if layer.device_error() != 0:
+        raise RuntimeError(f"device-side error during warm-up ({wl.name})")
+    counts = dbg["counts"].cpu().numpy()
+    launches = layer.last_kernel_launches
+    del dbg
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(lmoe.NUM_STAGES + 1)]
+           for _ in range(steps)]
+    for e in evs:  # create the events outside the timed region
+        for ev in e:
+            ev.record(stream)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    barrier(world)
+    with ClockSampler(local) as clk:
+        torch.cuda.synchronize()
+        start.record(stream)
+        for i in range(steps):
+            wl.forward(y=y, stage_events=evs[i])
+        end.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    ms = start.elapsed_time(end)
+    if layer.device_error() != 0:
+        raise RuntimeError(f"device-side error in the timed region ({wl.name})")
+    stage_ms = {name: float(np.mean([evs[i][s].elapsed_time(evs[i][s + 1])
+                                     for i in range(steps)]))
+                for s, name in enumerate(lmoe.STAGES)}
+    return {"ms": max_over_ranks(ms, world), "stage_ms": stage_ms, "counts": counts,
+            "touched": int((counts > 0).sum()), "launches": launches, "clocks": clk.summary(),
+            "y": y}
+
+
+def dominant_roofline(wl, r, peaks, peak_src, region_s):
+    """Roofline of the stage that takes the most time: algorithmic FLOP or bytes of one
+    launch over its mean CUDA-event duration, against the measured peak of its bound."""
+    sh = wl.sh
+    work = stage_work(sh, r["touched"], fp8=wl.fp8)
+    stage_ms = r["stage_ms"]
+    dom = max(stage_ms, key=stage_ms.get)
+    dw = work[dom]
+    t_s = stage_ms[dom] / 1e3
+    tflops, kind = pick_peak(peaks, region_s)
+    t_flop = dw["flop"] / (tflops * 1e12)
+    t_byte = dw["bytes"] / (peaks["hbm_gbs"] * 1e9)
+    if t_flop >= t_byte:
+        roof = {"bound": "tensor", "achieved": dw["flop"] / t_s / 1e12, "peak": tflops,
+                "unit": "TFLOP/s"}
+    else:
+        roof = {"bound": "hbm", "achieved": dw["bytes"] / t_s / 1e9, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s"}
+        kind = "HBM copy"
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    # the stored figures are captures of the prefill workload (in-batch thresholds)
+    roof["traffic"] = (ncu_traffic(dom, "stages_fp8" if wl.fp8 and dom.startswith("expert")
+                                   else "stages")
+                       if wl.name == "prefill" and wl.qb == "local" else None)
+    roof["kernel"] = dom
+    roof["peak_source"] = f"{peak_src} ({kind})"
+    roof["algorithmic"] = {"flop": dw["flop"], "bytes": dw["bytes"]}
+    stages = {}
+    for name in lmoe.STAGES:
+        sw_ = work[name]
+        t = stage_ms[name] / 1e3
+        stages[name] = {"ms": round(stage_ms[name], 4),
+                        "tflops": round(sw_["flop"] / t / 1e12, 1) if t > 0 and sw_["flop"] else None,
+                        "gbs": round(sw_["bytes"] / t / 1e9, 1) if t > 0 else None}
+    return roof, stages
+
+
+def load_summary(sh, counts):
+    fair = sh.T * sh.K / sh.E
+    return {"max_over_mean": float(counts.max() / fair),
+            "min_over_mean": float(counts.min() / fair),
+            "idle_experts": int((counts == 0).sum())}
+
+
+# The other workloads of the layer reported inside the headline line: steps per timed
+# region (each region stays well under a second).
+CONFIG_STEPS = {"decode": 60, "skew": 10, "e64": 40}
+
+
+def run_configs(args, dev, rank, world, local, stream, peaks, peak_src):
+    """Decode, skewed-router and reduced-pool (E=64) workloads, each timed as the headline
+    is (device-resident inputs, CUDA events, max over ranks)."""
+    out = {}
+    for name in ("decode", "skew", "e64"):
+        wl = Workload(name, dev, rank, world=world, expert_fp8=args.experts == "fp8")
+        steps = min(args.steps, CONFIG_STEPS[name])
+        r = time_workload(wl, steps, 3, world, local, stream)
+        sh = wl.sh
+        step_s = r["ms"] / 1e3 / steps
+        region_s = r["ms"] / 1e3
+        flop, nbytes = layer_work(sh, r["touched"], fp8=wl.fp8)
+        tflops, kind = pick_peak(peaks, region_s)
+        roof, stages = dominant_roofline(wl, r, peaks, peak_src, region_s)
+        c = {"workload": wl.config(world)["workload"], "steps": steps, "warmup": 3,
+             "ms_per_step": r["ms"] / steps, "value": world * sh.T / step_s, "unit": UNIT,
+             "tflops": flop / step_s / 1e12, "frac_bf16_peak": flop / step_s / 1e12 / tflops,
+             "bf16_peak": f"{tflops} TFLOP/s ({peak_src}, {kind})",
+             "experts_touched": r["touched"], "roofline": roof, "stages": stages,
+             "clocks": r["clocks"], "gpu_launches": r["launches"] * steps}
+        if name == "decode":
+            c["decode_weight_gbs"] = nbytes / step_s / 1e9
+            c["decode_frac_hbm"] = c["decode_weight_gbs"] / peaks["hbm_gbs"]
+            c["decode_target_frac_hbm"] = 0.70
+            c["decode_bytes"] = ("weights of the experts the step touches, the dense weights, "
+                                 "x, residual and y, each once")
+        if name == "skew":
+            c["load"] = {"before_balancing": wl.extra["load_before"],
+                         "after_balancing": load_summary(sh, r["counts"])}
+        else:
+            c["load"] = load_summary(sh, r["counts"])
+        out[name] = c
+        del wl, r
+        torch.cuda.empty_cache()
+    return out
 
 
 def run_ours(args):
@@ -412,43 +596,13 @@ def run_ours(args):
     wl = Workload(args.shape, dev, rank, overlap=args.overlap, shared_sms=args.shared_sms,
                   qb=args.qb, world=world, expert_fp8=args.experts == "fp8")
     sh, layer, x, w = wl.sh, wl.layer, wl.x, wl.w
-    y = torch.empty_like(x)
     stream = torch.cuda.current_stream()
 
-    # warm-up (also learns how many experts a step touches)
-    for _ in range(args.warmup):
-        _, dbg = wl.forward(y=y, debug=True)
-    torch.cuda.synchronize()
-    if layer.device_error() != 0:
-        raise RuntimeError("device-side error during warm-up")
-    counts = dbg["counts"].cpu().numpy()
-    touched = int((counts > 0).sum())
-    launches_per_step = layer.last_kernel_launches
-
     # ---- timed region: device-resident inputs
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(lmoe.NUM_STAGES + 1)]
-           for _ in range(args.steps)]
-    for e in evs:  # create the events outside the timed region
-        for ev in e:
-            ev.record(stream)
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    barrier(world)
-    with ClockSampler(local) as clk:
-        torch.cuda.synchronize()
-        start.record(stream)
-        for i in range(args.steps):
-            wl.forward(y=y, stage_events=evs[i])
-        end.record(stream)
-        torch.cuda.synchronize()
-    barrier(world)
-    ms = start.elapsed_time(end)
-    if layer.device_error() != 0:
-        raise RuntimeError("device-side error in the timed region")
-    ms_max = max_over_ranks(ms, world)
-    stage_ms = {name: float(np.mean([evs[i][s].elapsed_time(evs[i][s + 1])
-                                     for i in range(args.steps)]))
-                for s, name in enumerate(lmoe.STAGES)}
+    r = time_workload(wl, args.steps, args.warmup, world, local, stream)
+    ms_max, stage_ms, counts, touched = r["ms"], r["stage_ms"], r["counts"], r["touched"]
+    launches_per_step = r["launches"]
+    y = r["y"]
 
     # ---- end to end through the public API with host buffers: every step uploads its x
     # from pinned host memory and downloads its y; lmoe.HostPipeline overlaps one step's
@@ -480,6 +634,8 @@ def run_ours(args):
     torch.cuda.synchronize()
     barrier(world)
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
+    if wl.qb != "global":
+        del pipe
 
     T = sh.T
     value = world * T * args.steps / (ms_max / 1e3)
@@ -487,34 +643,9 @@ def run_ours(args):
     peaks, peak_src = load_peaks()
     flop, nbytes = layer_work(sh, touched, fp8=wl.fp8)
     step_s = ms_max / 1e3 / args.steps
-    work = stage_work(sh, touched, fp8=wl.fp8)
-    dom = max(stage_ms, key=stage_ms.get)
-    dw = work[dom]
-    t_s = stage_ms[dom] / 1e3
-    t_flop = dw["flop"] / (peaks["bf16_tflops_sustained"] * 1e12)
-    t_byte = dw["bytes"] / (peaks["hbm_gbs"] * 1e9)
-    if t_flop >= t_byte:
-        roof = {"bound": "tensor", "achieved": dw["flop"] / t_s / 1e12,
-                "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s"}
-    else:
-        roof = {"bound": "hbm", "achieved": dw["bytes"] / t_s / 1e9, "peak": peaks["hbm_gbs"],
-                "unit": "GB/s"}
-    roof["frac"] = roof["achieved"] / roof["peak"]
-    # the stored figures are captures of the prefill workload (in-batch thresholds)
-    roof["traffic"] = (ncu_traffic(dom, "stages_fp8" if wl.fp8 and dom.startswith("expert")
-                                   else "stages")
-                       if wl.name == "prefill" and wl.qb == "local" else None)
-    roof["kernel"] = dom
-    roof["peak_source"] = f"{peak_src} ({'bf16 sustained' if roof['bound'] == 'tensor' else 'HBM copy'})"
-    roof["algorithmic"] = {"flop": dw["flop"], "bytes": dw["bytes"]}
-
-    stages = {}
-    for name in lmoe.STAGES:
-        sw_ = work[name]
-        t = stage_ms[name] / 1e3
-        stages[name] = {"ms": round(stage_ms[name], 4),
-                        "tflops": round(sw_["flop"] / t / 1e12, 1) if t > 0 and sw_["flop"] else None,
-                        "gbs": round(sw_["bytes"] / t / 1e9, 1) if t > 0 else None}
+    region_s = ms_max / 1e3
+    tflops, kind = pick_peak(peaks, region_s)
+    roof, stages = dominant_roofline(wl, r, peaks, peak_src, region_s)
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
@@ -523,40 +654,35 @@ def run_ours(args):
             "data": "synthetic (seeded; random-init weights of the K3 layer shape)",
             "config": wl.config(world),
             "tflops": flop / step_s / 1e12,
-            "frac_bf16_peak": flop / step_s / 1e12 / peaks["bf16_tflops_sustained"],
-            "layer_roofline_ms": 1e3 * max(flop / (peaks["bf16_tflops_sustained"] * 1e12),
+            "frac_bf16_peak": flop / step_s / 1e12 / tflops,
+            "bf16_peak": f"{tflops} TFLOP/s ({peak_src}, {kind}: timed region {region_s:.3f} s)",
+            "layer_roofline_ms": 1e3 * max(flop / (tflops * 1e12),
                                            nbytes / (peaks["hbm_gbs"] * 1e9)),
             "experts_touched": touched,
             "roofline": roof, "stages": stages,
-            "clocks": clk.summary(),
+            "clocks": r["clocks"],
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": x.numel() * 2,
                     "d2h_bytes_per_step": y.numel() * 2,
                     "path": "lmoe.HostPipeline (copies overlapped across steps)"
                             if wl.qb != "global" else "Layer.forward_host (serial)"},
             "gpu_launches": launches_per_step * args.steps}
 
-    fair = sh.T * sh.K / sh.E
-    line["load"] = {"max_over_mean": float(counts.max() / fair),
-                    "min_over_mean": float(counts.min() / fair),
-                    "idle_experts": int((counts == 0).sum())}
+    line["load"] = load_summary(sh, counts)
     if wl.name == "skew":
         line["load"] = {"before_balancing": wl.extra["load_before"],
-                        "after_balancing": {"max_over_mean": float(counts.max() / fair),
-                                            "min_over_mean": float(counts.min() / fair)}}
+                        "after_balancing": load_summary(sh, counts)}
     if wl.name == "decode":
         line["decode_weight_gbs"] = layer_work(sh, touched, fp8=wl.fp8)[1] / step_s / 1e9
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        wh = host_weights(w)
-        xh = x.cpu()
-        n = args.cpu_tokens
-        if n <= 0:
-            # a bounded sample: about --cpu-seconds of host work, sized from a short probe
-            probe, _, _ = time_oracle(sh, wh, xh, 64)
-            n = int(min(T, max(64, probe * args.cpu_seconds)))
-        rate, dt, cores = time_oracle(sh, wh, xh, n)
-        line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
-                                "sample": f"{n} of the {T} tokens through the whole layer "
-                                          f"(fp64), thresholds over that sub-batch; {dt:.1f} s"}
+    # the CPU baseline runs on host copies; the device copies of this workload are freed
+    # before the other workloads are built
+    wh = host_weights(w) if rank == 0 and world == 1 and not args.no_cpu_baseline else None
+    xh = x.cpu() if wh is not None else None
+    if args.shape == "prefill" and not args.no_configs:
+        del wl, layer, x, w, y, r
+        torch.cuda.empty_cache()
+        line["configs"] = run_configs(args, dev, rank, world, local, stream, peaks, peak_src)
+    if wh is not None:
+        line["cpu_baseline"] = cpu_baseline(sh, wh, xh, args)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -717,10 +843,11 @@ def main():
     ap.add_argument("--shape", choices=sorted(SHAPES) + ["ep"], default="prefill",
                     help="workload (prefill is the headline; the others are extra lines)")
     ap.add_argument("--cpu-tokens", type=int, default=0,
-                    help="tokens in the timed CPU-oracle sample (0: sized by --cpu-seconds)")
-    ap.add_argument("--cpu-seconds", type=float, default=15.0,
-                    help="host time the CPU-oracle sample aims at")
+                    help="tokens of the fixed subset the CPU baseline runs the per-token rest "
+                         "of the layer on (0: 512)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="prefill: leave out the decode, skew and e64 workloads of the line")
     ap.add_argument("--overlap", action="store_true",
                     help="run the shared experts on a second stream beside the routed path")
     ap.add_argument("--shared-sms", type=int, default=0,

@@ -160,6 +160,12 @@ typedef struct lmoe_io {
                             that rounds it to bf16; y is exactly this value rounded to
                             nearest even.  For checking the arithmetic apart from the final
                             rounding; costs one extra fp32 store of the output */
+  const float *logit_bias; /* [E] fp32, or NULL: added to the router logits the layer
+                            computes, logits[t, e] = fl32(lat[t] . W_r[e] + logit_bias[e]),
+                            in the router GEMM's epilogue; thresholds, selection and gates
+                            all see the biased logits.  (A router with a per-expert bias; the
+                            skewed-router workload adds a Zipf bias this way.)  Ignored when
+                            logits_in is given. */
 } lmoe_io;
 
 /* lmoe_io.phase.  The layer splits where its only cross-batch quantity, the thresholds, is

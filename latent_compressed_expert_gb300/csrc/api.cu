@@ -3,10 +3,49 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "common.cuh"
 #include "kernels.cuh"
 
 namespace lmoe {
+
+// Per-stage NVTX ranges ("lmoe" domain, one range per stage of lmoe_forward around the
+// launches of that stage), so that a profiler can attribute and filter kernels by stage
+// (ncu --nvtx --nvtx-include "lmoe@expert_gate_up/").  Without an attached tool the NVTX
+// calls return at once.
+static const char* const STAGE_NAMES[LMOE_NUM_STAGES] = {
+    "latent_shared", "router", "thresholds", "route", "dispatch",
+    "expert_gate_up", "expert_down", "combine", "output"};
+
+static nvtxDomainHandle_t nvtx_domain() {
+  static nvtxDomainHandle_t d = nvtxDomainCreateA("lmoe");
+  return d;
+}
+
+class StageRanges {
+ public:
+  ~StageRanges() { close(); }
+  // ends the open stage's range and opens `stage`'s (none for LMOE_NUM_STAGES)
+  void enter(int stage) {
+    close();
+    if (stage < 0 || stage >= LMOE_NUM_STAGES) return;
+    nvtxEventAttributes_t a = {};
+    a.version = NVTX_VERSION;
+    a.size = NVTX_EVENT_ATTRIB_STRUCT_SIZE;
+    a.messageType = NVTX_MESSAGE_TYPE_ASCII;
+    a.message.ascii = STAGE_NAMES[stage];
+    nvtxDomainRangePushEx(nvtx_domain(), &a);
+    open_ = true;
+  }
+
+ private:
+  void close() {
+    if (open_) nvtxDomainRangePop(nvtx_domain());
+    open_ = false;
+  }
+  bool open_ = false;
+};
 
 static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -820,13 +859,16 @@ int lmoe_forward(const lmoe_dims* dims, const void* packed, const void* x, const
   if (opt.save_pre && (D.expert_fp8 || !aligned16(opt.save_pre))) return LMOE_ERR_INVALID_ARG;
   if (opt.save_pre_shared && !aligned16(opt.save_pre_shared)) return LMOE_ERR_INVALID_ARG;
   if (opt.y_f32_out && !aligned16(opt.y_f32_out)) return LMOE_ERR_INVALID_ARG;
+  if (opt.logit_bias && !aligned16(opt.logit_bias)) return LMOE_ERR_INVALID_ARG;
 
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   using bf = __nv_bfloat16;
   int launches = 0;
   // stage boundary: optional timing event; counts the kernels of the stage just finished
+  StageRanges ranges;
   auto mark = [&](int stage_done_next, int kernels) -> bool {
     launches += kernels;
+    ranges.enter(stage_done_next);
     if (!opt.stage_events) return true;
     cudaEvent_t ev = static_cast<cudaEvent_t>(opt.stage_events[stage_done_next]);
     return ev == nullptr || cudaEventRecord(ev, stream) == cudaSuccess;
@@ -965,6 +1007,7 @@ int lmoe_forward(const lmoe_dims* dims, const void* packed, const void* x, const
     g.epi = EPI_F32;
     g.outf = reinterpret_cast<float*>(ws + W.logits);
     g.ldf = D.E;
+    g.col_bias = opt.logit_bias;
     g.max_ctas = routed_ctas;
     if (want_t) {
       g.outf_t = logits_t;

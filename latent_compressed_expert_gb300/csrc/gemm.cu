@@ -177,6 +177,17 @@ __device__ __forceinline__ void epilogue_store(const GemmArgs& g, int row, int c
       store_bf16x32(g.out0 + r * g.ld0 + col0, v);
       break;
     case EPI_F32: {
+      if (g.col_bias) {
+        const float4* bp = reinterpret_cast<const float4*>(g.col_bias + col0);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const float4 b = __ldg(bp + q);
+          v[4 * q] += b.x;
+          v[4 * q + 1] += b.y;
+          v[4 * q + 2] += b.z;
+          v[4 * q + 3] += b.w;
+        }
+      }
       float4* o = reinterpret_cast<float4*>(g.outf + r * g.ldf + col0);
 #pragma unroll
       for (int q = 0; q < 8; ++q)
@@ -247,8 +258,9 @@ __device__ __forceinline__ void epilogue_store_partial(const GemmArgs& g, int ro
     if (i >= ncols) break;
     const int col = col0 + i;
     if (g.epi == EPI_F32) {
-      g.outf[r * g.ldf + col] = v[i];
-      if (g.outf_t) g.outf_t[static_cast<size_t>(col) * g.ldt + r] = v[i];
+      const float t = g.col_bias ? v[i] + __ldg(g.col_bias + col) : v[i];
+      g.outf[r * g.ldf + col] = t;
+      if (g.outf_t) g.outf_t[static_cast<size_t>(col) * g.ldt + r] = t;
     } else if (g.epi == EPI_BF16) {
       g.out0[r * g.ld0 + col] = __float2bfloat16_rn(v[i]);
     } else if (g.epi == EPI_RESID) {

@@ -51,6 +51,7 @@ struct GemmArgs {
   int ldf;
   float* outf_t;          // EPI_F32: optional transposed copy, outf_t[c * ldt + r]
   int ldt;
+  const float* col_bias;  // EPI_F32: optional per-column addend, outf[r, c] = acc + col_bias[c]
   const __nv_bfloat16* resid;
   int ldr;
   const float* addf;      // EPI_RESID: optional fp32 addend addf[r * lda + c]

@@ -43,7 +43,8 @@ class IO(ctypes.Structure):
                 ("aux_stream", _vp), ("aux_events", _vp * 2), ("shared_sms", _i),
                 ("phase", _i), ("cand_out", _vp), ("cand_k", _i),
                 ("tau_ema", _vp), ("ema_beta", _f), ("ema_first", _i), ("load_stats", _vp),
-                ("save_pre", _vp), ("save_pre_shared", _vp), ("y_f32_out", _vp)]
+                ("save_pre", _vp), ("save_pre_shared", _vp), ("y_f32_out", _vp),
+                ("logit_bias", _vp)]
 
 
 OVERLAP_MIN_T = 512  # LMOE_OVERLAP_MIN_T
@@ -414,7 +415,7 @@ class Layer:
                 stage_events=None, phase: int = PHASE_ALL, cand_k: int = 0,
                 tau_ema: torch.Tensor | None = None, ema_beta: float = 0.9,
                 ema_first: bool = False, load_stats: "LoadStats | None" = None,
-                train: bool = False):
+                train: bool = False, logit_bias: torch.Tensor | None = None):
         """One lmoe_forward call.  stage_events: optional list of NUM_STAGES + 1
         torch.cuda.Event(enable_timing=True) recorded at the stage boundaries.  After the
         call, ``self.last_kernel_launches`` holds the number of kernels it launched.
@@ -424,7 +425,8 @@ class Layer:
         batch's (ema_beta, ema_first) and routed against.  load_stats: a LoadStats that this
         step's per-expert counts are added to.  train: also keep the routed experts'
         pre-activations (lmoe_io.save_pre) for the next ``backward`` / ``backward_layer``
-        (needs ``enable_backward``)."""
+        (needs ``enable_backward``).  logit_bias: [E] fp32 added to the router logits the
+        layer computes (lmoe_io.logit_bias)."""
         sh = self.shape
         T = x.shape[0]
         if T > self.max_tokens:
@@ -455,6 +457,9 @@ class Layer:
         if logits_in is not None:
             _expect(logits_in, torch.float32, (T, sh.E), "logits_in")
             io.logits_in = _ptr(logits_in)
+        if logit_bias is not None:
+            _expect(logit_bias, torch.float32, (sh.E,), "logit_bias")
+            io.logit_bias = _ptr(logit_bias)
         if tau_ema is not None:
             _expect(tau_ema, torch.float32, (sh.E,), "tau_ema")
             io.tau_ema = _ptr(tau_ema)

@@ -133,9 +133,15 @@ def make_logits(T: int, E: int, seed: int, device="cpu", zipf_s: float | None = 
     dominate the raw scores."""
     z = _normal((T, E), scale, _gen(seed, f"logits/{T}x{E}", device), device, torch.float32)
     if zipf_s is not None:
-        rank = torch.randperm(E, generator=_gen(seed, f"zipf/{E}", device), device=device) + 1
-        z += (-zipf_s * torch.log(rank.to(torch.float32))).unsqueeze(0)
+        z += zipf_bias(E, seed, zipf_s, device).unsqueeze(0)
     return z
+
+
+def zipf_bias(E: int, seed: int, s: float = 1.1, device="cpu") -> torch.Tensor:
+    """Per-expert router bias [E] fp32 of the skewed-router workload: -s * ln(rank_e), with
+    rank a seeded permutation of 1..E."""
+    rank = torch.randperm(E, generator=_gen(seed, f"zipf/{E}", device), device=device) + 1
+    return (-s * torch.log(rank.to(torch.float32))).contiguous()
 
 
 def make_uniform_logits(T: int, E: int, seed: int, device="cpu", lo=-4.0, hi=4.0,

@@ -370,6 +370,34 @@ def test_shared_overlap_and_serial_paths(dev, oracle_mod, overlap):
     H.assert_layer_close(y, dbg["y_f32"], ref.y, f"mid/overlap={overlap}")
 
 
+@pytest.mark.parametrize("T", [1000, 64])
+def test_router_logit_bias(dev, T):
+    """lmoe_io.logit_bias: the router GEMM adds b_e to its fp32 accumulator (T = 64 through
+    the split-K sum), so the logits are exactly fl32(unbiased logits + b), the accumulator
+    being deterministic; the layer then routes on them as lmoe_route does, and the output
+    equals that of a call given those logits."""
+    sh = H.mid_shape(T)
+    w = synth.make_weights(sh, seed=41, device=dev)
+    layer = lmoe.Layer(sh, w)
+    x = synth.make_x(sh, seed=41, device=dev)
+    bias = synth.zipf_bias(sh.E, seed=41, device=dev)
+    _, d0 = layer.forward(x, residual=x, balance=False, debug=True)
+    y1, d1 = layer.forward(x, residual=x, balance=False, logit_bias=bias, debug=True)
+    y1 = y1.clone()
+    torch.cuda.synchronize()
+    assert layer.device_error() == 0
+    want = d0["logits"] + bias.unsqueeze(0)
+    assert torch.equal(d1["logits"].view(torch.int32), want.view(torch.int32))
+    idx, gate = lmoe.route(want, None, sh.K)
+    assert torch.equal(d1["idx"], idx) and torch.equal(d1["gate"].view(torch.int32),
+                                                       gate.view(torch.int32))
+    y2 = layer.forward(x, residual=x, balance=False, logits_in=want.contiguous())
+    torch.cuda.synchronize()
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+    # the bias moves load toward the favoured experts
+    assert int(d1["counts"].max()) > int(d0["counts"].max())
+
+
 def test_checked_mode_reports_nonfinite_logits(dev, monkeypatch):
     """LMOE_CHECK_FINITE=1: a NaN router logit is reported as an invalid argument through
     lmoe_last_device_error.  Without the check, NaN logits still select valid experts
