@@ -356,6 +356,7 @@ static int routed_bwd_back(const RoutedBwd& R, const float* dlat_add, float* dla
     g.err = err;
     g.timeout_ns = wait_limit_ns();
     g.mean_tokens = static_cast<int>(static_cast<int64_t>(TK) / E);
+    g.tokn = grouped_tokn(T, D.K, E);  // as the forward's dispatch built ct_off
     return g;
   };
   // 3. dh = do . W_ed (per expert, weights transposed)
@@ -1079,9 +1080,10 @@ int lmoe_forward(const lmoe_dims* dims, const void* packed, const void* x, const
   int32_t* ct_off = reinterpret_cast<int32_t*>(ws + W.ct_off);
   int32_t* inv = reinterpret_cast<int32_t*>(ws + W.inv);
   int32_t* src_tok = reinterpret_cast<int32_t*>(ws + W.src_tok);
+  const int tokn = grouped_tokn(T, D.K, D.E);
   rc = launch_dispatch(idx, T, D.E, D.K, reinterpret_cast<uint32_t*>(ws + W.masks),
-                       reinterpret_cast<uint32_t*>(ws + W.base), offsets, ct_off, inv, src_tok,
-                       opt.counts_out, err, stream);
+                       reinterpret_cast<uint32_t*>(ws + W.base), offsets, ct_off, tokn, inv,
+                       src_tok, opt.counts_out, err, stream);
   if (rc != LMOE_OK) return rc;
   if (opt.load_stats) {
     rc = launch_load_stats(nullptr, offsets, D.E, opt.load_stats, stream);
@@ -1127,6 +1129,7 @@ int lmoe_forward(const lmoe_dims* dims, const void* packed, const void* x, const
     g.timeout_ns = wait_limit_ns();
     g.max_ctas = routed_ctas;
     g.mean_tokens = static_cast<int>(static_cast<int64_t>(TK) / D.E);
+    g.tokn = tokn;
     rc = launch_grouped_gemm(pk + P.wgu, xop, static_cast<uint64_t>(T), D.L, g, stream);
     if (rc != LMOE_OK) return rc;
   }
@@ -1148,6 +1151,7 @@ int lmoe_forward(const lmoe_dims* dims, const void* packed, const void* x, const
     g.timeout_ns = wait_limit_ns();
     g.max_ctas = routed_ctas;
     g.mean_tokens = static_cast<int>(static_cast<int64_t>(TK) / D.E);
+    g.tokn = tokn;
     const void* xop = h;
     if (fp8) {
       // e4m3 SiTU outputs, one scale per (token, expert) row

@@ -32,13 +32,19 @@ constexpr int GLU_GROUP = 16;
 // Tokens per block in the dispatch (permute) kernels: one 32-bit mask word per expert.
 constexpr int DISPATCH_TOKENS = 32;
 
-// Largest token count (MMA N) of one routed-expert GEMM tile; an expert's token rows are cut
-// into chunks of at most this many.  192 covers the K3 prefill load (146 on average, under
-// 1.2x that at most with Quantile-Balancing thresholds) in one chunk.
-#ifndef LMOE_GROUPED_TOKN
-#define LMOE_GROUPED_TOKN 192
-#endif
-constexpr int GROUPED_TOKN = LMOE_GROUPED_TOKN;
+// Token chunks of the routed-expert GEMMs (MMA N): an expert's token rows are cut into
+// ceil(count / tokn) chunks of equal size (to one row), tokn = GROUPED_TOKN or, when experts
+// average more than that, GROUPED_TOKN_WIDE.  192 covers the K3 prefill load (146 on average,
+// under 1.2x that at most with Quantile-Balancing thresholds) in one chunk; at 585 tokens per
+// expert (T = 32768) 256 makes three chunks of 195 instead of four.
+constexpr int GROUPED_TOKN = 192;
+constexpr int GROUPED_TOKN_WIDE = 256;
+
+// The chunk size of a batch, a function of its dims only, so that the forward and the
+// backward, which reads the forward's chunk offsets, agree.
+inline int grouped_tokn(int64_t T, int K, int E) {
+  return E > 0 && T * K / E > GROUPED_TOKN ? GROUPED_TOKN_WIDE : GROUPED_TOKN;
+}
 
 __host__ __device__ inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 

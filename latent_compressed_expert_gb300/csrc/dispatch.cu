@@ -53,15 +53,15 @@ dispatch_mask_kernel(const int32_t* __restrict__ idx, int T, int E, int K,
 // across the warps, and a second pass over the strip writes the bases.  The counts go to
 // offsets[e]; the last CTA to finish (a fence and an atomic counter that the mask kernel
 // zeroed, no waiting) turns them into the exclusive scans offsets (rows) and ct_off (token
-// chunks of the routed-expert GEMMs, ceil(count / GROUPED_TOKN)).
+// chunks of the routed-expert GEMMs, ceil(count / tokn)).
 constexpr int SCAN_WARPS = 8;
 constexpr int SCAN_THREADS = SCAN_WARPS * 32;
 
 __global__ void __launch_bounds__(SCAN_THREADS)
 dispatch_scan_kernel(const uint32_t* __restrict__ masks, int nb, int E,
                      uint32_t* __restrict__ base, int32_t* __restrict__ offsets,
-                     int32_t* __restrict__ ct_off, int32_t* __restrict__ counts_out,
-                     uint32_t* __restrict__ done) {
+                     int32_t* __restrict__ ct_off, int tokn,
+                     int32_t* __restrict__ counts_out, uint32_t* __restrict__ done) {
   __shared__ uint32_t part[SCAN_WARPS][32];
   __shared__ int32_t wsum[2][SCAN_WARPS];
   __shared__ bool last;
@@ -108,7 +108,7 @@ dispatch_scan_kernel(const uint32_t* __restrict__ masks, int nb, int E,
   for (int i = e0; i < e1; ++i) {
     const int32_t c = __ldcg(offsets + i);
     c_rows += c;
-    c_chunks += static_cast<int32_t>(ceil_div(c, GROUPED_TOKN));
+    c_chunks += static_cast<int32_t>(ceil_div(c, tokn));
   }
   int32_t ir = c_rows, ic = c_chunks;  // inclusive scans within the warp
   for (int o = 1; o < 32; o <<= 1) {
@@ -139,7 +139,7 @@ dispatch_scan_kernel(const uint32_t* __restrict__ masks, int nb, int E,
     offsets[i] = pr;
     ct_off[i] = pc;
     pr += c;
-    pc += static_cast<int32_t>(ceil_div(c, GROUPED_TOKN));
+    pc += static_cast<int32_t>(ceil_div(c, tokn));
   }
   if (threadIdx.x == 0) {
     offsets[E] = tr;  // == T*K when every index was valid
@@ -359,8 +359,9 @@ combine_bulk_kernel(const __nv_bfloat16* __restrict__ o, const float* __restrict
 
 // ------------------------------------------------------------------------------------
 int launch_dispatch(const int32_t* idx, int T, int E, int K, uint32_t* masks, uint32_t* base,
-                    int32_t* offsets, int32_t* ct_off, int32_t* inv, int32_t* src_tok,
-                    int32_t* counts_out, uint32_t* err, cudaStream_t stream) {
+                    int32_t* offsets, int32_t* ct_off, int tokn, int32_t* inv,
+                    int32_t* src_tok, int32_t* counts_out, uint32_t* err, cudaStream_t stream) {
+  if (tokn < 1) return LMOE_ERR_INVALID_ARG;
   const int nb = static_cast<int>(ceil_div(T, DISPATCH_TOKENS));
   const size_t msmem = static_cast<size_t>(E) * sizeof(uint32_t);
   uint32_t* done = err + 1;  // the word after the error flag
@@ -372,7 +373,8 @@ int launch_dispatch(const int32_t* idx, int T, int E, int K, uint32_t* masks, ui
     return LMOE_ERR_CUDA;
   }
   if (launch_pdl(dispatch_scan_kernel, static_cast<unsigned>(ceil_div(E, 32)), SCAN_THREADS, 0,
-                 stream, masks, nb, E, base, offsets, ct_off, counts_out, done) != cudaSuccess)
+                 stream, masks, nb, E, base, offsets, ct_off, tokn, counts_out, done) !=
+      cudaSuccess)
     return LMOE_ERR_CUDA;
   if (nb > 0) {
     const int64_t pairs = static_cast<int64_t>(T) * K;

@@ -40,14 +40,22 @@ namespace lmoe {
 // stage: two MMAs per K-step into the two halves of TMEM, half the B bytes per FLOP, so the
 // same shared memory covers a longer load latency.  Its single accumulator is drained
 // before the next pair starts, so it serves long reductions (dense mode only).
+// TMEM is allocated in powers of two columns (32 at least).
+constexpr int tmem_alloc_cols(int cols) {
+  int n = 32;
+  while (n < cols) n *= 2;
+  return n;
+}
+
+// BN = 224 serves N = 896 (the router over 896 experts) in four whole column tiles.
 template <int BN, int MT>
 struct GemmCfg {
   static constexpr int A_BYTES = BLOCK_M * BLOCK_K * 2;  // one 128-row M-tile
   static constexpr int B_BYTES = BN * BLOCK_K * 2;
   static constexpr int STAGE_BYTES = MT * A_BYTES + B_BYTES;
-  static constexpr int STAGES = MT == 2 ? (BN == 256 ? 3 : 4) : (BN == 256 ? 4 : 6);
+  static constexpr int STAGES = BN >= 224 ? (MT == 2 ? 3 : 4) : (MT == 2 ? 4 : 6);
   static constexpr int ACC = MT == 2 ? 1 : 2;  // accumulator buffers of MT x BN columns
-  static constexpr int TMEM_COLS = 2 * BN;
+  static constexpr int TMEM_COLS = tmem_alloc_cols(2 * BN);
   static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
   static constexpr int NUM_BARS = 2 * STAGES + 6;
   static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
@@ -249,6 +257,42 @@ __device__ __forceinline__ void epilogue_store(const GemmArgs& g, int row, int c
   }
 }
 
+// EPI_RESID with the chunk's residual already loaded (raw bf16, 4 x 16 bytes): the dense
+// epilogue loads chunk i + 1's residual before it waits on chunk i's accumulator columns, so
+// the global-load latency is paid once per tile rather than once per 32-column chunk.
+__device__ __forceinline__ void store_resid_prefetched(const GemmArgs& g, int row, int col0,
+                                                       float (&v)[32], const uint4 (&rv)[4]) {
+  const size_t r = static_cast<size_t>(row);
+  if (g.addf) {
+    const float4* ap = reinterpret_cast<const float4*>(g.addf + r * g.lda + col0);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const float4 a = __ldg(ap + q);
+      v[4 * q] += a.x;
+      v[4 * q + 1] += a.y;
+      v[4 * q + 2] += a.z;
+      v[4 * q + 3] += a.w;
+    }
+  }
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&rv[q]);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = __bfloat1622float2(h[i]);
+      v[8 * q + 2 * i] += f.x;
+      v[8 * q + 2 * i + 1] += f.y;
+    }
+  }
+  if (g.outf) {  // the value before its rounding to bf16
+    float4* o = reinterpret_cast<float4*>(g.outf + r * g.ldf + col0);
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      o[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+  }
+  store_bf16x32(g.out0 + r * g.ld0 + col0, v);
+}
+
 // Last, partly valid 32-column slice (plain stores only; the GLU modes need whole slices).
 __device__ __forceinline__ void epilogue_store_partial(const GemmArgs& g, int row, int col0,
                                                    int ncols, const float (&v)[32]) {
@@ -279,8 +323,10 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB, const GemmArgs g) {
   using C = GemmCfg<BN, MT>;
   constexpr int TM = BLOCK_M * MT;
-  if constexpr (MT != 1) {
-    if (g.groups > 0) {  // tile pairs serve the dense mode only; the launcher never does this
+  if constexpr (MT != 1 || BN % 64 != 0) {
+    // tile pairs and 224-wide tiles serve the dense mode only (grouped-K loads B in 64-row
+    // boxes); the launcher never does this
+    if (g.groups > 0) {
       if (threadIdx.x == 0) atomicOr(g.err, DEVERR_BAD_INDEX);
       return;
     }
@@ -516,6 +562,33 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA,
             (g.groups > 0 && row_ok) ? (g.row_map ? __ldg(g.row_map + row) : row) : 0;
         const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                static_cast<uint32_t>((acc + h) * BN);
+        // Residual epilogue over whole 32-column chunks: chunk ch + 1's residual is loaded
+        // before chunk ch's accumulator columns are read (the condition is warp-uniform; the
+        // tcgen05.ld is executed by every lane, the global accesses by the rows inside M).
+        if (g.epi == EPI_RESID && g.resid != nullptr && g.ksplit <= 1 && g.groups == 0 &&
+            tc.n0 + BN <= g.N) {
+          const uint4* rrow = reinterpret_cast<const uint4*>(
+              g.resid + static_cast<size_t>(row_ok ? row : 0) * g.ldr + tc.n0);
+          uint4 rnext[4];
+          if (row_ok) {
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) rnext[q4] = __ldg(rrow + q4);
+          }
+#pragma unroll 1
+          for (int ch = 0; ch < BN / 32; ++ch) {
+            uint4 rcur[4];
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) rcur[q4] = rnext[q4];
+            if (row_ok && ch + 1 < BN / 32) {
+#pragma unroll
+              for (int q4 = 0; q4 < 4; ++q4) rnext[q4] = __ldg(rrow + 4 * (ch + 1) + q4);
+            }
+            float v[32];
+            ptx::tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(ch * 32), v);
+            if (row_ok) store_resid_prefetched(g, row, tc.n0 + ch * 32, v, rcur);
+          }
+          continue;
+        }
 #pragma unroll 1
         for (int ch = 0; ch < BN / 32; ++ch) {
           const int col0 = tc.n0 + ch * 32;
@@ -737,7 +810,12 @@ int launch_gemm(const void* A, uint64_t a_rows, int a_ld, const void* B, uint64_
   // 256-wide tiles unless N is small and not a multiple of 256 (a partial last column tile is
   // zero-filled by TMA and cut at N by the epilogue): the router's N = 896 runs as 4 column
   // tiles instead of 7, re-reading the latent half as often (61.9 -> 59.4 us at prefill)
-  const int bn = (g.N % 256 == 0 || g.N > 512) ? 256 : 128;
+  // N = 896 (the router over 896 experts): four whole 224-wide tiles instead of four 256-wide
+  // ones, the last half empty
+  const int bn = (g.groups == 0 && g.N % 256 != 0 && g.N > 512 && g.N % 224 == 0 &&
+                  g.N <= 4 * 224)
+                     ? 224
+                     : ((g.N % 256 == 0 || g.N > 512) ? 256 : 128);
   CUtensorMap ta, tb;
   if (g.groups > 0) {
     // MN-major: a_rows / b_rows count K rows; boxes of 64 columns x 64 rows
@@ -770,8 +848,9 @@ int launch_gemm(const void* A, uint64_t a_rows, int a_ld, const void* B, uint64_
       const int per = static_cast<int>(ceil_div(nkb, ks));
       GemmArgs gs = g;
       gs.ksplit = static_cast<int>(ceil_div(nkb, per));  // no slice is left empty
-      const int rc = bn == 256 ? launch_bn<256, 1>(ta, tb, gs, stream)
-                               : launch_bn<128, 1>(ta, tb, gs, stream);
+      const int rc = bn == 256   ? launch_bn<256, 1>(ta, tb, gs, stream)
+                     : bn == 224 ? launch_bn<224, 1>(ta, tb, gs, stream)
+                                 : launch_bn<128, 1>(ta, tb, gs, stream);
       if (rc != LMOE_OK) return rc;
       const int64_t chunks = static_cast<int64_t>(g.M) * ceil_div(g.N, 32);
       const bool warp = gs.ksplit >= SPLITK_WARP_MIN;
@@ -792,6 +871,8 @@ int launch_gemm(const void* A, uint64_t a_rows, int a_ld, const void* B, uint64_
                      ceil_div(g.M, 2 * BLOCK_M) * ceil_div(g.N, bn) >= 2 * static_cast<int64_t>(sms);
   if (bn == 256)
     return pairs ? launch_bn<256, 2>(ta, tb, g, stream) : launch_bn<256, 1>(ta, tb, g, stream);
+  if (bn == 224)
+    return pairs ? launch_bn<224, 2>(ta, tb, g, stream) : launch_bn<224, 1>(ta, tb, g, stream);
   return pairs ? launch_bn<128, 2>(ta, tb, g, stream) : launch_bn<128, 1>(ta, tb, g, stream);
 }
 

@@ -37,16 +37,30 @@ constexpr int GROUPED_BOX_T = 32;  // token rows per TMA box / padding granule o
 constexpr int GROUPED_STAGES_DEEP = 5;
 constexpr int GROUPED_STAGES_SHALLOW = 4;
 constexpr int GROUPED_SHALLOW_MIN_TOKENS = 32;
+// Weight-tile pairs: stages of two weight boxes and a token tile (56 or 64 KB): three fit.
+constexpr int GROUPED_STAGES_PAIR = 3;
+constexpr int GROUPED_PAIR_MIN_TOKENS = 64;  // experts' mean token count from which pairs run
 
-template <int STAGES_>
+// MW: weight row tiles per CTA tile.  MW = 2 ("weight-tile pairs") stages two 128-row
+// weight tiles of the same expert with one token tile and issues two MMAs per K-step, so
+// every gathered or loaded token row serves 256 output features: half the token bytes per
+// FLOP, for experts with many tokens, where the token rows and not the weights bound the
+// shared-memory fill.  Its accumulator pair fills TMEM (2 x 256 columns), so it is drained
+// while no MMA runs (the producer keeps loading the next tile meanwhile).
+// TOKN_: the largest token chunk the tile holds (the shared-memory token tile and the TMEM
+// columns of one accumulator); the chunks themselves are set by GroupedArgs::tokn <= TOKN_.
+template <int STAGES_, int MW_, int TOKN_>
 struct GroupedCfg {
-  static constexpr int TOKN = GROUPED_TOKN;               // max tokens (N) per tile
+  static constexpr int TOKN = TOKN_;                      // max tokens (N) per tile
+  static constexpr int MW = MW_;
   static constexpr int BOX_T = GROUPED_BOX_T;             // token rows per TMA box
-  static constexpr int A_BYTES = BLOCK_M * BLOCK_K * 2;   // 16 KB of weights
-  static constexpr int B_BYTES = TOKN * BLOCK_K * 2;      // up to 24 KB of activations
-  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int A_BYTES = BLOCK_M * BLOCK_K * 2;   // 16 KB per weight tile
+  static constexpr int W_BYTES = MW * A_BYTES;
+  static constexpr int B_BYTES = TOKN * BLOCK_K * 2;      // up to 32 KB of activations
+  static constexpr int STAGE_BYTES = W_BYTES + B_BYTES;
   static constexpr int STAGES = STAGES_;
-  static constexpr int ACC_COLS = 256;                    // TMEM columns between accumulators
+  static constexpr int ACC = MW == 2 ? 1 : 2;             // accumulator sets (double buffer)
+  static constexpr int ACC_COLS = 256;                    // TMEM columns per accumulator
   static constexpr int TMEM_COLS = 512;
   static constexpr int EPI_OFF = STAGES * STAGE_BYTES;   // per epilogue warp 32 x 32 bf16
   static constexpr int EPI_BYTES = 8 * 32 * 32 * 2;
@@ -54,14 +68,16 @@ struct GroupedCfg {
   static constexpr int NUM_BARS = 2 * STAGES + 5;
   static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
   static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;
+  static_assert(MW == 1 || MW == 2, "one or two weight tiles");
   static_assert(TOKN % BOX_T == 0 && TOKN % 16 == 0 && TOKN <= 256, "UMMA N range");
-  static_assert(TOKN <= ACC_COLS && 2 * ACC_COLS <= TMEM_COLS, "two accumulators");
+  static_assert(TOKN <= ACC_COLS && ACC * MW * ACC_COLS <= TMEM_COLS, "accumulators fit TMEM");
   static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "1024-aligned tiles");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
 
 // warp 0 TMA producer, warp 1 MMA, warps 2..5 epilogue, warps 6..9 row gatherers (used when
-// the activation rows are gathered through an index, idle otherwise)
+// the activation rows are gathered through an index; otherwise a second epilogue group for
+// the e4m3 down GEMM and for weight-tile pairs)
 constexpr int GROUPED_EPI_WARPS = 4;
 constexpr int GROUPED_GATHER_WARPS = 4;
 constexpr int GROUPED_GATHER_THREADS = GROUPED_GATHER_WARPS * 32;
@@ -71,14 +87,21 @@ struct GTile {
   int e;        // expert
   int w_row;    // row coordinate of the tile's first 128 x 64 weight box (tiled layout)
   int r0;       // first weight row within the expert (output feature)
+  int nw;       // weight tiles in this tile (MW, or 1 for an odd expert's last)
   int tok0;     // first token row (permuted order)
-  int ntok;     // valid token rows in this tile (1..TOKN)
+  int ntok;     // valid token rows in this tile (1..tokn)
   int npad;     // ntok rounded up to BOX_T
 };
 
+// Tile -> (expert, token chunk, weight tile group).  An expert's `count` token rows form
+// ceil(count / tokn) chunks of equal size (to one row); its MW-tile groups of weight rows are
+// enumerated fastest, so the tiles that share a chunk's token rows run at the same time on
+// neighbouring SMs.
+template <int MW>
 __device__ __forceinline__ GTile decode_gtile(const GroupedArgs& g, int mt, int tile) {
-  const int q = tile / mt;  // global (expert, chunk) index
-  int lo = 0, hi = g.E;     // ct_off[lo] <= q < ct_off[hi]
+  const int mg = (mt + MW - 1) / MW;  // weight tile groups per (expert, chunk)
+  const int q = tile / mg;            // global (expert, chunk) index
+  int lo = 0, hi = g.E;               // ct_off[lo] <= q < ct_off[hi]
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
     if (__ldg(g.ct_off + mid) <= q)
@@ -87,15 +110,20 @@ __device__ __forceinline__ GTile decode_gtile(const GroupedArgs& g, int mt, int 
       hi = mid;
   }
   const int e = lo;
-  const int chunk = q - __ldg(g.ct_off + e);
-  const int m = tile - q * mt;
+  const int c0 = __ldg(g.ct_off + e);
+  const int chunk = q - c0;
+  const int nchunk = __ldg(g.ct_off + e + 1) - c0;
+  const int m = (tile - q * mg) * MW;
   GTile t;
   t.e = e;
   t.r0 = m * BLOCK_M;
+  t.nw = min(MW, mt - m);
   t.w_row = (e * mt + m) * (g.Kd / BLOCK_K) * BLOCK_M;
-  t.tok0 = __ldg(g.seg_off + e) + chunk * GROUPED_TOKN;
-  const int end = __ldg(g.seg_off + e + 1);
-  t.ntok = min(GROUPED_TOKN, end - t.tok0);
+  const int seg0 = __ldg(g.seg_off + e);
+  const int cnt = __ldg(g.seg_off + e + 1) - seg0;
+  const int csz = (cnt + nchunk - 1) / nchunk;  // <= tokn; every chunk non-empty
+  t.tok0 = seg0 + chunk * csz;
+  t.ntok = min(csz, cnt - chunk * csz);
   t.npad = (t.ntok + GROUPED_BOX_T - 1) / GROUPED_BOX_T * GROUPED_BOX_T;
   return t;
 }
@@ -148,11 +176,11 @@ __device__ __forceinline__ float situ_close(float g, float v, float c, float inv
   return __fdividef(gc, 1.0f + __expf(fminf(-gc, 80.0f))) * vc;
 }
 
-template <int STAGES_, bool FP8>
+template <int STAGES_, bool FP8, int MW, int TOKN_>
 __global__ void __launch_bounds__(GROUPED_THREADS, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
                     const __grid_constant__ CUtensorMap tmX, const GroupedArgs g) {
-  using C = GroupedCfg<STAGES_>;
+  using C = GroupedCfg<STAGES_, MW, TOKN_>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = ptx::smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -181,9 +209,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
     }
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(&tfull[a], 1);
-      // with e4m3 operands and nothing gathered, warps 6..9 join the epilogue
-      ptx::mbar_init(&tempty[a],
-                     ((FP8 && !g.gather) ? 2 * GROUPED_EPI_WARPS : GROUPED_EPI_WARPS) * 32);
+      // with nothing gathered (the down GEMM), warps 6..9 join the epilogue for e4m3
+      // operands and for weight-tile pairs
+      ptx::mbar_init(&tempty[a], (((FP8 || MW == 2) && !g.gather) ? 2 * GROUPED_EPI_WARPS
+                                                                 : GROUPED_EPI_WARPS) * 32);
     }
     ptx::mbar_init(drain, 1);
     *abort_flag = 0;
@@ -203,7 +232,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
   const uint32_t tmem_base = *tmem_slot;
   pdl_wait();  // from here on: the previous kernel's outputs (segments, rows) are visible
   pdl_launch_dependents();
-  const int total = __ldg(g.ct_off + g.E) * mt;
+  const int total = __ldg(g.ct_off + g.E) * ((mt + MW - 1) / MW);
 
   if (warp == 0) {
     if (lane == 0) {
@@ -212,9 +241,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
       uint32_t it = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-        const GTile t = decode_gtile(g, mt, tile);
+        const GTile t = decode_gtile<MW>(g, mt, tile);
         const int nbox = g.gather ? 0 : t.npad / C::BOX_T;
-        const uint32_t bytes = C::A_BYTES + static_cast<uint32_t>(nbox) * C::BOX_T * BLOCK_K * 2;
+        const uint32_t bytes = static_cast<uint32_t>(t.nw) * C::A_BYTES +
+                               static_cast<uint32_t>(nbox) * C::BOX_T * BLOCK_K * 2;
         for (int kb = 0; kb < nk; ++kb, ++it) {
           const int s = static_cast<int>(it % C::STAGES);
           const uint32_t ph = (it / C::STAGES) & 1u;
@@ -224,12 +254,15 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
             break;
           }
           uint8_t* sa = smem + s * C::STAGE_BYTES;
-          uint8_t* sb = sa + C::A_BYTES;
+          uint8_t* sb = sa + C::W_BYTES;
           ptx::mbar_arrive_expect_tx(&full[s], bytes);
-          if (g.evict_first)
-            ptx::tma_load_2d_hint(sa, &tmW, &full[s], 0, t.w_row + kb * BLOCK_M, w_policy);
-          else
-            ptx::tma_load_2d(sa, &tmW, &full[s], 0, t.w_row + kb * BLOCK_M);
+          for (int w = 0; w < t.nw; ++w) {  // an expert's row tiles are nk boxes apart
+            const int wr = t.w_row + (w * nk + kb) * BLOCK_M;
+            if (g.evict_first)
+              ptx::tma_load_2d_hint(sa + w * C::A_BYTES, &tmW, &full[s], 0, wr, w_policy);
+            else
+              ptx::tma_load_2d(sa + w * C::A_BYTES, &tmW, &full[s], 0, wr);
+          }
           for (int b = 0; b < nbox; ++b)
             ptx::tma_load_2d(sb + b * C::BOX_T * BLOCK_K * 2, &tmX, &full[s], kb * BLOCK_K,
                              t.tok0 + b * C::BOX_T);
@@ -250,16 +283,18 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
       uint32_t it = 0;
       int lt = 0;
       for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++lt) {
-        const GTile t = decode_gtile(g, mt, tile);
+        const GTile t = decode_gtile<MW>(g, mt, tile);
         const uint32_t idesc = FP8 ? ptx::idesc_e4m3_f32(BLOCK_M, t.npad)
                                    : ptx::idesc_bf16_f32(BLOCK_M, t.npad);
-        const int acc = lt & 1;
-        const uint32_t aph = static_cast<uint32_t>(lt >> 1) & 1u;
+        const int acc = C::ACC == 2 ? (lt & 1) : 0;
+        const uint32_t aph = C::ACC == 2 ? (static_cast<uint32_t>(lt >> 1) & 1u)
+                                         : (static_cast<uint32_t>(lt) & 1u);
         if (!ptx::mbar_wait(&tempty[acc], aph ^ 1u, abort_flag, limit)) {
           graise(g, abort_flag, DEVERR_TIMEOUT_MMA);
           break;
         }
         ptx::tc_fence_after();
+        // weight tile w of the tile accumulates at TMEM columns (acc + w) * ACC_COLS
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * C::ACC_COLS);
         bool ok = true;
         for (int kb = 0; kb < nk; ++kb, ++it) {
@@ -273,15 +308,21 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
           ptx::tc_fence_after();
           if (g.gather) ptx::fence_proxy_async_smem();  // rows written by cp.async
           const uint32_t sa = ptx::smem_u32(smem + s * C::STAGE_BYTES);
-          const uint32_t sb = sa + C::A_BYTES;
+          const uint32_t sb = sa + C::W_BYTES;
 #pragma unroll
           for (int k = 0; k < BLOCK_K / 16; ++k) {  // 32 bytes of K per instruction
-            if constexpr (FP8)
-              ptx::umma_e4m3(d_tmem, ptx::smem_desc_sw128(sa + k * 32),
-                             ptx::smem_desc_sw128(sb + k * 32), idesc, (kb | k) != 0 ? 1u : 0u);
-            else
-              ptx::umma_bf16(d_tmem, ptx::smem_desc_sw128(sa + k * 32),
-                             ptx::smem_desc_sw128(sb + k * 32), idesc, (kb | k) != 0 ? 1u : 0u);
+#pragma unroll
+            for (int w = 0; w < MW; ++w) {
+              if (w >= t.nw) break;
+              const uint32_t dw = d_tmem + static_cast<uint32_t>(w * C::ACC_COLS);
+              const uint32_t aw = sa + w * C::A_BYTES + k * 32;
+              if constexpr (FP8)
+                ptx::umma_e4m3(dw, ptx::smem_desc_sw128(aw), ptx::smem_desc_sw128(sb + k * 32),
+                               idesc, (kb | k) != 0 ? 1u : 0u);
+              else
+                ptx::umma_bf16(dw, ptx::smem_desc_sw128(aw), ptx::smem_desc_sw128(sb + k * 32),
+                               idesc, (kb | k) != 0 ? 1u : 0u);
+            }
           }
           ptx::umma_commit(&empty[s]);
         }
@@ -291,7 +332,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
       ptx::umma_commit(drain);
       if (!gwait_drain(drain, 0u, limit)) graise(g, abort_flag, DEVERR_TIMEOUT_DRAIN);
     }
-  } else if (warp >= 2 + GROUPED_EPI_WARPS && (g.gather || !FP8)) {
+  } else if (warp >= 2 + GROUPED_EPI_WARPS && (g.gather || (!FP8 && MW == 1))) {
     // ------------------------------------------------------------ row gatherers (warps 6..9)
     // Thread gt copies 16-byte chunk (gt & 7) of rows gt/8 + 16 j of each stage's token
     // tile, from the activation row src = gather[permuted row], into the 128-byte-swizzled
@@ -303,7 +344,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
       uint32_t it = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-        const GTile t = decode_gtile(g, mt, tile);
+        const GTile t = decode_gtile<MW>(g, mt, tile);
         const __nv_bfloat16* src[J];
 #pragma unroll
         for (int j = 0; j < J; ++j) {
@@ -319,7 +360,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
             ok = false;
             break;
           }
-          const uint32_t sb = ptx::smem_u32(smem + s * C::STAGE_BYTES + C::A_BYTES);
+          const uint32_t sb = ptx::smem_u32(smem + s * C::STAGE_BYTES + C::W_BYTES);
 #pragma unroll
           for (int j = 0; j < J; ++j) {
             const int row = (gt >> 3) + 16 * j;
@@ -332,37 +373,41 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
       ptx::cp_async_wait_all();
     }
   } else {
-    // ------------------------------------------------------------ epilogue (warps 2..5, and
-    // 6..9 for the e4m3 down GEMM: two warps per TMEM lane quarter, even and odd chunks).
-    // Its mainloop is half as long as the bf16 one, so the output stores bound it; the bf16
-    // down GEMM measured slower with the second group (its warps only poll)
+    // ------------------------------------------------------------ epilogue (warps 2..5; with
+    // nothing gathered, also 6..9: for the e4m3 down GEMM the two groups take the even and
+    // odd token chunks -- its mainloop is half as long as the bf16 one, so the output stores
+    // bound it -- and for weight-tile pairs one weight tile each).  The bf16 down GEMM of
+    // single weight tiles measured slower with the second group (its warps only poll).
     const int q = warp & 3;  // TMEM lane quarter this warp may access
-    const int egroups = (FP8 && !g.gather) ? 2 : 1;
+    const bool two = (FP8 || MW == 2) && !g.gather;
     const int eg = (warp - 2) / GROUPED_EPI_WARPS;
+    const int ch0 = (two && MW == 1) ? eg : 0, chstep = (two && MW == 1) ? 2 : 1;
+    const int w0 = (two && MW == 2) ? eg : 0, wstep = (two && MW == 2) ? 2 : 1;
     const float c = g.c, inv_c = 1.0f / g.c;
     int lt = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++lt) {
-      const int acc = lt & 1;
-      const uint32_t aph = static_cast<uint32_t>(lt >> 1) & 1u;
+      const int acc = C::ACC == 2 ? (lt & 1) : 0;
+      const uint32_t aph = C::ACC == 2 ? (static_cast<uint32_t>(lt >> 1) & 1u)
+                                       : (static_cast<uint32_t>(lt) & 1u);
       // the tile and, with fp8, its scales are fetched before the accumulator is ready, so
       // their load latency hides under the tile's MMAs
-      const GTile t = decode_gtile(g, mt, tile);
-      const int r = t.r0 + q * 32 + lane;  // weight row of this thread within the expert
+      const GTile t = decode_gtile<MW>(g, mt, tile);
       constexpr int NCH = C::TOKN / 32;    // token chunks of a tile
       float w_s = 1.0f;
       float x_s[NCH];                      // lane l: scale of token 32 c + l of the tile
 #pragma unroll
-      for (int c = 0; c < NCH; ++c) x_s[c] = 0.0f;
-      if constexpr (FP8) {
-        w_s = __ldg(g.w_scale + static_cast<size_t>(t.e) * mt * BLOCK_M + r);
+      for (int cc = 0; cc < NCH; ++cc) x_s[cc] = 0.0f;
+      if constexpr (FP8) {  // one weight tile (MW == 1)
+        w_s = __ldg(g.w_scale + static_cast<size_t>(t.e) * mt * BLOCK_M + t.r0 + q * 32 + lane);
         int src[NCH];
 #pragma unroll
-        for (int c = 0; c < NCH; ++c) {
-          const int p = t.tok0 + c * 32 + lane;
-          src[c] = (c * 32 + lane < t.ntok) ? (g.gather ? __ldg(g.gather + p) : p) : -1;
+        for (int cc = 0; cc < NCH; ++cc) {
+          const int p = t.tok0 + cc * 32 + lane;
+          src[cc] = (cc * 32 + lane < t.ntok) ? (g.gather ? __ldg(g.gather + p) : p) : -1;
         }
 #pragma unroll
-        for (int c = 0; c < NCH; ++c) x_s[c] = src[c] >= 0 ? __ldg(g.x_scale + src[c]) : 0.0f;
+        for (int cc = 0; cc < NCH; ++cc)
+          x_s[cc] = src[cc] >= 0 ? __ldg(g.x_scale + src[cc]) : 0.0f;
       }
       const bool got = ptx::mbar_wait(&tfull[acc], aph, abort_flag, limit);
       if (!__all_sync(0xffffffffu, got)) {
@@ -370,61 +415,66 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
         break;
       }
       ptx::tc_fence_after();
-      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                             static_cast<uint32_t>(acc * C::ACC_COLS);
-      const bool row_ok = r < g.M_w;  // the last weight tile of an expert may be partial
 #pragma unroll 1
-      for (int ch = eg; ch * 32 < t.npad; ch += egroups) {
-        float v[32];
-        ptx::tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(ch * 32), v);
-        const int nv = min(32, t.ntok - ch * 32);
-        if constexpr (FP8) {
-          float xs = x_s[0];  // this chunk's scales (a register select, no local memory)
+      for (int w = w0; w < t.nw; w += wstep) {
+        const int r0w = t.r0 + w * BLOCK_M;    // first weight row of weight tile w
+        const int r = r0w + q * 32 + lane;     // weight row of this thread within the expert
+        const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                               static_cast<uint32_t>((acc + w) * C::ACC_COLS);
+        const bool row_ok = r < g.M_w;  // the last weight tile of an expert may be partial
+#pragma unroll 1
+        for (int ch = ch0; ch * 32 < t.npad; ch += chstep) {
+          float v[32];
+          ptx::tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(ch * 32), v);
+          const int nv = min(32, t.ntok - ch * 32);
+          if constexpr (FP8) {
+            float xs = x_s[0];  // this chunk's scales (a register select, no local memory)
 #pragma unroll
-          for (int c = 1; c < NCH; ++c) xs = ch == c ? x_s[c] : xs;
+            for (int cc = 1; cc < NCH; ++cc) xs = ch == cc ? x_s[cc] : xs;
 #pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] = v[j] * w_s * __shfl_sync(0xffffffffu, xs, j);
-        }
-        __nv_bfloat16* orow = g.out + static_cast<size_t>(t.tok0 + ch * 32) * g.ldo;
-        // through shared memory: the warp's 32 rows x 32 tokens become, per token, four
-        // 16-byte pieces of its output row, so a store instruction writes 8 tokens' rows
-        // instead of one
-        auto staged_store = [&](__nv_bfloat16* base, int ld) {
-          __nv_bfloat16* st = epi_stage + (warp - 2) * (32 * 32);
-#pragma unroll
-          for (int j = 0; j < 32; ++j) st[j * 32 + lane] = __float2bfloat16_rn(v[j]);
-          __syncwarp();
-          const int piece = lane & 3;
-#pragma unroll
-          for (int j0 = 0; j0 < 32; j0 += 8) {
-            const int j = j0 + (lane >> 2);
-            const uint4 val = *reinterpret_cast<const uint4*>(st + j * 32 + piece * 8);
-            if (j < nv)
-              *reinterpret_cast<uint4*>(base + static_cast<size_t>(t.tok0 + ch * 32 + j) * ld +
-                                        t.r0 + q * 32 + piece * 8) = val;
+            for (int j = 0; j < 32; ++j) v[j] = v[j] * w_s * __shfl_sync(0xffffffffu, xs, j);
           }
-          __syncwarp();
-        };
-        if (g.epi == EPI_SITU) {
-          if (g.pre) staged_store(g.pre, g.ldp);  // the pre-activations, for a backward pass
-          // rows r (gate, lanes 0..15) and r + 16 (value, lanes 16..31) of one 32-row group
-          // hold feature f; lanes 0..15 evaluate it for the even tokens, lanes 16..31 for
-          // the odd ones, so every SiTU evaluation uses the whole warp
-          const int f = ((t.r0 + q * 32) >> 1) + (lane & 15);
-          const bool hi = lane >= 16;
+          __nv_bfloat16* orow = g.out + static_cast<size_t>(t.tok0 + ch * 32) * g.ldo;
+          // through shared memory: the warp's 32 rows x 32 tokens become, per token, four
+          // 16-byte pieces of its output row, so a store instruction writes 8 tokens' rows
+          // instead of one
+          auto staged_store = [&](__nv_bfloat16* base, int ld) {
+            __nv_bfloat16* st = epi_stage + (warp - 2) * (32 * 32);
 #pragma unroll
-          for (int jp = 0; jp < 16; ++jp) {
-            const float x0 = __shfl_xor_sync(0xffffffffu, v[2 * jp], 16);
-            const float x1 = __shfl_xor_sync(0xffffffffu, v[2 * jp + 1], 16);
-            const float gv = hi ? x1 : v[2 * jp];       // gate of token 2jp (+1 on hi lanes)
-            const float vv = hi ? v[2 * jp + 1] : x0;   // value of the same token
-            const int j = 2 * jp + (hi ? 1 : 0);
-            // padding tokens hold finite values (a repeated valid row, or a zero scale)
-            const float hv = FP8 ? situ_close(gv, vv, c, inv_c) : situ_g(gv, vv, c, inv_c);
-            if (j < nv) orow[static_cast<size_t>(j) * g.ldo + f] = __float2bfloat16_rn(hv);
+            for (int j = 0; j < 32; ++j) st[j * 32 + lane] = __float2bfloat16_rn(v[j]);
+            __syncwarp();
+            const int piece = lane & 3;
+#pragma unroll
+            for (int j0 = 0; j0 < 32; j0 += 8) {
+              const int j = j0 + (lane >> 2);
+              const uint4 val = *reinterpret_cast<const uint4*>(st + j * 32 + piece * 8);
+              if (j < nv)
+                *reinterpret_cast<uint4*>(base + static_cast<size_t>(t.tok0 + ch * 32 + j) * ld +
+                                          r0w + q * 32 + piece * 8) = val;
+            }
+            __syncwarp();
+          };
+          if (g.epi == EPI_SITU) {
+            if (g.pre) staged_store(g.pre, g.ldp);  // the pre-activations, for a backward pass
+            // rows r (gate, lanes 0..15) and r + 16 (value, lanes 16..31) of one 32-row group
+            // hold feature f; lanes 0..15 evaluate it for the even tokens, lanes 16..31 for
+            // the odd ones, so every SiTU evaluation uses the whole warp
+            const int f = ((r0w + q * 32) >> 1) + (lane & 15);
+            const bool hi = lane >= 16;
+#pragma unroll
+            for (int jp = 0; jp < 16; ++jp) {
+              const float x0 = __shfl_xor_sync(0xffffffffu, v[2 * jp], 16);
+              const float x1 = __shfl_xor_sync(0xffffffffu, v[2 * jp + 1], 16);
+              const float gv = hi ? x1 : v[2 * jp];       // gate of token 2jp (+1 on hi lanes)
+              const float vv = hi ? v[2 * jp + 1] : x0;   // value of the same token
+              const int j = 2 * jp + (hi ? 1 : 0);
+              // padding tokens hold finite values (a repeated valid row, or a zero scale)
+              const float hv = FP8 ? situ_close(gv, vv, c, inv_c) : situ_g(gv, vv, c, inv_c);
+              if (j < nv) orow[static_cast<size_t>(j) * g.ldo + f] = __float2bfloat16_rn(hv);
+            }
+          } else if (row_ok) {
+            staged_store(g.out, g.ldo);
           }
-        } else if (row_ok) {
-          staged_store(g.out, g.ldo);
         }
       }
       ptx::tc_fence_before();
@@ -440,20 +490,23 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
   }
 }
 
-template <int STAGES_, bool FP8>
+template <int STAGES_, bool FP8, int MW, int TOKN_>
 static int launch_grouped_stages(const CUtensorMap& tw, const CUtensorMap& tx,
                                  const GroupedArgs& g, cudaStream_t stream) {
-  using C = GroupedCfg<STAGES_>;
-  if (cudaFuncSetAttribute(grouped_gemm_kernel<STAGES_, FP8>,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) != cudaSuccess)
+  static_assert(!(FP8 && MW == 2), "e4m3 operands run single weight tiles");
+  using C = GroupedCfg<STAGES_, MW, TOKN_>;
+  auto kernel = grouped_gemm_kernel<STAGES_, FP8, MW, TOKN_>;
+  if (g.tokn > TOKN_) return LMOE_ERR_UNSUPPORTED;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           C::SMEM_BYTES) != cudaSuccess)
     return LMOE_ERR_CUDA;
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return LMOE_ERR_CUDA;
   const int grid = (g.max_ctas > 0 && g.max_ctas < sms) ? g.max_ctas : sms;
-  return launch_pdl(grouped_gemm_kernel<STAGES_, FP8>, grid, GROUPED_THREADS, C::SMEM_BYTES,
-                    stream, tw, tx, g) == cudaSuccess
+  return launch_pdl(kernel, grid, GROUPED_THREADS, C::SMEM_BYTES, stream, tw, tx, g) ==
+                 cudaSuccess
              ? LMOE_OK
              : LMOE_ERR_CUDA;
 }
@@ -464,6 +517,7 @@ int launch_grouped_gemm(const void* W, const void* X, uint64_t x_rows, int x_ld,
   if (g.M_w <= 0 || g.Kd % kgran != 0 || g.Kd <= 0 || x_rows == 0) return LMOE_ERR_UNSUPPORTED;
   if (g.epi != EPI_SITU && g.epi != EPI_BF16) return LMOE_ERR_UNSUPPORTED;
   if (g.epi == EPI_SITU && g.M_w % BLOCK_M != 0) return LMOE_ERR_UNSUPPORTED;
+  if (g.tokn != GROUPED_TOKN && g.tokn != GROUPED_TOKN_WIDE) return LMOE_ERR_INVALID_ARG;
   if (g.fp8 && (!g.w_scale || !g.x_scale || x_ld % 2 != 0)) return LMOE_ERR_INVALID_ARG;
   if (g.pre && (g.epi != EPI_SITU || g.ldp % 8 != 0 || g.ldp < g.M_w ||
                 (reinterpret_cast<uintptr_t>(g.pre) & 15u)))
@@ -489,11 +543,29 @@ int launch_grouped_gemm(const void* W, const void* X, uint64_t x_rows, int x_ld,
   // prefill shape).  The down GEMM at prefill measured no gain (its output write-back shares
   // L2), so it keeps the default policy there.
   ga.evict_first = (g.epi == EPI_SITU || !shallow) ? 1 : 0;
-  if (g.fp8)
-    return shallow ? launch_grouped_stages<GROUPED_STAGES_SHALLOW, true>(tw, tx, ga, stream)
-                   : launch_grouped_stages<GROUPED_STAGES_DEEP, true>(tw, tx, ga, stream);
-  return shallow ? launch_grouped_stages<GROUPED_STAGES_SHALLOW, false>(tw, tx, ga, stream)
-                 : launch_grouped_stages<GROUPED_STAGES_DEEP, false>(tw, tx, ga, stream);
+  const bool wide = g.tokn > GROUPED_TOKN;
+  if (g.fp8) {
+    if (wide) return launch_grouped_stages<GROUPED_STAGES_SHALLOW, true, 1, GROUPED_TOKN_WIDE>(
+                  tw, tx, ga, stream);
+    return shallow ? launch_grouped_stages<GROUPED_STAGES_SHALLOW, true, 1, GROUPED_TOKN>(
+                         tw, tx, ga, stream)
+                   : launch_grouped_stages<GROUPED_STAGES_DEEP, true, 1, GROUPED_TOKN>(
+                         tw, tx, ga, stream);
+  }
+  // Weight-tile pairs when experts see many tokens (the token rows, re-read by every weight
+  // tile of their expert, bound the shared-memory fill there); single tiles at decode.
+  if (g.mean_tokens >= GROUPED_PAIR_MIN_TOKENS) {
+    if (wide) return launch_grouped_stages<GROUPED_STAGES_PAIR, false, 2, GROUPED_TOKN_WIDE>(
+                  tw, tx, ga, stream);
+    return launch_grouped_stages<GROUPED_STAGES_PAIR, false, 2, GROUPED_TOKN>(tw, tx, ga,
+                                                                              stream);
+  }
+  if (wide) return launch_grouped_stages<GROUPED_STAGES_SHALLOW, false, 1, GROUPED_TOKN_WIDE>(
+                tw, tx, ga, stream);
+  return shallow ? launch_grouped_stages<GROUPED_STAGES_SHALLOW, false, 1, GROUPED_TOKN>(
+                       tw, tx, ga, stream)
+                 : launch_grouped_stages<GROUPED_STAGES_DEEP, false, 1, GROUPED_TOKN>(
+                       tw, tx, ga, stream);
 }
 
 }  // namespace lmoe

@@ -94,7 +94,8 @@ struct GroupedArgs {
   int Kd;                 // reduction length (L for gate/value, I for down), multiple of 64
                           // (of 128 with fp8)
   const int32_t* seg_off; // [E+1] first token row of each expert's segment
-  const int32_t* ct_off;  // [E+1] prefix sum of ceil(count / GROUPED_TOKN)
+  const int32_t* ct_off;  // [E+1] prefix sum of ceil(count / tokn)
+  int tokn;               // chunk granularity ct_off was built with (grouped_tokn)
   const int32_t* gather;  // [rows] source row of each permuted row, or null: then the
                           // activation rows are the permuted rows themselves (TMA boxes)
   const __nv_bfloat16* x; // gathered activations [*, ldx] (with gather)
@@ -150,9 +151,10 @@ int launch_candidates(const float* z, int T, int E, int64_t stride_t, int64_t st
 int launch_transpose_f32(const float* in, int T, int E, float* out, cudaStream_t stream);
 // Checked mode: sets DEVERR_NONFINITE in *err if any of p[0, n) is NaN or infinite.
 int launch_finite_check(const float* p, int64_t n, uint32_t* err, cudaStream_t stream);
+// ct_off: prefix sums of ceil(count / tokn) (tokn = grouped_tokn of the batch).
 int launch_dispatch(const int32_t* idx, int T, int E, int K, uint32_t* masks, uint32_t* base,
-                    int32_t* offsets, int32_t* ct_off, int32_t* inv, int32_t* src_tok,
-                    int32_t* counts_out, uint32_t* err, cudaStream_t stream);
+                    int32_t* offsets, int32_t* ct_off, int tokn, int32_t* inv,
+                    int32_t* src_tok, int32_t* counts_out, uint32_t* err, cudaStream_t stream);
 int launch_combine(const __nv_bfloat16* o, const float* gate, const int32_t* inv,
                    const float* gamma, int T, int K, int L, float eps, __nv_bfloat16* z,
                    int ldz, uint32_t* err, unsigned long long timeout_ns, cudaStream_t stream);

@@ -27,7 +27,9 @@ def dev():
                                    (4096, 512, 256),
                                    # tile pairs (two M-tiles per CTA), 256- and 128-wide tiles;
                                    # M ragged, the last pair's second tile wholly past M
-                                   (20000, 3584, 2048), (26000, 384, 2048)])
+                                   (20000, 3584, 2048), (26000, 384, 2048),
+                                   # 224-wide tiles (N = 896 and 672), single and paired
+                                   (8192, 896, 3584), (300, 672, 512), (20000, 896, 2048)])
 def test_gemm_matches_float64(dev, M, N, K):
     g = torch.Generator(device=dev).manual_seed(M * 7 + N * 3 + K)
     A = torch.randn(M, K, generator=g, device=dev).to(torch.bfloat16)

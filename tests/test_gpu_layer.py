@@ -125,6 +125,10 @@ EDGE_SHAPES = [
     ("E1040", synth.LayerShape("e1040", T=300, d=256, L=128, E=1040, K=8, I=64, S=1, Is=64)),
     # a fair-share rank above 256 at T <= 8192: the radix thresholds on scores
     ("k300", synth.LayerShape("k300", T=2400, d=256, L=128, E=64, K=8, I=64, S=1, Is=64)),
+    # weight-tile pairs over an odd number of 128-row weight tiles (2I = L = 384), with ~150
+    # tokens per expert in one chunk, and with ~300 in two equal chunks of the 256 granule
+    ("pairs_odd", synth.LayerShape("po", T=1200, d=256, L=384, E=16, K=2, I=192, S=1, Is=64)),
+    ("wide_odd", synth.LayerShape("wo", T=2400, d=256, L=384, E=16, K=2, I=192, S=1, Is=64)),
 ]
 
 
