@@ -299,9 +299,13 @@ ROUTING = synth.LayerShape("routing", T=8192, d=512, L=256, E=896, K=16, I=64, S
 # the alternative pool the pages weigh against 896 / top-16: 448 experts, 8 per token
 POOL448 = synth.LayerShape("pool448", T=8192, d=7168, L=3584, E=448, K=8, I=512, S=2, Is=2048)
 WGRAD = synth.LayerShape("wgrad", T=584, d=7168, L=3584, E=64, K=16, I=512, S=2, Is=2048)
+# the skewed workload's expert load (~585 tokens per expert, tensor-bound routed GEMMs) on
+# 128 experts: a profiling case of a few GB
+SKEW_SMALL = synth.LayerShape("skew_small", T=4688, d=7168, L=3584, E=128, K=16, I=512, S=2,
+                              Is=2048)
 SHAPES = {"prefill": synth.PREFILL, "decode": synth.DECODE, "e64": synth.E64,
           "skew": synth.SKEW, "small": SMALL, "routing": ROUTING, "pool448": POOL448,
-          "wgrad": WGRAD}
+          "wgrad": WGRAD, "skew_small": SKEW_SMALL}
 DESCRIPTIONS = {
     "prefill": "K3 Stable Latent MoE layer, prefill: in-batch Quantile-Balancing thresholds; "
                "x~N(0,1) with 0.1% of elements x1000; residual = x",
@@ -320,6 +324,9 @@ DESCRIPTIONS = {
     "routing": "K3 routing shape with narrow widths (profiling case for the threshold, "
                "top-K and dispatch kernels at T=8192, E=896, top-16); x~N(0,1); in-batch "
                "thresholds",
+    "skew_small": "K3 widths, 128 experts, T=4688 (profiling case: ~585 tokens per expert as "
+                  "in the skewed workload after balancing, a few GB on the device); x~N(0,1); "
+                  "in-batch thresholds",
     "wgrad": "K3 widths, 64 experts, T=584 (profiling case for the backward's weight-gradient "
              "GEMMs: 146 tokens per expert as in prefill, a few GB on the device); x as in "
              "prefill",

@@ -317,7 +317,9 @@ __device__ __forceinline__ void epilogue_store_partial(const GemmArgs& g, int ro
   }
 }
 
-template <int BN, int MT>
+// RP: the residual epilogue with its residual prefetched one chunk ahead (the output GEMM);
+// a separate instantiation, so that the other epilogues keep their own code.
+template <int BN, int MT, bool RP>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
 gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB, const GemmArgs g) {
@@ -563,10 +565,10 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA,
         const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                static_cast<uint32_t>((acc + h) * BN);
         // Residual epilogue over whole 32-column chunks: chunk ch + 1's residual is loaded
-        // before chunk ch's accumulator columns are read (the condition is warp-uniform; the
-        // tcgen05.ld is executed by every lane, the global accesses by the rows inside M).
-        if (g.epi == EPI_RESID && g.resid != nullptr && g.ksplit <= 1 && g.groups == 0 &&
-            tc.n0 + BN <= g.N) {
+        // before chunk ch's accumulator columns are read (the launcher sets RP only for
+        // this case, so the condition is warp-uniform; the tcgen05.ld is executed by every
+        // lane, the global accesses by the rows inside M).
+        if constexpr (RP) {
           const uint4* rrow = reinterpret_cast<const uint4*>(
               g.resid + static_cast<size_t>(row_ok ? row : 0) * g.ldr + tc.n0);
           uint4 rnext[4];
@@ -771,11 +773,11 @@ bool make_tmap_bf16(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t col
   return r == CUDA_SUCCESS;
 }
 
-template <int BN, int MT>
+template <int BN, int MT, bool RP = false>
 static int launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& g,
                      cudaStream_t stream) {
   using C = GemmCfg<BN, MT>;
-  if (cudaFuncSetAttribute(gemm_tcgen05_kernel<BN, MT>,
+  if (cudaFuncSetAttribute(gemm_tcgen05_kernel<BN, MT, RP>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                            C::SMEM_BYTES) != cudaSuccess)
     return LMOE_ERR_CUDA;
@@ -788,7 +790,7 @@ static int launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArg
                         (g.groups > 0 ? g.groups : 1) * (g.ksplit > 1 ? g.ksplit : 1);
   if (tiles < grid) grid = static_cast<int>(tiles);
   if (grid <= 0) return LMOE_OK;
-  return launch_pdl(gemm_tcgen05_kernel<BN, MT>, grid, GEMM_THREADS, C::SMEM_BYTES, stream, ta, tb,
+  return launch_pdl(gemm_tcgen05_kernel<BN, MT, RP>, grid, GEMM_THREADS, C::SMEM_BYTES, stream, ta, tb,
                     g) ==
                  cudaSuccess
              ? LMOE_OK
@@ -812,8 +814,8 @@ int launch_gemm(const void* A, uint64_t a_rows, int a_ld, const void* B, uint64_
   // tiles instead of 7, re-reading the latent half as often (61.9 -> 59.4 us at prefill)
   // N = 896 (the router over 896 experts): four whole 224-wide tiles instead of four 256-wide
   // ones, the last half empty
-  const int bn = (g.groups == 0 && g.N % 256 != 0 && g.N > 512 && g.N % 224 == 0 &&
-                  g.N <= 4 * 224)
+  const int bn = (g.groups == 0 && g.M > BLOCK_M && g.N % 256 != 0 && g.N > 512 &&
+                  g.N % 224 == 0 && g.N <= 4 * 224)
                      ? 224
                      : ((g.N % 256 == 0 || g.N > 512) ? 256 : 128);
   CUtensorMap ta, tb;
@@ -869,6 +871,9 @@ int launch_gemm(const void* A, uint64_t a_rows, int a_ld, const void* B, uint64_
   // while no MMA runs, which only pays when the MMAs take far longer.
   const bool pairs = g.groups == 0 && g.Kd >= GEMM_PAIR_MIN_K &&
                      ceil_div(g.M, 2 * BLOCK_M) * ceil_div(g.N, bn) >= 2 * static_cast<int64_t>(sms);
+  // the output GEMM: residual epilogue over whole 256-column tiles
+  const bool rp = g.epi == EPI_RESID && g.resid != nullptr && g.N % 256 == 0;
+  if (bn == 256 && pairs && rp) return launch_bn<256, 2, true>(ta, tb, g, stream);
   if (bn == 256)
     return pairs ? launch_bn<256, 2>(ta, tb, g, stream) : launch_bn<256, 1>(ta, tb, g, stream);
   if (bn == 224)

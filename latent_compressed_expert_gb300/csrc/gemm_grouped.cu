@@ -37,7 +37,8 @@ constexpr int GROUPED_BOX_T = 32;  // token rows per TMA box / padding granule o
 constexpr int GROUPED_STAGES_DEEP = 5;
 constexpr int GROUPED_STAGES_SHALLOW = 4;
 constexpr int GROUPED_SHALLOW_MIN_TOKENS = 32;
-// Weight-tile pairs: stages of two weight boxes and a token tile (56 or 64 KB): three fit.
+// Weight-tile pairs: stages of two weight boxes and a token tile (56 or 64 KB): three fit,
+// four (56 KB) without the epilogue's output staging.
 constexpr int GROUPED_STAGES_PAIR = 3;
 constexpr int GROUPED_PAIR_MIN_TOKENS = 64;  // experts' mean token count from which pairs run
 
@@ -49,7 +50,10 @@ constexpr int GROUPED_PAIR_MIN_TOKENS = 64;  // experts' mean token count from w
 // while no MMA runs (the producer keeps loading the next tile meanwhile).
 // TOKN_: the largest token chunk the tile holds (the shared-memory token tile and the TMEM
 // columns of one accumulator); the chunks themselves are set by GroupedArgs::tokn <= TOKN_.
-template <int STAGES_, int MW_, int TOKN_>
+// STAGED: the epilogue's shared-memory staging of output rows (needed by the down GEMM and by
+// a gate/value GEMM that also stores its pre-activations); without it a gate/value ring of
+// weight-tile pairs has room for a fourth stage.
+template <int STAGES_, int MW_, int TOKN_, bool STAGED = true>
 struct GroupedCfg {
   static constexpr int TOKN = TOKN_;                      // max tokens (N) per tile
   static constexpr int MW = MW_;
@@ -63,7 +67,7 @@ struct GroupedCfg {
   static constexpr int ACC_COLS = 256;                    // TMEM columns per accumulator
   static constexpr int TMEM_COLS = 512;
   static constexpr int EPI_OFF = STAGES * STAGE_BYTES;   // per epilogue warp 32 x 32 bf16
-  static constexpr int EPI_BYTES = 8 * 32 * 32 * 2;
+  static constexpr int EPI_BYTES = STAGED ? 8 * 32 * 32 * 2 : 0;
   static constexpr int BAR_OFF = EPI_OFF + EPI_BYTES;
   static constexpr int NUM_BARS = 2 * STAGES + 5;
   static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
@@ -121,7 +125,8 @@ __device__ __forceinline__ GTile decode_gtile(const GroupedArgs& g, int mt, int 
   t.w_row = (e * mt + m) * (g.Kd / BLOCK_K) * BLOCK_M;
   const int seg0 = __ldg(g.seg_off + e);
   const int cnt = __ldg(g.seg_off + e + 1) - seg0;
-  const int csz = (cnt + nchunk - 1) / nchunk;  // <= tokn; every chunk non-empty
+  // <= tokn, and every chunk non-empty; most experts have one chunk (no division)
+  const int csz = nchunk == 1 ? cnt : (cnt + nchunk - 1) / nchunk;
   t.tok0 = seg0 + chunk * csz;
   t.ntok = min(csz, cnt - chunk * csz);
   t.npad = (t.ntok + GROUPED_BOX_T - 1) / GROUPED_BOX_T * GROUPED_BOX_T;
@@ -176,11 +181,11 @@ __device__ __forceinline__ float situ_close(float g, float v, float c, float inv
   return __fdividef(gc, 1.0f + __expf(fminf(-gc, 80.0f))) * vc;
 }
 
-template <int STAGES_, bool FP8, int MW, int TOKN_>
+template <int STAGES_, bool FP8, int MW, int TOKN_, bool STAGED>
 __global__ void __launch_bounds__(GROUPED_THREADS, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
                     const __grid_constant__ CUtensorMap tmX, const GroupedArgs g) {
-  using C = GroupedCfg<STAGES_, MW, TOKN_>;
+  using C = GroupedCfg<STAGES_, MW, TOKN_, STAGED>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = ptx::smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -256,12 +261,19 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
           uint8_t* sa = smem + s * C::STAGE_BYTES;
           uint8_t* sb = sa + C::W_BYTES;
           ptx::mbar_arrive_expect_tx(&full[s], bytes);
-          for (int w = 0; w < t.nw; ++w) {  // an expert's row tiles are nk boxes apart
-            const int wr = t.w_row + (w * nk + kb) * BLOCK_M;
+          if constexpr (MW == 1) {
             if (g.evict_first)
-              ptx::tma_load_2d_hint(sa + w * C::A_BYTES, &tmW, &full[s], 0, wr, w_policy);
+              ptx::tma_load_2d_hint(sa, &tmW, &full[s], 0, t.w_row + kb * BLOCK_M, w_policy);
             else
-              ptx::tma_load_2d(sa + w * C::A_BYTES, &tmW, &full[s], 0, wr);
+              ptx::tma_load_2d(sa, &tmW, &full[s], 0, t.w_row + kb * BLOCK_M);
+          } else {
+            for (int w = 0; w < t.nw; ++w) {  // an expert's row tiles are nk boxes apart
+              const int wr = t.w_row + (w * nk + kb) * BLOCK_M;
+              if (g.evict_first)
+                ptx::tma_load_2d_hint(sa + w * C::A_BYTES, &tmW, &full[s], 0, wr, w_policy);
+              else
+                ptx::tma_load_2d(sa + w * C::A_BYTES, &tmW, &full[s], 0, wr);
+            }
           }
           for (int b = 0; b < nbox; ++b)
             ptx::tma_load_2d(sb + b * C::BOX_T * BLOCK_K * 2, &tmX, &full[s], kb * BLOCK_K,
@@ -313,7 +325,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
           for (int k = 0; k < BLOCK_K / 16; ++k) {  // 32 bytes of K per instruction
 #pragma unroll
             for (int w = 0; w < MW; ++w) {
-              if (w >= t.nw) break;
+              if (MW > 1 && w >= t.nw) break;
               const uint32_t dw = d_tmem + static_cast<uint32_t>(w * C::ACC_COLS);
               const uint32_t aw = sa + w * C::A_BYTES + k * 32;
               if constexpr (FP8)
@@ -416,7 +428,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
       }
       ptx::tc_fence_after();
 #pragma unroll 1
-      for (int w = w0; w < t.nw; w += wstep) {
+      for (int w = w0; w < (MW == 1 ? 1 : t.nw); w += wstep) {
         const int r0w = t.r0 + w * BLOCK_M;    // first weight row of weight tile w
         const int r = r0w + q * 32 + lane;     // weight row of this thread within the expert
         const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
@@ -439,6 +451,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
           // 16-byte pieces of its output row, so a store instruction writes 8 tokens' rows
           // instead of one
           auto staged_store = [&](__nv_bfloat16* base, int ld) {
+            if constexpr (!STAGED) return;  // the launcher pairs these epilogues with staging
             __nv_bfloat16* st = epi_stage + (warp - 2) * (32 * 32);
 #pragma unroll
             for (int j = 0; j < 32; ++j) st[j * 32 + lane] = __float2bfloat16_rn(v[j]);
@@ -490,13 +503,14 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
   }
 }
 
-template <int STAGES_, bool FP8, int MW, int TOKN_>
+template <int STAGES_, bool FP8, int MW, int TOKN_, bool STAGED = true>
 static int launch_grouped_stages(const CUtensorMap& tw, const CUtensorMap& tx,
                                  const GroupedArgs& g, cudaStream_t stream) {
   static_assert(!(FP8 && MW == 2), "e4m3 operands run single weight tiles");
-  using C = GroupedCfg<STAGES_, MW, TOKN_>;
-  auto kernel = grouped_gemm_kernel<STAGES_, FP8, MW, TOKN_>;
+  using C = GroupedCfg<STAGES_, MW, TOKN_, STAGED>;
+  auto kernel = grouped_gemm_kernel<STAGES_, FP8, MW, TOKN_, STAGED>;
   if (g.tokn > TOKN_) return LMOE_ERR_UNSUPPORTED;
+  if (!STAGED && (g.epi != EPI_SITU || g.pre)) return LMOE_ERR_INVALID_ARG;
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            C::SMEM_BYTES) != cudaSuccess)
     return LMOE_ERR_CUDA;
@@ -557,6 +571,9 @@ int launch_grouped_gemm(const void* W, const void* X, uint64_t x_rows, int x_ld,
   if (g.mean_tokens >= GROUPED_PAIR_MIN_TOKENS) {
     if (wide) return launch_grouped_stages<GROUPED_STAGES_PAIR, false, 2, GROUPED_TOKN_WIDE>(
                   tw, tx, ga, stream);
+    if (g.epi == EPI_SITU && !g.pre)  // no output staging: four stages
+      return launch_grouped_stages<GROUPED_STAGES_PAIR + 1, false, 2, GROUPED_TOKN, false>(
+          tw, tx, ga, stream);
     return launch_grouped_stages<GROUPED_STAGES_PAIR, false, 2, GROUPED_TOKN>(tw, tx, ga,
                                                                               stream);
   }
