@@ -611,10 +611,10 @@ def run_ours(args):
     launches_per_step = r["launches"]
     y = r["y"]
 
-    # ---- end to end through the public API with host buffers: every step uploads its x
-    # from pinned host memory and downloads its y; lmoe.HostPipeline overlaps one step's
-    # copies with the neighbouring steps' compute (global thresholds need the collective
-    # between phases, so that mode uses the serial host path)
+    # ---- end to end through the C ABI with host buffers: every step uploads its x from
+    # pinned host memory and downloads its y; lmoe_forward_host (lmoe.HostPipeline) overlaps
+    # one step's copies with the neighbouring steps' compute (global thresholds need the
+    # collective between phases, so that mode uses the serial host path)
     x_host = x.cpu().pin_memory()
     y_host = torch.empty_like(x_host).pin_memory()
     if wl.qb == "global":
@@ -670,7 +670,9 @@ def run_ours(args):
             "clocks": r["clocks"],
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": x.numel() * 2,
                     "d2h_bytes_per_step": y.numel() * 2,
-                    "path": "lmoe.HostPipeline (copies overlapped across steps)"
+                    "path": "lmoe_forward_host (C ABI, pinned host x and y; copies on their "
+                            "own streams through 2 device staging slots, overlapped with the "
+                            "neighbouring steps' compute)"
                             if wl.qb != "global" else "Layer.forward_host (serial)"},
             "gpu_launches": launches_per_step * args.steps}
 

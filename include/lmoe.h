@@ -325,6 +325,42 @@ int lmoe_forward(const lmoe_dims *dims, const void *packed, const void *x,
                  const void *residual, void *y, void *workspace, size_t ws_bytes,
                  lmoe_io *io, void *stream);
 
+/* End-to-end calls from host memory, overlapped across consecutive batches.  The pages have
+ * no counterpart (this is how batches reach the layer, not the layer).  A pipe is a set of
+ * caller-owned resources: `depth` device staging slots (x and y buffers of max_tokens rows),
+ * three streams (upload, compute, download) and per-slot events.  lmoe_forward_host enqueues,
+ * for one batch in slot k = calls % depth: the copy of x_host into slot k's x buffer on the
+ * upload stream (after the forward that last read that buffer), lmoe_forward on the compute
+ * stream (after that copy, and after the download of slot k's previous output), and the copy
+ * of y into y_host on the download stream; then it increments `calls` and returns.  So batch
+ * i + 1's upload and batch i - 1's download run while batch i computes, and the forwards,
+ * which share one workspace, stay in order on the compute stream.
+ *   x_host, y_host: HOST memory [T, d] bf16 (page-locked, or the copies are not
+ *     asynchronous); they must stay valid until the download stream has passed this batch
+ *     (synchronise it before reading y_host).
+ *   residual_is_x: 1 = the layer's residual is x itself (the FFN's residual connection).
+ *   workspace, ws_bytes, io: as lmoe_forward (io->stage_events are recorded on the compute
+ *     stream).  Calls on one pipe must come from one host thread, in order.
+ * Errors: INVALID_ARG (null pointers, depth outside 1..LMOE_HOST_PIPE_MAX_DEPTH, T above
+ * max_tokens, misaligned buffers), and lmoe_forward's; nothing is enqueued when an argument
+ * is rejected. */
+#define LMOE_HOST_PIPE_MAX_DEPTH 4
+typedef struct lmoe_host_pipe {
+  int depth;        /* staging slots in use, 1..LMOE_HOST_PIPE_MAX_DEPTH */
+  int max_tokens;   /* rows each staging buffer holds */
+  void *x_dev[LMOE_HOST_PIPE_MAX_DEPTH];      /* [max_tokens, d] bf16 device buffers */
+  void *y_dev[LMOE_HOST_PIPE_MAX_DEPTH];      /* [max_tokens, d] bf16 device buffers */
+  void *upload, *compute, *download;          /* cudaStream_t, three distinct streams */
+  void *uploaded[LMOE_HOST_PIPE_MAX_DEPTH];   /* cudaEvent_t per slot */
+  void *computed[LMOE_HOST_PIPE_MAX_DEPTH];
+  void *downloaded[LMOE_HOST_PIPE_MAX_DEPTH];
+  unsigned long long calls;  /* batches enqueued on this pipe (start at 0; incremented) */
+} lmoe_host_pipe;
+
+int lmoe_forward_host(const lmoe_dims *dims, const void *packed, const void *x_host,
+                      int residual_is_x, void *y_host, void *workspace, size_t ws_bytes,
+                      lmoe_io *io, lmoe_host_pipe *pipe);
+
 /* Building block of lmoe_forward, exposed for verification: C = A . B^T on the tensor
  * cores (tcgen05, fp32 accumulation in TMEM), with A [M, Kd] and B [N, Kd] bf16 row-major
  * (K-major) and C [M, N] fp32.  Requires Kd % 64 == 0, N % 16 == 0, 16-byte aligned

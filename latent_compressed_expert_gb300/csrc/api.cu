@@ -821,6 +821,42 @@ int lmoe_last_device_error(void* workspace) {
   return LMOE_ERR_DEVICE_TIMEOUT;
 }
 
+}  // extern "C"
+
+// The argument checks of lmoe_forward for a batch of T > 0 tokens (LMOE_OK or the status
+// lmoe_forward returns before it enqueues anything).
+int lmoe::forward_args_check(const lmoe_dims* dims, const void* packed, const void* x,
+                             const void* residual, const void* y, const void* workspace,
+                             size_t ws_bytes, const lmoe_io* io) {
+  int rc = dims_supported(dims);
+  if (rc != LMOE_OK) return rc;
+  const lmoe_dims D = *dims;
+  lmoe_io opt{};
+  opt.balance = 1;
+  if (io) opt = *io;
+  if (opt.phase < LMOE_PHASE_ALL || opt.phase > LMOE_PHASE_EXPERTS) return LMOE_ERR_INVALID_ARG;
+  const bool front = opt.phase != LMOE_PHASE_EXPERTS;
+  const bool back = opt.phase != LMOE_PHASE_ROUTER;
+  if (opt.cand_out && (opt.phase != LMOE_PHASE_ROUTER || opt.cand_k < 1))
+    return LMOE_ERR_INVALID_ARG;
+  if (!packed || !workspace || (front && !x) || (back && !y)) return LMOE_ERR_INVALID_ARG;
+  if (!aligned16(packed) || !aligned16(workspace) || (front && !aligned16(x)) ||
+      (back && !aligned16(y)) || (residual && !aligned16(residual)))
+    return LMOE_ERR_INVALID_ARG;
+  if (back && ((x && y == x) || (residual && y == residual))) return LMOE_ERR_INVALID_ARG;
+  if (ws_bytes < workspace_layout(D).total_base) return LMOE_ERR_WORKSPACE_TOO_SMALL;
+  if ((opt.tau_in && !aligned16(opt.tau_in)) || (opt.logits_in && !aligned16(opt.logits_in)))
+    return LMOE_ERR_INVALID_ARG;
+  if (opt.tau_ema && !(opt.ema_beta >= 0.0f && opt.ema_beta <= 1.0f)) return LMOE_ERR_INVALID_ARG;
+  if (opt.save_pre && (D.expert_fp8 || !aligned16(opt.save_pre))) return LMOE_ERR_INVALID_ARG;
+  if (opt.save_pre_shared && !aligned16(opt.save_pre_shared)) return LMOE_ERR_INVALID_ARG;
+  if (opt.y_f32_out && !aligned16(opt.y_f32_out)) return LMOE_ERR_INVALID_ARG;
+  if (opt.logit_bias && !aligned16(opt.logit_bias)) return LMOE_ERR_INVALID_ARG;
+  return LMOE_OK;
+}
+
+extern "C" {
+
 int lmoe_forward(const lmoe_dims* dims, const void* packed, const void* x, const void* residual,
                  void* y, void* workspace, size_t ws_bytes, lmoe_io* io, void* stream_) {
   if (io) io->kernel_launches = 0;
@@ -842,25 +878,14 @@ int lmoe_forward(const lmoe_dims* dims, const void* packed, const void* x, const
                                static_cast<cudaStream_t>(stream_));
     return LMOE_OK;
   }
-  if (!packed || !workspace || (front && !x) || (back && !y)) return LMOE_ERR_INVALID_ARG;
-  if (!aligned16(packed) || !aligned16(workspace) || (front && !aligned16(x)) ||
-      (back && !aligned16(y)) || (residual && !aligned16(residual)))
-    return LMOE_ERR_INVALID_ARG;
-  if (back && ((x && y == x) || (residual && y == residual))) return LMOE_ERR_INVALID_ARG;
+  rc = forward_args_check(dims, packed, x, residual, y, workspace, ws_bytes, io);
+  if (rc != LMOE_OK) return rc;
   const WorkspaceLayout W = workspace_layout(D);
-  if (ws_bytes < W.total_base) return LMOE_ERR_WORKSPACE_TOO_SMALL;
   // Small whole-layer calls split the dense GEMMs' reductions when the workspace holds the
   // partials.  The two phases never do: a batch split across ranks then routes on logits
   // bit-identical to the whole batch's, whatever each part's size.
   const bool splitk =
       W.total > W.total_base && ws_bytes >= W.total && opt.phase == LMOE_PHASE_ALL;
-  if ((opt.tau_in && !aligned16(opt.tau_in)) || (opt.logits_in && !aligned16(opt.logits_in)))
-    return LMOE_ERR_INVALID_ARG;
-  if (opt.tau_ema && !(opt.ema_beta >= 0.0f && opt.ema_beta <= 1.0f)) return LMOE_ERR_INVALID_ARG;
-  if (opt.save_pre && (D.expert_fp8 || !aligned16(opt.save_pre))) return LMOE_ERR_INVALID_ARG;
-  if (opt.save_pre_shared && !aligned16(opt.save_pre_shared)) return LMOE_ERR_INVALID_ARG;
-  if (opt.y_f32_out && !aligned16(opt.y_f32_out)) return LMOE_ERR_INVALID_ARG;
-  if (opt.logit_bias && !aligned16(opt.logit_bias)) return LMOE_ERR_INVALID_ARG;
 
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   using bf = __nv_bfloat16;

@@ -26,6 +26,10 @@ struct WorkspaceLayout {
 
 PackedLayout packed_layout(const lmoe_dims& D);
 WorkspaceLayout workspace_layout(const lmoe_dims& D);
+// lmoe_forward's argument checks for T > 0 (LMOE_OK, or the status it would return).
+int forward_args_check(const lmoe_dims* dims, const void* packed, const void* x,
+                       const void* residual, const void* y, const void* workspace,
+                       size_t ws_bytes, const lmoe_io* io);
 
 // Epilogues of the tcgen05 GEMM.
 enum EpiMode : int {

@@ -48,6 +48,15 @@ class IO(ctypes.Structure):
 
 
 OVERLAP_MIN_T = 512  # LMOE_OVERLAP_MIN_T
+HOST_PIPE_MAX_DEPTH = 4  # LMOE_HOST_PIPE_MAX_DEPTH
+
+
+class HostPipe(ctypes.Structure):
+    _fields_ = [("depth", _i), ("max_tokens", _i), ("x_dev", _vp * HOST_PIPE_MAX_DEPTH),
+                ("y_dev", _vp * HOST_PIPE_MAX_DEPTH), ("upload", _vp), ("compute", _vp),
+                ("download", _vp), ("uploaded", _vp * HOST_PIPE_MAX_DEPTH),
+                ("computed", _vp * HOST_PIPE_MAX_DEPTH),
+                ("downloaded", _vp * HOST_PIPE_MAX_DEPTH), ("calls", ctypes.c_ulonglong)]
 
 # enum lmoe_phase
 PHASE_ALL, PHASE_ROUTER, PHASE_EXPERTS = 0, 1, 2
@@ -88,6 +97,8 @@ SIGNATURES = {
     "lmoe_gemm_bf16": (_i, [_vp, _vp, _vp, _i, _i, _i, _vp, _vp]),
     "lmoe_forward_noalloc": (_i, [ctypes.POINTER(Dims), _vp, _vp, _vp, _vp, ctypes.POINTER(IO),
                                   _vp]),
+    "lmoe_forward_host": (_i, [ctypes.POINTER(Dims), _vp, _vp, _i, _vp, _vp, _sz,
+                               ctypes.POINTER(IO), ctypes.POINTER(HostPipe)]),
     "lmoe_noalloc_last_device_error": (_i, []),
     "lmoe_last_device_error": (_i, [_vp]),
     "lmoe_error_string": (ctypes.c_char_p, [_i]),
@@ -669,17 +680,16 @@ class Layer:
 
 
 class HostPipeline:
-    """The layer on batches that live in pinned host memory, overlapped across batches.
-
-    Each ``submit`` copies x to the device on an upload stream, runs the layer on the
-    compute stream, and copies y back on a download stream, all asynchronous; with ``depth``
-    device buffer pairs, batch i+1's upload and batch i-1's download run while batch i
-    computes.  Events order every reuse: an x buffer is overwritten only after the forward
-    that read it, a y buffer only after its download.  The forward calls themselves stay in
-    order on one stream, so the layer's workspace is shared safely.  ``synchronize`` waits
-    for every submitted batch."""
+    """The layer on batches that live in pinned host memory, overlapped across batches: each
+    ``submit`` is one lmoe_forward_host call (the upload of x, the layer and the download of
+    y on three streams, through one of ``depth`` device staging slots), so batch i + 1's
+    upload and batch i - 1's download run while batch i computes.  The library orders every
+    reuse of a slot with the pipe's events; this class owns the slots, streams and events.
+    ``synchronize`` waits for every submitted batch."""
 
     def __init__(self, layer: "Layer", depth: int = 2):
+        if not 1 <= depth <= HOST_PIPE_MAX_DEPTH:
+            raise ValueError(f"lmoe: pipeline depth must be 1..{HOST_PIPE_MAX_DEPTH}")
         self.layer = layer
         self.depth = depth
         T, d = layer.max_tokens, layer.shape.d
@@ -689,35 +699,54 @@ class HostPipeline:
         self.up = torch.cuda.Stream(device=dev)
         self.compute = torch.cuda.Stream(device=dev)
         self.down = torch.cuda.Stream(device=dev)
-        self.uploaded = [torch.cuda.Event() for _ in range(depth)]
-        self.computed = [torch.cuda.Event() for _ in range(depth)]
-        self.downloaded = [torch.cuda.Event() for _ in range(depth)]
-        self.used = [False] * depth
-        self.n = 0
+        self.events = [[torch.cuda.Event() for _ in range(3)] for _ in range(depth)]
+        for evs in self.events:  # torch creates its events lazily: record each once
+            for ev in evs:
+                ev.record(self.compute)
+        self.compute.synchronize()
+        p = HostPipe()
+        p.depth, p.max_tokens = depth, T
+        for k in range(depth):
+            p.x_dev[k] = self.x[k].data_ptr()
+            p.y_dev[k] = self.y[k].data_ptr()
+            p.uploaded[k] = self.events[k][0].cuda_event
+            p.computed[k] = self.events[k][1].cuda_event
+            p.downloaded[k] = self.events[k][2].cuda_event
+        p.upload = self.up.cuda_stream
+        p.compute = self.compute.cuda_stream
+        p.download = self.down.cuda_stream
+        p.calls = 0
+        self.pipe = p
 
     def submit(self, x_host: torch.Tensor, y_host: torch.Tensor, residual_from_x: bool = True,
-               **kw):
-        """Enqueue one batch: x_host [T, d] bf16 pinned in, y_host pinned out.  Extra keyword
-        arguments go to ``Layer.forward``."""
-        k = self.n % self.depth
+               tau: torch.Tensor | None = None, balance: bool = True,
+               logit_bias: torch.Tensor | None = None):
+        """Enqueue one batch: x_host [T, d] bf16 pinned in, y_host pinned out."""
+        layer, sh = self.layer, self.layer.shape
         T = x_host.shape[0]
-        xd, yd = self.x[k][:T], self.y[k][:T]
-        if self.used[k]:
-            self.up.wait_event(self.computed[k])        # the forward that read x[k] is done
-            self.compute.wait_event(self.downloaded[k])  # y[k] has been read back
-        with torch.cuda.stream(self.up):
-            xd.copy_(x_host, non_blocking=True)
-            self.uploaded[k].record(self.up)
-        self.compute.wait_event(self.uploaded[k])
-        self.layer.forward(xd, residual=xd if residual_from_x else None, y=yd,
-                           stream=self.compute, **kw)
-        self.computed[k].record(self.compute)
-        self.down.wait_event(self.computed[k])
-        with torch.cuda.stream(self.down):
-            y_host.copy_(yd, non_blocking=True)
-            self.downloaded[k].record(self.down)
-        self.used[k] = True
-        self.n += 1
+        if T > layer.max_tokens:
+            raise ValueError(f"lmoe: {T} tokens exceed the pipeline's {layer.max_tokens}")
+        _expect(x_host, torch.bfloat16, (T, sh.d), "x_host")
+        _expect(y_host, torch.bfloat16, (T, sh.d), "y_host")
+        if x_host.is_cuda or y_host.is_cuda or not x_host.is_contiguous() or \
+                not y_host.is_contiguous():
+            raise ValueError("lmoe: x_host and y_host must be contiguous host tensors")
+        io = IO()
+        io.balance = 1 if balance else 0
+        if tau is not None:
+            _expect(tau, torch.float32, (sh.E,), "tau")
+            io.tau_in = _ptr(tau)
+        if logit_bias is not None:
+            _expect(logit_bias, torch.float32, (sh.E,), "logit_bias")
+            io.logit_bias = _ptr(logit_bias)
+        dims = dims_of(sh, T=T, expert_fp8=layer.expert_fp8)
+        _check(load().lmoe_forward_host(ctypes.byref(dims), _ptr(layer.packed),
+                                        ctypes.c_void_p(x_host.data_ptr()),
+                                        1 if residual_from_x else 0,
+                                        ctypes.c_void_p(y_host.data_ptr()),
+                                        _ptr(layer.workspace), layer.ws_bytes, ctypes.byref(io),
+                                        ctypes.byref(self.pipe)), "lmoe_forward_host")
+        layer.last_kernel_launches = io.kernel_launches
 
     def synchronize(self):
         for s in (self.up, self.compute, self.down):

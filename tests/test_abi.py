@@ -272,7 +272,7 @@ def _c_layout(struct, fields, tmp_path):
 
 
 @pytest.mark.parametrize("struct,cls", [("lmoe_dims", lmoe.Dims), ("lmoe_weights", lmoe.Weights),
-                                        ("lmoe_io", lmoe.IO)])
+                                        ("lmoe_io", lmoe.IO), ("lmoe_host_pipe", lmoe.HostPipe)])
 def test_binding_structs_match_the_header(struct, cls, tmp_path):
     """The ctypes mirrors of the header's structs have the same size and field offsets, so
     every option reaches the library in its own field."""
@@ -310,3 +310,39 @@ def test_fair_share_rank_matches_the_oracle(lib, oracle_mod):
     assert lib.lmoe_fair_share_rank(-1, 16, 896) == -1
     assert lib.lmoe_fair_share_rank(100, 0, 896) == -1
     assert lib.lmoe_fair_share_rank(100, 16, 0) == -1
+
+
+@no_gpu
+def test_forward_host_argument_checks(lib):
+    """lmoe_forward_host rejects a bad pipe or batch before it enqueues anything."""
+    d = lmoe.dims_of(synth.TINY)
+    fake = ctypes.c_void_p(1 << 20)
+    ws = lmoe.workspace_bytes(d)
+
+    def pipe(depth=2, max_tokens=synth.TINY.T):
+        p = lmoe.HostPipe()
+        p.depth, p.max_tokens = depth, max_tokens
+        for k in range(lmoe.HOST_PIPE_MAX_DEPTH):
+            p.x_dev[k] = (1 << 20) + (k << 16)
+            p.y_dev[k] = (1 << 24) + (k << 16)
+            p.uploaded[k] = p.computed[k] = p.downloaded[k] = 4096 + k
+        p.upload, p.compute, p.download = 8, 16, 24
+        return p
+
+    def call(p, x=fake, y=fake, dims=d):
+        return lib.lmoe_forward_host(ctypes.byref(dims), fake, x, 1, y, fake, ws, None,
+                                     ctypes.byref(p))
+
+    assert call(pipe(depth=0)) == lmoe.LMOE_ERR_INVALID_ARG
+    assert call(pipe(depth=lmoe.HOST_PIPE_MAX_DEPTH + 1)) == lmoe.LMOE_ERR_INVALID_ARG
+    assert call(pipe(max_tokens=synth.TINY.T - 1)) == lmoe.LMOE_ERR_INVALID_ARG
+    assert call(pipe(), x=None) == lmoe.LMOE_ERR_INVALID_ARG
+    assert call(pipe(), y=None) == lmoe.LMOE_ERR_INVALID_ARG
+    bad = lmoe.dims_of(synth.TINY)
+    bad.d = 100
+    assert call(pipe(), dims=bad) == lmoe.LMOE_ERR_UNSUPPORTED
+    p = pipe()
+    p.calls = 5
+    assert lib.lmoe_forward_host(ctypes.byref(d), fake, fake, 1, fake, fake, 16, None,
+                                 ctypes.byref(p)) == lmoe.LMOE_ERR_WORKSPACE_TOO_SMALL
+    assert p.calls == 5  # nothing was enqueued

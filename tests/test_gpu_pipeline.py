@@ -1,6 +1,7 @@
-"""The pipelined host path (lmoe.HostPipeline): batches in pinned host memory, copies on
-their own streams overlapped with the neighbouring batches' compute.  Every batch's output
-must equal the plain device call's, bit for bit, whatever the overlap."""
+"""The pipelined host path (lmoe_forward_host through lmoe.HostPipeline): batches in pinned
+host memory, copies on their own streams overlapped with the neighbouring batches' compute.
+Every batch's output must equal the plain device call's, bit for bit, whatever the overlap
+and whatever the batch sizes."""
 import pytest
 import torch
 
@@ -20,12 +21,12 @@ def dev():
     return torch.device("cuda:0")
 
 
-@pytest.mark.parametrize("depth", [1, 2, 3])
+@pytest.mark.parametrize("depth", [1, 2, 3, 4])
 def test_pipelined_batches_equal_plain_calls(dev, depth):
     sh = H.mid_shape()
     w = {k: v.to(dev) for k, v in synth.make_weights(sh, seed=61).items()}
     layer = lmoe.Layer(sh, w)
-    xs = [synth.make_x(sh, seed=61 + i) for i in range(5)]
+    xs = [synth.make_x(sh, seed=61 + i, T=(357 if i == 3 else sh.T)) for i in range(6)]
     ref = []
     for x in xs:
         xd = x.to(dev)
