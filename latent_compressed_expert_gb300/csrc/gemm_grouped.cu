@@ -405,12 +405,18 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
       // their load latency hides under the tile's MMAs
       const GTile t = decode_gtile<MW>(g, mt, tile);
       constexpr int NCH = C::TOKN / 32;    // token chunks of a tile
-      float w_s = 1.0f;
+      float w_s[MW];                       // this thread's weight row scale, per weight tile
       float x_s[NCH];                      // lane l: scale of token 32 c + l of the tile
 #pragma unroll
+      for (int w = 0; w < MW; ++w) w_s[w] = 1.0f;
+#pragma unroll
       for (int cc = 0; cc < NCH; ++cc) x_s[cc] = 0.0f;
-      if constexpr (FP8) {  // one weight tile (MW == 1)
-        w_s = __ldg(g.w_scale + static_cast<size_t>(t.e) * mt * BLOCK_M + t.r0 + q * 32 + lane);
+      if constexpr (FP8) {
+#pragma unroll
+        for (int w = 0; w < MW; ++w)  // rows past the expert's last tile: a finite dummy
+          w_s[w] = w < t.nw ? __ldg(g.w_scale + static_cast<size_t>(t.e) * mt * BLOCK_M + t.r0 +
+                                    w * BLOCK_M + q * 32 + lane)
+                            : 0.0f;
         int src[NCH];
 #pragma unroll
         for (int cc = 0; cc < NCH; ++cc) {
@@ -443,8 +449,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
             float xs = x_s[0];  // this chunk's scales (a register select, no local memory)
 #pragma unroll
             for (int cc = 1; cc < NCH; ++cc) xs = ch == cc ? x_s[cc] : xs;
+            float ws = w_s[0];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = v[j] * w_s * __shfl_sync(0xffffffffu, xs, j);
+            for (int ww = 1; ww < MW; ++ww) ws = w == ww ? w_s[ww] : ws;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = v[j] * ws * __shfl_sync(0xffffffffu, xs, j);
           }
           __nv_bfloat16* orow = g.out + static_cast<size_t>(t.tok0 + ch * 32) * g.ldo;
           // through shared memory: the warp's 32 rows x 32 tokens become, per token, four
@@ -506,7 +515,6 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
 template <int STAGES_, bool FP8, int MW, int TOKN_, bool STAGED = true>
 static int launch_grouped_stages(const CUtensorMap& tw, const CUtensorMap& tx,
                                  const GroupedArgs& g, cudaStream_t stream) {
-  static_assert(!(FP8 && MW == 2), "e4m3 operands run single weight tiles");
   using C = GroupedCfg<STAGES_, MW, TOKN_, STAGED>;
   auto kernel = grouped_gemm_kernel<STAGES_, FP8, MW, TOKN_, STAGED>;
   if (g.tokn > TOKN_) return LMOE_ERR_UNSUPPORTED;
@@ -558,7 +566,18 @@ int launch_grouped_gemm(const void* W, const void* X, uint64_t x_rows, int x_ld,
   // L2), so it keeps the default policy there.
   ga.evict_first = (g.epi == EPI_SITU || !shallow) ? 1 : 0;
   const bool wide = g.tokn > GROUPED_TOKN;
+  const bool pairs = g.mean_tokens >= GROUPED_PAIR_MIN_TOKENS;
   if (g.fp8) {
+    // e4m3 operands: pairs for the down GEMM only.  The gate/value GEMM's mainloop is half as
+    // long as the bf16 one while its SiTU epilogue (the accurate tanh) is heavier, so the pair's
+    // undivided accumulator, drained while no MMA runs, cost more than the token bytes saved
+    // (prefill 0.634 -> 0.681 ms, skew 2.09 -> 2.74 ms; down 0.586 -> 0.564, 2.34 -> 1.91).
+    if (pairs && g.epi != EPI_SITU) {
+      if (wide) return launch_grouped_stages<GROUPED_STAGES_PAIR, true, 2, GROUPED_TOKN_WIDE>(
+                    tw, tx, ga, stream);
+      return launch_grouped_stages<GROUPED_STAGES_PAIR, true, 2, GROUPED_TOKN>(tw, tx, ga,
+                                                                               stream);
+    }
     if (wide) return launch_grouped_stages<GROUPED_STAGES_SHALLOW, true, 1, GROUPED_TOKN_WIDE>(
                   tw, tx, ga, stream);
     return shallow ? launch_grouped_stages<GROUPED_STAGES_SHALLOW, true, 1, GROUPED_TOKN>(
@@ -568,7 +587,7 @@ int launch_grouped_gemm(const void* W, const void* X, uint64_t x_rows, int x_ld,
   }
   // Weight-tile pairs when experts see many tokens (the token rows, re-read by every weight
   // tile of their expert, bound the shared-memory fill there); single tiles at decode.
-  if (g.mean_tokens >= GROUPED_PAIR_MIN_TOKENS) {
+  if (pairs) {
     if (wide) return launch_grouped_stages<GROUPED_STAGES_PAIR, false, 2, GROUPED_TOKN_WIDE>(
                   tw, tx, ga, stream);
     if (g.epi == EPI_SITU && !g.pre)  // no output staging: four stages
