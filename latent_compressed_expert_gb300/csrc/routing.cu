@@ -603,6 +603,59 @@ thresholds_bound_kernel(const float* __restrict__ z, int T, int64_t stride_t, in
   if (threadIdx.x == 0) tau[e] = __uint_as_float(result);
 }
 
+// Quantile-Balancing thresholds for columns of at most THR_THREADS * THR_KPT = 32768 tokens and
+// any rank k (the bound form above needs k <= 256 and T <= 8192): one CTA of 1024 threads per
+// expert, thread i holding the scores of tokens i, i + 1024, ... in registers.  A bit-by-bit
+// search finds the largest v with #{scores >= v} >= k -- the k-th largest score -- each count
+// a block-wide sum: the threads' own counts, a warp reduction, then one warp over the 32 warp
+// sums (double-buffered, two barriers per bit).  Score bits are non-negative and below 2^30;
+// past T a key is 0, which no search value reaches.
+constexpr int THR_THREADS = 1024;
+constexpr int THR_KPT = 32;
+
+template <bool SCORES>
+__global__ void __launch_bounds__(THR_THREADS, 1)
+thresholds_regs_kernel(const float* __restrict__ z, int T, int64_t stride_t, int64_t stride_e,
+                       int k, float* __restrict__ tau) {
+  __shared__ uint32_t wsum[2][THR_THREADS / 32];
+  __shared__ uint32_t total[2];
+  pdl_wait();
+  pdl_launch_dependents();
+  const int e = blockIdx.x;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const float* col = z + static_cast<int64_t>(e) * stride_e;
+  uint32_t key[THR_KPT];
+#pragma unroll
+  for (int i = 0; i < THR_KPT; ++i) {  // every load in flight before any score is computed
+    const int t = static_cast<int>(threadIdx.x) + i * THR_THREADS;
+    key[i] = t < T ? __float_as_uint(__ldg(col + t * stride_t)) : 0u;
+  }
+#pragma unroll
+  for (int i = 0; i < THR_KPT; ++i) {
+    const int t = static_cast<int>(threadIdx.x) + i * THR_THREADS;
+    key[i] = t < T ? __float_as_uint(score_of<SCORES>(__uint_as_float(key[i]))) : 0u;
+  }
+  uint32_t result = 0u;
+#pragma unroll 1
+  for (int b = 29; b >= 0; --b) {
+    const uint32_t v = result | (1u << b);
+    uint32_t c = 0u;
+#pragma unroll
+    for (int i = 0; i < THR_KPT; ++i) c += key[i] >= v ? 1u : 0u;
+    c = __reduce_add_sync(0xffffffffu, c);
+    const int par = b & 1;
+    if (lane == 0) wsum[par][warp] = c;
+    __syncthreads();
+    if (warp == 0) {
+      const uint32_t sum = __reduce_add_sync(0xffffffffu, wsum[par][lane]);
+      if (lane == 0) total[par] = sum;
+    }
+    __syncthreads();
+    if (total[par] >= static_cast<uint32_t>(k)) result = v;
+  }
+  if (threadIdx.x == 0) tau[e] = __uint_as_float(result);
+}
+
 // Threshold candidates of one batch: column e of cand ([k, E], row stride ldc) receives the
 // logits of the min(k, T) tokens with the largest scores of expert e -- first those whose
 // score is above the min(k, T)-th largest, then tokens whose score equals it, both in token
@@ -772,6 +825,14 @@ int launch_thresholds(const float* z, int T, int E, int64_t stride_t, int64_t st
                              static_cast<int>(smem)) != cudaSuccess)
       return LMOE_ERR_CUDA;
     return launch_pdl(kern, E, TH_THREADS, smem, stream, z, T, stride_t, stride_e, k, tau) ==
+                   cudaSuccess
+               ? LMOE_OK
+               : LMOE_ERR_CUDA;
+  }
+  if (T <= THR_THREADS * THR_KPT) {
+    // register-resident bit search: any k, up to 32768 tokens
+    auto kern = scores ? thresholds_regs_kernel<true> : thresholds_regs_kernel<false>;
+    return launch_pdl(kern, E, THR_THREADS, 0, stream, z, T, stride_t, stride_e, k, tau) ==
                    cudaSuccess
                ? LMOE_OK
                : LMOE_ERR_CUDA;

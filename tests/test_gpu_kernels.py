@@ -93,7 +93,9 @@ def test_scores_sweep_bit_exact(dev, oracle_mod):
 
 THRESH_CASES = [(64, 16, 4, 0), (8192, 896, 16, 0), (32768, 896, 16, 0), (40000, 64, 4, 0),
                 (100, 32, 4, 1), (100, 32, 4, 100), (7, 16, 16, 0), (1, 896, 16, 0),
-                (3000, 448, 8, 0), (5000, 64, 4, 256), (5000, 64, 4, 257), (8193, 896, 16, 0)]
+                (3000, 448, 8, 0), (5000, 64, 4, 256), (5000, 64, 4, 257), (8193, 896, 16, 0),
+                # the register-resident bit search (T <= 32768, any rank): the extremes of k
+                (32768, 16, 16, 32768), (12345, 48, 8, 1), (20000, 32, 4, 4096)]
 
 
 @pytest.mark.parametrize("T,E,K,k_rank", THRESH_CASES)
