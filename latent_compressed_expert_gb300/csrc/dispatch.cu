@@ -257,53 +257,14 @@ combine_rmsnorm_kernel(const __nv_bfloat16* __restrict__ o, const float* __restr
   }
 }
 
-// Combine + RMSNorm with the token's K expert rows staged in shared memory by 1-D bulk
-// copies: one thread issues the K copies on one mbarrier, so a CTA has all K rows in
-// flight at once (K * L * 2 bytes; two CTAs per SM when that is at most COMBINE_BULK_MAX).
-// Then each thread sums its 8-feature vectors over the slots in slot order, the sum of
-// squares is reduced in the same fixed tree as above, and z is written.  The wait on the
-// copies is bounded; on time-out the CTA records the error bit and writes nothing.
-constexpr int COMBINE_BULK_MAX = 114688;  // bytes of staged rows per CTA (16 x 3584 bf16)
-__global__ void __launch_bounds__(COMBINE_MAX_THREADS)
-combine_bulk_kernel(const __nv_bfloat16* __restrict__ o, const float* __restrict__ gate,
-                    const int32_t* __restrict__ inv, const float* __restrict__ gamma, int T,
-                    int K, int L, float eps, __nv_bfloat16* __restrict__ z, int ldz,
-                    uint32_t* __restrict__ err, unsigned long long timeout_ns) {
-  extern __shared__ __align__(128) uint8_t cb_smem[];
-  __shared__ float gates[32];
-  __shared__ float warp_ss[32];
-  __shared__ __align__(8) uint64_t bar;
-  const int t = blockIdx.x;
-  const uint32_t row_bytes = static_cast<uint32_t>(L) * 2;
-  if (threadIdx.x == 0) {
-    ptx::mbar_init(&bar, 1);
-    ptx::fence_mbar_init();
-  }
-  __syncthreads();
-  pdl_wait();
-  pdl_launch_dependents();
-  if (threadIdx.x == 0) {
-    ptx::mbar_arrive_expect_tx(&bar, row_bytes * static_cast<uint32_t>(K));
-    for (int j = 0; j < K; ++j) {
-      const int row = __ldg(inv + static_cast<size_t>(t) * K + j);
-      ptx::bulk_load(cb_smem + static_cast<size_t>(j) * row_bytes,
-                     o + static_cast<size_t>(row) * L, row_bytes, &bar);
-    }
-  }
-  if (threadIdx.x < K) gates[threadIdx.x] = __ldg(gate + static_cast<size_t>(t) * K + threadIdx.x);
-  __shared__ int abort_flag;
-  if (threadIdx.x == 0) abort_flag = 0;
-  __syncthreads();
-  // every thread waits on the copies; the wait is bounded
-  const bool ok = ptx::mbar_wait(&bar, 0u, &abort_flag, timeout_ns);
-  if (!__syncthreads_and(ok ? 1 : 0)) {
-    if (threadIdx.x == 0) atomicOr(err, DEVERR_TIMEOUT_EPILOGUE);
-    // copies still in flight must land before the CTA exits (bounded again)
-    ptx::mbar_wait(&bar, 0u, &abort_flag, timeout_ns);
-    return;
-  }
+// z = gamma * u / sqrt(mean(u^2) + eps), u = sum_j gate_j rows[j] in slot order (fp32), from
+// a token's K expert rows staged in shared memory: thread i sums its 8-feature vectors i,
+// i + blockDim.x, ...; the sum of squares goes through a fixed tree (lanes, then warps).
+// Called by every thread of the CTA (it synchronises).
+__device__ __forceinline__ void combine_staged_rows(const uint4* rows, const float* gates,
+                                                    float* warp_ss, const float* gamma, int K,
+                                                    int L, float eps, __nv_bfloat16* zrow) {
   const int nvec = L / 8;
-  const uint4* rows = reinterpret_cast<const uint4*>(cb_smem);
   float u[COMBINE_MAX_VEC][8];
   float ss = 0.0f;
 #pragma unroll
@@ -352,9 +313,58 @@ combine_bulk_kernel(const __nv_bfloat16* __restrict__ o, const float* __restrict
       for (int i = 0; i < 4; ++i)
         ob[i] = __floats2bfloat162_rn(u[c][2 * i] * inv_rms * gm[2 * i],
                                       u[c][2 * i + 1] * inv_rms * gm[2 * i + 1]);
-      reinterpret_cast<uint4*>(z + static_cast<size_t>(t) * ldz)[v] = out;
+      reinterpret_cast<uint4*>(zrow)[v] = out;
     }
   }
+}
+
+// Combine + RMSNorm with the token's K expert rows staged in shared memory by 1-D bulk
+// copies: one thread issues the K copies on one mbarrier, so a CTA has all K rows in
+// flight at once (K * L * 2 bytes; two CTAs per SM when that is at most COMBINE_BULK_MAX).
+// Then each thread sums its 8-feature vectors over the slots in slot order, the sum of
+// squares is reduced in the same fixed tree as above, and z is written.  The wait on the
+// copies is bounded; on time-out the CTA records the error bit and writes nothing.
+constexpr int COMBINE_BULK_MAX = 114688;  // bytes of staged rows per CTA (16 x 3584 bf16)
+__global__ void __launch_bounds__(COMBINE_MAX_THREADS)
+combine_bulk_kernel(const __nv_bfloat16* __restrict__ o, const float* __restrict__ gate,
+                    const int32_t* __restrict__ inv, const float* __restrict__ gamma, int T,
+                    int K, int L, float eps, __nv_bfloat16* __restrict__ z, int ldz,
+                    uint32_t* __restrict__ err, unsigned long long timeout_ns) {
+  extern __shared__ __align__(128) uint8_t cb_smem[];
+  __shared__ float gates[32];
+  __shared__ float warp_ss[32];
+  __shared__ __align__(8) uint64_t bar;
+  const int t = blockIdx.x;
+  const uint32_t row_bytes = static_cast<uint32_t>(L) * 2;
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(&bar, 1);
+    ptx::fence_mbar_init();
+  }
+  __syncthreads();
+  pdl_wait();
+  pdl_launch_dependents();
+  if (threadIdx.x == 0) {
+    ptx::mbar_arrive_expect_tx(&bar, row_bytes * static_cast<uint32_t>(K));
+    for (int j = 0; j < K; ++j) {
+      const int row = __ldg(inv + static_cast<size_t>(t) * K + j);
+      ptx::bulk_load(cb_smem + static_cast<size_t>(j) * row_bytes,
+                     o + static_cast<size_t>(row) * L, row_bytes, &bar);
+    }
+  }
+  if (threadIdx.x < K) gates[threadIdx.x] = __ldg(gate + static_cast<size_t>(t) * K + threadIdx.x);
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) abort_flag = 0;
+  __syncthreads();
+  // every thread waits on the copies; the wait is bounded
+  const bool ok = ptx::mbar_wait(&bar, 0u, &abort_flag, timeout_ns);
+  if (!__syncthreads_and(ok ? 1 : 0)) {
+    if (threadIdx.x == 0) atomicOr(err, DEVERR_TIMEOUT_EPILOGUE);
+    // copies still in flight must land before the CTA exits (bounded again)
+    ptx::mbar_wait(&bar, 0u, &abort_flag, timeout_ns);
+    return;
+  }
+  combine_staged_rows(reinterpret_cast<const uint4*>(cb_smem), gates, warp_ss, gamma, K, L, eps,
+                      z + static_cast<size_t>(t) * ldz);
 }
 
 // ------------------------------------------------------------------------------------
