@@ -207,6 +207,24 @@ def test_fp8_small_batches_every_token(dev, oracle_mod, T):
                          max_excluded=max(MAX_EXCLUDED, 1.0 / T))  # one token at most
 
 
+def test_fp8_pairs_with_an_odd_tile_count(dev, oracle_mod):
+    """e4m3 down GEMM in weight-tile pairs over an odd number of 128-row tiles (L = 384), ~150
+    tokens per expert; every token against the oracle's FP8 path."""
+    sh = synth.LayerShape("fp8o", T=1200, d=256, L=384, E=16, K=2, I=128, S=1, Is=64)
+    w = synth.make_weights(sh, seed=91)
+    wd = {k: v.to(dev) for k, v in w.items()}
+    layer = lmoe.Layer(sh, wd, expert_fp8=True)
+    x = synth.make_x(sh, seed=92)
+    logits = synth.make_logits(sh.T, sh.E, seed=93)
+    y, dbg = layer.forward(x.to(dev), residual=x.to(dev), logits_in=logits.to(dev), debug=True)
+    torch.cuda.synchronize()
+    assert layer.device_error() == 0
+    ref = oracle_mod.forward(w, x, sh.K, residual=x, tau="batch", logits_in=logits.numpy(),
+                             expert_fp8=True, tie_margin=TIE_MARGIN)
+    assert np.array_equal(dbg["idx"].cpu().numpy(), ref.idx)
+    assert_close_fp8(y.float().cpu().numpy(), ref.y, ref.scale_ties == 0, tag="pairs odd")
+
+
 def test_fp8_forced_exact_tie(dev, oracle_mod):
     """A token whose latent is exact in fp32 on both sides and whose largest element sits
     exactly on a bf16 rounding tie (1 + 2^-8, between 1 and 1 + 2^-7): the oracle flags it,
