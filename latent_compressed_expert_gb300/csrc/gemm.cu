@@ -813,11 +813,12 @@ int launch_gemm(const void* A, uint64_t a_rows, int a_ld, const void* B, uint64_
   // zero-filled by TMA and cut at N by the epilogue): the router's N = 896 runs as 4 column
   // tiles instead of 7, re-reading the latent half as often (61.9 -> 59.4 us at prefill)
   // N = 896 (the router over 896 experts): four whole 224-wide tiles instead of four 256-wide
-  // ones, the last half empty
+  // ones, the last half empty.  A single M-tile (decode) takes 128-wide tiles: twice the column
+  // tiles to spread over the SMs before the reduction is split (decode 1.181 -> 1.166 ms)
   const int bn = (g.groups == 0 && g.M > BLOCK_M && g.N % 256 != 0 && g.N > 512 &&
                   g.N % 224 == 0 && g.N <= 4 * 224)
                      ? 224
-                     : ((g.N % 256 == 0 || g.N > 512) ? 256 : 128);
+                     : (g.M <= BLOCK_M ? 128 : ((g.N % 256 == 0 || g.N > 512) ? 256 : 128));
   CUtensorMap ta, tb;
   if (g.groups > 0) {
     // MN-major: a_rows / b_rows count K rows; boxes of 64 columns x 64 rows

@@ -41,3 +41,32 @@ def test_pipelined_batches_equal_plain_calls(dev, depth):
     assert layer.device_error() == 0
     for yh, r in zip(y_host, ref):
         assert torch.equal(yh.view(torch.int16), r.view(torch.int16))
+
+
+@pytest.mark.parametrize("T", [64, 1000])
+def test_forward_replays_from_a_cuda_graph(dev, T):
+    """lmoe_forward enqueues only kernels, memsets and event-free copies on its stream, so a
+    whole layer call (split-K dense GEMMs at T = 64, the routed GEMMs' pairs at T = 1000) can be
+    captured into a CUDA graph and replayed; each replay gives the eager call's bits."""
+    sh = H.mid_shape(T)
+    w = {k: v.to(dev) for k, v in synth.make_weights(sh, seed=63).items()}
+    layer = lmoe.Layer(sh, w)
+    x = synth.make_x(sh, seed=64).to(dev)
+    ref = layer.forward(x, residual=x).clone()
+    torch.cuda.synchronize()
+    y = torch.empty_like(x)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):  # warm up the kernels' attributes outside the capture
+        layer.forward(x, residual=x, y=y)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        layer.forward(x, residual=x, y=y)
+    for _ in range(2):
+        y.fill_(0)
+        graph.replay()
+        torch.cuda.synchronize()
+        assert layer.device_error() == 0
+        assert torch.equal(y.view(torch.int16), ref.view(torch.int16))
