@@ -257,21 +257,14 @@ combine_rmsnorm_kernel(const __nv_bfloat16* __restrict__ o, const float* __restr
   }
 }
 
-// z = gamma * u / sqrt(mean(u^2) + eps), u = sum_j gate_j rows[j] in slot order (fp32), from
-// a token's K expert rows staged in shared memory: thread i sums its 8-feature vectors i,
-// i + blockDim.x, ...; the sum of squares goes through a fixed tree (lanes, then warps).
-// Called by every thread of the CTA (it synchronises).
-__device__ __forceinline__ void combine_staged_rows(const uint4* rows, const float* gates,
-                                                    float* warp_ss, const float* gamma, int K,
-                                                    int L, float eps, __nv_bfloat16* zrow) {
+// u += gate_j rows[j] for the K staged rows j = 0..K-1, in that order (fp32 fused multiply-adds):
+// thread i owns the 8-feature vectors i, i + blockDim.x, ... of the token.
+__device__ __forceinline__ void combine_accumulate(const uint4* rows, const float* gates, int K,
+                                                   int L, float (&u)[COMBINE_MAX_VEC][8]) {
   const int nvec = L / 8;
-  float u[COMBINE_MAX_VEC][8];
-  float ss = 0.0f;
 #pragma unroll
   for (int c = 0; c < COMBINE_MAX_VEC; ++c) {
     const int v = threadIdx.x + c * blockDim.x;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) u[c][i] = 0.0f;
     if (v < nvec) {
       for (int j = 0; j < K; ++j) {
         const uint4 raw = rows[static_cast<size_t>(j) * nvec + v];
@@ -284,6 +277,21 @@ __device__ __forceinline__ void combine_staged_rows(const uint4* rows, const flo
           u[c][2 * i + 1] = fmaf(g, f.y, u[c][2 * i + 1]);
         }
       }
+    }
+  }
+}
+
+// z = gamma * u / sqrt(mean(u^2) + eps): the sum of squares of each thread's vectors, then a
+// fixed tree (lanes, then warps).  Called by every thread of the CTA (it synchronises).
+__device__ __forceinline__ void combine_finish(const float (&u)[COMBINE_MAX_VEC][8],
+                                               float* warp_ss, const float* gamma, int L,
+                                               float eps, __nv_bfloat16* zrow) {
+  const int nvec = L / 8;
+  float ss = 0.0f;
+#pragma unroll
+  for (int c = 0; c < COMBINE_MAX_VEC; ++c) {
+    const int v = threadIdx.x + c * blockDim.x;
+    if (v < nvec) {
 #pragma unroll
       for (int i = 0; i < 8; ++i) ss = fmaf(u[c][i], u[c][i], ss);
     }
@@ -318,6 +326,21 @@ __device__ __forceinline__ void combine_staged_rows(const uint4* rows, const flo
   }
 }
 
+// The token's K expert rows staged in shared memory, in rounds of `rpp` rows (all K at once
+// when rpp >= K): u accumulates in registers over the rounds in slot order, so a round size
+// changes the footprint, not the arithmetic.
+__device__ __forceinline__ void combine_staged_rows(const uint4* rows, const float* gates,
+                                                    float* warp_ss, const float* gamma, int K,
+                                                    int L, float eps, __nv_bfloat16* zrow) {
+  float u[COMBINE_MAX_VEC][8];
+#pragma unroll
+  for (int c = 0; c < COMBINE_MAX_VEC; ++c)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) u[c][i] = 0.0f;
+  combine_accumulate(rows, gates, K, L, u);
+  combine_finish(u, warp_ss, gamma, L, eps, zrow);
+}
+
 // Combine + RMSNorm with the token's K expert rows staged in shared memory by 1-D bulk
 // copies: one thread issues the K copies on one mbarrier, so a CTA has all K rows in
 // flight at once (K * L * 2 bytes; two CTAs per SM when that is at most COMBINE_BULK_MAX).
@@ -325,6 +348,7 @@ __device__ __forceinline__ void combine_staged_rows(const uint4* rows, const flo
 // squares is reduced in the same fixed tree as above, and z is written.  The wait on the
 // copies is bounded; on time-out the CTA records the error bit and writes nothing.
 constexpr int COMBINE_BULK_MAX = 114688;  // bytes of staged rows per CTA (16 x 3584 bf16)
+constexpr int COMBINE_ROUND_ROWS = 7;      // rows per round of combine_rounds_kernel (0: off)
 __global__ void __launch_bounds__(COMBINE_MAX_THREADS)
 combine_bulk_kernel(const __nv_bfloat16* __restrict__ o, const float* __restrict__ gate,
                     const int32_t* __restrict__ inv, const float* __restrict__ gamma, int T,
@@ -367,6 +391,64 @@ combine_bulk_kernel(const __nv_bfloat16* __restrict__ o, const float* __restrict
                       z + static_cast<size_t>(t) * ldz);
 }
 
+// The same combine with the token's rows staged in rounds of `rpp` (a buffer of rpp rows) and
+// two 8-feature vectors per thread: a CTA needs rpp * L * 2 bytes of shared memory and L / 16
+// threads, so more tokens are in flight per SM -- four at rpp = 7 and L = 3584 (50 KB and 224
+// threads each), against two when all 16 rows of a token are staged at once.  u accumulates in
+// the same slot order as combine_bulk_kernel; the sum of squares adds each thread's two vectors
+// before the tree, so z may differ from that kernel's in the last bit.
+__global__ void __launch_bounds__(COMBINE_MAX_THREADS)
+combine_rounds_kernel(const __nv_bfloat16* __restrict__ o, const float* __restrict__ gate,
+                      const int32_t* __restrict__ inv, const float* __restrict__ gamma, int T,
+                      int K, int L, float eps, __nv_bfloat16* __restrict__ z, int ldz, int rpp,
+                      uint32_t* __restrict__ err, unsigned long long timeout_ns) {
+  extern __shared__ __align__(128) uint8_t cr_smem[];
+  __shared__ float gates[32];
+  __shared__ float warp_ss[32];
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  const int t = blockIdx.x;
+  const uint32_t row_bytes = static_cast<uint32_t>(L) * 2;
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(&bar, 1);
+    abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  __syncthreads();
+  pdl_wait();
+  pdl_launch_dependents();
+  if (threadIdx.x < K) gates[threadIdx.x] = __ldg(gate + static_cast<size_t>(t) * K + threadIdx.x);
+  __syncthreads();
+  float u[COMBINE_MAX_VEC][8];
+#pragma unroll
+  for (int c = 0; c < COMBINE_MAX_VEC; ++c)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) u[c][i] = 0.0f;
+  int round = 0;
+  for (int j0 = 0; j0 < K; j0 += rpp, ++round) {
+    const int nr = K - j0 < rpp ? K - j0 : rpp;
+    if (threadIdx.x == 0) {
+      ptx::mbar_arrive_expect_tx(&bar, row_bytes * static_cast<uint32_t>(nr));
+      for (int j = 0; j < nr; ++j) {
+        const int row = __ldg(inv + static_cast<size_t>(t) * K + j0 + j);
+        ptx::bulk_load(cr_smem + static_cast<size_t>(j) * row_bytes,
+                       o + static_cast<size_t>(row) * L, row_bytes, &bar);
+      }
+    }
+    const bool ok = ptx::mbar_wait(&bar, static_cast<uint32_t>(round) & 1u, &abort_flag,
+                                   timeout_ns);
+    if (!__syncthreads_and(ok ? 1 : 0)) {
+      if (threadIdx.x == 0) atomicOr(err, DEVERR_TIMEOUT_EPILOGUE);
+      // copies still in flight must land before the CTA exits (bounded again)
+      ptx::mbar_wait(&bar, static_cast<uint32_t>(round) & 1u, &abort_flag, timeout_ns);
+      return;
+    }
+    combine_accumulate(reinterpret_cast<const uint4*>(cr_smem), gates + j0, nr, L, u);
+    __syncthreads();  // every thread is done with the buffer before the next round fills it
+  }
+  combine_finish(u, warp_ss, gamma, L, eps, z + static_cast<size_t>(t) * ldz);
+}
+
 // ------------------------------------------------------------------------------------
 int launch_dispatch(const int32_t* idx, int T, int E, int K, uint32_t* masks, uint32_t* base,
                     int32_t* offsets, int32_t* ct_off, int tokn, int32_t* inv,
@@ -404,6 +486,19 @@ int launch_combine(const __nv_bfloat16* o, const float* gate, const int32_t* inv
       ceil_div(nvec < COMBINE_MAX_THREADS ? nvec : COMBINE_MAX_THREADS, 32) * 32);
   if (nvec > COMBINE_MAX_VEC * threads) return LMOE_ERR_UNSUPPORTED;
   const size_t staged = static_cast<size_t>(K) * L * 2;
+  if (COMBINE_ROUND_ROWS > 0 && K > COMBINE_ROUND_ROWS && nvec % 2 == 0 &&
+      nvec / 2 <= COMBINE_MAX_THREADS && nvec / 2 >= 32) {
+    // rounds of COMBINE_ROUND_ROWS rows, two vectors per thread
+    const int th = static_cast<int>(ceil_div(nvec / 2, 32) * 32);
+    const size_t sm = static_cast<size_t>(COMBINE_ROUND_ROWS) * L * 2;
+    if (cudaFuncSetAttribute(combine_rounds_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(sm)) != cudaSuccess)
+      return LMOE_ERR_CUDA;
+    return launch_pdl(combine_rounds_kernel, T, th, sm, stream, o, gate, inv, gamma, T, K, L,
+                      eps, z, ldz, COMBINE_ROUND_ROWS, err, timeout_ns) == cudaSuccess
+               ? LMOE_OK
+               : LMOE_ERR_CUDA;
+  }
   if (staged <= static_cast<size_t>(COMBINE_BULK_MAX)) {
     if (cudaFuncSetAttribute(combine_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(staged)) != cudaSuccess)

@@ -431,8 +431,11 @@ def test_checked_mode_reports_nonfinite_logits(dev, monkeypatch):
 
 def test_decode_split_k_matches_unsplit(dev):
     """A small whole-layer batch splits the dense GEMMs' reductions (the workspace includes
-    the split-K region): three more launches, outputs within the layer's tolerance of the
-    unsplit call in a workspace without the region, routing identical."""
+    the split-K region): one more launch (the reduce) per split GEMM, outputs within the
+    layer's tolerance of the unsplit call in a workspace without the region, routing
+    identical.  Which GEMMs split depends on their column tiles against the SM count (at
+    T = 64 and these widths: the router and the output GEMM; the fused latent/shared GEMM
+    already has 92 column tiles of 128), so the test asks for at least one."""
     sh = synth.LayerShape("k3_decode_small", T=64, d=7168, L=3584, E=128, K=16, I=512, S=2,
                           Is=2048)
     w = synth.make_weights(sh, seed=31, device=dev)
@@ -451,7 +454,7 @@ def test_decode_split_k_matches_unsplit(dev):
         layer.ws_bytes = full
     torch.cuda.synchronize()
     assert layer.device_error() == 0
-    assert n1 == n2 + 3
+    assert n2 < n1 <= n2 + 3
     assert torch.equal(d1["idx"], d2["idx"])
     H.assert_close(y1.float().cpu().numpy(), y2.float().cpu().numpy().astype(np.float64),
                    "decode split-K vs unsplit")
