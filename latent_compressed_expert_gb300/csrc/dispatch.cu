@@ -326,6 +326,54 @@ __device__ __forceinline__ void combine_finish(const float (&u)[COMBINE_MAX_VEC]
   }
 }
 
+// The same normalisation for threads that hold two vectors (v and v + blockDim.x, blockDim.x a
+// multiple of 32), with the reduction tree of the one-vector-per-thread kernels above: vector v
+// is summed as lane v % 32 of warp v / 32 whichever thread holds it, and the final tree runs
+// over the same ceil(nvec / 32) warp sums.  So z has their bits, for any L up to 32 warps.
+__device__ __forceinline__ void combine_finish_pairs(const float (&u)[COMBINE_MAX_VEC][8],
+                                                     float* warp_ss, const float* gamma, int L,
+                                                     float eps, __nv_bfloat16* zrow) {
+  const int nvec = L / 8;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nwp = static_cast<int>(blockDim.x >> 5);
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    const int v = threadIdx.x + c * blockDim.x;
+    float ss = 0.0f;
+    if (v < nvec) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) ss = fmaf(u[c][i], u[c][i], ss);
+    }
+    for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+    if (lane == 0) warp_ss[warp + c * nwp] = ss;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const int nw = (nvec + 31) >> 5;
+    float v = lane < nw ? warp_ss[lane] : 0.0f;
+    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    if (lane == 0) warp_ss[0] = v;
+  }
+  __syncthreads();
+  const float inv_rms = rsqrtf(warp_ss[0] / static_cast<float>(L) + eps);
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    const int v = threadIdx.x + c * blockDim.x;
+    if (v < nvec) {
+      const float4 g0 = __ldg(reinterpret_cast<const float4*>(gamma) + 2 * v);
+      const float4 g1 = __ldg(reinterpret_cast<const float4*>(gamma) + 2 * v + 1);
+      const float gm[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+      uint4 out;
+      __nv_bfloat162* ob = reinterpret_cast<__nv_bfloat162*>(&out);
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        ob[i] = __floats2bfloat162_rn(u[c][2 * i] * inv_rms * gm[2 * i],
+                                      u[c][2 * i + 1] * inv_rms * gm[2 * i + 1]);
+      reinterpret_cast<uint4*>(zrow)[v] = out;
+    }
+  }
+}
+
 // The token's K expert rows staged in shared memory, in rounds of `rpp` rows (all K at once
 // when rpp >= K): u accumulates in registers over the rounds in slot order, so a round size
 // changes the footprint, not the arithmetic.
@@ -395,8 +443,9 @@ combine_bulk_kernel(const __nv_bfloat16* __restrict__ o, const float* __restrict
 // two 8-feature vectors per thread: a CTA needs rpp * L * 2 bytes of shared memory and L / 16
 // threads, so more tokens are in flight per SM -- four at rpp = 7 and L = 3584 (50 KB and 224
 // threads each), against two when all 16 rows of a token are staged at once.  u accumulates in
-// the same slot order as combine_bulk_kernel; the sum of squares adds each thread's two vectors
-// before the tree, so z may differ from that kernel's in the last bit.
+// the same slot order as combine_bulk_kernel and the norm takes the same tree, so z has that
+// kernel's bits (for L <= 4096, where it holds one vector per thread): the choice between the
+// two may depend on the batch size without a token's output depending on its batch.
 __global__ void __launch_bounds__(COMBINE_MAX_THREADS)
 combine_rounds_kernel(const __nv_bfloat16* __restrict__ o, const float* __restrict__ gate,
                       const int32_t* __restrict__ inv, const float* __restrict__ gamma, int T,
@@ -446,7 +495,7 @@ combine_rounds_kernel(const __nv_bfloat16* __restrict__ o, const float* __restri
     combine_accumulate(reinterpret_cast<const uint4*>(cr_smem), gates + j0, nr, L, u);
     __syncthreads();  // every thread is done with the buffer before the next round fills it
   }
-  combine_finish(u, warp_ss, gamma, L, eps, z + static_cast<size_t>(t) * ldz);
+  combine_finish_pairs(u, warp_ss, gamma, L, eps, z + static_cast<size_t>(t) * ldz);
 }
 
 // ------------------------------------------------------------------------------------
@@ -486,10 +535,19 @@ int launch_combine(const __nv_bfloat16* o, const float* gate, const int32_t* inv
       ceil_div(nvec < COMBINE_MAX_THREADS ? nvec : COMBINE_MAX_THREADS, 32) * 32);
   if (nvec > COMBINE_MAX_VEC * threads) return LMOE_ERR_UNSUPPORTED;
   const size_t staged = static_cast<size_t>(K) * L * 2;
-  if (COMBINE_ROUND_ROWS > 0 && K > COMBINE_ROUND_ROWS && nvec % 2 == 0 &&
-      nvec / 2 <= COMBINE_MAX_THREADS && nvec / 2 >= 32) {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return LMOE_ERR_CUDA;
+  // Rounds pay once tokens queue for the SMs; a batch whose CTAs are all resident at once with
+  // the whole-token staging (two per SM) is done in one round trip per token instead of three
+  // (decode, T = 64: 6.4 us against 10 us).
+  const bool rounds_pay = T > 2 * static_cast<int64_t>(sms) || staged > COMBINE_BULK_MAX;
+  // (nvec <= 512: the other kernels hold one vector per thread, whose tree the rounds follow)
+  if (COMBINE_ROUND_ROWS > 0 && rounds_pay && K > COMBINE_ROUND_ROWS && nvec >= 64 &&
+      nvec <= COMBINE_MAX_THREADS) {
     // rounds of COMBINE_ROUND_ROWS rows, two vectors per thread
-    const int th = static_cast<int>(ceil_div(nvec / 2, 32) * 32);
+    const int th = static_cast<int>(ceil_div(ceil_div(nvec, 2), 32) * 32);
     const size_t sm = static_cast<size_t>(COMBINE_ROUND_ROWS) * L * 2;
     if (cudaFuncSetAttribute(combine_rounds_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(sm)) != cudaSuccess)

@@ -129,6 +129,10 @@ EDGE_SHAPES = [
     # tokens per expert in one chunk, and with ~300 in two equal chunks of the 256 granule
     ("pairs_odd", synth.LayerShape("po", T=1200, d=256, L=384, E=16, K=2, I=192, S=1, Is=64)),
     ("wide_odd", synth.LayerShape("wo", T=2400, d=256, L=384, E=16, K=2, I=192, S=1, Is=64)),
+    # the same loads over an even number of weight tiles (2I = L = 256)
+    ("sm_pairs", synth.LayerShape("sp", T=1200, d=256, L=256, E=16, K=2, I=128, S=1, Is=64)),
+    ("sm_pairs_wide", synth.LayerShape("spw", T=2400, d=256, L=256, E=16, K=2, I=128, S=1,
+                                       Is=64)),
 ]
 
 
@@ -458,3 +462,36 @@ def test_decode_split_k_matches_unsplit(dev):
     assert torch.equal(d1["idx"], d2["idx"])
     H.assert_close(y1.float().cpu().numpy(), y2.float().cpu().numpy().astype(np.float64),
                    "decode split-K vs unsplit")
+
+
+@pytest.mark.parametrize("sh", [H.mid_shape(1000),
+                                synth.LayerShape("k3w", T=1000, d=7168, L=3584, E=32, K=16,
+                                                 I=128, S=1, Is=256)],
+                         ids=["mid", "k3_widths"])
+def test_output_independent_of_batch_size(dev, sh):
+    """A token's output bits do not depend on the batch it runs in (without split-K
+    reductions).  With given logits and thresholds the routing is per token; a 64-token batch
+    combines its rows with the
+    whole-token staging (every CTA resident at once), a 1000-token batch in rounds of seven
+    rows: both take the same slot-order sum and the same reduction tree, so the rows agree bit
+    for bit."""
+    _, layer = _layer(sh, seed=41, dev=dev)
+    x = synth.make_x(sh, seed=41).to(dev)
+    logits = synth.make_logits(sh.T, sh.E, seed=41).to(dev)
+    tau = torch.zeros(sh.E, dtype=torch.float32, device=dev)
+    y_big, d_big = layer.forward(x, residual=x, logits_in=logits, tau=tau, debug=True)
+    y_big = y_big.clone()
+    n = 64
+    xs = x[:n].contiguous()
+    # without the split-K region, which would change the small batch's dense reductions
+    full = layer.ws_bytes
+    layer.ws_bytes = lmoe.workspace_base_bytes(lmoe.dims_of(sh, T=n))
+    try:
+        y_small, d_small = layer.forward(xs, residual=xs, logits_in=logits[:n].contiguous(),
+                                         tau=tau, debug=True)
+    finally:
+        layer.ws_bytes = full
+    torch.cuda.synchronize()
+    assert layer.device_error() == 0
+    assert torch.equal(d_small["idx"], d_big["idx"][:n])
+    assert torch.equal(y_small.view(torch.int16), y_big[:n].view(torch.int16))
