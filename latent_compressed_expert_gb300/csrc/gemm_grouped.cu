@@ -41,6 +41,9 @@ constexpr int GROUPED_SHALLOW_MIN_TOKENS = 32;
 // four (56 KB) without the epilogue's output staging.
 constexpr int GROUPED_STAGES_PAIR = 3;
 constexpr int GROUPED_PAIR_MIN_TOKENS = 64;  // experts' mean token count from which pairs run
+// bf16 pairs over two SMs (cta_group::2, two weight tiles per SM; see grouped_gemm_pair_kernel)
+// for GEMMs whose token rows are loaded by TMA
+constexpr bool GROUPED_SM_PAIR = true;
 
 // MW: weight row tiles per CTA tile.  MW = 2 ("weight-tile pairs") stages two 128-row
 // weight tiles of the same expert with one token tile and issues two MMAs per K-step, so
@@ -100,37 +103,46 @@ struct GTile {
 // Tile -> (expert, token chunk, weight tile group).  An expert's `count` token rows form
 // ceil(count / tokn) chunks of equal size (to one row); its MW-tile groups of weight rows are
 // enumerated fastest, so the tiles that share a chunk's token rows run at the same time on
-// neighbouring SMs.
-template <int MW>
-__device__ __forceinline__ GTile decode_gtile(const GroupedArgs& g, int mt, int tile) {
+// neighbouring SMs.  `ld` reads entry i of the chunk prefix sum (which = 0) or of the expert
+// segment offsets (which = 1), from global memory or from a copy in shared memory.
+template <int MW, typename Load>
+__device__ __forceinline__ GTile decode_gtile_with(const GroupedArgs& g, int mt, int tile,
+                                                   Load ld) {
   const int mg = (mt + MW - 1) / MW;  // weight tile groups per (expert, chunk)
   const int q = tile / mg;            // global (expert, chunk) index
   int lo = 0, hi = g.E;               // ct_off[lo] <= q < ct_off[hi]
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
-    if (__ldg(g.ct_off + mid) <= q)
+    if (ld(0, mid) <= q)
       lo = mid;
     else
       hi = mid;
   }
   const int e = lo;
-  const int c0 = __ldg(g.ct_off + e);
+  const int c0 = ld(0, e);
   const int chunk = q - c0;
-  const int nchunk = __ldg(g.ct_off + e + 1) - c0;
+  const int nchunk = ld(0, e + 1) - c0;
   const int m = (tile - q * mg) * MW;
   GTile t;
   t.e = e;
   t.r0 = m * BLOCK_M;
   t.nw = min(MW, mt - m);
   t.w_row = (e * mt + m) * (g.Kd / BLOCK_K) * BLOCK_M;
-  const int seg0 = __ldg(g.seg_off + e);
-  const int cnt = __ldg(g.seg_off + e + 1) - seg0;
+  const int seg0 = ld(1, e);
+  const int cnt = ld(1, e + 1) - seg0;
   // <= tokn, and every chunk non-empty; most experts have one chunk (no division)
   const int csz = nchunk == 1 ? cnt : (cnt + nchunk - 1) / nchunk;
   t.tok0 = seg0 + chunk * csz;
   t.ntok = min(csz, cnt - chunk * csz);
   t.npad = (t.ntok + GROUPED_BOX_T - 1) / GROUPED_BOX_T * GROUPED_BOX_T;
   return t;
+}
+
+template <int MW>
+__device__ __forceinline__ GTile decode_gtile(const GroupedArgs& g, int mt, int tile) {
+  return decode_gtile_with<MW>(g, mt, tile, [&](int which, int i) {
+    return __ldg((which == 0 ? g.ct_off : g.seg_off) + i);
+  });
 }
 
 __device__ __forceinline__ void graise(const GroupedArgs& g, volatile int* abort_flag,
@@ -512,6 +524,336 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
   }
 }
 
+// ------------------------------------------------------------------------------------
+// Weight tiles over an SM pair (tcgen05 cta_group::2), for the GEMMs whose token rows are
+// loaded by TMA (the routed down GEMM, the backward's grouped GEMMs).
+//
+// A cluster of two CTAs on two SMs computes one (expert, token chunk, 512 weight rows) tile
+// with MMAs of M = 256: rank r holds weight tiles 2r and 2r + 1 (128 rows each) of the group
+// and the r-th half of the chunk's padded token rows (npad / 2, a multiple of 16).  Rank 0
+// issues the MMAs; each reads both CTAs' shared memory at the same offsets, and each CTA's
+// TMEM receives its 256 weight rows x all npad tokens.  Per K-block an SM stages 32 KB of
+// weights and at most 16 KB of token rows for 256 x npad x 64 of the MMA, against 32 KB +
+// 32 KB for the same share as a weight-tile pair on one SM.  The two accumulators take all
+// 512 TMEM columns and are drained while no MMA runs, as on one SM.  (With one weight tile per
+// CTA, two accumulator sets fit and the drain overlaps the next tile's MMAs; that measured
+// slower.  The gate/value GEMM, whose rows are gathered, stays on one SM: a gathered variant
+// with a forwarding thread for the peer's rows was slower there.)
+//
+// Synchronisation (every wait bounded):
+// - full[s] of rank 0 completes when both CTAs' TMA bytes for stage s have landed: rank 0's
+//   producer expects both CTAs' bytes, rank 1's copies complete on rank 0's barrier.
+// - empty[s] and tfull of both CTAs get one arrival each from rank 0's commits (multicast).
+// - tempty of rank 0 gets one arrival per epilogue warp of both CTAs (remote ones with the
+//   default arrive semantics: a release at cluster scope made each take ~1 us).
+// - a cluster barrier after the barriers are initialised, and one before TMEM is freed and the
+//   CTAs exit, so that neither CTA leaves while its peer may still signal its barriers or read
+//   its shared memory.
+template <int STAGES_, int TOKN_>
+struct GroupedPairCfg {
+  static constexpr int MW = 2;                           // weight tiles per CTA
+  static constexpr int TOKN = TOKN_;                     // max tokens (N) per cluster tile
+  static constexpr int HALF = TOKN / 2;                  // token rows per CTA
+  static constexpr int BOX_T = 16;                       // token rows per TMA box
+  static constexpr int A_BYTES = BLOCK_M * BLOCK_K * 2;  // 16 KB
+  static constexpr int W_BYTES = MW * A_BYTES;
+  static constexpr int B_BYTES = HALF * BLOCK_K * 2;     // up to 16 KB
+  static constexpr int STAGE_BYTES = W_BYTES + B_BYTES;
+  static constexpr int STAGES = STAGES_;
+  static constexpr int ACC_COLS = 256;                   // TMEM columns per weight tile
+  static constexpr int TMEM_COLS = 512;
+  static constexpr int EPI_WARPS = 8;                    // warps 2..9
+  static constexpr int EPI_OFF = STAGES * STAGE_BYTES;
+  static constexpr int EPI_BYTES = EPI_WARPS * 32 * 32 * 2;  // a 2 KB staging slot per warp
+  static constexpr int BAR_OFF = EPI_OFF + EPI_BYTES;
+  static constexpr int NUM_BARS = 2 * STAGES + 3;
+  static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
+  // copies of the chunk prefix sum and the expert segment offsets (E + 1 entries each) in the
+  // rest of the shared memory: the tile decode's binary search then costs shared-memory
+  // latency instead of 2-3 K cycles of dependent global loads per tile
+  static constexpr int TAB_OFF = MISC_OFF + 16;
+  static constexpr int TAB_ROOM = (232448 - 1024 - TAB_OFF) / 8;
+  static constexpr int TAB_CAP = TAB_ROOM < 2048 ? TAB_ROOM : 2048;  // entries per table
+  static constexpr int SMEM_BYTES = TAB_OFF + TAB_CAP * 8 + 1024;
+  static_assert(TOKN % 32 == 0 && TOKN <= ACC_COLS && MW * ACC_COLS <= TMEM_COLS,
+                "UMMA N range; the accumulators fit TMEM");
+  static_assert(TAB_CAP >= 1024, "room for the decode tables of up to 1023 experts");
+  static_assert(B_BYTES % 1024 == 0 && STAGE_BYTES % 1024 == 0, "1024-aligned tiles");
+  static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+};
+
+template <int STAGES_, int TOKN_>
+__global__ void __launch_bounds__(GROUPED_THREADS, 1)
+grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmW,
+                         const __grid_constant__ CUtensorMap tmX, const GroupedArgs g) {
+  using C = GroupedPairCfg<STAGES_, TOKN_>;
+  constexpr int MW = C::MW;
+  constexpr int CW = 2 * MW;  // weight tiles per cluster tile
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = ptx::smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
+  uint64_t* empty = full + C::STAGES;
+  uint64_t* tfull = empty + C::STAGES;
+  uint64_t* tempty = tfull + 1;
+  uint64_t* drain = tempty + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::MISC_OFF);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 4);
+  __nv_bfloat16* epi_stage = reinterpret_cast<__nv_bfloat16*>(smem + C::EPI_OFF);
+
+  const uint32_t rank = ptx::cluster_ctarank();  // rank 0 issues the MMAs
+  const bool lead = rank == 0;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int mt = g.M_w / BLOCK_M;  // a multiple of CW: the launcher checks
+  const int nk = g.Kd / BLOCK_K;
+  const uint64_t limit = g.timeout_ns;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      ptx::mbar_init(&full[s], 1);  // rank 0's producer; the bytes come from both CTAs
+      ptx::mbar_init(&empty[s], 1);
+    }
+    ptx::mbar_init(tfull, 1);
+    ptx::mbar_init(tempty, 2 * C::EPI_WARPS);
+    ptx::mbar_init(drain, 1);
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::prefetch_tmap(&tmW);
+    ptx::prefetch_tmap(&tmX);
+  }
+  ptx::cluster_sync();  // both CTAs' barriers exist before either signals the other's
+  if (warp == 1) {
+    ptx::tmem_alloc_pair(tmem_slot, C::TMEM_COLS);
+    ptx::tmem_relinquish_pair();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  pdl_wait();
+  pdl_launch_dependents();
+  int32_t* tab = reinterpret_cast<int32_t*>(smem + C::TAB_OFF);
+  const bool tab_smem = g.E < C::TAB_CAP;  // both tables' E + 1 entries fit
+  if (tab_smem) {
+    for (int i = threadIdx.x; i <= g.E; i += blockDim.x) {
+      tab[i] = __ldg(g.ct_off + i);
+      tab[C::TAB_CAP + i] = __ldg(g.seg_off + i);
+    }
+    __syncthreads();
+  }
+  auto decode = [&](int tile) {
+    return decode_gtile_with<CW>(g, mt, tile, [&](int which, int i) {
+      return tab_smem ? tab[which * C::TAB_CAP + i]
+                      : __ldg((which == 0 ? g.ct_off : g.seg_off) + i);
+    });
+  };
+  const int total = (tab_smem ? tab[g.E] : __ldg(g.ct_off + g.E)) * (mt / CW);
+  const int cid = static_cast<int>(ptx::cluster_id_x());
+  const int ncl = static_cast<int>(ptx::ncluster_x());
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ TMA producer (both ranks)
+      const uint64_t w_policy = ptx::l2_policy_evict_first();
+      uint32_t it = 0;
+      bool ok = true;
+      for (int tile = cid; ok && tile < total; tile += ncl) {
+        const GTile t = decode(tile);
+        const int half = t.npad / 2;
+        const int nbox = half / C::BOX_T;
+        const uint32_t bytes =  // both CTAs' copies: rank 0 expects them all
+            2u * (static_cast<uint32_t>(C::W_BYTES) +
+                  static_cast<uint32_t>(nbox) * C::BOX_T * BLOCK_K * 2u);
+        // this CTA's weight tiles are rank * MW .. rank * MW + MW - 1 of the cluster tile's;
+        // an expert's row tiles are nk boxes apart
+        const int wr0 = t.w_row + static_cast<int>(rank) * MW * nk * BLOCK_M;
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int s = static_cast<int>(it % C::STAGES);
+          const uint32_t ph = (it / C::STAGES) & 1u;
+          if (!ptx::mbar_wait(&empty[s], ph ^ 1u, abort_flag, limit)) {
+            graise(g, abort_flag, DEVERR_TIMEOUT_PRODUCER);
+            ok = false;
+            break;
+          }
+          uint8_t* sa = smem + s * C::STAGE_BYTES;
+          uint8_t* sb = sa + C::W_BYTES;
+          const uint32_t fb = ptx::mapa_shared(ptx::smem_u32(&full[s]), 0);
+          if (lead) ptx::mbar_arrive_expect_tx(&full[s], bytes);
+#pragma unroll
+          for (int w = 0; w < MW; ++w) {
+            const int wr = wr0 + (w * nk + kb) * BLOCK_M;
+            if (g.evict_first)
+              ptx::tma_load_2d_pair_hint(sa + w * C::A_BYTES, &tmW, fb, 0, wr, w_policy);
+            else
+              ptx::tma_load_2d_pair(sa + w * C::A_BYTES, &tmW, fb, 0, wr);
+          }
+          for (int b = 0; b < nbox; ++b)
+            ptx::tma_load_2d_pair(sb + b * C::BOX_T * BLOCK_K * 2, &tmX, fb, kb * BLOCK_K,
+                                  t.tok0 + static_cast<int>(rank) * half + b * C::BOX_T);
+        }
+      }
+      // rank 0's last full phases cover both CTAs' last copies: they land before the pair exits
+      if (lead) {
+        const uint32_t first = it > static_cast<uint32_t>(C::STAGES) ? it - C::STAGES : 0u;
+        for (uint32_t j = first; j < it; ++j) {
+          if (!ptx::mbar_wait(&full[j % C::STAGES], (j / C::STAGES) & 1u, abort_flag, limit)) {
+            graise(g, abort_flag, DEVERR_TIMEOUT_DRAIN);
+            break;
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && lead) {
+      // ------------------------------------------------------------ MMA issuer (rank 0)
+      uint32_t it = 0;
+      int lt = 0;
+      for (int tile = cid; tile < total; tile += ncl, ++lt) {
+        const GTile t = decode(tile);
+        const uint32_t idesc = ptx::idesc_bf16_f32(2 * BLOCK_M, t.npad);
+        if (!ptx::mbar_wait(tempty, (static_cast<uint32_t>(lt) & 1u) ^ 1u, abort_flag, limit)) {
+          graise(g, abort_flag, DEVERR_TIMEOUT_MMA);
+          break;
+        }
+        ptx::tc_fence_after();
+        bool ok = true;
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int s = static_cast<int>(it % C::STAGES);
+          const uint32_t ph = (it / C::STAGES) & 1u;
+          if (!ptx::mbar_wait(&full[s], ph, abort_flag, limit)) {
+            graise(g, abort_flag, DEVERR_TIMEOUT_MMA);
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t sa = ptx::smem_u32(smem + s * C::STAGE_BYTES);
+          const uint32_t sb = sa + C::W_BYTES;
+#pragma unroll
+          for (int k = 0; k < BLOCK_K / 16; ++k) {  // 32 bytes of K per instruction
+#pragma unroll
+            for (int w = 0; w < MW; ++w)  // weight tile w accumulates at TMEM column w * 256
+              ptx::umma_bf16_pair(tmem_base + static_cast<uint32_t>(w * C::ACC_COLS),
+                                  ptx::smem_desc_sw128(sa + w * C::A_BYTES + k * 32),
+                                  ptx::smem_desc_sw128(sb + k * 32), idesc,
+                                  (kb | k) != 0 ? 1u : 0u);
+          }
+          ptx::umma_commit_pair(&empty[s], 0x3);
+        }
+        if (!ok) break;
+        ptx::umma_commit_pair(tfull, 0x3);
+      }
+      ptx::umma_commit_pair(drain, 0x1);
+      if (!ptx::mbar_wait(drain, 0u, abort_flag, limit))
+        graise(g, abort_flag, DEVERR_TIMEOUT_DRAIN);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue (both ranks)
+    // warps 2..9; the two groups of four take the even and odd 32-token chunks.  A thread owns
+    // one weight row of each of this CTA's two tiles (TMEM lane quarter warp & 3) and writes it
+    // for the tokens of both halves, through a per-warp staging slot as 16-byte pieces of the
+    // token rows.
+    const int q = warp & 3;
+    const int eg = (warp - 2) / GROUPED_EPI_WARPS;
+    const uint32_t tempty_lead = ptx::mapa_shared(ptx::smem_u32(tempty), 0);
+    __nv_bfloat16* st = epi_stage + (warp - 2) * (32 * 32);
+    int lt = 0;
+    for (int tile = cid; tile < total; tile += ncl, ++lt) {
+      const GTile t = decode(tile);  // before the wait: its loads hide there
+      const bool got = ptx::mbar_wait(tfull, static_cast<uint32_t>(lt) & 1u, abort_flag, limit);
+      if (!__all_sync(0xffffffffu, got)) {
+        if (lane == 0) graise(g, abort_flag, DEVERR_TIMEOUT_EPILOGUE);
+        break;
+      }
+      ptx::tc_fence_after();
+#pragma unroll 1
+      for (int w = 0; w < MW; ++w) {
+        // this CTA's weight tile w: its first weight row within the expert
+        const int r0w = t.r0 + (static_cast<int>(rank) * MW + w) * BLOCK_M;
+        const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                               static_cast<uint32_t>(w * C::ACC_COLS);
+#pragma unroll 1
+        for (int ch = eg; ch * 32 < t.npad; ch += 2) {
+          float v[32];
+          ptx::tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(ch * 32), v);
+          const int nv = min(32, t.ntok - ch * 32);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) st[j * 32 + lane] = __float2bfloat16_rn(v[j]);
+          __syncwarp();
+          const int piece = lane & 3;
+#pragma unroll
+          for (int j0 = 0; j0 < 32; j0 += 8) {
+            const int j = j0 + (lane >> 2);
+            const uint4 val = *reinterpret_cast<const uint4*>(st + j * 32 + piece * 8);
+            if (j < nv)
+              *reinterpret_cast<uint4*>(g.out + static_cast<size_t>(t.tok0 + ch * 32 + j) * g.ldo +
+                                        r0w + q * 32 + piece * 8) = val;
+          }
+          __syncwarp();
+        }
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if (lead)
+          ptx::mbar_arrive(tempty);
+        else
+          ptx::mbar_arrive_cluster(tempty_lead);
+      }
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::cluster_sync();  // the peer is done with this CTA's barriers, shared memory and TMEM
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
+  }
+}
+
+template <int STAGES_, int TOKN_>
+static int launch_grouped_pair(const CUtensorMap& tw, const CUtensorMap& tx,
+                               const GroupedArgs& g, cudaStream_t stream) {
+  using C = GroupedPairCfg<STAGES_, TOKN_>;
+  auto kernel = grouped_gemm_pair_kernel<STAGES_, TOKN_>;
+  if (g.tokn > TOKN_) return LMOE_ERR_UNSUPPORTED;
+  if (g.gather || g.epi != EPI_BF16 || g.fp8 || g.M_w % (2 * C::MW * BLOCK_M) != 0)
+    return LMOE_ERR_INVALID_ARG;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           C::SMEM_BYTES) != cudaSuccess)
+    return LMOE_ERR_CUDA;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return LMOE_ERR_CUDA;
+  int pairs = sms / 2;
+  if (g.max_ctas > 0 && g.max_ctas / 2 < pairs) pairs = g.max_ctas / 2 > 0 ? g.max_ctas / 2 : 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * pairs);
+  cfg.blockDim = dim3(GROUPED_THREADS);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  // a persistent grid: no more pairs than can be resident at once (an SM pair shares a GPC)
+  int active = 0;
+  if (cudaOccupancyMaxActiveClusters(&active, kernel, &cfg) == cudaSuccess && active > 0 &&
+      active < pairs) {
+    pairs = active;
+    cfg.gridDim = dim3(2 * pairs);
+  }
+  return cudaLaunchKernelEx(&cfg, kernel, tw, tx, g) == cudaSuccess ? LMOE_OK : LMOE_ERR_CUDA;
+}
+
 template <int STAGES_, bool FP8, int MW, int TOKN_, bool STAGED = true>
 static int launch_grouped_stages(const CUtensorMap& tw, const CUtensorMap& tx,
                                  const GroupedArgs& g, cudaStream_t stream) {
@@ -587,6 +929,15 @@ int launch_grouped_gemm(const void* W, const void* X, uint64_t x_rows, int x_ld,
   }
   // Weight-tile pairs when experts see many tokens (the token rows, re-read by every weight
   // tile of their expert, bound the shared-memory fill there); single tiles at decode.
+  if (pairs && !g.gather && g.epi == EPI_BF16 && GROUPED_SM_PAIR && g.M_w % (4 * BLOCK_M) == 0) {
+    // ... over SM pairs, two weight tiles per SM, when the token rows come by TMA
+    CUtensorMap tx16;
+    if (!make_tmap_bf16(&tx16, X, x_rows, static_cast<uint64_t>(kd), static_cast<uint64_t>(ld),
+                        GroupedPairCfg<4, GROUPED_TOKN_WIDE>::BOX_T))
+      return LMOE_ERR_CUDA;
+    if (wide) return launch_grouped_pair<4, GROUPED_TOKN_WIDE>(tw, tx16, ga, stream);
+    return launch_grouped_pair<4, GROUPED_TOKN>(tw, tx16, ga, stream);
+  }
   if (pairs) {
     if (wide) return launch_grouped_stages<GROUPED_STAGES_PAIR, false, 2, GROUPED_TOKN_WIDE>(
                   tw, tx, ga, stream);

@@ -129,9 +129,11 @@ EDGE_SHAPES = [
     # tokens per expert in one chunk, and with ~300 in two equal chunks of the 256 granule
     ("pairs_odd", synth.LayerShape("po", T=1200, d=256, L=384, E=16, K=2, I=192, S=1, Is=64)),
     ("wide_odd", synth.LayerShape("wo", T=2400, d=256, L=384, E=16, K=2, I=192, S=1, Is=64)),
-    # the same loads over an even number of weight tiles (2I = L = 256)
-    ("sm_pairs", synth.LayerShape("sp", T=1200, d=256, L=256, E=16, K=2, I=128, S=1, Is=64)),
-    ("sm_pairs_wide", synth.LayerShape("spw", T=2400, d=256, L=256, E=16, K=2, I=128, S=1,
+    # the same loads over four weight tiles (2I = L = 512): with ~300 tokens per expert in two
+    # chunks of the 256 granule, weight tiles over SM pairs (two per SM), each SM holding half
+    # of a ragged chunk
+    ("sm_pairs", synth.LayerShape("sp", T=1200, d=256, L=512, E=16, K=2, I=256, S=1, Is=64)),
+    ("sm_pairs_wide", synth.LayerShape("spw", T=2400, d=256, L=512, E=16, K=2, I=256, S=1,
                                        Is=64)),
 ]
 
