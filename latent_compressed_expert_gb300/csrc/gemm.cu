@@ -773,6 +773,310 @@ bool make_tmap_bf16(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t col
   return r == CUDA_SUCCESS;
 }
 
+// ------------------------------------------------------------------------------------
+// Dense GEMM over an SM pair (tcgen05 cta_group::2).
+//
+// A cluster of two CTAs on two SMs computes a 256 x 256 output tile with MMAs of M = 256,
+// N = 256 issued by rank 0: rank r holds A's rows 128 r .. 128 r + 127 of the tile and B's
+// rows (output columns) 128 r .. 128 r + 127, and each MMA reads both CTAs' shared memory at
+// the same offsets.  Each CTA's TMEM receives its 128 output rows x all 256 columns, so an
+// accumulator set takes 256 columns and two fit: the epilogue drains tile i while the MMAs
+// of tile i + 1 run.  Per K-block an SM stages 16 KB of A and 16 KB of B for its 128 x 256 x
+// 64 share of the MMA -- the bytes per FLOP of a one-SM tile pair, whose accumulators take all
+// of TMEM and are drained while no MMA runs (12-16 % of the prefill GEMMs' time).  The
+// epilogue is the one-SM kernel's, row by row.
+//
+// Synchronisation (every wait bounded): full[s] of rank 0 completes when both CTAs' TMA bytes
+// for stage s have landed (rank 0's producer expects both; rank 1's copies complete on rank
+// 0's barrier); empty[s] and tfull[a] of both CTAs get one arrival each from rank 0's commits
+// (multicast); tempty[a] of rank 0 gets one arrival per epilogue warp of both CTAs; cluster
+// barriers bracket set-up and teardown, so that neither CTA leaves while its peer may still
+// signal its barriers or read its shared memory.
+constexpr int GEMM_PAIR_STAGES = 7;
+constexpr bool GEMM_SM_PAIR = true;  // the tile-pair GEMMs run over SM pairs
+
+struct GemmPairCfg {
+  static constexpr int BN = 256;                          // output columns per cluster tile
+  static constexpr int TM = 2 * BLOCK_M;                  // output rows per cluster tile
+  static constexpr int A_BYTES = BLOCK_M * BLOCK_K * 2;   // this CTA's 128 rows of A
+  static constexpr int B_BYTES = (BN / 2) * BLOCK_K * 2;  // this CTA's 128 rows of B
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;   // 32 KB
+  static constexpr int STAGES = GEMM_PAIR_STAGES;
+  static constexpr int TMEM_COLS = 512;                   // two accumulator sets of BN columns
+  static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
+  static constexpr int NUM_BARS = 2 * STAGES + 6;
+  static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
+  static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;  // + slack for 1024 alignment
+  static constexpr uint32_t IDESC = ptx::idesc_bf16_f32(TM, BN);
+  static_assert(2 * BN <= TMEM_COLS, "two accumulator sets fit TMEM");
+  static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "tiles must stay 1024-aligned");
+  static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+};
+
+// RP: the residual epilogue with its residual prefetched one chunk ahead (the output GEMM).
+template <bool RP>
+__global__ void __launch_bounds__(GEMM_THREADS, 1)
+gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                 const GemmArgs g) {
+  using C = GemmPairCfg;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = ptx::smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
+  uint64_t* empty = full + C::STAGES;
+  uint64_t* tfull = empty + C::STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint64_t* stall = drain + 1;  // never arrived on (fault-injection hook)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::MISC_OFF);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 4);
+
+  const uint32_t rank = ptx::cluster_ctarank();  // rank 0 issues the MMAs
+  const bool lead = rank == 0;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nt = (g.N + C::BN - 1) / C::BN;
+  const int mt = (g.M + C::TM - 1) / C::TM;
+  const int total = mt * nt;
+  const int nk = g.Kd / BLOCK_K;
+  const uint64_t limit = g.timeout_ns;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      ptx::mbar_init(&full[s], 1);  // rank 0's producer; the bytes come from both CTAs
+      ptx::mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      ptx::mbar_init(&tfull[a], 1);
+      ptx::mbar_init(&tempty[a], 2 * 4);  // lane 0 of the four epilogue warps of each CTA
+    }
+    ptx::mbar_init(drain, 1);
+    ptx::mbar_init(stall, 1);
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::prefetch_tmap(&tmA);
+    ptx::prefetch_tmap(&tmB);
+  }
+  ptx::cluster_sync();  // both CTAs' barriers exist before either signals the other's
+  if (warp == 1) {
+    ptx::tmem_alloc_pair(tmem_slot, C::TMEM_COLS);
+    ptx::tmem_relinquish_pair();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  pdl_wait();  // from here on: the previous kernel's outputs are visible
+  pdl_launch_dependents();
+  const int cid = static_cast<int>(ptx::cluster_id_x());
+  const int ncl = static_cast<int>(ptx::ncluster_x());
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ TMA producer (both ranks)
+      uint32_t it = 0;
+      bool ok = true;
+      for (int tile = cid; ok && tile < total; tile += ncl) {
+        const TileCoord tc = decode_tile<C::BN, C::TM>(g, nt, mt, tile);
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int s = static_cast<int>(it % C::STAGES);
+          const uint32_t ph = (it / C::STAGES) & 1u;
+          if (!ptx::mbar_wait(&empty[s], ph ^ 1u, abort_flag, limit)) {
+            raise_error(g, abort_flag, DEVERR_TIMEOUT_PRODUCER);
+            ok = false;
+            break;
+          }
+          uint8_t* sa = smem + s * C::STAGE_BYTES;
+          const uint32_t fb = ptx::mapa_shared(ptx::smem_u32(&full[s]), 0);
+          if (lead) ptx::mbar_arrive_expect_tx(&full[s], 2u * C::STAGE_BYTES);
+          // rows past M or N are zero-filled
+          ptx::tma_load_2d_pair(sa, &tmA, fb, kb * BLOCK_K,
+                                tc.a_row + static_cast<int>(rank) * BLOCK_M);
+          ptx::tma_load_2d_pair(sa + C::A_BYTES, &tmB, fb, kb * BLOCK_K,
+                                tc.b_row + static_cast<int>(rank) * (C::BN / 2));
+        }
+      }
+      // rank 0's last full phases cover both CTAs' last copies: they land before the pair exits
+      if (lead) {
+        const uint32_t first = it > static_cast<uint32_t>(C::STAGES) ? it - C::STAGES : 0u;
+        for (uint32_t j = first; j < it; ++j) {
+          if (!wait_drain(&full[j % C::STAGES], (j / C::STAGES) & 1u, limit)) {
+            raise_error(g, abort_flag, DEVERR_TIMEOUT_DRAIN);
+            break;
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && lead) {
+      // ------------------------------------------------------------ MMA issuer (rank 0)
+      uint32_t it = 0;
+      int lt = 0;
+      bool stalled = false;
+      if (g.inject_stall && !ptx::mbar_wait(stall, 0u, abort_flag, limit)) {
+        raise_error(g, abort_flag, DEVERR_TIMEOUT_MMA);
+        stalled = true;
+      }
+      for (int tile = cid; !stalled && tile < total; tile += ncl, ++lt) {
+        const int acc = lt & 1;
+        const uint32_t aph = static_cast<uint32_t>(lt >> 1) & 1u;
+        if (!ptx::mbar_wait(&tempty[acc], aph ^ 1u, abort_flag, limit)) {
+          raise_error(g, abort_flag, DEVERR_TIMEOUT_MMA);
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * C::BN);
+        bool ok = true;
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int s = static_cast<int>(it % C::STAGES);
+          const uint32_t ph = (it / C::STAGES) & 1u;
+          if (!ptx::mbar_wait(&full[s], ph, abort_flag, limit)) {
+            raise_error(g, abort_flag, DEVERR_TIMEOUT_MMA);
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t sa = ptx::smem_u32(smem + s * C::STAGE_BYTES);
+          const uint32_t sb = sa + C::A_BYTES;
+#pragma unroll
+          for (int k = 0; k < BLOCK_K / 16; ++k)
+            ptx::umma_bf16_pair(d_tmem, ptx::smem_desc_sw128(sa + k * 32),
+                                ptx::smem_desc_sw128(sb + k * 32), C::IDESC,
+                                (kb | k) != 0 ? 1u : 0u);
+          ptx::umma_commit_pair(&empty[s], 0x3);
+        }
+        if (!ok) break;
+        ptx::umma_commit_pair(&tfull[acc], 0x3);
+      }
+      // all MMAs issued by this thread complete before TMEM is released
+      ptx::umma_commit_pair(drain, 0x1);
+      if (!wait_drain(drain, 0u, limit)) raise_error(g, abort_flag, DEVERR_TIMEOUT_DRAIN);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue (warps 2..5, both
+    // ranks): a thread owns one of this CTA's 128 output rows and walks the tile's 256 columns
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const float c = g.c, inv_c = 1.0f / g.c;
+    const uint32_t tempty_lead0 = ptx::mapa_shared(ptx::smem_u32(&tempty[0]), 0);
+    const uint32_t tempty_lead1 = ptx::mapa_shared(ptx::smem_u32(&tempty[1]), 0);
+    int lt = 0;
+    for (int tile = cid; tile < total; tile += ncl, ++lt) {
+      const int acc = lt & 1;
+      const uint32_t aph = static_cast<uint32_t>(lt >> 1) & 1u;
+      const TileCoord tc = decode_tile<C::BN, C::TM>(g, nt, mt, tile);
+      const bool got = ptx::mbar_wait(&tfull[acc], aph, abort_flag, limit);
+      if (!__all_sync(0xffffffffu, got)) {
+        if (lane == 0) raise_error(g, abort_flag, DEVERR_TIMEOUT_EPILOGUE);
+        break;
+      }
+      ptx::tc_fence_after();
+      const int row = tc.a_row + static_cast<int>(rank) * BLOCK_M + q * 32 + lane;
+      const bool row_ok = row < g.M;
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                             static_cast<uint32_t>(acc * C::BN);
+      if constexpr (RP) {
+        // whole 32-column chunks (the launcher sets RP only for N a multiple of 256): chunk
+        // ch + 1's residual is loaded before chunk ch's accumulator columns are read
+        const uint4* rrow = reinterpret_cast<const uint4*>(
+            g.resid + static_cast<size_t>(row_ok ? row : 0) * g.ldr + tc.n0);
+        uint4 rnext[4];
+        if (row_ok) {
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) rnext[q4] = __ldg(rrow + q4);
+        }
+#pragma unroll 1
+        for (int ch = 0; ch < C::BN / 32; ++ch) {
+          uint4 rcur[4];
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) rcur[q4] = rnext[q4];
+          if (row_ok && ch + 1 < C::BN / 32) {
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) rnext[q4] = __ldg(rrow + 4 * (ch + 1) + q4);
+          }
+          float v[32];
+          ptx::tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(ch * 32), v);
+          if (row_ok) store_resid_prefetched(g, row, tc.n0 + ch * 32, v, rcur);
+        }
+      } else {
+#pragma unroll 1
+        for (int ch = 0; ch < C::BN / 32; ++ch) {
+          const int col0 = tc.n0 + ch * 32;
+          if (col0 >= g.N) break;  // uniform across the warp
+          float v[32];
+          ptx::tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(ch * 32), v);
+          if (row_ok) {
+            if (col0 + 32 <= g.N)
+              epilogue_store(g, row, col0, v, c, inv_c);
+            else
+              epilogue_store_partial(g, row, col0, g.N - col0, v);
+          }
+        }
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if (lead)
+          ptx::mbar_arrive(&tempty[acc]);
+        else
+          ptx::mbar_arrive_cluster(acc == 0 ? tempty_lead0 : tempty_lead1);
+      }
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::cluster_sync();  // the peer is done with this CTA's barriers, shared memory and TMEM
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
+  }
+}
+
+// tb: B's tensor map with 128-row boxes (each CTA of a pair loads half of a tile's columns).
+template <bool RP>
+static int launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& g,
+                       cudaStream_t stream) {
+  using C = GemmPairCfg;
+  auto kernel = gemm_pair_kernel<RP>;
+  if (g.groups > 0 || g.ksplit > 1) return LMOE_ERR_INVALID_ARG;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           C::SMEM_BYTES) != cudaSuccess)
+    return LMOE_ERR_CUDA;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return LMOE_ERR_CUDA;
+  int pairs = sms / 2;
+  if (g.max_ctas > 0 && g.max_ctas / 2 < pairs) pairs = g.max_ctas / 2 > 0 ? g.max_ctas / 2 : 1;
+  const int64_t tiles = ceil_div(g.M, C::TM) * ceil_div(g.N, C::BN);
+  if (tiles < pairs) pairs = static_cast<int>(tiles);
+  if (pairs <= 0) return LMOE_OK;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * pairs);
+  cfg.blockDim = dim3(GEMM_THREADS);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  // a persistent grid: no more pairs than can be resident at once (an SM pair shares a GPC)
+  int active = 0;
+  if (cudaOccupancyMaxActiveClusters(&active, kernel, &cfg) == cudaSuccess && active > 0 &&
+      active < pairs) {
+    pairs = active;
+    cfg.gridDim = dim3(2 * pairs);
+  }
+  return cudaLaunchKernelEx(&cfg, kernel, ta, tb, g) == cudaSuccess ? LMOE_OK : LMOE_ERR_CUDA;
+}
+
 template <int BN, int MT, bool RP = false>
 static int launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& g,
                      cudaStream_t stream) {
@@ -874,6 +1178,14 @@ int launch_gemm(const void* A, uint64_t a_rows, int a_ld, const void* B, uint64_
                      ceil_div(g.M, 2 * BLOCK_M) * ceil_div(g.N, bn) >= 2 * static_cast<int64_t>(sms);
   // the output GEMM: residual epilogue over whole 256-column tiles
   const bool rp = g.epi == EPI_RESID && g.resid != nullptr && g.N % 256 == 0;
+  if (GEMM_SM_PAIR && bn == 256 && pairs) {
+    // over SM pairs (gemm_pair_kernel): each CTA loads 128 of a tile's 256 B rows
+    CUtensorMap tb128;
+    if (!make_tmap_bf16(&tb128, B, b_rows, static_cast<uint64_t>(g.Kd),
+                        static_cast<uint64_t>(b_ld), GemmPairCfg::BN / 2))
+      return LMOE_ERR_CUDA;
+    return rp ? launch_pair<true>(ta, tb128, g, stream) : launch_pair<false>(ta, tb128, g, stream);
+  }
   if (bn == 256 && pairs && rp) return launch_bn<256, 2, true>(ta, tb, g, stream);
   if (bn == 256)
     return pairs ? launch_bn<256, 2>(ta, tb, g, stream) : launch_bn<256, 1>(ta, tb, g, stream);

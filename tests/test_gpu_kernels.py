@@ -28,6 +28,9 @@ def dev():
                                    # tile pairs (two M-tiles per CTA), 256- and 128-wide tiles;
                                    # M ragged, the last pair's second tile wholly past M
                                    (20000, 3584, 2048), (26000, 384, 2048),
+                                   # 256 x 256 tiles over SM pairs with N ragged: the last
+                                   # tile's 16 valid columns all in rank 0's half of B
+                                   (20000, 2832, 2048),
                                    # 224-wide tiles (N = 896 and 672), single and paired
                                    (8192, 896, 3584), (300, 672, 512), (20000, 896, 2048)])
 def test_gemm_matches_float64(dev, M, N, K):
