@@ -74,7 +74,14 @@ struct GroupedCfg {
   static constexpr int BAR_OFF = EPI_OFF + EPI_BYTES;
   static constexpr int NUM_BARS = 2 * STAGES + 5;
   static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
-  static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;
+  // copies of the chunk prefix sum and the expert segment offsets (E + 1 entries each) in
+  // whatever shared memory is left: when both fit, the tile decode's binary search costs
+  // shared-memory latency instead of 2-3 K cycles of dependent global loads per tile
+  static constexpr int TAB_OFF = MISC_OFF + 16;
+  static constexpr int TAB_ROOM = (232448 - 1024 - TAB_OFF) / 8;
+  static constexpr int TAB_CAP = TAB_ROOM < 2048 ? TAB_ROOM : 2048;  // entries per table
+  static constexpr int SMEM_BYTES = TAB_OFF + TAB_CAP * 8 + 1024;
+  static_assert(TAB_CAP >= 0, "shared memory budget");
   static_assert(MW == 1 || MW == 2, "one or two weight tiles");
   static_assert(TOKN % BOX_T == 0 && TOKN % 16 == 0 && TOKN <= 256, "UMMA N range");
   static_assert(TOKN <= ACC_COLS && ACC * MW * ACC_COLS <= TMEM_COLS, "accumulators fit TMEM");
@@ -249,7 +256,22 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
   const uint32_t tmem_base = *tmem_slot;
   pdl_wait();  // from here on: the previous kernel's outputs (segments, rows) are visible
   pdl_launch_dependents();
-  const int total = __ldg(g.ct_off + g.E) * ((mt + MW - 1) / MW);
+  int32_t* tab = reinterpret_cast<int32_t*>(smem + C::TAB_OFF);
+  const bool tab_smem = g.E < C::TAB_CAP;  // both tables' E + 1 entries fit
+  if (tab_smem) {
+    for (int i = threadIdx.x; i <= g.E; i += blockDim.x) {
+      tab[i] = __ldg(g.ct_off + i);
+      tab[C::TAB_CAP + i] = __ldg(g.seg_off + i);
+    }
+    __syncthreads();
+  }
+  auto decode = [&](int tile) {
+    return decode_gtile_with<MW>(g, mt, tile, [&](int which, int i) {
+      return tab_smem ? tab[which * C::TAB_CAP + i]
+                      : __ldg((which == 0 ? g.ct_off : g.seg_off) + i);
+    });
+  };
+  const int total = (tab_smem ? tab[g.E] : __ldg(g.ct_off + g.E)) * ((mt + MW - 1) / MW);
 
   if (warp == 0) {
     if (lane == 0) {
@@ -258,7 +280,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
       uint32_t it = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-        const GTile t = decode_gtile<MW>(g, mt, tile);
+        const GTile t = decode(tile);
         const int nbox = g.gather ? 0 : t.npad / C::BOX_T;
         const uint32_t bytes = static_cast<uint32_t>(t.nw) * C::A_BYTES +
                                static_cast<uint32_t>(nbox) * C::BOX_T * BLOCK_K * 2;
@@ -307,7 +329,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
       uint32_t it = 0;
       int lt = 0;
       for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++lt) {
-        const GTile t = decode_gtile<MW>(g, mt, tile);
+        const GTile t = decode(tile);
         const uint32_t idesc = FP8 ? ptx::idesc_e4m3_f32(BLOCK_M, t.npad)
                                    : ptx::idesc_bf16_f32(BLOCK_M, t.npad);
         const int acc = C::ACC == 2 ? (lt & 1) : 0;
@@ -368,7 +390,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
       uint32_t it = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-        const GTile t = decode_gtile<MW>(g, mt, tile);
+        const GTile t = decode(tile);
         const __nv_bfloat16* src[J];
 #pragma unroll
         for (int j = 0; j < J; ++j) {
@@ -415,7 +437,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
                                        : (static_cast<uint32_t>(lt) & 1u);
       // the tile and, with fp8, its scales are fetched before the accumulator is ready, so
       // their load latency hides under the tile's MMAs
-      const GTile t = decode_gtile<MW>(g, mt, tile);
+      const GTile t = decode(tile);
       constexpr int NCH = C::TOKN / 32;    // token chunks of a tile
       float w_s[MW];                       // this thread's weight row scale, per weight tile
       float x_s[NCH];                      // lane l: scale of token 32 c + l of the tile
