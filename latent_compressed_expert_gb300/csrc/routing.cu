@@ -656,6 +656,115 @@ thresholds_regs_kernel(const float* __restrict__ z, int T, int64_t stride_t, int
   if (threadIdx.x == 0) tau[e] = __uint_as_float(result);
 }
 
+// The bound-and-select form for columns of up to THR_THREADS * THR_KPT = 32768 tokens and
+// k <= THR_THREADS: one CTA of 1024 threads per expert, thread i holding the scores of tokens
+// i, i + 1024, ... in registers.  B, the k-th largest of the threads' maxima, bounds the k-th
+// largest score from below; at the fair-share rank ~2.6 % of a column's scores exceed it (the
+// skewed workload: ~850 of 32768 for k = 585), so the second bit search runs over at most
+// THW_BCAND candidates, a few per thread, with one barrier per bit instead of a block-wide
+// reduction of 32 keys per thread.  More than THW_BCAND scores > B: the bit search over the
+// registers, as in thresholds_regs_kernel.
+constexpr int THW_BCAND = 4096;
+static_assert(THW_BCAND % THR_THREADS == 0, "candidate slots per thread");
+
+template <bool SCORES>
+__global__ void __launch_bounds__(THR_THREADS, 1)
+thresholds_wide_kernel(const float* __restrict__ z, int T, int64_t stride_t, int64_t stride_e,
+                       int k, float* __restrict__ tau) {
+  __shared__ uint32_t cand[THW_BCAND];
+  __shared__ uint32_t wsum[2][THR_THREADS / 32];
+  __shared__ uint32_t total[2];
+  __shared__ uint32_t ncand;
+  pdl_wait();
+  pdl_launch_dependents();
+  const int e = blockIdx.x;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const float* col = z + static_cast<int64_t>(e) * stride_e;
+  if (threadIdx.x == 0) ncand = 0u;
+  uint32_t key[THR_KPT];
+#pragma unroll
+  for (int i = 0; i < THR_KPT; ++i) {  // every load in flight before any score is computed
+    const int t = static_cast<int>(threadIdx.x) + i * THR_THREADS;
+    key[i] = t < T ? __float_as_uint(__ldg(col + t * stride_t)) : 0u;
+  }
+  uint32_t mx = 0u;
+#pragma unroll
+  for (int i = 0; i < THR_KPT; ++i) {
+    const int t = static_cast<int>(threadIdx.x) + i * THR_THREADS;
+    key[i] = t < T ? __float_as_uint(score_of<SCORES>(__uint_as_float(key[i]))) : 0u;
+    mx = key[i] > mx ? key[i] : mx;
+  }
+  // B = the k-th largest of the threads' maxima
+  uint32_t bound = 0u;
+#pragma unroll 1
+  for (int b = 29; b >= 0; --b) {
+    const uint32_t v = bound | (1u << b);
+    if (__syncthreads_count(mx >= v) >= k) bound = v;
+  }
+  // scores > B: a warp scan of the threads' counts, one shared atomic per warp
+  int cnt = 0;
+#pragma unroll
+  for (int i = 0; i < THR_KPT; ++i) cnt += key[i] > bound ? 1 : 0;
+  int incl = cnt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  uint32_t base = 0u;
+  if (lane == 31) base = atomicAdd(&ncand, static_cast<uint32_t>(incl));
+  base = __shfl_sync(0xffffffffu, base, 31) + static_cast<uint32_t>(incl - cnt);
+  __syncthreads();
+  const uint32_t n = ncand;  // block-uniform
+  uint32_t result = bound;
+  if (n >= static_cast<uint32_t>(k) && n <= static_cast<uint32_t>(THW_BCAND)) {
+    uint32_t p = base;
+#pragma unroll
+    for (int i = 0; i < THR_KPT; ++i)
+      if (key[i] > bound) cand[p++] = key[i];
+    __syncthreads();
+    constexpr int SLOTS = THW_BCAND / THR_THREADS;
+    const int used = (static_cast<int>(n) + THR_THREADS - 1) / THR_THREADS;  // block-uniform
+    uint32_t cv[SLOTS];
+#pragma unroll
+    for (int j = 0; j < SLOTS; ++j) {
+      const uint32_t q = threadIdx.x + j * THR_THREADS;
+      cv[j] = q < n ? cand[q] : 0u;
+    }
+    result = 0u;
+#pragma unroll 1
+    for (int b = 29; b >= 0; --b) {
+      const uint32_t v = result | (1u << b);
+      int c = 0;
+#pragma unroll
+      for (int j = 0; j < SLOTS; ++j)
+        if (j < used) c += __syncthreads_count(cv[j] >= v);
+      if (c >= k) result = v;
+    }
+  } else if (n > static_cast<uint32_t>(THW_BCAND)) {
+    // the whole column's bit search over the registers (block-uniform branch)
+    result = 0u;
+#pragma unroll 1
+    for (int b = 29; b >= 0; --b) {
+      const uint32_t v = result | (1u << b);
+      uint32_t c = 0u;
+#pragma unroll
+      for (int i = 0; i < THR_KPT; ++i) c += key[i] >= v ? 1u : 0u;
+      c = __reduce_add_sync(0xffffffffu, c);
+      const int par = b & 1;
+      if (lane == 0) wsum[par][warp] = c;
+      __syncthreads();
+      if (warp == 0) {
+        const uint32_t sum = __reduce_add_sync(0xffffffffu, wsum[par][lane]);
+        if (lane == 0) total[par] = sum;
+      }
+      __syncthreads();
+      if (total[par] >= static_cast<uint32_t>(k)) result = v;
+    }
+  }
+  if (threadIdx.x == 0) tau[e] = __uint_as_float(result);
+}
+
 // Threshold candidates of one batch: column e of cand ([k, E], row stride ldc) receives the
 // logits of the min(k, T) tokens with the largest scores of expert e -- first those whose
 // score is above the min(k, T)-th largest, then tokens whose score equals it, both in token
@@ -825,6 +934,14 @@ int launch_thresholds(const float* z, int T, int E, int64_t stride_t, int64_t st
                              static_cast<int>(smem)) != cudaSuccess)
       return LMOE_ERR_CUDA;
     return launch_pdl(kern, E, TH_THREADS, smem, stream, z, T, stride_t, stride_e, k, tau) ==
+                   cudaSuccess
+               ? LMOE_OK
+               : LMOE_ERR_CUDA;
+  }
+  if (T <= THR_THREADS * THR_KPT && k <= THR_THREADS) {
+    // bound-and-select with 1024 threads: up to 32768 tokens, k <= 1024
+    auto kern = scores ? thresholds_wide_kernel<true> : thresholds_wide_kernel<false>;
+    return launch_pdl(kern, E, THR_THREADS, 0, stream, z, T, stride_t, stride_e, k, tau) ==
                    cudaSuccess
                ? LMOE_OK
                : LMOE_ERR_CUDA;

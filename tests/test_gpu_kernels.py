@@ -98,7 +98,27 @@ THRESH_CASES = [(64, 16, 4, 0), (8192, 896, 16, 0), (32768, 896, 16, 0), (40000,
                 (100, 32, 4, 1), (100, 32, 4, 100), (7, 16, 16, 0), (1, 896, 16, 0),
                 (3000, 448, 8, 0), (5000, 64, 4, 256), (5000, 64, 4, 257), (8193, 896, 16, 0),
                 # the register-resident bit search (T <= 32768, any rank): the extremes of k
-                (32768, 16, 16, 32768), (12345, 48, 8, 1), (20000, 32, 4, 4096)]
+                (32768, 16, 16, 32768), (12345, 48, 8, 1), (20000, 32, 4, 4096),
+                # the 1024-thread bound-and-select form: ~3600 candidates, four per thread
+                (32768, 64, 4, 1000)]
+
+
+def test_thresholds_many_scores_above_the_bound(dev, oracle_mod):
+    """T = 32768 tokens, k = 1000: token t is held by thread t % 1024 of the 1024-thread
+    selection.  Lifting the tokens of a few threads far above the rest puts the bound B (the
+    k-th largest of the threads' maxima) low in the remaining threads' range.  Column 1 (100
+    threads lifted) has ~6600 scores above B, past the 4096 candidates, so the selection falls
+    back to the bit search over its registers; column 0 (24 threads) has ~4090, all four
+    candidate slots of a thread in use; column 2 (none) ~3800."""
+    T, E, k = 32768, 3, 1000
+    g = torch.Generator().manual_seed(77)
+    lg = torch.randn(T, E, generator=g) * 0.1
+    t = torch.arange(T)
+    lg[(t % 1024) < 24, 0] += 8.0
+    lg[(t % 1024) < 100, 1] += 6.0
+    tau = lmoe.thresholds(lg.to(dev), 4, k)
+    ref = oracle_mod.thresholds(lg.numpy(), k)
+    assert np.array_equal(tau.cpu().numpy().view(np.int32), ref.view(np.int32))
 
 
 @pytest.mark.parametrize("T,E,K,k_rank", THRESH_CASES)
