@@ -31,6 +31,8 @@ def dev():
                                    # 256 x 256 tiles over SM pairs with N ragged: the last
                                    # tile's 16 valid columns all in rank 0's half of B
                                    (20000, 2832, 2048),
+                                   # the same with GEMM 1's reduction length (K = 7168)
+                                   (8192, 2560, 7168),
                                    # 224-wide tiles (N = 896 and 672), single and paired
                                    (8192, 896, 3584), (300, 672, 512), (20000, 896, 2048)])
 def test_gemm_matches_float64(dev, M, N, K):
