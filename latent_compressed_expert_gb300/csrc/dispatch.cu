@@ -48,13 +48,13 @@ dispatch_mask_kernel(const int32_t* __restrict__ idx, int T, int E, int K,
 }
 
 // Column scan: base[b][e] = picks of expert e in blocks < b, and the expert's count.  A CTA
-// owns 32 experts (one per lane, so every mask row is read as one 128-byte line); its 8 warps
+// owns 32 experts (one per lane, so every mask row is read as one 128-byte line); its 16 warps
 // split the blocks into strips: each thread sums its strip, the strips' sums are scanned
 // across the warps, and a second pass over the strip writes the bases.  The counts go to
 // offsets[e]; the last CTA to finish (a fence and an atomic counter that the mask kernel
 // zeroed, no waiting) turns them into the exclusive scans offsets (rows) and ct_off (token
 // chunks of the routed-expert GEMMs, ceil(count / tokn)).
-constexpr int SCAN_WARPS = 8;
+constexpr int SCAN_WARPS = 16;
 constexpr int SCAN_THREADS = SCAN_WARPS * 32;
 
 __global__ void __launch_bounds__(SCAN_THREADS)

@@ -795,12 +795,13 @@ bool make_tmap_bf16(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t col
 constexpr int GEMM_PAIR_STAGES = 7;
 constexpr bool GEMM_SM_PAIR = true;  // the tile-pair GEMMs run over SM pairs
 
+template <int BN_>
 struct GemmPairCfg {
-  static constexpr int BN = 256;                          // output columns per cluster tile
+  static constexpr int BN = BN_;                          // output columns per cluster tile
   static constexpr int TM = 2 * BLOCK_M;                  // output rows per cluster tile
   static constexpr int A_BYTES = BLOCK_M * BLOCK_K * 2;   // this CTA's 128 rows of A
   static constexpr int B_BYTES = (BN / 2) * BLOCK_K * 2;  // this CTA's 128 rows of B
-  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;   // 32 KB
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;   // 32 KB (BN = 256) or 30 KB
   static constexpr int STAGES = GEMM_PAIR_STAGES;
   static constexpr int TMEM_COLS = 512;                   // two accumulator sets of BN columns
   static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
@@ -808,17 +809,18 @@ struct GemmPairCfg {
   static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
   static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;  // + slack for 1024 alignment
   static constexpr uint32_t IDESC = ptx::idesc_bf16_f32(TM, BN);
-  static_assert(2 * BN <= TMEM_COLS, "two accumulator sets fit TMEM");
+  static_assert(BN % 32 == 0 && BN <= 256 && 2 * BN <= TMEM_COLS, "two accumulator sets fit TMEM");
   static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "tiles must stay 1024-aligned");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
 
-// RP: the residual epilogue with its residual prefetched one chunk ahead (the output GEMM).
-template <bool RP>
+// BN: 256, or 224 (the router over 896 experts: four whole column tiles).  RP: the residual
+// epilogue with its residual prefetched one chunk ahead (the output GEMM).
+template <int BN, bool RP>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
 gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const GemmArgs g) {
-  using C = GemmPairCfg;
+  using C = GemmPairCfg<BN>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = ptx::smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -1034,12 +1036,12 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
   }
 }
 
-// tb: B's tensor map with 128-row boxes (each CTA of a pair loads half of a tile's columns).
-template <bool RP>
+// tb: B's tensor map with BN / 2-row boxes (each CTA of a pair loads half of a tile's columns).
+template <int BN, bool RP>
 static int launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& g,
                        cudaStream_t stream) {
-  using C = GemmPairCfg;
-  auto kernel = gemm_pair_kernel<RP>;
+  using C = GemmPairCfg<BN>;
+  auto kernel = gemm_pair_kernel<BN, RP>;
   if (g.groups > 0 || g.ksplit > 1) return LMOE_ERR_INVALID_ARG;
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            C::SMEM_BYTES) != cudaSuccess)
@@ -1180,11 +1182,22 @@ int launch_gemm(const void* A, uint64_t a_rows, int a_ld, const void* B, uint64_
   const bool rp = g.epi == EPI_RESID && g.resid != nullptr && g.N % 256 == 0;
   if (GEMM_SM_PAIR && bn == 256 && pairs) {
     // over SM pairs (gemm_pair_kernel): each CTA loads 128 of a tile's 256 B rows
-    CUtensorMap tb128;
-    if (!make_tmap_bf16(&tb128, B, b_rows, static_cast<uint64_t>(g.Kd),
-                        static_cast<uint64_t>(b_ld), GemmPairCfg::BN / 2))
+    CUtensorMap tbh;
+    if (!make_tmap_bf16(&tbh, B, b_rows, static_cast<uint64_t>(g.Kd),
+                        static_cast<uint64_t>(b_ld), 128))
       return LMOE_ERR_CUDA;
-    return rp ? launch_pair<true>(ta, tb128, g, stream) : launch_pair<false>(ta, tb128, g, stream);
+    return rp ? launch_pair<256, true>(ta, tbh, g, stream)
+              : launch_pair<256, false>(ta, tbh, g, stream);
+  }
+  // 224-wide tiles (the router) over SM pairs once every SM pair has a tile: a single M-tile's
+  // 128 x 224 tile stages 44 KB per K-block for 448 MMA cycles on its SM, a pair's half 30 KB
+  if (GEMM_SM_PAIR && bn == 224 && g.Kd >= GEMM_PAIR_MIN_K &&
+      ceil_div(g.M, 2 * BLOCK_M) * ceil_div(g.N, bn) >= static_cast<int64_t>(sms) / 2) {
+    CUtensorMap tbh;
+    if (!make_tmap_bf16(&tbh, B, b_rows, static_cast<uint64_t>(g.Kd),
+                        static_cast<uint64_t>(b_ld), 112))
+      return LMOE_ERR_CUDA;
+    return launch_pair<224, false>(ta, tbh, g, stream);
   }
   if (bn == 256 && pairs && rp) return launch_bn<256, 2, true>(ta, tb, g, stream);
   if (bn == 256)
