@@ -70,3 +70,31 @@ def test_forward_replays_from_a_cuda_graph(dev, T):
         torch.cuda.synchronize()
         assert layer.device_error() == 0
         assert torch.equal(y.view(torch.int16), ref.view(torch.int16))
+
+
+def test_cluster_kernels_replay_from_a_cuda_graph(dev):
+    """The same at a size where the dense GEMMs and the down GEMM run over SM pairs (clusters of
+    two CTAs, launched with a cluster dimension): 8192 tokens, d = 2048, 1024 tokens per expert
+    in 256-token chunks.  Each replay gives the eager call's bits."""
+    sh = synth.LayerShape("pairgraph", T=8192, d=2048, L=2048, E=16, K=2, I=256, S=1, Is=256)
+    w = synth.make_weights(sh, seed=65, device=dev)
+    layer = lmoe.Layer(sh, w)
+    x = synth.make_x(sh, seed=66, device=dev)
+    ref = layer.forward(x, residual=x).clone()
+    torch.cuda.synchronize()
+    y = torch.empty_like(x)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        layer.forward(x, residual=x, y=y)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        layer.forward(x, residual=x, y=y)
+    for _ in range(2):
+        y.fill_(0)
+        graph.replay()
+        torch.cuda.synchronize()
+        assert layer.device_error() == 0
+        assert torch.equal(y.view(torch.int16), ref.view(torch.int16))
