@@ -126,6 +126,7 @@ WorkspaceLayout workspace_layout(const lmoe_dims& D) {
   W.base = take(nb * D.E * 4);
   W.offsets = take((static_cast<size_t>(D.E) + 1) * 4);
   W.ct_off = take((static_cast<size_t>(D.E) + 1) * 4);
+  W.ct_off_gu = take((static_cast<size_t>(D.E) + 1) * 4);
   W.inv = take(TK * 4);
   W.src_tok = take(TK * 4);
   W.h = take(TK * D.I * 2);
@@ -1106,9 +1107,12 @@ int lmoe_forward(const lmoe_dims* dims, const void* packed, const void* x, const
   int32_t* inv = reinterpret_cast<int32_t*>(ws + W.inv);
   int32_t* src_tok = reinterpret_cast<int32_t*>(ws + W.src_tok);
   const int tokn = grouped_tokn(T, D.K, D.E);
+  // the gate/value GEMM's own chunks when the batch's are wider
+  int32_t* ct_off_gu = tokn != GROUPED_TOKN ? reinterpret_cast<int32_t*>(ws + W.ct_off_gu) : ct_off;
   rc = launch_dispatch(idx, T, D.E, D.K, reinterpret_cast<uint32_t*>(ws + W.masks),
-                       reinterpret_cast<uint32_t*>(ws + W.base), offsets, ct_off, tokn, inv,
-                       src_tok, opt.counts_out, err, stream);
+                       reinterpret_cast<uint32_t*>(ws + W.base), offsets, ct_off, tokn,
+                       tokn != GROUPED_TOKN ? ct_off_gu : nullptr, GROUPED_TOKN, inv, src_tok,
+                       opt.counts_out, err, stream);
   if (rc != LMOE_OK) return rc;
   if (opt.load_stats) {
     rc = launch_load_stats(nullptr, offsets, D.E, opt.load_stats, stream);
@@ -1126,7 +1130,7 @@ int lmoe_forward(const lmoe_dims* dims, const void* packed, const void* x, const
     g.M_w = 2 * D.I;
     g.Kd = D.L;
     g.seg_off = offsets;
-    g.ct_off = ct_off;
+    g.ct_off = ct_off_gu;
     g.gather = src_tok;
     g.x = lat;
     g.ldx = D.L;
@@ -1154,7 +1158,7 @@ int lmoe_forward(const lmoe_dims* dims, const void* packed, const void* x, const
     g.timeout_ns = wait_limit_ns();
     g.max_ctas = routed_ctas;
     g.mean_tokens = static_cast<int>(static_cast<int64_t>(TK) / D.E);
-    g.tokn = tokn;
+    g.tokn = GROUPED_TOKN;
     rc = launch_grouped_gemm(pk + P.wgu, xop, static_cast<uint64_t>(T), D.L, g, stream);
     if (rc != LMOE_OK) return rc;
   }

@@ -41,7 +41,9 @@ constexpr int GROUPED_TOKN = 192;
 constexpr int GROUPED_TOKN_WIDE = 256;
 
 // The chunk size of a batch, a function of its dims only, so that the forward and the
-// backward, which reads the forward's chunk offsets, agree.
+// backward, which reads the forward's chunk offsets, agree.  The forward's gate/value GEMM
+// always takes GROUPED_TOKN chunks (its own prefix sum when the batch's are wider): with ~585
+// tokens per expert, 192-token chunks speed it up (3.40 -> 3.30 ms) but slow the down GEMM.
 inline int grouped_tokn(int64_t T, int K, int E) {
   return E > 0 && T * K / E > GROUPED_TOKN ? GROUPED_TOKN_WIDE : GROUPED_TOKN;
 }

@@ -60,10 +60,10 @@ constexpr int SCAN_THREADS = SCAN_WARPS * 32;
 __global__ void __launch_bounds__(SCAN_THREADS)
 dispatch_scan_kernel(const uint32_t* __restrict__ masks, int nb, int E,
                      uint32_t* __restrict__ base, int32_t* __restrict__ offsets,
-                     int32_t* __restrict__ ct_off, int tokn,
-                     int32_t* __restrict__ counts_out, uint32_t* __restrict__ done) {
+                     int32_t* __restrict__ ct_off, int tokn, int32_t* __restrict__ ct_off2,
+                     int tokn2, int32_t* __restrict__ counts_out, uint32_t* __restrict__ done) {
   __shared__ uint32_t part[SCAN_WARPS][32];
-  __shared__ int32_t wsum[2][SCAN_WARPS];
+  __shared__ int32_t wsum[3][SCAN_WARPS];
   __shared__ bool last;
   pdl_wait();
   pdl_launch_dependents();
@@ -104,33 +104,40 @@ dispatch_scan_kernel(const uint32_t* __restrict__ masks, int nb, int E,
   __threadfence();
   const int eper = (E + SCAN_THREADS - 1) / SCAN_THREADS;
   const int e0 = threadIdx.x * eper, e1 = min(E, e0 + eper);
-  int32_t c_rows = 0, c_chunks = 0;
+  const bool two = ct_off2 != nullptr;
+  int32_t c_rows = 0, c_chunks = 0, c_chunks2 = 0;
   for (int i = e0; i < e1; ++i) {
     const int32_t c = __ldcg(offsets + i);
     c_rows += c;
     c_chunks += static_cast<int32_t>(ceil_div(c, tokn));
+    if (two) c_chunks2 += static_cast<int32_t>(ceil_div(c, tokn2));
   }
-  int32_t ir = c_rows, ic = c_chunks;  // inclusive scans within the warp
+  int32_t ir = c_rows, ic = c_chunks, ic2 = c_chunks2;  // inclusive scans within the warp
   for (int o = 1; o < 32; o <<= 1) {
     const int32_t vr = __shfl_up_sync(0xffffffffu, ir, o);
     const int32_t vc = __shfl_up_sync(0xffffffffu, ic, o);
+    const int32_t vc2 = __shfl_up_sync(0xffffffffu, ic2, o);
     if (lane >= o) {
       ir += vr;
       ic += vc;
+      ic2 += vc2;
     }
   }
   if (lane == 31) {
     wsum[0][warp] = ir;
     wsum[1][warp] = ic;
+    wsum[2][warp] = ic2;
   }
   __syncthreads();
-  int32_t pr = ir - c_rows, pc = ic - c_chunks;
-  int32_t tr = 0, tc = 0;
+  int32_t pr = ir - c_rows, pc = ic - c_chunks, pc2 = ic2 - c_chunks2;
+  int32_t tr = 0, tc = 0, tc2 = 0;
   for (int w = 0; w < SCAN_WARPS; ++w) {
     pr += w < warp ? wsum[0][w] : 0;
     pc += w < warp ? wsum[1][w] : 0;
+    pc2 += w < warp ? wsum[2][w] : 0;
     tr += wsum[0][w];
     tc += wsum[1][w];
+    tc2 += wsum[2][w];
   }
   // every count was read above: the exclusive scans overwrite them in place
   __syncthreads();
@@ -140,10 +147,15 @@ dispatch_scan_kernel(const uint32_t* __restrict__ masks, int nb, int E,
     ct_off[i] = pc;
     pr += c;
     pc += static_cast<int32_t>(ceil_div(c, tokn));
+    if (two) {
+      ct_off2[i] = pc2;
+      pc2 += static_cast<int32_t>(ceil_div(c, tokn2));
+    }
   }
   if (threadIdx.x == 0) {
     offsets[E] = tr;  // == T*K when every index was valid
     ct_off[E] = tc;
+    if (two) ct_off2[E] = tc2;
   }
 }
 
@@ -500,9 +512,10 @@ combine_rounds_kernel(const __nv_bfloat16* __restrict__ o, const float* __restri
 
 // ------------------------------------------------------------------------------------
 int launch_dispatch(const int32_t* idx, int T, int E, int K, uint32_t* masks, uint32_t* base,
-                    int32_t* offsets, int32_t* ct_off, int tokn, int32_t* inv,
-                    int32_t* src_tok, int32_t* counts_out, uint32_t* err, cudaStream_t stream) {
-  if (tokn < 1) return LMOE_ERR_INVALID_ARG;
+                    int32_t* offsets, int32_t* ct_off, int tokn, int32_t* ct_off2, int tokn2,
+                    int32_t* inv, int32_t* src_tok, int32_t* counts_out, uint32_t* err,
+                    cudaStream_t stream) {
+  if (tokn < 1 || (ct_off2 && tokn2 < 1)) return LMOE_ERR_INVALID_ARG;
   const int nb = static_cast<int>(ceil_div(T, DISPATCH_TOKENS));
   const size_t msmem = static_cast<size_t>(E) * sizeof(uint32_t);
   uint32_t* done = err + 1;  // the word after the error flag
@@ -514,7 +527,8 @@ int launch_dispatch(const int32_t* idx, int T, int E, int K, uint32_t* masks, ui
     return LMOE_ERR_CUDA;
   }
   if (launch_pdl(dispatch_scan_kernel, static_cast<unsigned>(ceil_div(E, 32)), SCAN_THREADS, 0,
-                 stream, masks, nb, E, base, offsets, ct_off, tokn, counts_out, done) !=
+                 stream, masks, nb, E, base, offsets, ct_off, tokn, ct_off2, tokn2, counts_out,
+                 done) !=
       cudaSuccess)
     return LMOE_ERR_CUDA;
   if (nb > 0) {

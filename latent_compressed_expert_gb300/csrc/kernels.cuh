@@ -18,6 +18,7 @@ struct PackedLayout {
 struct WorkspaceLayout {
   size_t err, lat, logits, logits_t, scores, tau, idx, gate, masks, base, offsets, ct_off, inv,
       src_tok, h, o, zh, ys;
+  size_t ct_off_gu;           // the gate/value GEMM's chunk prefix sum (GROUPED_TOKN chunks)
   size_t lat8, slat, h8, sh;  // e4m3 experts: quantised latent and SiTU output, row scales
   size_t splitk;              // small batches: split-K partial sums of the dense GEMMs
   size_t total_base;          // bytes without the split-K region (which is optional)
@@ -155,10 +156,12 @@ int launch_candidates(const float* z, int T, int E, int64_t stride_t, int64_t st
 int launch_transpose_f32(const float* in, int T, int E, float* out, cudaStream_t stream);
 // Checked mode: sets DEVERR_NONFINITE in *err if any of p[0, n) is NaN or infinite.
 int launch_finite_check(const float* p, int64_t n, uint32_t* err, cudaStream_t stream);
-// ct_off: prefix sums of ceil(count / tokn) (tokn = grouped_tokn of the batch).
+// ct_off: prefix sums of ceil(count / tokn) (tokn = grouped_tokn of the batch); ct_off2, if
+// not null: the same for tokn2.
 int launch_dispatch(const int32_t* idx, int T, int E, int K, uint32_t* masks, uint32_t* base,
-                    int32_t* offsets, int32_t* ct_off, int tokn, int32_t* inv,
-                    int32_t* src_tok, int32_t* counts_out, uint32_t* err, cudaStream_t stream);
+                    int32_t* offsets, int32_t* ct_off, int tokn, int32_t* ct_off2, int tokn2,
+                    int32_t* inv, int32_t* src_tok, int32_t* counts_out, uint32_t* err,
+                    cudaStream_t stream);
 int launch_combine(const __nv_bfloat16* o, const float* gate, const int32_t* inv,
                    const float* gamma, int T, int K, int L, float eps, __nv_bfloat16* z,
                    int ldz, uint32_t* err, unsigned long long timeout_ns, cudaStream_t stream);
