@@ -1107,11 +1107,11 @@ int lmoe_forward(const lmoe_dims* dims, const void* packed, const void* x, const
   int32_t* inv = reinterpret_cast<int32_t*>(ws + W.inv);
   int32_t* src_tok = reinterpret_cast<int32_t*>(ws + W.src_tok);
   const int tokn = grouped_tokn(T, D.K, D.E);
-  // the gate/value GEMM's own chunks when the batch's are wider
-  int32_t* ct_off_gu = tokn != GROUPED_TOKN ? reinterpret_cast<int32_t*>(ws + W.ct_off_gu) : ct_off;
+  const int tokn_gu = grouped_tokn_gate_up(T, D.K, D.E, D.expert_fp8 != 0);
+  int32_t* ct_off_gu = tokn_gu != tokn ? reinterpret_cast<int32_t*>(ws + W.ct_off_gu) : ct_off;
   rc = launch_dispatch(idx, T, D.E, D.K, reinterpret_cast<uint32_t*>(ws + W.masks),
                        reinterpret_cast<uint32_t*>(ws + W.base), offsets, ct_off, tokn,
-                       tokn != GROUPED_TOKN ? ct_off_gu : nullptr, GROUPED_TOKN, inv, src_tok,
+                       tokn_gu != tokn ? ct_off_gu : nullptr, tokn_gu, inv, src_tok,
                        opt.counts_out, err, stream);
   if (rc != LMOE_OK) return rc;
   if (opt.load_stats) {
@@ -1158,7 +1158,7 @@ int lmoe_forward(const lmoe_dims* dims, const void* packed, const void* x, const
     g.timeout_ns = wait_limit_ns();
     g.max_ctas = routed_ctas;
     g.mean_tokens = static_cast<int>(static_cast<int64_t>(TK) / D.E);
-    g.tokn = GROUPED_TOKN;
+    g.tokn = tokn_gu;
     rc = launch_grouped_gemm(pk + P.wgu, xop, static_cast<uint64_t>(T), D.L, g, stream);
     if (rc != LMOE_OK) return rc;
   }

@@ -41,11 +41,17 @@ constexpr int GROUPED_TOKN = 192;
 constexpr int GROUPED_TOKN_WIDE = 256;
 
 // The chunk size of a batch, a function of its dims only, so that the forward and the
-// backward, which reads the forward's chunk offsets, agree.  The forward's gate/value GEMM
-// always takes GROUPED_TOKN chunks (its own prefix sum when the batch's are wider): with ~585
-// tokens per expert, 192-token chunks speed it up (3.40 -> 3.30 ms) but slow the down GEMM.
+// backward, which reads the forward's chunk offsets, agree.
 inline int grouped_tokn(int64_t T, int K, int E) {
   return E > 0 && T * K / E > GROUPED_TOKN ? GROUPED_TOKN_WIDE : GROUPED_TOKN;
+}
+
+// The forward's bf16 gate/value GEMM takes GROUPED_TOKN chunks whatever the batch's are (a
+// second prefix sum when they differ): with ~585 tokens per expert that made it 3.40 -> 3.30 ms,
+// while the down GEMM runs faster on the wider chunks.  The e4m3 gate/value GEMM (single weight
+// tiles) keeps the batch's chunks: 2.13 ms on them against 2.30 ms on GROUPED_TOKN ones.
+inline int grouped_tokn_gate_up(int64_t T, int K, int E, bool fp8) {
+  return fp8 ? grouped_tokn(T, K, E) : GROUPED_TOKN;
 }
 
 __host__ __device__ inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
