@@ -33,8 +33,11 @@ def dev():
                                    (20000, 2832, 2048),
                                    # the same with GEMM 1's reduction length (K = 7168)
                                    (8192, 2560, 7168),
-                                   # 224-wide tiles (N = 896 and 672), single and paired
-                                   (8192, 896, 3584), (300, 672, 512), (20000, 896, 2048)])
+                                   # 224-wide tiles (N = 896 and 672), single and paired;
+                                   # over SM pairs at 5000 rows, the last cluster tile's
+                                   # second 128 rows holding 8
+                                   (8192, 896, 3584), (300, 672, 512), (20000, 896, 2048),
+                                   (5000, 896, 3584)])
 def test_gemm_matches_float64(dev, M, N, K):
     g = torch.Generator(device=dev).manual_seed(M * 7 + N * 3 + K)
     A = torch.randn(M, K, generator=g, device=dev).to(torch.bfloat16)
