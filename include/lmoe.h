@@ -445,7 +445,7 @@ int lmoe_quantize_e4m3(const void *x, long long rows, int cols, uint8_t *codes, 
  * process starts.  Arguments and results are those of lmoe_forward without the workspace.
  * Scratch: a LMOE_NOALLOC_SCRATCH_BYTES (24 MiB) array in the library's device image,
  * reserved on every GPU that loads the library until the process exits.  It covers a K3
- * decode batch of up to 152 tokens (64 tokens need 10.07 MiB, or 22.07 MiB with the split-K
+ * decode batch of up to 152 tokens (64 tokens need 10.08 MiB, or 22.08 MiB with the split-K
  * region, which is used when it fits).  When the workspace without that region exceeds the
  * array, the call returns LMOE_ERR_WORKSPACE_TOO_SMALL and enqueues nothing.
  * Set-up: the first call in each CUDA context looks up the array's device address in that
