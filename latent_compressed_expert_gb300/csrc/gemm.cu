@@ -59,9 +59,11 @@ struct GemmCfg {
   static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
   static constexpr int NUM_BARS = 2 * STAGES + 6;
   static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
-  // grouped-K epilogue staging: 32 rows x 32 fp32 per epilogue warp
-  static constexpr int EPI_OFF = (MISC_OFF + 16 + 127) / 128 * 128;
-  static constexpr int EPI_BYTES = MT == 1 ? 4 * 32 * 32 * 4 : 0;
+  // grouped-K epilogue staging: two buffers of 32 rows x 32 fp32 per epilogue warp, 1024-byte
+  // aligned (their 16-byte chunks are placed with the 128-byte swizzle that the tensor stores
+  // writing them out apply)
+  static constexpr int EPI_OFF = (MISC_OFF + 16 + 1023) / 1024 * 1024;
+  static constexpr int EPI_BYTES = MT == 1 ? 2 * 4 * 32 * 32 * 4 : 0;
   static constexpr int SMEM_BYTES = EPI_OFF + EPI_BYTES + 1024;  // + slack for 1024 alignment
   static constexpr uint32_t IDESC = ptx::idesc_bf16_f32(BLOCK_M, BN);
   static constexpr uint32_t IDESC_MN = ptx::idesc_bf16_f32_mn(BLOCK_M, BN);
@@ -322,7 +324,8 @@ __device__ __forceinline__ void epilogue_store_partial(const GemmArgs& g, int ro
 template <int BN, int MT, bool RP>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
 gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA,
-                    const __grid_constant__ CUtensorMap tmB, const GemmArgs g) {
+                    const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmO, const GemmArgs g) {
   using C = GemmCfg<BN, MT>;
   constexpr int TM = BLOCK_M * MT;
   if constexpr (MT != 1 || BN % 64 != 0) {
@@ -541,7 +544,9 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA,
   } else {
     // ------------------------------------------------------------ epilogue (warps 2..5)
     const int q = warp & 3;  // TMEM lane quarter this warp may access
-    float* stage = reinterpret_cast<float*>(smem + C::EPI_OFF) + q * 32 * 32;
+    // this warp's two staging buffers (grouped-K): buffer b at EPI_OFF + (4 b + q) * 4 KB
+    float* stage0 = reinterpret_cast<float*>(smem + C::EPI_OFF) + q * 32 * 32;
+    int nst = 0;  // grouped-K chunks this warp has handed to tensor stores
     const float c = g.c, inv_c = 1.0f / g.c;
     int lt = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++lt) {
@@ -562,6 +567,12 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA,
         const bool row_ok = row < tc.row_end;
         const int orow =
             (g.groups > 0 && row_ok) ? (g.row_map ? __ldg(g.row_map + row) : row) : 0;
+        // grouped-K with tensor stores: the warp's rows 0..15 and 16..31 must each land on
+        // 16 consecutive output rows (the gate/value de-interleave keeps 16-row runs)
+        const int orun0 = __shfl_sync(0xffffffffu, orow, 0);
+        const int orun1 = __shfl_sync(0xffffffffu, orow, 16);
+        const bool tma_rows = g.out_tma && __all_sync(0xffffffffu, row_ok &&
+            orow == (lane < 16 ? orun0 + lane : orun1 + lane - 16));
         const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                static_cast<uint32_t>((acc + h) * BN);
         // Residual epilogue over whole 32-column chunks: chunk ch + 1's residual is loaded
@@ -604,13 +615,36 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA,
 #pragma unroll
               for (int i = 0; i < 32; ++i) v[i] = 0.0f;
             }
-            // Through this warp's staging buffer (16-byte chunks XOR-swizzled by row), so that
-            // each store instruction writes four whole 128-byte row segments instead of one
-            // 16-byte piece of 32 rows.
+            // Through this warp's staging buffer (16-byte chunks XOR-swizzled by row): either
+            // two tensor stores of 16 rows x 32 columns issued by lane 0, or store
+            // instructions that each write four whole 128-byte row segments.
+            float* stage = stage0 + (nst & 1) * (4 * 32 * 32);
+            if (tma_rows || nst > 0) {
+              // the store that last read this buffer (two chunks back) is done reading it;
+              // before thread stores, every earlier tensor store is
+              if (lane == 0) {
+                if (tma_rows)
+                  ptx::bulk_wait_group_read<1>();
+                else
+                  ptx::bulk_wait_group_read<0>();
+              }
+              __syncwarp();
+            }
 #pragma unroll
             for (int j = 0; j < 8; ++j)
               reinterpret_cast<float4*>(stage + lane * 32)[j ^ (lane & 7)] =
                   make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+            if (tma_rows) {
+              ptx::fence_proxy_async_smem();  // the rows, visible to the tensor store
+              __syncwarp();
+              if (lane == 0) {  // columns past N and rows past M are clipped by the map
+                ptx::tma_store_3d(&tmO, stage, col0, orun0, tc.grp);
+                ptx::tma_store_3d(&tmO, stage + 16 * 32, col0, orun1, tc.grp);
+                ptx::bulk_commit_group();
+              }
+              ++nst;
+              continue;
+            }
             __syncwarp();
             const int nvalid = min(32, g.N - col0);  // a multiple of 16
             const int c4 = lane & 7;
@@ -651,6 +685,8 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA,
       ptx::tc_fence_before();
       ptx::mbar_arrive(&tempty[acc]);
     }
+    // the tensor stores complete before the CTA leaves (they read its shared memory)
+    if (lane == 0 && nst > 0) ptx::bulk_wait_group_all();
   }
 
   ptx::tc_fence_before();
@@ -756,6 +792,28 @@ static PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
   return fn;
 }
 
+// fp32 output of `groups` row-major [rows, cols] matrices (row stride ld, group stride gstride
+// elements) as a 3-D tensor with boxes of 32 columns x 16 rows, 128-byte swizzled.
+static bool make_tmap_f32_out(CUtensorMap* m, const float* ptr, int cols, int rows, int groups,
+                              int ld, long long gstride) {
+  auto enc = tmap_encoder();
+  if (!enc || !ptr || rows <= 0 || cols <= 0 || groups <= 0 ||
+      (reinterpret_cast<uintptr_t>(ptr) & 15u) != 0 || ld % 4 != 0 || ld < cols)
+    return false;
+  const long long gs = groups > 1 ? gstride : static_cast<long long>(rows) * ld;
+  if (gs % 4 != 0 || gs < static_cast<long long>(rows) * ld) return false;
+  const cuuint64_t gdim[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
+                              static_cast<cuuint64_t>(groups)};
+  const cuuint64_t gstr[2] = {static_cast<cuuint64_t>(ld) * 4, static_cast<cuuint64_t>(gs) * 4};
+  const cuuint32_t box[3] = {32, 16, 1};
+  const cuuint32_t estride[3] = {1, 1, 1};
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(ptr), gdim,
+                         gstr, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 bool make_tmap_bf16(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint64_t ld,
                     uint32_t box_rows) {
   auto enc = tmap_encoder();
@@ -792,6 +850,9 @@ bool make_tmap_bf16(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t col
 // (multicast); tempty[a] of rank 0 gets one arrival per epilogue warp of both CTAs; cluster
 // barriers bracket set-up and teardown, so that neither CTA leaves while its peer may still
 // signal its barriers or read its shared memory.
+// The grouped-K epilogue writes its fp32 output with tensor stores from the staging buffers
+// (else with store instructions from its threads).
+constexpr bool GEMM_WGRAD_TMA_STORE = true;
 constexpr int GEMM_PAIR_STAGES = 7;
 constexpr bool GEMM_SM_PAIR = true;  // the tile-pair GEMMs run over SM pairs
 
@@ -1080,8 +1141,8 @@ static int launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const GemmA
 }
 
 template <int BN, int MT, bool RP = false>
-static int launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& g,
-                     cudaStream_t stream) {
+static int launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& to,
+                     const GemmArgs& g, cudaStream_t stream) {
   using C = GemmCfg<BN, MT>;
   if (cudaFuncSetAttribute(gemm_tcgen05_kernel<BN, MT, RP>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1096,15 +1157,17 @@ static int launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArg
                         (g.groups > 0 ? g.groups : 1) * (g.ksplit > 1 ? g.ksplit : 1);
   if (tiles < grid) grid = static_cast<int>(tiles);
   if (grid <= 0) return LMOE_OK;
-  return launch_pdl(gemm_tcgen05_kernel<BN, MT, RP>, grid, GEMM_THREADS, C::SMEM_BYTES, stream, ta, tb,
-                    g) ==
+  return launch_pdl(gemm_tcgen05_kernel<BN, MT, RP>, grid, GEMM_THREADS, C::SMEM_BYTES, stream,
+                    ta, tb, to, g) ==
                  cudaSuccess
              ? LMOE_OK
              : LMOE_ERR_CUDA;
 }
 
 int launch_gemm(const void* A, uint64_t a_rows, int a_ld, const void* B, uint64_t b_rows,
-                int b_ld, const GemmArgs& g, cudaStream_t stream) {
+                int b_ld, const GemmArgs& g_in, cudaStream_t stream) {
+  GemmArgs g = g_in;
+  g.out_tma = 0;  // set below, with the output tensor map it needs
   if (g.groups > 0 && (g.epi != EPI_F32 || !g.kseg)) return LMOE_ERR_INVALID_ARG;
   if (g.pre && ((g.epi != EPI_SITU && g.epi != EPI_SPLIT) || g.ldp % 8 ||
                 (reinterpret_cast<uintptr_t>(g.pre) & 15u)))
@@ -1125,7 +1188,7 @@ int launch_gemm(const void* A, uint64_t a_rows, int a_ld, const void* B, uint64_
                   g.N % 224 == 0 && g.N <= 4 * 224)
                      ? 224
                      : (g.M <= BLOCK_M ? 128 : ((g.N % 256 == 0 || g.N > 512) ? 256 : 128));
-  CUtensorMap ta, tb;
+  CUtensorMap ta, tb, to{};
   if (g.groups > 0) {
     // MN-major: a_rows / b_rows count K rows; boxes of 64 columns x 64 rows
     if (!make_tmap_bf16(&ta, A, a_rows, static_cast<uint64_t>(g.M), static_cast<uint64_t>(a_ld),
@@ -1133,6 +1196,12 @@ int launch_gemm(const void* A, uint64_t a_rows, int a_ld, const void* B, uint64_
         !make_tmap_bf16(&tb, B, b_rows, static_cast<uint64_t>(g.N), static_cast<uint64_t>(b_ld),
                         BLOCK_K))
       return LMOE_ERR_CUDA;
+    // the fp32 output as (columns, rows, groups), for the epilogue's tensor stores; without
+    // one (an unaligned output) the epilogue stores from its threads
+    g.out_tma = GEMM_WGRAD_TMA_STORE && make_tmap_f32_out(&to, g.outf, g.N, g.M, g.groups,
+                                                           g.ldf, g.group_stride)
+                    ? 1
+                    : 0;
   } else if (!make_tmap_bf16(&ta, A, a_rows, static_cast<uint64_t>(g.Kd),
                              static_cast<uint64_t>(a_ld), BLOCK_M) ||
              !make_tmap_bf16(&tb, B, b_rows, static_cast<uint64_t>(g.Kd),
@@ -1157,9 +1226,9 @@ int launch_gemm(const void* A, uint64_t a_rows, int a_ld, const void* B, uint64_
       const int per = static_cast<int>(ceil_div(nkb, ks));
       GemmArgs gs = g;
       gs.ksplit = static_cast<int>(ceil_div(nkb, per));  // no slice is left empty
-      const int rc = bn == 256   ? launch_bn<256, 1>(ta, tb, gs, stream)
-                     : bn == 224 ? launch_bn<224, 1>(ta, tb, gs, stream)
-                                 : launch_bn<128, 1>(ta, tb, gs, stream);
+      const int rc = bn == 256   ? launch_bn<256, 1>(ta, tb, to, gs, stream)
+                     : bn == 224 ? launch_bn<224, 1>(ta, tb, to, gs, stream)
+                                 : launch_bn<128, 1>(ta, tb, to, gs, stream);
       if (rc != LMOE_OK) return rc;
       const int64_t chunks = static_cast<int64_t>(g.M) * ceil_div(g.N, 32);
       const bool warp = gs.ksplit >= SPLITK_WARP_MIN;
@@ -1199,12 +1268,15 @@ int launch_gemm(const void* A, uint64_t a_rows, int a_ld, const void* B, uint64_
       return LMOE_ERR_CUDA;
     return launch_pair<224, false>(ta, tbh, g, stream);
   }
-  if (bn == 256 && pairs && rp) return launch_bn<256, 2, true>(ta, tb, g, stream);
+  if (bn == 256 && pairs && rp) return launch_bn<256, 2, true>(ta, tb, to, g, stream);
   if (bn == 256)
-    return pairs ? launch_bn<256, 2>(ta, tb, g, stream) : launch_bn<256, 1>(ta, tb, g, stream);
+    return pairs ? launch_bn<256, 2>(ta, tb, to, g, stream)
+                 : launch_bn<256, 1>(ta, tb, to, g, stream);
   if (bn == 224)
-    return pairs ? launch_bn<224, 2>(ta, tb, g, stream) : launch_bn<224, 1>(ta, tb, g, stream);
-  return pairs ? launch_bn<128, 2>(ta, tb, g, stream) : launch_bn<128, 1>(ta, tb, g, stream);
+    return pairs ? launch_bn<224, 2>(ta, tb, to, g, stream)
+                 : launch_bn<224, 1>(ta, tb, to, g, stream);
+  return pairs ? launch_bn<128, 2>(ta, tb, to, g, stream)
+               : launch_bn<128, 1>(ta, tb, to, g, stream);
 }
 
 }  // namespace lmoe

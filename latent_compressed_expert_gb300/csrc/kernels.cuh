@@ -67,6 +67,7 @@ struct GemmArgs {
   float c;                // SiTU cap
   uint32_t* err;          // device error flag (never null)
   unsigned long long timeout_ns;
+  int out_tma;            // set by launch_gemm: grouped-K output through tensor stores
   int inject_stall;       // test hook: the MMA role first waits on a barrier nobody arrives
                           // on, so every role runs into its bounded wait and aborts
   // Grouped-K mode (groups > 0): `groups` independent products C_q = A_q^T B_q with A and B
