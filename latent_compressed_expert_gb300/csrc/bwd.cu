@@ -355,8 +355,11 @@ transpose_rows_kernel(const __nv_bfloat16* __restrict__ x, int64_t ldx, int W, i
 }
 
 // out[p, :W] = x[idx[p], :W] for p < n (16-byte pieces; W, ldx and ldo multiples of 8).  One
-// warp per row; each lane issues four loads before their stores.
+// warp per row; each lane issues all its loads of a row (up to GATHER_VEC 16-byte pieces)
+// before their stores, and the stores stream (the rows are written once, while the source
+// rows, re-read by every slot of their token, stay in L2).
 constexpr int GATHER_WARPS = 8;
+constexpr int GATHER_VEC = 16;  // 16-byte pieces per lane held at once: W <= 4096 in one pass
 
 __global__ void __launch_bounds__(32 * GATHER_WARPS)
 gather_rows_kernel(const __nv_bfloat16* __restrict__ x, int64_t ldx,
@@ -370,17 +373,17 @@ gather_rows_kernel(const __nv_bfloat16* __restrict__ x, int64_t ldx,
   const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<int64_t>(__ldg(idx + p)) * ldx);
   uint4* dst = reinterpret_cast<uint4*>(out + p * ldo);
   const int nv = W / 8;
-  for (int v0 = 0; v0 < nv; v0 += 4 * 32) {
-    uint4 r[4];
+  for (int v0 = 0; v0 < nv; v0 += GATHER_VEC * 32) {
+    uint4 r[GATHER_VEC];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
+    for (int k = 0; k < GATHER_VEC; ++k) {
       const int v = v0 + k * 32 + lane;
       if (v < nv) r[k] = __ldg(src + v);
     }
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
+    for (int k = 0; k < GATHER_VEC; ++k) {
       const int v = v0 + k * 32 + lane;
-      if (v < nv) dst[v] = r[k];
+      if (v < nv) __stcs(dst + v, r[k]);
     }
   }
 }
