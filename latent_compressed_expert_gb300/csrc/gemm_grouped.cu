@@ -33,7 +33,9 @@ constexpr int GROUPED_BOX_T = 32;  // token rows per TMA box / padding granule o
 // the K3 shapes: the gate/value GEMM (long K, gathered rows) is fastest with the deepest ring
 // that fits (1.19 ms at 5 stages vs 1.28 at 4, prefill); the down GEMM (K = 512, writing the
 // expert outputs) with one stage less when experts see many tokens (0.75 ms at 4 vs 0.82 at
-// 5, prefill) but not at decode (~1 token per expert: 0.37 ms at 5 vs 0.39 at 4).
+// 5, prefill) but not at decode (~1 token per expert: 0.37 ms at 5 vs 0.39 at 4).  Single
+// weight tiles now serve only the e4m3 gate/value GEMM and the one that stores its
+// pre-activations, below GROUPED_PAIR_MIN_TOKENS tokens per expert (see launch_grouped_gemm).
 constexpr int GROUPED_STAGES_DEEP = 5;
 constexpr int GROUPED_STAGES_SHALLOW = 4;
 constexpr int GROUPED_SHALLOW_MIN_TOKENS = 32;
