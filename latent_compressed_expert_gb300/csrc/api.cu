@@ -126,7 +126,7 @@ WorkspaceLayout workspace_layout(const lmoe_dims& D) {
   W.base = take(nb * D.E * 4);
   W.offsets = take((static_cast<size_t>(D.E) + 1) * 4);
   W.ct_off = take((static_cast<size_t>(D.E) + 1) * 4);
-  W.ct_off_gu = take((static_cast<size_t>(D.E) + 1) * 4);
+  W.ct_off2 = take((static_cast<size_t>(D.E) + 1) * 4);
   W.inv = take(TK * 4);
   W.src_tok = take(TK * 4);
   W.h = take(TK * D.I * 2);
@@ -1106,13 +1106,19 @@ int lmoe_forward(const lmoe_dims* dims, const void* packed, const void* x, const
   int32_t* ct_off = reinterpret_cast<int32_t*>(ws + W.ct_off);
   int32_t* inv = reinterpret_cast<int32_t*>(ws + W.inv);
   int32_t* src_tok = reinterpret_cast<int32_t*>(ws + W.src_tok);
+  // Chunk prefix sums: the batch's (which the backward reads), and a second one for the routed
+  // GEMM that takes its own chunks -- the bf16 gate/value GEMM or the e4m3 down GEMM, never both
   const int tokn = grouped_tokn(T, D.K, D.E);
   const int tokn_gu = grouped_tokn_gate_up(T, D.K, D.E, D.expert_fp8 != 0);
-  int32_t* ct_off_gu = tokn_gu != tokn ? reinterpret_cast<int32_t*>(ws + W.ct_off_gu) : ct_off;
+  const int tokn_dn = grouped_tokn_down(T, D.K, D.E, D.expert_fp8 != 0);
+  if (tokn_gu != tokn && tokn_dn != tokn) return LMOE_ERR_UNSUPPORTED;
+  const int tokn2 = tokn_gu != tokn ? tokn_gu : tokn_dn;
+  int32_t* ct_off2 = tokn2 != tokn ? reinterpret_cast<int32_t*>(ws + W.ct_off2) : nullptr;
+  int32_t* ct_off_gu = tokn_gu != tokn ? ct_off2 : ct_off;
+  int32_t* ct_off_dn = tokn_dn != tokn ? ct_off2 : ct_off;
   rc = launch_dispatch(idx, T, D.E, D.K, reinterpret_cast<uint32_t*>(ws + W.masks),
-                       reinterpret_cast<uint32_t*>(ws + W.base), offsets, ct_off, tokn,
-                       tokn_gu != tokn ? ct_off_gu : nullptr, tokn_gu, inv, src_tok,
-                       opt.counts_out, err, stream);
+                       reinterpret_cast<uint32_t*>(ws + W.base), offsets, ct_off, tokn, ct_off2,
+                       tokn2, inv, src_tok, opt.counts_out, err, stream);
   if (rc != LMOE_OK) return rc;
   if (opt.load_stats) {
     rc = launch_load_stats(nullptr, offsets, D.E, opt.load_stats, stream);
@@ -1171,7 +1177,7 @@ int lmoe_forward(const lmoe_dims* dims, const void* packed, const void* x, const
     g.M_w = D.L;
     g.Kd = D.I;
     g.seg_off = offsets;
-    g.ct_off = ct_off;
+    g.ct_off = ct_off_dn;
     g.epi = EPI_BF16;
     g.out = o;
     g.ldo = D.L;
@@ -1180,7 +1186,7 @@ int lmoe_forward(const lmoe_dims* dims, const void* packed, const void* x, const
     g.timeout_ns = wait_limit_ns();
     g.max_ctas = routed_ctas;
     g.mean_tokens = static_cast<int>(static_cast<int64_t>(TK) / D.E);
-    g.tokn = tokn;
+    g.tokn = tokn_dn;
     const void* xop = h;
     if (fp8) {
       // e4m3 SiTU outputs, one scale per (token, expert) row

@@ -68,8 +68,10 @@ struct GroupedCfg {
   static constexpr int B_BYTES = TOKN * BLOCK_K * 2;      // up to 32 KB of activations
   static constexpr int STAGE_BYTES = W_BYTES + B_BYTES;
   static constexpr int STAGES = STAGES_;
-  static constexpr int ACC = MW == 2 ? 1 : 2;             // accumulator sets (double buffer)
-  static constexpr int ACC_COLS = 256;                    // TMEM columns per accumulator
+  // TMEM columns per weight tile's accumulator, and accumulator sets: two (the epilogue of
+  // one tile overlaps the next tile's MMAs) unless a weight-tile pair's 2 x 256 fill TMEM
+  static constexpr int ACC_COLS = (MW == 2 && TOKN <= 128) ? 128 : 256;
+  static constexpr int ACC = 2 * MW * ACC_COLS <= 512 ? 2 : 1;
   static constexpr int TMEM_COLS = 512;
   static constexpr int EPI_OFF = STAGES * STAGE_BYTES;   // per epilogue warp 32 x 32 bf16
   static constexpr int EPI_BYTES = STAGED ? 8 * 32 * 32 * 2 : 0;
@@ -342,8 +344,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
           break;
         }
         ptx::tc_fence_after();
-        // weight tile w of the tile accumulates at TMEM columns (acc + w) * ACC_COLS
-        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * C::ACC_COLS);
+        // weight tile w of the tile accumulates at TMEM columns (acc * MW + w) * ACC_COLS
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * MW * C::ACC_COLS);
         bool ok = true;
         for (int kb = 0; kb < nk; ++kb, ++it) {
           const int s = static_cast<int>(it % C::STAGES);
@@ -474,7 +476,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
         const int r0w = t.r0 + w * BLOCK_M;    // first weight row of weight tile w
         const int r = r0w + q * 32 + lane;     // weight row of this thread within the expert
         const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                               static_cast<uint32_t>((acc + w) * C::ACC_COLS);
+                               static_cast<uint32_t>((acc * MW + w) * C::ACC_COLS);
         const bool row_ok = r < g.M_w;  // the last weight tile of an expert may be partial
 #pragma unroll 1
         for (int ch = ch0; ch * 32 < t.npad; ch += chstep) {
@@ -905,7 +907,8 @@ int launch_grouped_gemm(const void* W, const void* X, uint64_t x_rows, int x_ld,
   if (g.M_w <= 0 || g.Kd % kgran != 0 || g.Kd <= 0 || x_rows == 0) return LMOE_ERR_UNSUPPORTED;
   if (g.epi != EPI_SITU && g.epi != EPI_BF16) return LMOE_ERR_UNSUPPORTED;
   if (g.epi == EPI_SITU && g.M_w % BLOCK_M != 0) return LMOE_ERR_UNSUPPORTED;
-  if (g.tokn != GROUPED_TOKN && g.tokn != GROUPED_TOKN_WIDE) return LMOE_ERR_INVALID_ARG;
+  if (g.tokn != GROUPED_TOKN && g.tokn != GROUPED_TOKN_WIDE && g.tokn != GROUPED_TOKN_NARROW)
+    return LMOE_ERR_INVALID_ARG;
   if (g.fp8 && (!g.w_scale || !g.x_scale || x_ld % 2 != 0)) return LMOE_ERR_INVALID_ARG;
   if (g.pre && (g.epi != EPI_SITU || g.ldp % 8 != 0 || g.ldp < g.M_w ||
                 (reinterpret_cast<uintptr_t>(g.pre) & 15u)))
@@ -947,6 +950,11 @@ int launch_grouped_gemm(const void* W, const void* X, uint64_t x_rows, int x_ld,
     // long as the bf16 one while its SiTU epilogue (the accurate tanh) is heavier, so the pair's
     // undivided accumulator, drained while no MMA runs, cost more than the token bytes saved
     // (prefill 0.634 -> 0.681 ms, skew 2.09 -> 2.74 ms; down 0.586 -> 0.564, 2.34 -> 1.91).
+    if (pairs && g.epi != EPI_SITU && g.tokn <= GROUPED_TOKN_NARROW)
+      // 128-token chunks (decode-like loads): two accumulator sets, so the drain, which bounds
+      // this GEMM (its K is 512 codes: four K-blocks), runs under the next tile's MMAs
+      return launch_grouped_stages<GROUPED_STAGES_PAIR + 1, true, 2, GROUPED_TOKN_NARROW>(
+          tw, tx, ga, stream);
     if (pairs && g.epi != EPI_SITU) {
       if (wide) return launch_grouped_stages<GROUPED_STAGES_PAIR, true, 2, GROUPED_TOKN_WIDE>(
                     tw, tx, ga, stream);

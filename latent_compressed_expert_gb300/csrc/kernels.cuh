@@ -18,7 +18,7 @@ struct PackedLayout {
 struct WorkspaceLayout {
   size_t err, lat, logits, logits_t, scores, tau, idx, gate, masks, base, offsets, ct_off, inv,
       src_tok, h, o, zh, ys;
-  size_t ct_off_gu;           // the gate/value GEMM's chunk prefix sum, if its own
+  size_t ct_off2;             // a routed GEMM's own chunk prefix sum (gate/value or down)
   size_t lat8, slat, h8, sh;  // e4m3 experts: quantised latent and SiTU output, row scales
   size_t splitk;              // small batches: split-K partial sums of the dense GEMMs
   size_t total_base;          // bytes without the split-K region (which is optional)
