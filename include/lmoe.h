@@ -369,6 +369,15 @@ int lmoe_forward_host(const lmoe_dims *dims, const void *packed, const void *x_h
 int lmoe_gemm_bf16(const void *A, const void *B, float *C, int M, int N, int Kd,
                    uint32_t *dev_flag, void *stream);
 
+/* Building block of lmoe_backward's weight gradients, exposed for verification: C = A^T . B
+ * summed over all T rows, with A [T, M] and B [T, N] bf16 row-major (token-major, read as
+ * MN-major tcgen05 operands) and C [M, N] fp32.  Requires M % 8 == 0, N % 16 == 0, T >= 0,
+ * 16-byte aligned pointers.  dev_words: four caller-owned device words, zeroed: word 0
+ * receives the error bits of a device-side wait that ran out, words 2 and 3 the row range
+ * {0, T} that the call writes there.  T == 0 writes C = 0. */
+int lmoe_gemm_wgrad_bf16(const void *A, const void *B, float *C, int M, int N, int T,
+                         uint32_t *dev_words, void *stream);
+
 /* Backward pass of the routed-expert branch.  [IK3] stabilizers passage: SiTU-GLU and the
  * RMSNorm after aggregation were introduced to keep training of the routed branch stable.
  * For the branch  h_j = SiTU(lat W_g[e_j]^T, lat W_v[e_j]^T),  o_j = h_j W_ed[e_j]^T,

@@ -592,6 +592,32 @@ int lmoe_gemm_bf16(const void* A, const void* B, float* C, int M, int N, int Kd,
                      static_cast<cudaStream_t>(stream));
 }
 
+int lmoe_gemm_wgrad_bf16(const void* A, const void* B, float* C, int M, int N, int T,
+                         uint32_t* dev_words, void* stream) {
+  if (M < 0 || N <= 0 || T < 0 || !C || !A || !B || !dev_words) return LMOE_ERR_INVALID_ARG;
+  if (M % 8 || N % 16) return LMOE_ERR_UNSUPPORTED;
+  if (!aligned16(A) || !aligned16(B) || !aligned16(C)) return LMOE_ERR_INVALID_ARG;
+  if (M == 0) return LMOE_OK;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (T == 0)
+    return cudaMemsetAsync(C, 0, static_cast<size_t>(M) * N * sizeof(float), st) == cudaSuccess
+               ? LMOE_OK
+               : LMOE_ERR_CUDA;
+  int32_t* seg = reinterpret_cast<int32_t*>(dev_words + 2);
+  int rc = launch_rowmap(0, 0, nullptr, seg, T, st);  // writes seg = {0, T} and no map
+  if (rc != LMOE_OK) return rc;
+  GemmArgs g = gemm_defaults(dev_words, 1.0f);
+  g.M = M;
+  g.N = N;
+  g.epi = EPI_F32;
+  g.outf = C;
+  g.ldf = N;
+  g.groups = 1;
+  g.kseg = seg;
+  g.kfull = T;
+  return launch_gemm(A, static_cast<uint64_t>(T), M, B, static_cast<uint64_t>(T), N, g, st);
+}
+
 size_t lmoe_packed_backward_bytes(const lmoe_dims* dims) {
   if (dims_supported(dims) != LMOE_OK || dims->expert_fp8) return 0;
   return bwd_packed_layout(*dims).total;
@@ -761,6 +787,7 @@ int lmoe_backward(const lmoe_dims* dims, const void* packed, const void* packed_
     g.ldf = N;
     g.groups = 1;
     g.kseg = seg1;
+    g.kfull = T;  // the one group is every row of the operands
     g.row_map = row_map;
     return launch_gemm(Am, static_cast<uint64_t>(T), a_ld, Bm, static_cast<uint64_t>(T), b_ld, g,
                        stream);

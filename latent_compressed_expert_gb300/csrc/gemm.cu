@@ -853,6 +853,7 @@ bool make_tmap_bf16(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t col
 // The grouped-K epilogue writes its fp32 output with tensor stores from the staging buffers
 // (else with store instructions from its threads).
 constexpr bool GEMM_WGRAD_TMA_STORE = true;
+constexpr bool GEMM_WGRAD_SM_PAIR = true;  // single-range weight gradients over SM pairs
 constexpr int GEMM_PAIR_STAGES = 7;
 constexpr bool GEMM_SM_PAIR = true;  // the tile-pair GEMMs run over SM pairs
 
@@ -870,18 +871,24 @@ struct GemmPairCfg {
   static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
   static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;  // + slack for 1024 alignment
   static constexpr uint32_t IDESC = ptx::idesc_bf16_f32(TM, BN);
+  static constexpr uint32_t IDESC_MN = ptx::idesc_bf16_f32_mn(TM, BN);
+  static constexpr int BOX_BYTES = 64 * BLOCK_K * 2;     // one 64 x 64 MN-major TMA box
   static_assert(BN % 32 == 0 && BN <= 256 && 2 * BN <= TMEM_COLS, "two accumulator sets fit TMEM");
   static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "tiles must stay 1024-aligned");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
 
 // BN: 256, or 224 (the router over 896 experts: four whole column tiles).  RP: the residual
-// epilogue with its residual prefetched one chunk ahead (the output GEMM).
-template <int BN, bool RP>
+// epilogue with its residual prefetched one chunk ahead (the output GEMM).  MN: a weight
+// gradient C = A^T B over all g.kfull rows of token-major A [kfull, M] and B [kfull, N], read
+// as MN-major operands in 64 x 64 boxes (rows past kfull are zero-filled by TMA); fp32 output
+// at row g.row_map[r] (or r).
+template <int BN, bool RP, bool MN = false>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
 gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const GemmArgs g) {
   using C = GemmPairCfg<BN>;
+  static_assert(!MN || (BN == 256 && !RP), "MN-major operands: 256-wide tiles, fp32 output");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = ptx::smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -901,7 +908,7 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
   const int nt = (g.N + C::BN - 1) / C::BN;
   const int mt = (g.M + C::TM - 1) / C::TM;
   const int total = mt * nt;
-  const int nk = g.Kd / BLOCK_K;
+  const int nk = MN ? (g.kfull + BLOCK_K - 1) / BLOCK_K : g.Kd / BLOCK_K;
   const uint64_t limit = g.timeout_ns;
 
   if (threadIdx.x == 0) {
@@ -954,11 +961,24 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
           uint8_t* sa = smem + s * C::STAGE_BYTES;
           const uint32_t fb = ptx::mapa_shared(ptx::smem_u32(&full[s]), 0);
           if (lead) ptx::mbar_arrive_expect_tx(&full[s], 2u * C::STAGE_BYTES);
-          // rows past M or N are zero-filled
-          ptx::tma_load_2d_pair(sa, &tmA, fb, kb * BLOCK_K,
-                                tc.a_row + static_cast<int>(rank) * BLOCK_M);
-          ptx::tma_load_2d_pair(sa + C::A_BYTES, &tmB, fb, kb * BLOCK_K,
-                                tc.b_row + static_cast<int>(rank) * (C::BN / 2));
+          if constexpr (MN) {
+            // this CTA's 128 columns of A and of B: two 64-column boxes of 64 K rows each
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+              ptx::tma_load_2d_pair(sa + i * C::BOX_BYTES, &tmA, fb,
+                                    tc.a_row + static_cast<int>(rank) * BLOCK_M + 64 * i,
+                                    kb * BLOCK_K);
+              ptx::tma_load_2d_pair(sa + C::A_BYTES + i * C::BOX_BYTES, &tmB, fb,
+                                    tc.b_row + static_cast<int>(rank) * (C::BN / 2) + 64 * i,
+                                    kb * BLOCK_K);
+            }
+          } else {
+            // rows past M or N are zero-filled
+            ptx::tma_load_2d_pair(sa, &tmA, fb, kb * BLOCK_K,
+                                  tc.a_row + static_cast<int>(rank) * BLOCK_M);
+            ptx::tma_load_2d_pair(sa + C::A_BYTES, &tmB, fb, kb * BLOCK_K,
+                                  tc.b_row + static_cast<int>(rank) * (C::BN / 2));
+          }
         }
       }
       // rank 0's last full phases cover both CTAs' last copies: they land before the pair exits
@@ -1004,10 +1024,16 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
           const uint32_t sa = ptx::smem_u32(smem + s * C::STAGE_BYTES);
           const uint32_t sb = sa + C::A_BYTES;
 #pragma unroll
-          for (int k = 0; k < BLOCK_K / 16; ++k)
-            ptx::umma_bf16_pair(d_tmem, ptx::smem_desc_sw128(sa + k * 32),
-                                ptx::smem_desc_sw128(sb + k * 32), C::IDESC,
-                                (kb | k) != 0 ? 1u : 0u);
+          for (int k = 0; k < BLOCK_K / 16; ++k) {
+            if constexpr (MN)  // 16 K rows = two 1024-byte atoms of each box
+              ptx::umma_bf16_pair(d_tmem, ptx::smem_desc_sw128_mn(sa + k * 2048, C::BOX_BYTES),
+                                  ptx::smem_desc_sw128_mn(sb + k * 2048, C::BOX_BYTES),
+                                  C::IDESC_MN, (kb | k) != 0 ? 1u : 0u);
+            else
+              ptx::umma_bf16_pair(d_tmem, ptx::smem_desc_sw128(sa + k * 32),
+                                  ptx::smem_desc_sw128(sb + k * 32), C::IDESC,
+                                  (kb | k) != 0 ? 1u : 0u);
+          }
           ptx::umma_commit_pair(&empty[s], 0x3);
         }
         if (!ok) break;
@@ -1037,6 +1063,8 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
       ptx::tc_fence_after();
       const int row = tc.a_row + static_cast<int>(rank) * BLOCK_M + q * 32 + lane;
       const bool row_ok = row < g.M;
+      // a weight gradient's output row (the row map de-interleaves gate/value rows)
+      const int orow = (MN && row_ok && g.row_map) ? __ldg(g.row_map + row) : row;
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                              static_cast<uint32_t>(acc * C::BN);
       if constexpr (RP) {
@@ -1071,9 +1099,9 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
           ptx::tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(ch * 32), v);
           if (row_ok) {
             if (col0 + 32 <= g.N)
-              epilogue_store(g, row, col0, v, c, inv_c);
+              epilogue_store(g, orow, col0, v, c, inv_c);
             else
-              epilogue_store_partial(g, row, col0, g.N - col0, v);
+              epilogue_store_partial(g, orow, col0, g.N - col0, v);
           }
         }
       }
@@ -1098,12 +1126,13 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
 }
 
 // tb: B's tensor map with BN / 2-row boxes (each CTA of a pair loads half of a tile's columns).
-template <int BN, bool RP>
+template <int BN, bool RP, bool MN = false>
 static int launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& g,
                        cudaStream_t stream) {
   using C = GemmPairCfg<BN>;
-  auto kernel = gemm_pair_kernel<BN, RP>;
-  if (g.groups > 0 || g.ksplit > 1) return LMOE_ERR_INVALID_ARG;
+  auto kernel = gemm_pair_kernel<BN, RP, MN>;
+  if (g.ksplit > 1 || (MN ? (g.groups != 1 || g.kfull <= 0 || g.epi != EPI_F32) : g.groups > 0))
+    return LMOE_ERR_INVALID_ARG;
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            C::SMEM_BYTES) != cudaSuccess)
     return LMOE_ERR_CUDA;
@@ -1212,6 +1241,12 @@ int launch_gemm(const void* A, uint64_t a_rows, int a_ld, const void* B, uint64_
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return LMOE_ERR_CUDA;
+  // A weight gradient over all rows of its operands (one group) with at least two 256 x 256
+  // cluster tiles per SM pair: over SM pairs, like the dense tile-pair GEMMs
+  if (GEMM_SM_PAIR && GEMM_WGRAD_SM_PAIR && g.groups == 1 && g.kfull > 0 && bn == 256 &&
+      static_cast<uint64_t>(g.kfull) == a_rows && static_cast<uint64_t>(g.kfull) == b_rows &&
+      ceil_div(g.M, 2 * BLOCK_M) * ceil_div(g.N, 256) >= 2 * static_cast<int64_t>(sms))
+    return launch_pair<256, false, true>(ta, tb, g, stream);
   // Split-K when one M-tile's column tiles would leave most SMs idle (small batches): each
   // slice of K-blocks is its own tile, and a second kernel adds the slices.
   if (g.groups == 0 && g.partial && g.M <= BLOCK_M) {

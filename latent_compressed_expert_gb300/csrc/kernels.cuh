@@ -80,6 +80,9 @@ struct GemmArgs {
   const int32_t* kseg;
   long long group_stride;
   const int32_t* row_map;
+  // groups == 1 whose range is every row [0, kfull) of A and B (kfull > 0; the caller knows
+  // it on the host): such a product may run over SM pairs, reading no kseg
+  int kfull;
   // Split-K (dense mode, set by the launcher when one M-tile leaves most SMs idle): slice s of
   // ksplit reduces its share of the K-blocks into partial[s, M, N] (fp32), and a second kernel
   // sums the slices in order and applies the epilogue.  partial: caller's scratch of

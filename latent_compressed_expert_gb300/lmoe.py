@@ -95,6 +95,7 @@ SIGNATURES = {
     "lmoe_forward": (_i, [ctypes.POINTER(Dims), _vp, _vp, _vp, _vp, _vp, _sz, ctypes.POINTER(IO),
                           _vp]),
     "lmoe_gemm_bf16": (_i, [_vp, _vp, _vp, _i, _i, _i, _vp, _vp]),
+    "lmoe_gemm_wgrad_bf16": (_i, [_vp, _vp, _vp, _i, _i, _i, _vp, _vp]),
     "lmoe_forward_noalloc": (_i, [ctypes.POINTER(Dims), _vp, _vp, _vp, _vp, ctypes.POINTER(IO),
                                   _vp]),
     "lmoe_forward_host": (_i, [ctypes.POINTER(Dims), _vp, _vp, _i, _vp, _vp, _sz,
@@ -385,6 +386,20 @@ def gemm_bf16(A: torch.Tensor, B: torch.Tensor, stream=None) -> torch.Tensor:
     _check(load().lmoe_gemm_bf16(_ptr(A), _ptr(B), _ptr(C), M, N, Kd, _ptr(flag),
                                  _stream(stream)), "lmoe_gemm_bf16")
     return C, flag
+
+
+def gemm_wgrad_bf16(A: torch.Tensor, B: torch.Tensor, stream=None) -> torch.Tensor:
+    """C = A^T . B (fp32) over all rows of token-major A [T, M] and B [T, N], as the backward's
+    weight gradients compute it."""
+    T, M = A.shape
+    N = B.shape[1]
+    _expect(A, torch.bfloat16, (T, M), "A")
+    _expect(B, torch.bfloat16, (T, N), "B")
+    C = torch.empty((M, N), dtype=torch.float32, device=A.device)
+    words = torch.zeros(4, dtype=torch.int32, device=A.device)
+    _check(load().lmoe_gemm_wgrad_bf16(_ptr(A), _ptr(B), _ptr(C), M, N, T, _ptr(words),
+                                       _stream(stream)), "lmoe_gemm_wgrad_bf16")
+    return C, words
 
 
 def last_device_error(workspace: torch.Tensor) -> int:

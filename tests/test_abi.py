@@ -141,6 +141,11 @@ def test_route_and_threshold_argument_checks(lib):
     assert lib.lmoe_gemm_bf16(fake, fake, fake, 4, 24, 64, fake, None) == lmoe.LMOE_ERR_UNSUPPORTED
     assert lib.lmoe_gemm_bf16(fake, fake, fake, 4, 32, 96, fake, None) == lmoe.LMOE_ERR_UNSUPPORTED
     assert lib.lmoe_gemm_bf16(fake, fake, fake, 4, 32, 64, None, None) == lmoe.LMOE_ERR_INVALID_ARG
+    assert lib.lmoe_gemm_wgrad_bf16(fake, fake, fake, 12, 32, 64, fake, None) == lmoe.LMOE_ERR_UNSUPPORTED
+    assert lib.lmoe_gemm_wgrad_bf16(fake, fake, fake, 16, 24, 64, fake, None) == lmoe.LMOE_ERR_UNSUPPORTED
+    assert lib.lmoe_gemm_wgrad_bf16(fake, fake, fake, 16, 32, -1, fake, None) == lmoe.LMOE_ERR_INVALID_ARG
+    assert lib.lmoe_gemm_wgrad_bf16(fake, fake, fake, 16, 32, 64, None, None) == lmoe.LMOE_ERR_INVALID_ARG
+    assert lib.lmoe_gemm_wgrad_bf16(fake, fake, fake, 0, 32, 64, fake, None) == lmoe.LMOE_OK
 
 
 def test_binding_refuses_cpu_tensors(lib):

@@ -51,6 +51,27 @@ def test_gemm_matches_float64(dev, M, N, K):
     assert bool((err <= bound).all()), float((err / bound).max())
 
 
+@pytest.mark.parametrize("M,N,T", [
+    # one-SM tiles (grouped-K mode, one group): ragged T, M below one tile, N ragged
+    (128, 256, 64), (200, 512, 1000), (1024, 3584, 146),
+    # 256 x 256 cluster tiles over SM pairs (at least two per SM pair): T ragged, M and N ragged
+    # across the pair, and T = 8192 as in the K3 prefill weight gradients
+    (4096, 5120, 1000), (4104, 5136, 777), (7168, 7680, 8192)])
+def test_weight_gradient_gemm_matches_float64(dev, M, N, T):
+    """C = A^T B over all T rows, the backward's weight-gradient form, against float64."""
+    g = torch.Generator(device=dev).manual_seed(M * 5 + N * 3 + T)
+    A = torch.randn(T, M, generator=g, device=dev).to(torch.bfloat16)
+    B = torch.randn(T, N, generator=g, device=dev).to(torch.bfloat16)
+    C, words = lmoe.gemm_wgrad_bf16(A, B)
+    torch.cuda.synchronize()
+    assert int(words[0]) == 0
+    ref = A.double().T @ B.double()
+    bound = max(T, 1) * 2.0 ** -23 * (A.double().abs().T @ B.double().abs()) + 1e-30
+    err = (C.double() - ref).abs()
+    assert bool((err <= bound).all()), float((err / bound).max())
+
+
+
 # ----------------------------------------------------------------------------------------
 # routing: bit-exact against the oracle on identical fp32 logits
 # ----------------------------------------------------------------------------------------
