@@ -52,7 +52,8 @@ constexpr bool GROUPED_SM_PAIR = true;
 // every gathered or loaded token row serves 256 output features: half the token bytes per
 // FLOP, for experts with many tokens, where the token rows and not the weights bound the
 // shared-memory fill.  Its accumulator pair fills TMEM (2 x 256 columns), so it is drained
-// while no MMA runs (the producer keeps loading the next tile meanwhile).
+// while no MMA runs (the producer keeps loading the next tile meanwhile) -- unless TOKN <= 128,
+// where two pairs of 2 x 128 columns fit and the drain overlaps the next tile's MMAs.
 // TOKN_: the largest token chunk the tile holds (the shared-memory token tile and the TMEM
 // columns of one accumulator); the chunks themselves are set by GroupedArgs::tokn <= TOKN_.
 // STAGED: the epilogue's shared-memory staging of output rows (needed by the down GEMM and by
