@@ -802,17 +802,39 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmW,
                                static_cast<uint32_t>(w * C::ACC_COLS);
 #pragma unroll 1
         for (int ch = eg; ch * 32 < t.npad; ch += 2) {
-          float v[32];
-          ptx::tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(ch * 32), v);
           const int nv = min(32, t.ntok - ch * 32);
+          // the warp's 32 weight rows x 32 tokens into the staging slot as [token][row] bf16,
+          // token rows of 64 bytes whose 16-byte pieces are XOR-swizzled by (token / 2) % 4:
+          // per 16 TMEM lanes, 8 x 8 blocks in fragment layout stored transposed (stmatrix)
 #pragma unroll
-          for (int j = 0; j < 32; ++j) st[j * 32 + lane] = __float2bfloat16_rn(v[j]);
+          for (int hf = 0; hf < 2; ++hf) {
+            float f[16];
+            ptx::tmem_ld_16x256b_x4(
+                tbase + (static_cast<uint32_t>(16 * hf) << 16) + static_cast<uint32_t>(ch * 32), f);
+            uint32_t m[8];  // m[2n]: rows 16hf + 0..7, m[2n + 1]: rows 16hf + 8..15; tokens 8n..
+#pragma unroll
+            for (int n = 0; n < 4; ++n) {
+              const __nv_bfloat162 a = __floats2bfloat162_rn(f[4 * n], f[4 * n + 1]);
+              const __nv_bfloat162 b = __floats2bfloat162_rn(f[4 * n + 2], f[4 * n + 3]);
+              m[2 * n] = *reinterpret_cast<const uint32_t*>(&a);
+              m[2 * n + 1] = *reinterpret_cast<const uint32_t*>(&b);
+            }
+#pragma unroll
+            for (int call = 0; call < 2; ++call) {
+              const int i = lane >> 3;  // the matrix whose row this thread addresses
+              const int tok = 8 * (2 * call + (i >> 1)) + (lane & 7);
+              const int pc = (2 * hf + (i & 1)) ^ ((tok >> 1) & 3);
+              ptx::stmatrix_x4_trans(ptx::smem_u32(st + tok * 32 + pc * 8), m[4 * call],
+                                     m[4 * call + 1], m[4 * call + 2], m[4 * call + 3]);
+            }
+          }
           __syncwarp();
           const int piece = lane & 3;
 #pragma unroll
           for (int j0 = 0; j0 < 32; j0 += 8) {
             const int j = j0 + (lane >> 2);
-            const uint4 val = *reinterpret_cast<const uint4*>(st + j * 32 + piece * 8);
+            const uint4 val =
+                *reinterpret_cast<const uint4*>(st + j * 32 + (piece ^ ((j >> 1) & 3)) * 8);
             if (j < nv)
               *reinterpret_cast<uint4*>(g.out + static_cast<size_t>(t.tok0 + ch * 32 + j) * g.ldo +
                                         r0w + q * 32 + piece * 8) = val;

@@ -230,6 +230,36 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, float (&v)[32
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// Warp-collective load of 16 TMEM lanes x 32 fp32 columns (shape 16x256b, four times along
+// the columns): for n = 0..3, thread t receives lane base + t/4 at columns 8n + 2(t%4) and
+// 8n + 2(t%4) + 1 (v[4n], v[4n+1]) and lane base + 8 + t/4 at the same columns (v[4n+2],
+// v[4n+3]) -- per 8 lanes x 8 columns, the fragment layout that stmatrix takes.
+__device__ __forceinline__ void tmem_ld_16x256b_x4(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x4.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Four 8 x 8 matrices of 16-bit elements, held in fragment layout (register i: matrix i;
+// thread t: row t/4, columns 2(t%4) and 2(t%4) + 1, the lower column in the low half),
+// stored transposed: the 16-byte row that thread 8i + j addresses receives column j of
+// matrix i.
+__device__ __forceinline__ void stmatrix_x4_trans(uint32_t smem_addr, uint32_t r0, uint32_t r1,
+                                                  uint32_t r2, uint32_t r3) {
+  asm volatile("stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(
+                   smem_addr),
+               "r"(r0), "r"(r1), "r"(r2), "r"(r3)
+               : "memory");
+}
+
 // ---------------------------------------------------------------- CTA pairs (cta_group::2)
 // A cluster of two CTAs on two SMs: rank 0 issues the MMAs over both CTAs' shared memory and
 // TMEM; the barriers it waits on also collect the peer's copies and arrivals.
