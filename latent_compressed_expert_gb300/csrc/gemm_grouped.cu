@@ -481,9 +481,75 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
         const bool row_ok = r < g.M_w;  // the last weight tile of an expert may be partial
 #pragma unroll 1
         for (int ch = ch0; ch * 32 < t.npad; ch += chstep) {
+          const int nv = min(32, t.ntok - ch * 32);
+          // The e4m3 down GEMM (weight-tile pairs, bf16 outputs; row_ok is warp-uniform: M_w
+          // is a multiple of 64): the warp's 32 rows x 32 tokens into its staging slot as token
+          // rows, per 16 TMEM lanes as 8 x 8 blocks in fragment layout stored transposed
+          // (stmatrix); the slot's 16-byte pieces are XOR-swizzled by (token / 2) % 4.  Only
+          // these instantiations carry it: compiled into the e4m3 gate/value GEMM it slowed
+          // that GEMM's SiTU epilogue (0.644 -> 0.785 ms at prefill) without running.
+          if constexpr (FP8 && MW == 2 && STAGED) {
+            if (g.epi != EPI_SITU) {
+              if (!row_ok) continue;
+              __nv_bfloat16* st = epi_stage + (warp - 2) * (32 * 32);
+              float xs = x_s[0], ws = w_s[0];  // lane l's token scale and row scale
+#pragma unroll
+              for (int cc = 1; cc < NCH; ++cc) xs = ch == cc ? x_s[cc] : xs;
+#pragma unroll
+              for (int ww = 1; ww < MW; ++ww) ws = w == ww ? w_s[ww] : ws;
+#pragma unroll
+              for (int hf = 0; hf < 2; ++hf) {
+                float f[16];
+                ptx::tmem_ld_16x256b_x4(tbase + (static_cast<uint32_t>(16 * hf) << 16) +
+                                            static_cast<uint32_t>(ch * 32),
+                                        f);
+                // e4m3 scales as v * ws * xs below, per (row, token) of the fragment
+                const float wa = __shfl_sync(0xffffffffu, ws, 16 * hf + (lane >> 2));
+                const float wb = __shfl_sync(0xffffffffu, ws, 16 * hf + 8 + (lane >> 2));
+#pragma unroll
+                for (int n = 0; n < 4; ++n) {
+                  const float xa = __shfl_sync(0xffffffffu, xs, 8 * n + 2 * (lane & 3));
+                  const float xb = __shfl_sync(0xffffffffu, xs, 8 * n + 2 * (lane & 3) + 1);
+                  f[4 * n] = f[4 * n] * wa * xa;
+                  f[4 * n + 1] = f[4 * n + 1] * wa * xb;
+                  f[4 * n + 2] = f[4 * n + 2] * wb * xa;
+                  f[4 * n + 3] = f[4 * n + 3] * wb * xb;
+                }
+                uint32_t m[8];
+#pragma unroll
+                for (int n = 0; n < 4; ++n) {
+                  const __nv_bfloat162 a = __floats2bfloat162_rn(f[4 * n], f[4 * n + 1]);
+                  const __nv_bfloat162 b = __floats2bfloat162_rn(f[4 * n + 2], f[4 * n + 3]);
+                  m[2 * n] = *reinterpret_cast<const uint32_t*>(&a);
+                  m[2 * n + 1] = *reinterpret_cast<const uint32_t*>(&b);
+                }
+#pragma unroll
+                for (int call = 0; call < 2; ++call) {
+                  const int i = lane >> 3;
+                  const int tok = 8 * (2 * call + (i >> 1)) + (lane & 7);
+                  const int pc = (2 * hf + (i & 1)) ^ ((tok >> 1) & 3);
+                  ptx::stmatrix_x4_trans(ptx::smem_u32(st + tok * 32 + pc * 8), m[4 * call],
+                                         m[4 * call + 1], m[4 * call + 2], m[4 * call + 3]);
+                }
+              }
+              __syncwarp();
+              const int piece = lane & 3;
+#pragma unroll
+              for (int j0 = 0; j0 < 32; j0 += 8) {
+                const int j = j0 + (lane >> 2);
+                const uint4 val =
+                    *reinterpret_cast<const uint4*>(st + j * 32 + (piece ^ ((j >> 1) & 3)) * 8);
+                if (j < nv)
+                  *reinterpret_cast<uint4*>(g.out +
+                                            static_cast<size_t>(t.tok0 + ch * 32 + j) * g.ldo +
+                                            r0w + q * 32 + piece * 8) = val;
+              }
+              __syncwarp();
+              continue;
+            }
+          }
           float v[32];
           ptx::tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(ch * 32), v);
-          const int nv = min(32, t.ntok - ch * 32);
           if constexpr (FP8) {
             float xs = x_s[0];  // this chunk's scales (a register select, no local memory)
 #pragma unroll
