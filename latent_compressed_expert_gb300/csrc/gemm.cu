@@ -814,6 +814,25 @@ static bool make_tmap_f32_out(CUtensorMap* m, const float* ptr, int cols, int ro
   return r == CUDA_SUCCESS;
 }
 
+// bf16 output rows [rows, cols] (row stride ld) for tensor stores of 32 x 32 boxes whose 64-byte
+// rows hold their 16-byte pieces XOR-swizzled by (row / 2) % 4 (the 64-byte swizzle).
+bool make_tmap_bf16_out32(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols,
+                          uint64_t ld) {
+  auto enc = tmap_encoder();
+  if (!enc || rows == 0 || cols == 0 || (reinterpret_cast<uintptr_t>(ptr) & 15u) != 0 ||
+      (ld * 2) % 16 != 0 || ld < cols)
+    return false;
+  const cuuint64_t gdim[2] = {cols, rows};
+  const cuuint64_t gstride[1] = {ld * 2};
+  const cuuint32_t box[2] = {32, 32};
+  const cuuint32_t estride[2] = {1, 1};
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), gdim,
+                         gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 bool make_tmap_bf16(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint64_t ld,
                     uint32_t box_rows) {
   auto enc = tmap_encoder();

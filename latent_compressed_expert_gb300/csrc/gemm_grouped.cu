@@ -46,6 +46,7 @@ constexpr int GROUPED_PAIR_MIN_TOKENS = 64;  // experts' mean token count from w
 // bf16 pairs over two SMs (cta_group::2, two weight tiles per SM; see grouped_gemm_pair_kernel)
 // for GEMMs whose token rows are loaded by TMA
 constexpr bool GROUPED_SM_PAIR = true;
+constexpr bool GROUPED_OUT_TMA_STORE = true;  // the pair kernel's whole output chunks by TMA
 
 // MW: weight row tiles per CTA tile.  MW = 2 ("weight-tile pairs") stages two 128-row
 // weight tiles of the same expert with one token tile and issues two MMAs per K-step, so
@@ -675,10 +676,13 @@ struct GroupedPairCfg {
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
 
+// tmO (used when g.out_tma): the output as 32 x 32 boxes with the 64-byte swizzle, the layout of
+// an epilogue warp's staging slot.
 template <int STAGES_, int TOKN_>
 __global__ void __launch_bounds__(GROUPED_THREADS, 1)
 grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmW,
-                         const __grid_constant__ CUtensorMap tmX, const GroupedArgs g) {
+                         const __grid_constant__ CUtensorMap tmX,
+                         const __grid_constant__ CUtensorMap tmO, const GroupedArgs g) {
   using C = GroupedPairCfg<STAGES_, TOKN_>;
   constexpr int MW = C::MW;
   constexpr int CW = 2 * MW;  // weight tiles per cluster tile
@@ -851,6 +855,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmW,
     const int eg = (warp - 2) / GROUPED_EPI_WARPS;
     const uint32_t tempty_lead = ptx::mapa_shared(ptx::smem_u32(tempty), 0);
     __nv_bfloat16* st = epi_stage + (warp - 2) * (32 * 32);
+    bool pending = false;  // a tensor store of the slot may still be reading it
     int lt = 0;
     for (int tile = cid; tile < total; tile += ncl, ++lt) {
       const GTile t = decode(tile);  // before the wait: its loads hide there
@@ -869,6 +874,11 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmW,
 #pragma unroll 1
         for (int ch = eg; ch * 32 < t.npad; ch += 2) {
           const int nv = min(32, t.ntok - ch * 32);
+          if (pending) {  // the slot's last tensor store has read it
+            if (lane == 0) ptx::bulk_wait_group_read<0>();
+            __syncwarp();
+            pending = false;
+          }
           // the warp's 32 weight rows x 32 tokens into the staging slot as [token][row] bf16,
           // token rows of 64 bytes whose 16-byte pieces are XOR-swizzled by (token / 2) % 4:
           // per 16 TMEM lanes, 8 x 8 blocks in fragment layout stored transposed (stmatrix)
@@ -894,6 +904,17 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmW,
                                      m[4 * call + 1], m[4 * call + 2], m[4 * call + 3]);
             }
           }
+          if (g.out_tma && nv == 32) {
+            // a whole chunk: one tensor store of the slot (32 rows of this warp x 32 tokens)
+            ptx::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              ptx::tma_store_2d(&tmO, st, r0w + q * 32, t.tok0 + ch * 32);
+              ptx::bulk_commit_group();
+            }
+            pending = true;
+            continue;
+          }
           __syncwarp();
           const int piece = lane & 3;
 #pragma unroll
@@ -917,6 +938,8 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmW,
           ptx::mbar_arrive_cluster(tempty_lead);
       }
     }
+    // the tensor stores complete before the CTA leaves (they read its shared memory)
+    if (lane == 0) ptx::bulk_wait_group_all();
   }
 
   ptx::tc_fence_before();
@@ -929,8 +952,12 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmW,
 }
 
 template <int STAGES_, int TOKN_>
-static int launch_grouped_pair(const CUtensorMap& tw, const CUtensorMap& tx,
-                               const GroupedArgs& g, cudaStream_t stream) {
+static int launch_grouped_pair(const CUtensorMap& tw, const CUtensorMap& tx, uint64_t x_rows,
+                               const GroupedArgs& g_in, cudaStream_t stream) {
+  // the output for tensor stores of whole 32-token chunks: it has the token operand's rows
+  GroupedArgs g = g_in;
+  CUtensorMap to{};
+  g.out_tma = GROUPED_OUT_TMA_STORE && make_tmap_bf16_out32(&to, g.out, x_rows, g.M_w, g.ldo);
   using C = GroupedPairCfg<STAGES_, TOKN_>;
   auto kernel = grouped_gemm_pair_kernel<STAGES_, TOKN_>;
   if (g.tokn > TOKN_) return LMOE_ERR_UNSUPPORTED;
@@ -966,7 +993,7 @@ static int launch_grouped_pair(const CUtensorMap& tw, const CUtensorMap& tx,
     pairs = active;
     cfg.gridDim = dim3(2 * pairs);
   }
-  return cudaLaunchKernelEx(&cfg, kernel, tw, tx, g) == cudaSuccess ? LMOE_OK : LMOE_ERR_CUDA;
+  return cudaLaunchKernelEx(&cfg, kernel, tw, tx, to, g) == cudaSuccess ? LMOE_OK : LMOE_ERR_CUDA;
 }
 
 template <int STAGES_, bool FP8, int MW, int TOKN_, bool STAGED = true>
@@ -1064,8 +1091,8 @@ int launch_grouped_gemm(const void* W, const void* X, uint64_t x_rows, int x_ld,
     if (!make_tmap_bf16(&tx16, X, x_rows, static_cast<uint64_t>(kd), static_cast<uint64_t>(ld),
                         GroupedPairCfg<4, GROUPED_TOKN_WIDE>::BOX_T))
       return LMOE_ERR_CUDA;
-    if (wide) return launch_grouped_pair<4, GROUPED_TOKN_WIDE>(tw, tx16, ga, stream);
-    return launch_grouped_pair<4, GROUPED_TOKN>(tw, tx16, ga, stream);
+    if (wide) return launch_grouped_pair<4, GROUPED_TOKN_WIDE>(tw, tx16, x_rows, ga, stream);
+    return launch_grouped_pair<4, GROUPED_TOKN>(tw, tx16, x_rows, ga, stream);
   }
   if (pairs) {
     if (wide) return launch_grouped_stages<GROUPED_STAGES_PAIR, false, 2, GROUPED_TOKN_WIDE>(

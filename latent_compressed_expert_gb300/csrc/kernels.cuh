@@ -118,6 +118,7 @@ struct GroupedArgs {
   int max_ctas;           // persistent grid limit (0: one CTA per SM)
   int mean_tokens;        // average tokens per expert (T*K/E): picks the pipeline depth
   int evict_first;        // set by the launcher: weights loaded with an L2 evict-first policy
+  int out_tma;            // set by the launcher: whole 32-token output chunks by tensor stores
   // e4m3 operands: W and x hold codes, Kd and ldx count codes, a K-block is 128 codes (the
   // same 128 bytes per row as 64 bf16); the accumulator is multiplied by the weight row's
   // and the activation row's scale in the epilogue
@@ -138,6 +139,8 @@ int launch_grouped_gemm(const void* W, const void* X, uint64_t x_rows, int x_ld,
 // 64 x box_rows box and the 128-byte swizzle.  Returns false on failure.
 bool make_tmap_bf16(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint64_t ld,
                     uint32_t box_rows);
+bool make_tmap_bf16_out32(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols,
+                          uint64_t ld);
 
 int launch_gemm(const void* A, uint64_t a_rows, int a_ld, const void* B, uint64_t b_rows,
                 int b_ld, const GemmArgs& args, cudaStream_t stream);
